@@ -1,0 +1,214 @@
+"""CPU oracle of the MoE layer forward -- TEST INFRASTRUCTURE ONLY.
+
+Only `tests/`, `__graft_entry__.smoke()` and the CPU-baseline leg of
+`bench.py` may import this package.  The product (the CUDA library under
+`mixture_experts_layer_fp32_gb300/` and its binding) never imports it; the
+two share no code.  The arithmetic lives in `moe_oracle.cpp` (plain C++,
+double precision); this module only marshals numpy arrays.
+
+Inputs are numpy arrays: fp32 arrays, or uint16 arrays holding bf16 bit
+patterns (widened exactly inside the oracle).
+"""
+
+import ctypes
+import os
+import subprocess
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.cpp")
+_LIBDIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_LIBDIR, "libmoe_oracle.so")
+_lib = None
+
+SCORES = {"softmax_post": 0, "softmax_pre": 1, "sigmoid": 2}
+POLICIES = {"probs": 0, "position": 1}
+
+
+def build(force=False):
+    """Compile the oracle into oracle/_build/libmoe_oracle.so (g++, -O2)."""
+    os.makedirs(_LIBDIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB_PATH)
+        i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+        L.oracle_router_logits.argtypes = [i64, i32, i32, vp, i32, vp, vp, vp, i32]
+        L.oracle_topk_scores.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp, i32]
+        L.oracle_capacity.argtypes = [i64, i32, i32, dbl, i64]
+        L.oracle_capacity.restype = i64
+        L.oracle_capacity_drop.argtypes = [i64, i32, i32, i64, i32, vp, vp, vp, vp]
+        L.oracle_permute.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp]
+        L.oracle_permute.restype = i64
+        L.oracle_expert_rows.argtypes = [i64, i32, i32, vp, i32, vp, vp, vp, vp, i32, vp, vp, i32]
+        L.oracle_combine.argtypes = [i64, i32, i32, vp, vp, vp, vp, i32]
+        L.oracle_forward_dense.argtypes = [i64, i32, i32, i32, i32, vp, i32, vp, vp, vp,
+                                           vp, vp, vp, i32, vp, i32]
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dtype_code(a):
+    if a.dtype == np.float32:
+        return 0
+    if a.dtype == np.uint16:
+        return 1
+    raise TypeError("oracle inputs are float32 or uint16 (bf16 bits), got %s" % a.dtype)
+
+
+def _c(a, dtype=None):
+    if a is None:
+        return None
+    a = np.asarray(a)
+    if dtype is not None:
+        a = a.astype(dtype, copy=False)
+    return np.ascontiguousarray(a)
+
+
+def bf16_bits_to_f32(a):
+    """Exact widening of bf16 bit patterns (uint16) to float32."""
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    return (a.astype(np.uint32) << 16).view(np.float32)
+
+
+def router_logits(x, Wg, gate_bias=None, nthreads=0):
+    x = _c(x)
+    Wg = _c(Wg, np.float32)
+    gate_bias = _c(gate_bias, np.float32)
+    T, h = x.shape
+    E = Wg.shape[1]
+    out = np.empty((T, E), np.float32)
+    _load().oracle_router_logits(T, h, E, _ptr(x), _dtype_code(x), _ptr(Wg), _ptr(gate_bias),
+                                 _ptr(out), nthreads)
+    return out
+
+
+def topk_scores(logits, k, score, expert_bias=None, nthreads=0):
+    logits = _c(logits, np.float32)
+    expert_bias = _c(expert_bias, np.float32)
+    T, E = logits.shape
+    idx = np.empty((T, k), np.int32)
+    prob = np.empty((T, k), np.float32)
+    margin = np.empty((T,), np.float32)
+    _load().oracle_topk_scores(T, E, k, SCORES[score], _ptr(logits), _ptr(expert_bias),
+                               _ptr(idx), _ptr(prob), _ptr(margin), nthreads)
+    return idx, prob, margin
+
+
+def capacity(T, E, k, capacity_factor, min_capacity=0):
+    return int(_load().oracle_capacity(T, E, k, float(capacity_factor), int(min_capacity)))
+
+
+def capacity_drop(topk_idx, topk_prob, E, cap, policy="probs"):
+    topk_idx = _c(topk_idx, np.int32)
+    prob = np.array(topk_prob, dtype=np.float32, copy=True)
+    T, k = topk_idx.shape
+    keep = np.empty((T, k), np.uint8)
+    kept = np.empty((E,), np.int32)
+    _load().oracle_capacity_drop(T, E, k, cap, POLICIES[policy], _ptr(topk_idx), _ptr(prob),
+                                 _ptr(keep), _ptr(kept))
+    return prob, keep, kept
+
+
+def permute(topk_idx, keep, E):
+    topk_idx = _c(topk_idx, np.int32)
+    keep = _c(keep, np.uint8)
+    T, k = topk_idx.shape
+    offsets = np.empty((E + 1,), np.int32)
+    row_map = np.empty((T, k), np.int32)
+    row_token = np.empty((T * k,), np.int32)
+    R = _load().oracle_permute(T, E, k, _ptr(topk_idx), _ptr(keep), _ptr(offsets),
+                               _ptr(row_map), _ptr(row_token))
+    return offsets, row_map, row_token[:R].copy()
+
+
+def expert_rows(x_rows, row_expert, W1, W3, W2, want_h_mid=False, nthreads=0):
+    """SwiGLU expert MLP on rows; returns y_rows [R,h] (and h_mid [R,f]) in float64."""
+    x_rows = _c(x_rows)
+    row_expert = _c(row_expert, np.int32)
+    W1, W3, W2 = _c(W1), _c(W3), _c(W2)
+    R, h = x_rows.shape
+    f = W1.shape[-1]
+    wd = _dtype_code(W1)
+    assert _dtype_code(W3) == wd and _dtype_code(W2) == wd
+    y = np.empty((R, h), np.float64)
+    hm = np.empty((R, f), np.float64) if want_h_mid else None
+    _load().oracle_expert_rows(R, h, f, _ptr(x_rows), _dtype_code(x_rows), _ptr(row_expert),
+                               _ptr(W1), _ptr(W3), _ptr(W2), wd, _ptr(hm), _ptr(y), nthreads)
+    return (y, hm) if want_h_mid else y
+
+
+def combine(y_perm, row_map, topk_prob, nthreads=0):
+    y_perm = _c(y_perm, np.float64)
+    row_map = _c(row_map, np.int32)
+    topk_prob = _c(topk_prob, np.float32)
+    T, k = row_map.shape
+    h = y_perm.shape[1]
+    y = np.empty((T, h), np.float64)
+    _load().oracle_combine(T, k, h, _ptr(y_perm), _ptr(row_map), _ptr(topk_prob), _ptr(y),
+                           nthreads)
+    return y
+
+
+def forward_dense(x, topk_idx, topk_prob, keep, W1, W3, W2, nthreads=0):
+    x = _c(x)
+    topk_idx = _c(topk_idx, np.int32)
+    topk_prob = _c(topk_prob, np.float32)
+    keep = _c(keep, np.uint8)
+    W1, W3, W2 = _c(W1), _c(W3), _c(W2)
+    T, h = x.shape
+    E, _, f = W1.shape
+    k = topk_idx.shape[1]
+    y = np.empty((T, h), np.float64)
+    _load().oracle_forward_dense(T, h, E, k, f, _ptr(x), _dtype_code(x), _ptr(topk_idx),
+                                 _ptr(topk_prob), _ptr(keep), _ptr(W1), _ptr(W3), _ptr(W2),
+                                 _dtype_code(W1), _ptr(y), nthreads)
+    return y
+
+
+def route(x, Wg, k, score, gate_bias=None, expert_bias=None, capacity_factor=0.0,
+          min_capacity=0, drop_policy="probs", nthreads=0):
+    """Router + optional capacity drop.  Returns a dict of numpy arrays."""
+    T = x.shape[0]
+    E = Wg.shape[1]
+    logits = router_logits(x, Wg, gate_bias, nthreads)
+    idx, prob, margin = topk_scores(logits, k, score, expert_bias, nthreads)
+    assigned = np.bincount(idx.reshape(-1), minlength=E).astype(np.int32)
+    cap = capacity(T, E, k, capacity_factor, min_capacity)
+    prob_final, keep, kept = capacity_drop(idx, prob, E, cap, drop_policy)
+    return {"logits": logits, "topk_idx": idx, "topk_prob_raw": prob, "margin": margin,
+            "assigned": assigned, "capacity": cap, "topk_prob": prob_final, "keep": keep,
+            "tokens_per_expert": kept}
+
+
+def forward(x, Wg, W1, W3, W2, k, score, gate_bias=None, expert_bias=None,
+            capacity_factor=0.0, min_capacity=0, drop_policy="probs", nthreads=0,
+            want_h_mid=False):
+    """The whole layer: route -> drop -> permute -> SwiGLU experts -> combine."""
+    r = route(x, Wg, k, score, gate_bias, expert_bias, capacity_factor, min_capacity,
+              drop_policy, nthreads)
+    E = Wg.shape[1]
+    offsets, row_map, row_token = permute(r["topk_idx"], r["keep"], E)
+    row_expert = np.repeat(np.arange(E, dtype=np.int32), np.diff(offsets))
+    x_perm = np.ascontiguousarray(np.asarray(x)[row_token])
+    res = expert_rows(x_perm, row_expert, W1, W3, W2, want_h_mid=want_h_mid, nthreads=nthreads)
+    y_perm, h_mid = (res if want_h_mid else (res, None))
+    y = combine(y_perm, row_map, r["topk_prob"], nthreads)
+    r.update({"offsets": offsets, "row_map": row_map, "row_token": row_token,
+              "x_perm": x_perm, "y_perm": y_perm, "h_mid": h_mid, "y": y})
+    return r

@@ -1,0 +1,329 @@
+// CPU oracle for the single-GPU MoE layer forward.  TEST INFRASTRUCTURE ONLY.
+//
+// Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+// load this library.  The product path (the CUDA library and its Python
+// binding) never calls it and shares no code with it.
+//
+// Every step is the plain definition written out in double precision over
+// the exact input values (bf16 inputs are widened exactly), one loop per
+// sum, summed in index order, no blocking, no fusion.  Threads only split
+// independent tokens / rows.  Sources, all from the pages on the subject:
+//   [MC]  "MoE我们喜欢你（三）：Megatron Core MoE 源码路径解析" (r00kie-liu.github.io)
+//         §2 main path, §3 Gating, §4 TopKRouter, §5 Score function,
+//         §8 Token dropping, §9 Token dispatcher, §10 Experts.
+//   [DS]  "MoE Internals: DeepSpeed-Megatron Expert Parallel Implementation"
+//         (duoan.github.io) §6 Inside DeepSpeed MoELayer, §8 The All-to-All path.
+// Readings where the pages are silent (tie order, the capacity formula's
+// body, SwiGLU, the combine order) are stated next to the code.
+//
+// Parity status: every function below is pinned by the CPU tests
+// (tests/test_oracle_pins.py, tests/test_golden.py).
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+enum { DT_F32 = 0, DT_BF16 = 1 };
+enum { SCORE_SOFTMAX_POST = 0, SCORE_SOFTMAX_PRE = 1, SCORE_SIGMOID = 2 };
+enum { DROP_PROBS = 0, DROP_POSITION = 1 };
+
+// Exact value of element i of a tensor stored as fp32 or as bf16 bits.
+inline double value_at(const void* p, int dtype, int64_t i) {
+  if (dtype == DT_F32) return (double)((const float*)p)[i];
+  uint32_t bits = (uint32_t)((const uint16_t*)p)[i] << 16;
+  float f;
+  std::memcpy(&f, &bits, 4);
+  return (double)f;
+}
+
+template <class Fn>
+void parallel_for(int64_t n, int nthreads, Fn fn) {
+  if (nthreads <= 0) nthreads = (int)std::max(1u, std::thread::hardware_concurrency());
+  if (n < 2 || nthreads == 1) {
+    for (int64_t i = 0; i < n; ++i) fn(i);
+    return;
+  }
+  nthreads = (int)std::min<int64_t>(nthreads, n);
+  std::vector<std::thread> pool;
+  for (int w = 0; w < nthreads; ++w) {
+    pool.emplace_back([=]() {
+      for (int64_t i = w; i < n; i += nthreads) fn(i);
+    });
+  }
+  for (auto& t : pool) t.join();
+}
+
+// Indices of the k largest values of v[0..n), largest first.  Equal values:
+// the lower index comes first (the pages leave torch.topk's tie order open;
+// this is the reading used everywhere in this project).
+void topk_desc(const float* v, int n, int k, int32_t* out_idx) {
+  std::vector<char> taken(n, 0);
+  for (int j = 0; j < k; ++j) {
+    int best = -1;
+    for (int e = 0; e < n; ++e) {
+      if (taken[e]) continue;
+      if (best < 0 || v[e] > v[best]) best = e;
+    }
+    taken[best] = 1;
+    out_idx[j] = best;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int oracle_abi_version(void) { return 1; }
+
+// [MC] §3 Gating: logits = x . Wg (+ bias) with the router math in fp32.
+// The oracle forms the exact sum in double over the exact fp32 values of x
+// and Wg (sum over i in index order), adds the bias, and rounds once to
+// fp32: "the exact value rounded once".
+//   x [T,h] (x_dtype), Wg [h,E] fp32 (row i holds the E gate weights of input
+//   feature i), gate_bias [E] or NULL, logits [T,E] fp32 out.
+void oracle_router_logits(int64_t T, int h, int E, const void* x, int x_dtype,
+                          const float* Wg, const float* gate_bias, float* logits,
+                          int nthreads) {
+  parallel_for(T, nthreads, [&](int64_t t) {
+    std::vector<double> acc(E, 0.0);
+    for (int i = 0; i < h; ++i) {
+      const double xi = value_at(x, x_dtype, t * (int64_t)h + i);
+      const float* wrow = Wg + (int64_t)i * E;
+      for (int e = 0; e < E; ++e) acc[e] += xi * (double)wrow[e];
+    }
+    for (int e = 0; e < E; ++e) {
+      double l = acc[e] + (gate_bias ? (double)gate_bias[e] : 0.0);
+      logits[t * E + e] = (float)l;
+    }
+  });
+}
+
+// [MC] §5 Score function (topk_routing_with_score_function):
+//  SOFTMAX_POST: scores, idx = topk(logits); probs = softmax(scores) over the k.
+//  SOFTMAX_PRE : scores = softmax(logits) over all E; probs, idx = topk(scores).
+//  SIGMOID     : s = sigmoid(logits); idx = topk(s + expert_bias) (the bias
+//                only chooses); probs = s[idx] / (sum s[idx] + 1e-20).
+// Selection is done on fp32 values (the router dtype of [MC] §3); each
+// score is formed in double and rounded once to fp32 before it is compared.
+// Outputs: topk_idx [T,k] (slot order = selection score, descending),
+// topk_prob [T,k] fp32, margin [T] = (k-th - (k+1)-th) selection score
+// (+inf when k == E) -- used by the input conditioner, not by the method.
+void oracle_topk_scores(int64_t T, int E, int k, int score, const float* logits,
+                        const float* expert_bias, int32_t* topk_idx, float* topk_prob,
+                        float* margin, int nthreads) {
+  parallel_for(T, nthreads, [&](int64_t t) {
+    const float* l = logits + t * E;
+    std::vector<float> s(E), sel(E);
+    if (score == SCORE_SOFTMAX_POST) {
+      for (int e = 0; e < E; ++e) s[e] = sel[e] = l[e];
+    } else if (score == SCORE_SOFTMAX_PRE) {
+      double m = -std::numeric_limits<double>::infinity();
+      for (int e = 0; e < E; ++e) m = std::max(m, (double)l[e]);
+      double z = 0.0;
+      for (int e = 0; e < E; ++e) z += std::exp((double)l[e] - m);
+      for (int e = 0; e < E; ++e) s[e] = sel[e] = (float)(std::exp((double)l[e] - m) / z);
+    } else {
+      for (int e = 0; e < E; ++e) {
+        s[e] = (float)(1.0 / (1.0 + std::exp(-(double)l[e])));
+        // scores_for_routing = scores + expert_bias, an fp32 addition
+        sel[e] = expert_bias ? (float)(s[e] + expert_bias[e]) : s[e];
+      }
+    }
+    const int kk = std::min(E, k + 1);
+    std::vector<int32_t> idx(kk);
+    topk_desc(sel.data(), E, kk, idx.data());
+    int32_t* oi = topk_idx + t * k;
+    float* op = topk_prob + t * k;
+    for (int j = 0; j < k; ++j) oi[j] = idx[j];
+    if (margin) {
+      margin[t] = (k < E) ? (float)((double)sel[idx[k - 1]] - (double)sel[idx[k]])
+                          : std::numeric_limits<float>::infinity();
+    }
+    if (score == SCORE_SOFTMAX_POST) {
+      double m = (double)s[idx[0]];
+      double z = 0.0;
+      for (int j = 0; j < k; ++j) z += std::exp((double)s[idx[j]] - m);
+      for (int j = 0; j < k; ++j) op[j] = (float)(std::exp((double)s[idx[j]] - m) / z);
+    } else if (score == SCORE_SOFTMAX_PRE) {
+      for (int j = 0; j < k; ++j) op[j] = s[idx[j]];
+    } else {
+      double z = 0.0;
+      for (int j = 0; j < k; ++j) z += (double)s[idx[j]];
+      for (int j = 0; j < k; ++j) op[j] = (float)((double)s[idx[j]] / (z + 1e-20));
+    }
+  });
+}
+
+// [MC] §8 Token dropping: get_capacity(num_tokens = T*k, E, capacity_factor).
+// The pages print the call but not its body; the reading used here is
+// ceil((T*k / E) * capacity_factor), raised to min_capacity.  Returns -1
+// (dropless) when capacity_factor <= 0.
+int64_t oracle_capacity(int64_t T, int E, int k, double capacity_factor, int64_t min_capacity) {
+  if (capacity_factor <= 0.0) return -1;
+  double c = std::ceil(((double)T * (double)k / (double)E) * capacity_factor);
+  int64_t cap = (int64_t)c;
+  if (cap < min_capacity) cap = min_capacity;
+  return cap;
+}
+
+// [MC] §8 apply_router_token_dropping, per expert column:
+//  - capacity > T: every routed pair is kept;
+//  - policy "probs": keep the `capacity` routed tokens with the largest
+//    probability (equal probabilities: lower token index kept -- the pages'
+//    topk(..., sorted=False) leaves this open);
+//  - policy "position": keep the first `capacity` routed tokens in token
+//    order (the plain reading of topk over the 0/1 routing map).
+// Dropped pairs get probability 0 (final_probs = probs * final_map) and no
+// renormalisation follows.  keep [T,k] u8 out; topk_prob updated in place;
+// kept_per_expert [E] out.
+void oracle_capacity_drop(int64_t T, int E, int k, int64_t capacity, int policy,
+                          const int32_t* topk_idx, float* topk_prob, uint8_t* keep,
+                          int32_t* kept_per_expert) {
+  for (int64_t p = 0; p < T * k; ++p) keep[p] = 1;
+  for (int e = 0; e < E; ++e) kept_per_expert[e] = 0;
+  // candidate pairs per expert, in token order
+  std::vector<std::vector<int64_t>> cand(E);
+  for (int64_t t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) cand[topk_idx[t * k + j]].push_back(t * k + j);
+  for (int e = 0; e < E; ++e) {
+    std::vector<int64_t>& c = cand[e];
+    if (capacity >= 0 && capacity <= T && (int64_t)c.size() > capacity) {
+      std::vector<int64_t> order = c;
+      if (policy == DROP_PROBS) {
+        std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
+          return topk_prob[a] > topk_prob[b];  // stable: ties stay in token order
+        });
+      }
+      for (size_t r = (size_t)capacity; r < order.size(); ++r) {
+        keep[order[r]] = 0;
+        topk_prob[order[r]] = 0.0f;
+      }
+    }
+    int32_t n = 0;
+    for (int64_t p : c) n += keep[p];
+    kept_per_expert[e] = n;
+  }
+}
+
+// [MC] §9 Token dispatcher (sequence-major -> expert-major) and [DS] §8
+// step 4 "permute tokens into expert order".  The pages print no permute
+// code; the reading: expert-major, and inside one expert ascending token
+// index (a stable permutation).  offsets [E+1] = exclusive prefix of the
+// kept counts; row_map [T,k] = row of pair (t,j) or -1 if dropped;
+// row_token [rows] = source token of each row.  Returns the row count.
+int64_t oracle_permute(int64_t T, int E, int k, const int32_t* topk_idx, const uint8_t* keep,
+                       int32_t* offsets, int32_t* row_map, int32_t* row_token) {
+  std::vector<int64_t> count(E, 0);
+  for (int64_t p = 0; p < T * k; ++p)
+    if (!keep || keep[p]) count[topk_idx[p]] += 1;
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = (int32_t)(offsets[e] + count[e]);
+  std::vector<int64_t> cursor(E);
+  for (int e = 0; e < E; ++e) cursor[e] = offsets[e];
+  for (int64_t t = 0; t < T; ++t) {
+    for (int j = 0; j < k; ++j) {
+      int64_t p = t * k + j;
+      if (keep && !keep[p]) {
+        row_map[p] = -1;
+        continue;
+      }
+      int64_t r = cursor[topk_idx[p]]++;
+      row_map[p] = (int32_t)r;
+      if (row_token) row_token[r] = (int32_t)t;
+    }
+  }
+  return offsets[E];
+}
+
+// [MC] §10 Experts (grouped expert MLP), one row at a time.  The expert MLP
+// is SwiGLU (the pages name the grouped MLP but not its activation):
+//   a = x.W1[e], g = x.W3[e], H = silu(a) * g with silu(a) = a / (1 + exp(-a)),
+//   Y = H.W2[e]
+// with W1/W3 [E,h,f] (row i = input feature i) and W2 [E,f,h].  Sums in
+// double over the exact inputs; H is kept in double (not rounded).
+//   rows: x_rows [R,h] (x_dtype) are the inputs; row_expert [R] their experts;
+//   h_mid [R,f] (double, may be NULL) and y_rows [R,h] (double) out.
+void oracle_expert_rows(int64_t R, int h, int f, const void* x_rows, int x_dtype,
+                        const int32_t* row_expert, const void* W1, const void* W3,
+                        const void* W2, int w_dtype, double* h_mid, double* y_rows,
+                        int nthreads) {
+  parallel_for(R, nthreads, [&](int64_t r) {
+    const int64_t e = row_expert[r];
+    std::vector<double> xv(h), a(f, 0.0), g(f, 0.0), H(f), y(h, 0.0);
+    for (int i = 0; i < h; ++i) xv[i] = value_at(x_rows, x_dtype, r * (int64_t)h + i);
+    const int64_t w13 = e * (int64_t)h * f;
+    for (int i = 0; i < h; ++i) {
+      const double xi = xv[i];
+      const int64_t base = w13 + (int64_t)i * f;
+      for (int c = 0; c < f; ++c) {
+        a[c] += xi * value_at(W1, w_dtype, base + c);
+        g[c] += xi * value_at(W3, w_dtype, base + c);
+      }
+    }
+    for (int c = 0; c < f; ++c) H[c] = a[c] / (1.0 + std::exp(-a[c])) * g[c];
+    const int64_t w2 = e * (int64_t)f * h;
+    for (int c = 0; c < f; ++c) {
+      const double hc = H[c];
+      const int64_t base = w2 + (int64_t)c * h;
+      for (int n = 0; n < h; ++n) y[n] += hc * value_at(W2, w_dtype, base + n);
+    }
+    if (h_mid)
+      for (int c = 0; c < f; ++c) h_mid[r * (int64_t)f + c] = H[c];
+    for (int n = 0; n < h; ++n) y_rows[r * (int64_t)h + n] = y[n];
+  });
+}
+
+// [MC] §2 combine / [DS] §8 step 8 "unpermute and combine outputs with gate
+// weights": y[t] = sum over kept slots j (in slot order) of
+// topk_prob[t,j] * y_perm[row_map[t,j]], in double.  A token whose pairs
+// were all dropped gets 0.  y_perm [rows,h] double, y [T,h] double out.
+void oracle_combine(int64_t T, int k, int h, const double* y_perm, const int32_t* row_map,
+                    const float* topk_prob, double* y, int nthreads) {
+  parallel_for(T, nthreads, [&](int64_t t) {
+    double* out = y + t * (int64_t)h;
+    for (int n = 0; n < h; ++n) out[n] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      int32_t r = row_map[t * k + j];
+      if (r < 0) continue;
+      const double p = (double)topk_prob[t * k + j];
+      const double* src = y_perm + (int64_t)r * h;
+      for (int n = 0; n < h; ++n) out[n] += p * src[n];
+    }
+  });
+}
+
+// A second, independent route to the layer output, for validating the
+// oracle on tiny inputs only: every expert is evaluated on every token (no
+// permutation, no row bookkeeping) and weighted by the token's kept
+// probability for that expert (0 if the expert was not selected or the
+// pair was dropped).  y [T,h] double out.
+void oracle_forward_dense(int64_t T, int h, int E, int k, int f, const void* x, int x_dtype,
+                          const int32_t* topk_idx, const float* topk_prob, const uint8_t* keep,
+                          const void* W1, const void* W3, const void* W2, int w_dtype, double* y,
+                          int nthreads) {
+  parallel_for(T, nthreads, [&](int64_t t) {
+    std::vector<double> out(h, 0.0), yrow(h);
+    for (int e = 0; e < E; ++e) {
+      double w = 0.0;
+      for (int j = 0; j < k; ++j)
+        if (topk_idx[t * k + j] == e && (!keep || keep[t * k + j])) w = (double)topk_prob[t * k + j];
+      // evaluate expert e on token t regardless of w
+      int32_t ee = e;
+      std::vector<uint8_t> xrow(h * (x_dtype == DT_F32 ? 4 : 2));
+      std::memcpy(xrow.data(), (const uint8_t*)x + t * (int64_t)h * (x_dtype == DT_F32 ? 4 : 2),
+                  xrow.size());
+      oracle_expert_rows(1, h, f, xrow.data(), x_dtype, &ee, W1, W3, W2, w_dtype, nullptr,
+                         yrow.data(), 1);
+      for (int n = 0; n < h; ++n) out[n] += w * yrow[n];
+    }
+    for (int n = 0; n < h; ++n) y[t * (int64_t)h + n] = out[n];
+  });
+}
+
+}  // extern "C"
