@@ -1,0 +1,477 @@
+"""Benchmark of the GB300 MoE layer forward (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl native|reference] [--no-e2e] [--no-cpu-baseline]
+
+A step is one MoE layer forward -- route, permute, grouped SwiGLU fc1,
+fc2, combine -- over one batch of T synthetic tokens already resident in
+HBM.  Each stage is bracketed by CUDA events on the stream the kernels are
+launched on; the L2 is flushed (a 512 MB write) between timed steps,
+outside the events.  `value` is tokens/s over all ranks (weak scaling:
+every rank runs its own replica of the workload, there is no exchange).
+`e2e` repeats the measurement through moe_forward with the step's input
+copied from pinned host memory and the output copied back inside the
+timed region.  `cpu_baseline` times the CPU oracle on a bounded sample of
+the same workload on the host cores.
+
+--impl reference times the CPU oracle alone on the same workload (a
+bounded sample of tokens per step) and prints the same JSON line with
+"impl": "reference".
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "MoE fwd tokens/sec"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "mixtral"
+STAGES = ["route", "permute", "fc1", "fc2", "combine"]
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--override", default="",
+                    help="comma list of workload fields to replace, e.g. T=2048,f=3584 "
+                         "(a shrunk case for profiling captures)")
+    return ap.parse_args()
+
+
+def workload_of(args):
+    w = synthetic.WORKLOADS[args.workload]
+    if args.override:
+        kv = dict(item.split("=") for item in args.override.split(","))
+        typed = {k: type(getattr(w, k))(v) for k, v in kv.items()}
+        w = synthetic.scaled(w, name=w.name + "_" + args.override.replace(",", "_"), **typed)
+    return w
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def workload_desc(w):
+    return {"workload": w.description, "name": w.name, "T": w.T, "h": w.h, "E": w.E, "k": w.k,
+            "f": w.f, "score": w.score, "capacity_factor": w.capacity_factor,
+            "l2": "flushed between timed steps (512 MB write outside the events)"}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, enabled=True):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+        if not enabled:
+            return
+        fd, self.path = tempfile.mkstemp(prefix="moe_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        # samples under load: power above the midpoint of the observed range
+        thr = 0.5 * (min(power) + max(power))
+        loaded = [s for s, p in zip(sm, power) if p >= thr] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power)}
+
+
+# ---------------------------------------------------------------- traffic
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel
+    source has not changed since it was captured (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    ent = d.get(kernel, {}).get(workload)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "mixture_experts_layer_fp32_gb300", "csrc", ent["source"])
+    with open(src, "rb") as fh:
+        if hashlib.sha256(fh.read()).hexdigest() != ent["sha256"]:
+            return None
+    return ent["dram_bytes_per_launch"]
+
+
+# ---------------------------------------------------------------- native arm
+
+def kernels_per_forward(w, cfg):
+    import mixture_experts_layer_fp32_gb300 as moe
+    cap = moe.capacity(cfg)
+    drops = 0 <= cap < w.T
+    route = 2 + (4 if drops else 0)   # logits, top-k (+ hist, scan, rank, select)
+    return route + 4 + 1 + 1 + 1      # permute hist/scan/rank/copy, fc1, fc2, combine
+
+
+def stage_work(w, R):
+    """Algorithmic work of each stage (bytes moved or flops), per forward."""
+    b = 4 if w.dtype == "f32" else 2
+    T, h, E, k, f = w.T, w.h, w.E, w.k, w.f
+    return {
+        "route": {"bytes": T * h * b + h * E * 4 + T * k * (4 + 4 + 1),
+                  "flops": 2 * T * h * E},
+        "permute": {"bytes": T * h * b + R * h * b + T * k * (4 + 1 + 4)},
+        "fc1": {"flops": 4 * R * h * f, "bytes": 2 * w.E * h * f * b + R * h * b + R * f * b},
+        "fc2": {"flops": 2 * R * f * h, "bytes": w.E * f * h * b + R * f * b + R * h * 4},
+        "combine": {"bytes": R * h * 4 + T * h * b + T * k * 8},
+    }
+
+
+def run_native(args, rank, world, local):
+    import mixture_experts_layer_fp32_gb300 as moe
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workload_of(args)
+    inp = synthetic.generate(w, device=dev, seed=w.seed + 1000 * rank)
+    cfg = moe.config(w.T, w.h, w.E, w.k, w.f, w.score, w.dtype, w.capacity_factor,
+                     w.min_capacity, w.drop_policy)
+    b = moe.Buffers(cfg, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        moe.route(cfg, inp["x"], inp["Wg"], inp["gate_bias"], inp["expert_bias"], b.topk_idx,
+                  b.topk_prob, b.keep, b.tokens_per_expert, None, b.ws)
+        if ev: ev[1].record(stream)
+        moe.permute(cfg, inp["x"], b.topk_idx, b.keep, b.x_perm, b.row_map, b.expert_offsets,
+                    b.ws)
+        if ev: ev[2].record(stream)
+        moe.grouped_fc1(cfg, b.x_perm, b.expert_offsets, inp["W1"], inp["W3"], b.h_mid, b.ws)
+        if ev: ev[3].record(stream)
+        moe.grouped_fc2(cfg, b.h_mid, b.expert_offsets, inp["W2"], b.y_perm, b.ws)
+        if ev: ev[4].record(stream)
+        moe.combine(cfg, b.y_perm, b.row_map, b.topk_prob, b.y)
+        if ev: ev[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    moe.check(b.ws)
+    R = int(b.expert_offsets[-1].item())
+    tpe = b.tokens_per_expert.cpu().numpy()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    clocks = ClockSampler(local, enabled=not args.no_clocks and rank == 0)
+    if clocks.proc is not None:
+        time.sleep(0.5)  # let the sampler start before the timed region
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        step(events[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    clk = clocks.stop()
+    moe.check(b.ws)
+
+    stage_ms = {s: [events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps)]
+                for j, s in enumerate(STAGES)}
+    step_ms = [events[i][0].elapsed_time(events[i][5]) for i in range(args.steps)]
+    ms = sum(step_ms) / len(step_ms)
+    ms_all = max_over_ranks(ms, world)
+
+    # ---- e2e: moe_forward with host (pinned) input and output in the timed region
+    e2e = None
+    if not args.no_e2e:
+        x_host = inp["x"].cpu().pin_memory()
+        y_host = torch.empty(b.y.shape, dtype=b.y.dtype).pin_memory()
+        x_dev = torch.empty_like(inp["x"])
+        y_dev = torch.empty_like(b.y)
+        ws2 = moe.alloc_workspace(cfg, dev)
+
+        def fwd():
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.forward(cfg, x_dev, inp["Wg"], inp["gate_bias"], inp["expert_bias"], inp["W1"],
+                        inp["W3"], inp["W2"], y_dev, ws2)
+            y_host.copy_(y_dev, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            fwd()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        barrier(world)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        moe.check(ws2)
+        e2e_ms = max_over_ranks(sum(a.elapsed_time(c) for a, c in ev) / args.steps, world)
+        e2e = {"value": world * w.T / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+               "d2h_bytes_per_step": y_host.numel() * y_host.element_size(),
+               "api": "moe_forward (C ABI) with pinned host x/y copies inside the timed region"}
+
+    if rank != 0:
+        return None
+
+    peaks = measured_peaks()
+    work = stage_work(w, R)
+    stages = {}
+    for s in STAGES:
+        t = sum(stage_ms[s]) / len(stage_ms[s])
+        ent = {"ms": t, "share": t / ms}
+        if "flops" in work[s]:
+            ent["tflops"] = work[s]["flops"] / (t * 1e-3) / 1e12
+        if "bytes" in work[s]:
+            ent["gbs"] = work[s]["bytes"] / (t * 1e-3) / 1e9
+        stages[s] = ent
+    gemm_ms = stages["fc1"]["ms"] + stages["fc2"]["ms"]
+    gemm_tflops = (work["fc1"]["flops"] + work["fc2"]["flops"]) / (gemm_ms * 1e-3) / 1e12
+
+    dom = max(STAGES, key=lambda s: stages[s]["ms"])
+    if dom in ("fc1", "fc2") and w.dtype == "bf16":
+        roof = {"kernel": "tc_grouped_kernel<%s>" % dom.upper(), "bound": "tensor",
+                "achieved": stages[dom]["tflops"], "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": stages[dom].get("gbs"),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"] if roof["achieved"] else None
+    roof["peak_source"] = "%s (MEASURED_PEAKS.json burst)" % peaks["source"] \
+        if peaks["source"] == "measured" else "fallback"
+    roof["traffic"] = recorded_traffic(dom, w.name)
+    roof["algorithmic_per_launch"] = work[dom].get("flops") if roof["unit"] == "TFLOP/s" \
+        else work[dom].get("bytes")
+
+    line = {
+        "metric": METRIC, "value": world * w.T / (ms_all / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded, x~N(0,%g), weights~N(0,%g), random-init)" % (w.x_std, w.w_std),
+        "config": dict(workload_desc(w), parallelism="replicas" if world > 1 else "single"),
+        "grouped_gemm_tflops": gemm_tflops,
+        "stages": stages,
+        "rows": R, "tokens_per_expert_cv": float(np.std(tpe) / max(np.mean(tpe), 1e-9)),
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": kernels_per_forward(w, cfg) * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+        "peaks": peaks,
+    }
+    return line
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def np_view(t):
+    """A CPU tensor as the numpy array the oracle takes (bf16 as uint16 bits)."""
+    if t is None:
+        return None
+    t = t.contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def oracle_sample_run(w, inp_cpu, tokens, nthreads=0):
+    """Oracle forward on the given token rows; returns seconds."""
+    import oracle
+    x = inp_cpu["x"][torch.from_numpy(tokens)]
+    t0 = time.perf_counter()
+    oracle.forward(np_view(x), np_view(inp_cpu["Wg"]), np_view(inp_cpu["W1"]),
+                   np_view(inp_cpu["W3"]), np_view(inp_cpu["W2"]), w.k, w.score,
+                   np_view(inp_cpu["gate_bias"]), np_view(inp_cpu["expert_bias"]),
+                   0.0 if w.capacity_factor <= 0 else w.capacity_factor * w.T / len(tokens),
+                   w.min_capacity, w.drop_policy, nthreads)
+    return time.perf_counter() - t0
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_inputs(w, device_inputs=None):
+    """The workload's inputs on the host (copied from the device if given)."""
+    if device_inputs is not None:
+        return {k: (None if v is None else v.detach().cpu()) for k, v in device_inputs.items()}
+    return synthetic.generate(w, device="cpu")
+
+
+def cpu_baseline(w, inp_cpu, budget_s=15.0):
+    """Oracle tokens/s on the host cores: a 4-token probe sizes one timed
+    sample of about `budget_s` seconds."""
+    cores = host_cores()
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(w.T, size=min(4, w.T), replace=False))
+    per_token = oracle_sample_run(w, inp_cpu, probe, cores) / len(probe)
+    n = int(min(w.T, max(4, budget_s / max(per_token, 1e-6))))
+    toks = np.sort(rng.choice(w.T, size=n, replace=False))
+    sec = oracle_sample_run(w, inp_cpu, toks, cores)
+    return {"value": n / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "cpu": cpu_model(), "seconds": sec,
+            "sample": "%d random tokens (fixed seed) of the %s workload; oracle forward (route, "
+                      "permute, SwiGLU experts, combine) in double on %d threads"
+                      % (n, w.name, cores)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = workload_of(args)
+    inp_cpu = cpu_inputs(w)
+    cores = host_cores()
+    rng = np.random.default_rng(1)
+    sample = 8 if w.T * w.k * w.h * w.f > 1e11 else 64
+    for _ in range(min(args.warmup, 1)):
+        oracle_sample_run(w, inp_cpu, np.sort(rng.choice(w.T, sample, replace=False)), cores)
+    times = []
+    for _ in range(args.steps):
+        toks = np.sort(rng.choice(w.T, sample, replace=False))
+        times.append(oracle_sample_run(w, inp_cpu, toks, cores))
+    sec = sum(times) / len(times)
+    value = sample / sec
+    desc = ("%d random tokens of the %s workload per step; CPU oracle (double) on %d threads"
+            % (sample, w.name, cores))
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_desc(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": desc, "cpu": cpu_model()},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = run_native(args, rank, world, local)
+    if line is not None and world == 1 and not args.no_cpu_baseline:
+        import mixture_experts_layer_fp32_gb300 as moe  # noqa: F401
+        w = workload_of(args)
+        dev_inp = synthetic.generate(w, device="cuda", seed=w.seed)
+        inp_cpu = cpu_inputs(w, dev_inp)
+        del dev_inp
+        line["cpu_baseline"] = cpu_baseline(w, inp_cpu)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE layer forward.
+ *
+ * One MoE layer forward on one GPU: route -> (capacity drop) -> permute ->
+ * grouped SwiGLU experts -> combine.  The operation is the one described on
+ * the page "MoE我们喜欢你（三）：Megatron Core MoE 源码路径解析"
+ * (r00kie-liu.github.io), §2 "MoE layer 主路径: route -> dispatch -> experts
+ * -> combine", with the router of §3-§5, token dropping of §8, the
+ * dispatcher's local permutation of §9 and the grouped experts of §10; and
+ * on "MoE Internals: DeepSpeed-Megatron Expert Parallel Implementation"
+ * (duoan.github.io), §8 "The All-to-All path" steps 2-4 and 6-8 (the
+ * all-to-all exchanges are absent: one GPU, no collectives).
+ *
+ * Conventions (all entry points):
+ *  - Pointers are DEVICE pointers owned by the caller, unless stated.  The
+ *    library never allocates device memory; scratch comes from `ws`.
+ *  - Every tensor is row-major and contiguous.  Device pointers must be
+ *    16-byte aligned (MOE_ERR_INVALID_ARG otherwise).
+ *  - Calls are asynchronous on `stream` and never synchronise the host.
+ *    Per-expert counts stay on the device.
+ *  - Argument errors are reported before anything is enqueued.  A failed
+ *    launch returns MOE_ERR_CUDA.  Device-side checks (an expert id out of
+ *    range, a bounded wait that ran out) set a sticky error word inside
+ *    `ws`; moe_check() reads and clears it.
+ *  - `ws` must be zero-filled once before its first use (the error word
+ *    lives at its start); it is carved internally and may be reused by any
+ *    call with the same configuration.  Its size is given by
+ *    moe_workspace_size().
+ *  - dtype: MOE_BF16 (x, W1/W3/W2, h_mid and y in bf16; tensor-core GEMMs
+ *    with fp32 accumulation) or MOE_F32 (everything fp32; SIMT fp32 GEMMs).
+ *    The router (Wg, biases, logits, probabilities) is always fp32, as the
+ *    router dtype of §3 of the Megatron Core page.
+ *  - Shape limits: 1 <= E <= 256, 1 <= k <= min(E, 8), T >= 0, h and f
+ *    multiples of 8.  The bf16 path further needs h % 256 == 0 and
+ *    f % 128 == 0 (MOE_ERR_UNSUPPORTED otherwise).
+ */
+#ifndef MOE_GB300_H_
+#define MOE_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+#define MOE_MAX_EXPERTS 256
+#define MOE_MAX_TOPK 8
+
+typedef struct CUstream_st* moe_stream_t; /* == cudaStream_t; NULL = legacy default stream */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = 2,   /* shape outside the limits above */
+  MOE_ERR_WORKSPACE = 3,     /* ws too small */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_CHECK = 5,  /* a kernel found an invalid index (moe_check) */
+  MOE_ERR_TIMEOUT = 6        /* a bounded device wait ran out (moe_check) */
+} moe_status;
+
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Score functions of §5 of the Megatron Core page (topk_routing_with_score_function). */
+typedef enum moe_score {
+  MOE_SCORE_SOFTMAX_POST = 0, /* top-k on logits, softmax over the k ("renormalised") */
+  MOE_SCORE_SOFTMAX_PRE = 1,  /* softmax over all E, then top-k, no renormalisation */
+  MOE_SCORE_SIGMOID = 2       /* sigmoid; expert_bias only chooses; p = s/(sum s + 1e-20) */
+} moe_score;
+
+/* Drop policies of §8 of the Megatron Core page (apply_router_token_dropping). */
+typedef enum moe_drop_policy {
+  MOE_DROP_PROBS = 0,    /* keep the `capacity` highest-probability tokens of an expert */
+  MOE_DROP_POSITION = 1  /* keep the first `capacity` tokens in token order */
+} moe_drop_policy;
+
+typedef struct moe_config {
+  int32_t num_tokens;     /* T */
+  int32_t hidden;         /* h */
+  int32_t num_experts;    /* E */
+  int32_t topk;           /* k */
+  int32_t ffn_hidden;     /* f, the expert's intermediate size */
+  int32_t score;          /* moe_score */
+  int32_t dtype;          /* moe_dtype */
+  int32_t drop_policy;    /* moe_drop_policy (used only when capacity_factor > 0) */
+  float capacity_factor;  /* <= 0: dropless */
+  int32_t min_capacity;   /* capacity is raised to at least this (default 0) */
+} moe_config;
+
+/* ABI version of the loaded library (MOE_ABI_VERSION). */
+int32_t moe_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status s);
+
+/* Text of the last CUDA runtime error behind an MOE_ERR_CUDA returned on the
+ * calling host thread ("" if none). */
+const char* moe_last_cuda_error(void);
+
+/* Per-expert capacity of §8 of the Megatron Core page: get_capacity(T*k, E, cf),
+ * read as ceil((T*k/E)*cf) raised to min_capacity.  *capacity = -1 when
+ * dropless (capacity_factor <= 0).  Host-only. */
+moe_status moe_capacity(const moe_config* cfg, int64_t* capacity);
+
+/* Bytes of workspace needed by every entry point for this configuration
+ * (the forward's need, which covers each stage).  Host-only. */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Row capacity of the permuted buffers: T*k (every pair kept). */
+moe_status moe_max_rows(const moe_config* cfg, int64_t* rows);
+
+/*
+ * Router: §3 gating (logits = x.Wg + gate_bias in fp32), §4-§5 scoring and
+ * top-k, and §8 token dropping when capacity_factor > 0.
+ *   x            [T,h]  dtype
+ *   Wg           [h,E]  fp32 (row i = the E gate weights of input feature i)
+ *   gate_bias    [E]    fp32 or NULL: added to the logits (a skew of the router)
+ *   expert_bias  [E]    fp32 or NULL: sigmoid score only; changes the choice,
+ *                       never the weights
+ *   topk_idx     [T,k]  int32 out: experts, by selection score descending
+ *                       (equal scores: lower expert index first)
+ *   topk_prob    [T,k]  fp32 out: combine weights; 0 for dropped pairs
+ *   keep         [T,k]  uint8 out: 1 kept, 0 dropped (all 1 when dropless)
+ *   tokens_per_expert [E] int32 out: kept pairs per expert
+ *   routing_map  [T,E]  uint8 out or NULL: 1 where (t,e) is a kept pair
+ */
+moe_status moe_route(const moe_config* cfg, const void* x, const float* Wg,
+                     const float* gate_bias, const float* expert_bias, int32_t* topk_idx,
+                     float* topk_prob, uint8_t* keep, int32_t* tokens_per_expert,
+                     uint8_t* routing_map, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Local permutation of §9 (dispatch_preprocess; sequence-major ->
+ * expert-major): kept pair (t,j) with expert e goes to row
+ * expert_offsets[e] + #{t' < t with a kept pair to e} (stable).
+ *   x              [T,h]       dtype
+ *   topk_idx, keep [T,k]       as produced by moe_route (keep may be NULL = all kept)
+ *   x_perm         [T*k,h]     dtype out: rows [0, R) filled, R = expert_offsets[E]
+ *   row_map        [T,k]       int32 out: row of each pair, -1 if dropped
+ *   expert_offsets [E+1]       int32 out: exclusive prefix of kept counts
+ * An expert id outside [0,E) is skipped and flagged (MOE_ERR_DEVICE_CHECK).
+ */
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                       const uint8_t* keep, void* x_perm, int32_t* row_map,
+                       int32_t* expert_offsets, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/*
+ * Grouped expert MLP of §10 (TEGroupedMLP: every local expert in one call),
+ * SwiGLU: for the rows [expert_offsets[e], expert_offsets[e+1]) of expert e,
+ *   h_mid = silu(x_perm . W1[e]) * (x_perm . W3[e]),  y_perm = h_mid . W2[e].
+ *   x_perm [T*k,h] dtype, W1/W3 [E,h,f] dtype, W2 [E,f,h] dtype,
+ *   h_mid [T*k,f] dtype out, y_perm [T*k,h] fp32 out (rows >= R untouched).
+ * moe_grouped_fc1 / moe_grouped_fc2 are the two halves.
+ */
+moe_status moe_grouped_mlp(const moe_config* cfg, const void* x_perm,
+                           const int32_t* expert_offsets, const void* W1, const void* W3,
+                           const void* W2, void* h_mid, float* y_perm, void* ws,
+                           size_t ws_bytes, moe_stream_t stream);
+moe_status moe_grouped_fc1(const moe_config* cfg, const void* x_perm,
+                           const int32_t* expert_offsets, const void* W1, const void* W3,
+                           void* h_mid, void* ws, size_t ws_bytes, moe_stream_t stream);
+moe_status moe_grouped_fc2(const moe_config* cfg, const void* h_mid,
+                           const int32_t* expert_offsets, const void* W2, float* y_perm,
+                           void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Combine (§2 combine / the unpermute-and-weight step 8 of the DeepSpeed
+ * page): y[t] = sum over kept slots j, in slot order, of
+ * topk_prob[t,j] * y_perm[row_map[t,j]], accumulated in fp32 and rounded
+ * once to dtype.  A token with no kept pair gets 0.
+ *   y_perm [T*k,h] fp32, row_map [T,k] int32, topk_prob [T,k] fp32, y [T,h] dtype out.
+ */
+moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* row_map,
+                       const float* topk_prob, void* y, moe_stream_t stream);
+
+/*
+ * The whole layer forward (route -> drop -> permute -> experts -> combine),
+ * enqueued on `stream` without a host synchronisation.  Intermediates live in
+ * `ws`.  topk_idx / topk_prob / tokens_per_expert may be NULL (kept in ws)
+ * or caller buffers of the shapes given for moe_route.
+ */
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
+                       const float* gate_bias, const float* expert_bias, const void* W1,
+                       const void* W3, const void* W2, void* y, int32_t* topk_idx,
+                       float* topk_prob, int32_t* tokens_per_expert, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/* Reads and clears the device error word in `ws` (synchronises `stream`):
+ * MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT.  *info (nullable) gets
+ * the first failing index or wait site. */
+moe_status moe_check(void* ws, moe_stream_t stream, int32_t* info);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H_ */

@@ -1,0 +1,214 @@
+"""ctypes binding of libmoe_gb300.so (include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the CUDA library.
+Tensors are torch CUDA tensors (contiguous); the current torch stream is
+passed to the library.  There is no CPU or PyTorch fallback: if the
+library is missing, `lib()` raises.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmoe_gb300.so")
+
+SCORE = {"softmax_post": 0, "softmax_pre": 1, "sigmoid": 2}
+DTYPE = {"f32": 0, "bf16": 1}
+DROP_POLICY = {"probs": 0, "position": 1}
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_CHECK", 6: "MOE_ERR_TIMEOUT"}
+
+# every function declared in include/moe.h
+EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_capacity",
+           "moe_workspace_size", "moe_max_rows", "moe_route", "moe_permute", "moe_grouped_mlp",
+           "moe_grouped_fc1", "moe_grouped_fc2", "moe_combine", "moe_forward", "moe_check"]
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("num_experts", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("ffn_hidden", ctypes.c_int32), ("score", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("drop_policy", ctypes.c_int32),
+                ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code, where, detail=""):
+        self.code = code
+        msg = "%s failed: %s" % (where, STATUS.get(code, code))
+        if detail:
+            msg += " (%s)" % detail
+        super().__init__(msg)
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libmoe_gb300.so is not built (expected at %s); run "
+                               "mixture_experts_layer_fp32_gb300.build.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, i32, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64
+        cfgp = ctypes.POINTER(MoeConfig)
+        sig = {
+            "moe_abi_version": ([], i32),
+            "moe_status_string": ([i32], ctypes.c_char_p),
+            "moe_last_cuda_error": ([], ctypes.c_char_p),
+            "moe_capacity": ([cfgp, ctypes.POINTER(i64)], i32),
+            "moe_workspace_size": ([cfgp, ctypes.POINTER(sz)], i32),
+            "moe_max_rows": ([cfgp, ctypes.POINTER(i64)], i32),
+            "moe_route": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_permute": ([cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_grouped_mlp": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_grouped_fc1": ([cfgp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_grouped_fc2": ([cfgp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_combine": ([cfgp, vp, vp, vp, vp, vp], i32),
+            "moe_forward": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_check": ([vp, vp, ctypes.POINTER(i32)], i32),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def config(T, h, E, k, f, score="softmax_post", dtype="bf16", capacity_factor=0.0,
+           min_capacity=0, drop_policy="probs"):
+    return MoeConfig(int(T), int(h), int(E), int(k), int(f), SCORE[score], DTYPE[dtype],
+                     DROP_POLICY[drop_policy], float(capacity_factor), int(min_capacity))
+
+
+def _check(code, where):
+    if code != 0:
+        detail = lib().moe_last_cuda_error().decode() if code == 4 else ""
+        raise MoeError(code, where, detail)
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device (no CPU path exists)")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ws(ws):
+    return _p(ws), ws.numel() * ws.element_size()
+
+
+def act_dtype(cfg):
+    return torch.float32 if cfg.dtype == DTYPE["f32"] else torch.bfloat16
+
+
+def capacity(cfg):
+    v = ctypes.c_int64()
+    _check(lib().moe_capacity(ctypes.byref(cfg), ctypes.byref(v)), "moe_capacity")
+    return v.value
+
+
+def workspace_size(cfg):
+    v = ctypes.c_size_t()
+    _check(lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(v)), "moe_workspace_size")
+    return v.value
+
+
+def max_rows(cfg):
+    v = ctypes.c_int64()
+    _check(lib().moe_max_rows(ctypes.byref(cfg), ctypes.byref(v)), "moe_max_rows")
+    return v.value
+
+
+def alloc_workspace(cfg, device="cuda"):
+    """Zero-filled workspace of moe_workspace_size(cfg) bytes."""
+    return torch.zeros(workspace_size(cfg), dtype=torch.uint8, device=device)
+
+
+def route(cfg, x, Wg, gate_bias, expert_bias, topk_idx, topk_prob, keep, tokens_per_expert,
+          routing_map, ws):
+    w, wb = _ws(ws)
+    _check(lib().moe_route(ctypes.byref(cfg), _p(x), _p(Wg), _p(gate_bias), _p(expert_bias),
+                           _p(topk_idx), _p(topk_prob), _p(keep), _p(tokens_per_expert),
+                           _p(routing_map), w, wb, _stream()), "moe_route")
+
+
+def permute(cfg, x, topk_idx, keep, x_perm, row_map, expert_offsets, ws):
+    w, wb = _ws(ws)
+    _check(lib().moe_permute(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(keep), _p(x_perm),
+                             _p(row_map), _p(expert_offsets), w, wb, _stream()), "moe_permute")
+
+
+def grouped_fc1(cfg, x_perm, expert_offsets, W1, W3, h_mid, ws):
+    w, wb = _ws(ws)
+    _check(lib().moe_grouped_fc1(ctypes.byref(cfg), _p(x_perm), _p(expert_offsets), _p(W1),
+                                 _p(W3), _p(h_mid), w, wb, _stream()), "moe_grouped_fc1")
+
+
+def grouped_fc2(cfg, h_mid, expert_offsets, W2, y_perm, ws):
+    w, wb = _ws(ws)
+    _check(lib().moe_grouped_fc2(ctypes.byref(cfg), _p(h_mid), _p(expert_offsets), _p(W2),
+                                 _p(y_perm), w, wb, _stream()), "moe_grouped_fc2")
+
+
+def grouped_mlp(cfg, x_perm, expert_offsets, W1, W3, W2, h_mid, y_perm, ws):
+    w, wb = _ws(ws)
+    _check(lib().moe_grouped_mlp(ctypes.byref(cfg), _p(x_perm), _p(expert_offsets), _p(W1),
+                                 _p(W3), _p(W2), _p(h_mid), _p(y_perm), w, wb, _stream()),
+           "moe_grouped_mlp")
+
+
+def combine(cfg, y_perm, row_map, topk_prob, y):
+    _check(lib().moe_combine(ctypes.byref(cfg), _p(y_perm), _p(row_map), _p(topk_prob), _p(y),
+                             _stream()), "moe_combine")
+
+
+def forward(cfg, x, Wg, gate_bias, expert_bias, W1, W3, W2, y, ws, topk_idx=None,
+            topk_prob=None, tokens_per_expert=None):
+    w, wb = _ws(ws)
+    _check(lib().moe_forward(ctypes.byref(cfg), _p(x), _p(Wg), _p(gate_bias), _p(expert_bias),
+                             _p(W1), _p(W3), _p(W2), _p(y), _p(topk_idx), _p(topk_prob),
+                             _p(tokens_per_expert), w, wb, _stream()), "moe_forward")
+
+
+def check(ws):
+    """Synchronises the current stream and raises if a kernel flagged an error."""
+    info = ctypes.c_int32(0)
+    code = lib().moe_check(_p(ws), _stream(), ctypes.byref(info))
+    if code != 0:
+        raise MoeError(code, "device check", "info=%d" % info.value)
+
+
+class Buffers:
+    """Device buffers of one forward, allocated with torch (plumbing only)."""
+
+    def __init__(self, cfg, device="cuda"):
+        T, h, E, k, f = cfg.num_tokens, cfg.hidden, cfg.num_experts, cfg.topk, cfg.ffn_hidden
+        R = max_rows(cfg)
+        dt = act_dtype(cfg)
+        d = torch.device(device)
+        self.topk_idx = torch.empty((T, k), dtype=torch.int32, device=d)
+        self.topk_prob = torch.empty((T, k), dtype=torch.float32, device=d)
+        self.keep = torch.empty((T, k), dtype=torch.uint8, device=d)
+        self.tokens_per_expert = torch.empty((E,), dtype=torch.int32, device=d)
+        self.routing_map = torch.empty((T, E), dtype=torch.uint8, device=d)
+        self.x_perm = torch.empty((R, h), dtype=dt, device=d)
+        self.row_map = torch.empty((T, k), dtype=torch.int32, device=d)
+        self.expert_offsets = torch.empty((E + 1,), dtype=torch.int32, device=d)
+        self.h_mid = torch.empty((R, f), dtype=dt, device=d)
+        self.y_perm = torch.empty((R, h), dtype=torch.float32, device=d)
+        self.y = torch.empty((T, h), dtype=dt, device=d)
+        self.ws = alloc_workspace(cfg, d)

@@ -1,0 +1,419 @@
+// C ABI of the MoE layer forward: argument validation, workspace carve-up and
+// the launch sequence of each stage.  No device memory is allocated here;
+// nothing synchronises the host except moe_check().
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  if (dev >= 64) {
+    int n = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
+  }
+  if (cache[dev] == 0) {
+    int n = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+}  // namespace moe
+
+namespace {
+
+using namespace moe;
+
+thread_local char g_last_cuda_error[256] = "";
+
+struct Layout {
+  size_t err, logits, assigned, tiles, cand_rowmap, cand_src, cand_off, cand_tiles;
+  size_t topk_idx, topk_prob, keep, tpe, offsets, row_map, x_perm, h_mid, y_perm, total;
+};
+
+size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+Layout make_layout(const moe_config& c) {
+  Layout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t r = o;
+    o = align_up(o + bytes);
+    return r;
+  };
+  const size_t T = c.num_tokens, k = c.topk, E = c.num_experts, h = c.hidden, f = c.ffn_hidden;
+  const size_t np = T * k;
+  const size_t nt = static_cast<size_t>(perm_tiles(static_cast<int64_t>(np)));
+  const size_t el = c.dtype == MOE_F32 ? 4 : 2;
+  L.err = take(kErrBytes);
+  L.logits = take(T * E * 4);
+  L.assigned = take(E * 4);
+  L.tiles = take(nt * E * 4);
+  L.cand_rowmap = take(np * 4);
+  L.cand_src = take(np * 4);
+  L.cand_off = take((E + 1) * 4);
+  L.cand_tiles = take(nt * E * 4);
+  L.topk_idx = take(np * 4);
+  L.topk_prob = take(np * 4);
+  L.keep = take(np);
+  L.tpe = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.row_map = take(np * 4);
+  L.x_perm = take(np * h * el);
+  L.h_mid = take(np * f * el);
+  L.y_perm = take(np * h * 4);
+  L.total = o;
+  return L;
+}
+
+moe_status validate(const moe_config* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->num_tokens < 0 || c->hidden <= 0 || c->num_experts <= 0 || c->topk <= 0 ||
+      c->ffn_hidden <= 0 || c->min_capacity < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->score < MOE_SCORE_SOFTMAX_POST || c->score > MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->drop_policy != MOE_DROP_PROBS && c->drop_policy != MOE_DROP_POSITION)
+    return MOE_ERR_INVALID_ARG;
+  if (isnan(c->capacity_factor) || isinf(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+  if (c->num_experts > MOE_MAX_EXPERTS || c->topk > MOE_MAX_TOPK || c->topk > c->num_experts)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->hidden % 8 != 0 || c->ffn_hidden % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->dtype == MOE_BF16 && (c->hidden % 256 != 0 || c->ffn_hidden % 128 != 0))
+    return MOE_ERR_UNSUPPORTED;
+  const int64_t np = static_cast<int64_t>(c->num_tokens) * c->topk;
+  if (np > (int64_t{1} << 30)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// A device tensor argument: nullptr allowed only when it has no elements.
+moe_status need(const void* p, size_t nelem, size_t align) {
+  if (nelem == 0) return MOE_OK;
+  if (p == nullptr) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(p) % align != 0) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+moe_status optional(const void* p, size_t align) {
+  if (p != nullptr && reinterpret_cast<uintptr_t>(p) % align != 0) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+#define MOE_TRY(expr)                          \
+  do {                                         \
+    const moe_status st_ = (expr);             \
+    if (st_ != MOE_OK) return st_;             \
+  } while (0)
+
+moe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s", cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+int64_t capacity_of(const moe_config& c) {
+  if (c.capacity_factor <= 0.f) return -1;
+  const double v = ceil((static_cast<double>(c.num_tokens) * c.topk / c.num_experts) *
+                        static_cast<double>(c.capacity_factor));
+  int64_t cap = static_cast<int64_t>(v);
+  if (cap < c.min_capacity) cap = c.min_capacity;
+  return cap;
+}
+
+moe_status check_ws(const moe_config& c, const void* ws, size_t ws_bytes) {
+  if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < make_layout(c).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+size_t elt(const moe_config& c) { return c.dtype == MOE_F32 ? 4 : 2; }
+
+// ---- stage bodies (arguments already validated) ----
+
+moe_status do_route(const moe_config& c, const void* x, const float* Wg, const float* gb,
+                    const float* eb, int32_t* topk_idx, float* topk_prob, uint8_t* keep,
+                    int32_t* tpe, uint8_t* routing_map, void* ws, cudaStream_t s) {
+  const Layout L = make_layout(c);
+  const int T = c.num_tokens, E = c.num_experts, k = c.topk;
+  int* err = at<int>(ws, L.err);
+  const int64_t cap = capacity_of(c);
+  const bool drops = cap >= 0 && cap < T;
+  MOE_CUDA(cudaMemsetAsync(tpe, 0, E * sizeof(int32_t), s));
+  if (T == 0) return MOE_OK;
+  float* logits = at<float>(ws, L.logits);
+  MOE_CUDA(launch_router_logits(T, c.hidden, E, c.dtype, x, Wg, gb, logits, s));
+  if (!drops) {
+    MOE_CUDA(launch_router_topk(T, E, k, c.score, logits, eb, topk_idx, topk_prob, keep,
+                                routing_map, tpe, err, s));
+    return MOE_OK;
+  }
+  int32_t* assigned = at<int32_t>(ws, L.assigned);
+  MOE_CUDA(cudaMemsetAsync(assigned, 0, E * sizeof(int32_t), s));
+  MOE_CUDA(launch_router_topk(T, E, k, c.score, logits, eb, topk_idx, topk_prob, keep, routing_map,
+                              assigned, err, s));
+  // candidate lists: every routed pair, expert-major, ascending token order
+  const int64_t np = static_cast<int64_t>(T) * k;
+  const int64_t nt = perm_tiles(np);
+  int32_t* ctiles = at<int32_t>(ws, L.cand_tiles);
+  int32_t* coff = at<int32_t>(ws, L.cand_off);
+  MOE_CUDA(launch_perm_hist(np, E, topk_idx, nullptr, ctiles, err, s));
+  MOE_CUDA(launch_perm_scan(nt, E, ctiles, coff, nullptr, s));
+  MOE_CUDA(launch_perm_rank(np, E, topk_idx, nullptr, ctiles, at<int32_t>(ws, L.cand_rowmap),
+                            at<int32_t>(ws, L.cand_src), s));
+  MOE_CUDA(launch_drop_select(T, E, k, cap, c.drop_policy, coff, at<int32_t>(ws, L.cand_src),
+                              topk_prob, keep, routing_map, tpe, s));
+  return MOE_OK;
+}
+
+moe_status do_permute(const moe_config& c, const void* x, const int32_t* topk_idx,
+                      const uint8_t* keep, void* x_perm, int32_t* row_map, int32_t* offsets,
+                      void* ws, cudaStream_t s) {
+  const Layout L = make_layout(c);
+  const int T = c.num_tokens, E = c.num_experts, k = c.topk;
+  int* err = at<int>(ws, L.err);
+  const int64_t np = static_cast<int64_t>(T) * k;
+  if (np == 0) {
+    MOE_CUDA(cudaMemsetAsync(offsets, 0, (E + 1) * sizeof(int32_t), s));
+    return MOE_OK;
+  }
+  int32_t* tiles = at<int32_t>(ws, L.tiles);
+  MOE_CUDA(launch_perm_hist(np, E, topk_idx, keep, tiles, err, s));
+  MOE_CUDA(launch_perm_scan(perm_tiles(np), E, tiles, offsets, nullptr, s));
+  MOE_CUDA(launch_perm_rank(np, E, topk_idx, keep, tiles, row_map, nullptr, s));
+  MOE_CUDA(launch_perm_copy(T, c.hidden, k, c.dtype, x, row_map, x_perm, s));
+  return MOE_OK;
+}
+
+moe_status do_fc1(const moe_config& c, const void* x_perm, const int32_t* offsets, const void* W1,
+                  const void* W3, void* h_mid, void* ws, cudaStream_t s) {
+  const Layout L = make_layout(c);
+  int* err = at<int>(ws, L.err);
+  const int64_t rows = static_cast<int64_t>(c.num_tokens) * c.topk;
+  if (c.dtype == MOE_F32)
+    MOE_CUDA(launch_simt_fc1(c.num_experts, c.hidden, c.ffn_hidden, rows,
+                             static_cast<const float*>(x_perm), offsets,
+                             static_cast<const float*>(W1), static_cast<const float*>(W3),
+                             static_cast<float*>(h_mid), err, s));
+  else
+    MOE_CUDA(launch_tc_fc1(c.num_experts, c.hidden, c.ffn_hidden, rows, x_perm, offsets, W1, W3,
+                           h_mid, err, s));
+  return MOE_OK;
+}
+
+moe_status do_fc2(const moe_config& c, const void* h_mid, const int32_t* offsets, const void* W2,
+                  float* y_perm, void* ws, cudaStream_t s) {
+  const Layout L = make_layout(c);
+  int* err = at<int>(ws, L.err);
+  const int64_t rows = static_cast<int64_t>(c.num_tokens) * c.topk;
+  if (c.dtype == MOE_F32)
+    MOE_CUDA(launch_simt_fc2(c.num_experts, c.hidden, c.ffn_hidden, rows,
+                             static_cast<const float*>(h_mid), offsets,
+                             static_cast<const float*>(W2), y_perm, err, s));
+  else
+    MOE_CUDA(launch_tc_fc2(c.num_experts, c.hidden, c.ffn_hidden, rows, h_mid, offsets, W2, y_perm,
+                           err, s));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char* moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+moe_status moe_capacity(const moe_config* cfg, int64_t* capacity) {
+  MOE_TRY(validate(cfg));
+  if (capacity == nullptr) return MOE_ERR_INVALID_ARG;
+  *capacity = capacity_of(*cfg);
+  return MOE_OK;
+}
+
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_max_rows(const moe_config* cfg, int64_t* rows) {
+  MOE_TRY(validate(cfg));
+  if (rows == nullptr) return MOE_ERR_INVALID_ARG;
+  *rows = static_cast<int64_t>(cfg->num_tokens) * cfg->topk;
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const float* Wg,
+                     const float* gate_bias, const float* expert_bias, int32_t* topk_idx,
+                     float* topk_prob, uint8_t* keep, int32_t* tokens_per_expert,
+                     uint8_t* routing_map, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  const size_t T = c.num_tokens, E = c.num_experts, k = c.topk;
+  MOE_TRY(need(x, T * c.hidden, 16));
+  MOE_TRY(need(Wg, c.hidden * E, 4));
+  MOE_TRY(optional(gate_bias, 4));
+  MOE_TRY(optional(expert_bias, 4));
+  MOE_TRY(need(topk_idx, T * k, 4));
+  MOE_TRY(need(topk_prob, T * k, 4));
+  MOE_TRY(need(keep, T * k, 1));
+  MOE_TRY(need(tokens_per_expert, E, 4));
+  MOE_TRY(optional(routing_map, 1));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  return do_route(c, x, Wg, gate_bias, expert_bias, topk_idx, topk_prob, keep, tokens_per_expert,
+                  routing_map, ws, stream);
+}
+
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                       const uint8_t* keep, void* x_perm, int32_t* row_map,
+                       int32_t* expert_offsets, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  const size_t T = c.num_tokens, k = c.topk;
+  MOE_TRY(need(x, T * c.hidden, 16));
+  MOE_TRY(need(topk_idx, T * k, 4));
+  MOE_TRY(optional(keep, 1));
+  MOE_TRY(need(x_perm, T * k * c.hidden, 16));
+  MOE_TRY(need(row_map, T * k, 4));
+  MOE_TRY(need(expert_offsets, c.num_experts + 1, 4));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  return do_permute(c, x, topk_idx, keep, x_perm, row_map, expert_offsets, ws, stream);
+}
+
+moe_status moe_grouped_fc1(const moe_config* cfg, const void* x_perm,
+                           const int32_t* expert_offsets, const void* W1, const void* W3,
+                           void* h_mid, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  const size_t R = static_cast<size_t>(c.num_tokens) * c.topk;
+  const size_t wsz = static_cast<size_t>(c.num_experts) * c.hidden * c.ffn_hidden;
+  MOE_TRY(need(x_perm, R * c.hidden, 16));
+  MOE_TRY(need(expert_offsets, c.num_experts + 1, 4));
+  MOE_TRY(need(W1, wsz, 16));
+  MOE_TRY(need(W3, wsz, 16));
+  MOE_TRY(need(h_mid, R * c.ffn_hidden, 16));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  return do_fc1(c, x_perm, expert_offsets, W1, W3, h_mid, ws, stream);
+}
+
+moe_status moe_grouped_fc2(const moe_config* cfg, const void* h_mid,
+                           const int32_t* expert_offsets, const void* W2, float* y_perm,
+                           void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  const size_t R = static_cast<size_t>(c.num_tokens) * c.topk;
+  const size_t wsz = static_cast<size_t>(c.num_experts) * c.hidden * c.ffn_hidden;
+  MOE_TRY(need(h_mid, R * c.ffn_hidden, 16));
+  MOE_TRY(need(expert_offsets, c.num_experts + 1, 4));
+  MOE_TRY(need(W2, wsz, 16));
+  MOE_TRY(need(y_perm, R * c.hidden, 16));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  return do_fc2(c, h_mid, expert_offsets, W2, y_perm, ws, stream);
+}
+
+moe_status moe_grouped_mlp(const moe_config* cfg, const void* x_perm,
+                           const int32_t* expert_offsets, const void* W1, const void* W3,
+                           const void* W2, void* h_mid, float* y_perm, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(moe_grouped_fc1(cfg, x_perm, expert_offsets, W1, W3, h_mid, ws, ws_bytes, stream));
+  return moe_grouped_fc2(cfg, h_mid, expert_offsets, W2, y_perm, ws, ws_bytes, stream);
+}
+
+moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* row_map,
+                       const float* topk_prob, void* y, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  const size_t T = c.num_tokens, k = c.topk;
+  MOE_TRY(need(y_perm, T * k * c.hidden, 16));
+  MOE_TRY(need(row_map, T * k, 4));
+  MOE_TRY(need(topk_prob, T * k, 4));
+  MOE_TRY(need(y, T * c.hidden, 16));
+  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, y_perm, row_map, topk_prob, y,
+                          stream));
+  return MOE_OK;
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
+                       const float* gate_bias, const float* expert_bias, const void* W1,
+                       const void* W3, const void* W2, void* y, int32_t* topk_idx,
+                       float* topk_prob, int32_t* tokens_per_expert, void* ws,
+                       size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  const size_t T = c.num_tokens, E = c.num_experts, k = c.topk, h = c.hidden;
+  const size_t wsz = E * h * c.ffn_hidden;
+  MOE_TRY(need(x, T * h, 16));
+  MOE_TRY(need(Wg, h * E, 4));
+  MOE_TRY(optional(gate_bias, 4));
+  MOE_TRY(optional(expert_bias, 4));
+  MOE_TRY(need(W1, wsz, 16));
+  MOE_TRY(need(W3, wsz, 16));
+  MOE_TRY(need(W2, wsz, 16));
+  MOE_TRY(need(y, T * h, 16));
+  MOE_TRY(optional(topk_idx, 4));
+  MOE_TRY(optional(topk_prob, 4));
+  MOE_TRY(optional(tokens_per_expert, 4));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  const Layout L = make_layout(c);
+  int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
+  float* prob = topk_prob ? topk_prob : at<float>(ws, L.topk_prob);
+  int32_t* tpe = tokens_per_expert ? tokens_per_expert : at<int32_t>(ws, L.tpe);
+  uint8_t* keep = at<uint8_t>(ws, L.keep);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* row_map = at<int32_t>(ws, L.row_map);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* h_mid = at<void>(ws, L.h_mid);
+  float* y_perm = at<float>(ws, L.y_perm);
+  (void)elt;
+  MOE_TRY(do_route(c, x, Wg, gate_bias, expert_bias, idx, prob, keep, tpe, nullptr, ws, stream));
+  MOE_TRY(do_permute(c, x, idx, keep, x_perm, row_map, offsets, ws, stream));
+  MOE_TRY(do_fc1(c, x_perm, offsets, W1, W3, h_mid, ws, stream));
+  MOE_TRY(do_fc2(c, h_mid, offsets, W2, y_perm, ws, stream));
+  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, y_perm, row_map, prob, y,
+                          stream));
+  return MOE_OK;
+}
+
+moe_status moe_check(void* ws, moe_stream_t stream, int32_t* info) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(cudaStreamSynchronize(stream));
+  int32_t w[2] = {0, 0};
+  MOE_CUDA(cudaMemcpyAsync(w, ws, sizeof(w), cudaMemcpyDeviceToHost, stream));
+  MOE_CUDA(cudaStreamSynchronize(stream));
+  if (info) *info = w[1];
+  if (w[0] == DEV_ERR_NONE) return MOE_OK;
+  MOE_CUDA(cudaMemsetAsync(ws, 0, sizeof(w), stream));
+  MOE_CUDA(cudaStreamSynchronize(stream));
+  return w[0] == DEV_ERR_TIMEOUT ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

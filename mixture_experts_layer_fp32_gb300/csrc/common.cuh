@@ -1,0 +1,72 @@
+// Internal declarations shared by the kernels and the C ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Device error word: the first 256 bytes of every workspace.
+//   word[0] = code (0 none, DEV_ERR_INDEX, DEV_ERR_TIMEOUT), word[1] = info.
+enum : int { DEV_ERR_NONE = 0, DEV_ERR_INDEX = 1, DEV_ERR_TIMEOUT = 2 };
+constexpr size_t kErrBytes = 256;
+
+__device__ __forceinline__ void report_error(int* err, int code, int info) {
+  if (err == nullptr) return;
+  if (atomicCAS(err, 0, code) == 0) atomicExch(err + 1, info);
+}
+
+// Pairs handled by one permutation tile (256 threads x 8 pairs).
+constexpr int kPermTile = 2048;
+constexpr int kPermThreads = 256;
+
+inline int64_t perm_tiles(int64_t npairs) { return (npairs + kPermTile - 1) / kPermTile; }
+
+// ---- router ----
+cudaError_t launch_router_logits(int T, int h, int E, int dtype, const void* x, const float* Wg,
+                                 const float* gate_bias, float* logits, cudaStream_t s);
+cudaError_t launch_router_topk(int T, int E, int k, int score, const float* logits,
+                               const float* expert_bias, int32_t* topk_idx, float* topk_prob,
+                               uint8_t* keep, uint8_t* routing_map, int32_t* counts, int* err,
+                               cudaStream_t s);
+cudaError_t launch_drop_select(int T, int E, int k, int64_t capacity, int policy,
+                               const int32_t* cand_offsets, const int32_t* cand_pair,
+                               float* topk_prob, uint8_t* keep, uint8_t* routing_map,
+                               int32_t* kept_per_expert, cudaStream_t s);
+
+// ---- permutation / combine ----
+cudaError_t launch_perm_hist(int64_t npairs, int E, const int32_t* topk_idx, const uint8_t* keep,
+                             int32_t* tile_counts, int* err, cudaStream_t s);
+cudaError_t launch_perm_scan(int64_t ntiles, int E, int32_t* tile_counts, int32_t* offsets,
+                             int32_t* tokens_per_expert, cudaStream_t s);
+cudaError_t launch_perm_rank(int64_t npairs, int E, const int32_t* topk_idx, const uint8_t* keep,
+                             const int32_t* tile_base, int32_t* row_map, int32_t* row_src,
+                             cudaStream_t s);
+cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, const int32_t* row_map,
+                             void* x_perm, cudaStream_t s);
+cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
+                           const int32_t* row_map, const float* topk_prob, void* y, cudaStream_t s);
+
+// ---- grouped GEMMs ----
+// fp32 SIMT path (dtype MOE_F32)
+cudaError_t launch_simt_fc1(int E, int h, int f, int64_t max_rows, const float* x_perm,
+                            const int32_t* offsets, const float* W1, const float* W3,
+                            float* h_mid, int* err, cudaStream_t s);
+cudaError_t launch_simt_fc2(int E, int h, int f, int64_t max_rows, const float* h_mid,
+                            const int32_t* offsets, const float* W2, float* y_perm, int* err,
+                            cudaStream_t s);
+// tcgen05 path (dtype MOE_BF16)
+cudaError_t launch_tc_fc1(int E, int h, int f, int64_t max_rows, const void* x_perm,
+                          const int32_t* offsets, const void* W1, const void* W3, void* h_mid,
+                          int* err, cudaStream_t s);
+cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_mid,
+                          const int32_t* offsets, const void* W2, float* y_perm, int* err,
+                          cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace moe

@@ -1,0 +1,470 @@
+// bf16 grouped expert MLP on the 5th-generation tensor cores (tcgen05).
+//
+// Grouped expert MLP of §10 of "MoE我们喜欢你（三）：Megatron Core MoE 源码路径解析"
+// (r00kie-liu.github.io): all local experts' GEMMs in one launch
+// (TEGroupedMLP / GroupedLinear on that page), with SwiGLU experts:
+//   fc1:  H[r, :] = silu(X[r, :] . W1[e]) * (X[r, :] . W3[e])   (bf16 out)
+//   fc2:  Y[r, :] = H[r, :] . W2[e]                              (fp32 out)
+// for the rows r of expert e, [offsets[e], offsets[e+1]).
+//
+// Design (one CTA per SM, persistent):
+//  * Output tile 128 rows x 256 fp32 accumulator columns in TMEM.  fc1's
+//    256 columns are 128 columns of W1 next to the same 128 columns of W3,
+//    so one M=128,N=256,K=16 MMA produces both halves of the SwiGLU and the
+//    epilogue pairs column j with column 128+j.  fc2's 256 columns are 256
+//    columns of W2.
+//  * The tile list is built on the device from the expert offsets (written
+//    by the permutation kernel): expert e owns ceil(rows_e/128) row blocks x
+//    n-tiles, row blocks inner so that CTAs running together share the
+//    weight tile (L2) and the expert's rows.  No host synchronisation.
+//  * Warp roles: warp 0 lane 0 issues TMA loads (A tile 128x64 and four
+//    64x64 weight boxes per stage, 128-byte swizzle, 4-stage ring), warp 1
+//    allocates TMEM and lane 0 issues tcgen05.mma, warps 2-5 drain TMEM with
+//    tcgen05.ld, apply the epilogue and store.  Two accumulator buffers
+//    (2 x 256 of the 512 TMEM columns) overlap the epilogue of one tile with
+//    the main loop of the next.
+//  * A tile's rows past its expert's end are computed but never stored;
+//    rows past the buffer end are zero-filled by TMA.
+//  * Weights stay in the caller's [E, K, N] layout (N contiguous): the B
+//    operand is MN-major in shared memory.  Activations are K-major.
+//  * Every wait is bounded: after ~2 s without progress the CTA records
+//    MOE_ERR_TIMEOUT in the workspace error word, lets its in-flight copies
+//    and MMAs finish (again bounded), frees its TMEM and exits.
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;                      // MMA N = accumulator columns
+constexpr int BK = 64;                       // bf16 elements in one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+constexpr int BOX_BYTES = 64 * BK * 2;       // 8 KB: 64 (N) x 64 (K) weight box
+constexpr int B_BYTES = 4 * BOX_BYTES;       // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_COLS = BN;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int THREADS = 192;
+constexpr int NUM_BARS = 2 * STAGES + 5;     // full, empty, acc_full[2], acc_empty[2], drain
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 +
+                           2 * (MOE_MAX_EXPERTS + 1) * 4;
+constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, /*b_mn_major=*/true);
+constexpr long long kWaitCycles = 4000000000LL;
+
+enum { FC1 = 0, FC2 = 1 };
+
+struct TcArgs {
+  const int32_t* offsets;
+  int E;
+  int num_n_tiles;
+  int k_blocks;
+  int64_t max_rows;
+  void* out;
+  int ldo;
+  int* err;
+};
+
+struct Ctl {
+  uint64_t* bar;
+  volatile int* abort_flag;
+  int* err;
+  __device__ uint32_t full(int s) const { return ptx::smem_u32(bar + s); }
+  __device__ uint32_t empty(int s) const { return ptx::smem_u32(bar + STAGES + s); }
+  __device__ uint32_t acc_full(int b) const { return ptx::smem_u32(bar + 2 * STAGES + b); }
+  __device__ uint32_t acc_empty(int b) const { return ptx::smem_u32(bar + 2 * STAGES + 2 + b); }
+  __device__ uint32_t drain() const { return ptx::smem_u32(bar + 2 * STAGES + 4); }
+
+  // Bounded wait.  Returns false on timeout (recorded) or, when
+  // `honour_abort`, as soon as another role has given up.
+  __device__ bool wait(uint32_t b, uint32_t parity, int site, bool honour_abort = true) const {
+    const long long t0 = clock64();
+    while (!ptx::mbar_try_wait(b, parity)) {
+      if (honour_abort && *abort_flag) return false;
+      if (clock64() - t0 > kWaitCycles) {
+        *abort_flag = 1;
+        report_error(err, DEV_ERR_TIMEOUT, site);
+        return false;
+      }
+    }
+    return true;
+  }
+};
+
+__device__ __forceinline__ void decode_tile(int tile, const int* tstart, const int* off, int E,
+                                            int& e, int& m0, int& rend, int& nt) {
+  int lo = 0, hi = E;  // largest e in [0, E) with tstart[e] <= tile
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tstart[mid] <= tile) lo = mid; else hi = mid;
+  }
+  e = lo;
+  const int mt = (off[e + 1] - off[e] + BM - 1) / BM;
+  const int u = tile - tstart[e];
+  nt = u / mt;
+  m0 = off[e] + (u - nt * mt) * BM;
+  rend = off[e + 1];
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float silu_mul(float a, float g) { return a / (1.0f + __expf(-a)) * g; }
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB0,
+                      const __grid_constant__ CUtensorMap tmB1, TcArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* off = reinterpret_cast<int*>(tmem_slot + 4);
+  int* tstart = off + (MOE_MAX_EXPERTS + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = args.E;
+  const int NT = args.num_n_tiles;
+  const int KB = args.k_blocks;
+  const Ctl ctl{bars, abort_flag, args.err};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(ctl.full(s), 1);
+      ptx::mbar_init(ctl.empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ctl.acc_full(b), 1);
+      ptx::mbar_init(ctl.acc_empty(b), 4);
+    }
+    ptx::mbar_init(ctl.drain(), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB0);
+    ptx::prefetch_tensormap(&tmB1);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = args.offsets[e];
+  __syncthreads();
+  if (warp == 0) {
+    // tile prefix over experts: lane handles experts [8*lane, 8*lane + 8)
+    constexpr int PER = MOE_MAX_EXPERTS / 32;
+    int v[PER];
+    int run = 0;
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane * PER + i;
+      int t = 0;
+      if (e < E) {
+        const int rows = off[e + 1] - off[e];
+        ok = ok && rows >= 0;
+        t = ((rows + BM - 1) / BM) * NT;
+      }
+      v[i] = t;
+      run += t;
+    }
+    if (lane == 0) ok = ok && off[0] == 0 && static_cast<int64_t>(off[E]) <= args.max_rows;
+    ok = __all_sync(0xffffffffu, ok);
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int excl = incl - run;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane * PER + i;
+      if (e < E) tstart[e] = ok ? excl : 0;
+      excl += v[i];
+    }
+    if (lane == 31) tstart[E] = ok ? excl : 0;
+    if (!ok && lane == 0 && blockIdx.x == 0) report_error(args.err, DEV_ERR_INDEX, -1);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = tstart[E];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t fill_parity = 0, filled = 0;  // per stage: parity of its last fill
+      bool alive = true;
+      for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x) {
+        int e, m0, rend, nt;
+        decode_tile(tile, tstart, off, E, e, m0, rend, nt);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ctl.wait(ctl.empty(stage), phase ^ 1u, 1)) {
+            alive = false;
+            break;
+          }
+          const uint32_t fb = ctl.full(stage);
+          ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t a = ptx::smem_u32(stages + stage * STAGE_BYTES);
+          const uint32_t b = a + A_BYTES;
+          const int kc = kb * BK;
+          ptx::tma_load_2d(a, &tmA, kc, m0, fb);
+          if (MODE == FC1) {
+            const int n0 = nt * (BN / 2);
+            ptx::tma_load_3d(b, &tmB0, n0, kc, e, fb);
+            ptx::tma_load_3d(b + BOX_BYTES, &tmB0, n0 + 64, kc, e, fb);
+            ptx::tma_load_3d(b + 2 * BOX_BYTES, &tmB1, n0, kc, e, fb);
+            ptx::tma_load_3d(b + 3 * BOX_BYTES, &tmB1, n0 + 64, kc, e, fb);
+          } else {
+            const int n0 = nt * BN;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ptx::tma_load_3d(b + q * BOX_BYTES, &tmB0, n0 + 64 * q, kc, e, fb);
+          }
+          filled |= 1u << stage;
+          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (alive) {
+        // every filled stage released by the MMA warp: its commit-arrivals
+        // have landed and no copy is in flight
+        for (int i = 0; i < STAGES; ++i) {
+          if (!ctl.wait(ctl.empty(stage), phase ^ 1u, 2, false)) break;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      } else {
+        // give up: only wait (bounded) for the copies this thread issued
+        for (int s = 0; s < STAGES; ++s)
+          if (filled >> s & 1u) ctl.wait(ctl.full(s), fill_parity >> s & 1u, 3, false);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      bool alive = true;
+      int it = 0;
+      for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!ctl.wait(ctl.acc_empty(buf), aph ^ 1u, 4)) {
+          alive = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + buf * ACC_COLS;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ctl.wait(ctl.full(stage), phase, 5)) {
+            alive = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a = ptx::smem_u32(stages + stage * STAGE_BYTES);
+          const uint32_t b = a + A_BYTES;
+#pragma unroll
+          for (int s = 0; s < BK / 16; ++s) {
+            // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; a K step
+            //    of 16 bf16 moves 32 B inside the swizzled row.
+            // B: MN-major, 128-byte swizzle; 64-column chunks (boxes) 8 KB
+            //    apart (LBO), 8-row K groups 1024 B apart (SBO); a K step of
+            //    16 rows moves 2048 B.
+            const uint64_t adesc = ptx::sw128_desc(a + s * 32, 16, 1024);
+            const uint64_t bdesc = ptx::sw128_desc(b + s * 2048, BOX_BYTES, 1024);
+            ptx::umma_bf16(d, adesc, bdesc, IDESC, (kb | s) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit(ctl.empty(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!alive) break;
+        ptx::umma_commit(ctl.acc_full(buf));
+      }
+      if (!alive) {
+        ptx::umma_commit(ctl.drain());
+        ctl.wait(ctl.drain(), 0, 6, false);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lane quarter this warp may read
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      const int buf = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      int e, m0, rend, nt;
+      decode_tile(tile, tstart, off, E, e, m0, rend, nt);
+      bool ok = ctl.wait(ctl.acc_full(buf), aph, 7);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int row = m0 + q * 32 + lane;
+      const bool valid = row < rend;
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
+      if (MODE == FC1) {
+        __nv_bfloat16* out =
+            static_cast<__nv_bfloat16*>(args.out) + static_cast<int64_t>(row) * args.ldo + nt * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t a[32], g[32];
+          ptx::tmem_ld32(tb + c, a);
+          ptx::tmem_ld32(tb + BN / 2 + c, g);
+          ptx::tmem_wait_ld();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 0]), __uint_as_float(g[8 * v + 0])),
+                                silu_mul(__uint_as_float(a[8 * v + 1]), __uint_as_float(g[8 * v + 1])));
+              w.y = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 2]), __uint_as_float(g[8 * v + 2])),
+                                silu_mul(__uint_as_float(a[8 * v + 3]), __uint_as_float(g[8 * v + 3])));
+              w.z = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 4]), __uint_as_float(g[8 * v + 4])),
+                                silu_mul(__uint_as_float(a[8 * v + 5]), __uint_as_float(g[8 * v + 5])));
+              w.w = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 6]), __uint_as_float(g[8 * v + 6])),
+                                silu_mul(__uint_as_float(a[8 * v + 7]), __uint_as_float(g[8 * v + 7])));
+              dst[v] = w;
+            }
+          }
+        }
+      } else {
+        float* out = static_cast<float*>(args.out) + static_cast<int64_t>(row) * args.ldo + nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t y[32];
+          ptx::tmem_ld32(tb + c, y);
+          ptx::tmem_wait_ld();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(out + c);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(y[4 * v]), __uint_as_float(y[4 * v + 1]),
+                                   __uint_as_float(y[4 * v + 2]), __uint_as_float(y[4 * v + 3]));
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ctl.acc_empty(buf));
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 2-D bf16 activation map [rows, inner], box 64 (inner) x 128 (rows).
+bool map_rows(CUtensorMap* m, const void* ptr, int64_t inner, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+  cuuint32_t box[2] = {BK, BM};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 weight map [E, K, N] (N contiguous), box 64 (N) x 64 (K) x 1.
+bool map_weights(CUtensorMap* m, const void* ptr, int64_t N, int64_t K, int64_t E) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K),
+                        static_cast<cuuint64_t>(E)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(N * K) * 2};
+  cuuint32_t box[3] = {64, BK, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                      const TcArgs& args, cudaStream_t s) {
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaError_t st = cudaGetDevice(&dev);
+  if (st != cudaSuccess) return st;
+  if (dev < 64 && !configured[dev]) {
+    st = cudaFuncSetAttribute(tc_grouped_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SMEM_BYTES);
+    if (st != cudaSuccess) return st;
+    configured[dev] = true;
+  }
+  const int64_t max_tiles = ((args.max_rows + BM - 1) / BM + args.E) * args.num_n_tiles;
+  int64_t grid = device_sm_count();
+  if (grid > max_tiles) grid = max_tiles;
+  if (grid <= 0) return cudaSuccess;
+  tc_grouped_kernel<MODE><<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, s>>>(a, b0, b1, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_fc1(int E, int h, int f, int64_t max_rows, const void* x_perm,
+                          const int32_t* offsets, const void* W1, const void* W3, void* h_mid,
+                          int* err, cudaStream_t s) {
+  if (max_rows == 0) return cudaSuccess;
+  CUtensorMap a, b0, b1;
+  if (!map_rows(&a, x_perm, h, max_rows) || !map_weights(&b0, W1, f, h, E) ||
+      !map_weights(&b1, W3, f, h, E))
+    return cudaErrorInvalidValue;
+  TcArgs args{offsets, E, f / (BN / 2), h / BK, max_rows, h_mid, f, err};
+  return launch_tc<FC1>(a, b0, b1, args, s);
+}
+
+cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_mid,
+                          const int32_t* offsets, const void* W2, float* y_perm, int* err,
+                          cudaStream_t s) {
+  if (max_rows == 0) return cudaSuccess;
+  CUtensorMap a, b0;
+  if (!map_rows(&a, h_mid, f, max_rows) || !map_weights(&b0, W2, h, f, E))
+    return cudaErrorInvalidValue;
+  TcArgs args{offsets, E, h / BN, f / BK, max_rows, y_perm, h, err};
+  return launch_tc<FC2>(a, b0, b0, args, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,299 @@
+// Local permutation (dispatch_preprocess) and combine of the MoE layer forward.
+//
+// Permutation, after the page "MoE我们喜欢你（三）：Megatron Core MoE 源码路径解析"
+// (r00kie-liu.github.io) §9 (sequence-major -> expert-major) and step 4 of
+// §8 "The All-to-All path" of "MoE Internals: DeepSpeed-Megatron Expert
+// Parallel Implementation" (duoan.github.io).  Rows are expert-major and,
+// inside an expert, in ascending token order (a stable counting sort of the
+// T*k (token, slot) pairs keyed by expert):
+//   perm_hist_kernel  per tile of 2048 pairs: kept-pair count per expert
+//   perm_scan_kernel  one CTA: per-expert prefix over tiles, expert offsets
+//   perm_rank_kernel  per tile: stable rank of each pair inside its tile
+//                     (warp match_any + per-warp counts) -> row_map
+//   perm_copy_kernel  per token: read the x row once (16-byte vectors),
+//                     write it to each of its kept rows
+//
+// Combine, after §2 (combine) of the Megatron Core page and step 8 of §8 of
+// the DeepSpeed page (unpermute, weight by the router probabilities):
+//   combine_kernel    per token: gather its k rows, fp32 weighted sum in
+//                     slot order, one rounding to the output dtype
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(kPermThreads)
+    perm_hist_kernel(int64_t npairs, int E, const int32_t* __restrict__ topk_idx,
+                     const uint8_t* __restrict__ keep, int32_t* __restrict__ tile_counts,
+                     int* __restrict__ err) {
+  __shared__ int hist[MOE_MAX_EXPERTS];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kPermTile;
+  for (int i = threadIdx.x; i < kPermTile; i += blockDim.x) {
+    const int64_t p = base + i;
+    if (p < npairs && (keep == nullptr || keep[p])) {
+      const int e = topk_idx[p];
+      if (e >= 0 && e < E)
+        atomicAdd(&hist[e], 1);
+      else
+        report_error(err, DEV_ERR_INDEX, static_cast<int>(p));
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    tile_counts[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+// tile_counts [ntiles][E]: counts in, first row of each (tile, expert) out.
+__global__ void __launch_bounds__(1024)
+    perm_scan_kernel(int64_t ntiles, int E, int32_t* __restrict__ tile_counts,
+                     int32_t* __restrict__ offsets, int32_t* __restrict__ tokens_per_expert) {
+  __shared__ int total[MOE_MAX_EXPERTS];
+  __shared__ int start[MOE_MAX_EXPERTS + 1];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+    for (int64_t t = 0; t < ntiles; ++t) {
+      const int c = tile_counts[t * E + e];
+      tile_counts[t * E + e] = s;
+      s += c;
+    }
+    total[e] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {  // exclusive scan of E <= 256 totals by one warp
+    const int lane = threadIdx.x;
+    int v[MOE_MAX_EXPERTS / 32];
+    int run = 0;
+#pragma unroll
+    for (int i = 0; i < MOE_MAX_EXPERTS / 32; ++i) {
+      const int e = lane * (MOE_MAX_EXPERTS / 32) + i;
+      v[i] = (e < E) ? total[e] : 0;
+      run += v[i];
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int excl = incl - run;
+#pragma unroll
+    for (int i = 0; i < MOE_MAX_EXPERTS / 32; ++i) {
+      const int e = lane * (MOE_MAX_EXPERTS / 32) + i;
+      if (e <= E) start[e] = excl;
+      excl += v[i];
+    }
+    if (lane == 31 && E == MOE_MAX_EXPERTS) start[E] = excl;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = start[e];
+  if (tokens_per_expert)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) tokens_per_expert[e] = total[e];
+  for (int64_t i = threadIdx.x; i < ntiles * E; i += blockDim.x)
+    tile_counts[i] += start[i % E];
+}
+
+constexpr int kWarps = kPermThreads / 32;
+constexpr int kChunks = kPermTile / kPermThreads;  // 32-pair chunks per warp
+
+__global__ void __launch_bounds__(kPermThreads)
+    perm_rank_kernel(int64_t npairs, int E, const int32_t* __restrict__ topk_idx,
+                     const uint8_t* __restrict__ keep, const int32_t* __restrict__ tile_base,
+                     int32_t* __restrict__ row_map, int32_t* __restrict__ row_src) {
+  __shared__ int cnt[kWarps][MOE_MAX_EXPERTS];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kWarps * MOE_MAX_EXPERTS; i += blockDim.x) (&cnt[0][0])[i] = 0;
+  __syncthreads();
+
+  // warp w owns pairs [base + w*256, base + w*256 + 256), processed in
+  // chunks of 32 consecutive pairs; the tile order is (warp, chunk, lane),
+  // which is the pair order.
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kPermTile + warp * (kChunks * 32);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int key[kChunks], rank[kChunks];
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int64_t p = base + c * 32 + lane;
+    int e = -1;
+    if (p < npairs && (keep == nullptr || keep[p])) {
+      e = topk_idx[p];
+      if (e < 0 || e >= E) e = -1;  // flagged by perm_hist_kernel
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int before = 0;
+    if (e >= 0) before = cnt[warp][e];
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp][e] = before + __popc(peers);
+    __syncwarp();
+    key[c] = e;
+    rank[c] = before + __popc(peers & lt_mask);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int s = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int v = cnt[w][e];
+      cnt[w][e] = s;
+      s += v;
+    }
+  }
+  __syncthreads();
+  const int32_t* tb = tile_base + static_cast<int64_t>(blockIdx.x) * E;
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int64_t p = base + c * 32 + lane;
+    if (p >= npairs) continue;
+    const int e = key[c];
+    if (e >= 0) {
+      const int row = tb[e] + cnt[warp][e] + rank[c];
+      row_map[p] = row;
+      if (row_src) row_src[row] = static_cast<int32_t>(p);
+    } else {
+      row_map[p] = -1;
+    }
+  }
+}
+
+constexpr int kCopyThreads = 128;
+constexpr int kCopyUnroll = 4;
+
+// x_perm[row_map[t, j]] = x[t] for every kept slot j; 16-byte vectors.
+__global__ void __launch_bounds__(kCopyThreads)
+    perm_copy_kernel(int T, int row_vecs, int k, const uint4* __restrict__ x,
+                     const int32_t* __restrict__ row_map, uint4* __restrict__ x_perm) {
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    int rows[MOE_MAX_TOPK];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) rows[j] = (j < k) ? row_map[(int64_t)t * k + j] : -1;
+    const uint4* src = x + (int64_t)t * row_vecs;
+    for (int v0 = threadIdx.x; v0 < row_vecs; v0 += kCopyThreads * kCopyUnroll) {
+      uint4 buf[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int v = v0 + u * kCopyThreads;
+        if (v < row_vecs) buf[u] = __ldcs(src + v);
+      }
+#pragma unroll
+      for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+        if (rows[j] < 0) continue;
+        uint4* dst = x_perm + (int64_t)rows[j] * row_vecs;
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+          const int v = v0 + u * kCopyThreads;
+          if (v < row_vecs) dst[v] = buf[u];
+        }
+      }
+    }
+  }
+}
+
+template <typename OT>
+struct Out4;
+template <>
+struct Out4<float> {
+  __device__ static void store(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
+};
+template <>
+struct Out4<__nv_bfloat16> {
+  __device__ static void store(__nv_bfloat16* p, float4 v) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    __stcs(reinterpret_cast<uint2*>(p), u);
+  }
+};
+
+constexpr int kCombineThreads = 256;
+
+template <typename OT>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(int T, int h, int k, const float* __restrict__ y_perm,
+                   const int32_t* __restrict__ row_map, const float* __restrict__ topk_prob,
+                   OT* __restrict__ y) {
+  const int h4 = h >> 2;
+  const int64_t max_rows = static_cast<int64_t>(T) * k;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    int rows[MOE_MAX_TOPK];
+    float p[MOE_MAX_TOPK];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+      rows[j] = (j < k) ? row_map[(int64_t)t * k + j] : -1;
+      if (rows[j] >= max_rows) rows[j] = -1;  // a row outside y_perm is treated as dropped
+      p[j] = (rows[j] >= 0) ? topk_prob[(int64_t)t * k + j] : 0.f;
+    }
+    for (int v = threadIdx.x; v < h4; v += kCombineThreads) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+        if (rows[j] < 0) continue;
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(y_perm + (int64_t)rows[j] * h) + v);
+        acc.x = fmaf(p[j], a.x, acc.x);
+        acc.y = fmaf(p[j], a.y, acc.y);
+        acc.z = fmaf(p[j], a.z, acc.z);
+        acc.w = fmaf(p[j], a.w, acc.w);
+      }
+      Out4<OT>::store(y + (int64_t)t * h + 4 * v, acc);
+    }
+  }
+}
+
+int grid_for_tokens(int T, int per_sm) {
+  const int cap = device_sm_count() * per_sm;
+  return T < cap ? T : cap;
+}
+
+}  // namespace
+
+cudaError_t launch_perm_hist(int64_t npairs, int E, const int32_t* topk_idx, const uint8_t* keep,
+                             int32_t* tile_counts, int* err, cudaStream_t s) {
+  const int64_t nt = perm_tiles(npairs);
+  if (nt == 0) return cudaSuccess;
+  perm_hist_kernel<<<static_cast<unsigned>(nt), kPermThreads, 0, s>>>(npairs, E, topk_idx, keep,
+                                                                       tile_counts, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_perm_scan(int64_t ntiles, int E, int32_t* tile_counts, int32_t* offsets,
+                             int32_t* tokens_per_expert, cudaStream_t s) {
+  perm_scan_kernel<<<1, 1024, 0, s>>>(ntiles, E, tile_counts, offsets, tokens_per_expert);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_perm_rank(int64_t npairs, int E, const int32_t* topk_idx, const uint8_t* keep,
+                             const int32_t* tile_base, int32_t* row_map, int32_t* row_src,
+                             cudaStream_t s) {
+  const int64_t nt = perm_tiles(npairs);
+  if (nt == 0) return cudaSuccess;
+  perm_rank_kernel<<<static_cast<unsigned>(nt), kPermThreads, 0, s>>>(npairs, E, topk_idx, keep,
+                                                                       tile_base, row_map, row_src);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, const int32_t* row_map,
+                             void* x_perm, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int row_vecs = h * (dtype == MOE_F32 ? 4 : 2) / 16;
+  perm_copy_kernel<<<grid_for_tokens(T, 16), kCopyThreads, 0, s>>>(
+      T, row_vecs, k, static_cast<const uint4*>(x), row_map, static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
+                           const int32_t* row_map, const float* topk_prob, void* y, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int grid = grid_for_tokens(T, 8);
+  if (dtype == MOE_F32)
+    combine_kernel<float><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob,
+                                                           static_cast<float*>(y));
+  else
+    combine_kernel<__nv_bfloat16><<<grid, kCombineThreads, 0, s>>>(
+        T, h, k, y_perm, row_map, topk_prob, static_cast<__nv_bfloat16*>(y));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

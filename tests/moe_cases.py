@@ -1,0 +1,207 @@
+"""Shared helpers of the parity tests: seeded inputs conditioned on the
+routing margin (using the oracle), oracle runs, GPU runs through the C ABI,
+and the comparisons with their tolerances.
+
+Tolerances (fixed here, used by every parity test):
+  * integer / index outputs (topk_idx, keep, tokens_per_expert, offsets,
+    row_map) and permuted rows: bit-exact;
+  * router probabilities: |gpu - oracle| <= 1e-5 * |oracle| + 1e-6;
+  * fp32 outputs: |gpu - oracle| <= 1e-4 * (|oracle| + RMS(oracle))
+    (1e-4 relative, with an RMS floor for entries near zero where a
+    relative bound is meaningless for any summation order);
+  * bf16 outputs: max (|gpu - oracle| - half_ulp_bf16(oracle)) <= 2e-2 * RMS(oracle)
+    -- the bound applies to the error beyond the output's own rounding to
+    bf16, which alone reaches 2^-8 * max|y| (more than 2e-2 * RMS whenever
+    max|y| > 5 RMS, e.g. with dropped tokens' zero rows);
+  * bf16-stored intermediates (h_mid): |gpu - oracle| <= 2^-7 * |oracle| +
+    1e-2 * RMS(oracle) -- the SwiGLU output is heavy-tailed, so bf16
+    storage rounding of its largest entries alone exceeds 2e-2 * RMS; the
+    layer output y is near-Gaussian and keeps the 2e-2 * RMS bound.
+"""
+
+import numpy as np
+import torch
+
+import oracle
+import synthetic
+
+MARGIN = 1e-3        # selection-score gap between the k-th and (k+1)-th expert
+CAP_MARGIN = 1e-5    # probability gap at each overflowing expert's capacity boundary
+PROB_RTOL, PROB_ATOL = 1e-5, 1e-6
+F32_RTOL = 1e-4
+BF16_RMS_TOL = 2e-2
+BF16_ULP = 2.0 ** -7
+BF16_STORED_RMS_TOL = 1e-2
+
+
+def np_view(t):
+    """A CPU torch tensor as the numpy array the oracle takes."""
+    if t is None:
+        return None
+    t = t.detach().to("cpu").contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def _cap_boundary_bad(r, w):
+    """Tokens sitting on a capacity boundary closer than CAP_MARGIN."""
+    cap = r["capacity"]
+    if cap < 0 or cap >= w.T or w.drop_policy != "probs":
+        return []
+    idx, p = r["topk_idx"], r["topk_prob_raw"]
+    bad = []
+    for e in np.nonzero(r["assigned"] > cap)[0]:
+        tok, slot = np.nonzero(idx == e)
+        pe = p[tok, slot].astype(np.float64)
+        order = np.argsort(-pe, kind="stable")
+        if pe[order[cap - 1]] - pe[order[cap]] < CAP_MARGIN:
+            bad.append(int(tok[order[cap]]))
+    return bad
+
+
+def condition_inputs(w, inp, max_rounds=64, nthreads=0):
+    """Redraw x rows until every token's top-k margin is >= MARGIN (and the
+    capacity boundaries are clear).  Returns the oracle routing of the
+    final x.  `inp["x"]` is updated in place (CPU or CUDA tensor)."""
+    x = inp["x"]
+    Wg = np_view(inp["Wg"])
+    gb, eb = np_view(inp["gate_bias"]), np_view(inp["expert_bias"])
+    x_cpu = x.detach().to("cpu").clone()
+    for rnd in range(max_rounds):
+        r = oracle.route(np_view(x_cpu), Wg, w.k, w.score, gb, eb, w.capacity_factor,
+                         w.min_capacity, w.drop_policy, nthreads)
+        bad = sorted(set(np.nonzero(r["margin"] < MARGIN)[0].tolist()) |
+                     set(_cap_boundary_bad(r, w)))
+        if not bad:
+            if x.device.type != "cpu":
+                x.copy_(x_cpu.to(x.device))
+            else:
+                x.copy_(x_cpu)
+            return r
+        x_cpu[torch.tensor(bad)] = synthetic.redraw_x_rows(w, rnd, len(bad))
+    raise RuntimeError("margin conditioning did not converge")
+
+
+def make_case(w, device="cpu", nthreads=0):
+    inp = synthetic.generate(w, device=device)
+    r = condition_inputs(w, inp, nthreads=nthreads)
+    return inp, r
+
+
+def oracle_forward(w, inp, nthreads=0, want_h_mid=True):
+    return oracle.forward(np_view(inp["x"]), np_view(inp["Wg"]), np_view(inp["W1"]),
+                          np_view(inp["W3"]), np_view(inp["W2"]), w.k, w.score,
+                          np_view(inp["gate_bias"]), np_view(inp["expert_bias"]),
+                          w.capacity_factor, w.min_capacity, w.drop_policy, nthreads,
+                          want_h_mid=want_h_mid)
+
+
+def gpu_config(w):
+    import mixture_experts_layer_fp32_gb300 as moe
+    return moe.config(w.T, w.h, w.E, w.k, w.f, w.score, w.dtype, w.capacity_factor,
+                      w.min_capacity, w.drop_policy)
+
+
+def to_dev(inp, device="cuda"):
+    return {k: (None if v is None else v.to(device).contiguous()) for k, v in inp.items()}
+
+
+def gpu_stages(w, dinp, with_routing_map=True):
+    """Run the five stages through the C ABI; returns the Buffers object."""
+    import mixture_experts_layer_fp32_gb300 as moe
+    cfg = gpu_config(w)
+    b = moe.Buffers(cfg)
+    moe.route(cfg, dinp["x"], dinp["Wg"], dinp["gate_bias"], dinp["expert_bias"], b.topk_idx,
+              b.topk_prob, b.keep, b.tokens_per_expert,
+              b.routing_map if with_routing_map else None, b.ws)
+    moe.permute(cfg, dinp["x"], b.topk_idx, b.keep, b.x_perm, b.row_map, b.expert_offsets, b.ws)
+    moe.grouped_fc1(cfg, b.x_perm, b.expert_offsets, dinp["W1"], dinp["W3"], b.h_mid, b.ws)
+    moe.grouped_fc2(cfg, b.h_mid, b.expert_offsets, dinp["W2"], b.y_perm, b.ws)
+    moe.combine(cfg, b.y_perm, b.row_map, b.topk_prob, b.y)
+    moe.check(b.ws)
+    return b
+
+
+def gpu_forward(w, dinp):
+    import mixture_experts_layer_fp32_gb300 as moe
+    cfg = gpu_config(w)
+    ws = moe.alloc_workspace(cfg)
+    y = torch.empty((w.T, w.h), dtype=moe.act_dtype(cfg), device="cuda")
+    idx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+    prob = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+    tpe = torch.empty((w.E,), dtype=torch.int32, device="cuda")
+    moe.forward(cfg, dinp["x"], dinp["Wg"], dinp["gate_bias"], dinp["expert_bias"], dinp["W1"],
+                dinp["W3"], dinp["W2"], y, ws, idx, prob, tpe)
+    moe.check(ws)
+    return y, idx, prob, tpe
+
+
+# ------------------------------------------------------------ comparisons
+
+def assert_equal(name, got, want):
+    got = np.asarray(got)
+    want = np.asarray(want)
+    assert got.shape == want.shape, (name, got.shape, want.shape)
+    bad = np.nonzero(got != want)
+    assert bad[0].size == 0, "%s: %d mismatches, first at %s: got %s want %s" % (
+        name, bad[0].size, tuple(b[0] for b in bad), got[tuple(b[0] for b in bad)],
+        want[tuple(b[0] for b in bad)])
+
+
+def assert_probs(got, want):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    err = np.abs(got - want) - (PROB_RTOL * np.abs(want) + PROB_ATOL)
+    assert np.all(err <= 0), "probs: max excess %g" % err.max()
+
+
+def half_ulp_bf16(v):
+    """Half the bf16 spacing at |v| (the largest error of a correct rounding)."""
+    a = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - 8), 0.0)
+
+
+def rms(a):
+    a = np.asarray(a, np.float64)
+    return float(np.sqrt(np.mean(a * a))) if a.size else 0.0
+
+
+def assert_close(name, got, want, dtype):
+    """got: GPU values (any float), want: oracle float64."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape, (name, got.shape, want.shape)
+    if want.size == 0:
+        return
+    assert np.all(np.isfinite(got)), "%s: non-finite GPU values" % name
+    r = rms(want)
+    d = np.abs(got - want)
+    if dtype == "bf16":
+        # error beyond the output's own rounding to bf16 (half an ulp of the
+        # exact value), bounded by 2e-2 * RMS
+        excess = d - half_ulp_bf16(want)
+        tol = BF16_RMS_TOL * r
+        assert excess.max() <= tol, "%s: max err beyond rounding %g > %g (= 2e-2 * RMS %g)" % (
+            name, excess.max(), tol, r)
+    elif dtype == "bf16_stored":
+        # a bf16-stored intermediate: one bf16 ulp (2^-7 relative) for the
+        # storage rounding plus 1e-2 * RMS for the accumulation
+        lim = BF16_ULP * np.abs(want) + BF16_STORED_RMS_TOL * r
+        i = np.argmax(d - lim)
+        assert d.reshape(-1)[i] <= lim.reshape(-1)[i], "%s: err %g > %g (want %g)" % (
+            name, d.reshape(-1)[i], lim.reshape(-1)[i], want.reshape(-1)[i])
+    else:
+        lim = (F32_RTOL * (np.abs(want) + r)).reshape(-1)
+        d = d.reshape(-1)
+        i = int(np.argmax(d - lim))
+        assert d[i] <= lim[i], "%s: err %g > %g at %d (want %g)" % (name, d[i], lim[i], i,
+                                                                      want.reshape(-1)[i])
+
+
+def to_np(t):
+    t = t.detach().to("cpu")
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.numpy()
