@@ -187,6 +187,31 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
                        float* topk_prob, int32_t* tokens_per_expert, void* ws,
                        size_t ws_bytes, moe_stream_t stream);
 
+/*
+ * moe_permute without a workspace argument.  This entry point is not a step
+ * of the MoE method (the pages have no counterpart); it exists for callers
+ * that cannot give the library any device memory beyond their inputs and
+ * outputs -- a fixed memory budget reserved at start-up, a host framework
+ * that forbids allocating outside its own pools, a latency-critical path
+ * that must not call cudaMalloc/cudaFree (they may synchronise the device).
+ * Its scratch is a fixed array of MOE_PERMUTE_NOALLOC_MAX_COUNTERS int32
+ * counters (256 KB) inside the library, held by every GPU that loads the
+ * library until exit.  It allocates nothing.
+ *   Arguments, outputs and results are those of moe_permute.
+ *   Limit: ceil(T*k/2048) * E <= MOE_PERMUTE_NOALLOC_MAX_COUNTERS, otherwise
+ *   MOE_ERR_UNSUPPORTED is returned before anything is enqueued.
+ *   All calls share the array: calls whose kernels overlap on the GPU race
+ *   and corrupt each other; order them (one stream, or events).
+ *   The first call on a device looks the array's address up on that device
+ *   (it must be the current device); make it before any stream capture.
+ *   Expert ids outside [0,E) are skipped (row_map -1) without a device
+ *   error report.
+ */
+#define MOE_PERMUTE_NOALLOC_MAX_COUNTERS 65536
+moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                               const uint8_t* keep, void* x_perm, int32_t* row_map,
+                               int32_t* expert_offsets, moe_stream_t stream);
+
 /* Reads and clears the device error word in `ws` (synchronises `stream`):
  * MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT.  *info (nullable) gets
  * the first failing index or wait site. */

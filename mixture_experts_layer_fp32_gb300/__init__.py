@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     lib,
     max_rows,
     permute,
+    permute_noalloc,
     route,
     workspace_size,
 )

@@ -23,7 +23,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 # every function declared in include/moe.h
 EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_capacity",
            "moe_workspace_size", "moe_max_rows", "moe_route", "moe_permute", "moe_grouped_mlp",
-           "moe_grouped_fc1", "moe_grouped_fc2", "moe_combine", "moe_forward", "moe_check"]
+           "moe_grouped_fc1", "moe_grouped_fc2", "moe_combine", "moe_forward", "moe_check",
+           "moe_permute_noalloc"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -70,6 +71,7 @@ def lib():
             "moe_combine": ([cfgp, vp, vp, vp, vp, vp], i32),
             "moe_forward": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_check": ([vp, vp, ctypes.POINTER(i32)], i32),
+            "moe_permute_noalloc": ([cfgp, vp, vp, vp, vp, vp, vp, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -150,6 +152,14 @@ def permute(cfg, x, topk_idx, keep, x_perm, row_map, expert_offsets, ws):
     w, wb = _ws(ws)
     _check(lib().moe_permute(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(keep), _p(x_perm),
                              _p(row_map), _p(expert_offsets), w, wb, _stream()), "moe_permute")
+
+
+def permute_noalloc(cfg, x, topk_idx, keep, x_perm, row_map, expert_offsets):
+    """moe_permute without a workspace (scratch in a fixed array inside the
+    library; for callers that cannot provide device memory)."""
+    _check(lib().moe_permute_noalloc(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(keep),
+                                     _p(x_perm), _p(row_map), _p(expert_offsets), _stream()),
+           "moe_permute_noalloc")
 
 
 def grouped_fc1(cfg, x_perm, expert_offsets, W1, W3, h_mid, ws):

@@ -1,0 +1,103 @@
+// moe_permute_noalloc: the token permutation without a caller workspace.
+//
+// Some callers cannot hand this library any device memory beyond their
+// inputs and outputs: code that runs with a fixed memory budget reserved at
+// start-up, plugins inside a host framework that forbids allocating outside
+// its own pools, and latency-critical paths that must not call cudaMalloc /
+// cudaFree (those calls may synchronise the whole device).  This entry point
+// serves them.  The only scratch the permutation needs -- one counter per
+// (tile of 2048 token-slot pairs, expert) -- lives in the fixed array below,
+// which every GPU that loads the library holds until the process exits.
+//
+// Limits and sharing:
+//  * at most kScratchInts counters: ceil(T*k / 2048) * E <= 65536, otherwise
+//    the call returns MOE_ERR_UNSUPPORTED before enqueuing anything;
+//  * every call shares the array and it keeps the last call's contents.
+//    Each call writes every counter it later reads, so nothing has to start
+//    at zero; but calls whose kernels overlap on the GPU (different streams,
+//    no ordering between them) race on the array and corrupt each other;
+//  * expert ids outside [0, E) are skipped (their row_map entry is -1)
+//    without being reported: there is no workspace to hold an error word;
+//  * the first call on a device looks up the array's device address there
+//    (cudaGetSymbolAddress, with that device current).  Make that first call
+//    before any stream capture on the device.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int64_t kScratchInts = MOE_PERMUTE_NOALLOC_MAX_COUNTERS;  // 256 KB per device
+
+static __device__ __align__(256) int32_t g_perm_scratch[kScratchInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+int32_t* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Device address of g_perm_scratch on the current device (set up once per
+// device).  Returns nullptr and the CUDA error on failure.
+int32_t* scratch_on_current_device(cudaError_t* err) {
+  int dev = -1;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_perm_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+  }
+  *err = cudaSuccess;
+  return g_scratch_addr[dev];
+}
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
+                                          const int32_t* topk_idx, const uint8_t* keep,
+                                          void* x_perm, int32_t* row_map,
+                                          int32_t* expert_offsets, moe_stream_t stream) {
+  using namespace moe;
+  if (cfg == nullptr) return MOE_ERR_INVALID_ARG;
+  size_t ws_unused = 0;
+  const moe_status v = moe_workspace_size(cfg, &ws_unused);  // validates the configuration
+  if (v != MOE_OK) return v;
+  const moe_config& c = *cfg;
+  const int64_t np = static_cast<int64_t>(c.num_tokens) * c.topk;
+  const int64_t ntiles = perm_tiles(np);
+  if (ntiles * c.num_experts > kScratchInts) return MOE_ERR_UNSUPPORTED;
+  if (expert_offsets == nullptr || !aligned(expert_offsets, 4)) return MOE_ERR_INVALID_ARG;
+  if (np > 0) {
+    if (x == nullptr || topk_idx == nullptr || x_perm == nullptr || row_map == nullptr)
+      return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(x_perm, 16) || !aligned(topk_idx, 4) || !aligned(row_map, 4))
+      return MOE_ERR_INVALID_ARG;
+  }
+  cudaError_t err = cudaSuccess;
+  int32_t* scratch = scratch_on_current_device(&err);
+  if (scratch == nullptr) return MOE_ERR_CUDA;
+  if (np == 0) {
+    return cudaMemsetAsync(expert_offsets, 0, (c.num_experts + 1) * sizeof(int32_t), stream) ==
+                   cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+  }
+  if (launch_perm_hist(np, c.num_experts, topk_idx, keep, scratch, nullptr, stream) != cudaSuccess ||
+      launch_perm_scan(ntiles, c.num_experts, scratch, expert_offsets, nullptr, stream) !=
+          cudaSuccess ||
+      launch_perm_rank(np, c.num_experts, topk_idx, keep, scratch, row_map, nullptr, stream) !=
+          cudaSuccess ||
+      launch_perm_copy(c.num_tokens, c.hidden, c.topk, c.dtype, x, row_map, x_perm, stream) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
