@@ -251,7 +251,7 @@ def run_native(args, rank, world, local):
                 for j, s in enumerate(STAGES)}
     step_ms = [events[i][0].elapsed_time(events[i][5]) for i in range(args.steps)]
     ms = sum(step_ms) / len(step_ms)
-    ms_all = max_over_ranks(ms, world)
+    ms_all, tokens_per_s = job_throughput(ms, w.T, world)
 
     # ---- e2e: moe_forward with host (pinned) input and output in the timed region
     e2e = None
@@ -321,7 +321,7 @@ def run_native(args, rank, world, local):
         else work[dom].get("bytes")
 
     line = {
-        "metric": METRIC, "value": world * w.T / (ms_all / 1e3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded, x~N(0,%g), weights~N(0,%g), random-init)" % (w.x_std, w.w_std),
@@ -344,12 +344,20 @@ def barrier(world):
         torch.distributed.barrier()
 
 
-def max_over_ranks(v, world):
+def max_over_ranks(v, world, device="cuda"):
+    """The largest per-rank value (the slowest replica sets the job time)."""
     if world == 1:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(ms_local, tokens_per_rank, world, device="cuda"):
+    """Whole-job tokens/s of `world` replicas: all ranks' tokens over the
+    slowest rank's step time.  Returns (max ms per step, tokens/s)."""
+    ms = max_over_ranks(ms_local, world, device)
+    return ms, world * tokens_per_rank / (ms / 1e3)
 
 
 # ---------------------------------------------------------------- oracle timing

@@ -62,25 +62,35 @@ def _cap_boundary_bad(r, w):
 
 def condition_inputs(w, inp, max_rounds=64, nthreads=0):
     """Redraw x rows until every token's top-k margin is >= MARGIN (and the
-    capacity boundaries are clear).  Returns the oracle routing of the
-    final x.  `inp["x"]` is updated in place (CPU or CUDA tensor)."""
+    capacity boundaries are clear).  Only redrawn rows are routed again.
+    Returns the oracle routing of the final x.  `inp["x"]` is updated in
+    place (CPU or CUDA tensor)."""
     x = inp["x"]
     Wg = np_view(inp["Wg"])
     gb, eb = np_view(inp["gate_bias"]), np_view(inp["expert_bias"])
     x_cpu = x.detach().to("cpu").clone()
+    logits = oracle.router_logits(np_view(x_cpu), Wg, gb, nthreads)
+    idx, prob, margin = oracle.topk_scores(logits, w.k, w.score, eb, nthreads)
     for rnd in range(max_rounds):
-        r = oracle.route(np_view(x_cpu), Wg, w.k, w.score, gb, eb, w.capacity_factor,
-                         w.min_capacity, w.drop_policy, nthreads)
-        bad = sorted(set(np.nonzero(r["margin"] < MARGIN)[0].tolist()) |
-                     set(_cap_boundary_bad(r, w)))
+        part = {"capacity": oracle.capacity(w.T, w.E, w.k, w.capacity_factor, w.min_capacity),
+                "topk_idx": idx, "topk_prob_raw": prob,
+                "assigned": np.bincount(idx.reshape(-1), minlength=w.E)}
+        bad = sorted(set(np.nonzero(margin < MARGIN)[0].tolist()) |
+                     set(_cap_boundary_bad(part, w)))
         if not bad:
-            if x.device.type != "cpu":
-                x.copy_(x_cpu.to(x.device))
-            else:
-                x.copy_(x_cpu)
-            return r
-        x_cpu[torch.tensor(bad)] = synthetic.redraw_x_rows(w, rnd, len(bad))
-    raise RuntimeError("margin conditioning did not converge")
+            break
+        rows = torch.tensor(bad)
+        x_cpu[rows] = synthetic.redraw_x_rows(w, rnd, len(bad))
+        sub = oracle.router_logits(np_view(x_cpu[rows]), Wg, gb, nthreads)
+        i2, p2, m2 = oracle.topk_scores(sub, w.k, w.score, eb, nthreads)
+        idx[bad], prob[bad], margin[bad] = i2, p2, m2
+    else:
+        raise RuntimeError("margin conditioning did not converge")
+    x.copy_(x_cpu.to(x.device))
+    r = oracle.route(np_view(x_cpu), Wg, w.k, w.score, gb, eb, w.capacity_factor,
+                     w.min_capacity, w.drop_policy, nthreads)
+    assert np.all(r["margin"] >= MARGIN)
+    return r
 
 
 def make_case(w, device="cpu", nthreads=0):
@@ -205,3 +215,23 @@ def to_np(t):
     if t.dtype == torch.bfloat16:
         t = t.float()
     return t.numpy()
+
+
+def compare_all(w, inp, ref, b):
+    """Every output of a staged GPU run against the oracle (small cases)."""
+    assert_equal("topk_idx", to_np(b.topk_idx), ref["topk_idx"])
+    assert_equal("keep", to_np(b.keep), ref["keep"])
+    assert_equal("tokens_per_expert", to_np(b.tokens_per_expert), ref["tokens_per_expert"])
+    assert_probs(to_np(b.topk_prob), ref["topk_prob"])
+    assert_equal("expert_offsets", to_np(b.expert_offsets), ref["offsets"])
+    assert_equal("row_map", to_np(b.row_map), ref["row_map"])
+    R = int(ref["offsets"][-1])
+    got = b.x_perm[:R].detach().cpu()
+    want = inp["x"].detach().cpu()[torch.from_numpy(ref["row_token"]).long()]
+    if got.dtype == torch.bfloat16:
+        got, want = got.view(torch.int16), want.view(torch.int16)
+    assert torch.equal(got, want)
+    assert_close("h_mid", to_np(b.h_mid[:R]), ref["h_mid"],
+                 "bf16_stored" if w.dtype == "bf16" else w.dtype)
+    assert_close("y_perm", to_np(b.y_perm[:R]), ref["y_perm"], w.dtype)
+    assert_close("y", to_np(b.y), ref["y"], w.dtype)

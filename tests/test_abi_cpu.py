@@ -1,0 +1,144 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function that include/moe.h declares, and rejects bad arguments on the host
+before anything would be enqueued (no call here reaches the CUDA runtime)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+FAKE = 0x10000          # a 16-byte-aligned address that is never dereferenced
+MISALIGNED = 0x10004
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_layer_fp32_gb300 import build
+    build.build()
+    import mixture_experts_layer_fp32_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("moe_route", "moe_permute", "moe_grouped_mlp", "moe_combine", "moe_forward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(moe):
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert sorted(moe.EXPORTS) == declared_functions()
+    assert moe.lib().moe_abi_version() == 1
+    assert moe.lib().moe_status_string(3) == b"MOE_ERR_WORKSPACE"
+
+
+def _status(moe, fn, *args):
+    return getattr(moe.lib(), fn)(*args)
+
+
+def _cfgp(cfg):
+    return ctypes.byref(cfg)
+
+
+@pytest.mark.parametrize("field,value,want", [
+    ("num_tokens", -1, INVALID), ("hidden", 0, INVALID), ("num_experts", 0, INVALID),
+    ("topk", 0, INVALID), ("ffn_hidden", -8, INVALID), ("score", 3, INVALID),
+    ("dtype", 2, INVALID), ("drop_policy", 5, INVALID), ("min_capacity", -1, INVALID),
+    ("num_experts", 257, UNSUPPORTED), ("topk", 9, UNSUPPORTED), ("hidden", 4100, UNSUPPORTED),
+    ("ffn_hidden", 1500, UNSUPPORTED), ("hidden", 4092, UNSUPPORTED),
+])
+def test_config_validation(moe, field, value, want):
+    cfg = moe.config(T=64, h=4096, E=8, k=2, f=1536)
+    setattr(cfg, field, value)
+    size = ctypes.c_size_t()
+    assert _status(moe, "moe_workspace_size", _cfgp(cfg), ctypes.byref(size)) == want
+
+
+def test_topk_larger_than_experts(moe):
+    cfg = moe.config(T=64, h=4096, E=4, k=5, f=1536)
+    size = ctypes.c_size_t()
+    assert _status(moe, "moe_workspace_size", _cfgp(cfg), ctypes.byref(size)) == UNSUPPORTED
+
+
+def test_fp32_path_accepts_small_multiples_of_8(moe):
+    cfg = moe.config(T=64, h=136, E=8, k=2, f=200, dtype="f32")
+    size = ctypes.c_size_t()
+    assert _status(moe, "moe_workspace_size", _cfgp(cfg), ctypes.byref(size)) == OK
+    assert size.value > 0
+
+
+def test_capacity_matches_reading(moe):
+    cfg = moe.config(T=32768, h=1024, E=64, k=1, f=4096, score="softmax_pre",
+                     capacity_factor=1.25)
+    assert moe.capacity(cfg) == 640
+    assert moe.capacity(moe.config(T=10, h=256, E=4, k=2, f=128, capacity_factor=1.1)) == 6
+    assert moe.capacity(moe.config(T=10, h=256, E=4, k=2, f=128)) == -1
+
+
+def _route_args(cfg, ws_bytes, **over):
+    a = dict(x=FAKE, Wg=FAKE, gb=None, eb=None, idx=FAKE, prob=FAKE, keep=FAKE, tpe=FAKE, rm=None,
+             ws=FAKE, ws_bytes=ws_bytes, stream=None)
+    a.update(over)
+    return (ctypes.byref(cfg), a["x"], a["Wg"], a["gb"], a["eb"], a["idx"], a["prob"], a["keep"],
+            a["tpe"], a["rm"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_route_rejects_null_misaligned_and_small_workspace(moe):
+    cfg = moe.config(T=128, h=4096, E=8, k=2, f=1536)
+    need = moe.workspace_size(cfg)
+    lib = moe.lib()
+    assert lib.moe_route(*_route_args(cfg, need, x=None)) == INVALID
+    assert lib.moe_route(*_route_args(cfg, need, idx=None)) == INVALID
+    assert lib.moe_route(*_route_args(cfg, need, x=MISALIGNED)) == INVALID
+    assert lib.moe_route(*_route_args(cfg, need, ws=None)) == INVALID
+    assert lib.moe_route(*_route_args(cfg, need - 1)) == WORKSPACE
+
+
+def test_forward_and_stage_argument_checks(moe):
+    cfg = moe.config(T=128, h=4096, E=8, k=2, f=1536)
+    need = moe.workspace_size(cfg)
+    lib = moe.lib()
+    # moe_forward: W2 missing
+    assert lib.moe_forward(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, FAKE,
+                           None, None, None, FAKE, need, None) == INVALID
+    # moe_permute: x_perm misaligned
+    assert lib.moe_permute(ctypes.byref(cfg), FAKE, FAKE, None, MISALIGNED, FAKE, FAKE, FAKE,
+                           need, None) == INVALID
+    # moe_grouped_fc1: workspace too small
+    assert lib.moe_grouped_fc1(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16,
+                               None) == WORKSPACE
+    # moe_combine: y missing
+    assert lib.moe_combine(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, None) == INVALID
+    # moe_check: no workspace
+    assert lib.moe_check(None, None, None) == INVALID
+
+
+def test_permute_noalloc_host_checks(moe):
+    lib = moe.lib()
+    big = moe.config(T=70000, h=256, E=256, k=8, f=128)
+    assert lib.moe_permute_noalloc(ctypes.byref(big), FAKE, FAKE, None, FAKE, FAKE, FAKE,
+                                   None) == UNSUPPORTED
+    small = moe.config(T=100, h=256, E=8, k=2, f=128)
+    assert lib.moe_permute_noalloc(ctypes.byref(small), None, FAKE, None, FAKE, FAKE, FAKE,
+                                   None) == INVALID
+
+
+def test_binding_refuses_cpu_tensors(moe):
+    import torch
+    cfg = moe.config(T=4, h=256, E=4, k=2, f=128)
+    x = torch.zeros(4, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        moe.permute(cfg, x, x, None, x, x, x, x)
