@@ -314,6 +314,8 @@ def run_native(args, rank, world, local):
         roof = {"kernel": dom, "bound": "hbm", "achieved": stages[dom].get("gbs"),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["achieved"] else None
+    if roof["bound"] == "tensor" and peaks.get("bf16_tflops_sustained"):
+        roof["frac_of_sustained_peak"] = roof["achieved"] / peaks["bf16_tflops_sustained"]
     roof["peak_source"] = "%s (MEASURED_PEAKS.json burst)" % peaks["source"] \
         if peaks["source"] == "measured" else "fallback"
     roof["traffic"] = recorded_traffic(dom, w.name)

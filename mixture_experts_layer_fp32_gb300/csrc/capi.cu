@@ -54,7 +54,7 @@ Layout make_layout(const moe_config& c) {
   const size_t nt = static_cast<size_t>(perm_tiles(static_cast<int64_t>(np)));
   const size_t el = c.dtype == MOE_F32 ? 4 : 2;
   L.err = take(kErrBytes);
-  L.logits = take(T * E * 4);
+  L.logits = take(T * E * 4 * kRouterMaxSplits);
   L.assigned = take(E * 4);
   L.tiles = take(nt * E * 4);
   L.cand_rowmap = take(np * 4);
@@ -155,16 +155,17 @@ moe_status do_route(const moe_config& c, const void* x, const float* Wg, const f
   MOE_CUDA(cudaMemsetAsync(tpe, 0, E * sizeof(int32_t), s));
   if (T == 0) return MOE_OK;
   float* logits = at<float>(ws, L.logits);
-  MOE_CUDA(launch_router_logits(T, c.hidden, E, c.dtype, x, Wg, gb, logits, s));
+  int nsplit = 1;
+  MOE_CUDA(launch_router_logits(T, c.hidden, E, c.dtype, x, Wg, logits, &nsplit, s));
   if (!drops) {
-    MOE_CUDA(launch_router_topk(T, E, k, c.score, logits, eb, topk_idx, topk_prob, keep,
-                                routing_map, tpe, err, s));
+    MOE_CUDA(launch_router_topk(T, E, k, c.score, logits, nsplit, gb, eb, topk_idx, topk_prob,
+                                keep, routing_map, tpe, err, s));
     return MOE_OK;
   }
   int32_t* assigned = at<int32_t>(ws, L.assigned);
   MOE_CUDA(cudaMemsetAsync(assigned, 0, E * sizeof(int32_t), s));
-  MOE_CUDA(launch_router_topk(T, E, k, c.score, logits, eb, topk_idx, topk_prob, keep, routing_map,
-                              assigned, err, s));
+  MOE_CUDA(launch_router_topk(T, E, k, c.score, logits, nsplit, gb, eb, topk_idx, topk_prob, keep,
+                              routing_map, assigned, err, s));
   // candidate lists: every routed pair, expert-major, ascending token order
   const int64_t np = static_cast<int64_t>(T) * k;
   const int64_t nt = perm_tiles(np);

@@ -27,10 +27,14 @@ constexpr int kPermThreads = 256;
 inline int64_t perm_tiles(int64_t npairs) { return (npairs + kPermTile - 1) / kPermTile; }
 
 // ---- router ----
+// Router logits without the gate bias, as nsplit partial sums [nsplit][T][E]
+// (nsplit <= kRouterMaxSplits) that the top-k kernel adds in order.
+constexpr int kRouterMaxSplits = 16;
 cudaError_t launch_router_logits(int T, int h, int E, int dtype, const void* x, const float* Wg,
-                                 const float* gate_bias, float* logits, cudaStream_t s);
-cudaError_t launch_router_topk(int T, int E, int k, int score, const float* logits,
-                               const float* expert_bias, int32_t* topk_idx, float* topk_prob,
+                                 float* partials, int* nsplit, cudaStream_t s);
+cudaError_t launch_router_topk(int T, int E, int k, int score, const float* logits, int nsplit,
+                               const float* gate_bias, const float* expert_bias,
+                               int32_t* topk_idx, float* topk_prob,
                                uint8_t* keep, uint8_t* routing_map, int32_t* counts, int* err,
                                cudaStream_t s);
 cudaError_t launch_drop_select(int T, int E, int k, int64_t capacity, int policy,

@@ -49,12 +49,12 @@ struct XVec<__nv_bfloat16> {
   }
 };
 
-// logits[t, e] = sum_i x[t, i] * Wg[i, e] + gate_bias[e], fp32 FMA.
+// partial logits[t, e] = sum_i x[t, i] * Wg[i, e], fp32 FMA (the gate bias is
+// added by the top-k kernel).
 template <int BT, int ET, int TT, int TE, int BK, typename XT>
 __global__ void __launch_bounds__(kRouteThreads)
     router_logits_kernel(int T, int h, int E, const XT* __restrict__ x,
-                         const float* __restrict__ Wg, const float* __restrict__ gate_bias,
-                         float* __restrict__ logits) {
+                         const float* __restrict__ Wg, float* __restrict__ logits) {
   constexpr int NTE = ET / TE;
   constexpr int NTT = BT / TT;
   static_assert(NTE * NTT == kRouteThreads, "thread layout");
@@ -153,30 +153,355 @@ __global__ void __launch_bounds__(kRouteThreads)
 #pragma unroll
     for (int j = 0; j < TE; ++j) {
       const int e = e0 + te * TE + j;
-      if (e < E) logits[(int64_t)t * E + e] = acc[i][j] + (gate_bias ? gate_bias[e] : 0.f);
+      if (e < E) logits[(int64_t)t * E + e] = acc[i][j];
     }
   }
 }
 
 template <typename XT, int ET, int TE, int TT, int BK>
 cudaError_t launch_logits_variant(int T, int h, int E, const XT* x, const float* Wg,
-                                  const float* gb, float* logits, cudaStream_t s) {
+                                  float* logits, cudaStream_t s) {
   constexpr int NTE = ET / TE;
   constexpr int NTT = kRouteThreads / NTE;
   constexpr int BT = NTT * TT;
   dim3 grid((T + BT - 1) / BT, (E + ET - 1) / ET);
-  router_logits_kernel<BT, ET, TT, TE, BK, XT><<<grid, kRouteThreads, 0, s>>>(T, h, E, x, Wg, gb,
+  router_logits_kernel<BT, ET, TT, TE, BK, XT><<<grid, kRouteThreads, 0, s>>>(T, h, E, x, Wg,
                                                                               logits);
+  return cudaGetLastError();
+}
+
+// Small-E logits (E <= 8): the gate rows of one slice of h, padded to 8
+// experts, sit in shared memory; each warp takes 4 tokens at a time, lane l
+// streams the 16-byte x vectors l, l+32, ... of that slice of those 4 rows
+// (kept packed in registers, several loads in flight per lane) and
+// accumulates 4 x 8 partial dot products; a 5-step shuffle reduce-scatter
+// then leaves the total of (token l/8, expert l%8) in lane l.  gridDim.y
+// splits h into slices (two CTAs fit per SM); each slice writes its own
+// partial sums.
+constexpr int kSmallE = 8;
+constexpr int kSmallTok = 4;
+constexpr int kSmallUnroll = 4;
+
+// Gate row r (8 fp32) is two 16-byte chunks, 2r and 2r+1.  Lanes read rows
+// 8 apart, i.e. chunks 256 bytes apart: all in one bank group.  XOR-ing the
+// chunk's position inside its 128-byte line with (chunk / 16) % 8 spreads a
+// quarter-warp over the 8 bank groups.
+__device__ __forceinline__ int swz_chunk(int i) { return (i & ~7) | ((i & 7) ^ ((i >> 4) & 7)); }
+
+template <typename XT>
+struct Packed;  // element c of a 16-byte vector kept as raw bits
+template <>
+struct Packed<float> {
+  __device__ static float at(const uint4& q, int c) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    return __uint_as_float(w[c]);
+  }
+};
+template <>
+struct Packed<__nv_bfloat16> {
+  __device__ static float at(const uint4& q, int c) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    const uint32_t b = (c & 1) ? (w[c >> 1] & 0xFFFF0000u) : (w[c >> 1] << 16);
+    return __uint_as_float(b);
+  }
+};
+
+template <typename XT>
+__global__ void __launch_bounds__(kRouteThreads, 2)
+    router_logits_small_e_kernel(int T, int h, int E, int hslice, const XT* __restrict__ x,
+                                 const float* __restrict__ Wg, float* __restrict__ partials) {
+  extern __shared__ __align__(16) float wsm_small[];  // [hslice][8], chunk-swizzled
+  const int hb = blockIdx.y * hslice;                  // first feature of this slice
+  const int hn = min(hslice, h - hb);                  // features in this slice
+  float* logits = partials + (int64_t)blockIdx.y * T * E;
+  if (E == kSmallE && (reinterpret_cast<uintptr_t>(Wg) & 15) == 0) {
+    // 16-byte copies, 8 loads in flight per thread before their stores
+    const float4* src = reinterpret_cast<const float4*>(Wg + (int64_t)hb * kSmallE);
+    float4* dst = reinterpret_cast<float4*>(wsm_small);
+    const int n4 = hn * kSmallE / 4;
+    for (int i0 = threadIdx.x; i0 < n4; i0 += blockDim.x * 8) {
+      float4 r[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u * (int)blockDim.x < n4) r[u] = src[i0 + u * blockDim.x];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u * (int)blockDim.x < n4) dst[swz_chunk(i0 + u * blockDim.x)] = r[u];
+    }
+  } else {
+    for (int i0 = threadIdx.x; i0 < hn * kSmallE; i0 += blockDim.x * 8) {
+      float r[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * blockDim.x;
+        const int row = i / kSmallE, e = i % kSmallE;
+        r[u] = (i < hn * kSmallE && e < E) ? Wg[(int64_t)(hb + row) * E + e] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < hn * kSmallE) wsm_small[swz_chunk(i >> 2) * 4 + (i & 3)] = r[u];
+      }
+    }
+  }
+  __syncthreads();
+  constexpr int V = XVec<XT>::N;
+  const int nvec = hn / V;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int groups = (T + kSmallTok - 1) / kSmallTok;
+  const uint4* xq = reinterpret_cast<const uint4*>(x);
+  const int row_vecs = h / V;
+  const int vb = hb / V;
+  for (int g = blockIdx.x * (kRouteThreads / 32) + warp; g < groups;
+       g += gridDim.x * (kRouteThreads / 32)) {
+    const int t0 = g * kSmallTok;
+    float acc[kSmallTok * kSmallE];
+#pragma unroll
+    for (int i = 0; i < kSmallTok * kSmallE; ++i) acc[i] = 0.f;
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kSmallUnroll) {
+      uint4 xr[kSmallUnroll][kSmallTok];
+#pragma unroll
+      for (int u = 0; u < kSmallUnroll; ++u) {
+        const int v = v0 + 32 * u;
+#pragma unroll
+        for (int tk = 0; tk < kSmallTok; ++tk)
+          xr[u][tk] = (v < nvec && t0 + tk < T) ? xq[(int64_t)(t0 + tk) * row_vecs + vb + v]
+                                                 : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kSmallUnroll; ++u) {
+        const int v = v0 + 32 * u;
+        if (v >= nvec) break;
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          const float4* wr = reinterpret_cast<const float4*>(wsm_small);
+          const int chunk = 2 * (v * V + c);
+          const float4 w0 = wr[swz_chunk(chunk)], w1 = wr[swz_chunk(chunk + 1)];
+          const float w[kSmallE] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+          for (int tk = 0; tk < kSmallTok; ++tk) {
+            const float xe = Packed<XT>::at(xr[u][tk], c);
+#pragma unroll
+            for (int e = 0; e < kSmallE; ++e)
+              acc[tk * kSmallE + e] = fmaf(xe, w[e], acc[tk * kSmallE + e]);
+          }
+        }
+      }
+    }
+    // reduce-scatter: after the step with offset o, a lane keeps the half of
+    // its values selected by (lane & o); at the end lane l holds index l.
+#pragma unroll
+    for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int j = 0; j < n / 2; ++j) {
+        const float keep = upper ? acc[j + n / 2] : acc[j];
+        const float send = upper ? acc[j] : acc[j + n / 2];
+        acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    const int t = t0 + lane / kSmallE;
+    const int e = lane % kSmallE;
+    if (t < T && e < E) logits[(int64_t)t * E + e] = acc[0];
+  }
+}
+
+constexpr int kSmallESliceMax = 3072;  // 3072 x 8 x 4 B = 96 KB: two CTAs per SM
+constexpr int kSmallEMaxHidden = 6 * kSmallESliceMax;
+
+template <typename XT>
+cudaError_t launch_logits_small_e(int T, int h, int E, const XT* x, const float* Wg,
+                                  float* partials, int* nsplit, cudaStream_t s) {
+  // slices of whole 16-byte vectors, at most kSmallESliceMax features each
+  constexpr int V = XVec<XT>::N;
+  int slices = (h + kSmallESliceMax - 1) / kSmallESliceMax;
+  if (slices < 2 && h >= 1024) slices = 2;
+  int hslice = (h / V + slices - 1) / slices * V;
+  slices = (h + hslice - 1) / hslice;
+  *nsplit = slices;
+  const int smem = hslice * kSmallE * static_cast<int>(sizeof(float));
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaError_t st = cudaGetDevice(&dev);
+  if (st != cudaSuccess) return st;
+  if (dev < 64 && !configured[dev]) {
+    st = cudaFuncSetAttribute(router_logits_small_e_kernel<XT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmallESliceMax * kSmallE * static_cast<int>(sizeof(float)));
+    if (st != cudaSuccess) return st;
+    configured[dev] = true;
+  }
+  const int groups = (T + kSmallTok - 1) / kSmallTok;
+  int gx = (groups + kRouteThreads / 32 - 1) / (kRouteThreads / 32);
+  const int cap = (2 * device_sm_count() + slices - 1) / slices;
+  if (gx > cap) gx = cap;
+  router_logits_small_e_kernel<XT><<<dim3(gx, slices), kRouteThreads, smem, s>>>(
+      T, h, E, hslice, x, Wg, partials);
+  return cudaGetLastError();
+}
+
+// Large-E logits: a register-blocked SGEMM.  CTA tile 128 tokens x BN
+// experts, K in chunks of 16 (double-buffered through shared memory), each
+// thread an 8 x 8 micro-tile made of two 4-wide halves (rows ty*4 and
+// 64+ty*4, columns tx*4 and BN/2+tx*4) so that a quarter-warp's 16-byte
+// shared loads are contiguous.  gridDim.z splits K; each split writes its own
+// partial sums, which the top-k kernel adds in split order.
+constexpr int kGemmBM = 128;
+constexpr int kGemmBK = 16;
+constexpr int kMaxSplits = kRouterMaxSplits;
+
+template <int BN, typename XT>
+__global__ void __launch_bounds__(BN * 2, 256 / BN)
+    router_sgemm_kernel(int T, int h, int E, int k_per_split, const XT* __restrict__ x,
+                        const float* __restrict__ Wg, float* __restrict__ partials) {
+  constexpr int TX = BN / 8;          // threads along experts
+  constexpr int NT = TX * 16;         // threads
+  constexpr int V = XVec<XT>::N;
+  constexpr int AV = kGemmBM * kGemmBK / V;      // x vectors per tile
+  constexpr int APT = (AV + NT - 1) / NT;
+  constexpr int BV = kGemmBK * BN / 4;           // Wg float4 per tile
+  constexpr int BPT = BV / NT;
+  __shared__ __align__(16) float As[2][kGemmBK][kGemmBM];
+  __shared__ __align__(16) float Bs[2][kGemmBK][BN];
+
+  const int tid = threadIdx.x;
+  const int tx = tid % TX, ty = tid / TX;
+  const int t0 = blockIdx.x * kGemmBM;
+  const int e0 = blockIdx.y * BN;
+  const int kbeg = blockIdx.z * k_per_split;
+  const int kend = min(h, kbeg + k_per_split);
+  float* out = partials + (int64_t)blockIdx.z * T * E;
+
+  float ar[APT][V];
+  float4 br[BPT];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int r = 0; r < APT; ++r) {
+      const int v = tid + r * NT;
+      const int row = v / (kGemmBK / V), kk = (v % (kGemmBK / V)) * V;
+      if (v < AV && t0 + row < T && k0 + kk < kend) {
+        XVec<XT>::load(x + (int64_t)(t0 + row) * h + k0 + kk, ar[r]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < V; ++c) ar[r][c] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < BPT; ++r) {
+      const int v = tid + r * NT;
+      const int kk = v / (BN / 4), cc = (v % (BN / 4)) * 4;
+      br[r] = (k0 + kk < kend && e0 + cc < E)
+                  ? *reinterpret_cast<const float4*>(Wg + (int64_t)(k0 + kk) * E + e0 + cc)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  auto store = [&](int buf) {
+#pragma unroll
+    for (int r = 0; r < APT; ++r) {
+      const int v = tid + r * NT;
+      if (v < AV) {
+        const int row = v / (kGemmBK / V), kk = (v % (kGemmBK / V)) * V;
+#pragma unroll
+        for (int c = 0; c < V; ++c) As[buf][kk + c][row] = ar[r][c];
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < BPT; ++r) {
+      const int v = tid + r * NT;
+      const int kk = v / (BN / 4), cc = (v % (BN / 4)) * 4;
+      *reinterpret_cast<float4*>(&Bs[buf][kk][cc]) = br[r];
+    }
+  };
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  const int nk = (kend - kbeg + kGemmBK - 1) / kGemmBK;
+  if (nk > 0) {
+    load(kbeg);
+    store(0);
+  }
+  __syncthreads();
+  for (int kt = 0; kt < nk; ++kt) {
+    const int cur = kt & 1;
+    if (kt + 1 < nk) load(kbeg + (kt + 1) * kGemmBK);
+#pragma unroll
+    for (int kk = 0; kk < kGemmBK; ++kk) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][kk][BN / 2 + tx * 4]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    if (kt + 1 < nk) store(cur ^ 1);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
+    if (t >= T) continue;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int e = e0 + half * (BN / 2) + tx * 4;
+      if (e < E)  // E % 4 == 0 on this path: the 4 columns are all valid
+        *reinterpret_cast<float4*>(out + (int64_t)t * E + e) =
+            make_float4(acc[i][half * 4], acc[i][half * 4 + 1], acc[i][half * 4 + 2],
+                        acc[i][half * 4 + 3]);
+    }
+  }
+}
+
+template <int BN, typename XT>
+cudaError_t launch_sgemm(int T, int h, int E, const XT* x, const float* Wg, float* partials,
+                         int max_splits, int* nsplit, cudaStream_t s) {
+  // choose the split count that minimises the most CTAs any SM runs, per
+  // unit of split work: ceil(tiles * S / SMs) / S (plus a small cost per
+  // split for the partial sums), with at least 16 K chunks per split
+  const int tiles = ((T + kGemmBM - 1) / kGemmBM) * ((E + BN - 1) / BN);
+  const int sms = device_sm_count();
+  int splits = 1;
+  double best = 1e30;
+  for (int S = 1; S <= max_splits && S <= h / 256; ++S) {
+    const double cost = double((int64_t(tiles) * S + sms - 1) / sms) / S + 0.002 * S;
+    if (cost < best - 1e-9) {
+      best = cost;
+      splits = S;
+    }
+  }
+  int kps = (h + splits - 1) / splits;
+  kps = (kps + kGemmBK - 1) / kGemmBK * kGemmBK;
+  splits = (h + kps - 1) / kps;
+  *nsplit = splits;
+  dim3 grid((T + kGemmBM - 1) / kGemmBM, (E + BN - 1) / BN, splits);
+  router_sgemm_kernel<BN, XT><<<grid, BN * 2, 0, s>>>(T, h, E, kps, x, Wg, partials);
   return cudaGetLastError();
 }
 
 template <typename XT>
 cudaError_t launch_logits_typed(int T, int h, int E, const XT* x, const float* Wg,
-                                const float* gb, float* logits, cudaStream_t s) {
-  if (E <= 8) return launch_logits_variant<XT, 8, 1, 1, 64>(T, h, E, x, Wg, gb, logits, s);
-  if (E <= 16) return launch_logits_variant<XT, 16, 2, 1, 64>(T, h, E, x, Wg, gb, logits, s);
-  if (E <= 32) return launch_logits_variant<XT, 32, 4, 1, 64>(T, h, E, x, Wg, gb, logits, s);
-  return launch_logits_variant<XT, 64, 4, 4, 32>(T, h, E, x, Wg, gb, logits, s);
+                                float* partials, int max_splits, int* nsplit, cudaStream_t s) {
+  *nsplit = 1;
+  const bool wg16 = (reinterpret_cast<uintptr_t>(Wg) & 15) == 0;  // 16-byte gate loads
+  if (E <= kSmallE && h <= kSmallEMaxHidden)
+    return launch_logits_small_e<XT>(T, h, E, x, Wg, partials, nsplit, s);
+  if (wg16 && E % 4 == 0 && E >= 64) {
+    if (E % 128 == 0)
+      return launch_sgemm<128, XT>(T, h, E, x, Wg, partials, max_splits, nsplit, s);
+    return launch_sgemm<64, XT>(T, h, E, x, Wg, partials, max_splits, nsplit, s);
+  }
+  if (E <= 8) return launch_logits_variant<XT, 8, 1, 1, 64>(T, h, E, x, Wg, partials, s);
+  if (E <= 16) return launch_logits_variant<XT, 16, 2, 1, 64>(T, h, E, x, Wg, partials, s);
+  if (E <= 32) return launch_logits_variant<XT, 32, 4, 1, 64>(T, h, E, x, Wg, partials, s);
+  return launch_logits_variant<XT, 64, 4, 4, 32>(T, h, E, x, Wg, partials, s);
 }
 
 // ------------------------------------------------------------------ top-k
@@ -188,6 +513,7 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 
 __global__ void __launch_bounds__(256)
     router_topk_kernel(int T, int E, int k, int score, const float* __restrict__ logits,
+                       int nsplit, const float* __restrict__ gate_bias,
                        const float* __restrict__ expert_bias, int32_t* __restrict__ topk_idx,
                        float* __restrict__ topk_prob, uint8_t* __restrict__ keep,
                        uint8_t* __restrict__ routing_map, int32_t* __restrict__ counts,
@@ -200,12 +526,18 @@ __global__ void __launch_bounds__(256)
   const int warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
   for (int t = blockIdx.x * nwarps + warp; t < T; t += gridDim.x * nwarps) {
-    const float* lrow = logits + (int64_t)t * E;
+    // logits = (partial sums in split order) + gate bias
     float s[kMaxPerLane], sel[kMaxPerLane];
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
       const int e = lane + 32 * i;
-      s[i] = (e < E) ? lrow[e] : -FLT_MAX;
+      if (e < E) {
+        float l = logits[(int64_t)t * E + e];
+        for (int sp = 1; sp < nsplit; ++sp) l += logits[((int64_t)sp * T + t) * E + e];
+        s[i] = gate_bias ? l + gate_bias[e] : l;
+      } else {
+        s[i] = -FLT_MAX;
+      }
     }
     if (score == MOE_SCORE_SOFTMAX_PRE) {
       float m = -FLT_MAX;
@@ -401,17 +733,19 @@ __global__ void __launch_bounds__(1024)
 }  // namespace
 
 cudaError_t launch_router_logits(int T, int h, int E, int dtype, const void* x, const float* Wg,
-                                 const float* gate_bias, float* logits, cudaStream_t s) {
+                                 float* partials, int* nsplit, cudaStream_t s) {
+  *nsplit = 1;
   if (T == 0) return cudaSuccess;
   if (dtype == MOE_F32)
-    return launch_logits_typed<float>(T, h, E, static_cast<const float*>(x), Wg, gate_bias,
-                                      logits, s);
+    return launch_logits_typed<float>(T, h, E, static_cast<const float*>(x), Wg, partials,
+                                      kMaxSplits, nsplit, s);
   return launch_logits_typed<__nv_bfloat16>(T, h, E, static_cast<const __nv_bfloat16*>(x), Wg,
-                                            gate_bias, logits, s);
+                                            partials, kMaxSplits, nsplit, s);
 }
 
-cudaError_t launch_router_topk(int T, int E, int k, int score, const float* logits,
-                               const float* expert_bias, int32_t* topk_idx, float* topk_prob,
+cudaError_t launch_router_topk(int T, int E, int k, int score, const float* logits, int nsplit,
+                               const float* gate_bias, const float* expert_bias,
+                               int32_t* topk_idx, float* topk_prob,
                                uint8_t* keep, uint8_t* routing_map, int32_t* counts, int* err,
                                cudaStream_t s) {
   if (T == 0) return cudaSuccess;
@@ -420,7 +754,8 @@ cudaError_t launch_router_topk(int T, int E, int k, int score, const float* logi
   const int cap = device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   router_topk_kernel<<<blocks, 32 * warps_per_block, 0, s>>>(
-      T, E, k, score, logits, expert_bias, topk_idx, topk_prob, keep, routing_map, counts, err);
+      T, E, k, score, logits, nsplit, gate_bias, expert_bias, topk_idx, topk_prob, keep,
+      routing_map, counts, err);
   return cudaGetLastError();
 }
 
