@@ -18,7 +18,7 @@
 //    n-tiles, row blocks inner so that CTAs running together share the
 //    weight tile (L2) and the expert's rows.  No host synchronisation.
 //  * Warp roles: warp 0 lane 0 issues TMA loads (A tile 128x64 and four
-//    64x64 weight boxes per stage, 128-byte swizzle, 4-stage ring), warp 1
+//    64xBK weight boxes per stage; a 4-deep ring of K=64 stages), warp 1
 //    allocates TMEM and lane 0 issues tcgen05.mma, warps 2-5 drain TMEM with
 //    tcgen05.ld, apply the epilogue and store.  Two accumulator buffers
 //    (2 x 256 of the 512 TMEM columns) overlap the epilogue of one tile with
@@ -38,12 +38,23 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 256;                      // MMA N = accumulator columns
-constexpr int BK = 64;                       // bf16 elements in one 128-byte swizzle row
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;         // 16 KB
-constexpr int BOX_BYTES = 64 * BK * 2;       // 8 KB: 64 (N) x 64 (K) weight box
-constexpr int B_BYTES = 4 * BOX_BYTES;       // 32 KB
+// K per pipeline stage.  64 (the default) gives 48 KB stages and a 4-deep
+// ring; 32 gives 24 KB stages and a 9-deep ring.  Measured on GB300 with the
+// Mixtral-shaped workload: 64 runs at ~1670 TFLOP/s, 32 at ~1000 (twice the
+// per-stage barrier/TMA work and half-width A rows outweigh the deeper ring).
+#ifndef MOE_TC_BK
+#define MOE_TC_BK 64
+#endif
+constexpr int BK = MOE_TC_BK;
+static_assert(BK == 32 || BK == 64, "K per stage");
+constexpr int A_BYTES = BM * BK * 2;         // BK=32: 8 KB (64-byte rows, 64-byte swizzle)
+constexpr int BOX_BYTES = 64 * BK * 2;       // 64 (N) x BK (K) weight box, 128-byte swizzle
+constexpr int B_BYTES = 4 * BOX_BYTES;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SMEM_BUDGET = 227 * 1024;
+constexpr int STAGES = (SMEM_BUDGET - 1024 - 4096) / STAGE_BYTES;  // 9 (BK=32) or 4 (BK=64)
+constexpr uint32_t A_LAYOUT = (BK == 64) ? ptx::kLayoutSw128 : ptx::kLayoutSw64;
+constexpr uint32_t A_SBO = 8 * BK * 2;       // 8-row groups of A
 constexpr int ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int THREADS = 192;
@@ -282,12 +293,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t b = a + A_BYTES;
 #pragma unroll
           for (int s = 0; s < BK / 16; ++s) {
-            // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; a K step
-            //    of 16 bf16 moves 32 B inside the swizzled row.
-            // B: MN-major, 128-byte swizzle; 64-column chunks (boxes) 8 KB
-            //    apart (LBO), 8-row K groups 1024 B apart (SBO); a K step of
-            //    16 rows moves 2048 B.
-            const uint64_t adesc = ptx::sw128_desc(a + s * 32, 16, 1024);
+            // A: K-major, rows of BK bf16 (64 or 128 bytes) with the matching
+            //    swizzle, 8-row groups A_SBO apart; a K step of 16 bf16 moves
+            //    32 B inside the swizzled row.
+            // B: MN-major, 128-byte swizzle; 64-column chunks (boxes)
+            //    BOX_BYTES apart (LBO), 8-row K groups 1024 B apart (SBO); a K
+            //    step of 16 rows moves 2048 B.
+            const uint64_t adesc = ptx::smem_desc(a + s * 32, 16, A_SBO, A_LAYOUT);
             const uint64_t bdesc = ptx::sw128_desc(b + s * 2048, BOX_BYTES, 1024);
             ptx::umma_bf16(d, adesc, bdesc, IDESC, (kb | s) != 0 ? 1u : 0u);
           }
@@ -394,7 +406,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 activation map [rows, inner], box 64 (inner) x 128 (rows).
+// 2-D bf16 activation map [rows, inner], box BK (inner) x 128 (rows), with the
+// swizzle whose span equals the box's row (64 or 128 bytes).
 bool map_rows(CUtensorMap* m, const void* ptr, int64_t inner, int64_t rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
@@ -403,11 +416,12 @@ bool map_rows(CUtensorMap* m, const void* ptr, int64_t inner, int64_t rows) {
   cuuint32_t box[2] = {BK, BM};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D bf16 weight map [E, K, N] (N contiguous), box 64 (N) x 64 (K) x 1.
+// 3-D bf16 weight map [E, K, N] (N contiguous), box 64 (N) x BK (K) x 1.
 bool map_weights(CUtensorMap* m, const void* ptr, int64_t N, int64_t K, int64_t E) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
