@@ -59,8 +59,13 @@ constexpr int ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int THREADS = 192;
 constexpr int NUM_BARS = 2 * STAGES + 5;     // full, empty, acc_full[2], acc_empty[2], drain
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16 +
+// fc2 epilogue staging: per epilogue warp a 32 x 32 fp32 tile with rows padded
+// to 36 floats (16-byte accesses of a quarter-warp hit distinct banks).
+constexpr int EPI_PITCH = 36;
+constexpr int EPI_BYTES = 4 * 32 * EPI_PITCH * 4;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16 +
                            2 * (MOE_MAX_EXPERTS + 1) * 4;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, /*b_mn_major=*/true);
 constexpr long long kWaitCycles = 4000000000LL;
 
@@ -134,7 +139,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  float* epi = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* off = reinterpret_cast<int*>(tmem_slot + 4);
@@ -330,19 +336,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      const int row = m0 + q * 32 + lane;
-      const bool valid = row < rend;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
+      float* etile = epi + q * (32 * EPI_PITCH);  // this warp's staging tile
+      const int rbase = m0 + q * 32;  // this warp's first row; lane l holds row rbase + l
+      const int sub = lane >> 3;
+      const int col4 = (lane & 7) * 4;
       if (MODE == FC1) {
-        __nv_bfloat16* out =
-            static_cast<__nv_bfloat16*>(args.out) + static_cast<int64_t>(row) * args.ldo + nt * (BN / 2);
+        // silu(a) * g, packed to bf16: each lane writes 64 contiguous bytes
+        // of its own row per 32-column chunk (whole 32-byte sectors; staging
+        // through shared memory as fc2 does was measured slower here).
+        const int row = rbase + lane;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) +
+                             static_cast<int64_t>(row) * args.ldo + nt * (BN / 2);
 #pragma unroll 1
         for (int c = 0; c < BN / 2; c += 32) {
           uint32_t a[32], g[32];
           ptx::tmem_ld32(tb + c, a);
           ptx::tmem_ld32(tb + BN / 2 + c, g);
           ptx::tmem_wait_ld();
-          if (valid) {
+          if (row < rend) {
             uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -360,19 +372,31 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else {
-        float* out = static_cast<float*>(args.out) + static_cast<int64_t>(row) * args.ldo + nt * BN;
+        // Stage the warp's 32 rows x 32 columns in shared memory, then store
+        // them by row segments: lanes 8s..8s+7 write the 128 contiguous bytes
+        // of one row, 4 rows per instruction (full lines, not one 16-byte
+        // piece of 32 different rows).
+        float* out0 = static_cast<float*>(args.out) + nt * BN;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t y[32];
           ptx::tmem_ld32(tb + c, y);
           ptx::tmem_wait_ld();
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(out + c);
+          float4* mine = reinterpret_cast<float4*>(etile + lane * EPI_PITCH);
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(__uint_as_float(y[4 * v]), __uint_as_float(y[4 * v + 1]),
-                                   __uint_as_float(y[4 * v + 2]), __uint_as_float(y[4 * v + 3]));
+          for (int v = 0; v < 8; ++v)
+            mine[v] = make_float4(__uint_as_float(y[4 * v]), __uint_as_float(y[4 * v + 1]),
+                                  __uint_as_float(y[4 * v + 2]), __uint_as_float(y[4 * v + 3]));
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int r = it * 4 + sub;
+            const float4 val = *reinterpret_cast<const float4*>(etile + r * EPI_PITCH + col4);
+            if (rbase + r < rend)
+              *reinterpret_cast<float4*>(out0 + static_cast<int64_t>(rbase + r) * args.ldo + c +
+                                         col4) = val;
           }
+          __syncwarp();
         }
       }
       ptx::tc_fence_before();
