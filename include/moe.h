@@ -217,6 +217,16 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32
  * the first failing index or wait site. */
 moe_status moe_check(void* ws, moe_stream_t stream, int32_t* info);
 
+/* Failure-detection self-test (not a step of the method): enqueues one
+ * thread that waits, through the same bounded-wait routine the grouped GEMM
+ * uses for its pipeline barriers, on a barrier that nothing ever signals.
+ * After `limit_cycles` SM clock cycles (> 0) the wait gives up, MOE_ERR_TIMEOUT
+ * is recorded in the error word of `ws` (at least 256 bytes, 16-byte
+ * aligned) and the kernel returns normally; moe_check(ws) then reports
+ * MOE_ERR_TIMEOUT and the CUDA context remains usable. */
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_cycles,
+                                     moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,5 +29,6 @@ from ._binding import (  # noqa: F401
     permute,
     permute_noalloc,
     route,
+    selftest_wait_timeout,
     workspace_size,
 )

@@ -24,7 +24,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_capacity",
            "moe_workspace_size", "moe_max_rows", "moe_route", "moe_permute", "moe_grouped_mlp",
            "moe_grouped_fc1", "moe_grouped_fc2", "moe_combine", "moe_forward", "moe_check",
-           "moe_permute_noalloc"]
+           "moe_permute_noalloc", "moe_selftest_wait_timeout"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -72,6 +72,7 @@ def lib():
             "moe_forward": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_check": ([vp, vp, ctypes.POINTER(i32)], i32),
             "moe_permute_noalloc": ([cfgp, vp, vp, vp, vp, vp, vp, vp], i32),
+            "moe_selftest_wait_timeout": ([vp, sz, i64, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -192,6 +193,13 @@ def forward(cfg, x, Wg, gate_bias, expert_bias, W1, W3, W2, y, ws, topk_idx=None
     _check(lib().moe_forward(ctypes.byref(cfg), _p(x), _p(Wg), _p(gate_bias), _p(expert_bias),
                              _p(W1), _p(W3), _p(W2), _p(y), _p(topk_idx), _p(topk_prob),
                              _p(tokens_per_expert), w, wb, _stream()), "moe_forward")
+
+
+def selftest_wait_timeout(ws, limit_cycles):
+    """Enqueue a bounded wait that is made to run out (see include/moe.h)."""
+    w, wb = _ws(ws)
+    _check(lib().moe_selftest_wait_timeout(w, wb, int(limit_cycles), _stream()),
+           "moe_selftest_wait_timeout")
 
 
 def check(ws):

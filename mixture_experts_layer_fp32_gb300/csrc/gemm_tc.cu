@@ -95,16 +95,11 @@ struct Ctl {
   // Bounded wait.  Returns false on timeout (recorded) or, when
   // `honour_abort`, as soon as another role has given up.
   __device__ bool wait(uint32_t b, uint32_t parity, int site, bool honour_abort = true) const {
-    const long long t0 = clock64();
-    while (!ptx::mbar_try_wait(b, parity)) {
-      if (honour_abort && *abort_flag) return false;
-      if (clock64() - t0 > kWaitCycles) {
-        *abort_flag = 1;
-        report_error(err, DEV_ERR_TIMEOUT, site);
-        return false;
-      }
-    }
-    return true;
+    bool timed_out;
+    if (ptx::mbar_wait_bounded(b, parity, kWaitCycles, abort_flag, honour_abort, &timed_out))
+      return true;
+    if (timed_out) report_error(err, DEV_ERR_TIMEOUT, site);
+    return false;
   }
 };
 

@@ -42,6 +42,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Bounded wait for the phase of `parity` on an mbarrier.  Gives up after
+// `limit` SM clock cycles (returns false), and -- when `honour_abort` -- as
+// soon as *abort_flag is set by another thread of the CTA.  On a timeout it
+// sets *abort_flag and returns false; the caller records the error.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit,
+                                                  volatile int* abort_flag, bool honour_abort,
+                                                  bool* timed_out) {
+  const long long t0 = clock64();
+  *timed_out = false;
+  while (!mbar_try_wait(bar, parity)) {
+    if (honour_abort && *abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      *abort_flag = 1;
+      *timed_out = true;
+      return false;
+    }
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");

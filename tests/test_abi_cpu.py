@@ -142,3 +142,11 @@ def test_binding_refuses_cpu_tensors(moe):
     x = torch.zeros(4, 256, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         moe.permute(cfg, x, x, None, x, x, x, x)
+
+
+def test_selftest_wait_timeout_host_checks(moe):
+    lib = moe.lib()
+    assert lib.moe_selftest_wait_timeout(None, 4096, 1000, None) == INVALID
+    assert lib.moe_selftest_wait_timeout(FAKE, 100, 1000, None) == INVALID     # too small for the error word
+    assert lib.moe_selftest_wait_timeout(FAKE, 4096, 0, None) == INVALID
+    assert lib.moe_selftest_wait_timeout(MISALIGNED, 4096, 1000, None) == INVALID
