@@ -30,6 +30,8 @@
 //  * Every wait is bounded: after ~2 s without progress the CTA records
 //    MOE_ERR_TIMEOUT in the workspace error word, lets its in-flight copies
 //    and MMAs finish (again bounded), frees its TMEM and exits.
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -82,15 +84,19 @@ struct TcArgs {
   int* err;
 };
 
-struct Ctl {
+// Barriers of an NS-stage ring: full[NS], empty[NS], acc_full[2],
+// acc_empty[2], drain.
+template <int NS>
+struct CtlN {
   uint64_t* bar;
   volatile int* abort_flag;
   int* err;
+  uint32_t peer_abort = 0;  // pair kernel: the other CTA's abort flag (shared::cluster)
   __device__ uint32_t full(int s) const { return ptx::smem_u32(bar + s); }
-  __device__ uint32_t empty(int s) const { return ptx::smem_u32(bar + STAGES + s); }
-  __device__ uint32_t acc_full(int b) const { return ptx::smem_u32(bar + 2 * STAGES + b); }
-  __device__ uint32_t acc_empty(int b) const { return ptx::smem_u32(bar + 2 * STAGES + 2 + b); }
-  __device__ uint32_t drain() const { return ptx::smem_u32(bar + 2 * STAGES + 4); }
+  __device__ uint32_t empty(int s) const { return ptx::smem_u32(bar + NS + s); }
+  __device__ uint32_t acc_full(int b) const { return ptx::smem_u32(bar + 2 * NS + b); }
+  __device__ uint32_t acc_empty(int b) const { return ptx::smem_u32(bar + 2 * NS + 2 + b); }
+  __device__ uint32_t drain() const { return ptx::smem_u32(bar + 2 * NS + 4); }
 
   // Bounded wait.  Returns false on timeout (recorded) or, when
   // `honour_abort`, as soon as another role has given up.
@@ -98,11 +104,18 @@ struct Ctl {
     bool timed_out;
     if (ptx::mbar_wait_bounded(b, parity, kWaitCycles, abort_flag, honour_abort, &timed_out))
       return true;
-    if (timed_out) report_error(err, DEV_ERR_TIMEOUT, site);
+    if (timed_out) {
+      report_error(err, DEV_ERR_TIMEOUT, site);
+      if (peer_abort) ptx::st_cluster_u32(peer_abort, 1u);
+    }
     return false;
   }
 };
+using Ctl = CtlN<STAGES>;
 
+// Tile `tile` of the device-built list: expert e, first row m0 of its row
+// block (ROWS rows per block), the expert's row end, and the n-tile.
+template <int ROWS = BM>
 __device__ __forceinline__ void decode_tile(int tile, const int* tstart, const int* off, int E,
                                             int& e, int& m0, int& rend, int& nt) {
   int lo = 0, hi = E;  // largest e in [0, E) with tstart[e] <= tile
@@ -111,11 +124,53 @@ __device__ __forceinline__ void decode_tile(int tile, const int* tstart, const i
     if (tstart[mid] <= tile) lo = mid; else hi = mid;
   }
   e = lo;
-  const int mt = (off[e + 1] - off[e] + BM - 1) / BM;
+  const int mt = (off[e + 1] - off[e] + ROWS - 1) / ROWS;
   const int u = tile - tstart[e];
   nt = u / mt;
-  m0 = off[e] + (u - nt * mt) * BM;
+  m0 = off[e] + (u - nt * mt) * ROWS;
   rend = off[e + 1];
+}
+
+// Per-expert tile prefix (tstart[0..E]) from the expert offsets, by warp 0:
+// expert e owns ceil(rows_e / ROWS) x NT tiles.  Inconsistent offsets (not
+// starting at 0, decreasing, or past max_rows) give an empty list and a
+// recorded device error.
+template <int ROWS>
+__device__ __forceinline__ void build_tile_prefix(const int* off, int* tstart, int E, int NT,
+                                                  int64_t max_rows, int* err, int lane) {
+  constexpr int PER = MOE_MAX_EXPERTS / 32;  // lane handles experts [8*lane, 8*lane + 8)
+  int v[PER];
+  int run = 0;
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane * PER + i;
+    int t = 0;
+    if (e < E) {
+      const int rows = off[e + 1] - off[e];
+      ok = ok && rows >= 0;
+      t = ((rows + ROWS - 1) / ROWS) * NT;
+    }
+    v[i] = t;
+    run += t;
+  }
+  if (lane == 0) ok = ok && off[0] == 0 && static_cast<int64_t>(off[E]) <= max_rows;
+  ok = __all_sync(0xffffffffu, ok);
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  int excl = incl - run;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane * PER + i;
+    if (e < E) tstart[e] = ok ? excl : 0;
+    excl += v[i];
+  }
+  if (lane == 31) tstart[E] = ok ? excl : 0;
+  if (!ok && lane == 0 && blockIdx.x == 0) report_error(err, DEV_ERR_INDEX, -1);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -124,6 +179,75 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __device__ __forceinline__ float silu_mul(float a, float g) { return a / (1.0f + __expf(-a)) * g; }
+
+// Drain one accumulator buffer into the output: this warp's 32 TMEM lanes at
+// `tb` hold rows rbase .. rbase+31 (lane l holds row rbase + l) of a tile of
+// n-tile `nt`; rows at or past `rend` belong to no row of this expert and are
+// not stored.  fc1 applies silu(a) * g and stores bf16, fc2 stores fp32.
+template <int MODE>
+__device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, int rbase, int rend,
+                                                  int nt, const TcArgs& args, int lane) {
+  const int sub = lane >> 3;
+  const int col4 = (lane & 7) * 4;
+  if (MODE == FC1) {
+    // silu(a) * g, packed to bf16: each lane writes 64 contiguous bytes
+    // of its own row per 32-column chunk (whole 32-byte sectors; staging
+    // through shared memory as fc2 does was measured slower here).
+    const int row = rbase + lane;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) +
+                         static_cast<int64_t>(row) * args.ldo + nt * (BN / 2);
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      uint32_t a[32], g[32];
+      ptx::tmem_ld32(tb + c, a);
+      ptx::tmem_ld32(tb + BN / 2 + c, g);
+      ptx::tmem_wait_ld();
+      if (row < rend) {
+        uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 0]), __uint_as_float(g[8 * v + 0])),
+                            silu_mul(__uint_as_float(a[8 * v + 1]), __uint_as_float(g[8 * v + 1])));
+          w.y = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 2]), __uint_as_float(g[8 * v + 2])),
+                            silu_mul(__uint_as_float(a[8 * v + 3]), __uint_as_float(g[8 * v + 3])));
+          w.z = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 4]), __uint_as_float(g[8 * v + 4])),
+                            silu_mul(__uint_as_float(a[8 * v + 5]), __uint_as_float(g[8 * v + 5])));
+          w.w = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 6]), __uint_as_float(g[8 * v + 6])),
+                            silu_mul(__uint_as_float(a[8 * v + 7]), __uint_as_float(g[8 * v + 7])));
+          dst[v] = w;
+        }
+      }
+    }
+  } else {
+    // Stage the warp's 32 rows x 32 columns in shared memory, then store
+    // them by row segments: lanes 8s..8s+7 write the 128 contiguous bytes
+    // of one row, 4 rows per instruction (full lines, not one 16-byte
+    // piece of 32 different rows).
+    float* out0 = static_cast<float*>(args.out) + nt * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t y[32];
+      ptx::tmem_ld32(tb + c, y);
+      ptx::tmem_wait_ld();
+      float4* mine = reinterpret_cast<float4*>(etile + lane * EPI_PITCH);
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        mine[v] = make_float4(__uint_as_float(y[4 * v]), __uint_as_float(y[4 * v + 1]),
+                              __uint_as_float(y[4 * v + 2]), __uint_as_float(y[4 * v + 3]));
+      __syncwarp();
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int r = it * 4 + sub;
+        const float4 val = *reinterpret_cast<const float4*>(etile + r * EPI_PITCH + col4);
+        if (rbase + r < rend)
+          *reinterpret_cast<float4*>(out0 + static_cast<int64_t>(rbase + r) * args.ldo + c +
+                                     col4) = val;
+      }
+      __syncwarp();
+    }
+  }
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -170,42 +294,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = args.offsets[e];
   __syncthreads();
-  if (warp == 0) {
-    // tile prefix over experts: lane handles experts [8*lane, 8*lane + 8)
-    constexpr int PER = MOE_MAX_EXPERTS / 32;
-    int v[PER];
-    int run = 0;
-    bool ok = true;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int e = lane * PER + i;
-      int t = 0;
-      if (e < E) {
-        const int rows = off[e + 1] - off[e];
-        ok = ok && rows >= 0;
-        t = ((rows + BM - 1) / BM) * NT;
-      }
-      v[i] = t;
-      run += t;
-    }
-    if (lane == 0) ok = ok && off[0] == 0 && static_cast<int64_t>(off[E]) <= args.max_rows;
-    ok = __all_sync(0xffffffffu, ok);
-    int incl = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    int excl = incl - run;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int e = lane * PER + i;
-      if (e < E) tstart[e] = ok ? excl : 0;
-      excl += v[i];
-    }
-    if (lane == 31) tstart[E] = ok ? excl : 0;
-    if (!ok && lane == 0 && blockIdx.x == 0) report_error(args.err, DEV_ERR_INDEX, -1);
-  }
+  if (warp == 0) build_tile_prefix<BM>(off, tstart, E, NT, args.max_rows, args.err, lane);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -334,66 +423,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
       float* etile = epi + q * (32 * EPI_PITCH);  // this warp's staging tile
       const int rbase = m0 + q * 32;  // this warp's first row; lane l holds row rbase + l
-      const int sub = lane >> 3;
-      const int col4 = (lane & 7) * 4;
-      if (MODE == FC1) {
-        // silu(a) * g, packed to bf16: each lane writes 64 contiguous bytes
-        // of its own row per 32-column chunk (whole 32-byte sectors; staging
-        // through shared memory as fc2 does was measured slower here).
-        const int row = rbase + lane;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) +
-                             static_cast<int64_t>(row) * args.ldo + nt * (BN / 2);
-#pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
-          uint32_t a[32], g[32];
-          ptx::tmem_ld32(tb + c, a);
-          ptx::tmem_ld32(tb + BN / 2 + c, g);
-          ptx::tmem_wait_ld();
-          if (row < rend) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 0]), __uint_as_float(g[8 * v + 0])),
-                                silu_mul(__uint_as_float(a[8 * v + 1]), __uint_as_float(g[8 * v + 1])));
-              w.y = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 2]), __uint_as_float(g[8 * v + 2])),
-                                silu_mul(__uint_as_float(a[8 * v + 3]), __uint_as_float(g[8 * v + 3])));
-              w.z = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 4]), __uint_as_float(g[8 * v + 4])),
-                                silu_mul(__uint_as_float(a[8 * v + 5]), __uint_as_float(g[8 * v + 5])));
-              w.w = pack_bf16x2(silu_mul(__uint_as_float(a[8 * v + 6]), __uint_as_float(g[8 * v + 6])),
-                                silu_mul(__uint_as_float(a[8 * v + 7]), __uint_as_float(g[8 * v + 7])));
-              dst[v] = w;
-            }
-          }
-        }
-      } else {
-        // Stage the warp's 32 rows x 32 columns in shared memory, then store
-        // them by row segments: lanes 8s..8s+7 write the 128 contiguous bytes
-        // of one row, 4 rows per instruction (full lines, not one 16-byte
-        // piece of 32 different rows).
-        float* out0 = static_cast<float*>(args.out) + nt * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t y[32];
-          ptx::tmem_ld32(tb + c, y);
-          ptx::tmem_wait_ld();
-          float4* mine = reinterpret_cast<float4*>(etile + lane * EPI_PITCH);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            mine[v] = make_float4(__uint_as_float(y[4 * v]), __uint_as_float(y[4 * v + 1]),
-                                  __uint_as_float(y[4 * v + 2]), __uint_as_float(y[4 * v + 3]));
-          __syncwarp();
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int r = it * 4 + sub;
-            const float4 val = *reinterpret_cast<const float4*>(etile + r * EPI_PITCH + col4);
-            if (rbase + r < rend)
-              *reinterpret_cast<float4*>(out0 + static_cast<int64_t>(rbase + r) * args.ldo + c +
-                                         col4) = val;
-          }
-          __syncwarp();
-        }
-      }
+      drain_accumulator<MODE>(tb, etile, rbase, rend, nt, args, lane);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ctl.acc_empty(buf));
@@ -403,6 +433,226 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ SM pairs
+// The same grouped GEMM on pairs of SMs: a 2-CTA cluster shares each MMA
+// (tcgen05 cta_group::2).  One M=256,N=256,K=16 MMA covers 256 rows; the
+// A rows are split 128/128 between the two CTAs' shared memories and so are
+// the 256 B columns, so each SM stages half of the weight tile it multiplies
+// by (half the shared-memory and L2 traffic per MMA of the one-SM kernel).
+// A stage is then 32 KB per CTA (A 128x64, B 64x128), which leaves room for
+// a 6-deep ring instead of 4.
+//  * fc1: rank 0 stages 128 columns of W1, rank 1 the same 128 columns of
+//    W3, so accumulator column j and 128+j are again the SwiGLU pair; fc2:
+//    rank r stages W2 columns nt*256 + 128r .. +127.
+//  * Both CTAs' producers load their own halves; the copies of both count on
+//    rank 0's full barrier (armed by rank 0 with both halves' bytes).  Rank 0
+//    issues the MMAs; its commits arrive on the empty/acc_full barriers of
+//    both CTAs.  Each CTA's TMEM holds the accumulator rows of its A half,
+//    and its epilogue warps drain them and arrive on rank 0's acc_empty.
+//  * A timed-out wait also raises the other CTA's abort flag, so the pair
+//    gives up together; every cross-CTA access happens before the final
+//    cluster barrier.
+constexpr int PM = 2 * BM;                      // rows per pair tile
+constexpr int P_STAGE_BYTES = A_BYTES + 2 * BOX_BYTES;
+constexpr int P_STAGES = (SMEM_BUDGET - 1024 - EPI_BYTES - 4096) / P_STAGE_BYTES;  // 6 (BK=64)
+constexpr int P_NUM_BARS = 2 * P_STAGES + 5;
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + EPI_BYTES + P_NUM_BARS * 8 + 16 +
+                             2 * (MOE_MAX_EXPERTS + 1) * 4;
+static_assert(P_SMEM_BYTES <= SMEM_BUDGET, "shared memory budget (pair)");
+static_assert(P_STAGES <= 32, "stage bit masks");
+constexpr uint32_t P_IDESC = ptx::idesc_bf16_f32(PM, BN, /*b_mn_major=*/true);
+// Bounded pause that lets a CTA's own in-flight copies land when it gives up
+// (their completion is counted on the other CTA's barrier).
+constexpr long long kPeerDrainCycles = 20000000LL;
+using PairCtl = CtlN<P_STAGES>;
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    tc_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB0,
+                           const __grid_constant__ CUtensorMap tmB1, TcArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  float* epi = reinterpret_cast<float*>(smem + P_STAGES * P_STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES + EPI_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + P_NUM_BARS);
+  int* abort_word = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* abort_flag = abort_word;
+  int* off = reinterpret_cast<int*>(tmem_slot + 4);
+  int* tstart = off + (MOE_MAX_EXPERTS + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+  const int E = args.E;
+  const int NT = args.num_n_tiles;
+  const int KB = args.k_blocks;
+  const PairCtl ctl{bars, abort_flag, args.err,
+                    ptx::mapa_shared(ptx::smem_u32(abort_word), rank ^ 1u)};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      ptx::mbar_init(ctl.full(s), 1);
+      ptx::mbar_init(ctl.empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ctl.acc_full(b), 1);
+      ptx::mbar_init(ctl.acc_empty(b), 8);  // 4 epilogue warps in each CTA
+    }
+    ptx::mbar_init(ctl.drain(), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB0);
+    ptx::prefetch_tensormap(&tmB1);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
+    ptx::tmem_relinquish_pair();
+  }
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = args.offsets[e];
+  __syncthreads();
+  if (warp == 0) build_tile_prefix<PM>(off, tstart, E, NT, args.max_rows, args.err, lane);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers initialised before any cross-CTA signal
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = tstart[E];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t fill_parity = 0, filled = 0;
+      bool alive = true;
+      const CUtensorMap* tmB = (MODE == FC1 && rank == 1) ? &tmB1 : &tmB0;
+      for (int tile = pair; alive && tile < total; tile += npairs) {
+        int e, m0, rend, nt;
+        decode_tile<PM>(tile, tstart, off, E, e, m0, rend, nt);
+        const int n0 = (MODE == FC1) ? nt * (BN / 2) : nt * BN + static_cast<int>(rank) * (BN / 2);
+        const int a_row = m0 + static_cast<int>(rank) * BM;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ctl.wait(ctl.empty(stage), phase ^ 1u, 1)) {
+            alive = false;
+            break;
+          }
+          if (rank == 0) ptx::mbar_arrive_expect_tx(ctl.full(stage), 2 * P_STAGE_BYTES);
+          const uint32_t fb = ptx::mapa_shared(ctl.full(stage), 0);
+          const uint32_t a = ptx::smem_u32(stages + stage * P_STAGE_BYTES);
+          const uint32_t b = a + A_BYTES;
+          const int kc = kb * BK;
+          ptx::tma_load_2d_pair(a, &tmA, kc, a_row, fb);
+          ptx::tma_load_3d_pair(b, tmB, n0, kc, e, fb);
+          ptx::tma_load_3d_pair(b + BOX_BYTES, tmB, n0 + 64, kc, e, fb);
+          filled |= 1u << stage;
+          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (alive) {
+        // every filled stage released by the MMAs (the commits arrive in both CTAs)
+        for (int i = 0; i < P_STAGES; ++i) {
+          if (!ctl.wait(ctl.empty(stage), phase ^ 1u, 2, false)) break;
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      } else if (rank == 0) {
+        for (int s = 0; s < P_STAGES; ++s)
+          if (filled >> s & 1u) ctl.wait(ctl.full(s), fill_parity >> s & 1u, 3, false);
+      } else {
+        const long long t0 = clock64();
+        while (clock64() - t0 < kPeerDrainCycles) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------ MMA issuer (rank 0)
+      int stage = 0;
+      uint32_t phase = 0;
+      bool alive = true;
+      int it = 0;
+      for (int tile = pair; alive && tile < total; tile += npairs, ++it) {
+        const int buf = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!ctl.wait(ctl.acc_empty(buf), aph ^ 1u, 4)) {
+          alive = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + buf * ACC_COLS;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ctl.wait(ctl.full(stage), phase, 5)) {
+            alive = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a = ptx::smem_u32(stages + stage * P_STAGE_BYTES);
+          const uint32_t b = a + A_BYTES;
+#pragma unroll
+          for (int s = 0; s < BK / 16; ++s) {
+            // same descriptors as the one-SM kernel, read at the same
+            // offsets in both CTAs' shared memories; B has two 64-column
+            // boxes per CTA
+            const uint64_t adesc = ptx::smem_desc(a + s * 32, 16, A_SBO, A_LAYOUT);
+            const uint64_t bdesc = ptx::sw128_desc(b + s * 2048, BOX_BYTES, 1024);
+            ptx::umma_bf16_pair(d, adesc, bdesc, P_IDESC, (kb | s) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit_pair(ctl.empty(stage), 3);
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!alive) break;
+        ptx::umma_commit_pair(ctl.acc_full(buf), 3);
+      }
+      if (!alive) {
+        ptx::umma_commit_pair(ctl.drain(), 1);
+        ctl.wait(ctl.drain(), 0, 6, false);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps 2..5 (both CTAs)
+    const int q = warp & 3;
+    int it = 0;
+    for (int tile = pair; tile < total; tile += npairs, ++it) {
+      const int buf = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      int e, m0, rend, nt;
+      decode_tile<PM>(tile, tstart, off, E, e, m0, rend, nt);
+      bool ok = ctl.wait(ctl.acc_full(buf), aph, 7);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
+      float* etile = epi + q * (32 * EPI_PITCH);
+      const int rbase = m0 + static_cast<int>(rank) * BM + q * 32;
+      drain_accumulator<MODE>(tb, etile, rbase, rend, nt, args, lane);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ctl.acc_empty(buf), 0));
+    }
+  }
+  __syncthreads();
+  ptx::cluster_sync();  // no cross-CTA access after this point
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -475,6 +725,64 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   return cudaGetLastError();
 }
 
+// Pairs of SMs that can be resident at once for the pair kernel (0: none, or
+// the query failed).
+template <int MODE>
+int pair_slots() {
+  static int cache[64] = {0};  // per device; -1 = queried, unusable
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = P_SMEM_BYTES;
+    if (cudaFuncSetAttribute(tc_grouped_pair_kernel<MODE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             P_SMEM_BYTES) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, tc_grouped_pair_kernel<MODE>, &cfg) != cudaSuccess ||
+        n <= 0) {
+      cudaGetLastError();  // clear a failed query; the one-SM kernel is used instead
+      n = -1;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev] > 0 ? cache[dev] : 0;
+}
+
+template <int MODE>
+cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                           const TcArgs& args, int slots, cudaStream_t s) {
+  const int64_t max_tiles = ((args.max_rows + PM - 1) / PM + args.E) * args.num_n_tiles;
+  int64_t pairs = slots;
+  if (pairs > max_tiles) pairs = max_tiles;
+  if (pairs <= 0) return cudaSuccess;
+  tc_grouped_pair_kernel<MODE><<<static_cast<unsigned>(2 * pairs), THREADS, P_SMEM_BYTES, s>>>(
+      a, b0, b1, args);
+  return cudaGetLastError();
+}
+
+// Experts averaging at least this many rows run on SM pairs (256-row tiles);
+// fewer rows per expert keep 128-row tiles on single SMs, where a 256-row
+// tile would mostly compute rows that are not stored.  MOE_TC_PAIR=0 / =1 in
+// the environment forces one kernel or the other (a tuning override).
+constexpr int64_t kPairMinRows = 768;
+
+template <int MODE>
+cudaError_t launch_grouped(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                           const TcArgs& args, cudaStream_t s) {
+  const char* force = getenv("MOE_TC_PAIR");
+  bool pair = args.max_rows >= static_cast<int64_t>(args.E) * kPairMinRows;
+  if (force && force[0] == '0') pair = false;
+  if (force && force[0] == '1') pair = true;
+  if (pair) {
+    const int slots = pair_slots<MODE>();
+    if (slots > 0) return launch_tc_pair<MODE>(a, b0, b1, args, slots, s);
+  }
+  return launch_tc<MODE>(a, b0, b1, args, s);
+}
+
 }  // namespace
 
 cudaError_t launch_tc_fc1(int E, int h, int f, int64_t max_rows, const void* x_perm,
@@ -486,7 +794,7 @@ cudaError_t launch_tc_fc1(int E, int h, int f, int64_t max_rows, const void* x_p
       !map_weights(&b1, W3, f, h, E))
     return cudaErrorInvalidValue;
   TcArgs args{offsets, E, f / (BN / 2), h / BK, max_rows, h_mid, f, err};
-  return launch_tc<FC1>(a, b0, b1, args, s);
+  return launch_grouped<FC1>(a, b0, b1, args, s);
 }
 
 cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_mid,
@@ -497,7 +805,7 @@ cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_m
   if (!map_rows(&a, h_mid, f, max_rows) || !map_weights(&b0, W2, h, f, E))
     return cudaErrorInvalidValue;
   TcArgs args{offsets, E, h / BN, f / BK, max_rows, y_perm, h, err};
-  return launch_tc<FC2>(a, b0, b0, args, s);
+  return launch_grouped<FC2>(a, b0, b0, args, s);
 }
 
 }  // namespace moe
