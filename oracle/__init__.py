@@ -196,10 +196,26 @@ def route(x, Wg, k, score, gate_bias=None, expert_bias=None, capacity_factor=0.0
             "tokens_per_expert": kept}
 
 
+def shared_expert(x, W1s, W3s, W2s, want_h_mid=False, nthreads=0):
+    """The shared expert of the Megatron Core page (§11; the layer forward of
+    §2 adds it: hidden = shared_expert(hidden_in) + routed output): one SwiGLU
+    MLP applied to every token, no router.  It is the same SwiGLU row
+    computation as a routed expert, with every row on the single expert 0.
+    W1s/W3s [h,fs], W2s [fs,h].  Returns y_shared [T,h] (and h_mid_s [T,fs])
+    in float64."""
+    x = _c(x)
+    T = x.shape[0]
+    expert = np.zeros(T, np.int32)
+    return expert_rows(x, expert, _c(W1s)[None], _c(W3s)[None], _c(W2s)[None],
+                       want_h_mid=want_h_mid, nthreads=nthreads)
+
+
 def forward(x, Wg, W1, W3, W2, k, score, gate_bias=None, expert_bias=None,
             capacity_factor=0.0, min_capacity=0, drop_policy="probs", nthreads=0,
-            want_h_mid=False):
-    """The whole layer: route -> drop -> permute -> SwiGLU experts -> combine."""
+            want_h_mid=False, W1s=None, W3s=None, W2s=None):
+    """The whole layer: route -> drop -> permute -> SwiGLU experts -> combine,
+    plus the shared expert's output when W1s/W3s/W2s are given (added to the
+    routed sum in double: y = sum_j p_j Y_j + Y_shared)."""
     r = route(x, Wg, k, score, gate_bias, expert_bias, capacity_factor, min_capacity,
               drop_policy, nthreads)
     E = Wg.shape[1]
@@ -209,6 +225,10 @@ def forward(x, Wg, W1, W3, W2, k, score, gate_bias=None, expert_bias=None,
     res = expert_rows(x_perm, row_expert, W1, W3, W2, want_h_mid=want_h_mid, nthreads=nthreads)
     y_perm, h_mid = (res if want_h_mid else (res, None))
     y = combine(y_perm, row_map, r["topk_prob"], nthreads)
+    if W1s is not None:
+        y_shared, h_mid_s = shared_expert(x, W1s, W3s, W2s, want_h_mid=True, nthreads=nthreads)
+        r.update({"y_routed": y, "y_shared": y_shared, "h_mid_s": h_mid_s})
+        y = y + y_shared
     r.update({"offsets": offsets, "row_map": row_map, "row_token": row_token,
               "x_perm": x_perm, "y_perm": y_perm, "h_mid": h_mid, "y": y})
     return r

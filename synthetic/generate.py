@@ -24,6 +24,9 @@ _ID_W3 = 4
 _ID_W2 = 5
 _ID_EXPERT_BIAS = 6
 _ID_EXPERT_RANK = 7
+_ID_W1S = 8
+_ID_W3S = 9
+_ID_W2S = 10
 _ID_X_REDRAW = 1000
 
 
@@ -60,10 +63,13 @@ def logit_std(w: Workload) -> float:
 
 
 def expert_weights(w: Workload, which: str, e: int, device="cpu", seed=None):
-    """W1[e] or W3[e] ([h,f]) or W2[e] ([f,h]) in the workload dtype."""
+    """W1[e] or W3[e] ([h,f]) or W2[e] ([f,h]) in the workload dtype; with
+    which = W1s / W3s ([h,shared_f]) or W2s ([shared_f,h]) the shared expert's."""
     seed = w.seed if seed is None else seed
-    tid = {"W1": _ID_W1, "W3": _ID_W3, "W2": _ID_W2}[which]
-    shape = (w.h, w.f) if which in ("W1", "W3") else (w.f, w.h)
+    tid = {"W1": _ID_W1, "W3": _ID_W3, "W2": _ID_W2,
+           "W1s": _ID_W1S, "W3s": _ID_W3S, "W2s": _ID_W2S}[which]
+    f = w.shared_f if which.endswith("s") else w.f
+    shape = (w.h, f) if which[:2] in ("W1", "W3") else (f, w.h)
     return _normal(shape, w.w_std, _gen(device, seed, tid, e), device, _torch_dtype(w))
 
 
@@ -79,7 +85,8 @@ def generate(w: Workload, device="cpu", seed=None, with_experts=True):
 
     Returns a dict with x [T,h], Wg [h,E] fp32, gate_bias [E] fp32 or None,
     expert_bias [E] fp32 or None and, if `with_experts`, W1/W3 [E,h,f] and
-    W2 [E,f,h] in the workload dtype.
+    W2 [E,f,h] in the workload dtype (plus W1s/W3s [h,shared_f] and W2s
+    [shared_f,h] when the workload has a shared expert).
     """
     seed = w.seed if seed is None else seed
     dt = _torch_dtype(w)
@@ -107,6 +114,9 @@ def generate(w: Workload, device="cpu", seed=None, with_experts=True):
             for e in range(w.E):
                 t[e] = expert_weights(w, name, e, device=device, seed=seed)
             out[name] = t
+        if w.shared_f > 0:
+            for name in ("W1s", "W3s", "W2s"):
+                out[name] = expert_weights(w, name, 0, device=device, seed=seed)
     return out
 
 

@@ -14,6 +14,9 @@ factor, expert weights W1/W3 [E,h,f] and W2 [E,f,h]).  Names:
   f=1536, expert loads skewed to Zipf(s=1.1) through a gate-logit bias.
 * ``switch``     - Switch-style top-1 with capacity factor 1.25: T=32768,
   h=1024, E=64, f=4096, four hot experts at 4x the mean load, so drops occur.
+* ``dsv3_shared`` - ``dsv3`` plus one shared expert of width 2048 (DeepSeek-V3
+  has one shared expert as wide as a routed one) that every token goes
+  through, added to the routed output.
 """
 
 from dataclasses import dataclass, replace
@@ -43,6 +46,7 @@ class Workload:
     drop_policy: str = "probs"     # "probs" or "position"
     gate_bias: Optional[str] = None      # None, "zipf:<s>" or "hot:<n>:<mult>"
     expert_bias: Optional[str] = None    # None or "uniform:<a>" (selection only)
+    shared_f: int = 0              # > 0: a shared expert of this SwiGLU width
     description: str = ""
 
     @property
@@ -87,6 +91,10 @@ WORKLOADS = {
                     "E=64, capacity factor 1.25, SwiGLU f=4096, 4 hot experts at 4x "
                     "mean load"),
 }
+WORKLOADS["dsv3_shared"] = replace(
+    WORKLOADS["dsv3"], name="dsv3_shared", shared_f=2048,
+    description="dsv3 plus one shared SwiGLU expert (width 2048) applied to every token and "
+                "added to the routed output")
 
 
 def scaled(name_or_workload, **overrides) -> Workload:

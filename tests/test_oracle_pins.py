@@ -346,3 +346,54 @@ def test_forward_bf16_inputs_equal_widened_f32():
     a = oracle.forward(bits(xf), Wg, *[bits(w) for w in Ws], k, "softmax_post")
     b = oracle.forward(xf.float().numpy(), Wg, *[w.float().numpy() for w in Ws], k, "softmax_post")
     np.testing.assert_array_equal(a["y"], b["y"])
+
+
+# ----------------------------------------------------------- shared expert --
+
+def test_shared_expert_one_hot_closed_form():
+    # x = e_i: y_shared = (silu(W1s[i,:]) * W3s[i,:]) . W2s for every token,
+    # whatever the routing; a transposed W1s/W3s (or W2s) would pick a column.
+    T, h, E, k, f, fs = 7, 7, 3, 2, 4, 5
+    r = rng(100)
+    x = np.eye(h, dtype=np.float32)[r.permutation(h)[:T]]
+    Wg = r.standard_normal((h, E)).astype(np.float32)
+    W1, W3, W2 = _weights(101, E, h, f)
+    W1s, W3s, W2s = (r.standard_normal(s).astype(np.float32) for s in ((h, fs), (h, fs), (fs, h)))
+    out = oracle.forward(x, Wg, W1, W3, W2, k, "softmax_post", W1s=W1s, W3s=W3s, W2s=W2s)
+    for t in range(T):
+        i = int(np.argmax(x[t]))
+        a, g = W1s[i].astype(np.float64), W3s[i].astype(np.float64)
+        H = a * expit(a) * g
+        np.testing.assert_allclose(out["h_mid_s"][t], H, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(out["y_shared"][t], H @ W2s.astype(np.float64),
+                                   rtol=1e-12, atol=1e-14)
+    # the layer output is the routed output plus the shared one
+    np.testing.assert_allclose(out["y"], out["y_routed"] + out["y_shared"], rtol=0, atol=0)
+
+
+def test_shared_expert_equals_a_routed_expert_with_probability_one():
+    # one routed expert, top-1 post-softmax (p = 1 exactly) and identical
+    # weights: the routed output and the shared one coincide, and y doubles
+    T, h, f = 9, 6, 5
+    r = rng(102)
+    x = r.standard_normal((T, h)).astype(np.float32)
+    Wg = r.standard_normal((h, 1)).astype(np.float32)
+    W1, W3, W2 = _weights(103, 1, h, f)
+    out = oracle.forward(x, Wg, W1, W3, W2, 1, "softmax_post", W1s=W1[0], W3s=W3[0], W2s=W2[0])
+    assert np.all(out["topk_prob"] == 1.0)
+    np.testing.assert_array_equal(out["y_shared"], out["y_routed"])
+    np.testing.assert_array_equal(out["y"], 2.0 * out["y_routed"])
+
+
+def test_shared_expert_zero_down_projection_leaves_routed_output():
+    T, h, E, k, f, fs = 10, 8, 4, 2, 6, 4
+    r = rng(104)
+    x = r.standard_normal((T, h)).astype(np.float32)
+    Wg = r.standard_normal((h, E)).astype(np.float32)
+    W1, W3, W2 = _weights(105, E, h, f)
+    W1s, W3s = (r.standard_normal((h, fs)).astype(np.float32) for _ in range(2))
+    base = oracle.forward(x, Wg, W1, W3, W2, k, "softmax_post")
+    out = oracle.forward(x, Wg, W1, W3, W2, k, "softmax_post", W1s=W1s, W3s=W3s,
+                         W2s=np.zeros((fs, h), np.float32))
+    assert np.all(out["y_shared"] == 0.0)
+    np.testing.assert_array_equal(out["y"], base["y"])
