@@ -41,6 +41,23 @@ METRIC = "MoE fwd tokens/sec"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "mixtral"
 STAGES = ["route", "permute", "fc1", "fc2", "combine"]
+# experts averaging at least this many rows run on the SM-pair GEMM kernel
+# (the library's selection rule; MOE_TC_PAIR=0/1 overrides it)
+PAIR_MIN_ROWS = 768
+
+
+def stages_of(w):
+    """Timed stages of one forward (the shared expert between fc2 and combine)."""
+    return STAGES[:4] + (["shared"] if w.shared_f > 0 else []) + STAGES[4:]
+
+
+def gemm_kernel_name(w, rows, stage):
+    force = os.environ.get("MOE_TC_PAIR", "")
+    pair = rows >= (1 if stage == "shared" else w.E) * PAIR_MIN_ROWS
+    if force[:1] in ("0", "1"):
+        pair = force[:1] == "1"
+    base = "tc_grouped_pair_kernel" if pair else "tc_grouped_kernel"
+    return "%s<%s>" % (base, "FC1" if stage in ("fc1", "shared") else "FC2")
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -90,6 +107,7 @@ def measured_peaks():
 def workload_desc(w):
     return {"workload": w.description, "name": w.name, "T": w.T, "h": w.h, "E": w.E, "k": w.k,
             "f": w.f, "score": w.score, "capacity_factor": w.capacity_factor,
+            "shared_f": w.shared_f,
             "l2": "flushed between timed steps (512 MB write outside the events)"}
 
 
@@ -180,7 +198,8 @@ def kernels_per_forward(w, cfg):
     cap = moe.capacity(cfg)
     drops = 0 <= cap < w.T
     route = 2 + (4 if drops else 0)   # logits, top-k (+ hist, scan, rank, select)
-    return route + 4 + 1 + 1 + 1      # permute hist/scan/rank/copy, fc1, fc2, combine
+    shared = 2 if w.shared_f > 0 else 0  # the shared expert's fc1 and fc2
+    return route + 4 + 1 + 1 + shared + 1  # permute hist/scan/rank/copy, fc1, fc2, combine
 
 
 def stage_work(w, R):
@@ -193,7 +212,9 @@ def stage_work(w, R):
         "permute": {"bytes": T * h * b + R * h * b + T * k * (4 + 1 + 4)},
         "fc1": {"flops": 4 * R * h * f, "bytes": 2 * w.E * h * f * b + R * h * b + R * f * b},
         "fc2": {"flops": 2 * R * f * h, "bytes": w.E * f * h * b + R * f * b + R * h * 4},
-        "combine": {"bytes": R * h * 4 + T * h * b + T * k * 8},
+        "combine": {"bytes": R * h * 4 + T * h * b + T * k * 8 + (T * h * 4 if w.shared_f else 0)},
+        "shared": {"flops": 6 * T * h * w.shared_f,
+                   "bytes": 3 * h * w.shared_f * b + T * h * b + 2 * T * w.shared_f * b + T * h * 4},
     }
 
 
@@ -209,6 +230,10 @@ def run_native(args, rank, world, local):
     b = moe.Buffers(cfg, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    stage_names = stages_of(w)
+    if w.shared_f > 0:
+        h_mid_s = torch.empty((w.T, w.shared_f), dtype=moe.act_dtype(cfg), device=dev)
+        y_shared = torch.empty((w.T, w.h), dtype=torch.float32, device=dev)
 
     def step(ev=None):
         if ev: ev[0].record(stream)
@@ -222,16 +247,24 @@ def run_native(args, rank, world, local):
         if ev: ev[3].record(stream)
         moe.grouped_fc2(cfg, b.h_mid, b.expert_offsets, inp["W2"], b.y_perm, b.ws)
         if ev: ev[4].record(stream)
-        moe.combine(cfg, b.y_perm, b.row_map, b.topk_prob, b.y)
-        if ev: ev[5].record(stream)
+        if w.shared_f > 0:
+            moe.shared_expert(cfg, w.shared_f, inp["x"], inp["W1s"], inp["W3s"], inp["W2s"],
+                              h_mid_s, y_shared, b.ws)
+            if ev: ev[5].record(stream)
+            moe.combine_shared(cfg, b.y_perm, b.row_map, b.topk_prob, y_shared, b.y)
+        else:
+            moe.combine(cfg, b.y_perm, b.row_map, b.topk_prob, b.y)
+        if ev: ev[-1].record(stream)
 
+    fma_tflops = fp32_fma_rate(moe, dev, stream)
     for _ in range(args.warmup):
         step()
     moe.check(b.ws)
     R = int(b.expert_offsets[-1].item())
     tpe = b.tokens_per_expert.cpu().numpy()
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
+              for _ in range(args.steps)]
     clocks = ClockSampler(local, enabled=not args.no_clocks and rank == 0)
     if clocks.proc is not None:
         time.sleep(0.5)  # let the sampler start before the timed region
@@ -248,8 +281,8 @@ def run_native(args, rank, world, local):
     moe.check(b.ws)
 
     stage_ms = {s: [events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps)]
-                for j, s in enumerate(STAGES)}
-    step_ms = [events[i][0].elapsed_time(events[i][5]) for i in range(args.steps)]
+                for j, s in enumerate(stage_names)}
+    step_ms = [events[i][0].elapsed_time(events[i][-1]) for i in range(args.steps)]
     ms = sum(step_ms) / len(step_ms)
     ms_all, tokens_per_s = job_throughput(ms, w.T, world)
 
@@ -260,12 +293,20 @@ def run_native(args, rank, world, local):
         y_host = torch.empty(b.y.shape, dtype=b.y.dtype).pin_memory()
         x_dev = torch.empty_like(inp["x"])
         y_dev = torch.empty_like(b.y)
-        ws2 = moe.alloc_workspace(cfg, dev)
+        if w.shared_f > 0:
+            ws2 = moe.alloc_workspace_shared(cfg, w.shared_f, dev)
+        else:
+            ws2 = moe.alloc_workspace(cfg, dev)
 
         def fwd():
             x_dev.copy_(x_host, non_blocking=True)
-            moe.forward(cfg, x_dev, inp["Wg"], inp["gate_bias"], inp["expert_bias"], inp["W1"],
-                        inp["W3"], inp["W2"], y_dev, ws2)
+            if w.shared_f > 0:
+                moe.forward_shared(cfg, w.shared_f, x_dev, inp["Wg"], inp["gate_bias"],
+                                   inp["expert_bias"], inp["W1"], inp["W3"], inp["W2"],
+                                   inp["W1s"], inp["W3s"], inp["W2s"], y_dev, ws2)
+            else:
+                moe.forward(cfg, x_dev, inp["Wg"], inp["gate_bias"], inp["expert_bias"],
+                            inp["W1"], inp["W3"], inp["W2"], y_dev, ws2)
             y_host.copy_(y_dev, non_blocking=True)
 
         for _ in range(max(1, args.warmup)):
@@ -286,7 +327,8 @@ def run_native(args, rank, world, local):
         e2e = {"value": world * w.T / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                "d2h_bytes_per_step": y_host.numel() * y_host.element_size(),
-               "api": "moe_forward (C ABI) with pinned host x/y copies inside the timed region"}
+               "api": "%s (C ABI) with pinned host x/y copies inside the timed region"
+                      % ("moe_forward_shared" if w.shared_f > 0 else "moe_forward")}
 
     if rank != 0:
         return None
@@ -294,7 +336,7 @@ def run_native(args, rank, world, local):
     peaks = measured_peaks()
     work = stage_work(w, R)
     stages = {}
-    for s in STAGES:
+    for s in stage_names:
         t = sum(stage_ms[s]) / len(stage_ms[s])
         ent = {"ms": t, "share": t / ms}
         if "flops" in work[s]:
@@ -302,12 +344,17 @@ def run_native(args, rank, world, local):
         if "bytes" in work[s]:
             ent["gbs"] = work[s]["bytes"] / (t * 1e-3) / 1e9
         stages[s] = ent
+    # the fp32 router GEMM at E >= 64 is bound by the FMA pipe: its fraction of
+    # the FMA rate measured in this run (the small-E router is HBM-bound)
+    if w.E >= 64:
+        stages["route"]["alu_frac"] = stages["route"]["tflops"] / fma_tflops
+    peaks["fp32_fma_tflops"] = fma_tflops
     gemm_ms = stages["fc1"]["ms"] + stages["fc2"]["ms"]
     gemm_tflops = (work["fc1"]["flops"] + work["fc2"]["flops"]) / (gemm_ms * 1e-3) / 1e12
 
-    dom = max(STAGES, key=lambda s: stages[s]["ms"])
+    dom = max(stage_names, key=lambda s: stages[s]["ms"])
     if dom in ("fc1", "fc2") and w.dtype == "bf16":
-        roof = {"kernel": "tc_grouped_kernel<%s>" % dom.upper(), "bound": "tensor",
+        roof = {"kernel": gemm_kernel_name(w, w.T * w.k, dom), "bound": "tensor",
                 "achieved": stages[dom]["tflops"], "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s"}
     else:
@@ -339,6 +386,24 @@ def run_native(args, rank, world, local):
         "peaks": peaks,
     }
     return line
+
+
+def fp32_fma_rate(moe, dev, stream, iters=4096, reps=5):
+    """FP32 FMA TFLOP/s of this GPU (the library's FMA-chain probe, best of
+    `reps` event-timed launches after one warm-up launch)."""
+    out = torch.zeros(4 * torch.cuda.get_device_properties(dev).multi_processor_count,
+                      dtype=torch.float32, device=dev)
+    moe.probe_fp32_fma(iters, out)
+    best = None
+    for _ in range(reps):
+        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        flops = moe.probe_fp32_fma(iters, out)
+        c.record(stream)
+        c.synchronize()
+        t = a.elapsed_time(c) * 1e-3
+        best = t if best is None or t < best else best
+    return flops / best / 1e12
 
 
 def barrier(world):
@@ -379,11 +444,12 @@ def oracle_sample_run(w, inp_cpu, tokens, nthreads=0):
     import oracle
     x = inp_cpu["x"][torch.from_numpy(tokens)]
     t0 = time.perf_counter()
+    shared = {n: np_view(inp_cpu[n]) for n in ("W1s", "W3s", "W2s")} if w.shared_f > 0 else {}
     oracle.forward(np_view(x), np_view(inp_cpu["Wg"]), np_view(inp_cpu["W1"]),
                    np_view(inp_cpu["W3"]), np_view(inp_cpu["W2"]), w.k, w.score,
                    np_view(inp_cpu["gate_bias"]), np_view(inp_cpu["expert_bias"]),
                    0.0 if w.capacity_factor <= 0 else w.capacity_factor * w.T / len(tokens),
-                   w.min_capacity, w.drop_policy, nthreads)
+                   w.min_capacity, w.drop_policy, nthreads, **shared)
     return time.perf_counter() - t0
 
 

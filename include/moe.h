@@ -188,6 +188,49 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
                        size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * Shared expert (§11 of the Megatron Core page, and the layer forward of its
+ * §2: hidden = shared_expert(hidden_in) + routed output): one dense SwiGLU MLP
+ * of width fs that every token goes through, chosen by no router, its output
+ * added to the routed experts' combined output.
+ *
+ * moe_shared_expert: y_shared = (silu(x . W1s) * (x . W3s)) . W2s for all T
+ * tokens (the grouped MLP kernels run as one dense group of T rows).
+ *   fs: the shared expert's hidden width, > 0, a multiple of 8 (MOE_F32) or
+ *       of 128 (MOE_BF16), else MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED.
+ *   x [T,h] dtype, W1s/W3s [h,fs] dtype, W2s [fs,h] dtype,
+ *   h_mid_s [T,fs] dtype out (scratch the caller owns), y_shared [T,h] fp32 out.
+ *   ws / ws_bytes: a workspace of moe_workspace_size(cfg) bytes or more
+ *   (only its error word is used).
+ *
+ * moe_combine_shared: moe_combine with the shared row added after the routed
+ * slots, still in fp32 and rounded once: y[t] = sum_j p[t,j] * y_perm[..] +
+ * y_shared[t].  y_shared may be NULL (then it is moe_combine).
+ *
+ * moe_workspace_size_shared: bytes of the workspace moe_forward_shared needs
+ * (moe_workspace_size plus room for h_mid_s and y_shared).
+ *
+ * moe_forward_shared: moe_forward plus the shared expert.  The shared path
+ * does not depend on the routing, so it is enqueued on a second stream of
+ * the library's (forked from `stream` by an event and joined back before the
+ * combine; capturable in a CUDA graph like the rest).  Same arguments as
+ * moe_forward plus fs and the shared weights; ws is moe_workspace_size_shared
+ * bytes.
+ */
+moe_status moe_shared_expert(const moe_config* cfg, int32_t fs, const void* x, const void* W1s,
+                             const void* W3s, const void* W2s, void* h_mid_s, float* y_shared,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+moe_status moe_combine_shared(const moe_config* cfg, const float* y_perm, const int32_t* row_map,
+                              const float* topk_prob, const float* y_shared, void* y,
+                              moe_stream_t stream);
+moe_status moe_workspace_size_shared(const moe_config* cfg, int32_t fs, size_t* bytes);
+moe_status moe_forward_shared(const moe_config* cfg, int32_t fs, const void* x, const float* Wg,
+                              const float* gate_bias, const float* expert_bias, const void* W1,
+                              const void* W3, const void* W2, const void* W1s, const void* W3s,
+                              const void* W2s, void* y, int32_t* topk_idx, float* topk_prob,
+                              int32_t* tokens_per_expert, void* ws, size_t ws_bytes,
+                              moe_stream_t stream);
+
+/*
  * moe_permute without a workspace argument.  This entry point is not a step
  * of the MoE method (the pages have no counterpart); it exists for callers
  * that cannot give the library any device memory beyond their inputs and
@@ -226,6 +269,15 @@ moe_status moe_check(void* ws, moe_stream_t stream, int32_t* info);
  * MOE_ERR_TIMEOUT and the CUDA context remains usable. */
 moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_cycles,
                                      moe_stream_t stream);
+
+/* Measurement probe (not a step of the method): enqueues a kernel of pure
+ * fp32 FMA chains (4 CTAs of 256 threads per SM; per thread `iters` > 0
+ * rounds of 128 FMAs in 8 independent chains) and returns in *flops (host) the
+ * floating-point operations it performs; the caller times it with events on
+ * `stream`.  `out` is a device buffer of 4 * SM-count floats that is written
+ * only if the chains produce NaN (never, for these constants).  It gives the
+ * FP32 FMA-pipe rate that bounds the fp32 router GEMM. */
+moe_status moe_probe_fp32_fma(int64_t iters, float* out, double* flops, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

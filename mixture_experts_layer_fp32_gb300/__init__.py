@@ -16,11 +16,14 @@ from ._binding import (  # noqa: F401
     Buffers,
     act_dtype,
     alloc_workspace,
+    alloc_workspace_shared,
     capacity,
     check,
     combine,
+    combine_shared,
     config,
     forward,
+    forward_shared,
     grouped_fc1,
     grouped_fc2,
     grouped_mlp,
@@ -28,7 +31,10 @@ from ._binding import (  # noqa: F401
     max_rows,
     permute,
     permute_noalloc,
+    probe_fp32_fma,
     route,
     selftest_wait_timeout,
+    shared_expert,
     workspace_size,
+    workspace_size_shared,
 )

@@ -24,7 +24,9 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_capacity",
            "moe_workspace_size", "moe_max_rows", "moe_route", "moe_permute", "moe_grouped_mlp",
            "moe_grouped_fc1", "moe_grouped_fc2", "moe_combine", "moe_forward", "moe_check",
-           "moe_permute_noalloc", "moe_selftest_wait_timeout"]
+           "moe_permute_noalloc", "moe_selftest_wait_timeout", "moe_shared_expert",
+           "moe_combine_shared", "moe_workspace_size_shared", "moe_forward_shared",
+           "moe_probe_fp32_fma"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -73,6 +75,12 @@ def lib():
             "moe_check": ([vp, vp, ctypes.POINTER(i32)], i32),
             "moe_permute_noalloc": ([cfgp, vp, vp, vp, vp, vp, vp, vp], i32),
             "moe_selftest_wait_timeout": ([vp, sz, i64, vp], i32),
+            "moe_shared_expert": ([cfgp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_combine_shared": ([cfgp, vp, vp, vp, vp, vp, vp], i32),
+            "moe_workspace_size_shared": ([cfgp, i32, ctypes.POINTER(sz)], i32),
+            "moe_forward_shared": ([cfgp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                    vp, vp, sz, vp], i32),
+            "moe_probe_fp32_fma": ([i64, vp, ctypes.POINTER(ctypes.c_double), vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -193,6 +201,50 @@ def forward(cfg, x, Wg, gate_bias, expert_bias, W1, W3, W2, y, ws, topk_idx=None
     _check(lib().moe_forward(ctypes.byref(cfg), _p(x), _p(Wg), _p(gate_bias), _p(expert_bias),
                              _p(W1), _p(W3), _p(W2), _p(y), _p(topk_idx), _p(topk_prob),
                              _p(tokens_per_expert), w, wb, _stream()), "moe_forward")
+
+
+def workspace_size_shared(cfg, fs):
+    v = ctypes.c_size_t()
+    _check(lib().moe_workspace_size_shared(ctypes.byref(cfg), int(fs), ctypes.byref(v)),
+           "moe_workspace_size_shared")
+    return v.value
+
+
+def alloc_workspace_shared(cfg, fs, device="cuda"):
+    """Zero-filled workspace for forward_shared (moe_workspace_size_shared bytes)."""
+    return torch.zeros(workspace_size_shared(cfg, fs), dtype=torch.uint8, device=device)
+
+
+def shared_expert(cfg, fs, x, W1s, W3s, W2s, h_mid_s, y_shared, ws):
+    w, wb = _ws(ws)
+    _check(lib().moe_shared_expert(ctypes.byref(cfg), int(fs), _p(x), _p(W1s), _p(W3s), _p(W2s),
+                                   _p(h_mid_s), _p(y_shared), w, wb, _stream()),
+           "moe_shared_expert")
+
+
+def combine_shared(cfg, y_perm, row_map, topk_prob, y_shared, y):
+    _check(lib().moe_combine_shared(ctypes.byref(cfg), _p(y_perm), _p(row_map), _p(topk_prob),
+                                    _p(y_shared), _p(y), _stream()), "moe_combine_shared")
+
+
+def forward_shared(cfg, fs, x, Wg, gate_bias, expert_bias, W1, W3, W2, W1s, W3s, W2s, y, ws,
+                   topk_idx=None, topk_prob=None, tokens_per_expert=None):
+    w, wb = _ws(ws)
+    _check(lib().moe_forward_shared(ctypes.byref(cfg), int(fs), _p(x), _p(Wg), _p(gate_bias),
+                                    _p(expert_bias), _p(W1), _p(W3), _p(W2), _p(W1s), _p(W3s),
+                                    _p(W2s), _p(y), _p(topk_idx), _p(topk_prob),
+                                    _p(tokens_per_expert), w, wb, _stream()),
+           "moe_forward_shared")
+
+
+def probe_fp32_fma(iters, out):
+    """Enqueue the FP32 FMA-rate probe; returns the flops it performs (time it
+    with CUDA events on the current stream).  `out`: float32 device buffer of
+    4 * SM-count elements."""
+    flops = ctypes.c_double()
+    _check(lib().moe_probe_fp32_fma(int(iters), _p(out), ctypes.byref(flops), _stream()),
+           "moe_probe_fp32_fma")
+    return flops.value
 
 
 def selftest_wait_timeout(ws, limit_cycles):

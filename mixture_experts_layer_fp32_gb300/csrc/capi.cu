@@ -5,6 +5,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -129,10 +131,32 @@ int64_t capacity_of(const moe_config& c) {
   return cap;
 }
 
-moe_status check_ws(const moe_config& c, const void* ws, size_t ws_bytes) {
+moe_status check_ws(const moe_config& c, const void* ws, size_t ws_bytes, size_t need_bytes = 0) {
   if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 16 != 0) return MOE_ERR_INVALID_ARG;
-  if (ws_bytes < make_layout(c).total) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < (need_bytes ? need_bytes : make_layout(c).total)) return MOE_ERR_WORKSPACE;
   return MOE_OK;
+}
+
+// The shared expert's width: positive, and a multiple of the GEMM's column
+// granularity (8 for the fp32 path, 128 for the tensor-core path).
+moe_status validate_fs(const moe_config& c, int32_t fs) {
+  if (fs <= 0) return MOE_ERR_INVALID_ARG;
+  if (fs % 8 != 0 || (c.dtype == MOE_BF16 && fs % 128 != 0)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// moe_forward_shared's workspace: the routed layout, then h_mid_s [T,fs]
+// (dtype) and y_shared [T,h] fp32.
+struct SharedLayout {
+  size_t h_mid_s, y_shared, total;
+};
+SharedLayout make_shared_layout(const moe_config& c, int32_t fs) {
+  SharedLayout S;
+  const size_t T = c.num_tokens, el = c.dtype == MOE_F32 ? 4 : 2;
+  S.h_mid_s = make_layout(c).total;
+  S.y_shared = align_up(S.h_mid_s + T * static_cast<size_t>(fs) * el);
+  S.total = align_up(S.y_shared + T * static_cast<size_t>(c.hidden) * 4);
+  return S;
 }
 
 template <typename T>
@@ -140,7 +164,6 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
-size_t elt(const moe_config& c) { return c.dtype == MOE_F32 ? 4 : 2; }
 
 // ---- stage bodies (arguments already validated) ----
 
@@ -227,6 +250,79 @@ moe_status do_fc2(const moe_config& c, const void* h_mid, const int32_t* offsets
   else
     MOE_CUDA(launch_tc_fc2(c.num_experts, c.hidden, c.ffn_hidden, rows, h_mid, offsets, W2, y_perm,
                            err, s));
+  return MOE_OK;
+}
+
+// Shared expert: the grouped MLP kernels as one dense group of all T rows of x.
+moe_status do_shared(const moe_config& c, int32_t fs, const void* x, const void* W1s,
+                     const void* W3s, const void* W2s, void* h_mid_s, float* y_shared, int* err,
+                     cudaStream_t s) {
+  const int64_t T = c.num_tokens;
+  if (c.dtype == MOE_F32) {
+    MOE_CUDA(launch_simt_fc1(1, c.hidden, fs, T, static_cast<const float*>(x), nullptr,
+                             static_cast<const float*>(W1s), static_cast<const float*>(W3s),
+                             static_cast<float*>(h_mid_s), err, s));
+    MOE_CUDA(launch_simt_fc2(1, c.hidden, fs, T, static_cast<const float*>(h_mid_s), nullptr,
+                             static_cast<const float*>(W2s), y_shared, err, s));
+  } else {
+    MOE_CUDA(launch_tc_fc1(1, c.hidden, fs, T, x, nullptr, W1s, W3s, h_mid_s, err, s));
+    MOE_CUDA(launch_tc_fc2(1, c.hidden, fs, T, h_mid_s, nullptr, W2s, y_shared, err, s));
+  }
+  return MOE_OK;
+}
+
+// Buffers of the routed path inside the workspace (or the caller's).
+struct Routed {
+  int32_t* idx;
+  float* prob;
+  int32_t* tpe;
+  int32_t* row_map;
+  float* y_perm;
+};
+
+// route -> drop -> permute -> fc1 -> fc2 of moe_forward, on `stream`.
+moe_status routed_path(const moe_config& c, const void* x, const float* Wg,
+                       const float* gate_bias, const float* expert_bias, const void* W1,
+                       const void* W3, const void* W2, int32_t* topk_idx, float* topk_prob,
+                       int32_t* tokens_per_expert, void* ws, cudaStream_t stream, Routed* out) {
+  const Layout L = make_layout(c);
+  int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
+  float* prob = topk_prob ? topk_prob : at<float>(ws, L.topk_prob);
+  int32_t* tpe = tokens_per_expert ? tokens_per_expert : at<int32_t>(ws, L.tpe);
+  uint8_t* keep = at<uint8_t>(ws, L.keep);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* row_map = at<int32_t>(ws, L.row_map);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* h_mid = at<void>(ws, L.h_mid);
+  float* y_perm = at<float>(ws, L.y_perm);
+  MOE_TRY(do_route(c, x, Wg, gate_bias, expert_bias, idx, prob, keep, tpe, nullptr, ws, stream));
+  MOE_TRY(do_permute(c, x, idx, keep, x_perm, row_map, offsets, ws, stream));
+  MOE_TRY(do_fc1(c, x_perm, offsets, W1, W3, h_mid, ws, stream));
+  MOE_TRY(do_fc2(c, h_mid, offsets, W2, y_perm, ws, stream));
+  *out = Routed{idx, prob, tpe, row_map, y_perm};
+  return MOE_OK;
+}
+
+// The library's second stream per device (for the shared expert) and the
+// fork / join events; created on first use, kept until exit.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+moe_status side_stream(SideStream** out) {
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  SideStream& ss = g_side[dev];
+  if (ss.stream == nullptr) {
+    MOE_CUDA(cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming));
+    MOE_CUDA(cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming));
+    MOE_CUDA(cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking));
+  }
+  *out = &ss;
   return MOE_OK;
 }
 
@@ -358,8 +454,104 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
   MOE_TRY(need(row_map, T * k, 4));
   MOE_TRY(need(topk_prob, T * k, 4));
   MOE_TRY(need(y, T * c.hidden, 16));
-  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, y_perm, row_map, topk_prob, y,
-                          stream));
+  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, y_perm, row_map, topk_prob,
+                          nullptr, y, stream));
+  return MOE_OK;
+}
+
+moe_status moe_combine_shared(const moe_config* cfg, const float* y_perm, const int32_t* row_map,
+                              const float* topk_prob, const float* y_shared, void* y,
+                              moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  const size_t T = c.num_tokens, k = c.topk;
+  MOE_TRY(need(y_perm, T * k * c.hidden, 16));
+  MOE_TRY(need(row_map, T * k, 4));
+  MOE_TRY(need(topk_prob, T * k, 4));
+  MOE_TRY(optional(y_shared, 16));
+  MOE_TRY(need(y, T * c.hidden, 16));
+  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, y_perm, row_map, topk_prob,
+                          y_shared, y, stream));
+  return MOE_OK;
+}
+
+moe_status moe_shared_expert(const moe_config* cfg, int32_t fs, const void* x, const void* W1s,
+                             const void* W3s, const void* W2s, void* h_mid_s, float* y_shared,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_fs(c, fs));
+  const size_t T = c.num_tokens, h = c.hidden;
+  MOE_TRY(need(x, T * h, 16));
+  MOE_TRY(need(W1s, h * fs, 16));
+  MOE_TRY(need(W3s, h * fs, 16));
+  MOE_TRY(need(W2s, h * fs, 16));
+  MOE_TRY(need(h_mid_s, T * fs, 16));
+  MOE_TRY(need(y_shared, T * h, 16));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  return do_shared(c, fs, x, W1s, W3s, W2s, h_mid_s, y_shared,
+                   at<int>(ws, make_layout(c).err), stream);
+}
+
+moe_status moe_workspace_size_shared(const moe_config* cfg, int32_t fs, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  MOE_TRY(validate_fs(*cfg, fs));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = make_shared_layout(*cfg, fs).total;
+  return MOE_OK;
+}
+
+moe_status moe_forward_shared(const moe_config* cfg, int32_t fs, const void* x, const float* Wg,
+                              const float* gate_bias, const float* expert_bias, const void* W1,
+                              const void* W3, const void* W2, const void* W1s, const void* W3s,
+                              const void* W2s, void* y, int32_t* topk_idx, float* topk_prob,
+                              int32_t* tokens_per_expert, void* ws, size_t ws_bytes,
+                              moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_fs(c, fs));
+  const size_t T = c.num_tokens, E = c.num_experts, h = c.hidden;
+  const size_t wsz = E * h * c.ffn_hidden;
+  MOE_TRY(need(x, T * h, 16));
+  MOE_TRY(need(Wg, h * E, 4));
+  MOE_TRY(optional(gate_bias, 4));
+  MOE_TRY(optional(expert_bias, 4));
+  MOE_TRY(need(W1, wsz, 16));
+  MOE_TRY(need(W3, wsz, 16));
+  MOE_TRY(need(W2, wsz, 16));
+  MOE_TRY(need(W1s, h * fs, 16));
+  MOE_TRY(need(W3s, h * fs, 16));
+  MOE_TRY(need(W2s, h * fs, 16));
+  MOE_TRY(need(y, T * h, 16));
+  MOE_TRY(optional(topk_idx, 4));
+  MOE_TRY(optional(topk_prob, 4));
+  MOE_TRY(optional(tokens_per_expert, 4));
+  const SharedLayout S = make_shared_layout(c, fs);
+  MOE_TRY(check_ws(c, ws, ws_bytes, S.total));
+  void* h_mid_s = at<void>(ws, S.h_mid_s);
+  float* y_shared = at<float>(ws, S.y_shared);
+  int* err = at<int>(ws, make_layout(c).err);
+
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream* side = nullptr;
+  MOE_TRY(side_stream(&side));
+  // fork: the shared expert on the side stream, after everything already on `stream`
+  MOE_CUDA(cudaEventRecord(side->fork, stream));
+  MOE_CUDA(cudaStreamWaitEvent(side->stream, side->fork, 0));
+  const moe_status st_side = do_shared(c, fs, x, W1s, W3s, W2s, h_mid_s, y_shared, err,
+                                       side->stream);
+  const cudaError_t rec = cudaEventRecord(side->join, side->stream);
+  Routed r{};
+  const moe_status st = routed_path(c, x, Wg, gate_bias, expert_bias, W1, W3, W2, topk_idx,
+                                    topk_prob, tokens_per_expert, ws, stream, &r);
+  // join even after a failure, so that `stream` never stays forked (a capture
+  // in progress would be invalidated)
+  const cudaError_t wait = rec == cudaSuccess ? cudaStreamWaitEvent(stream, side->join, 0) : rec;
+  MOE_TRY(st_side);
+  MOE_TRY(st);
+  MOE_CUDA(wait);
+  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm, r.row_map, r.prob,
+                          y_shared, y, stream));
   return MOE_OK;
 }
 
@@ -370,7 +562,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
                        size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
-  const size_t T = c.num_tokens, E = c.num_experts, k = c.topk, h = c.hidden;
+  const size_t T = c.num_tokens, E = c.num_experts, h = c.hidden;
   const size_t wsz = E * h * c.ffn_hidden;
   MOE_TRY(need(x, T * h, 16));
   MOE_TRY(need(Wg, h * E, 4));
@@ -384,23 +576,11 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
   MOE_TRY(optional(topk_prob, 4));
   MOE_TRY(optional(tokens_per_expert, 4));
   MOE_TRY(check_ws(c, ws, ws_bytes));
-  const Layout L = make_layout(c);
-  int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
-  float* prob = topk_prob ? topk_prob : at<float>(ws, L.topk_prob);
-  int32_t* tpe = tokens_per_expert ? tokens_per_expert : at<int32_t>(ws, L.tpe);
-  uint8_t* keep = at<uint8_t>(ws, L.keep);
-  int32_t* offsets = at<int32_t>(ws, L.offsets);
-  int32_t* row_map = at<int32_t>(ws, L.row_map);
-  void* x_perm = at<void>(ws, L.x_perm);
-  void* h_mid = at<void>(ws, L.h_mid);
-  float* y_perm = at<float>(ws, L.y_perm);
-  (void)elt;
-  MOE_TRY(do_route(c, x, Wg, gate_bias, expert_bias, idx, prob, keep, tpe, nullptr, ws, stream));
-  MOE_TRY(do_permute(c, x, idx, keep, x_perm, row_map, offsets, ws, stream));
-  MOE_TRY(do_fc1(c, x_perm, offsets, W1, W3, h_mid, ws, stream));
-  MOE_TRY(do_fc2(c, h_mid, offsets, W2, y_perm, ws, stream));
-  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, y_perm, row_map, prob, y,
-                          stream));
+  Routed r;
+  MOE_TRY(routed_path(c, x, Wg, gate_bias, expert_bias, W1, W3, W2, topk_idx, topk_prob,
+                      tokens_per_expert, ws, stream, &r));
+  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm, r.row_map, r.prob,
+                          nullptr, y, stream));
   return MOE_OK;
 }
 

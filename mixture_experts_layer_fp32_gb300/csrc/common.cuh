@@ -52,10 +52,13 @@ cudaError_t launch_perm_rank(int64_t npairs, int E, const int32_t* topk_idx, con
                              cudaStream_t s);
 cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, const int32_t* row_map,
                              void* x_perm, cudaStream_t s);
+// y_shared [T, h] fp32 (nullable): the shared expert's output, added last
 cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
-                           const int32_t* row_map, const float* topk_prob, void* y, cudaStream_t s);
+                           const int32_t* row_map, const float* topk_prob, const float* y_shared,
+                           void* y, cudaStream_t s);
 
 // ---- grouped GEMMs ----
+// offsets == nullptr: one dense group (E must be 1) over rows [0, max_rows)
 // fp32 SIMT path (dtype MOE_F32)
 cudaError_t launch_simt_fc1(int E, int h, int f, int64_t max_rows, const float* x_perm,
                             const int32_t* offsets, const float* W1, const float* W3,

@@ -27,7 +27,9 @@ __global__ void __launch_bounds__(SThreads)
   __shared__ __align__(16) float Bs0[SBK][SBN];
   __shared__ __align__(16) float Bs1[SWIGLU ? SBK : 1][SWIGLU ? SBN : 4];
 
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = offsets[e];
+  // no offsets array: one dense group (E = 1) over rows [0, max_rows)
+  for (int e = threadIdx.x; e <= E; e += blockDim.x)
+    off[e] = offsets ? offsets[e] : (e == 0 ? 0 : static_cast<int>(max_rows));
   __syncthreads();
   if (threadIdx.x == 0) {
     bool ok = off[0] == 0;

@@ -5,7 +5,9 @@
 // (TEGroupedMLP / GroupedLinear on that page), with SwiGLU experts:
 //   fc1:  H[r, :] = silu(X[r, :] . W1[e]) * (X[r, :] . W3[e])   (bf16 out)
 //   fc2:  Y[r, :] = H[r, :] . W2[e]                              (fp32 out)
-// for the rows r of expert e, [offsets[e], offsets[e+1]).
+// for the rows r of expert e, [offsets[e], offsets[e+1]).  With no offsets
+// array the launch is one dense group (E = 1) over rows [0, max_rows): the
+// shared expert, applied to every token.
 //
 // Design (one CTA per SM, persistent):
 //  * Output tile 128 rows x 256 fp32 accumulator columns in TMEM.  fc1's
@@ -129,6 +131,13 @@ __device__ __forceinline__ void decode_tile(int tile, const int* tstart, const i
   nt = u / mt;
   m0 = off[e] + (u - nt * mt) * ROWS;
   rend = off[e + 1];
+}
+
+// Expert offsets into shared memory.  Without an offsets array (dense
+// mode, E = 1) the single group is rows [0, max_rows).
+__device__ __forceinline__ void load_offsets(int* off, const TcArgs& args) {
+  for (int e = threadIdx.x; e <= args.E; e += blockDim.x)
+    off[e] = args.offsets ? args.offsets[e] : (e == 0 ? 0 : static_cast<int>(args.max_rows));
 }
 
 // Per-expert tile prefix (tstart[0..E]) from the expert offsets, by warp 0:
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
     ptx::tmem_relinquish();
   }
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = args.offsets[e];
+  load_offsets(off, args);
   __syncthreads();
   if (warp == 0) build_tile_prefix<BM>(off, tstart, E, NT, args.max_rows, args.err, lane);
   ptx::tc_fence_before();
@@ -517,7 +526,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), TMEM_COLS);
     ptx::tmem_relinquish_pair();
   }
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = args.offsets[e];
+  load_offsets(off, args);
   __syncthreads();
   if (warp == 0) build_tile_prefix<PM>(off, tstart, E, NT, args.max_rows, args.err, lane);
   ptx::tc_fence_before();

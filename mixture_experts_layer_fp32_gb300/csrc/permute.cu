@@ -16,7 +16,8 @@
 // Combine, after §2 (combine) of the Megatron Core page and step 8 of §8 of
 // the DeepSpeed page (unpermute, weight by the router probabilities):
 //   combine_kernel    per token: gather its k rows, fp32 weighted sum in
-//                     slot order, one rounding to the output dtype
+//                     slot order, plus the shared expert's row when there is
+//                     one, one rounding to the output dtype
 #include "common.cuh"
 
 namespace moe {
@@ -214,7 +215,7 @@ template <typename OT>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(int T, int h, int k, const float* __restrict__ y_perm,
                    const int32_t* __restrict__ row_map, const float* __restrict__ topk_prob,
-                   OT* __restrict__ y) {
+                   const float* __restrict__ y_shared, OT* __restrict__ y) {
   const int h4 = h >> 2;
   const int64_t max_rows = static_cast<int64_t>(T) * k;
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
@@ -236,6 +237,13 @@ __global__ void __launch_bounds__(kCombineThreads)
         acc.y = fmaf(p[j], a.y, acc.y);
         acc.z = fmaf(p[j], a.z, acc.z);
         acc.w = fmaf(p[j], a.w, acc.w);
+      }
+      if (y_shared) {  // the shared expert's output, added after the routed sum
+        const float4 b = __ldcs(reinterpret_cast<const float4*>(y_shared + (int64_t)t * h) + v);
+        acc.x += b.x;
+        acc.y += b.y;
+        acc.z += b.z;
+        acc.w += b.w;
       }
       Out4<OT>::store(y + (int64_t)t * h + 4 * v, acc);
     }
@@ -284,15 +292,16 @@ cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, cons
 }
 
 cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
-                           const int32_t* row_map, const float* topk_prob, void* y, cudaStream_t s) {
+                           const int32_t* row_map, const float* topk_prob, const float* y_shared,
+                           void* y, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int grid = grid_for_tokens(T, 8);
   if (dtype == MOE_F32)
     combine_kernel<float><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob,
-                                                           static_cast<float*>(y));
+                                                           y_shared, static_cast<float*>(y));
   else
     combine_kernel<__nv_bfloat16><<<grid, kCombineThreads, 0, s>>>(
-        T, h, k, y_perm, row_map, topk_prob, static_cast<__nv_bfloat16*>(y));
+        T, h, k, y_perm, row_map, topk_prob, y_shared, static_cast<__nv_bfloat16*>(y));
   return cudaGetLastError();
 }
 

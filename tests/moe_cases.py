@@ -100,11 +100,14 @@ def make_case(w, device="cpu", nthreads=0):
 
 
 def oracle_forward(w, inp, nthreads=0, want_h_mid=True):
+    shared = {}
+    if w.shared_f > 0:
+        shared = {n: np_view(inp[n]) for n in ("W1s", "W3s", "W2s")}
     return oracle.forward(np_view(inp["x"]), np_view(inp["Wg"]), np_view(inp["W1"]),
                           np_view(inp["W3"]), np_view(inp["W2"]), w.k, w.score,
                           np_view(inp["gate_bias"]), np_view(inp["expert_bias"]),
                           w.capacity_factor, w.min_capacity, w.drop_policy, nthreads,
-                          want_h_mid=want_h_mid)
+                          want_h_mid=want_h_mid, **shared)
 
 
 def gpu_config(w):
@@ -128,7 +131,14 @@ def gpu_stages(w, dinp, with_routing_map=True):
     moe.permute(cfg, dinp["x"], b.topk_idx, b.keep, b.x_perm, b.row_map, b.expert_offsets, b.ws)
     moe.grouped_fc1(cfg, b.x_perm, b.expert_offsets, dinp["W1"], dinp["W3"], b.h_mid, b.ws)
     moe.grouped_fc2(cfg, b.h_mid, b.expert_offsets, dinp["W2"], b.y_perm, b.ws)
-    moe.combine(cfg, b.y_perm, b.row_map, b.topk_prob, b.y)
+    if w.shared_f > 0:
+        b.h_mid_s = torch.empty((w.T, w.shared_f), dtype=moe.act_dtype(cfg), device="cuda")
+        b.y_shared = torch.empty((w.T, w.h), dtype=torch.float32, device="cuda")
+        moe.shared_expert(cfg, w.shared_f, dinp["x"], dinp["W1s"], dinp["W3s"], dinp["W2s"],
+                          b.h_mid_s, b.y_shared, b.ws)
+        moe.combine_shared(cfg, b.y_perm, b.row_map, b.topk_prob, b.y_shared, b.y)
+    else:
+        moe.combine(cfg, b.y_perm, b.row_map, b.topk_prob, b.y)
     moe.check(b.ws)
     return b
 
@@ -141,8 +151,14 @@ def gpu_forward(w, dinp):
     idx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
     prob = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
     tpe = torch.empty((w.E,), dtype=torch.int32, device="cuda")
-    moe.forward(cfg, dinp["x"], dinp["Wg"], dinp["gate_bias"], dinp["expert_bias"], dinp["W1"],
-                dinp["W3"], dinp["W2"], y, ws, idx, prob, tpe)
+    if w.shared_f > 0:
+        ws = moe.alloc_workspace_shared(cfg, w.shared_f)
+        moe.forward_shared(cfg, w.shared_f, dinp["x"], dinp["Wg"], dinp["gate_bias"],
+                           dinp["expert_bias"], dinp["W1"], dinp["W3"], dinp["W2"], dinp["W1s"],
+                           dinp["W3s"], dinp["W2s"], y, ws, idx, prob, tpe)
+    else:
+        moe.forward(cfg, dinp["x"], dinp["Wg"], dinp["gate_bias"], dinp["expert_bias"],
+                    dinp["W1"], dinp["W3"], dinp["W2"], y, ws, idx, prob, tpe)
     moe.check(ws)
     return y, idx, prob, tpe
 
@@ -234,4 +250,8 @@ def compare_all(w, inp, ref, b):
     assert_close("h_mid", to_np(b.h_mid[:R]), ref["h_mid"],
                  "bf16_stored" if w.dtype == "bf16" else w.dtype)
     assert_close("y_perm", to_np(b.y_perm[:R]), ref["y_perm"], w.dtype)
+    if w.shared_f > 0:
+        assert_close("h_mid_s", to_np(b.h_mid_s), ref["h_mid_s"],
+                     "bf16_stored" if w.dtype == "bf16" else w.dtype)
+        assert_close("y_shared", to_np(b.y_shared), ref["y_shared"], w.dtype)
     assert_close("y", to_np(b.y), ref["y"], w.dtype)

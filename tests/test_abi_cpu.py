@@ -150,3 +150,29 @@ def test_selftest_wait_timeout_host_checks(moe):
     assert lib.moe_selftest_wait_timeout(FAKE, 100, 1000, None) == INVALID     # too small for the error word
     assert lib.moe_selftest_wait_timeout(FAKE, 4096, 0, None) == INVALID
     assert lib.moe_selftest_wait_timeout(MISALIGNED, 4096, 1000, None) == INVALID
+
+
+def test_shared_expert_host_checks(moe):
+    lib = moe.lib()
+    cfg = moe.config(T=128, h=4096, E=8, k=2, f=1536)
+    size = ctypes.c_size_t()
+    assert lib.moe_workspace_size_shared(ctypes.byref(cfg), 0, ctypes.byref(size)) == INVALID
+    assert lib.moe_workspace_size_shared(ctypes.byref(cfg), 200, ctypes.byref(size)) == UNSUPPORTED
+    assert lib.moe_workspace_size_shared(ctypes.byref(cfg), 256, ctypes.byref(size)) == OK
+    # routed workspace + h_mid_s [T,256] bf16 + y_shared [T,h] fp32
+    assert size.value >= moe.workspace_size(cfg) + 128 * 256 * 2 + 128 * 4096 * 4
+    f32 = moe.config(T=16, h=136, E=4, k=2, f=200, dtype="f32")
+    assert lib.moe_workspace_size_shared(ctypes.byref(f32), 72, ctypes.byref(size)) == OK
+    need = moe.workspace_size(cfg)
+    # moe_shared_expert: x missing, then a misaligned W2s
+    assert lib.moe_shared_expert(ctypes.byref(cfg), 256, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                 need, None) == INVALID
+    assert lib.moe_shared_expert(ctypes.byref(cfg), 256, FAKE, FAKE, FAKE, MISALIGNED, FAKE, FAKE,
+                                 FAKE, need, None) == INVALID
+    # moe_forward_shared: the routed workspace size is too small for it
+    assert lib.moe_forward_shared(ctypes.byref(cfg), 256, FAKE, FAKE, None, None, FAKE, FAKE, FAKE,
+                                  FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, need,
+                                  None) == WORKSPACE
+    # moe_combine_shared: y_shared is optional but must be aligned
+    assert lib.moe_combine_shared(ctypes.byref(cfg), FAKE, FAKE, FAKE, MISALIGNED, FAKE,
+                                  None) == INVALID

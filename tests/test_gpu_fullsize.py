@@ -1,4 +1,4 @@
-"""Parity at the five workloads' full sizes, in the launch configuration the
+"""Parity at every workload's full size, in the launch configuration the
 benchmark times (the same C-ABI stage calls and kernels).
 
 Checked in full: routing (topk_idx, keep, tokens_per_expert bit-exact,
@@ -21,7 +21,8 @@ from moe_cases import (assert_close, assert_equal, assert_probs, condition_input
 
 pytestmark = pytest.mark.gpu
 
-MAX_EXPERTS = {"tiny_fp32": 8, "mixtral": 8, "dsv3": 48, "qwen3": 48, "switch": 32}
+MAX_EXPERTS = {"tiny_fp32": 8, "mixtral": 8, "dsv3": 48, "dsv3_shared": 48, "qwen3": 48,
+               "switch": 32}
 MAX_TOKENS = 32
 
 
@@ -107,7 +108,15 @@ def test_sampled_outputs_full(full):
     for n, (i, j) in enumerate(pairs):
         local_map[i, j] = n
     y_ref = oracle.combine(y_rows, local_map, r["topk_prob"][toks])
-    assert_close("y", to_np(b.y[torch.from_numpy(toks).to(b.y.device)]), y_ref, w.dtype)
+    tsel = torch.from_numpy(toks).to(b.y.device)
+    if w.shared_f > 0:
+        ys, hs = oracle.shared_expert(np_view(x_cpu), *(np_view(inp[n].cpu()) for n in
+                                                       ("W1s", "W3s", "W2s")), want_h_mid=True)
+        assert_close("h_mid_s", to_np(b.h_mid_s[tsel]), hs,
+                     "bf16_stored" if w.dtype == "bf16" else w.dtype)
+        assert_close("y_shared", to_np(b.y_shared[tsel]), ys, w.dtype)
+        y_ref = y_ref + ys
+    assert_close("y", to_np(b.y[tsel]), y_ref, w.dtype)
     if w.capacity_factor > 0:
         all_dropped = (r["keep"][toks] == 0).all(axis=1)
         assert np.all(y_ref[all_dropped] == 0)
