@@ -21,7 +21,7 @@ _LIBDIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_LIBDIR, "libmoe_oracle.so")
 _lib = None
 
-SCORES = {"softmax_post": 0, "softmax_pre": 1, "sigmoid": 2}
+SCORES = {"softmax_post": 0, "softmax_pre": 1, "sigmoid": 2, "sqrtsoftplus": 3}
 POLICIES = {"probs": 0, "position": 1}
 
 
@@ -45,7 +45,7 @@ def _load():
         L = ctypes.CDLL(_LIB_PATH)
         i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
         L.oracle_router_logits.argtypes = [i64, i32, i32, vp, i32, vp, vp, vp, i32]
-        L.oracle_topk_scores.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp, i32]
+        L.oracle_topk_scores.argtypes = [i64, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i32]
         L.oracle_capacity.argtypes = [i64, i32, i32, dbl, i64]
         L.oracle_capacity.restype = i64
         L.oracle_capacity_drop.argtypes = [i64, i32, i32, i64, i32, vp, vp, vp, vp]
@@ -98,15 +98,21 @@ def router_logits(x, Wg, gate_bias=None, nthreads=0):
     return out
 
 
-def topk_scores(logits, k, score, expert_bias=None, nthreads=0):
+def topk_scores(logits, k, score, expert_bias=None, nthreads=0, num_groups=0, group_topk=0):
+    """Scores and top-k of [MC] §5; num_groups > 1 turns on group-limited
+    top-k (group_topk of num_groups groups kept)."""
     logits = _c(logits, np.float32)
     expert_bias = _c(expert_bias, np.float32)
     T, E = logits.shape
+    if num_groups > 1:
+        assert E % num_groups == 0 and 1 <= group_topk <= min(num_groups, k)
+        assert k <= group_topk * (E // num_groups)
     idx = np.empty((T, k), np.int32)
     prob = np.empty((T, k), np.float32)
     margin = np.empty((T,), np.float32)
-    _load().oracle_topk_scores(T, E, k, SCORES[score], _ptr(logits), _ptr(expert_bias),
-                               _ptr(idx), _ptr(prob), _ptr(margin), nthreads)
+    _load().oracle_topk_scores(T, E, k, SCORES[score], int(num_groups), int(group_topk),
+                               _ptr(logits), _ptr(expert_bias), _ptr(idx), _ptr(prob),
+                               _ptr(margin), nthreads)
     return idx, prob, margin
 
 
@@ -182,12 +188,13 @@ def forward_dense(x, topk_idx, topk_prob, keep, W1, W3, W2, nthreads=0):
 
 
 def route(x, Wg, k, score, gate_bias=None, expert_bias=None, capacity_factor=0.0,
-          min_capacity=0, drop_policy="probs", nthreads=0):
+          min_capacity=0, drop_policy="probs", nthreads=0, num_groups=0, group_topk=0):
     """Router + optional capacity drop.  Returns a dict of numpy arrays."""
     T = x.shape[0]
     E = Wg.shape[1]
     logits = router_logits(x, Wg, gate_bias, nthreads)
-    idx, prob, margin = topk_scores(logits, k, score, expert_bias, nthreads)
+    idx, prob, margin = topk_scores(logits, k, score, expert_bias, nthreads, num_groups,
+                                    group_topk)
     assigned = np.bincount(idx.reshape(-1), minlength=E).astype(np.int32)
     cap = capacity(T, E, k, capacity_factor, min_capacity)
     prob_final, keep, kept = capacity_drop(idx, prob, E, cap, drop_policy)
@@ -212,12 +219,12 @@ def shared_expert(x, W1s, W3s, W2s, want_h_mid=False, nthreads=0):
 
 def forward(x, Wg, W1, W3, W2, k, score, gate_bias=None, expert_bias=None,
             capacity_factor=0.0, min_capacity=0, drop_policy="probs", nthreads=0,
-            want_h_mid=False, W1s=None, W3s=None, W2s=None):
+            want_h_mid=False, W1s=None, W3s=None, W2s=None, num_groups=0, group_topk=0):
     """The whole layer: route -> drop -> permute -> SwiGLU experts -> combine,
     plus the shared expert's output when W1s/W3s/W2s are given (added to the
     routed sum in double: y = sum_j p_j Y_j + Y_shared)."""
     r = route(x, Wg, k, score, gate_bias, expert_bias, capacity_factor, min_capacity,
-              drop_policy, nthreads)
+              drop_policy, nthreads, num_groups, group_topk)
     E = Wg.shape[1]
     offsets, row_map, row_token = permute(r["topk_idx"], r["keep"], E)
     row_expert = np.repeat(np.arange(E, dtype=np.int32), np.diff(offsets))

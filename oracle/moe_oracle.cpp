@@ -30,7 +30,7 @@
 namespace {
 
 enum { DT_F32 = 0, DT_BF16 = 1 };
-enum { SCORE_SOFTMAX_POST = 0, SCORE_SOFTMAX_PRE = 1, SCORE_SIGMOID = 2 };
+enum { SCORE_SOFTMAX_POST = 0, SCORE_SOFTMAX_PRE = 1, SCORE_SIGMOID = 2, SCORE_SQRTSOFTPLUS = 3 };
 enum { DROP_PROBS = 0, DROP_POSITION = 1 };
 
 // Exact value of element i of a tensor stored as fp32 or as bf16 bits.
@@ -79,7 +79,7 @@ void topk_desc(const float* v, int n, int k, int32_t* out_idx) {
 
 extern "C" {
 
-int oracle_abi_version(void) { return 1; }
+int oracle_abi_version(void) { return 2; }
 
 // [MC] §3 Gating: logits = x . Wg (+ bias) with the router math in fp32.
 // The oracle forms the exact sum in double over the exact fp32 values of x
@@ -105,45 +105,91 @@ void oracle_router_logits(int64_t T, int h, int E, const void* x, int x_dtype,
 }
 
 // [MC] §5 Score function (topk_routing_with_score_function):
-//  SOFTMAX_POST: scores, idx = topk(logits); probs = softmax(scores) over the k.
-//  SOFTMAX_PRE : scores = softmax(logits) over all E; probs, idx = topk(scores).
-//  SIGMOID     : s = sigmoid(logits); idx = topk(s + expert_bias) (the bias
-//                only chooses); probs = s[idx] / (sum s[idx] + 1e-20).
+//  SOFTMAX_POST : scores, idx = topk(logits); probs = softmax(scores) over the k.
+//  SOFTMAX_PRE  : scores = softmax(logits) over all E; probs, idx = topk(scores).
+//  SIGMOID      : s = sigmoid(logits); idx = topk(s + expert_bias) (the bias
+//                 only chooses); probs = s[idx] / (sum s[idx] + 1e-20).
+//  SQRTSOFTPLUS : s = sqrt(softplus(logits)), softplus(l) = log(1 + e^l);
+//                 choice and weights as for SIGMOID.
 // Selection is done on fp32 values (the router dtype of [MC] §3); each
 // score is formed in double and rounded once to fp32 before it is compared.
+//
+// Group-limited top-k (the page passes num_groups and group_topk to
+// compute_topk but does not print its body).  Reading, the group-limited
+// routing of DeepSeek-V3: the E experts form num_groups contiguous groups
+// of E/num_groups; a group's score is the sum of its m = k/group_topk largest
+// selection scores (in double, largest first, rounded once to fp32); the
+// group_topk groups with the largest scores are kept (equal scores: lower
+// group index first) and the top-k is taken over the kept groups' experts
+// only.  num_groups <= 1 switches grouping off.
+//
 // Outputs: topk_idx [T,k] (slot order = selection score, descending),
-// topk_prob [T,k] fp32, margin [T] = (k-th - (k+1)-th) selection score
-// (+inf when k == E) -- used by the input conditioner, not by the method.
-void oracle_topk_scores(int64_t T, int E, int k, int score, const float* logits,
-                        const float* expert_bias, int32_t* topk_idx, float* topk_prob,
-                        float* margin, int nthreads) {
+// topk_prob [T,k] fp32, margin [T] = the smaller of (k-th - (k+1)-th
+// selection score among the eligible experts) and, with groups,
+// (group_topk-th - next group score); +inf where there is no next one.
+// The margin is used by the input conditioner, not by the method.
+void oracle_topk_scores(int64_t T, int E, int k, int score, int num_groups, int group_topk,
+                        const float* logits, const float* expert_bias, int32_t* topk_idx,
+                        float* topk_prob, float* margin, int nthreads) {
+  const double inf = std::numeric_limits<double>::infinity();
   parallel_for(T, nthreads, [&](int64_t t) {
     const float* l = logits + t * E;
     std::vector<float> s(E), sel(E);
     if (score == SCORE_SOFTMAX_POST) {
       for (int e = 0; e < E; ++e) s[e] = sel[e] = l[e];
     } else if (score == SCORE_SOFTMAX_PRE) {
-      double m = -std::numeric_limits<double>::infinity();
+      double m = -inf;
       for (int e = 0; e < E; ++e) m = std::max(m, (double)l[e]);
       double z = 0.0;
       for (int e = 0; e < E; ++e) z += std::exp((double)l[e] - m);
       for (int e = 0; e < E; ++e) s[e] = sel[e] = (float)(std::exp((double)l[e] - m) / z);
     } else {
       for (int e = 0; e < E; ++e) {
-        s[e] = (float)(1.0 / (1.0 + std::exp(-(double)l[e])));
+        const double x = (double)l[e];
+        if (score == SCORE_SIGMOID) {
+          s[e] = (float)(1.0 / (1.0 + std::exp(-x)));
+        } else {
+          // log(1 + e^x), written so that e^x cannot overflow
+          const double softplus = std::max(x, 0.0) + std::log1p(std::exp(-std::fabs(x)));
+          s[e] = (float)std::sqrt(softplus);
+        }
         // scores_for_routing = scores + expert_bias, an fp32 addition
         sel[e] = expert_bias ? (float)(s[e] + expert_bias[e]) : s[e];
       }
     }
+    // experts a token may choose (all, or those of the kept groups)
+    std::vector<float> cand(sel);
+    double group_margin = inf;
+    if (num_groups > 1) {
+      const int per = E / num_groups, m = k / group_topk;
+      std::vector<float> gscore(num_groups);
+      std::vector<int32_t> top(m);
+      for (int g = 0; g < num_groups; ++g) {
+        topk_desc(sel.data() + (int64_t)g * per, per, m, top.data());
+        double sum = 0.0;
+        for (int j = 0; j < m; ++j) sum += (double)sel[g * per + top[j]];
+        gscore[g] = (float)sum;
+      }
+      const int gk = std::min(num_groups, group_topk + 1);
+      std::vector<int32_t> gidx(gk);
+      topk_desc(gscore.data(), num_groups, gk, gidx.data());
+      std::vector<char> kept(num_groups, 0);
+      for (int j = 0; j < group_topk; ++j) kept[gidx[j]] = 1;
+      for (int e = 0; e < E; ++e)
+        if (!kept[e / per]) cand[e] = -std::numeric_limits<float>::infinity();
+      if (group_topk < num_groups)
+        group_margin = (double)gscore[gidx[group_topk - 1]] - (double)gscore[gidx[group_topk]];
+    }
     const int kk = std::min(E, k + 1);
     std::vector<int32_t> idx(kk);
-    topk_desc(sel.data(), E, kk, idx.data());
+    topk_desc(cand.data(), E, kk, idx.data());
     int32_t* oi = topk_idx + t * k;
     float* op = topk_prob + t * k;
     for (int j = 0; j < k; ++j) oi[j] = idx[j];
     if (margin) {
-      margin[t] = (k < E) ? (float)((double)sel[idx[k - 1]] - (double)sel[idx[k]])
-                          : std::numeric_limits<float>::infinity();
+      double em = inf;
+      if (k < E && std::isfinite(cand[idx[k]])) em = (double)cand[idx[k - 1]] - (double)cand[idx[k]];
+      margin[t] = (float)std::min(em, group_margin);
     }
     if (score == SCORE_SOFTMAX_POST) {
       double m = (double)s[idx[0]];

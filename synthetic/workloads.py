@@ -14,6 +14,9 @@ factor, expert weights W1/W3 [E,h,f] and W2 [E,f,h]).  Names:
   f=1536, expert loads skewed to Zipf(s=1.1) through a gate-logit bias.
 * ``switch``     - Switch-style top-1 with capacity factor 1.25: T=32768,
   h=1024, E=64, f=4096, four hot experts at 4x the mean load, so drops occur.
+* ``dsv3_grouped`` - ``dsv3`` with DeepSeek-V3's group-limited routing: the 256
+  experts form 8 groups of 32 and each token may only choose among the 4
+  groups whose two best selection scores sum highest.
 * ``dsv3_shared`` - ``dsv3`` plus one shared expert of width 2048 (DeepSeek-V3
   has one shared expert as wide as a routed one) that every token goes
   through, added to the routed output.
@@ -47,6 +50,8 @@ class Workload:
     gate_bias: Optional[str] = None      # None, "zipf:<s>" or "hot:<n>:<mult>"
     expert_bias: Optional[str] = None    # None or "uniform:<a>" (selection only)
     shared_f: int = 0              # > 0: a shared expert of this SwiGLU width
+    num_groups: int = 0            # > 1: group-limited top-k over this many expert groups
+    group_topk: int = 0            # groups kept per token when num_groups > 1
     description: str = ""
 
     @property
@@ -91,6 +96,10 @@ WORKLOADS = {
                     "E=64, capacity factor 1.25, SwiGLU f=4096, 4 hot experts at 4x "
                     "mean load"),
 }
+WORKLOADS["dsv3_grouped"] = replace(
+    WORKLOADS["dsv3"], name="dsv3_grouped", num_groups=8, group_topk=4,
+    description="dsv3 with group-limited routing: 8 expert groups of 32, the 4 best groups "
+                "(group score = sum of its top-2 selection scores) kept per token")
 WORKLOADS["dsv3_shared"] = replace(
     WORKLOADS["dsv3"], name="dsv3_shared", shared_f=2048,
     description="dsv3 plus one shared SwiGLU expert (width 2048) applied to every token and "

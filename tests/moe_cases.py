@@ -70,7 +70,8 @@ def condition_inputs(w, inp, max_rounds=64, nthreads=0):
     gb, eb = np_view(inp["gate_bias"]), np_view(inp["expert_bias"])
     x_cpu = x.detach().to("cpu").clone()
     logits = oracle.router_logits(np_view(x_cpu), Wg, gb, nthreads)
-    idx, prob, margin = oracle.topk_scores(logits, w.k, w.score, eb, nthreads)
+    groups = (w.num_groups, w.group_topk)
+    idx, prob, margin = oracle.topk_scores(logits, w.k, w.score, eb, nthreads, *groups)
     for rnd in range(max_rounds):
         part = {"capacity": oracle.capacity(w.T, w.E, w.k, w.capacity_factor, w.min_capacity),
                 "topk_idx": idx, "topk_prob_raw": prob,
@@ -82,13 +83,13 @@ def condition_inputs(w, inp, max_rounds=64, nthreads=0):
         rows = torch.tensor(bad)
         x_cpu[rows] = synthetic.redraw_x_rows(w, rnd, len(bad))
         sub = oracle.router_logits(np_view(x_cpu[rows]), Wg, gb, nthreads)
-        i2, p2, m2 = oracle.topk_scores(sub, w.k, w.score, eb, nthreads)
+        i2, p2, m2 = oracle.topk_scores(sub, w.k, w.score, eb, nthreads, *groups)
         idx[bad], prob[bad], margin[bad] = i2, p2, m2
     else:
         raise RuntimeError("margin conditioning did not converge")
     x.copy_(x_cpu.to(x.device))
     r = oracle.route(np_view(x_cpu), Wg, w.k, w.score, gb, eb, w.capacity_factor,
-                     w.min_capacity, w.drop_policy, nthreads)
+                     w.min_capacity, w.drop_policy, nthreads, *groups)
     assert np.all(r["margin"] >= MARGIN)
     return r
 
@@ -107,7 +108,8 @@ def oracle_forward(w, inp, nthreads=0, want_h_mid=True):
                           np_view(inp["W3"]), np_view(inp["W2"]), w.k, w.score,
                           np_view(inp["gate_bias"]), np_view(inp["expert_bias"]),
                           w.capacity_factor, w.min_capacity, w.drop_policy, nthreads,
-                          want_h_mid=want_h_mid, **shared)
+                          want_h_mid=want_h_mid, num_groups=w.num_groups,
+                          group_topk=w.group_topk, **shared)
 
 
 def gpu_config(w):

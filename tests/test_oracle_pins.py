@@ -397,3 +397,105 @@ def test_shared_expert_zero_down_projection_leaves_routed_output():
                          W2s=np.zeros((fs, h), np.float32))
     assert np.all(out["y_shared"] == 0.0)
     np.testing.assert_array_equal(out["y"], base["y"])
+
+
+# ------------------------------------------------ router variants (sqrtsoftplus, groups) --
+
+def _sqrtsoftplus(l):
+    return np.sqrt(np.logaddexp(0.0, np.asarray(l, np.float64)))
+
+
+def test_sqrtsoftplus_all_experts_closed_form():
+    # k = E: every expert is chosen, in descending score order, with weight s / sum(s)
+    T, E = 7, 6
+    logits = (3.0 * rng(110).standard_normal((T, E))).astype(np.float32)
+    idx, prob, _ = oracle.topk_scores(logits, E, "sqrtsoftplus")
+    s = _sqrtsoftplus(logits).astype(np.float32).astype(np.float64)
+    for t in range(T):
+        np.testing.assert_array_equal(idx[t], np.argsort(-s[t], kind="stable"))
+        np.testing.assert_allclose(prob[t], s[t][idx[t]] / s[t].sum(), rtol=1e-6)
+
+
+def test_sqrtsoftplus_large_logits_do_not_overflow():
+    logits = np.array([[100.0, -100.0, 0.0, 88.0]], np.float32)
+    idx, prob, _ = oracle.topk_scores(logits, 4, "sqrtsoftplus")
+    s = np.array([10.0, np.sqrt(np.log1p(np.exp(-100.0))), np.sqrt(np.log(2.0)), np.sqrt(88.0)])
+    assert list(idx[0]) == [0, 3, 2, 1]
+    np.testing.assert_allclose(prob[0], s[idx[0]] / s.sum(), rtol=1e-6)
+
+
+def test_sqrtsoftplus_bias_only_chooses():
+    T, E, k = 5, 6, 2
+    logits = rng(111).standard_normal((T, E)).astype(np.float32)
+    eb = np.zeros(E, np.float32)
+    eb[4] = 10.0  # expert 4 always chosen, its weight from the unbiased score
+    idx, prob, _ = oracle.topk_scores(logits, k, "sqrtsoftplus", eb)
+    s = _sqrtsoftplus(logits).astype(np.float32).astype(np.float64)
+    for t in range(T):
+        assert idx[t, 0] == 4
+        other = max((e for e in range(E) if e != 4), key=lambda e: (s[t, e], -e))
+        assert idx[t, 1] == other
+        np.testing.assert_allclose(prob[t], s[t][idx[t]] / s[t][idx[t]].sum(), rtol=1e-6)
+
+
+def _grouped_brute_force(sel, k, G, gk):
+    """Group-limited choice by exhaustive search: the kept groups are the
+    gk-subset with the largest total group score (group score = the sum of the
+    group's k//gk largest values, each group's best m-subset found by
+    enumeration); the chosen experts are the k-subset of the kept groups'
+    experts with the largest total score, listed by score."""
+    E = sel.shape[0]
+    per, m = E // G, k // gk
+    gscore = []
+    for g in range(G):
+        vals = sel[g * per:(g + 1) * per].astype(np.float64)
+        gscore.append(max(sum(c) for c in itertools.combinations(vals, m)))
+    groups = max(itertools.combinations(range(G), gk), key=lambda c: sum(gscore[g] for g in c))
+    elig = [e for e in range(E) if e // per in groups]
+    best = max(itertools.combinations(elig, k), key=lambda c: sum(float(sel[e]) for e in c))
+    return sorted(best, key=lambda e: -float(sel[e]))
+
+
+@pytest.mark.parametrize("score,E,k,G,gk", [("softmax_post", 8, 2, 4, 2), ("sigmoid", 12, 4, 4, 2),
+                                            ("sqrtsoftplus", 12, 3, 3, 1),
+                                            ("softmax_pre", 8, 4, 2, 2)])
+def test_group_limited_topk_brute_force(score, E, k, G, gk):
+    T = 40
+    r = rng(112)
+    logits = r.standard_normal((T, E)).astype(np.float32)
+    eb = r.uniform(-0.1, 0.1, E).astype(np.float32) if score in ("sigmoid", "sqrtsoftplus") else None
+    idx, prob, margin = oracle.topk_scores(logits, k, score, eb, num_groups=G, group_topk=gk)
+    # selection scores as the pages define them (fp32 values)
+    if score == "softmax_post":
+        sel = logits
+    elif score == "softmax_pre":
+        from scipy.special import softmax as sm
+        sel = sm(logits.astype(np.float64), axis=1).astype(np.float32)
+    else:
+        s = expit(logits.astype(np.float64)) if score == "sigmoid" else _sqrtsoftplus(logits)
+        sel = s.astype(np.float32) + (eb if eb is not None else 0)
+    for t in range(T):
+        assert list(idx[t]) == _grouped_brute_force(sel[t], k, G, gk), t
+        assert margin[t] >= 0
+
+
+def test_group_limited_special_cases_equal_ungrouped():
+    T, E, k = 30, 16, 4
+    logits = rng(113).standard_normal((T, E)).astype(np.float32)
+    base = oracle.topk_scores(logits, k, "sigmoid")
+    for G, gk in ((1, 1), (2, 2), (4, 4)):   # one group, or every group kept
+        got = oracle.topk_scores(logits, k, "sigmoid", num_groups=G, group_topk=gk)
+        np.testing.assert_array_equal(got[0], base[0])
+        np.testing.assert_array_equal(got[1], base[1])
+
+
+def test_group_limited_keeps_experts_inside_chosen_groups():
+    # group 1's best two scores dominate, group 0 has the single best expert:
+    # with one group kept, group 1 wins (sum of top-2) although it lacks the max
+    logits = np.array([[5.0, -9.0, -9.0, -9.0, 4.0, 3.9, -9.0, -9.0]], np.float32)
+    idx, prob, margin = oracle.topk_scores(logits, 2, "softmax_post", num_groups=2, group_topk=1)
+    assert list(idx[0]) == [4, 5]
+    # next eligible expert is -9 (k-th 3.9); group scores 7.9 against -4.0
+    np.testing.assert_allclose(margin[0], min(3.9 - (-9.0), (4.0 + 3.9) - (5.0 - 9.0)), rtol=1e-6)
+    idx_u, _, _ = oracle.topk_scores(logits, 2, "softmax_post")
+    assert list(idx_u[0]) == [0, 4]
