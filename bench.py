@@ -107,7 +107,7 @@ def measured_peaks():
 def workload_desc(w):
     return {"workload": w.description, "name": w.name, "T": w.T, "h": w.h, "E": w.E, "k": w.k,
             "f": w.f, "score": w.score, "capacity_factor": w.capacity_factor,
-            "shared_f": w.shared_f,
+            "shared_f": w.shared_f, "num_groups": w.num_groups, "group_topk": w.group_topk,
             "l2": "flushed between timed steps (512 MB write outside the events)"}
 
 
@@ -226,7 +226,7 @@ def run_native(args, rank, world, local):
     w = workload_of(args)
     inp = synthetic.generate(w, device=dev, seed=w.seed + 1000 * rank)
     cfg = moe.config(w.T, w.h, w.E, w.k, w.f, w.score, w.dtype, w.capacity_factor,
-                     w.min_capacity, w.drop_policy)
+                     w.min_capacity, w.drop_policy, w.num_groups, w.group_topk)
     b = moe.Buffers(cfg, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)

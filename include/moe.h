@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 #define MOE_MAX_EXPERTS 256
 #define MOE_MAX_TOPK 8
 
@@ -66,7 +66,8 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 typedef enum moe_score {
   MOE_SCORE_SOFTMAX_POST = 0, /* top-k on logits, softmax over the k ("renormalised") */
   MOE_SCORE_SOFTMAX_PRE = 1,  /* softmax over all E, then top-k, no renormalisation */
-  MOE_SCORE_SIGMOID = 2       /* sigmoid; expert_bias only chooses; p = s/(sum s + 1e-20) */
+  MOE_SCORE_SIGMOID = 2,      /* sigmoid; expert_bias only chooses; p = s/(sum s + 1e-20) */
+  MOE_SCORE_SQRTSOFTPLUS = 3  /* s = sqrt(softplus(l)); bias and weights as for sigmoid */
 } moe_score;
 
 /* Drop policies of §8 of the Megatron Core page (apply_router_token_dropping). */
@@ -86,6 +87,16 @@ typedef struct moe_config {
   int32_t drop_policy;    /* moe_drop_policy (used only when capacity_factor > 0) */
   float capacity_factor;  /* <= 0: dropless */
   int32_t min_capacity;   /* capacity is raised to at least this (default 0) */
+  /* Group-limited top-k (compute_topk(scores, topk, num_groups, group_topk) of
+   * §5; the page does not print its body).  num_groups <= 1: off.  Otherwise
+   * the experts form num_groups contiguous groups of E/num_groups; a group's
+   * score is the sum of its k/group_topk largest selection scores; each token
+   * keeps the group_topk best groups (equal scores: lower group first) and
+   * takes its top-k among their experts.  Needs E % num_groups == 0,
+   * num_groups <= 32, 1 <= group_topk <= min(num_groups, k) and
+   * k <= group_topk * E/num_groups (MOE_ERR_UNSUPPORTED otherwise). */
+  int32_t num_groups;
+  int32_t group_topk;
 } moe_config;
 
 /* ABI version of the loaded library (MOE_ABI_VERSION). */
@@ -116,8 +127,8 @@ moe_status moe_max_rows(const moe_config* cfg, int64_t* rows);
  *   x            [T,h]  dtype
  *   Wg           [h,E]  fp32 (row i = the E gate weights of input feature i)
  *   gate_bias    [E]    fp32 or NULL: added to the logits (a skew of the router)
- *   expert_bias  [E]    fp32 or NULL: sigmoid score only; changes the choice,
- *                       never the weights
+ *   expert_bias  [E]    fp32 or NULL: sigmoid / sqrtsoftplus scores only;
+ *                       changes the choice, never the weights
  *   topk_idx     [T,k]  int32 out: experts, by selection score descending
  *                       (equal scores: lower expert index first)
  *   topk_prob    [T,k]  fp32 out: combine weights; 0 for dropped pairs

@@ -14,7 +14,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libmoe_gb300.so")
 
-SCORE = {"softmax_post": 0, "softmax_pre": 1, "sigmoid": 2}
+SCORE = {"softmax_post": 0, "softmax_pre": 1, "sigmoid": 2, "sqrtsoftplus": 3}
 DTYPE = {"f32": 0, "bf16": 1}
 DROP_POLICY = {"probs": 0, "position": 1}
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
@@ -34,7 +34,8 @@ class MoeConfig(ctypes.Structure):
                 ("num_experts", ctypes.c_int32), ("topk", ctypes.c_int32),
                 ("ffn_hidden", ctypes.c_int32), ("score", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("drop_policy", ctypes.c_int32),
-                ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int32)]
+                ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int32),
+                ("num_groups", ctypes.c_int32), ("group_topk", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -91,9 +92,10 @@ def lib():
 
 
 def config(T, h, E, k, f, score="softmax_post", dtype="bf16", capacity_factor=0.0,
-           min_capacity=0, drop_policy="probs"):
+           min_capacity=0, drop_policy="probs", num_groups=0, group_topk=0):
     return MoeConfig(int(T), int(h), int(E), int(k), int(f), SCORE[score], DTYPE[dtype],
-                     DROP_POLICY[drop_policy], float(capacity_factor), int(min_capacity))
+                     DROP_POLICY[drop_policy], float(capacity_factor), int(min_capacity),
+                     int(num_groups), int(group_topk))
 
 
 def _check(code, where):

@@ -81,7 +81,9 @@ moe_status validate(const moe_config* c) {
   if (c->num_tokens < 0 || c->hidden <= 0 || c->num_experts <= 0 || c->topk <= 0 ||
       c->ffn_hidden <= 0 || c->min_capacity < 0)
     return MOE_ERR_INVALID_ARG;
-  if (c->score < MOE_SCORE_SOFTMAX_POST || c->score > MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (c->score < MOE_SCORE_SOFTMAX_POST || c->score > MOE_SCORE_SQRTSOFTPLUS)
+    return MOE_ERR_INVALID_ARG;
+  if (c->num_groups < 0 || c->group_topk < 0) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c->drop_policy != MOE_DROP_PROBS && c->drop_policy != MOE_DROP_POSITION)
     return MOE_ERR_INVALID_ARG;
@@ -91,6 +93,12 @@ moe_status validate(const moe_config* c) {
   if (c->hidden % 8 != 0 || c->ffn_hidden % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (c->dtype == MOE_BF16 && (c->hidden % 256 != 0 || c->ffn_hidden % 128 != 0))
     return MOE_ERR_UNSUPPORTED;
+  if (c->num_groups > 1) {
+    const int G = c->num_groups;
+    if (G > 32 || c->num_experts % G != 0 || c->group_topk < 1 || c->group_topk > G ||
+        c->group_topk > c->topk || c->topk > c->group_topk * (c->num_experts / G))
+      return MOE_ERR_UNSUPPORTED;
+  }
   const int64_t np = static_cast<int64_t>(c->num_tokens) * c->topk;
   if (np > (int64_t{1} << 30)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -181,14 +189,14 @@ moe_status do_route(const moe_config& c, const void* x, const float* Wg, const f
   int nsplit = 1;
   MOE_CUDA(launch_router_logits(T, c.hidden, E, c.dtype, x, Wg, logits, &nsplit, s));
   if (!drops) {
-    MOE_CUDA(launch_router_topk(T, E, k, c.score, logits, nsplit, gb, eb, topk_idx, topk_prob,
-                                keep, routing_map, tpe, err, s));
+    MOE_CUDA(launch_router_topk(T, E, k, c.score, c.num_groups, c.group_topk, logits, nsplit, gb,
+                                eb, topk_idx, topk_prob, keep, routing_map, tpe, err, s));
     return MOE_OK;
   }
   int32_t* assigned = at<int32_t>(ws, L.assigned);
   MOE_CUDA(cudaMemsetAsync(assigned, 0, E * sizeof(int32_t), s));
-  MOE_CUDA(launch_router_topk(T, E, k, c.score, logits, nsplit, gb, eb, topk_idx, topk_prob, keep,
-                              routing_map, assigned, err, s));
+  MOE_CUDA(launch_router_topk(T, E, k, c.score, c.num_groups, c.group_topk, logits, nsplit, gb,
+                              eb, topk_idx, topk_prob, keep, routing_map, assigned, err, s));
   // candidate lists: every routed pair, expert-major, ascending token order
   const int64_t np = static_cast<int64_t>(T) * k;
   const int64_t nt = perm_tiles(np);

@@ -32,7 +32,9 @@ inline int64_t perm_tiles(int64_t npairs) { return (npairs + kPermTile - 1) / kP
 constexpr int kRouterMaxSplits = 16;
 cudaError_t launch_router_logits(int T, int h, int E, int dtype, const void* x, const float* Wg,
                                  float* partials, int* nsplit, cudaStream_t s);
-cudaError_t launch_router_topk(int T, int E, int k, int score, const float* logits, int nsplit,
+// num_groups > 1: group-limited top-k (group_topk groups kept per token)
+cudaError_t launch_router_topk(int T, int E, int k, int score, int num_groups, int group_topk,
+                               const float* logits, int nsplit,
                                const float* gate_bias, const float* expert_bias,
                                int32_t* topk_idx, float* topk_prob,
                                uint8_t* keep, uint8_t* routing_map, int32_t* counts, int* err,

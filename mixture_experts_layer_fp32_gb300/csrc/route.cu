@@ -1,16 +1,20 @@
 // Router of the MoE layer forward, following the page "MoE我们喜欢你（三）：
 // Megatron Core MoE 源码路径解析" (r00kie-liu.github.io):
 //   §3 Gating            logits = x . Wg (+ bias) with the router math in fp32
-//   §4-§5 Score function softmax before/after top-k, or sigmoid with a
-//                        choice-only expert bias and renormalisation
+//   §4-§5 Score function softmax before/after top-k, or sigmoid / sqrtsoftplus
+//                        with a choice-only expert bias and renormalisation;
+//                        optionally group-limited (compute_topk's num_groups,
+//                        group_topk: the best group_topk groups by the sum of
+//                        their k/group_topk best scores, top-k inside them)
 //   §8 Token dropping    per-expert capacity, policy "probs" or "position"
 //
 // Kernels:
 //   router_logits_kernel  fp32 SIMT GEMM, CTA tile BT tokens x ET experts,
 //                         K staged through shared memory in BK chunks
 //                         (double-buffered), each thread a TT x TE micro-tile.
-//   router_topk_kernel    one warp per token: scores, top-k by k rounds of a
-//                         warp arg-max (ties -> lower expert id), weights,
+//   router_topk_kernel    one warp per token: scores, (group scores and the
+//                         kept groups), top-k by k rounds of a warp arg-max
+//                         (ties -> lower expert / group id), weights,
 //                         per-expert counts via a block histogram.
 //   drop_select_kernel    one CTA per expert: if over capacity, a radix
 //                         select over 64-bit keys (prob bits, then ~token)
@@ -506,25 +510,29 @@ cudaError_t launch_logits_typed(int T, int h, int E, const XT* x, const float* W
 
 // ------------------------------------------------------------------ top-k
 constexpr int kMaxPerLane = MOE_MAX_EXPERTS / 32;  // 8
+constexpr int kTopkWarps = 8;                       // warps (tokens in flight) per CTA
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
 __global__ void __launch_bounds__(256)
-    router_topk_kernel(int T, int E, int k, int score, const float* __restrict__ logits,
+    router_topk_kernel(int T, int E, int k, int score, int num_groups, int group_topk,
+                       const float* __restrict__ logits,
                        int nsplit, const float* __restrict__ gate_bias,
                        const float* __restrict__ expert_bias, int32_t* __restrict__ topk_idx,
                        float* __restrict__ topk_prob, uint8_t* __restrict__ keep,
                        uint8_t* __restrict__ routing_map, int32_t* __restrict__ counts,
                        int* __restrict__ err) {
   __shared__ int hist[MOE_MAX_EXPERTS];
+  __shared__ float gsel[kTopkWarps][MOE_MAX_EXPERTS];  // per warp: a token's selection scores
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
+  const int per_group = num_groups > 1 ? E / num_groups : E;
   for (int t = blockIdx.x * nwarps + warp; t < T; t += gridDim.x * nwarps) {
     // logits = (partial sums in split order) + gate bias
     float s[kMaxPerLane], sel[kMaxPerLane];
@@ -560,12 +568,17 @@ __global__ void __launch_bounds__(256)
         s[i] = (e < E) ? s[i] / z : 0.f;
         sel[i] = (e < E) ? s[i] : -FLT_MAX;
       }
-    } else if (score == MOE_SCORE_SIGMOID) {
+    } else if (score == MOE_SCORE_SIGMOID || score == MOE_SCORE_SQRTSOFTPLUS) {
 #pragma unroll
       for (int i = 0; i < kMaxPerLane; ++i) {
         const int e = lane + 32 * i;
         if (e < E) {
-          s[i] = 1.f / (1.f + expf(-s[i]));
+          if (score == MOE_SCORE_SIGMOID) {
+            s[i] = 1.f / (1.f + expf(-s[i]));
+          } else {
+            // softplus(l) = log(1 + e^l) = max(l, 0) + log1p(e^-|l|): no overflow
+            s[i] = sqrtf(fmaxf(s[i], 0.f) + log1pf(expf(-fabsf(s[i]))));
+          }
           sel[i] = expert_bias ? s[i] + expert_bias[e] : s[i];
         } else {
           s[i] = 0.f;
@@ -577,8 +590,61 @@ __global__ void __launch_bounds__(256)
       for (int i = 0; i < kMaxPerLane; ++i) sel[i] = s[i];
     }
 
-    // k rounds of a warp-wide arg-max over the not-yet-taken experts
+    // group-limited top-k: lane g < num_groups scores group g (the sum of its
+    // k/group_topk best selection scores, largest first), then group_topk
+    // rounds of a warp arg-max keep the best groups; the other groups'
+    // experts are marked taken so that the expert rounds skip them
     uint32_t taken = 0;
+    if (num_groups > 1) {
+#pragma unroll
+      for (int i = 0; i < kMaxPerLane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) gsel[warp][e] = sel[i];
+      }
+      __syncwarp();
+      float gs = -INFINITY;
+      if (lane < num_groups) {
+        const float* g = gsel[warp] + lane * per_group;
+        const int m = k / group_topk;
+        uint32_t used[MOE_MAX_EXPERTS / 32] = {0, 0, 0, 0, 0, 0, 0, 0};
+        gs = 0.f;
+        for (int r = 0; r < m; ++r) {
+          float bv = -INFINITY;
+          int bi = 0x7fffffff;
+          for (int c = 0; c < per_group; ++c)
+            if (!(used[c >> 5] >> (c & 31) & 1u) && better(g[c], c, bv, bi)) {
+              bv = g[c];
+              bi = c;
+            }
+          if (bi >= per_group) break;  // only on NaN scores (reported by the expert rounds)
+          used[bi >> 5] |= 1u << (bi & 31);
+          gs += bv;
+        }
+      }
+      __syncwarp();  // gsel is rewritten for the next token
+      uint32_t kept = 0;
+      for (int r = 0; r < group_topk; ++r) {
+        float bv = (lane < num_groups && !(kept >> lane & 1u)) ? gs : -INFINITY;
+        int bi = (lane < num_groups && !(kept >> lane & 1u)) ? lane : 0x7fffffff;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (better(ov, oi, bv, bi)) {
+            bv = ov;
+            bi = oi;
+          }
+        }
+        if (bi < num_groups) kept |= 1u << bi;
+      }
+#pragma unroll
+      for (int i = 0; i < kMaxPerLane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !(kept >> (e / per_group) & 1u)) taken |= 1u << i;
+      }
+    }
+
+    // k rounds of a warp-wide arg-max over the not-yet-taken experts
     int my_idx = -1;   // lane j < k keeps slot j
     float my_s = 0.f;
     for (int j = 0; j < k; ++j) {
@@ -743,18 +809,20 @@ cudaError_t launch_router_logits(int T, int h, int E, int dtype, const void* x, 
                                             partials, kMaxSplits, nsplit, s);
 }
 
-cudaError_t launch_router_topk(int T, int E, int k, int score, const float* logits, int nsplit,
+cudaError_t launch_router_topk(int T, int E, int k, int score, int num_groups, int group_topk,
+                               const float* logits, int nsplit,
                                const float* gate_bias, const float* expert_bias,
                                int32_t* topk_idx, float* topk_prob,
                                uint8_t* keep, uint8_t* routing_map, int32_t* counts, int* err,
                                cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int warps_per_block = 8;
+  const int warps_per_block = kTopkWarps;
   int blocks = (T + warps_per_block - 1) / warps_per_block;
   const int cap = device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   router_topk_kernel<<<blocks, 32 * warps_per_block, 0, s>>>(
-      T, E, k, score, logits, nsplit, gate_bias, expert_bias, topk_idx, topk_prob, keep,
+      T, E, k, score, num_groups, group_topk, logits, nsplit, gate_bias, expert_bias, topk_idx,
+      topk_prob, keep,
       routing_map, counts, err);
   return cudaGetLastError();
 }

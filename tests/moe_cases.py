@@ -115,7 +115,7 @@ def oracle_forward(w, inp, nthreads=0, want_h_mid=True):
 def gpu_config(w):
     import mixture_experts_layer_fp32_gb300 as moe
     return moe.config(w.T, w.h, w.E, w.k, w.f, w.score, w.dtype, w.capacity_factor,
-                      w.min_capacity, w.drop_policy)
+                      w.min_capacity, w.drop_policy, w.num_groups, w.group_topk)
 
 
 def to_dev(inp, device="cuda"):

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_function(moe):
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
     assert sorted(moe.EXPORTS) == declared_functions()
-    assert moe.lib().moe_abi_version() == 1
+    assert moe.lib().moe_abi_version() == 2
     assert moe.lib().moe_status_string(3) == b"MOE_ERR_WORKSPACE"
 
 
@@ -55,9 +55,10 @@ def _cfgp(cfg):
 
 @pytest.mark.parametrize("field,value,want", [
     ("num_tokens", -1, INVALID), ("hidden", 0, INVALID), ("num_experts", 0, INVALID),
-    ("topk", 0, INVALID), ("ffn_hidden", -8, INVALID), ("score", 3, INVALID),
+    ("topk", 0, INVALID), ("ffn_hidden", -8, INVALID),
     ("dtype", 2, INVALID), ("drop_policy", 5, INVALID), ("min_capacity", -1, INVALID),
     ("num_experts", 257, UNSUPPORTED), ("topk", 9, UNSUPPORTED), ("hidden", 4100, UNSUPPORTED),
+    ("score", 4, INVALID), ("num_groups", -1, INVALID), ("group_topk", -2, INVALID),
     ("ffn_hidden", 1500, UNSUPPORTED), ("hidden", 4092, UNSUPPORTED),
 ])
 def test_config_validation(moe, field, value, want):
@@ -176,3 +177,26 @@ def test_shared_expert_host_checks(moe):
     # moe_combine_shared: y_shared is optional but must be aligned
     assert lib.moe_combine_shared(ctypes.byref(cfg), FAKE, FAKE, FAKE, MISALIGNED, FAKE,
                                   None) == INVALID
+
+
+@pytest.mark.parametrize("E,k,G,gk,want", [
+    (256, 8, 8, 4, OK), (256, 8, 1, 0, OK), (256, 8, 0, 5, OK),   # off when num_groups <= 1
+    (256, 8, 6, 2, UNSUPPORTED),    # E not a multiple of the groups
+    (256, 8, 64, 4, UNSUPPORTED),   # more than 32 groups
+    (256, 8, 8, 0, UNSUPPORTED), (256, 8, 8, 9, UNSUPPORTED),  # group_topk out of [1, min(G,k)]
+    (16, 4, 4, 1, OK), (16, 6, 4, 1, UNSUPPORTED),  # k above group_topk * E/G
+    (8, 2, 4, 4, UNSUPPORTED),      # group_topk above k
+])
+def test_group_limited_config_validation(moe, E, k, G, gk, want):
+    cfg = moe.config(T=64, h=4096, E=E, k=k, f=1536, score="sigmoid", num_groups=G, group_topk=gk)
+    size = ctypes.c_size_t()
+    assert _status(moe, "moe_workspace_size", _cfgp(cfg), ctypes.byref(size)) == want
+
+
+def test_config_struct_matches_header(moe):
+    # field order and size of moe_config in include/moe.h
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct moe_config \{(.*?)\} moe_config;", text, re.S).group(1)
+    fields = re.findall(r"(\w+)\s*;", body)
+    assert fields == [f for f, _ in moe.MoeConfig._fields_]
+    assert ctypes.sizeof(moe.MoeConfig) == 4 * len(fields)

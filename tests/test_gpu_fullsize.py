@@ -21,8 +21,8 @@ from moe_cases import (assert_close, assert_equal, assert_probs, condition_input
 
 pytestmark = pytest.mark.gpu
 
-MAX_EXPERTS = {"tiny_fp32": 8, "mixtral": 8, "dsv3": 48, "dsv3_shared": 48, "qwen3": 48,
-               "switch": 32}
+MAX_EXPERTS = {"tiny_fp32": 8, "mixtral": 8, "dsv3": 48, "dsv3_grouped": 48, "dsv3_shared": 48,
+               "qwen3": 48, "switch": 32}
 MAX_TOKENS = 32
 
 
