@@ -286,49 +286,61 @@ def run_native(args, rank, world, local):
     ms = sum(step_ms) / len(step_ms)
     ms_all, tokens_per_s = job_throughput(ms, w.T, world)
 
-    # ---- e2e: moe_forward with host (pinned) input and output in the timed region
+    # ---- e2e: through the C ABI with host (pinned) input and output, copies
+    # inside the timed region
     e2e = None
     if not args.no_e2e:
         x_host = inp["x"].cpu().pin_memory()
         y_host = torch.empty(b.y.shape, dtype=b.y.dtype).pin_memory()
-        x_dev = torch.empty_like(inp["x"])
-        y_dev = torch.empty_like(b.y)
         if w.shared_f > 0:
+            # moe_forward_shared on device buffers, torch copies around it
+            x_dev = torch.empty_like(inp["x"])
+            y_dev = torch.empty_like(b.y)
             ws2 = moe.alloc_workspace_shared(cfg, w.shared_f, dev)
+
+            def run(n):
+                for _ in range(n):
+                    x_dev.copy_(x_host, non_blocking=True)
+                    moe.forward_shared(cfg, w.shared_f, x_dev, inp["Wg"], inp["gate_bias"],
+                                       inp["expert_bias"], inp["W1"], inp["W3"], inp["W2"],
+                                       inp["W1s"], inp["W3s"], inp["W2s"], y_dev, ws2)
+                    y_host.copy_(y_dev, non_blocking=True)
+            api = ("moe_forward_shared (C ABI) with pinned host x/y copied by torch on the same "
+                   "stream inside the timed region, one step at a time")
         else:
-            ws2 = moe.alloc_workspace(cfg, dev)
+            # moe_forward_host: every step's input copied from the pinned host buffer and its
+            # output copied back (stride 0: one buffer reused), the copies of neighbouring
+            # steps overlapping the compute of the current one
+            ws2 = moe.alloc_workspace_host(cfg, dev)
 
-        def fwd():
-            x_dev.copy_(x_host, non_blocking=True)
-            if w.shared_f > 0:
-                moe.forward_shared(cfg, w.shared_f, x_dev, inp["Wg"], inp["gate_bias"],
-                                   inp["expert_bias"], inp["W1"], inp["W3"], inp["W2"],
-                                   inp["W1s"], inp["W3s"], inp["W2s"], y_dev, ws2)
-            else:
-                moe.forward(cfg, x_dev, inp["Wg"], inp["gate_bias"], inp["expert_bias"],
-                            inp["W1"], inp["W3"], inp["W2"], y_dev, ws2)
-            y_host.copy_(y_dev, non_blocking=True)
+            def run(n):
+                moe.forward_host(cfg, x_host, y_host, inp["Wg"], inp["gate_bias"],
+                                 inp["expert_bias"], inp["W1"], inp["W3"], inp["W2"], ws2,
+                                 num_batches=n)
+            api = ("moe_forward_host (C ABI): %d batches from a pinned host buffer, each batch's "
+                   "H2D input and D2H output copy inside the timed region, pipelined on the "
+                   "library's copy streams" % args.steps)
 
-        for _ in range(max(1, args.warmup)):
-            fwd()
+        run(max(1, args.warmup))
         torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+        a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)
-            ev[i][0].record(stream)
-            fwd()
-            ev[i][1].record(stream)
+        a.record(stream)
+        run(args.steps)
+        c.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         moe.check(ws2)
-        e2e_ms = max_over_ranks(sum(a.elapsed_time(c) for a, c in ev) / args.steps, world)
+        e2e_ms = max_over_ranks(a.elapsed_time(c) / args.steps, world)
         e2e = {"value": world * w.T / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                "d2h_bytes_per_step": y_host.numel() * y_host.element_size(),
-               "api": "%s (C ABI) with pinned host x/y copies inside the timed region"
-                      % ("moe_forward_shared" if w.shared_f > 0 else "moe_forward")}
+               "api": api,
+               "l2": "not flushed between e2e steps; the expert weights read every step "
+                     "(%.0f MB) %s the 129 MB L2" % (
+                         3 * w.E * w.h * w.f * (4 if w.dtype == "f32" else 2) / 1e6,
+                         "exceed" if 3 * w.E * w.h * w.f * (4 if w.dtype == "f32" else 2)
+                         > 129e6 else "fit in")}
 
     if rank != 0:
         return None

@@ -242,6 +242,33 @@ moe_status moe_forward_shared(const moe_config* cfg, int32_t fs, const void* x, 
                               moe_stream_t stream);
 
 /*
+ * The layer forward over a sequence of batches held in HOST memory (not a
+ * step of the method: the serving loop around moe_forward).  For each batch
+ * b in [0, num_batches): its input x_host + b*x_batch_stride ([T,h] dtype)
+ * is copied to the device, the forward of moe_forward runs on `stream`, and
+ * its output [T,h] dtype is copied to y_host + b*y_batch_stride.  A stride of
+ * 0 reuses one host buffer for every batch (each batch still copies it).
+ * The copies run on the library's two copy streams, double-buffered in the
+ * workspace, so batch b+1's input and batch b-1's output move while batch b
+ * computes.  Everything is enqueued asynchronously: the outputs are on the
+ * host once `stream` is synchronised (the copy streams are joined to it).
+ * Host buffers should be page-locked (cudaHostAlloc / pinned); pageable
+ * memory works but the copies then serialise with the host.
+ *   ws: moe_workspace_size_host bytes (moe_workspace_size + 4 staging
+ *   buffers of T*h elements).  Router outputs stay in the workspace.
+ * Errors as moe_forward; MOE_ERR_INVALID_ARG for num_batches < 0, a missing
+ * host buffer, or 0 < y_batch_stride < T*h*elt with num_batches > 1.
+ * The first call on a device creates the copy streams; make it before any
+ * stream capture.
+ */
+moe_status moe_workspace_size_host(const moe_config* cfg, size_t* bytes);
+moe_status moe_forward_host(const moe_config* cfg, int32_t num_batches, const void* x_host,
+                            size_t x_batch_stride, void* y_host, size_t y_batch_stride,
+                            const float* Wg, const float* gate_bias, const float* expert_bias,
+                            const void* W1, const void* W3, const void* W2, void* ws,
+                            size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_permute without a workspace argument.  This entry point is not a step
  * of the MoE method (the pages have no counterpart); it exists for callers
  * that cannot give the library any device memory beyond their inputs and

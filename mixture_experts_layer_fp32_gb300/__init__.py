@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     Buffers,
     act_dtype,
     alloc_workspace,
+    alloc_workspace_host,
     alloc_workspace_shared,
     capacity,
     check,
@@ -23,6 +24,7 @@ from ._binding import (  # noqa: F401
     combine_shared,
     config,
     forward,
+    forward_host,
     forward_shared,
     grouped_fc1,
     grouped_fc2,
@@ -36,5 +38,6 @@ from ._binding import (  # noqa: F401
     selftest_wait_timeout,
     shared_expert,
     workspace_size,
+    workspace_size_host,
     workspace_size_shared,
 )

@@ -26,7 +26,7 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_c
            "moe_grouped_fc1", "moe_grouped_fc2", "moe_combine", "moe_forward", "moe_check",
            "moe_permute_noalloc", "moe_selftest_wait_timeout", "moe_shared_expert",
            "moe_combine_shared", "moe_workspace_size_shared", "moe_forward_shared",
-           "moe_probe_fp32_fma"]
+           "moe_probe_fp32_fma", "moe_workspace_size_host", "moe_forward_host"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -82,6 +82,9 @@ def lib():
             "moe_forward_shared": ([cfgp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                     vp, vp, sz, vp], i32),
             "moe_probe_fp32_fma": ([i64, vp, ctypes.POINTER(ctypes.c_double), vp], i32),
+            "moe_workspace_size_host": ([cfgp, ctypes.POINTER(sz)], i32),
+            "moe_forward_host": ([cfgp, i32, vp, sz, vp, sz, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+                                 i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -111,6 +114,17 @@ def _p(t):
         raise TypeError("expected a torch tensor")
     if not t.is_cuda:
         raise ValueError("tensors must live on a CUDA device (no CPU path exists)")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _host(t):
+    """Pointer of a HOST tensor (the host-I/O entry point's batches)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if t.is_cuda:
+        raise ValueError("x_host / y_host must be host tensors (ideally pinned)")
     if not t.is_contiguous():
         raise ValueError("tensors must be contiguous")
     return t.data_ptr()
@@ -237,6 +251,39 @@ def forward_shared(cfg, fs, x, Wg, gate_bias, expert_bias, W1, W3, W2, W1s, W3s,
                                     _p(W2s), _p(y), _p(topk_idx), _p(topk_prob),
                                     _p(tokens_per_expert), w, wb, _stream()),
            "moe_forward_shared")
+
+
+def workspace_size_host(cfg):
+    v = ctypes.c_size_t()
+    _check(lib().moe_workspace_size_host(ctypes.byref(cfg), ctypes.byref(v)),
+           "moe_workspace_size_host")
+    return v.value
+
+
+def alloc_workspace_host(cfg, device="cuda"):
+    """Zero-filled workspace for forward_host (moe_workspace_size_host bytes)."""
+    return torch.zeros(workspace_size_host(cfg), dtype=torch.uint8, device=device)
+
+
+def forward_host(cfg, x_host, y_host, Wg, gate_bias, expert_bias, W1, W3, W2, ws,
+                 num_batches=None):
+    """The forward over host batches x_host [B,T,h] -> y_host [B,T,h] (or one
+    [T,h] buffer reused num_batches times, stride 0), copies pipelined with
+    compute on the library's copy streams.  Asynchronous on the current
+    stream."""
+    T, h = cfg.num_tokens, cfg.hidden
+    if num_batches is None:
+        num_batches = x_host.shape[0] if x_host.dim() == 3 else 1
+    xs = x_host[0].numel() * x_host.element_size() if x_host.dim() == 3 else 0
+    ys = y_host[0].numel() * y_host.element_size() if y_host.dim() == 3 else 0
+    for t, stride in ((x_host, xs), (y_host, ys)):
+        per = T * h * t.element_size()
+        if (t.numel() * t.element_size()) < (per if stride == 0 else per * num_batches):
+            raise ValueError("host buffer smaller than its batches")
+    w, wb = _ws(ws)
+    _check(lib().moe_forward_host(ctypes.byref(cfg), int(num_batches), _host(x_host), xs,
+                                  _host(y_host), ys, _p(Wg), _p(gate_bias), _p(expert_bias),
+                                  _p(W1), _p(W3), _p(W2), w, wb, _stream()), "moe_forward_host")
 
 
 def probe_fp32_fma(iters, out):

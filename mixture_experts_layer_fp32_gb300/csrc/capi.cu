@@ -334,6 +334,57 @@ moe_status side_stream(SideStream** out) {
   return MOE_OK;
 }
 
+// The library's host-I/O streams per device for moe_forward_host: one for
+// host->device copies, one for device->host copies, and the events that
+// order them against the compute stream (per staging slot: input ready,
+// input free, output ready, output free; plus the entry fork and the two
+// final joins).  Created on first use, kept until exit.
+struct CopyStreams {
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t x_ready[2] = {}, x_free[2] = {}, y_ready[2] = {}, y_free[2] = {};
+  cudaEvent_t fork = nullptr, h2d_done = nullptr, d2h_done = nullptr;
+};
+std::mutex g_copy_mu;
+CopyStreams g_copy[64];
+
+moe_status copy_streams(CopyStreams** out) {
+  int dev = 0;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  CopyStreams& cs = g_copy[dev];
+  if (cs.h2d == nullptr) {
+    cudaEvent_t* evs[] = {&cs.x_ready[0], &cs.x_ready[1], &cs.x_free[0], &cs.x_free[1],
+                          &cs.y_ready[0], &cs.y_ready[1], &cs.y_free[0], &cs.y_free[1],
+                          &cs.fork,       &cs.h2d_done,   &cs.d2h_done};
+    for (cudaEvent_t* e : evs) MOE_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+    MOE_CUDA(cudaStreamCreateWithFlags(&cs.d2h, cudaStreamNonBlocking));
+    MOE_CUDA(cudaStreamCreateWithFlags(&cs.h2d, cudaStreamNonBlocking));
+  }
+  *out = &cs;
+  return MOE_OK;
+}
+
+// moe_forward_host's workspace: the routed layout, then two input staging
+// buffers [T,h] (dtype) and two output staging buffers [T,h] (dtype).
+struct HostLayout {
+  size_t x_stage[2], y_stage[2], total;
+};
+HostLayout make_host_layout(const moe_config& c) {
+  HostLayout H;
+  const size_t row = static_cast<size_t>(c.num_tokens) * c.hidden * (c.dtype == MOE_F32 ? 4 : 2);
+  size_t o = make_layout(c).total;
+  for (int i = 0; i < 2; ++i) {
+    H.x_stage[i] = o;
+    o = align_up(o + row);
+  }
+  for (int i = 0; i < 2; ++i) {
+    H.y_stage[i] = o;
+    o = align_up(o + row);
+  }
+  H.total = o;
+  return H;
+}
+
 }  // namespace
 
 extern "C" {
@@ -589,6 +640,87 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
                       tokens_per_expert, ws, stream, &r));
   MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm, r.row_map, r.prob,
                           nullptr, y, stream));
+  return MOE_OK;
+}
+
+moe_status moe_workspace_size_host(const moe_config* cfg, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = make_host_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_forward_host(const moe_config* cfg, int32_t num_batches, const void* x_host,
+                            size_t x_batch_stride, void* y_host, size_t y_batch_stride,
+                            const float* Wg, const float* gate_bias, const float* expert_bias,
+                            const void* W1, const void* W3, const void* W2, void* ws,
+                            size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  if (num_batches < 0) return MOE_ERR_INVALID_ARG;
+  const size_t T = c.num_tokens, E = c.num_experts, h = c.hidden;
+  const size_t row_bytes = T * h * (c.dtype == MOE_F32 ? 4 : 2);
+  const size_t wsz = E * h * c.ffn_hidden;
+  if (num_batches > 0 && row_bytes > 0 && (x_host == nullptr || y_host == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (num_batches > 1 && y_batch_stride != 0 && y_batch_stride < row_bytes)
+    return MOE_ERR_INVALID_ARG;  // output batches would overlap
+  MOE_TRY(need(Wg, h * E, 4));
+  MOE_TRY(optional(gate_bias, 4));
+  MOE_TRY(optional(expert_bias, 4));
+  MOE_TRY(need(W1, wsz, 16));
+  MOE_TRY(need(W3, wsz, 16));
+  MOE_TRY(need(W2, wsz, 16));
+  const HostLayout H = make_host_layout(c);
+  MOE_TRY(check_ws(c, ws, ws_bytes, H.total));
+  if (num_batches == 0) return MOE_OK;
+
+  std::lock_guard<std::mutex> lock(g_copy_mu);
+  CopyStreams* cs = nullptr;
+  MOE_TRY(copy_streams(&cs));
+  // both copy streams start after everything already enqueued on `stream`
+  MOE_CUDA(cudaEventRecord(cs->fork, stream));
+  MOE_CUDA(cudaStreamWaitEvent(cs->h2d, cs->fork, 0));
+  MOE_CUDA(cudaStreamWaitEvent(cs->d2h, cs->fork, 0));
+  moe_status st = MOE_OK;
+  for (int32_t b = 0; b < num_batches && st == MOE_OK; ++b) {
+    const int slot = b & 1;
+    void* xs = at<void>(ws, H.x_stage[slot]);
+    void* ys = at<void>(ws, H.y_stage[slot]);
+    const char* xb = static_cast<const char*>(x_host) + static_cast<size_t>(b) * x_batch_stride;
+    char* yb = static_cast<char*>(y_host) + static_cast<size_t>(b) * y_batch_stride;
+    // input copy: after the forward that last read this staging slot
+    st = cuda_status(cudaStreamWaitEvent(cs->h2d, cs->x_free[slot], 0));
+    if (st == MOE_OK && row_bytes)
+      st = cuda_status(cudaMemcpyAsync(xs, xb, row_bytes, cudaMemcpyHostToDevice, cs->h2d));
+    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->x_ready[slot], cs->h2d));
+    // forward: after its input landed and the output slot was copied out
+    if (st == MOE_OK) st = cuda_status(cudaStreamWaitEvent(stream, cs->x_ready[slot], 0));
+    if (st == MOE_OK) st = cuda_status(cudaStreamWaitEvent(stream, cs->y_free[slot], 0));
+    Routed r{};
+    if (st == MOE_OK)
+      st = routed_path(c, xs, Wg, gate_bias, expert_bias, W1, W3, W2, nullptr, nullptr, nullptr,
+                       ws, stream, &r);
+    if (st == MOE_OK)
+      st = cuda_status(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm,
+                                      r.row_map, r.prob, nullptr, ys, stream));
+    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->x_free[slot], stream));
+    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->y_ready[slot], stream));
+    // output copy: after the forward wrote it
+    if (st == MOE_OK) st = cuda_status(cudaStreamWaitEvent(cs->d2h, cs->y_ready[slot], 0));
+    if (st == MOE_OK && row_bytes)
+      st = cuda_status(cudaMemcpyAsync(yb, ys, row_bytes, cudaMemcpyDeviceToHost, cs->d2h));
+    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->y_free[slot], cs->d2h));
+  }
+  // join: `stream` completes only after every copy (also after a failure, so
+  // that no copy stream is left running ahead of the caller's stream)
+  const cudaError_t j1 = cudaEventRecord(cs->h2d_done, cs->h2d);
+  const cudaError_t j2 = cudaEventRecord(cs->d2h_done, cs->d2h);
+  const cudaError_t w1 = j1 == cudaSuccess ? cudaStreamWaitEvent(stream, cs->h2d_done, 0) : j1;
+  const cudaError_t w2 = j2 == cudaSuccess ? cudaStreamWaitEvent(stream, cs->d2h_done, 0) : j2;
+  MOE_TRY(st);
+  MOE_CUDA(w1);
+  MOE_CUDA(w2);
   return MOE_OK;
 }
 

@@ -200,3 +200,21 @@ def test_config_struct_matches_header(moe):
     fields = re.findall(r"(\w+)\s*;", body)
     assert fields == [f for f, _ in moe.MoeConfig._fields_]
     assert ctypes.sizeof(moe.MoeConfig) == 4 * len(fields)
+
+
+def test_forward_host_host_checks(moe):
+    lib = moe.lib()
+    cfg = moe.config(T=128, h=4096, E=8, k=2, f=1536)
+    size = ctypes.c_size_t()
+    assert lib.moe_workspace_size_host(ctypes.byref(cfg), ctypes.byref(size)) == OK
+    need = size.value
+    assert need >= moe.workspace_size(cfg) + 4 * 128 * 4096 * 2
+    row = 128 * 4096 * 2
+    call = lambda nb, x, xs, y, ys, ws_bytes: lib.moe_forward_host(
+        ctypes.byref(cfg), nb, x, xs, y, ys, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, ws_bytes,
+        None)
+    assert call(-1, FAKE, 0, FAKE, 0, need) == INVALID
+    assert call(2, None, 0, FAKE, 0, need) == INVALID           # no input buffer
+    assert call(2, FAKE, 0, FAKE, row - 2, need) == INVALID     # output batches overlap
+    assert call(2, FAKE, row, FAKE, row, need - 1) == WORKSPACE  # routed ws is not enough
+    assert call(0, FAKE, 0, FAKE, 0, need) == OK                 # nothing to do, nothing enqueued
