@@ -55,6 +55,12 @@ def _load():
         L.oracle_combine.argtypes = [i64, i32, i32, vp, vp, vp, vp, i32]
         L.oracle_forward_dense.argtypes = [i64, i32, i32, i32, i32, vp, i32, vp, vp, vp,
                                            vp, vp, vp, i32, vp, i32]
+        L.oracle_quantize_rows_e4m3.argtypes = [i64, i32, vp, i32, vp, vp, i32]
+        L.oracle_quantize_cols_e4m3.argtypes = [i64, i32, i32, vp, i32, vp, vp, i32]
+        L.oracle_expert_rows_fp8.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                             vp, vp, vp, vp, i32]
+        L.oracle_e4m3_values.argtypes = [vp]
+        L.oracle_e4m3_codes.argtypes = [i64, vp, vp]
         _lib = L
     return _lib
 
@@ -238,4 +244,90 @@ def forward(x, Wg, W1, W3, W2, k, score, gate_bias=None, expert_bias=None,
         y = y + y_shared
     r.update({"offsets": offsets, "row_map": row_map, "row_token": row_token,
               "x_perm": x_perm, "y_perm": y_perm, "h_mid": h_mid, "y": y})
+    return r
+
+
+# ------------------------------------------------------------------- FP8 --
+
+def e4m3_values():
+    """The value of every E4M3 code 0..255 (float64; NaN for the NaN codes)."""
+    out = np.empty(256, np.float64)
+    _load().oracle_e4m3_values(_ptr(out))
+    return out
+
+
+def e4m3_codes(v):
+    """E4M3 codes (nearest, ties to even, saturating at 448) of float64 values."""
+    v = _c(np.asarray(v, np.float64), np.float64)
+    out = np.empty(v.shape, np.uint8)
+    _load().oracle_e4m3_codes(v.size, _ptr(v), _ptr(out))
+    return out
+
+
+def quantize_rows_e4m3(x, nthreads=0):
+    """Per-row power-of-two-scaled E4M3: x [rows, cols] -> (codes, scales [rows])."""
+    x = _c(x)
+    rows, cols = x.shape
+    codes = np.empty((rows, cols), np.uint8)
+    scales = np.empty((rows,), np.float32)
+    _load().oracle_quantize_rows_e4m3(rows, cols, _ptr(x), _dtype_code(x), _ptr(codes),
+                                      _ptr(scales), nthreads)
+    return codes, scales
+
+
+def quantize_cols_e4m3(W, nthreads=0):
+    """Per-output-channel E4M3 of W [E,K,N] -> (codes [E,N,K], scales [E,N])."""
+    W = _c(W)
+    E, K, N = W.shape
+    codes = np.empty((E, N, K), np.uint8)
+    scales = np.empty((E, N), np.float32)
+    _load().oracle_quantize_cols_e4m3(E, K, N, _ptr(W), _dtype_code(W), _ptr(codes),
+                                      _ptr(scales), nthreads)
+    return codes, scales
+
+
+def quantize_experts_e4m3(W1, W3, W2, nthreads=0):
+    """The FP8 form of the expert weights: dict of W1q/W3q [E,f,h], W2q [E,h,f]
+    codes and s1/s3 [E,f], s2 [E,h] scales."""
+    W1q, s1 = quantize_cols_e4m3(W1, nthreads)
+    W3q, s3 = quantize_cols_e4m3(W3, nthreads)
+    W2q, s2 = quantize_cols_e4m3(W2, nthreads)
+    return {"W1q": W1q, "s1": s1, "W3q": W3q, "s3": s3, "W2q": W2q, "s2": s2}
+
+
+def expert_rows_fp8(xq, xs, row_expert, q, nthreads=0):
+    """FP8 SwiGLU rows: returns dict y_rows [R,h], h_mid [R,f] (bf16 values),
+    hq [R,f] codes, hs [R] scales (float64 / uint8 / float32)."""
+    xq = _c(xq, np.uint8)
+    xs = _c(xs, np.float32)
+    row_expert = _c(row_expert, np.int32)
+    R, h = xq.shape
+    f = q["W1q"].shape[1]
+    y = np.empty((R, h), np.float64)
+    hm = np.empty((R, f), np.float64)
+    hq = np.empty((R, f), np.uint8)
+    hs = np.empty((R,), np.float32)
+    _load().oracle_expert_rows_fp8(R, h, f, _ptr(xq), _ptr(xs), _ptr(row_expert),
+                                   _ptr(_c(q["W1q"], np.uint8)), _ptr(_c(q["s1"], np.float32)),
+                                   _ptr(_c(q["W3q"], np.uint8)), _ptr(_c(q["s3"], np.float32)),
+                                   _ptr(_c(q["W2q"], np.uint8)), _ptr(_c(q["s2"], np.float32)),
+                                   _ptr(hm), _ptr(hq), _ptr(hs), _ptr(y), nthreads)
+    return {"y_rows": y, "h_mid": hm, "hq": hq, "hs": hs}
+
+
+def forward_fp8(x, Wg, q, k, score, gate_bias=None, expert_bias=None, capacity_factor=0.0,
+                min_capacity=0, drop_policy="probs", nthreads=0, num_groups=0, group_topk=0):
+    """The layer with FP8 experts: route -> drop -> permute -> (x quantised per
+    token) FP8 SwiGLU experts -> combine.  q: quantize_experts_e4m3(...)."""
+    r = route(x, Wg, k, score, gate_bias, expert_bias, capacity_factor, min_capacity,
+              drop_policy, nthreads, num_groups, group_topk)
+    E = Wg.shape[1]
+    offsets, row_map, row_token = permute(r["topk_idx"], r["keep"], E)
+    row_expert = np.repeat(np.arange(E, dtype=np.int32), np.diff(offsets))
+    xq, xs = quantize_rows_e4m3(x, nthreads)
+    res = expert_rows_fp8(xq[row_token], xs[row_token], row_expert, q, nthreads)
+    y = combine(res["y_rows"], row_map, r["topk_prob"], nthreads)
+    r.update({"offsets": offsets, "row_map": row_map, "row_token": row_token, "xq": xq,
+              "xs": xs, "y_perm": res["y_rows"], "h_mid": res["h_mid"], "hq": res["hq"],
+              "hs": res["hs"], "y": y})
     return r

@@ -75,11 +75,69 @@ void topk_desc(const float* v, int n, int k, int32_t* out_idx) {
   }
 }
 
+// ------------------------------------------------------------ FP8 (E4M3)
+// The 8-bit float E4M3 of the OCP 8-bit floating point specification: sign
+// bit, 4 exponent bits (bias 7), 3 mantissa bits; no infinities; S.1111.111
+// is NaN; largest finite value 448 = 1.75 * 2^8; smallest normal 2^-6;
+// subnormals m/8 * 2^-6.  Codes 0..126 are the non-negative finite values in
+// increasing order.
+double e4m3_value(uint8_t c) {
+  const int ex = (c >> 3) & 15, m = c & 7;
+  if (ex == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+  const double v = ex == 0 ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, ex - 7);
+  return (c & 0x80) ? -v : v;
+}
+
+// The nearest finite E4M3 value to v (ties: the even code, i.e. mantissa
+// bit 0 clear); magnitudes at or beyond 448 give 448 (saturation); NaN gives
+// the NaN code 0x7F.
+uint8_t e4m3_code(double v) {
+  static const std::vector<double> table = [] {
+    std::vector<double> t(127);
+    for (int c = 0; c < 127; ++c) t[c] = e4m3_value((uint8_t)c);
+    return t;
+  }();
+  if (std::isnan(v)) return 0x7F;
+  const uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
+  const double a = std::fabs(v);
+  if (a >= table[126]) return sign | 126;
+  const int hi = (int)(std::upper_bound(table.begin(), table.end(), a) - table.begin());
+  const int lo = hi - 1;  // table[lo] <= a < table[hi]
+  const double dl = a - table[lo], dh = table[hi] - a;
+  const int c = dl < dh ? lo : dh < dl ? hi : ((lo & 1) ? hi : lo);
+  return sign | (uint8_t)c;
+}
+
+// Power-of-two scale of a row or column whose largest magnitude is amax:
+// the smallest integer e with amax * 2^-e <= 448, so that every scaled value
+// is finite in E4M3.  amax zero or below the smallest normal fp32: e = 0.
+int fp8_scale_exp(double amax) {
+  if (!(amax >= std::ldexp(1.0, -126))) return 0;
+  int e = -400;
+  while (std::ldexp(amax, -e) > 448.0) ++e;
+  return e;
+}
+
+// The nearest bf16 value to v (ties: even), as a double.
+double bf16_round(double v) {
+  const float f = (float)v;
+  uint32_t bits;
+  std::memcpy(&bits, &f, 4);
+  const uint32_t lo_bits = bits & 0xFFFF0000u, hi_bits = lo_bits + 0x10000u;
+  float lo, hi;
+  std::memcpy(&lo, &lo_bits, 4);
+  std::memcpy(&hi, &hi_bits, 4);
+  const double dl = std::fabs(v - (double)lo), dh = std::fabs((double)hi - v);
+  if (dl < dh) return lo;
+  if (dh < dl) return hi;
+  return (lo_bits & 0x10000u) ? hi : lo;
+}
+
 }  // namespace
 
 extern "C" {
 
-int oracle_abi_version(void) { return 2; }
+int oracle_abi_version(void) { return 3; }
 
 // [MC] §3 Gating: logits = x . Wg (+ bias) with the router math in fp32.
 // The oracle forms the exact sum in double over the exact fp32 values of x
@@ -370,6 +428,107 @@ void oracle_forward_dense(int64_t T, int h, int E, int k, int f, const void* x, 
     }
     for (int n = 0; n < h; ++n) y[t * (int64_t)h + n] = out[n];
   });
+}
+
+// ------------------------------------------------------------ FP8 experts
+// FP8 variant of the grouped expert MLP ([MC] §10 experts; the Megatron Core
+// report names FP8 GEMMs as its most effective single optimisation but
+// prints no scaling recipe).  Reading used here: E4M3 values with one
+// power-of-two scale per token row of the activations and one per output
+// channel of every weight matrix (the scale of fp8_scale_exp), fp32-exact
+// dequantisation value = code value * 2^e.
+
+// Row quantisation: x [rows, cols] (x_dtype) -> codes [rows, cols] and
+// scales [rows] (= 2^e of each row's largest magnitude).
+void oracle_quantize_rows_e4m3(int64_t rows, int cols, const void* x, int x_dtype,
+                               uint8_t* codes, float* scales, int nthreads) {
+  parallel_for(rows, nthreads, [&](int64_t r) {
+    double amax = 0.0;
+    for (int c = 0; c < cols; ++c)
+      amax = std::max(amax, std::fabs(value_at(x, x_dtype, r * (int64_t)cols + c)));
+    const int e = fp8_scale_exp(amax);
+    scales[r] = (float)std::ldexp(1.0, e);
+    for (int c = 0; c < cols; ++c)
+      codes[r * (int64_t)cols + c] =
+          e4m3_code(std::ldexp(value_at(x, x_dtype, r * (int64_t)cols + c), -e));
+  });
+}
+
+// Weight quantisation per output channel: W [E][K][N] (w_dtype) -> codes
+// [E][N][K] (K contiguous: each output channel's weights in a row) and
+// scales [E][N] (2^e of the channel's largest magnitude over K).
+void oracle_quantize_cols_e4m3(int64_t E, int K, int N, const void* W, int w_dtype,
+                               uint8_t* codes, float* scales, int nthreads) {
+  parallel_for(E * N, nthreads, [&](int64_t en) {
+    const int64_t e = en / N, n = en % N;
+    const int64_t base = e * (int64_t)K * N + n;
+    double amax = 0.0;
+    for (int k = 0; k < K; ++k) amax = std::max(amax, std::fabs(value_at(W, w_dtype, base + (int64_t)k * N)));
+    const int ex = fp8_scale_exp(amax);
+    scales[en] = (float)std::ldexp(1.0, ex);
+    for (int k = 0; k < K; ++k)
+      codes[en * (int64_t)K + k] = e4m3_code(std::ldexp(value_at(W, w_dtype, base + (int64_t)k * N), -ex));
+  });
+}
+
+// SwiGLU expert rows on FP8 operands:
+//   a = (sum_i x(i) w1(c,i)) * sx * s1(c),  g likewise with W3,
+//   H = silu(a) * g, rounded to bf16 (the stored intermediate), then
+//   quantised per row (hq, hs) and
+//   y(n) = (sum_c h(c) w2(n,c)) * hs * s2(n)
+// where x(i), w(c,i), h(c) are E4M3 code values; sums in double.
+//   xq [R,h] codes, xs [R]; W1q/W3q [E,f,h] codes, s1/s3 [E,f];
+//   W2q [E,h,f] codes, s2 [E,h]; h_mid [R,f] (bf16 values, may be NULL),
+//   hq [R,f] codes and hs [R] (may be NULL), y_rows [R,h] out.
+void oracle_expert_rows_fp8(int64_t R, int h, int f, const uint8_t* xq, const float* xs,
+                            const int32_t* row_expert, const uint8_t* W1q, const float* s1,
+                            const uint8_t* W3q, const float* s3, const uint8_t* W2q,
+                            const float* s2, double* h_mid, uint8_t* hq, float* hs,
+                            double* y_rows, int nthreads) {
+  parallel_for(R, nthreads, [&](int64_t r) {
+    const int64_t e = row_expert[r];
+    std::vector<double> xv(h), H(f);
+    for (int i = 0; i < h; ++i) xv[i] = e4m3_value(xq[r * (int64_t)h + i]);
+    double amax = 0.0;
+    for (int c = 0; c < f; ++c) {
+      const uint8_t* w1 = W1q + (e * f + c) * (int64_t)h;
+      const uint8_t* w3 = W3q + (e * f + c) * (int64_t)h;
+      double a = 0.0, g = 0.0;
+      for (int i = 0; i < h; ++i) {
+        a += xv[i] * e4m3_value(w1[i]);
+        g += xv[i] * e4m3_value(w3[i]);
+      }
+      a *= (double)xs[r] * (double)s1[e * f + c];
+      g *= (double)xs[r] * (double)s3[e * f + c];
+      H[c] = bf16_round(a / (1.0 + std::exp(-a)) * g);
+      amax = std::max(amax, std::fabs(H[c]));
+    }
+    const int ex = fp8_scale_exp(amax);
+    const double scale = std::ldexp(1.0, ex);
+    std::vector<double> hv(f);
+    for (int c = 0; c < f; ++c) {
+      const uint8_t code = e4m3_code(std::ldexp(H[c], -ex));
+      hv[c] = e4m3_value(code);
+      if (hq) hq[r * (int64_t)f + c] = code;
+      if (h_mid) h_mid[r * (int64_t)f + c] = H[c];
+    }
+    if (hs) hs[r] = (float)scale;
+    for (int n = 0; n < h; ++n) {
+      const uint8_t* w2 = W2q + (e * h + n) * (int64_t)f;
+      double y = 0.0;
+      for (int c = 0; c < f; ++c) y += hv[c] * e4m3_value(w2[c]);
+      y_rows[r * (int64_t)h + n] = y * scale * (double)s2[e * h + n];
+    }
+  });
+}
+
+// The E4M3 value of every code 0..255 (for the pins).
+void oracle_e4m3_values(double* out) {
+  for (int c = 0; c < 256; ++c) out[c] = e4m3_value((uint8_t)c);
+}
+// E4M3 codes of n doubles (for the pins).
+void oracle_e4m3_codes(int64_t n, const double* v, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_code(v[i]);
 }
 
 }  // extern "C"
