@@ -110,9 +110,11 @@ uint8_t e4m3_code(double v) {
 
 // Power-of-two scale of a row or column whose largest magnitude is amax:
 // the smallest integer e with amax * 2^-e <= 448, so that every scaled value
-// is finite in E4M3.  amax zero or below the smallest normal fp32: e = 0.
+// is finite in E4M3.  amax below 2^-100 (zero included), infinite or NaN:
+// e = 0 (such a row's scaled values are then exact fp32 products, and 2^-e
+// stays an ordinary fp32 power of two for every other row).
 int fp8_scale_exp(double amax) {
-  if (!(amax >= std::ldexp(1.0, -126))) return 0;
+  if (!(amax >= std::ldexp(1.0, -100)) || !std::isfinite(amax)) return 0;
   int e = -400;
   while (std::ldexp(amax, -e) > 448.0) ++e;
   return e;

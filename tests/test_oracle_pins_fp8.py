@@ -80,6 +80,19 @@ def test_quantize_rows_scale_rule_and_codes(dtype):
     assert scales[5] == 1.0
 
 
+def test_scale_rule_edges():
+    x = np.zeros((4, 8), np.float32)
+    x[0, 0] = 2.0 ** -101           # below 2^-100: scale 1, codes 0
+    x[1, 0] = 2.0 ** -99            # smallest e: 2^-99 / 2^e <= 448 -> e = -107
+    x[2, 0] = np.float32(3.4e38)    # largest magnitudes: e = 120
+    x[3, 0] = np.inf                # infinite: scale 1, saturated code
+    codes, scales = oracle.quantize_rows_e4m3(x)
+    assert scales[0] == 1.0 and codes[0, 0] == 0
+    assert scales[1] == 2.0 ** -107 and oracle.e4m3_values()[codes[1, 0]] == 256.0
+    assert scales[2] == 2.0 ** 120
+    assert scales[3] == 1.0 and codes[3, 0] == 0x7E
+
+
 def test_quantize_cols_is_rows_of_the_transpose():
     W = rng(121).standard_normal((3, 40, 24)).astype(np.float32)
     W[1, :, 7] *= 1e4
