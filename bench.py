@@ -71,6 +71,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--precision", default="bf16", choices=["bf16", "e4m3"],
+                    help="expert GEMM operands: bf16 (the default workload) or E4M3 (FP8 "
+                         "experts, weights quantised once outside the timed region)")
     ap.add_argument("--override", default="",
                     help="comma list of workload fields to replace, e.g. T=2048,f=3584 "
                          "(a shrunk case for profiling captures)")
@@ -193,25 +196,30 @@ def recorded_traffic(kernel, workload):
 
 # ---------------------------------------------------------------- native arm
 
-def kernels_per_forward(w, cfg):
+def kernels_per_forward(w, cfg, fp8=False):
     import mixture_experts_layer_fp32_gb300 as moe
     cap = moe.capacity(cfg)
     drops = 0 <= cap < w.T
     route = 2 + (4 if drops else 0)   # logits, top-k (+ hist, scan, rank, select)
     shared = 2 if w.shared_f > 0 else 0  # the shared expert's fc1 and fc2
-    return route + 4 + 1 + 1 + shared + 1  # permute hist/scan/rank/copy, fc1, fc2, combine
+    quant = 2 if fp8 else 0           # E4M3: x rows before the permute, h rows before fc2
+    return route + 4 + 1 + 1 + shared + quant + 1  # permute hist/scan/rank/copy, fc1, fc2, combine
 
 
-def stage_work(w, R):
-    """Algorithmic work of each stage (bytes moved or flops), per forward."""
+def stage_work(w, R, fp8=False):
+    """Algorithmic work of each stage (bytes moved or flops), per forward.
+    fp8: E4M3 expert operands (1-byte codes of x_perm, the weights and the
+    SwiGLU output; fc2 also reads the bf16 SwiGLU output once to quantise it)."""
     b = 4 if w.dtype == "f32" else 2
+    q = 1 if fp8 else b          # bytes of a GEMM operand element
     T, h, E, k, f = w.T, w.h, w.E, w.k, w.f
     return {
         "route": {"bytes": T * h * b + h * E * 4 + T * k * (4 + 4 + 1),
                   "flops": 2 * T * h * E},
-        "permute": {"bytes": T * h * b + R * h * b + T * k * (4 + 1 + 4)},
-        "fc1": {"flops": 4 * R * h * f, "bytes": 2 * w.E * h * f * b + R * h * b + R * f * b},
-        "fc2": {"flops": 2 * R * f * h, "bytes": w.E * f * h * b + R * f * b + R * h * 4},
+        "permute": {"bytes": T * h * b + R * h * q + T * k * (4 + 1 + 4)},
+        "fc1": {"flops": 4 * R * h * f, "bytes": 2 * w.E * h * f * q + R * h * q + R * f * b},
+        "fc2": {"flops": 2 * R * f * h,
+                "bytes": w.E * f * h * q + R * f * b + (2 * R * f if fp8 else 0) + R * h * 4},
         "combine": {"bytes": R * h * 4 + T * h * b + T * k * 8 + (T * h * 4 if w.shared_f else 0)},
         "shared": {"flops": 6 * T * h * w.shared_f,
                    "bytes": 3 * h * w.shared_f * b + T * h * b + 2 * T * w.shared_f * b + T * h * 4},
@@ -235,17 +243,38 @@ def run_native(args, rank, world, local):
         h_mid_s = torch.empty((w.T, w.shared_f), dtype=moe.act_dtype(cfg), device=dev)
         y_shared = torch.empty((w.T, w.h), dtype=torch.float32, device=dev)
 
+    fp8 = args.precision == "e4m3"
+    if fp8:
+        if w.dtype != "bf16" or w.shared_f > 0:
+            raise SystemExit("--precision e4m3 needs a bf16 workload without a shared expert")
+        q = moe.E4m3Experts(cfg, inp["W1"], inp["W3"], inp["W2"])  # once, outside the timing
+        b.ws = moe.alloc_workspace_e4m3(cfg, dev)
+        Rmax = w.T * w.k
+        xq = torch.empty((Rmax, w.h), dtype=torch.uint8, device=dev)
+        xs = torch.empty((Rmax,), dtype=torch.float32, device=dev)
+        hq = torch.empty((Rmax, w.f), dtype=torch.uint8, device=dev)
+        hs = torch.empty((Rmax,), dtype=torch.float32, device=dev)
+
     def step(ev=None):
         if ev: ev[0].record(stream)
         moe.route(cfg, inp["x"], inp["Wg"], inp["gate_bias"], inp["expert_bias"], b.topk_idx,
                   b.topk_prob, b.keep, b.tokens_per_expert, None, b.ws)
         if ev: ev[1].record(stream)
-        moe.permute(cfg, inp["x"], b.topk_idx, b.keep, b.x_perm, b.row_map, b.expert_offsets,
-                    b.ws)
-        if ev: ev[2].record(stream)
-        moe.grouped_fc1(cfg, b.x_perm, b.expert_offsets, inp["W1"], inp["W3"], b.h_mid, b.ws)
-        if ev: ev[3].record(stream)
-        moe.grouped_fc2(cfg, b.h_mid, b.expert_offsets, inp["W2"], b.y_perm, b.ws)
+        if fp8:
+            moe.permute_e4m3(cfg, inp["x"], b.topk_idx, b.keep, xq, xs, b.row_map,
+                             b.expert_offsets, b.ws)
+            if ev: ev[2].record(stream)
+            moe.grouped_fc1_e4m3(cfg, xq, xs, b.expert_offsets, q, b.h_mid, b.ws)
+            if ev: ev[3].record(stream)
+            moe.grouped_fc2_e4m3(cfg, b.h_mid, b.expert_offsets, q, hq, hs, b.y_perm, b.ws)
+        else:
+            moe.permute(cfg, inp["x"], b.topk_idx, b.keep, b.x_perm, b.row_map,
+                        b.expert_offsets, b.ws)
+            if ev: ev[2].record(stream)
+            moe.grouped_fc1(cfg, b.x_perm, b.expert_offsets, inp["W1"], inp["W3"], b.h_mid,
+                            b.ws)
+            if ev: ev[3].record(stream)
+            moe.grouped_fc2(cfg, b.h_mid, b.expert_offsets, inp["W2"], b.y_perm, b.ws)
         if ev: ev[4].record(stream)
         if w.shared_f > 0:
             moe.shared_expert(cfg, w.shared_f, inp["x"], inp["W1s"], inp["W3s"], inp["W2s"],
@@ -292,7 +321,20 @@ def run_native(args, rank, world, local):
     if not args.no_e2e:
         x_host = inp["x"].cpu().pin_memory()
         y_host = torch.empty(b.y.shape, dtype=b.y.dtype).pin_memory()
-        if w.shared_f > 0:
+        if fp8:
+            x_dev = torch.empty_like(inp["x"])
+            y_dev = torch.empty_like(b.y)
+            ws2 = moe.alloc_workspace_e4m3(cfg, dev)
+
+            def run(n):
+                for _ in range(n):
+                    x_dev.copy_(x_host, non_blocking=True)
+                    moe.forward_e4m3(cfg, x_dev, inp["Wg"], inp["gate_bias"], inp["expert_bias"],
+                                     q, y_dev, ws2)
+                    y_host.copy_(y_dev, non_blocking=True)
+            api = ("moe_forward_e4m3 (C ABI) with pinned host x/y copied by torch on the same "
+                   "stream inside the timed region, one step at a time")
+        elif w.shared_f > 0:
             # moe_forward_shared on device buffers, torch copies around it
             x_dev = torch.empty_like(inp["x"])
             y_dev = torch.empty_like(b.y)
@@ -346,7 +388,7 @@ def run_native(args, rank, world, local):
         return None
 
     peaks = measured_peaks()
-    work = stage_work(w, R)
+    work = stage_work(w, R, fp8)
     stages = {}
     for s in stage_names:
         t = sum(stage_ms[s]) / len(stage_ms[s])
@@ -366,33 +408,39 @@ def run_native(args, rank, world, local):
 
     dom = max(stage_names, key=lambda s: stages[s]["ms"])
     if dom in ("fc1", "fc2") and w.dtype == "bf16":
-        roof = {"kernel": gemm_kernel_name(w, w.T * w.k, dom), "bound": "tensor",
-                "achieved": stages[dom]["tflops"], "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s"}
+        # E4M3 MMAs: the measured bf16 peak x the nominal FP8/bf16 ratio (4.5 / 2.25)
+        ratio = 2.0 if fp8 else 1.0
+        roof = {"kernel": gemm_kernel_name(w, w.T * w.k, dom) + ("[E4M3]" if fp8 else ""),
+                "bound": "tensor", "achieved": stages[dom]["tflops"],
+                "peak": ratio * peaks["bf16_tflops"], "unit": "TFLOP/s"}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": stages[dom].get("gbs"),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["achieved"] else None
     if roof["bound"] == "tensor" and peaks.get("bf16_tflops_sustained"):
-        roof["frac_of_sustained_peak"] = roof["achieved"] / peaks["bf16_tflops_sustained"]
-    roof["peak_source"] = "%s (MEASURED_PEAKS.json burst)" % peaks["source"] \
+        roof["frac_of_sustained_peak"] = roof["achieved"] / (
+            (2.0 if fp8 else 1.0) * peaks["bf16_tflops_sustained"])
+    roof["peak_source"] = "%s (MEASURED_PEAKS.json burst%s)" % (
+        peaks["source"], " x 2, the nominal E4M3/bf16 ratio" if fp8 else "") \
         if peaks["source"] == "measured" else "fallback"
-    roof["traffic"] = recorded_traffic(dom, w.name)
+    roof["traffic"] = None if fp8 else recorded_traffic(dom, w.name)
     roof["algorithmic_per_launch"] = work[dom].get("flops") if roof["unit"] == "TFLOP/s" \
         else work[dom].get("bytes")
 
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 experts, bf16 activations" if fp8 else w.dtype,
         "data": "synthetic (seeded, x~N(0,%g), weights~N(0,%g), random-init)" % (w.x_std, w.w_std),
-        "config": dict(workload_desc(w), parallelism="replicas" if world > 1 else "single"),
+        "config": dict(workload_desc(w), parallelism="replicas" if world > 1 else "single",
+                       precision=args.precision),
         "grouped_gemm_tflops": gemm_tflops,
         "stages": stages,
         "rows": R, "tokens_per_expert_cv": float(np.std(tpe) / max(np.mean(tpe), 1e-9)),
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": kernels_per_forward(w, cfg) * args.steps,
+        "gpu_launches": kernels_per_forward(w, cfg, fp8) * args.steps,
         "clocks": clk,
         "wall_s_timed_region": t_wall,
         "peaks": peaks,

@@ -242,6 +242,70 @@ moe_status moe_forward_shared(const moe_config* cfg, int32_t fs, const void* x, 
                               moe_stream_t stream);
 
 /*
+ * FP8 experts.  The Megatron Core report on GB300 names FP8 GEMMs as its
+ * most effective single optimisation but prints no scaling recipe; the one
+ * used here: E4M3 codes (OCP 8-bit float, round-to-nearest-even, saturating
+ * at 448) with one power-of-two scale 2^e per token row of x (and per row of
+ * the SwiGLU output) and per output channel of every weight matrix, e the
+ * smallest integer with amax * 2^-e <= 448 (amax below 2^-100 or not
+ * finite: e = 0).  The grouped GEMMs run on E4M3 tensor-core MMAs
+ * (kind::f8f6f4) with fp32 accumulation; scales are applied in the
+ * epilogues; the SwiGLU output is rounded to bf16, quantised per row, and
+ * the down projection runs on E4M3 as well.  Routing, permutation and the
+ * combine are those of the bf16 path.  Needs dtype MOE_BF16 (x and y bf16;
+ * MOE_ERR_UNSUPPORTED otherwise).
+ *
+ * moe_quantize_rows_e4m3: in [rows, cols] bf16 -> codes [rows, cols] uint8
+ *   and scales [rows] fp32 (2^e).  cols % 16 == 0.
+ * moe_quantize_experts_e4m3: the expert weights in E4M3, once, K-major
+ *   (one row of codes per output channel): W1/W3 [E,h,f] bf16 -> W1q/W3q
+ *   [E,f,h] codes and s1/s3 [E,f] scales; W2 [E,f,h] -> W2q [E,h,f] and
+ *   s2 [E,h].  Scale arrays 16-byte aligned.
+ * moe_workspace_size_e4m3: workspace bytes of the E4M3 entry points.
+ * moe_permute_e4m3: moe_permute on E4M3 rows: x quantised per token, the
+ *   kept pairs' code rows x_perm_q [T*k,h] and their scales x_perm_scale
+ *   [T*k] in expert-major order; row_map and expert_offsets as moe_permute.
+ * moe_grouped_mlp_e4m3: the E4M3 SwiGLU experts: h_mid [T*k,f] bf16,
+ *   h_q [T*k,f] codes and h_scale [T*k] (the quantised SwiGLU output), and
+ *   y_perm [T*k,h] fp32 out; rows >= expert_offsets[E] untouched.
+ *   moe_grouped_fc1_e4m3 / moe_grouped_fc2_e4m3 are its two halves: fc1
+ *   writes h_mid; fc2 quantises h_mid's rows (h_q, h_scale) and writes y_perm.
+ * moe_forward_e4m3: the whole layer with E4M3 experts (arguments of
+ *   moe_forward, with the quantised weights and their scales).
+ */
+moe_status moe_quantize_rows_e4m3(int64_t rows, int32_t cols, const void* in, uint8_t* codes,
+                                  float* scales, moe_stream_t stream);
+moe_status moe_quantize_experts_e4m3(const moe_config* cfg, const void* W1, const void* W3,
+                                     const void* W2, uint8_t* W1q, uint8_t* W3q, uint8_t* W2q,
+                                     float* s1, float* s3, float* s2, moe_stream_t stream);
+moe_status moe_workspace_size_e4m3(const moe_config* cfg, size_t* bytes);
+moe_status moe_permute_e4m3(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                            const uint8_t* keep, uint8_t* x_perm_q, float* x_perm_scale,
+                            int32_t* row_map, int32_t* expert_offsets, void* ws,
+                            size_t ws_bytes, moe_stream_t stream);
+moe_status moe_grouped_mlp_e4m3(const moe_config* cfg, const uint8_t* x_perm_q,
+                                const float* x_perm_scale, const int32_t* expert_offsets,
+                                const uint8_t* W1q, const float* s1, const uint8_t* W3q,
+                                const float* s3, const uint8_t* W2q, const float* s2,
+                                void* h_mid, uint8_t* h_q, float* h_scale, float* y_perm,
+                                void* ws, size_t ws_bytes, moe_stream_t stream);
+moe_status moe_grouped_fc1_e4m3(const moe_config* cfg, const uint8_t* x_perm_q,
+                                const float* x_perm_scale, const int32_t* expert_offsets,
+                                const uint8_t* W1q, const float* s1, const uint8_t* W3q,
+                                const float* s3, void* h_mid, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
+moe_status moe_grouped_fc2_e4m3(const moe_config* cfg, const void* h_mid,
+                                const int32_t* expert_offsets, const uint8_t* W2q,
+                                const float* s2, uint8_t* h_q, float* h_scale, float* y_perm,
+                                void* ws, size_t ws_bytes, moe_stream_t stream);
+moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* Wg,
+                            const float* gate_bias, const float* expert_bias, const uint8_t* W1q,
+                            const float* s1, const uint8_t* W3q, const float* s3,
+                            const uint8_t* W2q, const float* s2, void* y, int32_t* topk_idx,
+                            float* topk_prob, int32_t* tokens_per_expert, void* ws,
+                            size_t ws_bytes, moe_stream_t stream);
+
+/*
  * The layer forward over a sequence of batches held in HOST memory (not a
  * step of the method: the serving loop around moe_forward).  For each batch
  * b in [0, num_batches): its input x_host + b*x_batch_stride ([T,h] dtype)

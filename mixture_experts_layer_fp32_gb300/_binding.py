@@ -26,7 +26,10 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_c
            "moe_grouped_fc1", "moe_grouped_fc2", "moe_combine", "moe_forward", "moe_check",
            "moe_permute_noalloc", "moe_selftest_wait_timeout", "moe_shared_expert",
            "moe_combine_shared", "moe_workspace_size_shared", "moe_forward_shared",
-           "moe_probe_fp32_fma", "moe_workspace_size_host", "moe_forward_host"]
+           "moe_probe_fp32_fma", "moe_workspace_size_host", "moe_forward_host",
+           "moe_quantize_rows_e4m3", "moe_quantize_experts_e4m3", "moe_workspace_size_e4m3",
+           "moe_permute_e4m3", "moe_grouped_mlp_e4m3", "moe_forward_e4m3",
+           "moe_grouped_fc1_e4m3", "moe_grouped_fc2_e4m3"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -85,6 +88,14 @@ def lib():
             "moe_workspace_size_host": ([cfgp, ctypes.POINTER(sz)], i32),
             "moe_forward_host": ([cfgp, i32, vp, sz, vp, sz, vp, vp, vp, vp, vp, vp, vp, sz, vp],
                                  i32),
+            "moe_quantize_rows_e4m3": ([i64, i32, vp, vp, vp, vp], i32),
+            "moe_quantize_experts_e4m3": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp], i32),
+            "moe_workspace_size_e4m3": ([cfgp, ctypes.POINTER(sz)], i32),
+            "moe_permute_e4m3": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_grouped_mlp_e4m3": ([cfgp] + [vp] * 13 + [vp, sz, vp], i32),
+            "moe_forward_e4m3": ([cfgp] + [vp] * 14 + [vp, sz, vp], i32),
+            "moe_grouped_fc1_e4m3": ([cfgp] + [vp] * 8 + [vp, sz, vp], i32),
+            "moe_grouped_fc2_e4m3": ([cfgp] + [vp] * 7 + [vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -284,6 +295,86 @@ def forward_host(cfg, x_host, y_host, Wg, gate_bias, expert_bias, W1, W3, W2, ws
     _check(lib().moe_forward_host(ctypes.byref(cfg), int(num_batches), _host(x_host), xs,
                                   _host(y_host), ys, _p(Wg), _p(gate_bias), _p(expert_bias),
                                   _p(W1), _p(W3), _p(W2), w, wb, _stream()), "moe_forward_host")
+
+
+# ------------------------------------------------------------- E4M3 experts
+
+def quantize_rows_e4m3(x, codes, scales):
+    """x [rows, cols] bf16 -> codes [rows, cols] uint8, scales [rows] fp32."""
+    rows, cols = x.shape
+    _check(lib().moe_quantize_rows_e4m3(rows, cols, _p(x), _p(codes), _p(scales), _stream()),
+           "moe_quantize_rows_e4m3")
+
+
+class E4m3Experts:
+    """The expert weights in E4M3 (device tensors): W1q/W3q [E,f,h], W2q [E,h,f]
+    uint8 codes, s1/s3 [E,f] and s2 [E,h] fp32 scales."""
+
+    def __init__(self, cfg, W1, W3, W2):
+        E, h, f = cfg.num_experts, cfg.hidden, cfg.ffn_hidden
+        d = W1.device
+        self.W1q = torch.empty((E, f, h), dtype=torch.uint8, device=d)
+        self.W3q = torch.empty((E, f, h), dtype=torch.uint8, device=d)
+        self.W2q = torch.empty((E, h, f), dtype=torch.uint8, device=d)
+        self.s1 = torch.empty((E, f), dtype=torch.float32, device=d)
+        self.s3 = torch.empty((E, f), dtype=torch.float32, device=d)
+        self.s2 = torch.empty((E, h), dtype=torch.float32, device=d)
+        _check(lib().moe_quantize_experts_e4m3(ctypes.byref(cfg), _p(W1), _p(W3), _p(W2),
+                                               _p(self.W1q), _p(self.W3q), _p(self.W2q),
+                                               _p(self.s1), _p(self.s3), _p(self.s2), _stream()),
+               "moe_quantize_experts_e4m3")
+
+
+def workspace_size_e4m3(cfg):
+    v = ctypes.c_size_t()
+    _check(lib().moe_workspace_size_e4m3(ctypes.byref(cfg), ctypes.byref(v)),
+           "moe_workspace_size_e4m3")
+    return v.value
+
+
+def alloc_workspace_e4m3(cfg, device="cuda"):
+    return torch.zeros(workspace_size_e4m3(cfg), dtype=torch.uint8, device=device)
+
+
+def permute_e4m3(cfg, x, topk_idx, keep, x_perm_q, x_perm_scale, row_map, expert_offsets, ws):
+    w, wb = _ws(ws)
+    _check(lib().moe_permute_e4m3(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(keep), _p(x_perm_q),
+                                  _p(x_perm_scale), _p(row_map), _p(expert_offsets), w, wb,
+                                  _stream()), "moe_permute_e4m3")
+
+
+def grouped_mlp_e4m3(cfg, x_perm_q, x_perm_scale, expert_offsets, q, h_mid, h_q, h_scale,
+                     y_perm, ws):
+    w, wb = _ws(ws)
+    _check(lib().moe_grouped_mlp_e4m3(ctypes.byref(cfg), _p(x_perm_q), _p(x_perm_scale),
+                                      _p(expert_offsets), _p(q.W1q), _p(q.s1), _p(q.W3q),
+                                      _p(q.s3), _p(q.W2q), _p(q.s2), _p(h_mid), _p(h_q),
+                                      _p(h_scale), _p(y_perm), w, wb, _stream()),
+           "moe_grouped_mlp_e4m3")
+
+
+def grouped_fc1_e4m3(cfg, x_perm_q, x_perm_scale, expert_offsets, q, h_mid, ws):
+    w, wb = _ws(ws)
+    _check(lib().moe_grouped_fc1_e4m3(ctypes.byref(cfg), _p(x_perm_q), _p(x_perm_scale),
+                                      _p(expert_offsets), _p(q.W1q), _p(q.s1), _p(q.W3q),
+                                      _p(q.s3), _p(h_mid), w, wb, _stream()),
+           "moe_grouped_fc1_e4m3")
+
+
+def grouped_fc2_e4m3(cfg, h_mid, expert_offsets, q, h_q, h_scale, y_perm, ws):
+    w, wb = _ws(ws)
+    _check(lib().moe_grouped_fc2_e4m3(ctypes.byref(cfg), _p(h_mid), _p(expert_offsets),
+                                      _p(q.W2q), _p(q.s2), _p(h_q), _p(h_scale), _p(y_perm), w,
+                                      wb, _stream()), "moe_grouped_fc2_e4m3")
+
+
+def forward_e4m3(cfg, x, Wg, gate_bias, expert_bias, q, y, ws, topk_idx=None, topk_prob=None,
+                 tokens_per_expert=None):
+    w, wb = _ws(ws)
+    _check(lib().moe_forward_e4m3(ctypes.byref(cfg), _p(x), _p(Wg), _p(gate_bias),
+                                  _p(expert_bias), _p(q.W1q), _p(q.s1), _p(q.W3q), _p(q.s3),
+                                  _p(q.W2q), _p(q.s2), _p(y), _p(topk_idx), _p(topk_prob),
+                                  _p(tokens_per_expert), w, wb, _stream()), "moe_forward_e4m3")
 
 
 def probe_fp32_fma(iters, out):

@@ -334,6 +334,77 @@ moe_status side_stream(SideStream** out) {
   return MOE_OK;
 }
 
+// FP8 (E4M3) workspace: the routed layout (its h_mid holds the bf16 SwiGLU
+// output), then x codes [T,h] and token scales [T], the permuted codes
+// [T*k,h] and their row scales [T*k], the SwiGLU codes [T*k,f] and scales.
+struct E4m3Layout {
+  size_t xq, xs, xperm_q, xperm_s, hq, hs, total;
+};
+E4m3Layout make_e4m3_layout(const moe_config& c) {
+  E4m3Layout Q;
+  const size_t T = c.num_tokens, np = T * c.topk, h = c.hidden, f = c.ffn_hidden;
+  size_t o = make_layout(c).total;
+  auto take = [&](size_t bytes) {
+    const size_t r = o;
+    o = align_up(o + bytes);
+    return r;
+  };
+  Q.xq = take(T * h);
+  Q.xs = take(T * 4);
+  Q.xperm_q = take(np * h);
+  Q.xperm_s = take(np * 4);
+  Q.hq = take(np * f);
+  Q.hs = take(np * 4);
+  Q.total = o;
+  return Q;
+}
+
+moe_status validate_e4m3(const moe_config& c) {
+  return c.dtype == MOE_BF16 ? MOE_OK : MOE_ERR_UNSUPPORTED;  // bf16 in/out, E4M3 experts
+}
+
+// E4M3 permute: quantise x per token, rank the pairs, copy code rows and scales.
+moe_status do_permute_e4m3(const moe_config& c, const void* x, const int32_t* topk_idx,
+                           const uint8_t* keep, uint8_t* xperm_q, float* xperm_s,
+                           int32_t* row_map, int32_t* offsets, void* ws, cudaStream_t s) {
+  const Layout L = make_layout(c);
+  const E4m3Layout Q = make_e4m3_layout(c);
+  const int T = c.num_tokens, E = c.num_experts, k = c.topk;
+  int* err = at<int>(ws, L.err);
+  const int64_t np = static_cast<int64_t>(T) * k;
+  if (np == 0) {
+    MOE_CUDA(cudaMemsetAsync(offsets, 0, (E + 1) * sizeof(int32_t), s));
+    return MOE_OK;
+  }
+  uint8_t* xq = at<uint8_t>(ws, Q.xq);
+  float* xs = at<float>(ws, Q.xs);
+  MOE_CUDA(launch_quantize_rows(T, c.hidden, x, xq, xs, nullptr, s));
+  int32_t* tiles = at<int32_t>(ws, L.tiles);
+  MOE_CUDA(launch_perm_hist(np, E, topk_idx, keep, tiles, err, s));
+  MOE_CUDA(launch_perm_scan(perm_tiles(np), E, tiles, offsets, nullptr, s));
+  MOE_CUDA(launch_perm_rank(np, E, topk_idx, keep, tiles, row_map, nullptr, s));
+  MOE_CUDA(launch_perm_copy_rows(T, c.hidden, k, xq, row_map, xperm_q, xs, xperm_s, s));
+  return MOE_OK;
+}
+
+// E4M3 experts: fc1 (scaled, SwiGLU, bf16 h_mid), per-row quantisation of the
+// rows that exist (expert_offsets[E] on the device), fc2 (scaled, fp32).
+moe_status do_mlp_e4m3(const moe_config& c, const uint8_t* xperm_q, const float* xperm_s,
+                       const int32_t* offsets, const uint8_t* W1q, const float* s1,
+                       const uint8_t* W3q, const float* s3, const uint8_t* W2q, const float* s2,
+                       void* h_mid, uint8_t* hq, float* hs, float* y_perm, void* ws,
+                       cudaStream_t s) {
+  const Layout L = make_layout(c);
+  int* err = at<int>(ws, L.err);
+  const int64_t rows = static_cast<int64_t>(c.num_tokens) * c.topk;
+  const int E = c.num_experts, h = c.hidden, f = c.ffn_hidden;
+  MOE_CUDA(launch_tc_fc1_e4m3(E, h, f, rows, xperm_q, xperm_s, nullptr, offsets, W1q, s1, W3q,
+                              s3, h_mid, err, s));
+  MOE_CUDA(launch_quantize_rows(rows, f, h_mid, hq, hs, offsets + E, s));
+  MOE_CUDA(launch_tc_fc2_e4m3(E, h, f, rows, hq, hs, offsets, W2q, s2, y_perm, err, s));
+  return MOE_OK;
+}
+
 // The library's host-I/O streams per device for moe_forward_host: one for
 // host->device copies, one for device->host copies, and the events that
 // order them against the compute stream (per staging slot: input ready,
@@ -640,6 +711,192 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
                       tokens_per_expert, ws, stream, &r));
   MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm, r.row_map, r.prob,
                           nullptr, y, stream));
+  return MOE_OK;
+}
+
+moe_status moe_quantize_rows_e4m3(int64_t rows, int32_t cols, const void* in, uint8_t* codes,
+                                  float* scales, moe_stream_t stream) {
+  if (rows < 0 || cols <= 0) return MOE_ERR_INVALID_ARG;
+  if (cols % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  const size_t n = static_cast<size_t>(rows) * cols;
+  MOE_TRY(need(in, n, 16));
+  MOE_TRY(need(codes, n, 16));
+  MOE_TRY(need(scales, static_cast<size_t>(rows), 4));
+  MOE_CUDA(launch_quantize_rows(rows, cols, in, codes, scales, nullptr, stream));
+  return MOE_OK;
+}
+
+moe_status moe_quantize_experts_e4m3(const moe_config* cfg, const void* W1, const void* W3,
+                                     const void* W2, uint8_t* W1q, uint8_t* W3q, uint8_t* W2q,
+                                     float* s1, float* s3, float* s2, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_e4m3(c));
+  const size_t E = c.num_experts, h = c.hidden, f = c.ffn_hidden, wsz = E * h * f;
+  for (const void* p : {W1, W3, W2}) MOE_TRY(need(p, wsz, 16));
+  for (const void* p : {static_cast<const void*>(W1q), static_cast<const void*>(W3q),
+                        static_cast<const void*>(W2q)})
+    MOE_TRY(need(p, wsz, 16));
+  MOE_TRY(need(s1, E * f, 16));
+  MOE_TRY(need(s3, E * f, 16));
+  MOE_TRY(need(s2, E * h, 16));
+  MOE_CUDA(launch_quantize_cols(c.num_experts, c.hidden, c.ffn_hidden, W1, W1q, s1, stream));
+  MOE_CUDA(launch_quantize_cols(c.num_experts, c.hidden, c.ffn_hidden, W3, W3q, s3, stream));
+  MOE_CUDA(launch_quantize_cols(c.num_experts, c.ffn_hidden, c.hidden, W2, W2q, s2, stream));
+  return MOE_OK;
+}
+
+moe_status moe_workspace_size_e4m3(const moe_config* cfg, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  MOE_TRY(validate_e4m3(*cfg));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = make_e4m3_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_permute_e4m3(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                            const uint8_t* keep, uint8_t* x_perm_q, float* x_perm_scale,
+                            int32_t* row_map, int32_t* expert_offsets, void* ws,
+                            size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_e4m3(c));
+  const size_t T = c.num_tokens, k = c.topk;
+  MOE_TRY(need(x, T * c.hidden, 16));
+  MOE_TRY(need(topk_idx, T * k, 4));
+  MOE_TRY(optional(keep, 1));
+  MOE_TRY(need(x_perm_q, T * k * c.hidden, 16));
+  MOE_TRY(need(x_perm_scale, T * k, 4));
+  MOE_TRY(need(row_map, T * k, 4));
+  MOE_TRY(need(expert_offsets, c.num_experts + 1, 4));
+  MOE_TRY(check_ws(c, ws, ws_bytes, make_e4m3_layout(c).total));
+  return do_permute_e4m3(c, x, topk_idx, keep, x_perm_q, x_perm_scale, row_map, expert_offsets,
+                         ws, stream);
+}
+
+moe_status moe_grouped_mlp_e4m3(const moe_config* cfg, const uint8_t* x_perm_q,
+                                const float* x_perm_scale, const int32_t* expert_offsets,
+                                const uint8_t* W1q, const float* s1, const uint8_t* W3q,
+                                const float* s3, const uint8_t* W2q, const float* s2,
+                                void* h_mid, uint8_t* h_q, float* h_scale, float* y_perm,
+                                void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_e4m3(c));
+  const size_t R = static_cast<size_t>(c.num_tokens) * c.topk, E = c.num_experts;
+  const size_t h = c.hidden, f = c.ffn_hidden, wsz = E * h * f;
+  MOE_TRY(need(x_perm_q, R * h, 16));
+  MOE_TRY(need(x_perm_scale, R, 4));
+  MOE_TRY(need(expert_offsets, E + 1, 4));
+  MOE_TRY(need(W1q, wsz, 16));
+  MOE_TRY(need(W3q, wsz, 16));
+  MOE_TRY(need(W2q, wsz, 16));
+  MOE_TRY(need(s1, E * f, 16));
+  MOE_TRY(need(s3, E * f, 16));
+  MOE_TRY(need(s2, E * h, 16));
+  MOE_TRY(need(h_mid, R * f, 16));
+  MOE_TRY(need(h_q, R * f, 16));
+  MOE_TRY(need(h_scale, R, 4));
+  MOE_TRY(need(y_perm, R * h, 16));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  return do_mlp_e4m3(c, x_perm_q, x_perm_scale, expert_offsets, W1q, s1, W3q, s3, W2q, s2, h_mid,
+                     h_q, h_scale, y_perm, ws, stream);
+}
+
+moe_status moe_grouped_fc1_e4m3(const moe_config* cfg, const uint8_t* x_perm_q,
+                                const float* x_perm_scale, const int32_t* expert_offsets,
+                                const uint8_t* W1q, const float* s1, const uint8_t* W3q,
+                                const float* s3, void* h_mid, void* ws, size_t ws_bytes,
+                                moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_e4m3(c));
+  const size_t R = static_cast<size_t>(c.num_tokens) * c.topk, E = c.num_experts;
+  const size_t h = c.hidden, f = c.ffn_hidden, wsz = E * h * f;
+  MOE_TRY(need(x_perm_q, R * h, 16));
+  MOE_TRY(need(x_perm_scale, R, 4));
+  MOE_TRY(need(expert_offsets, E + 1, 4));
+  MOE_TRY(need(W1q, wsz, 16));
+  MOE_TRY(need(W3q, wsz, 16));
+  MOE_TRY(need(s1, E * f, 16));
+  MOE_TRY(need(s3, E * f, 16));
+  MOE_TRY(need(h_mid, R * f, 16));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  int* err = at<int>(ws, make_layout(c).err);
+  MOE_CUDA(launch_tc_fc1_e4m3(c.num_experts, c.hidden, c.ffn_hidden, static_cast<int64_t>(R),
+                              x_perm_q, x_perm_scale, nullptr, expert_offsets, W1q, s1, W3q, s3,
+                              h_mid, err, stream));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_fc2_e4m3(const moe_config* cfg, const void* h_mid,
+                                const int32_t* expert_offsets, const uint8_t* W2q,
+                                const float* s2, uint8_t* h_q, float* h_scale, float* y_perm,
+                                void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_e4m3(c));
+  const size_t R = static_cast<size_t>(c.num_tokens) * c.topk, E = c.num_experts;
+  const size_t h = c.hidden, f = c.ffn_hidden;
+  MOE_TRY(need(h_mid, R * f, 16));
+  MOE_TRY(need(expert_offsets, E + 1, 4));
+  MOE_TRY(need(W2q, E * h * f, 16));
+  MOE_TRY(need(s2, E * h, 16));
+  MOE_TRY(need(h_q, R * f, 16));
+  MOE_TRY(need(h_scale, R, 4));
+  MOE_TRY(need(y_perm, R * h, 16));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  int* err = at<int>(ws, make_layout(c).err);
+  MOE_CUDA(launch_quantize_rows(static_cast<int64_t>(R), c.ffn_hidden, h_mid, h_q, h_scale,
+                                expert_offsets + c.num_experts, stream));
+  MOE_CUDA(launch_tc_fc2_e4m3(c.num_experts, c.hidden, c.ffn_hidden, static_cast<int64_t>(R), h_q,
+                              h_scale, expert_offsets, W2q, s2, y_perm, err, stream));
+  return MOE_OK;
+}
+
+moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* Wg,
+                            const float* gate_bias, const float* expert_bias, const uint8_t* W1q,
+                            const float* s1, const uint8_t* W3q, const float* s3,
+                            const uint8_t* W2q, const float* s2, void* y, int32_t* topk_idx,
+                            float* topk_prob, int32_t* tokens_per_expert, void* ws,
+                            size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_e4m3(c));
+  const size_t T = c.num_tokens, E = c.num_experts, h = c.hidden, f = c.ffn_hidden;
+  const size_t wsz = E * h * f;
+  MOE_TRY(need(x, T * h, 16));
+  MOE_TRY(need(Wg, h * E, 4));
+  MOE_TRY(optional(gate_bias, 4));
+  MOE_TRY(optional(expert_bias, 4));
+  MOE_TRY(need(W1q, wsz, 16));
+  MOE_TRY(need(W3q, wsz, 16));
+  MOE_TRY(need(W2q, wsz, 16));
+  MOE_TRY(need(s1, E * f, 16));
+  MOE_TRY(need(s3, E * f, 16));
+  MOE_TRY(need(s2, E * h, 16));
+  MOE_TRY(need(y, T * h, 16));
+  MOE_TRY(optional(topk_idx, 4));
+  MOE_TRY(optional(topk_prob, 4));
+  MOE_TRY(optional(tokens_per_expert, 4));
+  const E4m3Layout Q = make_e4m3_layout(c);
+  MOE_TRY(check_ws(c, ws, ws_bytes, Q.total));
+  const Layout L = make_layout(c);
+  int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
+  float* prob = topk_prob ? topk_prob : at<float>(ws, L.topk_prob);
+  int32_t* tpe = tokens_per_expert ? tokens_per_expert : at<int32_t>(ws, L.tpe);
+  uint8_t* keep = at<uint8_t>(ws, L.keep);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* row_map = at<int32_t>(ws, L.row_map);
+  uint8_t* xperm_q = at<uint8_t>(ws, Q.xperm_q);
+  float* xperm_s = at<float>(ws, Q.xperm_s);
+  MOE_TRY(do_route(c, x, Wg, gate_bias, expert_bias, idx, prob, keep, tpe, nullptr, ws, stream));
+  MOE_TRY(do_permute_e4m3(c, x, idx, keep, xperm_q, xperm_s, row_map, offsets, ws, stream));
+  MOE_TRY(do_mlp_e4m3(c, xperm_q, xperm_s, offsets, W1q, s1, W3q, s3, W2q, s2,
+                      at<void>(ws, L.h_mid), at<uint8_t>(ws, Q.hq), at<float>(ws, Q.hs),
+                      at<float>(ws, L.y_perm), ws, stream));
+  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, at<float>(ws, L.y_perm),
+                          row_map, prob, nullptr, y, stream));
   return MOE_OK;
 }
 

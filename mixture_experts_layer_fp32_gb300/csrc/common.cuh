@@ -54,6 +54,10 @@ cudaError_t launch_perm_rank(int64_t npairs, int E, const int32_t* topk_idx, con
                              cudaStream_t s);
 cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, const int32_t* row_map,
                              void* x_perm, cudaStream_t s);
+// rows of row_bytes (a multiple of 16); with tok_scale, row_scale[row] = tok_scale[token]
+cudaError_t launch_perm_copy_rows(int T, int row_bytes, int k, const void* x,
+                                  const int32_t* row_map, void* x_perm, const float* tok_scale,
+                                  float* row_scale, cudaStream_t s);
 // y_shared [T, h] fp32 (nullable): the shared expert's output, added last
 cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
                            const int32_t* row_map, const float* topk_prob, const float* y_shared,
@@ -75,6 +79,27 @@ cudaError_t launch_tc_fc1(int E, int h, int f, int64_t max_rows, const void* x_p
 cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_mid,
                           const int32_t* offsets, const void* W2, float* y_perm, int* err,
                           cudaStream_t s);
+
+// E4M3 operands (kind::f8f6f4): xq / hq [rows, K] codes with per-row scales
+// (x's through row_src: row r uses x_scale[row_src[r]]), K-major weights
+// W1q/W3q [E,f,h], W2q [E,h,f] with per-channel scales s1/s3 [E,f], s2 [E,h]
+cudaError_t launch_tc_fc1_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* xq,
+                               const float* x_scale, const int32_t* row_src,
+                               const int32_t* offsets, const uint8_t* W1q, const float* s1,
+                               const uint8_t* W3q, const float* s3, void* h_mid, int* err,
+                               cudaStream_t s);
+cudaError_t launch_tc_fc2_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* hq,
+                               const float* h_scale, const int32_t* offsets, const uint8_t* W2q,
+                               const float* s2, float* y_perm, int* err, cudaStream_t s);
+
+// ---- E4M3 quantisation (FP8 experts) ----
+// rows of bf16 [rows, cols] -> codes + per-row power-of-two scales (rows >=
+// *row_count skipped when row_count is given); cols % 16 == 0
+cudaError_t launch_quantize_rows(int64_t rows, int cols, const void* in, uint8_t* codes,
+                                 float* scales, const int32_t* row_count, cudaStream_t s);
+// W [E][K][N] bf16 -> codes [E][N][K] + per-channel scales [E][N]; K, N % 64 == 0
+cudaError_t launch_quantize_cols(int E, int K, int N, const void* W, uint8_t* codes,
+                                 float* scales, cudaStream_t s);
 
 int device_sm_count();
 

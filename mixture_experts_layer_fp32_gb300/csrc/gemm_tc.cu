@@ -71,6 +71,11 @@ constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 
                            2 * (MOE_MAX_EXPERTS + 1) * 4;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, /*b_mn_major=*/true);
+// E4M3 operands: a stage holds 128 K values (128 bytes per row, the same
+// bytes as 64 bf16), the MMA takes K = 32, and B is K-major (one row of
+// 128 bytes per output channel), 128-row boxes of 16 KB.
+constexpr int KE_FP8 = 128;
+constexpr uint32_t IDESC_F8 = ptx::idesc_e4m3_f32(BM, BN);
 constexpr long long kWaitCycles = 4000000000LL;
 
 enum { FC1 = 0, FC2 = 1 };
@@ -84,6 +89,14 @@ struct TcArgs {
   void* out;
   int ldo;
   int* err;
+  // E4M3 operands only: A row r's scale is row_scale[row_src ? row_src[r] : r];
+  // output channel n of expert e has scale col_scale0[e * ncols + n] (W1 or W2)
+  // and, for fc1's gate half, col_scale1[e * ncols + n] (W3)
+  const float* row_scale = nullptr;
+  const int32_t* row_src = nullptr;
+  const float* col_scale0 = nullptr;
+  const float* col_scale1 = nullptr;
+  int ncols = 0;
 };
 
 // Barriers of an NS-stage ring: full[NS], empty[NS], acc_full[2],
@@ -193,11 +206,17 @@ __device__ __forceinline__ float silu_mul(float a, float g) { return a / (1.0f +
 // `tb` hold rows rbase .. rbase+31 (lane l holds row rbase + l) of a tile of
 // n-tile `nt`; rows at or past `rend` belong to no row of this expert and are
 // not stored.  fc1 applies silu(a) * g and stores bf16, fc2 stores fp32.
-template <int MODE>
+template <int MODE, bool FP8>
 __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, int rbase, int rend,
-                                                  int nt, const TcArgs& args, int lane) {
+                                                  int nt, int e, const TcArgs& args, int lane) {
   const int sub = lane >> 3;
   const int col4 = (lane & 7) * 4;
+  // E4M3: this lane's row scale (rows past the expert's end are not read)
+  float rs = 1.f;
+  if (FP8 && rbase + lane < rend) {
+    const int r = rbase + lane;
+    rs = args.row_scale[args.row_src ? args.row_src[r] : r];
+  }
   if (MODE == FC1) {
     // silu(a) * g, packed to bf16: each lane writes 64 contiguous bytes
     // of its own row per 32-column chunk (whole 32-byte sectors; staging
@@ -213,6 +232,22 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, int
       ptx::tmem_wait_ld();
       if (row < rend) {
         uint4* dst = reinterpret_cast<uint4*>(out + c);
+        if (FP8) {  // acc * row scale * channel scale (W1 half and W3 half)
+          const int64_t cb = static_cast<int64_t>(e) * args.ncols + nt * (BN / 2) + c;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 u = __ldg(reinterpret_cast<const float4*>(args.col_scale0 + cb + j));
+            const float4 v = __ldg(reinterpret_cast<const float4*>(args.col_scale1 + cb + j));
+            a[j] = __float_as_uint(__uint_as_float(a[j]) * (rs * u.x));
+            a[j + 1] = __float_as_uint(__uint_as_float(a[j + 1]) * (rs * u.y));
+            a[j + 2] = __float_as_uint(__uint_as_float(a[j + 2]) * (rs * u.z));
+            a[j + 3] = __float_as_uint(__uint_as_float(a[j + 3]) * (rs * u.w));
+            g[j] = __float_as_uint(__uint_as_float(g[j]) * (rs * v.x));
+            g[j + 1] = __float_as_uint(__uint_as_float(g[j + 1]) * (rs * v.y));
+            g[j + 2] = __float_as_uint(__uint_as_float(g[j + 2]) * (rs * v.z));
+            g[j + 3] = __float_as_uint(__uint_as_float(g[j + 3]) * (rs * v.w));
+          }
+        }
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           uint4 w;
@@ -240,10 +275,22 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, int
       ptx::tmem_ld32(tb + c, y);
       ptx::tmem_wait_ld();
       float4* mine = reinterpret_cast<float4*>(etile + lane * EPI_PITCH);
+      if (FP8) {  // acc * row scale * channel scale
+        const float* cs = args.col_scale0 + static_cast<int64_t>(e) * args.ncols + nt * BN + c;
 #pragma unroll
-      for (int v = 0; v < 8; ++v)
-        mine[v] = make_float4(__uint_as_float(y[4 * v]), __uint_as_float(y[4 * v + 1]),
-                              __uint_as_float(y[4 * v + 2]), __uint_as_float(y[4 * v + 3]));
+        for (int v = 0; v < 8; ++v) {
+          const float4 u = __ldg(reinterpret_cast<const float4*>(cs + 4 * v));
+          mine[v] = make_float4(__uint_as_float(y[4 * v]) * (rs * u.x),
+                                __uint_as_float(y[4 * v + 1]) * (rs * u.y),
+                                __uint_as_float(y[4 * v + 2]) * (rs * u.z),
+                                __uint_as_float(y[4 * v + 3]) * (rs * u.w));
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          mine[v] = make_float4(__uint_as_float(y[4 * v]), __uint_as_float(y[4 * v + 1]),
+                                __uint_as_float(y[4 * v + 2]), __uint_as_float(y[4 * v + 3]));
+      }
       __syncwarp();
 #pragma unroll
       for (int it = 0; it < 8; ++it) {
@@ -258,7 +305,7 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, int
   }
 }
 
-template <int MODE>
+template <int MODE, bool FP8>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB0,
@@ -329,9 +376,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
           const uint32_t a = ptx::smem_u32(stages + stage * STAGE_BYTES);
           const uint32_t b = a + A_BYTES;
-          const int kc = kb * BK;
+          const int kc = kb * (FP8 ? KE_FP8 : BK);
           ptx::tma_load_2d(a, &tmA, kc, m0, fb);
-          if (MODE == FC1) {
+          if (FP8) {
+            // K-major weight rows: two boxes of 128 output channels x 128 K
+            const int n0 = MODE == FC1 ? nt * (BN / 2) : nt * BN;
+            ptx::tma_load_3d(b, &tmB0, kc, n0, e, fb);
+            if (MODE == FC1)
+              ptx::tma_load_3d(b + 2 * BOX_BYTES, &tmB1, kc, n0, e, fb);
+            else
+              ptx::tma_load_3d(b + 2 * BOX_BYTES, &tmB0, kc, n0 + BN / 2, e, fb);
+          } else if (MODE == FC1) {
             const int n0 = nt * (BN / 2);
             ptx::tma_load_3d(b, &tmB0, n0, kc, e, fb);
             ptx::tma_load_3d(b + BOX_BYTES, &tmB0, n0 + 64, kc, e, fb);
@@ -390,6 +445,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           ptx::tc_fence_after();
           const uint32_t a = ptx::smem_u32(stages + stage * STAGE_BYTES);
           const uint32_t b = a + A_BYTES;
+          if (FP8) {
+            // A and B both K-major, 128-byte swizzled rows, 8-row groups 1 KB
+            // apart; a K step of 32 E4M3 values moves 32 B inside the row.
+#pragma unroll
+            for (int s = 0; s < KE_FP8 / 32; ++s) {
+              const uint64_t adesc = ptx::smem_desc(a + s * 32, 16, 1024, ptx::kLayoutSw128);
+              const uint64_t bdesc = ptx::smem_desc(b + s * 32, 16, 1024, ptx::kLayoutSw128);
+              ptx::umma_e4m3(d, adesc, bdesc, IDESC_F8, (kb | s) != 0 ? 1u : 0u);
+            }
+          } else {
 #pragma unroll
           for (int s = 0; s < BK / 16; ++s) {
             // A: K-major, rows of BK bf16 (64 or 128 bytes) with the matching
@@ -401,6 +466,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t adesc = ptx::smem_desc(a + s * 32, 16, A_SBO, A_LAYOUT);
             const uint64_t bdesc = ptx::sw128_desc(b + s * 2048, BOX_BYTES, 1024);
             ptx::umma_bf16(d, adesc, bdesc, IDESC, (kb | s) != 0 ? 1u : 0u);
+          }
           }
           ptx::umma_commit(ctl.empty(stage));
           if (++stage == STAGES) {
@@ -432,7 +498,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
       float* etile = epi + q * (32 * EPI_PITCH);  // this warp's staging tile
       const int rbase = m0 + q * 32;  // this warp's first row; lane l holds row rbase + l
-      drain_accumulator<MODE>(tb, etile, rbase, rend, nt, args, lane);
+      drain_accumulator<MODE, FP8>(tb, etile, rbase, rend, nt, e, args, lane);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ctl.acc_empty(buf));
@@ -473,12 +539,13 @@ constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + EPI_BYTES + P_NUM
 static_assert(P_SMEM_BYTES <= SMEM_BUDGET, "shared memory budget (pair)");
 static_assert(P_STAGES <= 32, "stage bit masks");
 constexpr uint32_t P_IDESC = ptx::idesc_bf16_f32(PM, BN, /*b_mn_major=*/true);
+constexpr uint32_t P_IDESC_F8 = ptx::idesc_e4m3_f32(PM, BN);
 // Bounded pause that lets a CTA's own in-flight copies land when it gives up
 // (their completion is counted on the other CTA's barrier).
 constexpr long long kPeerDrainCycles = 20000000LL;
 using PairCtl = CtlN<P_STAGES>;
 
-template <int MODE>
+template <int MODE, bool FP8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB0,
@@ -558,10 +625,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t fb = ptx::mapa_shared(ctl.full(stage), 0);
           const uint32_t a = ptx::smem_u32(stages + stage * P_STAGE_BYTES);
           const uint32_t b = a + A_BYTES;
-          const int kc = kb * BK;
+          const int kc = kb * (FP8 ? KE_FP8 : BK);
           ptx::tma_load_2d_pair(a, &tmA, kc, a_row, fb);
-          ptx::tma_load_3d_pair(b, tmB, n0, kc, e, fb);
-          ptx::tma_load_3d_pair(b + BOX_BYTES, tmB, n0 + 64, kc, e, fb);
+          if (FP8) {
+            // K-major weight rows: one box of this CTA's 128 output channels x 128 K
+            ptx::tma_load_3d_pair(b, tmB, kc, n0, e, fb);
+          } else {
+            ptx::tma_load_3d_pair(b, tmB, n0, kc, e, fb);
+            ptx::tma_load_3d_pair(b + BOX_BYTES, tmB, n0 + 64, kc, e, fb);
+          }
           filled |= 1u << stage;
           fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == P_STAGES) {
@@ -612,14 +684,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           ptx::tc_fence_after();
           const uint32_t a = ptx::smem_u32(stages + stage * P_STAGE_BYTES);
           const uint32_t b = a + A_BYTES;
+          if (FP8) {
+            // both operands K-major (128-byte rows), K = 32 per MMA
 #pragma unroll
-          for (int s = 0; s < BK / 16; ++s) {
-            // same descriptors as the one-SM kernel, read at the same
-            // offsets in both CTAs' shared memories; B has two 64-column
-            // boxes per CTA
-            const uint64_t adesc = ptx::smem_desc(a + s * 32, 16, A_SBO, A_LAYOUT);
-            const uint64_t bdesc = ptx::sw128_desc(b + s * 2048, BOX_BYTES, 1024);
-            ptx::umma_bf16_pair(d, adesc, bdesc, P_IDESC, (kb | s) != 0 ? 1u : 0u);
+            for (int s = 0; s < KE_FP8 / 32; ++s) {
+              const uint64_t adesc = ptx::smem_desc(a + s * 32, 16, 1024, ptx::kLayoutSw128);
+              const uint64_t bdesc = ptx::smem_desc(b + s * 32, 16, 1024, ptx::kLayoutSw128);
+              ptx::umma_e4m3_pair(d, adesc, bdesc, P_IDESC_F8, (kb | s) != 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int s = 0; s < BK / 16; ++s) {
+              // same descriptors as the one-SM kernel, read at the same
+              // offsets in both CTAs' shared memories; B has two 64-column
+              // boxes per CTA
+              const uint64_t adesc = ptx::smem_desc(a + s * 32, 16, A_SBO, A_LAYOUT);
+              const uint64_t bdesc = ptx::sw128_desc(b + s * 2048, BOX_BYTES, 1024);
+              ptx::umma_bf16_pair(d, adesc, bdesc, P_IDESC, (kb | s) != 0 ? 1u : 0u);
+            }
           }
           ptx::umma_commit_pair(ctl.empty(stage), 3);
           if (++stage == P_STAGES) {
@@ -651,7 +733,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
       float* etile = epi + q * (32 * EPI_PITCH);
       const int rbase = m0 + static_cast<int>(rank) * BM + q * 32;
-      drain_accumulator<MODE>(tb, etile, rbase, rend, nt, args, lane);
+      drain_accumulator<MODE, FP8>(tb, etile, rbase, rend, nt, e, args, lane);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ctl.acc_empty(buf), 0));
@@ -713,7 +795,33 @@ bool map_weights(CUtensorMap* m, const void* ptr, int64_t N, int64_t K, int64_t 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
+// E4M3 maps: activations [rows, K] bytes, box 128 (K) x 128 (rows); K-major
+// weights [E, N, K] bytes, box 128 (K) x 128 (N) x 1; both 128-byte swizzle.
+bool map_rows_e4m3(CUtensorMap* m, const void* ptr, int64_t K, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  cuuint32_t box[2] = {KE_FP8, BM};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool map_weights_e4m3(CUtensorMap* m, const void* ptr, int64_t K, int64_t N, int64_t E) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(E)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N * K)};
+  cuuint32_t box[3] = {KE_FP8, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE, bool FP8>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                       const TcArgs& args, cudaStream_t s) {
   static bool configured[64] = {false};
@@ -721,8 +829,8 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   cudaError_t st = cudaGetDevice(&dev);
   if (st != cudaSuccess) return st;
   if (dev < 64 && !configured[dev]) {
-    st = cudaFuncSetAttribute(tc_grouped_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SMEM_BYTES);
+    st = cudaFuncSetAttribute(tc_grouped_kernel<MODE, FP8>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (st != cudaSuccess) return st;
     configured[dev] = true;
   }
@@ -730,13 +838,14 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   int64_t grid = device_sm_count();
   if (grid > max_tiles) grid = max_tiles;
   if (grid <= 0) return cudaSuccess;
-  tc_grouped_kernel<MODE><<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, s>>>(a, b0, b1, args);
+  tc_grouped_kernel<MODE, FP8><<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, s>>>(a, b0, b1,
+                                                                                     args);
   return cudaGetLastError();
 }
 
 // Pairs of SMs that can be resident at once for the pair kernel (0: none, or
 // the query failed).
-template <int MODE>
+template <int MODE, bool FP8>
 int pair_slots() {
   static int cache[64] = {0};  // per device; -1 = queried, unusable
   int dev = 0;
@@ -747,10 +856,11 @@ int pair_slots() {
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = P_SMEM_BYTES;
-    if (cudaFuncSetAttribute(tc_grouped_pair_kernel<MODE>,
+    if (cudaFuncSetAttribute(tc_grouped_pair_kernel<MODE, FP8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              P_SMEM_BYTES) != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&n, tc_grouped_pair_kernel<MODE>, &cfg) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, tc_grouped_pair_kernel<MODE, FP8>, &cfg) !=
+            cudaSuccess ||
         n <= 0) {
       cudaGetLastError();  // clear a failed query; the one-SM kernel is used instead
       n = -1;
@@ -760,14 +870,14 @@ int pair_slots() {
   return cache[dev] > 0 ? cache[dev] : 0;
 }
 
-template <int MODE>
+template <int MODE, bool FP8>
 cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                            const TcArgs& args, int slots, cudaStream_t s) {
   const int64_t max_tiles = ((args.max_rows + PM - 1) / PM + args.E) * args.num_n_tiles;
   int64_t pairs = slots;
   if (pairs > max_tiles) pairs = max_tiles;
   if (pairs <= 0) return cudaSuccess;
-  tc_grouped_pair_kernel<MODE><<<static_cast<unsigned>(2 * pairs), THREADS, P_SMEM_BYTES, s>>>(
+  tc_grouped_pair_kernel<MODE, FP8><<<static_cast<unsigned>(2 * pairs), THREADS, P_SMEM_BYTES, s>>>(
       a, b0, b1, args);
   return cudaGetLastError();
 }
@@ -778,7 +888,7 @@ cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b0, const CU
 // the environment forces one kernel or the other (a tuning override).
 constexpr int64_t kPairMinRows = 768;
 
-template <int MODE>
+template <int MODE, bool FP8>
 cudaError_t launch_grouped(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                            const TcArgs& args, cudaStream_t s) {
   const char* force = getenv("MOE_TC_PAIR");
@@ -786,10 +896,10 @@ cudaError_t launch_grouped(const CUtensorMap& a, const CUtensorMap& b0, const CU
   if (force && force[0] == '0') pair = false;
   if (force && force[0] == '1') pair = true;
   if (pair) {
-    const int slots = pair_slots<MODE>();
-    if (slots > 0) return launch_tc_pair<MODE>(a, b0, b1, args, slots, s);
+    const int slots = pair_slots<MODE, FP8>();
+    if (slots > 0) return launch_tc_pair<MODE, FP8>(a, b0, b1, args, slots, s);
   }
-  return launch_tc<MODE>(a, b0, b1, args, s);
+  return launch_tc<MODE, FP8>(a, b0, b1, args, s);
 }
 
 }  // namespace
@@ -803,7 +913,7 @@ cudaError_t launch_tc_fc1(int E, int h, int f, int64_t max_rows, const void* x_p
       !map_weights(&b1, W3, f, h, E))
     return cudaErrorInvalidValue;
   TcArgs args{offsets, E, f / (BN / 2), h / BK, max_rows, h_mid, f, err};
-  return launch_grouped<FC1>(a, b0, b1, args, s);
+  return launch_grouped<FC1, false>(a, b0, b1, args, s);
 }
 
 cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_mid,
@@ -814,7 +924,40 @@ cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_m
   if (!map_rows(&a, h_mid, f, max_rows) || !map_weights(&b0, W2, h, f, E))
     return cudaErrorInvalidValue;
   TcArgs args{offsets, E, h / BN, f / BK, max_rows, y_perm, h, err};
-  return launch_grouped<FC2>(a, b0, b0, args, s);
+  return launch_grouped<FC2, false>(a, b0, b0, args, s);
+}
+
+cudaError_t launch_tc_fc1_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* xq,
+                               const float* x_scale, const int32_t* row_src,
+                               const int32_t* offsets, const uint8_t* W1q, const float* s1,
+                               const uint8_t* W3q, const float* s3, void* h_mid, int* err,
+                               cudaStream_t s) {
+  if (max_rows == 0) return cudaSuccess;
+  CUtensorMap a, b0, b1;
+  if (!map_rows_e4m3(&a, xq, h, max_rows) || !map_weights_e4m3(&b0, W1q, h, f, E) ||
+      !map_weights_e4m3(&b1, W3q, h, f, E))
+    return cudaErrorInvalidValue;
+  TcArgs args{offsets, E, f / (BN / 2), h / KE_FP8, max_rows, h_mid, f, err};
+  args.row_scale = x_scale;
+  args.row_src = row_src;
+  args.col_scale0 = s1;
+  args.col_scale1 = s3;
+  args.ncols = f;
+  return launch_grouped<FC1, true>(a, b0, b1, args, s);
+}
+
+cudaError_t launch_tc_fc2_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* hq,
+                               const float* h_scale, const int32_t* offsets, const uint8_t* W2q,
+                               const float* s2, float* y_perm, int* err, cudaStream_t s) {
+  if (max_rows == 0) return cudaSuccess;
+  CUtensorMap a, b0;
+  if (!map_rows_e4m3(&a, hq, f, max_rows) || !map_weights_e4m3(&b0, W2q, f, h, E))
+    return cudaErrorInvalidValue;
+  TcArgs args{offsets, E, h / BN, f / KE_FP8, max_rows, y_perm, h, err};
+  args.row_scale = h_scale;
+  args.col_scale0 = s2;
+  args.ncols = h;
+  return launch_grouped<FC2, true>(a, b0, b0, args, s);
 }
 
 }  // namespace moe

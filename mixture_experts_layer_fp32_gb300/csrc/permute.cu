@@ -162,13 +162,17 @@ constexpr int kCopyThreads = 128;
 constexpr int kCopyUnroll = 4;
 
 // x_perm[row_map[t, j]] = x[t] for every kept slot j; 16-byte vectors.
+// With token scales (E4M3 rows), row_scale[row_map[t, j]] = tok_scale[t] too.
 __global__ void __launch_bounds__(kCopyThreads)
     perm_copy_kernel(int T, int row_vecs, int k, const uint4* __restrict__ x,
-                     const int32_t* __restrict__ row_map, uint4* __restrict__ x_perm) {
+                     const int32_t* __restrict__ row_map, uint4* __restrict__ x_perm,
+                     const float* __restrict__ tok_scale, float* __restrict__ row_scale) {
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     int rows[MOE_MAX_TOPK];
 #pragma unroll
     for (int j = 0; j < MOE_MAX_TOPK; ++j) rows[j] = (j < k) ? row_map[(int64_t)t * k + j] : -1;
+    if (tok_scale && threadIdx.x < k && rows[threadIdx.x] >= 0)
+      row_scale[rows[threadIdx.x]] = tok_scale[t];
     const uint4* src = x + (int64_t)t * row_vecs;
     for (int v0 = threadIdx.x; v0 < row_vecs; v0 += kCopyThreads * kCopyUnroll) {
       uint4 buf[kCopyUnroll];
@@ -284,10 +288,17 @@ cudaError_t launch_perm_rank(int64_t npairs, int E, const int32_t* topk_idx, con
 
 cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, const int32_t* row_map,
                              void* x_perm, cudaStream_t s) {
+  return launch_perm_copy_rows(T, h * (dtype == MOE_F32 ? 4 : 2), k, x, row_map, x_perm, nullptr,
+                               nullptr, s);
+}
+
+cudaError_t launch_perm_copy_rows(int T, int row_bytes, int k, const void* x,
+                                  const int32_t* row_map, void* x_perm, const float* tok_scale,
+                                  float* row_scale, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int row_vecs = h * (dtype == MOE_F32 ? 4 : 2) / 16;
   perm_copy_kernel<<<grid_for_tokens(T, 16), kCopyThreads, 0, s>>>(
-      T, row_vecs, k, static_cast<const uint4*>(x), row_map, static_cast<uint4*>(x_perm));
+      T, row_bytes / 16, k, static_cast<const uint4*>(x), row_map, static_cast<uint4*>(x_perm),
+      tok_scale, row_scale);
   return cudaGetLastError();
 }
 

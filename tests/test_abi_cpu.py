@@ -218,3 +218,19 @@ def test_forward_host_host_checks(moe):
     assert call(2, FAKE, 0, FAKE, row - 2, need) == INVALID     # output batches overlap
     assert call(2, FAKE, row, FAKE, row, need - 1) == WORKSPACE  # routed ws is not enough
     assert call(0, FAKE, 0, FAKE, 0, need) == OK                 # nothing to do, nothing enqueued
+
+
+def _declared_arg_counts():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(moe_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_header(moe):
+    counts = _declared_arg_counts()
+    lib = moe.lib()
+    for name in moe.EXPORTS:
+        assert len(getattr(lib, name).argtypes) == counts[name], name

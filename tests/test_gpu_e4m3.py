@@ -1,0 +1,189 @@
+"""The FP8 (E4M3) expert path against the oracle's FP8 arithmetic.
+
+Bit-exact: the quantisers (per-row codes and power-of-two scales of x and
+of bf16 matrices with crafted rounding ties; per-channel K-major codes of
+the expert weights), the routing, the permutation and the permuted code
+rows.  Within tolerance: the bf16 SwiGLU output (one bf16 ulp), its E4M3
+codes (equal up to rare one-code flips where GPU and oracle round the
+SwiGLU output differently), y_perm and y (2e-2 of the RMS beyond the
+output's own rounding).  Both tensor-core GEMM kernels are forced on the
+same cases; moe_forward_e4m3 reproduces the staged calls bit for bit.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from moe_cases import (assert_close, assert_equal, assert_probs, gpu_config, make_case, np_view,
+                       to_dev, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return np_view(t.detach().cpu())
+
+
+def _gpu_quantize_rows(x):
+    import mixture_experts_layer_fp32_gb300 as moe
+    codes = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+    scales = torch.empty((x.shape[0],), dtype=torch.float32, device="cuda")
+    moe.quantize_rows_e4m3(x.cuda().contiguous(), codes, scales)
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), scales.cpu().numpy()
+
+
+def test_quantize_rows_bit_exact_with_ties_and_ranges():
+    r = np.random.default_rng(130)
+    x = (r.standard_normal((300, 512)) * np.exp(r.uniform(-30, 30, (300, 1)))).astype(np.float32)
+    x[0] = 0.0
+    x[1, :] = 2.0 ** -105                      # below 2^-100: scale 1
+    # rounding ties in E4M3 (midpoints of neighbouring codes) at scale 1
+    mids = np.array([1.0625, 1.1875, 3 * 2.0 ** -10, 2.0 ** -10, 13.5, 240.0, 208.0, 448.0])
+    x[2, :mids.size] = mids
+    x[2, mids.size:] = 0.5
+    x[3, :mids.size] = -mids
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    codes, scales = _gpu_quantize_rows(xb)
+    want_c, want_s = oracle.quantize_rows_e4m3(_bits(xb))
+    assert_equal("codes", codes, want_c)
+    assert_equal("scales", scales.view(np.uint32), want_s.view(np.uint32))
+
+
+def test_quantize_experts_bit_exact():
+    import mixture_experts_layer_fp32_gb300 as moe
+    w = synthetic.scaled("mixtral", T=16, h=512, f=384, E=3, seed=131)
+    inp = synthetic.generate(w)
+    inp["W2"][1, 7, :] *= 1e3                   # a channel with a far larger range
+    cfg = gpu_config(w)
+    q = moe.E4m3Experts(cfg, inp["W1"].cuda(), inp["W3"].cuda(), inp["W2"].cuda())
+    torch.cuda.synchronize()
+    want = oracle.quantize_experts_e4m3(_bits(inp["W1"]), _bits(inp["W3"]), _bits(inp["W2"]))
+    for n in ("W1q", "W3q", "W2q"):
+        assert_equal(n, getattr(q, n).cpu().numpy(), want[n])
+    for n in ("s1", "s3", "s2"):
+        assert_equal(n, getattr(q, n).cpu().numpy().view(np.uint32), want[n].view(np.uint32))
+
+
+CASES = {
+    "mixtral_e4": synthetic.scaled("mixtral", T=1200, h=512, f=384, E=4, seed=132),
+    "qwen3_sparse": synthetic.scaled("qwen3", T=300, h=256, f=256, seed=133),
+    "switch_drop": synthetic.scaled("switch", T=2048, h=256, f=256, seed=134),
+    "dsv3_grouped": synthetic.scaled("dsv3_grouped", T=400, h=512, f=256, E=64, seed=135),
+}
+
+
+def oracle_forward_e4m3(w, inp):
+    q = oracle.quantize_experts_e4m3(_bits(inp["W1"]), _bits(inp["W3"]), _bits(inp["W2"]))
+    return oracle.forward_fp8(_bits(inp["x"]), _bits(inp["Wg"]), q, w.k, w.score,
+                              np_view(inp["gate_bias"]), np_view(inp["expert_bias"]),
+                              w.capacity_factor, w.min_capacity, w.drop_policy,
+                              num_groups=w.num_groups, group_topk=w.group_topk)
+
+
+def gpu_stages_e4m3(w, d):
+    import mixture_experts_layer_fp32_gb300 as moe
+    cfg = gpu_config(w)
+    b = moe.Buffers(cfg)
+    ws = moe.alloc_workspace_e4m3(cfg)
+    q = moe.E4m3Experts(cfg, d["W1"], d["W3"], d["W2"])
+    R = w.T * w.k
+    b.x_perm_q = torch.empty((R, w.h), dtype=torch.uint8, device="cuda")
+    b.x_perm_s = torch.empty((R,), dtype=torch.float32, device="cuda")
+    b.h_q = torch.empty((R, w.f), dtype=torch.uint8, device="cuda")
+    b.h_s = torch.empty((R,), dtype=torch.float32, device="cuda")
+    moe.route(cfg, d["x"], d["Wg"], d["gate_bias"], d["expert_bias"], b.topk_idx, b.topk_prob,
+              b.keep, b.tokens_per_expert, None, ws)
+    moe.permute_e4m3(cfg, d["x"], b.topk_idx, b.keep, b.x_perm_q, b.x_perm_s, b.row_map,
+                     b.expert_offsets, ws)
+    moe.grouped_mlp_e4m3(cfg, b.x_perm_q, b.x_perm_s, b.expert_offsets, q, b.h_mid, b.h_q,
+                         b.h_s, b.y_perm, ws)
+    moe.combine(cfg, b.y_perm, b.row_map, b.topk_prob, b.y)
+    moe.check(ws)
+    b.q, b.ws_e4m3 = q, ws
+    return b
+
+
+@pytest.fixture(scope="module", params=sorted(CASES))
+def case(request):
+    w = CASES[request.param]
+    inp, _ = make_case(w)
+    ref = oracle_forward_e4m3(w, inp)
+    return w, inp, ref, to_dev(inp)
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_e4m3_layer_matches_oracle(case, kernel, monkeypatch):
+    w, inp, ref, d = case
+    monkeypatch.setenv("MOE_TC_PAIR", "1" if kernel == "pair" else "0")
+    b = gpu_stages_e4m3(w, d)
+    torch.cuda.synchronize()
+    assert_equal("topk_idx", to_np(b.topk_idx), ref["topk_idx"])
+    assert_equal("keep", to_np(b.keep), ref["keep"])
+    assert_probs(to_np(b.topk_prob), ref["topk_prob"])
+    assert_equal("expert_offsets", to_np(b.expert_offsets), ref["offsets"])
+    assert_equal("row_map", to_np(b.row_map), ref["row_map"])
+    R = int(ref["offsets"][-1])
+    assert_equal("x_perm_q", to_np(b.x_perm_q[:R]), ref["xq"][ref["row_token"]])
+    assert_equal("x_perm_scale", to_np(b.x_perm_s[:R]).view(np.uint32),
+                 ref["xs"][ref["row_token"]].view(np.uint32))
+    assert_close("h_mid", to_np(b.h_mid[:R]), ref["h_mid"], "bf16_stored")
+    hq = to_np(b.h_q[:R]).astype(np.int32)
+    diff = hq != ref["hq"].astype(np.int32)
+    assert diff.mean() < 2e-3, diff.mean()
+    if diff.any():  # only neighbouring codes, and only where the row scales agree
+        same_scale = to_np(b.h_s[:R]) == ref["hs"]
+        d_rows = np.nonzero(diff)[0]
+        assert np.all(np.abs(hq - ref["hq"].astype(np.int32))[diff][same_scale[d_rows]] == 1)
+    assert_close("y_perm", to_np(b.y_perm[:R]), ref["y_perm"], "bf16")
+    assert_close("y", to_np(b.y), ref["y"], w.dtype)
+
+
+def test_e4m3_forward_reproduces_stages(case):
+    import mixture_experts_layer_fp32_gb300 as moe
+    w, inp, ref, d = case
+    b = gpu_stages_e4m3(w, d)
+    cfg = gpu_config(w)
+    ws = moe.alloc_workspace_e4m3(cfg)
+    y = torch.empty_like(b.y)
+    idx = torch.empty_like(b.topk_idx)
+    moe.forward_e4m3(cfg, d["x"], d["Wg"], d["gate_bias"], d["expert_bias"], b.q, y, ws, idx)
+    moe.check(ws)
+    assert torch.equal(idx, b.topk_idx)
+    assert torch.equal(y, b.y)
+
+
+def test_e4m3_close_to_the_bf16_layer(case):
+    # quantisation error of the whole layer against the unquantised oracle
+    w, inp, ref, d = case
+    from moe_cases import oracle_forward
+    exact = oracle_forward(w, inp)
+    rel = np.sqrt(np.mean((ref["y"] - exact["y"]) ** 2) / np.mean(exact["y"] ** 2))
+    assert rel < 0.1, rel
+
+
+def test_e4m3_rejects_fp32_config():
+    import mixture_experts_layer_fp32_gb300 as moe
+    cfg = moe.config(T=16, h=256, E=4, k=2, f=128, dtype="f32")
+    with pytest.raises(moe.MoeError):
+        moe.workspace_size_e4m3(cfg)
+
+
+def test_e4m3_stage_halves_equal_grouped_mlp(case):
+    import mixture_experts_layer_fp32_gb300 as moe
+    w, inp, ref, d = case
+    b = gpu_stages_e4m3(w, d)
+    cfg = gpu_config(w)
+    h_mid = torch.empty_like(b.h_mid)
+    h_q = torch.empty_like(b.h_q)
+    h_s = torch.empty_like(b.h_s)
+    y_perm = torch.empty_like(b.y_perm)
+    moe.grouped_fc1_e4m3(cfg, b.x_perm_q, b.x_perm_s, b.expert_offsets, b.q, h_mid, b.ws_e4m3)
+    moe.grouped_fc2_e4m3(cfg, h_mid, b.expert_offsets, b.q, h_q, h_s, y_perm, b.ws_e4m3)
+    moe.check(b.ws_e4m3)
+    R = int(ref["offsets"][-1])
+    assert torch.equal(h_mid[:R], b.h_mid[:R])
+    assert torch.equal(h_q[:R], b.h_q[:R])
+    assert torch.equal(y_perm[:R], b.y_perm[:R])
