@@ -335,10 +335,10 @@ moe_status side_stream(SideStream** out) {
 }
 
 // FP8 (E4M3) workspace: the routed layout (its h_mid holds the bf16 SwiGLU
-// output), then x codes [T,h] and token scales [T], the permuted codes
-// [T*k,h] and their row scales [T*k], the SwiGLU codes [T*k,f] and scales.
+// output), then the permuted codes [T*k,h] and their row scales [T*k], the
+// SwiGLU codes [T*k,f] and scales.
 struct E4m3Layout {
-  size_t xq, xs, xperm_q, xperm_s, hq, hs, total;
+  size_t xperm_q, xperm_s, hq, hs, total;
 };
 E4m3Layout make_e4m3_layout(const moe_config& c) {
   E4m3Layout Q;
@@ -349,8 +349,6 @@ E4m3Layout make_e4m3_layout(const moe_config& c) {
     o = align_up(o + bytes);
     return r;
   };
-  Q.xq = take(T * h);
-  Q.xs = take(T * 4);
   Q.xperm_q = take(np * h);
   Q.xperm_s = take(np * 4);
   Q.hq = take(np * f);
@@ -368,7 +366,6 @@ moe_status do_permute_e4m3(const moe_config& c, const void* x, const int32_t* to
                            const uint8_t* keep, uint8_t* xperm_q, float* xperm_s,
                            int32_t* row_map, int32_t* offsets, void* ws, cudaStream_t s) {
   const Layout L = make_layout(c);
-  const E4m3Layout Q = make_e4m3_layout(c);
   const int T = c.num_tokens, E = c.num_experts, k = c.topk;
   int* err = at<int>(ws, L.err);
   const int64_t np = static_cast<int64_t>(T) * k;
@@ -376,14 +373,11 @@ moe_status do_permute_e4m3(const moe_config& c, const void* x, const int32_t* to
     MOE_CUDA(cudaMemsetAsync(offsets, 0, (E + 1) * sizeof(int32_t), s));
     return MOE_OK;
   }
-  uint8_t* xq = at<uint8_t>(ws, Q.xq);
-  float* xs = at<float>(ws, Q.xs);
-  MOE_CUDA(launch_quantize_rows(T, c.hidden, x, xq, xs, nullptr, s));
   int32_t* tiles = at<int32_t>(ws, L.tiles);
   MOE_CUDA(launch_perm_hist(np, E, topk_idx, keep, tiles, err, s));
   MOE_CUDA(launch_perm_scan(perm_tiles(np), E, tiles, offsets, nullptr, s));
   MOE_CUDA(launch_perm_rank(np, E, topk_idx, keep, tiles, row_map, nullptr, s));
-  MOE_CUDA(launch_perm_copy_rows(T, c.hidden, k, xq, row_map, xperm_q, xs, xperm_s, s));
+  MOE_CUDA(launch_perm_copy_e4m3(T, c.hidden, k, x, row_map, xperm_q, xperm_s, s));
   return MOE_OK;
 }
 

@@ -54,10 +54,10 @@ cudaError_t launch_perm_rank(int64_t npairs, int E, const int32_t* topk_idx, con
                              cudaStream_t s);
 cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, const int32_t* row_map,
                              void* x_perm, cudaStream_t s);
-// rows of row_bytes (a multiple of 16); with tok_scale, row_scale[row] = tok_scale[token]
-cudaError_t launch_perm_copy_rows(int T, int row_bytes, int k, const void* x,
-                                  const int32_t* row_map, void* x_perm, const float* tok_scale,
-                                  float* row_scale, cudaStream_t s);
+// E4M3 rows: x bf16 [T,h] quantised per token on the way; codes and the
+// token's scale go to each kept row
+cudaError_t launch_perm_copy_e4m3(int T, int h, int k, const void* x, const int32_t* row_map,
+                                  uint8_t* x_perm_q, float* row_scale, cudaStream_t s);
 // y_shared [T, h] fp32 (nullable): the shared expert's output, added last
 cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
                            const int32_t* row_map, const float* topk_prob, const float* y_shared,

@@ -12,6 +12,8 @@
 //                     (warp match_any + per-warp counts) -> row_map
 //   perm_copy_kernel  per token: read the x row once (16-byte vectors),
 //                     write it to each of its kept rows
+//   perm_copy_e4m3_kernel  the same for E4M3 rows: the token's row is
+//                     quantised once (power-of-two scale) on the way
 //
 // Combine, after §2 (combine) of the Megatron Core page and step 8 of §8 of
 // the DeepSpeed page (unpermute, weight by the router probabilities):
@@ -19,6 +21,7 @@
 //                     slot order, plus the shared expert's row when there is
 //                     one, one rounding to the output dtype
 #include "common.cuh"
+#include "e4m3.cuh"
 
 namespace moe {
 namespace {
@@ -162,17 +165,13 @@ constexpr int kCopyThreads = 128;
 constexpr int kCopyUnroll = 4;
 
 // x_perm[row_map[t, j]] = x[t] for every kept slot j; 16-byte vectors.
-// With token scales (E4M3 rows), row_scale[row_map[t, j]] = tok_scale[t] too.
 __global__ void __launch_bounds__(kCopyThreads)
     perm_copy_kernel(int T, int row_vecs, int k, const uint4* __restrict__ x,
-                     const int32_t* __restrict__ row_map, uint4* __restrict__ x_perm,
-                     const float* __restrict__ tok_scale, float* __restrict__ row_scale) {
+                     const int32_t* __restrict__ row_map, uint4* __restrict__ x_perm) {
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     int rows[MOE_MAX_TOPK];
 #pragma unroll
     for (int j = 0; j < MOE_MAX_TOPK; ++j) rows[j] = (j < k) ? row_map[(int64_t)t * k + j] : -1;
-    if (tok_scale && threadIdx.x < k && rows[threadIdx.x] >= 0)
-      row_scale[rows[threadIdx.x]] = tok_scale[t];
     const uint4* src = x + (int64_t)t * row_vecs;
     for (int v0 = threadIdx.x; v0 < row_vecs; v0 += kCopyThreads * kCopyUnroll) {
       uint4 buf[kCopyUnroll];
@@ -191,6 +190,45 @@ __global__ void __launch_bounds__(kCopyThreads)
           if (v < row_vecs) dst[v] = buf[u];
         }
       }
+    }
+  }
+}
+
+// E4M3 rows (FP8 experts): the token's bf16 row is reduced to its largest
+// magnitude, converted once to E4M3 with the row's power-of-two scale, and
+// the codes go to each kept row together with the scale.  h % 16 == 0.
+__global__ void __launch_bounds__(kCopyThreads)
+    perm_copy_e4m3_kernel(int T, int h, int k, const uint4* __restrict__ x,
+                          const int32_t* __restrict__ row_map, uint8_t* __restrict__ x_perm_q,
+                          float* __restrict__ row_scale) {
+  __shared__ float red[kCopyThreads / 32];
+  const int groups = h / 16;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    int rows[MOE_MAX_TOPK];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) rows[j] = (j < k) ? row_map[(int64_t)t * k + j] : -1;
+    const uint4* src = x + (int64_t)t * (h / 8);
+    float m = 0.f;
+    for (int g = threadIdx.x; g < groups; g += kCopyThreads)
+      m = e4m3::amax_bf16x8(src[2 * g + 1], e4m3::amax_bf16x8(src[2 * g], m));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < kCopyThreads / 32; ++w) m = fmaxf(m, red[w]);
+    __syncthreads();  // red is rewritten for the next token
+    const int e = e4m3::scale_exp(m);
+    const float inv = e4m3::pow2f(-e);
+    if (threadIdx.x < k && rows[threadIdx.x] >= 0) row_scale[rows[threadIdx.x]] = e4m3::pow2f(e);
+    for (int g = threadIdx.x; g < groups; g += kCopyThreads) {
+      const uint4 c = e4m3::quantize16(src[2 * g], src[2 * g + 1], inv);
+#pragma unroll
+      for (int j = 0; j < MOE_MAX_TOPK; ++j)
+        if (rows[j] >= 0)
+          *reinterpret_cast<uint4*>(x_perm_q + (int64_t)rows[j] * h + 16 * g) = c;
     }
   }
 }
@@ -288,17 +326,18 @@ cudaError_t launch_perm_rank(int64_t npairs, int E, const int32_t* topk_idx, con
 
 cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, const int32_t* row_map,
                              void* x_perm, cudaStream_t s) {
-  return launch_perm_copy_rows(T, h * (dtype == MOE_F32 ? 4 : 2), k, x, row_map, x_perm, nullptr,
-                               nullptr, s);
+  if (T == 0) return cudaSuccess;
+  const int row_vecs = h * (dtype == MOE_F32 ? 4 : 2) / 16;
+  perm_copy_kernel<<<grid_for_tokens(T, 16), kCopyThreads, 0, s>>>(
+      T, row_vecs, k, static_cast<const uint4*>(x), row_map, static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
 }
 
-cudaError_t launch_perm_copy_rows(int T, int row_bytes, int k, const void* x,
-                                  const int32_t* row_map, void* x_perm, const float* tok_scale,
-                                  float* row_scale, cudaStream_t s) {
+cudaError_t launch_perm_copy_e4m3(int T, int h, int k, const void* x, const int32_t* row_map,
+                                  uint8_t* x_perm_q, float* row_scale, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  perm_copy_kernel<<<grid_for_tokens(T, 16), kCopyThreads, 0, s>>>(
-      T, row_bytes / 16, k, static_cast<const uint4*>(x), row_map, static_cast<uint4*>(x_perm),
-      tok_scale, row_scale);
+  perm_copy_e4m3_kernel<<<grid_for_tokens(T, 16), kCopyThreads, 0, s>>>(
+      T, h, k, static_cast<const uint4*>(x), row_map, x_perm_q, row_scale);
   return cudaGetLastError();
 }
 

@@ -7,110 +7,108 @@
 // are round-to-nearest-even with saturation at 448 (cvt.rn.satfinite).
 //
 // Kernels:
-//   quantize_rows_kernel   one CTA per row: the row's largest magnitude, its
-//                          scale, then 16 codes per thread step (two 16-byte
-//                          bf16 loads, one 16-byte store)
+//   quantize_rows_kernel   a warp (rows up to 2048) or a CTA (up to 32768)
+//                          per row, the row held in registers: its largest
+//                          magnitude, its scale, 16 codes per 16-byte store
 //   col_scale_kernel       one thread per weight column (output channel):
 //                          the largest magnitude over K -> the channel scale
 //   quantize_cols_kernel   64 (K) x 64 (N) tiles through shared memory:
 //                          codes written K-major ([E][N][K]), 16 per thread
-#include <cuda_fp8.h>
-
 #include "common.cuh"
+#include "e4m3.cuh"
 
 namespace moe {
 namespace {
 
+using e4m3::pow2f;
+using e4m3::scale_exp;
+
 constexpr int kQThreads = 256;
 
-// e of the recipe from the bits of amax (>= 0): amax = m * 2^E with m in
-// [0.5, 1); 448 = 0.875 * 2^9, so e = E - 9 when m <= 0.875 (mantissa field
-// <= 0x600000) and E - 8 otherwise.
-__device__ __forceinline__ int fp8_scale_exp(float amax) {
-  const uint32_t b = __float_as_uint(amax);
-  const int field = static_cast<int>((b >> 23) & 0xffu);
-  if (!(amax >= 0x1p-100f) || field == 0xff) return 0;
-  const int E = field - 126;
-  return (b & 0x7fffffu) <= 0x600000u ? E - 9 : E - 8;
-}
-
-// 2^e as a float, for e in [-126, 127]
-__device__ __forceinline__ float pow2f(int e) {
-  return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-}
-
-__device__ __forceinline__ void bf16x8_to_float(const uint4& u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
-
-// 16 floats (already scaled) -> 16 E4M3 codes in a uint4
-__device__ __forceinline__ uint4 to_e4m3x16(const float (&v)[16]) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_fp8x2_storage_t lo =
-        __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i], v[4 * i + 1]), __NV_SATFINITE, __NV_E4M3);
-    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-        make_float2(v[4 * i + 2], v[4 * i + 3]), __NV_SATFINITE, __NV_E4M3);
-    w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-__device__ __forceinline__ float block_max(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();  // red is reused row after row
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  v = lane < (kQThreads / 32) ? red[lane] : 0.f;
-#pragma unroll
-  for (int o = 4; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return __shfl_sync(0xffffffffu, v, 0);
-}
-
 // in [rows, cols] bf16 -> codes [rows, cols], scales [rows]; with row_count
-// (device) only rows < *row_count are written.  cols % 16 == 0.
+// (device) only rows < *row_count are written; cols % 16 == 0.
+// A team of TPR threads (32 to 256, the smallest that covers the row with
+// G groups of 16 values per thread) takes a row; each thread keeps its
+// groups in registers, so the row is read from memory once: largest
+// magnitude (shuffles, plus shared memory across the team's warps), scale,
+// codes.  Rows wider than 256 * 16 * G take the fallback below, which reads
+// the row twice.
+template <int TPR, int G>
 __global__ void __launch_bounds__(kQThreads)
     quantize_rows_kernel(int64_t rows, int cols, const __nv_bfloat16* __restrict__ in,
                          uint8_t* __restrict__ codes, float* __restrict__ scales,
                          const int32_t* __restrict__ row_count) {
+  constexpr int TEAMS = kQThreads / TPR;
   __shared__ float red[kQThreads / 32];
   const int64_t n = row_count ? min(rows, static_cast<int64_t>(*row_count)) : rows;
+  const int t = threadIdx.x % TPR, lane = threadIdx.x & 31;
   const int groups = cols / 16;
-  for (int64_t r = blockIdx.x; r < n; r += gridDim.x) {
-    const uint4* src = reinterpret_cast<const uint4*>(in + r * cols);
+  // every thread runs the same number of row iterations (the CTA-wide
+  // reduction below needs all of them)
+  for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * TEAMS; r0 < n;
+       r0 += static_cast<int64_t>(gridDim.x) * TEAMS) {
+    const int64_t r = r0 + threadIdx.x / TPR;
+    const bool live = r < n;
+    const uint4* src = reinterpret_cast<const uint4*>(in + (live ? r : 0) * cols);
+    uint4 v[2 * G];
     float m = 0.f;
-    for (int g = threadIdx.x; g < groups; g += kQThreads) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float f[8];
-        bf16x8_to_float(src[2 * g + h], f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    for (int i = 0; i < G; ++i) {
+      const int g = t + i * TPR;
+      if (live && g < groups) {
+        v[2 * i] = src[2 * g];
+        v[2 * i + 1] = src[2 * g + 1];
+        m = e4m3::amax_bf16x8(v[2 * i + 1], e4m3::amax_bf16x8(v[2 * i], m));
       }
     }
-    m = block_max(m, red);
-    const int e = fp8_scale_exp(m);
-    if (threadIdx.x == 0) scales[r] = pow2f(e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (TPR > 32) {
+      constexpr int W = TPR / 32;  // warps per team
+      if (lane == 0) red[threadIdx.x >> 5] = m;
+      __syncthreads();
+      const int w0 = (threadIdx.x / TPR) * W;
+      m = red[w0];
+#pragma unroll
+      for (int w = 1; w < W; ++w) m = fmaxf(m, red[w0 + w]);
+      __syncthreads();  // red is rewritten for the next row
+    }
+    if (!live) continue;
+    const int e = scale_exp(m);
+    if (t == 0) scales[r] = pow2f(e);
     const float inv = pow2f(-e);
     uint4* dst = reinterpret_cast<uint4*>(codes + r * cols);
-    for (int g = threadIdx.x; g < groups; g += kQThreads) {
-      float v[16], f[8];
-      bf16x8_to_float(src[2 * g], f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = f[i] * inv;
-      bf16x8_to_float(src[2 * g + 1], f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[8 + i] = f[i] * inv;
-      dst[g] = to_e4m3x16(v);
+    for (int i = 0; i < G; ++i) {
+      const int g = t + i * TPR;
+      if (g < groups) dst[g] = e4m3::quantize16(v[2 * i], v[2 * i + 1], inv);
     }
+  }
+}
+
+// Fallback for rows wider than 32768: one warp per row, read twice.
+__global__ void __launch_bounds__(kQThreads)
+    quantize_wide_rows_kernel(int64_t rows, int cols, const __nv_bfloat16* __restrict__ in,
+                              uint8_t* __restrict__ codes, float* __restrict__ scales,
+                              const int32_t* __restrict__ row_count) {
+  const int64_t n = row_count ? min(rows, static_cast<int64_t>(*row_count)) : rows;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kQThreads / 32);
+  const int groups = cols / 16;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (kQThreads / 32) + (threadIdx.x >> 5); r < n;
+       r += warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(in + r * cols);
+    float m = 0.f;
+    for (int g = lane; g < groups; g += 32)
+      m = e4m3::amax_bf16x8(src[2 * g + 1], e4m3::amax_bf16x8(src[2 * g], m));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int e = scale_exp(m);
+    if (lane == 0) scales[r] = pow2f(e);
+    const float inv = pow2f(-e);
+    uint4* dst = reinterpret_cast<uint4*>(codes + r * cols);
+    for (int g = lane; g < groups; g += 32)
+      dst[g] = e4m3::quantize16(src[2 * g], src[2 * g + 1], inv);
   }
 }
 
@@ -123,7 +121,7 @@ __global__ void __launch_bounds__(kQThreads)
   const __nv_bfloat16* w = W + static_cast<int64_t>(e) * K * N + n;
   float m = 0.f;
   for (int k = 0; k < K; ++k) m = fmaxf(m, fabsf(__bfloat162float(w[static_cast<int64_t>(k) * N])));
-  scales[static_cast<int64_t>(e) * N + n] = pow2f(fp8_scale_exp(m));
+  scales[static_cast<int64_t>(e) * N + n] = pow2f(scale_exp(m));
 }
 
 // W [E][K][N] bf16 -> codes [E][N][K] with the channel scales of
@@ -138,7 +136,8 @@ __global__ void __launch_bounds__(kQThreads)
   for (int i = threadIdx.x; i < 64 * 8; i += kQThreads) {  // 64 rows x 8 vectors of 8 bf16
     const int kk = i >> 3, v = i & 7;
     float f[8];
-    bf16x8_to_float(*reinterpret_cast<const uint4*>(w + static_cast<int64_t>(k0 + kk) * N + n0 + 8 * v), f);
+    e4m3::bf16x8_to_float(
+        *reinterpret_cast<const uint4*>(w + static_cast<int64_t>(k0 + kk) * N + n0 + 8 * v), f);
 #pragma unroll
     for (int j = 0; j < 8; ++j) tile[kk][8 * v + j] = f[j];
   }
@@ -150,7 +149,7 @@ __global__ void __launch_bounds__(kQThreads)
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = tile[16 * g + j][nn] * inv;
   *reinterpret_cast<uint4*>(codes + (static_cast<int64_t>(e) * N + n0 + nn) * K + k0 + 16 * g) =
-      to_e4m3x16(v);
+      e4m3::to_codes16(v);
 }
 
 }  // namespace
@@ -158,10 +157,32 @@ __global__ void __launch_bounds__(kQThreads)
 cudaError_t launch_quantize_rows(int64_t rows, int cols, const void* in, uint8_t* codes,
                                  float* scales, const int32_t* row_count, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  int64_t grid = static_cast<int64_t>(device_sm_count()) * 8;
-  if (grid > rows) grid = rows;
-  quantize_rows_kernel<<<static_cast<unsigned>(grid), kQThreads, 0, s>>>(
-      rows, cols, static_cast<const __nv_bfloat16*>(in), codes, scales, row_count);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(in);
+  const int groups = cols / 16;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+  auto grid = [&](int rows_per_cta) {
+    const int64_t need = (rows + rows_per_cta - 1) / rows_per_cta;
+    return static_cast<unsigned>(need < cap ? need : cap);
+  };
+  // team size: the smallest power of two >= 32 with 4 groups per thread
+  if (groups <= 32 * 4)
+    quantize_rows_kernel<32, 4><<<grid(8), kQThreads, 0, s>>>(rows, cols, x, codes, scales,
+                                                               row_count);
+  else if (groups <= 64 * 4)
+    quantize_rows_kernel<64, 4><<<grid(4), kQThreads, 0, s>>>(rows, cols, x, codes, scales,
+                                                               row_count);
+  else if (groups <= 128 * 4)
+    quantize_rows_kernel<128, 4><<<grid(2), kQThreads, 0, s>>>(rows, cols, x, codes, scales,
+                                                                row_count);
+  else if (groups <= 256 * 4)
+    quantize_rows_kernel<256, 4><<<grid(1), kQThreads, 0, s>>>(rows, cols, x, codes, scales,
+                                                                row_count);
+  else if (groups <= 256 * 8)
+    quantize_rows_kernel<256, 8><<<grid(1), kQThreads, 0, s>>>(rows, cols, x, codes, scales,
+                                                                row_count);
+  else
+    quantize_wide_rows_kernel<<<grid(kQThreads / 32), kQThreads, 0, s>>>(rows, cols, x, codes,
+                                                                       scales, row_count);
   return cudaGetLastError();
 }
 

@@ -35,9 +35,12 @@ def _gpu_quantize_rows(x):
     return codes.cpu().numpy(), scales.cpu().numpy()
 
 
-def test_quantize_rows_bit_exact_with_ties_and_ranges():
+@pytest.mark.parametrize("rows,cols", [(300, 512), (100, 4096), (70, 6144), (40, 16384),
+                                       (33, 14336), (20, 20480), (9, 33280)])
+def test_quantize_rows_bit_exact_with_ties_and_ranges(rows, cols):
+    # a warp per row (<= 2048 values), a CTA per row (<= 32768), the wide fallback
     r = np.random.default_rng(130)
-    x = (r.standard_normal((300, 512)) * np.exp(r.uniform(-30, 30, (300, 1)))).astype(np.float32)
+    x = (r.standard_normal((rows, cols)) * np.exp(r.uniform(-30, 30, (rows, 1)))).astype(np.float32)
     x[0] = 0.0
     x[1, :] = 2.0 ** -105                      # below 2^-100: scale 1
     # rounding ties in E4M3 (midpoints of neighbouring codes) at scale 1
