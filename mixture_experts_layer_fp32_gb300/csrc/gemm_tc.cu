@@ -29,6 +29,12 @@
 //    rows past the buffer end are zero-filled by TMA.
 //  * Weights stay in the caller's [E, K, N] layout (N contiguous): the B
 //    operand is MN-major in shared memory.  Activations are K-major.
+//  * E4M3 variant (template flag FP8; the FP8 experts): both operands are
+//    E4M3 codes and K-major (the weights are quantised once into [E, N, K]),
+//    a stage carries 128 K values (the same 128-byte swizzled rows), the MMA
+//    is kind::f8f6f4 with K = 32, and the epilogue multiplies the fp32
+//    accumulator by the row scale and the output channel's scale.
+//  * tc_grouped_pair_kernel (below) runs the same tiles on pairs of SMs.
 //  * Every wait is bounded: after ~2 s without progress the CTA records
 //    MOE_ERR_TIMEOUT in the workspace error word, lets its in-flight copies
 //    and MMAs finish (again bounded), frees its TMEM and exits.
