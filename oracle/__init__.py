@@ -59,6 +59,9 @@ def _load():
         L.oracle_quantize_cols_e4m3.argtypes = [i64, i32, i32, vp, i32, vp, vp, i32]
         L.oracle_expert_rows_fp8.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                              vp, vp, vp, vp, i32]
+        L.oracle_backward.argtypes = [i64, i32, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp,
+                                      vp, vp, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp,
+                                      vp, i32]
         L.oracle_e4m3_values.argtypes = [vp]
         L.oracle_e4m3_codes.argtypes = [i64, vp, vp]
         _lib = L
@@ -331,3 +334,35 @@ def forward_fp8(x, Wg, q, k, score, gate_bias=None, expert_bias=None, capacity_f
               "xs": xs, "y_perm": res["y_rows"], "h_mid": res["h_mid"], "hq": res["hq"],
               "hs": res["hs"], "y": y})
     return r
+
+
+# -------------------------------------------------------------- backward --
+
+def backward(x, Wg, W1, W3, W2, k, score, topk_idx, topk_prob, keep, dy, gate_bias=None,
+             expert_bias=None, nthreads=0):
+    """Gradients of sum(dy * y) for the routing decisions topk_idx / keep and
+    the combine weights topk_prob (as route() returns them).  Returns a dict of float64 arrays: dx [T,h],
+    dWg [h,E], dgate_bias [E], dW1/dW3 [E,h,f], dW2 [E,f,h], dlogits [T,E]."""
+    x, dy = _c(x), _c(dy)
+    Wg = _c(Wg, np.float32)
+    gate_bias = _c(gate_bias, np.float32)
+    expert_bias = _c(expert_bias, np.float32)
+    W1, W3, W2 = _c(W1), _c(W3), _c(W2)
+    topk_idx = _c(topk_idx, np.int32)
+    topk_prob = _c(topk_prob, np.float32)
+    keep = _c(keep, np.uint8)
+    T, h = x.shape
+    E = Wg.shape[1]
+    f = W1.shape[-1]
+    wd = _dtype_code(W1)
+    out = {"dx": np.empty((T, h)), "dWg": np.empty((h, E)), "dgate_bias": np.empty(E),
+           "dW1": np.empty((E, h, f)), "dW3": np.empty((E, h, f)), "dW2": np.empty((E, f, h)),
+           "dlogits": np.empty((T, E))}
+    _load().oracle_backward(T, h, E, k, f, SCORES[score], _ptr(x), _dtype_code(x), _ptr(Wg),
+                            _ptr(gate_bias), _ptr(expert_bias), _ptr(W1), _ptr(W3), _ptr(W2), wd,
+                            _ptr(topk_idx), _ptr(topk_prob), _ptr(keep), _ptr(dy),
+                            _dtype_code(dy),
+                            _ptr(out["dx"]), _ptr(out["dWg"]), _ptr(out["dgate_bias"]),
+                            _ptr(out["dW1"]), _ptr(out["dW3"]), _ptr(out["dW2"]),
+                            _ptr(out["dlogits"]), nthreads)
+    return out

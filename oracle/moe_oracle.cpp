@@ -139,7 +139,7 @@ double bf16_round(double v) {
 
 extern "C" {
 
-int oracle_abi_version(void) { return 3; }
+int oracle_abi_version(void) { return 4; }
 
 // [MC] §3 Gating: logits = x . Wg (+ bias) with the router math in fp32.
 // The oracle forms the exact sum in double over the exact fp32 values of x
@@ -522,6 +522,189 @@ void oracle_expert_rows_fp8(int64_t R, int h, int f, const uint8_t* xq, const fl
       y_rows[r * (int64_t)h + n] = y * scale * (double)s2[e * h + n];
     }
   });
+}
+
+// ------------------------------------------------------------ backward
+// Gradient of L = sum(dy * y) through the layer for fixed routing decisions
+// (top-k choice, capacity drop): the training-side counterpart of the
+// forward above, derived by the chain rule from the same definitions.
+// y weights each expert output by the forward's fp32 combine weight
+// (topk_prob, an input as a training step saves it), so dY uses that value;
+// the derivatives of the scores are taken in double.
+// Discrete decisions carry no gradient; the expert bias only chooses and
+// gets none.  Per kept pair (t,j) of expert e with weight p:
+//   dY = p dy[t],  dp = <dy[t], Y>,  dH = dY . W2[e]^T,
+//   da = dH * g * silu'(a),  dg = dH * silu(a)   (silu'(a) = s (1 + a (1 - s)), s = sigmoid(a)),
+//   dx[t] += da . W1[e]^T + dg . W3[e]^T,
+//   dW2[e] += H^T dY,  dW1[e] += x^T da,  dW3[e] += x^T dg,
+// and through the router: dlogits from dp by the score function's
+// derivative (only the k chosen experts carry a weight; dropped pairs have
+// dp = 0 but stay in the renormalisation), then
+//   dWg = x^T dlogits,  dgate_bias = sum_t dlogits,  dx[t] += dlogits[t] . Wg^T.
+// All sums in double over the exact inputs.  Outputs: dx [T,h], dWg [h,E],
+// dgb [E], dW1/dW3 [E,h,f], dW2 [E,f,h], dlogits [T,E] (may be NULL).
+void oracle_backward(int64_t T, int h, int E, int k, int f, int score, const void* x,
+                     int x_dtype, const float* Wg, const float* gate_bias,
+                     const float* expert_bias, const void* W1, const void* W3, const void* W2,
+                     int w_dtype, const int32_t* topk_idx, const float* topk_prob,
+                     const uint8_t* keep, const void* dy,
+                     int dy_dtype, double* dx, double* dWg, double* dgb, double* dW1, double* dW3,
+                     double* dW2, double* dlogits_out, int nthreads) {
+  // logits, as the forward forms them (exact sum rounded once to fp32)
+  std::vector<float> logits((size_t)T * E);
+  oracle_router_logits(T, h, E, x, x_dtype, Wg, gate_bias, logits.data(), nthreads);
+  std::vector<double> dl((size_t)T * E, 0.0);
+  // per kept pair: da, dg ([f]) and dY ([h]) for the weight gradients
+  std::vector<double> pda((size_t)T * k * f, 0.0), pdg((size_t)T * k * f, 0.0);
+  std::vector<double> pH((size_t)T * k * f, 0.0), pdY((size_t)T * k * h, 0.0);
+  parallel_for(T, nthreads, [&](int64_t t) {
+    const float* l = logits.data() + t * E;
+    std::vector<double> s(E), xv(h), dyv(h), dxt(h, 0.0);
+    for (int i = 0; i < h; ++i) {
+      xv[i] = value_at(x, x_dtype, t * (int64_t)h + i);
+      dyv[i] = value_at(dy, dy_dtype, t * (int64_t)h + i);
+    }
+    // scores s (double) and the chosen-expert weights p_j (before the drop)
+    for (int e = 0; e < E; ++e) {
+      const double z = (double)l[e];
+      if (score == SCORE_SIGMOID) s[e] = 1.0 / (1.0 + std::exp(-z));
+      else if (score == SCORE_SQRTSOFTPLUS) s[e] = std::sqrt(std::max(z, 0.0) + std::log1p(std::exp(-std::fabs(z))));
+      else s[e] = z;
+    }
+    if (score == SCORE_SOFTMAX_PRE) {
+      double m = -std::numeric_limits<double>::infinity(), zsum = 0.0;
+      for (int e = 0; e < E; ++e) m = std::max(m, s[e]);
+      for (int e = 0; e < E; ++e) zsum += std::exp(s[e] - m);
+      for (int e = 0; e < E; ++e) s[e] = std::exp(s[e] - m) / zsum;
+    }
+    std::vector<double> p(k), dp(k, 0.0);
+    const int32_t* idx = topk_idx + t * k;
+    if (score == SCORE_SOFTMAX_POST) {
+      double m = s[idx[0]], zsum = 0.0;
+      for (int j = 0; j < k; ++j) m = std::max(m, s[idx[j]]);
+      for (int j = 0; j < k; ++j) zsum += std::exp(s[idx[j]] - m);
+      for (int j = 0; j < k; ++j) p[j] = std::exp(s[idx[j]] - m) / zsum;
+    } else if (score == SCORE_SOFTMAX_PRE) {
+      for (int j = 0; j < k; ++j) p[j] = s[idx[j]];
+    } else {
+      double zsum = 0.0;
+      for (int j = 0; j < k; ++j) zsum += s[idx[j]];
+      for (int j = 0; j < k; ++j) p[j] = s[idx[j]] / (zsum + 1e-20);
+    }
+    // experts of the kept pairs
+    for (int j = 0; j < k; ++j) {
+      if (keep && !keep[t * k + j]) continue;
+      const int64_t e = idx[j], pr = t * k + j;
+      std::vector<double> a(f, 0.0), g(f, 0.0), H(f), Y(h, 0.0);
+      for (int i = 0; i < h; ++i) {
+        const int64_t base = (e * h + i) * (int64_t)f;
+        for (int c = 0; c < f; ++c) {
+          a[c] += xv[i] * value_at(W1, w_dtype, base + c);
+          g[c] += xv[i] * value_at(W3, w_dtype, base + c);
+        }
+      }
+      for (int c = 0; c < f; ++c) H[c] = a[c] / (1.0 + std::exp(-a[c])) * g[c];
+      for (int c = 0; c < f; ++c) {
+        const int64_t base = (e * f + c) * (int64_t)h;
+        for (int n = 0; n < h; ++n) Y[n] += H[c] * value_at(W2, w_dtype, base + n);
+      }
+      double dot = 0.0;
+      for (int n = 0; n < h; ++n) dot += dyv[n] * Y[n];
+      dp[j] = dot;
+      // y weights Y by the forward's fp32 combine weight, so that is dY's factor
+      const double pf = (double)topk_prob[pr];
+      double* dYp = &pdY[pr * h];
+      for (int n = 0; n < h; ++n) dYp[n] = pf * dyv[n];
+      for (int c = 0; c < f; ++c) {
+        const int64_t base = (e * f + c) * (int64_t)h;
+        double dH = 0.0;
+        for (int n = 0; n < h; ++n) dH += dYp[n] * value_at(W2, w_dtype, base + n);
+        const double sg = 1.0 / (1.0 + std::exp(-a[c]));
+        pda[pr * f + c] = dH * g[c] * sg * (1.0 + a[c] * (1.0 - sg));
+        pdg[pr * f + c] = dH * a[c] * sg;
+        pH[pr * f + c] = H[c];
+      }
+      for (int i = 0; i < h; ++i) {
+        const int64_t base = (e * h + i) * (int64_t)f;
+        double acc = 0.0;
+        for (int c = 0; c < f; ++c)
+          acc += pda[pr * f + c] * value_at(W1, w_dtype, base + c) +
+                 pdg[pr * f + c] * value_at(W3, w_dtype, base + c);
+        dxt[i] += acc;
+      }
+    }
+    // router: dlogits from dp through the score function
+    double* dlt = &dl[t * E];
+    if (score == SCORE_SOFTMAX_POST) {
+      double sdp = 0.0;
+      for (int j = 0; j < k; ++j) sdp += p[j] * dp[j];
+      for (int j = 0; j < k; ++j) dlt[idx[j]] += p[j] * (dp[j] - sdp);
+    } else if (score == SCORE_SOFTMAX_PRE) {
+      std::vector<double> ds(E, 0.0);
+      for (int j = 0; j < k; ++j) ds[idx[j]] += dp[j];
+      double sds = 0.0;
+      for (int e = 0; e < E; ++e) sds += s[e] * ds[e];
+      for (int e = 0; e < E; ++e) dlt[e] = s[e] * (ds[e] - sds);
+    } else {
+      double zsum = 0.0, spd = 0.0;
+      for (int j = 0; j < k; ++j) zsum += s[idx[j]];
+      const double Z = zsum + 1e-20;
+      for (int j = 0; j < k; ++j) spd += dp[j] * s[idx[j]];
+      for (int j = 0; j < k; ++j) {
+        const int e = idx[j];
+        const double ds = dp[j] / Z - spd / (Z * Z);
+        const double z = (double)l[e];
+        const double deriv = score == SCORE_SIGMOID ? s[e] * (1.0 - s[e])
+                                                    : (1.0 / (1.0 + std::exp(-z))) / (2.0 * s[e]);
+        dlt[e] += ds * deriv;
+      }
+    }
+    (void)expert_bias;  // choice only: no gradient
+    for (int i = 0; i < h; ++i) {
+      double acc = 0.0;
+      for (int e = 0; e < E; ++e) acc += dlt[e] * (double)Wg[(int64_t)i * E + e];
+      dx[t * (int64_t)h + i] = dxt[i] + acc;
+    }
+  });
+  // router weight and bias gradients
+  parallel_for(h, nthreads, [&](int64_t i) {
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int64_t t = 0; t < T; ++t) acc += value_at(x, x_dtype, t * (int64_t)h + i) * dl[t * E + e];
+      dWg[i * E + e] = acc;
+    }
+  });
+  for (int e = 0; e < E; ++e) {
+    double acc = 0.0;
+    for (int64_t t = 0; t < T; ++t) acc += dl[t * E + e];
+    dgb[e] = acc;
+  }
+  // expert weight gradients, per expert (pairs in token order)
+  parallel_for(E, nthreads, [&](int64_t e) {
+    for (int64_t i = 0; i < (int64_t)h * f; ++i) dW1[e * (int64_t)h * f + i] = dW3[e * (int64_t)h * f + i] = 0.0;
+    for (int64_t i = 0; i < (int64_t)f * h; ++i) dW2[e * (int64_t)f * h + i] = 0.0;
+    for (int64_t t = 0; t < T; ++t)
+      for (int j = 0; j < k; ++j) {
+        if (topk_idx[t * k + j] != e || (keep && !keep[t * k + j])) continue;
+        const int64_t pr = t * k + j;
+        for (int i = 0; i < h; ++i) {
+          const double xi = value_at(x, x_dtype, t * (int64_t)h + i);
+          double* w1 = dW1 + (e * h + i) * (int64_t)f;
+          double* w3 = dW3 + (e * h + i) * (int64_t)f;
+          for (int c = 0; c < f; ++c) {
+            w1[c] += xi * pda[pr * f + c];
+            w3[c] += xi * pdg[pr * f + c];
+          }
+        }
+        for (int c = 0; c < f; ++c) {
+          double* w2 = dW2 + (e * f + c) * (int64_t)h;
+          const double Hc = pH[pr * f + c];
+          for (int n = 0; n < h; ++n) w2[n] += Hc * pdY[pr * h + n];
+        }
+      }
+  });
+  if (dlogits_out)
+    for (size_t i = 0; i < dl.size(); ++i) dlogits_out[i] = dl[i];
 }
 
 // The E4M3 value of every code 0..255 (for the pins).
