@@ -306,6 +306,37 @@ moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* W
                             size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * Backward of the layer (the training step every page's training system
+ * runs; the pages print no backward, so it is the chain rule on the
+ * forward's definitions): gradients of L = sum(dy * y) for the routing
+ * decisions the forward took.  The top-k choice and the capacity drop carry
+ * no gradient; the expert bias only chooses and gets none.  Per kept pair:
+ * dY = p dy, dp = <dy, Y>, dH = dY W2^T, SwiGLU backward (a and g
+ * recomputed by fc1), dX = [da|dg] [W1;W3]^T, dW2 = H^T dY, dW1 = X^T da,
+ * dW3 = X^T dg; the router gets dlogits from dp through the score function,
+ * dWg = x^T dlogits, dgate_bias = sum_t dlogits, and dx gains dlogits Wg^T.
+ * bf16 only (MOE_ERR_UNSUPPORTED for MOE_F32): the expert GEMMs run on the
+ * tensor cores (dgrad with the weights read in place, wgrad reducing over
+ * each expert's rows); dY, dH, da and dg are rounded to bf16 as GEMM
+ * operands; accumulation is fp32.
+ *   Saved from the forward (the staged calls' outputs): topk_idx and
+ *   topk_prob [T,k] (moe_route), row_map [T,k], expert_offsets [E+1] and
+ *   x_perm [T*k,h] (moe_permute), h_mid [T*k,f] and y_perm [T*k,h] fp32
+ *   (moe_grouped_mlp).  Parameters as in moe_forward.
+ *   dy [T,h] bf16 in; dx [T,h] bf16 out; dWg [h,E], dgate_bias [E]
+ *   (nullable), dW1/dW3 [E,h,f], dW2 [E,f,h] fp32 out (overwritten).
+ *   ws: moe_workspace_size_backward bytes (zero-filled once).
+ */
+moe_status moe_workspace_size_backward(const moe_config* cfg, size_t* bytes);
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* Wg,
+                        const float* gate_bias, const void* W1, const void* W3, const void* W2,
+                        const int32_t* topk_idx, const float* topk_prob, const int32_t* row_map,
+                        const int32_t* expert_offsets, const void* x_perm, const void* h_mid,
+                        const float* y_perm, const void* dy, void* dx, float* dWg,
+                        float* dgate_bias, float* dW1, float* dW3, float* dW2, void* ws,
+                        size_t ws_bytes, moe_stream_t stream);
+
+/*
  * The layer forward over a sequence of batches held in HOST memory (not a
  * step of the method: the serving loop around moe_forward).  For each batch
  * b in [0, num_batches): its input x_host + b*x_batch_stride ([T,h] dtype)

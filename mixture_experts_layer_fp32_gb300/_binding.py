@@ -29,7 +29,8 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_c
            "moe_probe_fp32_fma", "moe_workspace_size_host", "moe_forward_host",
            "moe_quantize_rows_e4m3", "moe_quantize_experts_e4m3", "moe_workspace_size_e4m3",
            "moe_permute_e4m3", "moe_grouped_mlp_e4m3", "moe_forward_e4m3",
-           "moe_grouped_fc1_e4m3", "moe_grouped_fc2_e4m3"]
+           "moe_grouped_fc1_e4m3", "moe_grouped_fc2_e4m3", "moe_workspace_size_backward",
+           "moe_backward"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -96,6 +97,8 @@ def lib():
             "moe_forward_e4m3": ([cfgp] + [vp] * 14 + [vp, sz, vp], i32),
             "moe_grouped_fc1_e4m3": ([cfgp] + [vp] * 8 + [vp, sz, vp], i32),
             "moe_grouped_fc2_e4m3": ([cfgp] + [vp] * 7 + [vp, sz, vp], i32),
+            "moe_workspace_size_backward": ([cfgp, ctypes.POINTER(sz)], i32),
+            "moe_backward": ([cfgp] + [vp] * 20 + [vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -375,6 +378,44 @@ def forward_e4m3(cfg, x, Wg, gate_bias, expert_bias, q, y, ws, topk_idx=None, to
                                   _p(expert_bias), _p(q.W1q), _p(q.s1), _p(q.W3q), _p(q.s3),
                                   _p(q.W2q), _p(q.s2), _p(y), _p(topk_idx), _p(topk_prob),
                                   _p(tokens_per_expert), w, wb, _stream()), "moe_forward_e4m3")
+
+
+# ------------------------------------------------------------------ backward
+
+def workspace_size_backward(cfg):
+    v = ctypes.c_size_t()
+    _check(lib().moe_workspace_size_backward(ctypes.byref(cfg), ctypes.byref(v)),
+           "moe_workspace_size_backward")
+    return v.value
+
+
+def alloc_workspace_backward(cfg, device="cuda"):
+    return torch.zeros(workspace_size_backward(cfg), dtype=torch.uint8, device=device)
+
+
+class Grads:
+    """Gradient buffers of one backward (dx bf16, the rest fp32)."""
+
+    def __init__(self, cfg, device="cuda"):
+        T, h, E, f = cfg.num_tokens, cfg.hidden, cfg.num_experts, cfg.ffn_hidden
+        d = torch.device(device)
+        self.dx = torch.empty((T, h), dtype=act_dtype(cfg), device=d)
+        self.dWg = torch.empty((h, E), dtype=torch.float32, device=d)
+        self.dgate_bias = torch.empty((E,), dtype=torch.float32, device=d)
+        self.dW1 = torch.empty((E, h, f), dtype=torch.float32, device=d)
+        self.dW3 = torch.empty((E, h, f), dtype=torch.float32, device=d)
+        self.dW2 = torch.empty((E, f, h), dtype=torch.float32, device=d)
+
+
+def backward(cfg, x, Wg, gate_bias, W1, W3, W2, saved, dy, g, ws):
+    """saved: a Buffers object after the staged forward (topk_idx, topk_prob,
+    row_map, expert_offsets, x_perm, h_mid, y_perm); g: Grads."""
+    w, wb = _ws(ws)
+    _check(lib().moe_backward(ctypes.byref(cfg), _p(x), _p(Wg), _p(gate_bias), _p(W1), _p(W3),
+                              _p(W2), _p(saved.topk_idx), _p(saved.topk_prob), _p(saved.row_map),
+                              _p(saved.expert_offsets), _p(saved.x_perm), _p(saved.h_mid),
+                              _p(saved.y_perm), _p(dy), _p(g.dx), _p(g.dWg), _p(g.dgate_bias),
+                              _p(g.dW1), _p(g.dW3), _p(g.dW2), w, wb, _stream()), "moe_backward")
 
 
 def probe_fp32_fma(iters, out):

@@ -1,0 +1,363 @@
+// Backward of the MoE layer around the expert GEMMs: the gradient of
+// L = sum(dy * y) for fixed routing decisions (the chain rule on the forward
+// of the Megatron Core page: combine of §2, score functions of §5, gating of
+// §3).  The expert GEMMs' backward lives in gemm_tc.cu / gemm_wgrad.cu.
+//
+// Kernels:
+//   combine_bwd_kernel  per token: for each kept slot j, dY_perm[row] =
+//                       p[t,j] dy[t] (bf16) and dp[t,j] = <dy[t], y_perm[row]>
+//   router_bwd_kernel   one warp per token: dlogits from dp through the score
+//                       function (softmax after / before top-k, sigmoid,
+//                       sqrtsoftplus with renormalisation), fp32
+//   dwg_kernel          dWg [h,E] = x^T dlogits: 64 x 64 output tiles, the
+//                       token dimension streamed through shared memory
+//   dgb_kernel          dgate_bias[e] = sum_t dlogits[t,e], one CTA per expert
+//   dx_router_kernel    dx_router [T,h] = dlogits . Wg^T: 64 x 64 tiles
+// The token gradient dx = sum_j dx_perm[row(t,j)] + dx_router[t] is the
+// combine kernel with unit weights and dx_router as its addend.
+#include <float.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBwdThreads = 128;
+
+// dy [T,h] bf16, y_perm [rows,h] fp32 -> dY_perm [rows,h] bf16, dp [T,k] fp32
+__global__ void __launch_bounds__(kBwdThreads)
+    combine_bwd_kernel(int T, int h, int k, const __nv_bfloat16* __restrict__ dy,
+                       const int32_t* __restrict__ row_map, const float* __restrict__ topk_prob,
+                       const float* __restrict__ y_perm, __nv_bfloat16* __restrict__ dY_perm,
+                       float* __restrict__ dp) {
+  __shared__ float red[kBwdThreads / 32][MOE_MAX_TOPK];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int h8 = h / 8;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    int rows[MOE_MAX_TOPK];
+    float p[MOE_MAX_TOPK], dot[MOE_MAX_TOPK];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+      rows[j] = j < k ? row_map[(int64_t)t * k + j] : -1;
+      p[j] = rows[j] >= 0 ? topk_prob[(int64_t)t * k + j] : 0.f;
+      dot[j] = 0.f;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(dy + (int64_t)t * h);
+    for (int v = threadIdx.x; v < h8; v += kBwdThreads) {
+      const uint4 u = src[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      float d[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        d[2 * i] = __uint_as_float(w[i] << 16);
+        d[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+#pragma unroll
+      for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+        if (rows[j] < 0) continue;
+        const float4* yp = reinterpret_cast<const float4*>(y_perm + (int64_t)rows[j] * h) + 2 * v;
+        const float4 y0 = yp[0], y1 = yp[1];
+        dot[j] += d[0] * y0.x + d[1] * y0.y + d[2] * y0.z + d[3] * y0.w + d[4] * y1.x +
+                  d[5] * y1.y + d[6] * y1.z + d[7] * y1.w;
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          __nv_bfloat162 b = __floats2bfloat162_rn(p[j] * d[2 * i], p[j] * d[2 * i + 1]);
+          o[i] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        reinterpret_cast<uint4*>(dY_perm + (int64_t)rows[j] * h)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+      float v = dot[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) red[warp][j] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < k) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kBwdThreads / 32; ++w) v += red[w][threadIdx.x];
+      dp[(int64_t)t * k + threadIdx.x] = rows[threadIdx.x] >= 0 ? v : 0.f;
+    }
+    __syncthreads();
+  }
+}
+
+constexpr int kPerLane = MOE_MAX_EXPERTS / 32;
+
+// logits: nsplit partial sums [S,T,E] (added in split order) + gate bias.
+__global__ void __launch_bounds__(256)
+    router_bwd_kernel(int T, int E, int k, int score, const float* __restrict__ logits, int nsplit,
+                      const float* __restrict__ gate_bias, const int32_t* __restrict__ topk_idx,
+                      const float* __restrict__ dp, float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  for (int t = blockIdx.x * nwarps + (threadIdx.x >> 5); t < T; t += gridDim.x * nwarps) {
+    float l[kPerLane], s[kPerLane], dl[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+      const int e = lane + 32 * i;
+      dl[i] = 0.f;
+      if (e < E) {
+        float v = logits[(int64_t)t * E + e];
+        for (int sp = 1; sp < nsplit; ++sp) v += logits[((int64_t)sp * T + t) * E + e];
+        l[i] = gate_bias ? v + gate_bias[e] : v;
+      } else {
+        l[i] = -FLT_MAX;
+      }
+      s[i] = l[i];
+    }
+    // the chosen experts, their scores and dp (lane j holds slot j)
+    int my_e = -1;
+    float my_dp = 0.f;
+    if (lane < k) {
+      my_e = topk_idx[(int64_t)t * k + lane];
+      my_dp = dp[(int64_t)t * k + lane];
+    }
+    if (score == MOE_SCORE_SOFTMAX_PRE) {
+      float m = -FLT_MAX;
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) m = fmaxf(m, s[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float z = 0.f;
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) {
+        s[i] = (lane + 32 * i < E) ? expf(s[i] - m) : 0.f;
+        z += s[i];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) s[i] /= z;
+    } else if (score == MOE_SCORE_SIGMOID || score == MOE_SCORE_SQRTSOFTPLUS) {
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) {
+        if (lane + 32 * i >= E) {
+          s[i] = 0.f;
+          continue;
+        }
+        s[i] = score == MOE_SCORE_SIGMOID
+                   ? 1.f / (1.f + expf(-l[i]))
+                   : sqrtf(fmaxf(l[i], 0.f) + log1pf(expf(-fabsf(l[i]))));
+      }
+    }
+    // score of each chosen expert, gathered to its slot's lane
+    float my_s = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int e = __shfl_sync(0xffffffffu, my_e, j);
+      float v = 0.f;
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i)
+        if (lane + 32 * i == e) v = s[i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == j) my_s = v;
+    }
+    float add = 0.f;  // this lane's slot's contribution to dlogits[my_e]
+    if (score == MOE_SCORE_SOFTMAX_POST) {
+      float m = lane < k ? my_s : -FLT_MAX;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const float ex = lane < k ? expf(my_s - m) : 0.f;
+      float z = ex;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      const float p = ex / z;
+      float sdp = p * my_dp;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sdp += __shfl_xor_sync(0xffffffffu, sdp, o);
+      add = lane < k ? p * (my_dp - sdp) : 0.f;
+    } else if (score == MOE_SCORE_SOFTMAX_PRE) {
+      // ds = dp at the chosen experts; dl = s (ds - <ds, s>)
+      float sds = lane < k ? my_dp * my_s : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sds += __shfl_xor_sync(0xffffffffu, sds, o);
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) dl[i] = -s[i] * sds;
+      add = lane < k ? my_s * my_dp : 0.f;
+    } else {
+      float z = lane < k ? my_s : 0.f, spd = lane < k ? my_dp * my_s : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        z += __shfl_xor_sync(0xffffffffu, z, o);
+        spd += __shfl_xor_sync(0xffffffffu, spd, o);
+      }
+      z += 1e-20f;
+      const float ds = my_dp / z - spd / (z * z);
+      float lv = 0.f;  // the chosen expert's logit
+      for (int j = 0; j < k; ++j) {
+        const int e = __shfl_sync(0xffffffffu, my_e, j);
+        float v = 0.f;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i)
+          if (lane + 32 * i == e) v = l[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == j) lv = v;
+      }
+      const float deriv = score == MOE_SCORE_SIGMOID ? my_s * (1.f - my_s)
+                                                    : (1.f / (1.f + expf(-lv))) / (2.f * my_s);
+      add = lane < k ? ds * deriv : 0.f;
+    }
+    // scatter the k slot contributions onto their experts (distinct experts)
+    for (int j = 0; j < k; ++j) {
+      const int e = __shfl_sync(0xffffffffu, my_e, j);
+      const float a = __shfl_sync(0xffffffffu, add, j);
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i)
+        if (lane + 32 * i == e) dl[i] += a;
+    }
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) dlogits[(int64_t)t * E + e] = dl[i];
+    }
+  }
+}
+
+// dWg [h,E] = x^T dl: tile 64 (h) x 64 (E), tokens streamed 32 at a time;
+// 256 threads, 4 x 4 outputs each.
+__global__ void __launch_bounds__(256)
+    dwg_kernel(int T, int h, int E, const __nv_bfloat16* __restrict__ x,
+               const float* __restrict__ dl, float* __restrict__ dWg) {
+  __shared__ float xs[32][64 + 4];
+  __shared__ float ls[32][64 + 4];
+  const int i0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16
+  float acc[4][4] = {};
+  for (int t0 = 0; t0 < T; t0 += 32) {
+    for (int v = threadIdx.x; v < 32 * 64; v += 256) {
+      const int tt = v >> 6, c = v & 63;
+      const int t = t0 + tt;
+      xs[tt][c] = (t < T && i0 + c < h) ? __bfloat162float(x[(int64_t)t * h + i0 + c]) : 0.f;
+      ls[tt][c] = (t < T && e0 + c < E) ? dl[(int64_t)t * E + e0 + c] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int tt = 0; tt < 32; ++tt) {
+      float a[4], b[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = xs[tt][ty * 4 + r];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) b[c] = ls[tt][tx * 4 + c];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = i0 + ty * 4 + r, e = e0 + tx * 4 + c;
+      if (i < h && e < E) dWg[(int64_t)i * E + e] = acc[r][c];
+    }
+}
+
+// dgate_bias[e] = sum over tokens of dl[t,e] (fixed order: strided partial
+// sums, then a tree over the block)
+__global__ void __launch_bounds__(256)
+    dgb_kernel(int T, int E, const float* __restrict__ dl, float* __restrict__ dgb) {
+  __shared__ float red[256];
+  const int e = blockIdx.x;
+  float v = 0.f;
+  for (int t = threadIdx.x; t < T; t += 256) v += dl[(int64_t)t * E + e];
+  red[threadIdx.x] = v;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) dgb[e] = red[0];
+}
+
+// dx_router [T,h] = dl [T,E] . Wg^T (Wg [h,E]): tile 64 tokens x 64 of h,
+// E in chunks of 32 through shared memory; 4 x 4 outputs per thread.
+__global__ void __launch_bounds__(256)
+    dx_router_kernel(int T, int h, int E, const float* __restrict__ dl,
+                     const float* __restrict__ Wg, float* __restrict__ out) {
+  __shared__ float ls[32][64 + 4];  // [e][t]
+  __shared__ float ws[32][64 + 4];  // [e][i]
+  const int t0 = blockIdx.x * 64, i0 = blockIdx.y * 64;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  for (int e0 = 0; e0 < E; e0 += 32) {
+    for (int v = threadIdx.x; v < 32 * 64; v += 256) {
+      const int rr = v >> 5, ee = v & 31;  // row of the tile, expert in the chunk
+      const int e = e0 + ee;
+      ls[ee][rr] = (t0 + rr < T && e < E) ? dl[(int64_t)(t0 + rr) * E + e] : 0.f;
+      ws[ee][rr] = (i0 + rr < h && e < E) ? Wg[(int64_t)(i0 + rr) * E + e] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int ee = 0; ee < 32; ++ee) {
+      float a[4], b[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = ls[ee][ty * 4 + r];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) b[c] = ws[ee][tx * 4 + c];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int t = t0 + ty * 4 + r, i = i0 + tx * 4 + c;
+      if (t < T && i < h) out[(int64_t)t * h + i] = acc[r][c];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine_bwd(int T, int h, int k, const void* dy, const int32_t* row_map,
+                               const float* topk_prob, const float* y_perm, void* dY_perm,
+                               float* dp, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int cap = device_sm_count() * 16;
+  combine_bwd_kernel<<<T < cap ? T : cap, kBwdThreads, 0, s>>>(
+      T, h, k, static_cast<const __nv_bfloat16*>(dy), row_map, topk_prob, y_perm,
+      static_cast<__nv_bfloat16*>(dY_perm), dp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_bwd(int T, int E, int k, int score, const float* logits, int nsplit,
+                              const float* gate_bias, const int32_t* topk_idx, const float* dp,
+                              float* dlogits, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  int blocks = (T + 7) / 8;
+  const int cap = device_sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  router_bwd_kernel<<<blocks, 256, 0, s>>>(T, E, k, score, logits, nsplit, gate_bias, topk_idx,
+                                           dp, dlogits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_param_grads(int T, int h, int E, const void* x, const float* dl,
+                                      float* dWg, float* dgb, cudaStream_t s) {
+  dwg_kernel<<<dim3((h + 63) / 64, (E + 63) / 64), 256, 0, s>>>(
+      T, h, E, static_cast<const __nv_bfloat16*>(x), dl, dWg);
+  cudaError_t st = cudaGetLastError();
+  if (st != cudaSuccess || dgb == nullptr) return st;
+  dgb_kernel<<<E, 256, 0, s>>>(T, E, dl, dgb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dx_router(int T, int h, int E, const float* dl, const float* Wg, float* out,
+                             cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  dx_router_kernel<<<dim3((T + 63) / 64, (h + 63) / 64), 256, 0, s>>>(T, h, E, dl, Wg, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

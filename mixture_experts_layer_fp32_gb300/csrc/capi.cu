@@ -399,6 +399,35 @@ moe_status do_mlp_e4m3(const moe_config& c, const uint8_t* xperm_q, const float*
   return MOE_OK;
 }
 
+// Backward workspace: error word, router partial logits [S,T,E], dp [T,k],
+// dlogits [T,E], dx_router [T,h] fp32, dY_perm [T*k,h] bf16, dH [T*k,f] bf16,
+// dA = [da | dg] [T*k,2f] bf16, dx_perm [T*k,h] fp32.
+struct BwdLayout {
+  size_t err, logits, dp, dl, dx_router, dY_perm, dH, dA, dx_perm, total;
+};
+BwdLayout make_bwd_layout(const moe_config& c) {
+  BwdLayout B;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t r = o;
+    o = align_up(o + bytes);
+    return r;
+  };
+  const size_t T = c.num_tokens, E = c.num_experts, k = c.topk, h = c.hidden, f = c.ffn_hidden;
+  const size_t R = T * k;
+  B.err = take(kErrBytes);
+  B.logits = take(T * E * 4 * kRouterMaxSplits);
+  B.dp = take(T * k * 4);
+  B.dl = take(T * E * 4);
+  B.dx_router = take(T * h * 4);
+  B.dY_perm = take(R * h * 2);
+  B.dH = take(R * f * 2);
+  B.dA = take(R * 2 * f * 2);
+  B.dx_perm = take(R * h * 4);
+  B.total = o;
+  return B;
+}
+
 // The library's host-I/O streams per device for moe_forward_host: one for
 // host->device copies, one for device->host copies, and the events that
 // order them against the compute stream (per staging slot: input ready,
@@ -891,6 +920,84 @@ moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* W
                       at<float>(ws, L.y_perm), ws, stream));
   MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, at<float>(ws, L.y_perm),
                           row_map, prob, nullptr, y, stream));
+  return MOE_OK;
+}
+
+moe_status moe_workspace_size_backward(const moe_config* cfg, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = make_bwd_layout(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_backward(const moe_config* cfg, const void* x, const float* Wg,
+                        const float* gate_bias, const void* W1, const void* W3, const void* W2,
+                        const int32_t* topk_idx, const float* topk_prob, const int32_t* row_map,
+                        const int32_t* expert_offsets, const void* x_perm, const void* h_mid,
+                        const float* y_perm, const void* dy, void* dx, float* dWg,
+                        float* dgate_bias, float* dW1, float* dW3, float* dW2, void* ws,
+                        size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const size_t T = c.num_tokens, E = c.num_experts, k = c.topk, h = c.hidden, f = c.ffn_hidden;
+  const size_t R = T * k, wsz = E * h * f;
+  MOE_TRY(need(x, T * h, 16));
+  MOE_TRY(need(Wg, h * E, 4));
+  MOE_TRY(optional(gate_bias, 4));
+  MOE_TRY(need(W1, wsz, 16));
+  MOE_TRY(need(W3, wsz, 16));
+  MOE_TRY(need(W2, wsz, 16));
+  MOE_TRY(need(topk_idx, T * k, 4));
+  MOE_TRY(need(topk_prob, T * k, 4));
+  MOE_TRY(need(row_map, T * k, 4));
+  MOE_TRY(need(expert_offsets, E + 1, 4));
+  MOE_TRY(need(x_perm, R * h, 16));
+  MOE_TRY(need(h_mid, R * f, 16));
+  MOE_TRY(need(y_perm, R * h, 16));
+  MOE_TRY(need(dy, T * h, 16));
+  MOE_TRY(need(dx, T * h, 16));
+  MOE_TRY(need(dWg, h * E, 4));
+  MOE_TRY(optional(dgate_bias, 4));
+  MOE_TRY(need(dW1, wsz, 16));
+  MOE_TRY(need(dW3, wsz, 16));
+  MOE_TRY(need(dW2, wsz, 16));
+  const BwdLayout B = make_bwd_layout(c);
+  MOE_TRY(check_ws(c, ws, ws_bytes, B.total));
+  int* err = at<int>(ws, B.err);
+  const int Ti = c.num_tokens, Ei = c.num_experts, ki = c.topk, hi = c.hidden, fi = c.ffn_hidden;
+  const int64_t rows = static_cast<int64_t>(R);
+  float* logits = at<float>(ws, B.logits);
+  float* dp = at<float>(ws, B.dp);
+  float* dl = at<float>(ws, B.dl);
+  float* dx_router = at<float>(ws, B.dx_router);
+  void* dY_perm = at<void>(ws, B.dY_perm);
+  void* dH = at<void>(ws, B.dH);
+  void* dA = at<void>(ws, B.dA);
+  float* dx_perm = at<float>(ws, B.dx_perm);
+  // router: logits again (the forward does not keep them), then its gradients
+  int nsplit = 1;
+  MOE_CUDA(launch_router_logits(Ti, hi, Ei, c.dtype, x, Wg, logits, &nsplit, stream));
+  MOE_CUDA(launch_combine_bwd(Ti, hi, ki, dy, row_map, topk_prob, y_perm, dY_perm, dp, stream));
+  MOE_CUDA(launch_router_bwd(Ti, Ei, ki, c.score, logits, nsplit, gate_bias, topk_idx, dp, dl,
+                             stream));
+  MOE_CUDA(launch_router_param_grads(Ti, hi, Ei, x, dl, dWg, dgate_bias, stream));
+  MOE_CUDA(launch_dx_router(Ti, hi, Ei, dl, Wg, dx_router, stream));
+  // experts: dgrad chain, then the token gradient, then the weight gradients
+  MOE_CUDA(launch_tc_dgrad_fc2(Ei, hi, fi, rows, dY_perm, expert_offsets, W2, dH, err, stream));
+  MOE_CUDA(launch_tc_fc1_bwd(Ei, hi, fi, rows, x_perm, expert_offsets, W1, W3, dH, dA, err,
+                             stream));
+  MOE_CUDA(launch_tc_dgrad_fc1(Ei, hi, fi, rows, dA, expert_offsets, W1, W3, dx_perm, err,
+                               stream));
+  MOE_CUDA(launch_combine(Ti, hi, ki, c.dtype, dx_perm, row_map, nullptr, dx_router, dx, stream));
+  MOE_CUDA(launch_tc_wgrad(Ei, fi, hi, rows, h_mid, fi, dY_perm, hi, expert_offsets, dW2, err,
+                           stream));
+  MOE_CUDA(launch_tc_wgrad(Ei, hi, fi, rows, x_perm, hi, dA, 2 * fi, expert_offsets, dW1, err,
+                           stream));
+  MOE_CUDA(launch_tc_wgrad(Ei, hi, fi, rows, x_perm, hi,
+                           static_cast<const __nv_bfloat16*>(dA) + fi, 2 * fi, expert_offsets,
+                           dW3, err, stream));
   return MOE_OK;
 }
 

@@ -58,7 +58,8 @@ cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, cons
 // token's scale go to each kept row
 cudaError_t launch_perm_copy_e4m3(int T, int h, int k, const void* x, const int32_t* row_map,
                                   uint8_t* x_perm_q, float* row_scale, cudaStream_t s);
-// y_shared [T, h] fp32 (nullable): the shared expert's output, added last
+// y_shared [T, h] fp32 (nullable): the shared expert's output, added last;
+// topk_prob nullable: unit weights (the backward's sum of dx rows)
 cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
                            const int32_t* row_map, const float* topk_prob, const float* y_shared,
                            void* y, cudaStream_t s);
@@ -91,6 +92,38 @@ cudaError_t launch_tc_fc1_e4m3(int E, int h, int f, int64_t max_rows, const uint
 cudaError_t launch_tc_fc2_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* hq,
                                const float* h_scale, const int32_t* offsets, const uint8_t* W2q,
                                const float* s2, float* y_perm, int* err, cudaStream_t s);
+
+// backward (bf16): fc2 dgrad dH [rows,f] = dY [rows,h] . W2[e]^T; fc1 recompute
+// with the SwiGLU backward dA [rows,2f] = [da | dg] from dH; fc1 dgrad
+// dX [rows,h] fp32 = dA . [W1[e] ; W3[e]]^T
+cudaError_t launch_tc_dgrad_fc2(int E, int h, int f, int64_t max_rows, const void* dY,
+                                const int32_t* offsets, const void* W2, void* dH, int* err,
+                                cudaStream_t s);
+cudaError_t launch_tc_fc1_bwd(int E, int h, int f, int64_t max_rows, const void* x_perm,
+                              const int32_t* offsets, const void* W1, const void* W3,
+                              const void* dH, void* dA, int* err, cudaStream_t s);
+cudaError_t launch_tc_dgrad_fc1(int E, int h, int f, int64_t max_rows, const void* dA,
+                                const int32_t* offsets, const void* W1, const void* W3,
+                                float* dX, int* err, cudaStream_t s);
+
+// wgrad: dW [E, M, N] fp32 = per expert X_e^T . Y_e over the expert's rows
+// (X [rows, M] with row stride ldx, Y [rows, N] with row stride ldy, bf16);
+// M % 128 == 0, N % 128 == 0; an expert without rows gets zeros
+cudaError_t launch_tc_wgrad(int E, int M, int N, int64_t max_rows, const void* X, int ldx,
+                            const void* Y, int ldy, const int32_t* offsets, float* dW, int* err,
+                            cudaStream_t s);
+
+// ---- backward around the GEMMs (backward.cu)
+cudaError_t launch_combine_bwd(int T, int h, int k, const void* dy, const int32_t* row_map,
+                               const float* topk_prob, const float* y_perm, void* dY_perm,
+                               float* dp, cudaStream_t s);
+cudaError_t launch_router_bwd(int T, int E, int k, int score, const float* logits, int nsplit,
+                              const float* gate_bias, const int32_t* topk_idx, const float* dp,
+                              float* dlogits, cudaStream_t s);
+cudaError_t launch_router_param_grads(int T, int h, int E, const void* x, const float* dl,
+                                      float* dWg, float* dgb, cudaStream_t s);
+cudaError_t launch_dx_router(int T, int h, int E, const float* dl, const float* Wg, float* out,
+                             cudaStream_t s);
 
 // ---- E4M3 quantisation (FP8 experts) ----
 // rows of bf16 [rows, cols] -> codes + per-row power-of-two scales (rows >=

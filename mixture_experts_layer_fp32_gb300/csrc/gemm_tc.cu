@@ -82,9 +82,20 @@ constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, /*b_mn_major=*/true);
 // 128 bytes per output channel), 128-row boxes of 16 KB.
 constexpr int KE_FP8 = 128;
 constexpr uint32_t IDESC_F8 = ptx::idesc_e4m3_f32(BM, BN);
+// bf16 with B K-major (the backward's dgrad GEMMs)
+constexpr uint32_t IDESC_KB = ptx::idesc_bf16_f32(BM, BN, /*b_mn_major=*/false);
 constexpr long long kWaitCycles = 4000000000LL;
 
-enum { FC1 = 0, FC2 = 1 };
+// Forward modes FC1 (SwiGLU, bf16 out) and FC2 (fp32 out); backward modes:
+//   FC1_BWD    the FC1 mainloop recomputes a = X.W1 and g = X.W3; the epilogue
+//              reads dH and writes da = dH g silu'(a) and dg = dH silu(a)
+//              (bf16) side by side into rows of 2f: [da | dg]
+//   DGRAD_BF16 C = A . B^T with B K-major (a weight read in place, one row per
+//              output column), bf16 out: fc2's dH = dY . W2[e]^T
+//   DGRAD_F32  the same with K split between two weights (the first kb_split
+//              K blocks from tmB0, the rest from tmB1), fp32 out: fc1's
+//              dX = [da | dg] . [W1[e] ; W3[e]]^T
+enum { FC1 = 0, FC2 = 1, FC1_BWD = 2, DGRAD_BF16 = 3, DGRAD_F32 = 4 };
 
 struct TcArgs {
   const int32_t* offsets;
@@ -103,6 +114,11 @@ struct TcArgs {
   const float* col_scale0 = nullptr;
   const float* col_scale1 = nullptr;
   int ncols = 0;
+  // FC1_BWD: dH [rows, ncols] bf16 (row stride ldaux); DGRAD_F32: K blocks
+  // taken from tmB0 before tmB1
+  const void* aux = nullptr;
+  int ldaux = 0;
+  int kb_split = 0;
 };
 
 // Barriers of an NS-stage ring: full[NS], empty[NS], acc_full[2],
@@ -269,6 +285,76 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, int
         }
       }
     }
+  } else if (MODE == FC1_BWD) {
+    // SwiGLU backward on the recomputed a (columns 0..127) and g (128..255):
+    // each lane reads its row's 32 dH values per chunk (64 contiguous
+    // bytes) and writes 64 bytes of da and of dg.
+    const int row = rbase + lane;
+    const int64_t col0 = static_cast<int64_t>(nt) * (BN / 2);
+    const __nv_bfloat16* dh = static_cast<const __nv_bfloat16*>(args.aux) +
+                              static_cast<int64_t>(row) * args.ldaux + col0;
+    __nv_bfloat16* da_out = static_cast<__nv_bfloat16*>(args.out) +
+                            static_cast<int64_t>(row) * args.ldo + col0;
+    __nv_bfloat16* dg_out = da_out + args.ncols;
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      uint32_t a[32], g[32];
+      ptx::tmem_ld32(tb + c, a);
+      ptx::tmem_ld32(tb + BN / 2 + c, g);
+      ptx::tmem_wait_ld();
+      if (row < rend) {
+        const uint4* src = reinterpret_cast<const uint4*>(dh + c);
+        uint4* dst_a = reinterpret_cast<uint4*>(da_out + c);
+        uint4* dst_g = reinterpret_cast<uint4*>(dg_out + c);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 hv = src[v];
+          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+          uint32_t oa[4], og[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float r_a[2], r_g[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int j = 8 * v + 2 * q + u;
+              const float dH = __uint_as_float(u ? (hw[q] & 0xffff0000u) : (hw[q] << 16));
+              const float av = __uint_as_float(a[j]), gv = __uint_as_float(g[j]);
+              const float sg = 1.0f / (1.0f + __expf(-av));
+              r_a[u] = dH * gv * (sg * (1.0f + av * (1.0f - sg)));
+              r_g[u] = dH * (av * sg);
+            }
+            oa[q] = pack_bf16x2(r_a[0], r_a[1]);
+            og[q] = pack_bf16x2(r_g[0], r_g[1]);
+          }
+          dst_a[v] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+          dst_g[v] = make_uint4(og[0], og[1], og[2], og[3]);
+        }
+      }
+    }
+  } else if (MODE == DGRAD_BF16) {
+    // plain bf16 output, 256 columns: each lane writes 64 bytes of its row per
+    // chunk; chunks at or past ncols (the last tile when ncols % 256 == 128)
+    // are not stored
+    const int row = rbase + lane;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) +
+                         static_cast<int64_t>(row) * args.ldo + static_cast<int64_t>(nt) * BN;
+    const int valid = min(BN, args.ncols - nt * BN);
+#pragma unroll 1
+    for (int c = 0; c < valid; c += 32) {
+      uint32_t y[32];
+      ptx::tmem_ld32(tb + c, y);
+      ptx::tmem_wait_ld();
+      if (row < rend) {
+        uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[v] = make_uint4(
+              pack_bf16x2(__uint_as_float(y[8 * v]), __uint_as_float(y[8 * v + 1])),
+              pack_bf16x2(__uint_as_float(y[8 * v + 2]), __uint_as_float(y[8 * v + 3])),
+              pack_bf16x2(__uint_as_float(y[8 * v + 4]), __uint_as_float(y[8 * v + 5])),
+              pack_bf16x2(__uint_as_float(y[8 * v + 6]), __uint_as_float(y[8 * v + 7])));
+      }
+    }
   } else {
     // Stage the warp's 32 rows x 32 columns in shared memory, then store
     // them by row segments: lanes 8s..8s+7 write the 128 contiguous bytes
@@ -392,12 +478,19 @@ __global__ void __launch_bounds__(THREADS, 1)
               ptx::tma_load_3d(b + 2 * BOX_BYTES, &tmB1, kc, n0, e, fb);
             else
               ptx::tma_load_3d(b + 2 * BOX_BYTES, &tmB0, kc, n0 + BN / 2, e, fb);
-          } else if (MODE == FC1) {
+          } else if (MODE == FC1 || MODE == FC1_BWD) {
             const int n0 = nt * (BN / 2);
             ptx::tma_load_3d(b, &tmB0, n0, kc, e, fb);
             ptx::tma_load_3d(b + BOX_BYTES, &tmB0, n0 + 64, kc, e, fb);
             ptx::tma_load_3d(b + 2 * BOX_BYTES, &tmB1, n0, kc, e, fb);
             ptx::tma_load_3d(b + 3 * BOX_BYTES, &tmB1, n0 + 64, kc, e, fb);
+          } else if (MODE == DGRAD_BF16 || MODE == DGRAD_F32) {
+            // K-major weight rows: two boxes of 128 output columns x 64 K
+            const bool first = MODE == DGRAD_BF16 || kb < args.kb_split;
+            const CUtensorMap* m = first ? &tmB0 : &tmB1;
+            const int k1 = first ? kc : kc - args.kb_split * BK;
+            ptx::tma_load_3d(b, m, k1, nt * BN, e, fb);
+            ptx::tma_load_3d(b + 2 * BOX_BYTES, m, k1, nt * BN + BN / 2, e, fb);
           } else {
             const int n0 = nt * BN;
 #pragma unroll
@@ -459,6 +552,14 @@ __global__ void __launch_bounds__(THREADS, 1)
               const uint64_t adesc = ptx::smem_desc(a + s * 32, 16, 1024, ptx::kLayoutSw128);
               const uint64_t bdesc = ptx::smem_desc(b + s * 32, 16, 1024, ptx::kLayoutSw128);
               ptx::umma_e4m3(d, adesc, bdesc, IDESC_F8, (kb | s) != 0 ? 1u : 0u);
+            }
+          } else if (MODE == DGRAD_BF16 || MODE == DGRAD_F32) {
+            // B K-major like A: 128-byte rows, 8-row groups 1 KB apart
+#pragma unroll
+            for (int s = 0; s < BK / 16; ++s) {
+              const uint64_t adesc = ptx::smem_desc(a + s * 32, 16, A_SBO, A_LAYOUT);
+              const uint64_t bdesc = ptx::smem_desc(b + s * 32, 16, 1024, ptx::kLayoutSw128);
+              ptx::umma_bf16(d, adesc, bdesc, IDESC_KB, (kb | s) != 0 ? 1u : 0u);
             }
           } else {
 #pragma unroll
@@ -827,6 +928,22 @@ bool map_weights_e4m3(CUtensorMap* m, const void* ptr, int64_t K, int64_t N, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 K-major weight view [E, N, K] of a weight stored [E][N][K] (K
+// contiguous), box 64 (K) x 128 (N) x 1, 128-byte swizzle: W2 [E, f, h] seen
+// with K = h for fc2's dgrad, W1/W3 [E, h, f] with K = f for fc1's.
+bool map_weights_kmajor(CUtensorMap* m, const void* ptr, int64_t K, int64_t N, int64_t E) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(E)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(N * K) * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MODE, bool FP8>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                       const TcArgs& args, cudaStream_t s) {
@@ -931,6 +1048,52 @@ cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_m
     return cudaErrorInvalidValue;
   TcArgs args{offsets, E, h / BN, f / BK, max_rows, y_perm, h, err};
   return launch_grouped<FC2, false>(a, b0, b0, args, s);
+}
+
+// ---- backward GEMMs (one-SM kernel, bf16 operands, 64-wide K stages)
+
+cudaError_t launch_tc_dgrad_fc2(int E, int h, int f, int64_t max_rows, const void* dY,
+                                const int32_t* offsets, const void* W2, void* dH, int* err,
+                                cudaStream_t s) {
+  if (BK != 64) return cudaErrorNotSupported;
+  if (max_rows == 0) return cudaSuccess;
+  CUtensorMap a, b0;
+  if (!map_rows(&a, dY, h, max_rows) || !map_weights_kmajor(&b0, W2, h, f, E))
+    return cudaErrorInvalidValue;
+  // f % 128 == 0: the last 256-column tile may hold only 128 valid columns
+  TcArgs args{offsets, E, (f + BN - 1) / BN, h / BK, max_rows, dH, f, err};
+  args.ncols = f;
+  return launch_tc<DGRAD_BF16, false>(a, b0, b0, args, s);
+}
+
+cudaError_t launch_tc_fc1_bwd(int E, int h, int f, int64_t max_rows, const void* x_perm,
+                              const int32_t* offsets, const void* W1, const void* W3,
+                              const void* dH, void* dA, int* err, cudaStream_t s) {
+  if (BK != 64) return cudaErrorNotSupported;
+  if (max_rows == 0) return cudaSuccess;
+  CUtensorMap a, b0, b1;
+  if (!map_rows(&a, x_perm, h, max_rows) || !map_weights(&b0, W1, f, h, E) ||
+      !map_weights(&b1, W3, f, h, E))
+    return cudaErrorInvalidValue;
+  TcArgs args{offsets, E, f / (BN / 2), h / BK, max_rows, dA, 2 * f, err};
+  args.aux = dH;
+  args.ldaux = f;
+  args.ncols = f;
+  return launch_tc<FC1_BWD, false>(a, b0, b1, args, s);
+}
+
+cudaError_t launch_tc_dgrad_fc1(int E, int h, int f, int64_t max_rows, const void* dA,
+                                const int32_t* offsets, const void* W1, const void* W3,
+                                float* dX, int* err, cudaStream_t s) {
+  if (BK != 64) return cudaErrorNotSupported;
+  if (max_rows == 0) return cudaSuccess;
+  CUtensorMap a, b0, b1;
+  if (!map_rows(&a, dA, 2 * f, max_rows) || !map_weights_kmajor(&b0, W1, f, h, E) ||
+      !map_weights_kmajor(&b1, W3, f, h, E))
+    return cudaErrorInvalidValue;
+  TcArgs args{offsets, E, h / BN, 2 * f / BK, max_rows, dX, h, err};
+  args.kb_split = f / BK;
+  return launch_tc<DGRAD_F32, false>(a, b0, b1, args, s);
 }
 
 cudaError_t launch_tc_fc1_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* xq,

@@ -267,7 +267,8 @@ __global__ void __launch_bounds__(kCombineThreads)
     for (int j = 0; j < MOE_MAX_TOPK; ++j) {
       rows[j] = (j < k) ? row_map[(int64_t)t * k + j] : -1;
       if (rows[j] >= max_rows) rows[j] = -1;  // a row outside y_perm is treated as dropped
-      p[j] = (rows[j] >= 0) ? topk_prob[(int64_t)t * k + j] : 0.f;
+      // no weights (the backward's unpermute-sum of dx rows): weight 1
+      p[j] = (rows[j] >= 0) ? (topk_prob ? topk_prob[(int64_t)t * k + j] : 1.f) : 0.f;
     }
     for (int v = threadIdx.x; v < h4; v += kCombineThreads) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -1,0 +1,137 @@
+"""The layer backward on the GPU against the oracle's backward.
+
+After the staged bf16 forward, moe_backward gives dx, dWg, dgate_bias and
+dW1/dW3/dW2 for a seeded dy.  The oracle computes the same gradients in
+double from the exact inputs, for the routing the forward took and the
+forward's fp32 combine weights.  The GPU rounds dY, dH, da and dg to bf16
+(they are GEMM operands) and accumulates in fp32.  Those three chained
+roundings (each at most 2^-9 relative) leave an RMS error of about 0.3% of
+each gradient (measured), with heavy-tailed extremes where few rows make a
+rank-1 weight gradient.  Criteria: relative L2 error <= 1e-2 for every
+gradient and <= 3e-2 for each expert's weight gradients (a wrong term, row
+mask or transposition gives >= 10%), every element within 0.15 of the
+gradient's RMS, and exact zeros for experts without rows (dx, bf16, is held
+to the same criteria).  Cases cover every score function,
+capacity drops, group-limited routing, experts without rows, and
+f % 256 == 128 (a half last tile in fc2's dgrad).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from moe_cases import gpu_config, gpu_stages, make_case, np_view, rms, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "mixtral_f384": synthetic.scaled("mixtral", T=600, h=512, f=384, E=4, seed=161),
+    "dsv3_sigmoid": synthetic.scaled("dsv3", T=400, h=512, f=256, E=32, k=4, seed=162),
+    "qwen3_zipf": synthetic.scaled("qwen3", T=300, h=256, f=256, seed=163),
+    "switch_drop": synthetic.scaled("switch", T=1500, h=256, f=256, E=16, seed=164),
+    "sqrtsoftplus": synthetic.scaled("dsv3", T=300, h=256, f=128, E=16, k=2,
+                                     score="sqrtsoftplus", seed=165),
+    "grouped": synthetic.scaled("dsv3_grouped", T=300, h=256, f=128, E=64, seed=166),
+}
+
+
+def _dy(w, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn((w.T, w.h), generator=g).to(torch.bfloat16)
+
+
+def rel_l2(got, want):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    n = np.linalg.norm(want)
+    return np.linalg.norm(got - want) / n if n > 0 else np.linalg.norm(got)
+
+
+def assert_grad(name, got, want):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape, name
+    assert np.all(np.isfinite(got)), name
+    r = rel_l2(got, want)
+    assert r <= 1e-2, "%s: relative L2 error %g > 1e-2" % (name, r)
+    tol = 0.15 * rms(want)
+    err = np.abs(got - want).max()
+    assert err <= tol, "%s: max error %g > %g (0.15 * RMS)" % (name, err, tol)
+
+
+@pytest.fixture(scope="module", params=sorted(CASES))
+def case(request):
+    import mixture_experts_layer_fp32_gb300 as moe
+    w = CASES[request.param]
+    inp, r = make_case(w)
+    dy = _dy(w, 170)
+    d = to_dev(inp)
+    b = gpu_stages(w, d)
+    cfg = gpu_config(w)
+    g = moe.Grads(cfg)
+    ws = moe.alloc_workspace_backward(cfg)
+    moe.backward(cfg, d["x"], d["Wg"], d["gate_bias"], d["W1"], d["W3"], d["W2"], b, dy.cuda(), g,
+                 ws)
+    moe.check(ws)
+    torch.cuda.synchronize()
+    ref = oracle.backward(np_view(inp["x"]), np_view(inp["Wg"]), np_view(inp["W1"]),
+                          np_view(inp["W3"]), np_view(inp["W2"]), w.k, w.score, r["topk_idx"],
+                          r["topk_prob"], r["keep"], np_view(dy), np_view(inp["gate_bias"]),
+                          np_view(inp["expert_bias"]))
+    return w, r, g, ref
+
+
+def test_token_gradient(case):
+    w, r, g, ref = case
+    assert_grad("dx", to_np(g.dx), ref["dx"])
+
+
+def test_router_gradients(case):
+    w, r, g, ref = case
+    if np.all(ref["dWg"] == 0):   # top-1 after softmax: p == 1, nothing reaches the router
+        assert np.all(to_np(g.dWg) == 0)
+        return
+    assert_grad("dWg", to_np(g.dWg), ref["dWg"])
+    assert_grad("dgate_bias", to_np(g.dgate_bias), ref["dgate_bias"])
+
+
+def test_expert_weight_gradients(case):
+    w, r, g, ref = case
+    for n in ("dW1", "dW3", "dW2"):
+        got = to_np(getattr(g, n))
+        assert_grad(n, got, ref[n])
+        for e in np.nonzero(r["tokens_per_expert"] > 0)[0]:
+            re = rel_l2(got[e], ref[n][e])
+            assert re <= 3e-2, "%s expert %d: relative L2 error %g" % (n, e, re)
+    empty = np.nonzero(r["tokens_per_expert"] == 0)[0]
+    for e in empty:  # an expert without rows gets exact zeros
+        for n in ("dW1", "dW3", "dW2"):
+            assert np.all(to_np(getattr(g, n)[e]) == 0.0), (n, e)
+
+
+def test_backward_is_deterministic(case):
+    import mixture_experts_layer_fp32_gb300 as moe
+    w, r, g, ref = case
+    inp, _ = make_case(w)
+    d = to_dev(inp)
+    b = gpu_stages(w, d)
+    cfg = gpu_config(w)
+    ws = moe.alloc_workspace_backward(cfg)
+    outs = []
+    for _ in range(2):
+        g2 = moe.Grads(cfg)
+        moe.backward(cfg, d["x"], d["Wg"], d["gate_bias"], d["W1"], d["W3"], d["W2"], b,
+                     _dy(w, 170).cuda(), g2, ws)
+        outs.append(g2)
+    torch.cuda.synchronize()
+    for n in ("dx", "dWg", "dW1", "dW3", "dW2"):
+        assert torch.equal(getattr(outs[0], n), getattr(outs[1], n)), n
+
+
+def test_backward_rejects_fp32():
+    import mixture_experts_layer_fp32_gb300 as moe
+    cfg = moe.config(T=16, h=136, E=4, k=2, f=200, dtype="f32")
+    with pytest.raises(moe.MoeError):
+        moe.workspace_size_backward(cfg)
