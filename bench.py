@@ -74,6 +74,9 @@ def parse():
     ap.add_argument("--precision", default="bf16", choices=["bf16", "e4m3"],
                     help="expert GEMM operands: bf16 (the default workload) or E4M3 (FP8 "
                          "experts, weights quantised once outside the timed region)")
+    ap.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
+                    help="time the layer forward (the default) or its backward (after one "
+                         "staged forward; dy seeded)")
     ap.add_argument("--override", default="",
                     help="comma list of workload fields to replace, e.g. T=2048,f=3584 "
                          "(a shrunk case for profiling captures)")
@@ -291,6 +294,8 @@ def run_native(args, rank, world, local):
     moe.check(b.ws)
     R = int(b.expert_offsets[-1].item())
     tpe = b.tokens_per_expert.cpu().numpy()
+    if args.which == "backward":
+        return run_backward(args, moe, w, cfg, inp, b, R, flush, stream, world, rank, local)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
               for _ in range(args.steps)]
@@ -464,6 +469,67 @@ def fp32_fma_rate(moe, dev, stream, iters=4096, reps=5):
         t = a.elapsed_time(c) * 1e-3
         best = t if best is None or t < best else best
     return flops / best / 1e12
+
+
+def run_backward(args, moe, w, cfg, inp, b, R, flush, stream, world, rank, local):
+    """Time moe_backward (the saved buffers of one staged forward, a seeded dy)."""
+    if w.dtype != "bf16" or args.precision != "bf16":
+        raise SystemExit("--pass backward needs a bf16 workload and --precision bf16")
+    dev = b.y.device
+    g = torch.Generator(device="cpu").manual_seed(w.seed + 7)
+    dy = torch.randn((w.T, w.h), generator=g).to(torch.bfloat16).to(dev)
+    grads = moe.Grads(cfg, dev)
+    ws = moe.alloc_workspace_backward(cfg, dev)
+
+    def bwd():
+        moe.backward(cfg, inp["x"], inp["Wg"], inp["gate_bias"], inp["W1"], inp["W3"], inp["W2"],
+                     b, dy, grads, ws)
+
+    for _ in range(max(3, args.warmup)):
+        bwd()
+    moe.check(ws)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local, enabled=not args.no_clocks and rank == 0)
+    if clocks.proc is not None:
+        time.sleep(0.5)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        bwd()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    moe.check(ws)
+    ms = sum(a.elapsed_time(c) for a, c in ev) / args.steps
+    ms_all, tokens_per_s = job_throughput(ms, w.T, world)
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    # expert GEMMs of the backward: fc2 dgrad 2Rfh, fc1 recompute 4Rhf, fc1
+    # dgrad 4Rhf, wgrad 2Rfh + 4Rhf
+    gemm_flops = 16 * R * w.h * w.f
+    achieved = gemm_flops / (ms * 1e-3) / 1e12
+    return {
+        "metric": "MoE bwd tokens/sec", "value": tokens_per_s, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded inputs and dy, random-init weights)",
+        "config": dict(workload_desc(w), parallelism="replicas" if world > 1 else "single",
+                       precision=args.precision, pass_="backward"),
+        "rows": R,
+        "roofline": {"kernel": "whole backward (expert GEMM flops / backward time)",
+                     "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "traffic": None, "algorithmic_per_launch": gemm_flops},
+        "e2e": None,
+        "gpu_launches": 14 * args.steps,  # moe_backward launches 14 kernels
+        "clocks": clk,
+        "peaks": peaks,
+    }
 
 
 def barrier(world):

@@ -10,7 +10,9 @@
 //                       function (softmax after / before top-k, sigmoid,
 //                       sqrtsoftplus with renormalisation), fp32
 //   dwg_kernel          dWg [h,E] = x^T dlogits: 64 x 64 output tiles, the
-//                       token dimension streamed through shared memory
+//                       tokens split across CTAs (partial sums added in
+//                       split order by dwg_reduce_kernel) and streamed
+//                       through shared memory
 //   dgb_kernel          dgate_bias[e] = sum_t dlogits[t,e], one CTA per expert
 //   dx_router_kernel    dx_router [T,h] = dlogits . Wg^T: 64 x 64 tiles
 // The token gradient dx = sum_j dx_perm[row(t,j)] + dx_router[t] is the
@@ -220,21 +222,25 @@ __global__ void __launch_bounds__(256)
 }
 
 // dWg [h,E] = x^T dl: tile 64 (h) x 64 (E), tokens streamed 32 at a time;
-// 256 threads, 4 x 4 outputs each.
+// 256 threads, 4 x 4 outputs each.  gridDim.z splits the tokens: split z
+// covers tokens [z * tps, (z+1) * tps) and writes its own partial sums
+// (out + z * h * E), which dwg_reduce_kernel adds in split order.
 __global__ void __launch_bounds__(256)
-    dwg_kernel(int T, int h, int E, const __nv_bfloat16* __restrict__ x,
-               const float* __restrict__ dl, float* __restrict__ dWg) {
+    dwg_kernel(int T, int h, int E, int tps, const __nv_bfloat16* __restrict__ x,
+               const float* __restrict__ dl, float* __restrict__ out) {
   __shared__ float xs[32][64 + 4];
   __shared__ float ls[32][64 + 4];
   const int i0 = blockIdx.x * 64, e0 = blockIdx.y * 64;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16
+  const int tbeg = blockIdx.z * tps, tend = min(T, tbeg + tps);
+  float* dWg = out + static_cast<int64_t>(blockIdx.z) * h * E;
   float acc[4][4] = {};
-  for (int t0 = 0; t0 < T; t0 += 32) {
+  for (int t0 = tbeg; t0 < tend; t0 += 32) {
     for (int v = threadIdx.x; v < 32 * 64; v += 256) {
       const int tt = v >> 6, c = v & 63;
       const int t = t0 + tt;
-      xs[tt][c] = (t < T && i0 + c < h) ? __bfloat162float(x[(int64_t)t * h + i0 + c]) : 0.f;
-      ls[tt][c] = (t < T && e0 + c < E) ? dl[(int64_t)t * E + e0 + c] : 0.f;
+      xs[tt][c] = (t < tend && i0 + c < h) ? __bfloat162float(x[(int64_t)t * h + i0 + c]) : 0.f;
+      ls[tt][c] = (t < tend && e0 + c < E) ? dl[(int64_t)t * E + e0 + c] : 0.f;
     }
     __syncthreads();
 #pragma unroll 8
@@ -258,6 +264,17 @@ __global__ void __launch_bounds__(256)
       const int i = i0 + ty * 4 + r, e = e0 + tx * 4 + c;
       if (i < h && e < E) dWg[(int64_t)i * E + e] = acc[r][c];
     }
+}
+
+// dWg = the S partial sums of dwg_kernel, added in split order
+__global__ void __launch_bounds__(256)
+    dwg_reduce_kernel(int64_t n, int S, const float* __restrict__ part, float* __restrict__ dWg) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * 256) {
+    float v = part[i];
+    for (int z = 1; z < S; ++z) v += part[z * n + i];
+    dWg[i] = v;
+  }
 }
 
 // dgate_bias[e] = sum over tokens of dl[t,e] (fixed order: strided partial
@@ -343,11 +360,32 @@ cudaError_t launch_router_bwd(int T, int E, int k, int score, const float* logit
   return cudaGetLastError();
 }
 
+int dwg_splits(int T, int h, int E) {
+  // about four CTAs per SM over (h tiles) x (E tiles) x splits, each split
+  // at least 256 tokens, at most 32 splits
+  const int64_t tiles = static_cast<int64_t>((h + 63) / 64) * ((E + 63) / 64);
+  int64_t S = (4LL * device_sm_count() + tiles - 1) / tiles;
+  const int64_t by_tokens = (T + 255) / 256;
+  if (S > by_tokens) S = by_tokens;
+  if (S > 32) S = 32;
+  return S < 1 ? 1 : static_cast<int>(S);
+}
+
 cudaError_t launch_router_param_grads(int T, int h, int E, const void* x, const float* dl,
-                                      float* dWg, float* dgb, cudaStream_t s) {
-  dwg_kernel<<<dim3((h + 63) / 64, (E + 63) / 64), 256, 0, s>>>(
-      T, h, E, static_cast<const __nv_bfloat16*>(x), dl, dWg);
+                                      float* dWg, float* part, float* dgb, cudaStream_t s) {
+  const int S = dwg_splits(T, h, E);
+  const int tps = S > 1 ? (T + S - 1) / S : (T > 0 ? T : 1);
+  dwg_kernel<<<dim3((h + 63) / 64, (E + 63) / 64, S), 256, 0, s>>>(
+      T, h, E, tps, static_cast<const __nv_bfloat16*>(x), dl, S > 1 ? part : dWg);
   cudaError_t st = cudaGetLastError();
+  if (st != cudaSuccess) return st;
+  if (S > 1) {
+    const int64_t n = static_cast<int64_t>(h) * E;
+    int64_t grid = (n + 255) / 256;
+    if (grid > 4LL * device_sm_count()) grid = 4LL * device_sm_count();
+    dwg_reduce_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(n, S, part, dWg);
+    st = cudaGetLastError();
+  }
   if (st != cudaSuccess || dgb == nullptr) return st;
   dgb_kernel<<<E, 256, 0, s>>>(T, E, dl, dgb);
   return cudaGetLastError();

@@ -400,10 +400,10 @@ moe_status do_mlp_e4m3(const moe_config& c, const uint8_t* xperm_q, const float*
 }
 
 // Backward workspace: error word, router partial logits [S,T,E], dp [T,k],
-// dlogits [T,E], dx_router [T,h] fp32, dY_perm [T*k,h] bf16, dH [T*k,f] bf16,
+// dlogits [T,E], dWg partial sums, dx_router [T,h] fp32, dY_perm [T*k,h] bf16, dH [T*k,f] bf16,
 // dA = [da | dg] [T*k,2f] bf16, dx_perm [T*k,h] fp32.
 struct BwdLayout {
-  size_t err, logits, dp, dl, dx_router, dY_perm, dH, dA, dx_perm, total;
+  size_t err, logits, dp, dl, dwg_part, dx_router, dY_perm, dH, dA, dx_perm, total;
 };
 BwdLayout make_bwd_layout(const moe_config& c) {
   BwdLayout B;
@@ -419,6 +419,7 @@ BwdLayout make_bwd_layout(const moe_config& c) {
   B.logits = take(T * E * 4 * kRouterMaxSplits);
   B.dp = take(T * k * 4);
   B.dl = take(T * E * 4);
+  B.dwg_part = take(static_cast<size_t>(dwg_splits(c.num_tokens, c.hidden, c.num_experts)) * h * E * 4);
   B.dx_router = take(T * h * 4);
   B.dY_perm = take(R * h * 2);
   B.dH = take(R * f * 2);
@@ -982,7 +983,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* Wg,
   MOE_CUDA(launch_combine_bwd(Ti, hi, ki, dy, row_map, topk_prob, y_perm, dY_perm, dp, stream));
   MOE_CUDA(launch_router_bwd(Ti, Ei, ki, c.score, logits, nsplit, gate_bias, topk_idx, dp, dl,
                              stream));
-  MOE_CUDA(launch_router_param_grads(Ti, hi, Ei, x, dl, dWg, dgate_bias, stream));
+  MOE_CUDA(launch_router_param_grads(Ti, hi, Ei, x, dl, dWg, at<float>(ws, B.dwg_part),
+                                     dgate_bias, stream));
   MOE_CUDA(launch_dx_router(Ti, hi, Ei, dl, Wg, dx_router, stream));
   // experts: dgrad chain, then the token gradient, then the weight gradients
   MOE_CUDA(launch_tc_dgrad_fc2(Ei, hi, fi, rows, dY_perm, expert_offsets, W2, dH, err, stream));

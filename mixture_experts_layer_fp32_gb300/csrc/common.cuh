@@ -120,8 +120,10 @@ cudaError_t launch_combine_bwd(int T, int h, int k, const void* dy, const int32_
 cudaError_t launch_router_bwd(int T, int E, int k, int score, const float* logits, int nsplit,
                               const float* gate_bias, const int32_t* topk_idx, const float* dp,
                               float* dlogits, cudaStream_t s);
+// dWg partial sums need dwg_splits(T, h, E) * h * E floats at `part`
+int dwg_splits(int T, int h, int E);
 cudaError_t launch_router_param_grads(int T, int h, int E, const void* x, const float* dl,
-                                      float* dWg, float* dgb, cudaStream_t s);
+                                      float* dWg, float* part, float* dgb, cudaStream_t s);
 cudaError_t launch_dx_router(int T, int h, int E, const float* dl, const float* Wg, float* out,
                              cudaStream_t s);
 

@@ -14,11 +14,17 @@
 //    MN-major in shared memory (X's M and Y's N contiguous): per stage two
 //    64 (M) x 64 (rows) boxes of X and four 64 (N) x 64 (rows) boxes of Y,
 //    128-byte swizzle, 48 KB, 4 stages.
-//  * An expert's last block also fetches the next expert's rows.  The whole
-//    producer warp waits for that block's copies, zeroes its K rows past the
-//    expert's end in every box (a swizzled 128-byte row stays one row), makes
-//    the writes visible to the tensor core (fence.proxy.async) and releases
-//    the stage on a second barrier, which the MMA thread waits on instead.
+//  * An expert's last block also fetches the next expert's rows.  A seventh
+//    warp walks the same tiles: for such a block it waits for the copies,
+//    zeroes the K rows past the expert's end in every box of both operands
+//    (a swizzled 128-byte row stays one row; rows past the permuted rows may
+//    hold any bits, so B is cleared too), makes the writes visible to the
+//    tensor core (fence.proxy.async) and releases the stage on a second
+//    barrier, which the MMA thread waits on instead.  The TMA producer never
+//    waits for a copy.  The zeroing warp consumes every stage (it waits for
+//    each fill and arrives on the stage's empty barrier beside the MMA's
+//    commit), so it can neither lap the producer nor be lapped by it and
+//    every parity wait sees the phase it means.
 //  * Every wait is bounded as in the forward kernel (error word, abort flag,
 //    drain before TMEM is freed).
 #include "common.cuh"
@@ -32,7 +38,7 @@ constexpr int W_BOX = 64 * WK * 2;                 // 64 (M or N) x 64 rows, bf1
 constexpr int W_A_BYTES = 2 * W_BOX;
 constexpr int W_STAGE = W_A_BYTES + 4 * W_BOX;     // 48 KB
 constexpr int W_STAGES = 4;
-constexpr int W_THREADS = 192;
+constexpr int W_THREADS = 224;                     // TMA, MMA, 4 epilogue warps, tail zeroing
 constexpr int W_PITCH = 36;
 constexpr int W_EPI_BYTES = 4 * 32 * W_PITCH * 4;
 constexpr int W_NUM_BARS = 3 * W_STAGES + 5;       // full, masked, empty, acc_full[2], acc_empty[2], drain
@@ -101,7 +107,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     for (int s = 0; s < W_STAGES; ++s) {
       ptx::mbar_init(ctl.full(s), 1);
       ptx::mbar_init(ctl.masked(s), 1);
-      ptx::mbar_init(ctl.empty(s), 1);
+      ptx::mbar_init(ctl.empty(s), 2);  // MMA commit + zeroing warp
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ctl.acc_full(b), 1);
@@ -133,59 +139,39 @@ __global__ void __launch_bounds__(W_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer (the whole warp)
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t fill_parity = 0, filled = 0;
-    bool alive = true;
-    for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x) {
-      int e, m0, n0;
-      decode_wtile(tile, MT, NT, e, m0, n0);
-      const int r0 = off[e], rows = off[e + 1] - off[e];
-      const int KB = (rows + WK - 1) / WK;
-      for (int kb = 0; kb < KB; ++kb) {
-        if (!__all_sync(0xffffffffu, ctl.wait(ctl.empty(stage), phase ^ 1u, 11))) {
-          alive = false;
-          break;
-        }
-        const uint32_t a = ptx::smem_u32(stages + stage * W_STAGE);
-        const uint32_t b = a + W_A_BYTES;
-        const int row = r0 + kb * WK;
-        if (lane == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t fill_parity = 0, filled = 0;
+      bool alive = true;
+      for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x) {
+        int e, m0, n0;
+        decode_wtile(tile, MT, NT, e, m0, n0);
+        const int r0 = off[e], rows = off[e + 1] - off[e];
+        const int KB = (rows + WK - 1) / WK;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ctl.wait(ctl.empty(stage), phase ^ 1u, 11)) {
+            alive = false;
+            break;
+          }
+          const uint32_t a = ptx::smem_u32(stages + stage * W_STAGE);
+          const uint32_t b = a + W_A_BYTES;
+          const int row = r0 + kb * WK;
           const uint32_t fb = ctl.full(stage);
           ptx::mbar_arrive_expect_tx(fb, W_STAGE);
           ptx::tma_load_2d(a, &tmX, m0, row, fb);
           ptx::tma_load_2d(a + W_BOX, &tmX, m0 + 64, row, fb);
 #pragma unroll
           for (int q = 0; q < 4; ++q) ptx::tma_load_2d(b + q * W_BOX, &tmY, n0 + 64 * q, row, fb);
-        }
-        filled |= 1u << stage;
-        fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
-        const int valid = min(WK, rows - kb * WK);
-        if (valid < WK) {
-          // the expert ends inside this block: zero K rows [valid, 64) of all
-          // six boxes once the copies have landed, then release the stage
-          if (!__all_sync(0xffffffffu, ctl.wait(ctl.full(stage), phase, 12))) {
-            alive = false;
-            break;
+          filled |= 1u << stage;
+          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == W_STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
-          uint4* base = reinterpret_cast<uint4*>(stages + stage * W_STAGE);
-          const int n = (WK - valid) * 8;  // 16-byte words per box
-          for (int i = lane; i < 6 * n; i += 32) {
-            const int box = i / n, w = i - box * n;
-            base[box * (W_BOX / 16) + valid * 8 + w] = make_uint4(0u, 0u, 0u, 0u);
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(ctl.masked(stage));
-        }
-        if (++stage == W_STAGES) {
-          stage = 0;
-          phase ^= 1u;
         }
       }
-    }
-    if (lane == 0) {
       if (alive) {
         for (int i = 0; i < W_STAGES; ++i) {
           if (!ctl.wait(ctl.empty(stage), phase ^ 1u, 13, false)) break;
@@ -197,6 +183,40 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       } else {
         for (int s = 0; s < W_STAGES; ++s)
           if (filled >> s & 1u) ctl.wait(ctl.full(s), fill_parity >> s & 1u, 14, false);
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------ tail zeroing (the whole warp)
+    int stage = 0;
+    uint32_t phase = 0;
+    bool alive = true;
+    for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x) {
+      int e, m0, n0;
+      decode_wtile(tile, MT, NT, e, m0, n0);
+      const int rows = off[e + 1] - off[e];
+      const int KB = (rows + WK - 1) / WK;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int valid = min(WK, rows - kb * WK);
+        if (!__all_sync(0xffffffffu, ctl.wait(ctl.full(stage), phase, 12))) {
+          alive = false;
+          break;
+        }
+        if (valid < WK) {
+          uint4* base = reinterpret_cast<uint4*>(stages + stage * W_STAGE);
+          const int n = (WK - valid) * 8;  // 16-byte words per box
+          for (int i = lane; i < 6 * n; i += 32) {
+            const int box = i / n, w = i - box * n;
+            base[box * (W_BOX / 16) + valid * 8 + w] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ctl.masked(stage));
+        }
+        if (lane == 0) ptx::mbar_arrive(ctl.empty(stage));
+        if (++stage == W_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
   } else if (warp == 1) {
@@ -253,7 +273,7 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         ctl.wait(ctl.drain(), 0, 18, false);
       }
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------ epilogue warps 2..5
     const int q = warp & 3;
     float* etile = epi + q * (32 * W_PITCH);
