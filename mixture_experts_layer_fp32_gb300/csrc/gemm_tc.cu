@@ -626,9 +626,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 // by (half the shared-memory and L2 traffic per MMA of the one-SM kernel).
 // A stage is then 32 KB per CTA (A 128x64, B 64x128), which leaves room for
 // a 6-deep ring instead of 4.
-//  * fc1: rank 0 stages 128 columns of W1, rank 1 the same 128 columns of
-//    W3, so accumulator column j and 128+j are again the SwiGLU pair; fc2:
-//    rank r stages W2 columns nt*256 + 128r .. +127.
+//  * fc1 (and its backward recompute): rank 0 stages 128 columns of W1,
+//    rank 1 the same 128 columns of W3, so accumulator column j and 128+j
+//    are again the SwiGLU pair; fc2: rank r stages W2 columns
+//    nt*256 + 128r .. +127; the dgrad modes: rank r stages the K-major rows
+//    nt*256 + 128r .. +127 of the weight (one 128 x 64 box).
 //  * Both CTAs' producers load their own halves; the copies of both count on
 //    rank 0's full barrier (armed by rank 0 with both halves' bytes).  Rank 0
 //    issues the MMAs; its commits arrive on the empty/acc_full barriers of
@@ -647,6 +649,7 @@ static_assert(P_SMEM_BYTES <= SMEM_BUDGET, "shared memory budget (pair)");
 static_assert(P_STAGES <= 32, "stage bit masks");
 constexpr uint32_t P_IDESC = ptx::idesc_bf16_f32(PM, BN, /*b_mn_major=*/true);
 constexpr uint32_t P_IDESC_F8 = ptx::idesc_e4m3_f32(PM, BN);
+constexpr uint32_t P_IDESC_KB = ptx::idesc_bf16_f32(PM, BN, /*b_mn_major=*/false);
 // Bounded pause that lets a CTA's own in-flight copies land when it gives up
 // (their completion is counted on the other CTA's barrier).
 constexpr long long kPeerDrainCycles = 20000000LL;
@@ -717,11 +720,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       uint32_t fill_parity = 0, filled = 0;
       bool alive = true;
-      const CUtensorMap* tmB = (MODE == FC1 && rank == 1) ? &tmB1 : &tmB0;
+      // FC1 and its backward: rank 0 holds W1's 128 columns, rank 1 W3's
+      constexpr bool kGate = MODE == FC1 || MODE == FC1_BWD;
+      constexpr bool kDgrad = MODE == DGRAD_BF16 || MODE == DGRAD_F32;
+      const CUtensorMap* tmB = (kGate && rank == 1) ? &tmB1 : &tmB0;
       for (int tile = pair; alive && tile < total; tile += npairs) {
         int e, m0, rend, nt;
         decode_tile<PM>(tile, tstart, off, E, e, m0, rend, nt);
-        const int n0 = (MODE == FC1) ? nt * (BN / 2) : nt * BN + static_cast<int>(rank) * (BN / 2);
+        const int n0 = kGate ? nt * (BN / 2) : nt * BN + static_cast<int>(rank) * (BN / 2);
         const int a_row = m0 + static_cast<int>(rank) * BM;
         for (int kb = 0; kb < KB; ++kb) {
           if (!ctl.wait(ctl.empty(stage), phase ^ 1u, 1)) {
@@ -737,6 +743,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if (FP8) {
             // K-major weight rows: one box of this CTA's 128 output channels x 128 K
             ptx::tma_load_3d_pair(b, tmB, kc, n0, e, fb);
+          } else if (kDgrad) {
+            // K-major weight rows: one box of this CTA's 128 output columns x
+            // 64 K, from the weight that holds this K block
+            const bool first = MODE == DGRAD_BF16 || kb < args.kb_split;
+            ptx::tma_load_3d_pair(b, first ? &tmB0 : &tmB1, first ? kc : kc - args.kb_split * BK,
+                                  n0, e, fb);
           } else {
             ptx::tma_load_3d_pair(b, tmB, n0, kc, e, fb);
             ptx::tma_load_3d_pair(b + BOX_BYTES, tmB, n0 + 64, kc, e, fb);
@@ -798,6 +810,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               const uint64_t adesc = ptx::smem_desc(a + s * 32, 16, 1024, ptx::kLayoutSw128);
               const uint64_t bdesc = ptx::smem_desc(b + s * 32, 16, 1024, ptx::kLayoutSw128);
               ptx::umma_e4m3_pair(d, adesc, bdesc, P_IDESC_F8, (kb | s) != 0 ? 1u : 0u);
+            }
+          } else if (MODE == DGRAD_BF16 || MODE == DGRAD_F32) {
+            // B K-major like A in each CTA: 128 rows of 128 bytes, 8-row
+            // groups 1 KB apart
+#pragma unroll
+            for (int s = 0; s < BK / 16; ++s) {
+              const uint64_t adesc = ptx::smem_desc(a + s * 32, 16, A_SBO, A_LAYOUT);
+              const uint64_t bdesc = ptx::smem_desc(b + s * 32, 16, 1024, ptx::kLayoutSw128);
+              ptx::umma_bf16_pair(d, adesc, bdesc, P_IDESC_KB, (kb | s) != 0 ? 1u : 0u);
             }
           } else {
 #pragma unroll
@@ -1050,7 +1071,8 @@ cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_m
   return launch_grouped<FC2, false>(a, b0, b0, args, s);
 }
 
-// ---- backward GEMMs (one-SM kernel, bf16 operands, 64-wide K stages)
+// ---- backward GEMMs (bf16 operands, 64-wide K stages; SM pairs by the
+// forward's rule)
 
 cudaError_t launch_tc_dgrad_fc2(int E, int h, int f, int64_t max_rows, const void* dY,
                                 const int32_t* offsets, const void* W2, void* dH, int* err,
@@ -1063,7 +1085,7 @@ cudaError_t launch_tc_dgrad_fc2(int E, int h, int f, int64_t max_rows, const voi
   // f % 128 == 0: the last 256-column tile may hold only 128 valid columns
   TcArgs args{offsets, E, (f + BN - 1) / BN, h / BK, max_rows, dH, f, err};
   args.ncols = f;
-  return launch_tc<DGRAD_BF16, false>(a, b0, b0, args, s);
+  return launch_grouped<DGRAD_BF16, false>(a, b0, b0, args, s);
 }
 
 cudaError_t launch_tc_fc1_bwd(int E, int h, int f, int64_t max_rows, const void* x_perm,
@@ -1079,7 +1101,7 @@ cudaError_t launch_tc_fc1_bwd(int E, int h, int f, int64_t max_rows, const void*
   args.aux = dH;
   args.ldaux = f;
   args.ncols = f;
-  return launch_tc<FC1_BWD, false>(a, b0, b1, args, s);
+  return launch_grouped<FC1_BWD, false>(a, b0, b1, args, s);
 }
 
 cudaError_t launch_tc_dgrad_fc1(int E, int h, int f, int64_t max_rows, const void* dA,
@@ -1093,7 +1115,7 @@ cudaError_t launch_tc_dgrad_fc1(int E, int h, int f, int64_t max_rows, const voi
     return cudaErrorInvalidValue;
   TcArgs args{offsets, E, h / BN, 2 * f / BK, max_rows, dX, h, err};
   args.kb_split = f / BK;
-  return launch_tc<DGRAD_F32, false>(a, b0, b1, args, s);
+  return launch_grouped<DGRAD_F32, false>(a, b0, b1, args, s);
 }
 
 cudaError_t launch_tc_fc1_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* xq,

@@ -14,13 +14,14 @@
 //    MN-major in shared memory (X's M and Y's N contiguous): per stage two
 //    64 (M) x 64 (rows) boxes of X and four 64 (N) x 64 (rows) boxes of Y,
 //    128-byte swizzle, 48 KB, 4 stages.
-//  * An expert's last block also fetches the next expert's rows.  A seventh
-//    warp walks the same tiles: for such a block it waits for the copies,
-//    zeroes the K rows past the expert's end in every box of both operands
-//    (a swizzled 128-byte row stays one row; rows past the permuted rows may
-//    hold any bits, so B is cleared too), makes the writes visible to the
-//    tensor core (fence.proxy.async) and releases the stage on a second
-//    barrier, which the MMA thread waits on instead.  The TMA producer never
+//  * An expert's last block also fetches the next expert's rows.  The MMA
+//    steps 16 rows at a time, so it issues only the steps that hold one of
+//    the expert's rows, and a seventh warp clears the rest of the last such
+//    step: it waits for the copies, zeroes those (at most 15) rows in every
+//    box of both operands (a swizzled 128-byte row stays one row; rows past
+//    the permuted rows may hold any bits, so B is cleared too), makes the
+//    writes visible to the tensor core (fence.proxy.async) and releases the
+//    stage on a second barrier, which the MMA thread waits on instead.  The TMA producer never
 //    waits for a copy.  The zeroing warp consumes every stage (it waits for
 //    each fill and arrives on the stage's empty barrier beside the MMA's
 //    commit), so it can neither lap the producer nor be lapped by it and
@@ -202,12 +203,12 @@ __global__ void __launch_bounds__(W_THREADS, 1)
           break;
         }
         if (valid < WK) {
-          uint4* base = reinterpret_cast<uint4*>(stages + stage * W_STAGE);
-          const int n = (WK - valid) * 8;  // 16-byte words per box
-          for (int i = lane; i < 6 * n; i += 32) {
-            const int box = i / n, w = i - box * n;
-            base[box * (W_BOX / 16) + valid * 8 + w] = make_uint4(0u, 0u, 0u, 0u);
-          }
+          // rows [valid, valid rounded up to 16) are read by the last MMA step
+          const int n = (((valid + 15) & ~15) - valid) * 8;  // 16-byte words per box
+          uint4* base = reinterpret_cast<uint4*>(stages + stage * W_STAGE) + valid * 8;
+#pragma unroll
+          for (int box = 0; box < 6; ++box)
+            for (int i = lane; i < n; i += 32) base[box * (W_BOX / 16) + i] = make_uint4(0u, 0u, 0u, 0u);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(ctl.masked(stage));
@@ -240,7 +241,8 @@ __global__ void __launch_bounds__(W_THREADS, 1)
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + buf * WN;
         for (int kb = 0; kb < KB; ++kb) {
-          const bool tail = rows - kb * WK < WK;
+          const int valid = min(WK, rows - kb * WK);
+          const bool tail = valid < WK;
           const bool ok = tail ? ctl.wait(ctl.masked(stage), mpar >> stage & 1u, 16)
                                : ctl.wait(ctl.full(stage), phase, 17);
           if (!ok) {
@@ -251,8 +253,10 @@ __global__ void __launch_bounds__(W_THREADS, 1)
           ptx::tc_fence_after();
           const uint32_t a = ptx::smem_u32(stages + stage * W_STAGE);
           const uint32_t b = a + W_A_BYTES;
+          const int steps = (valid + 15) >> 4;
 #pragma unroll
           for (int s = 0; s < WK / 16; ++s) {
+            if (s >= steps) break;
             // both MN-major: 64-wide chunks one box apart (LBO), 8-row K
             // groups 1 KB apart (SBO); a K step of 16 rows moves 2 KB
             const uint64_t adesc = ptx::sw128_desc(a + s * 2048, W_BOX, 1024);

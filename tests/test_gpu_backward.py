@@ -13,7 +13,9 @@ mask or transposition gives >= 10%), every element within 0.15 of the
 gradient's RMS, and exact zeros for experts without rows (dx, bf16, is held
 to the same criteria).  Cases cover every score function,
 capacity drops, group-limited routing, experts without rows, and
-f % 256 == 128 (a half last tile in fc2's dgrad).
+f % 256 == 128 (a half last tile in fc2's dgrad); each runs with the
+backward's dgrad and recompute GEMMs on single SMs and on SM pairs (forced
+through the MOE_TC_PAIR override).
 """
 
 import numpy as np
@@ -61,10 +63,12 @@ def assert_grad(name, got, want):
     assert err <= tol, "%s: max error %g > %g (0.15 * RMS)" % (name, err, tol)
 
 
-@pytest.fixture(scope="module", params=sorted(CASES))
+@pytest.fixture(scope="module", params=[(n, k) for n in sorted(CASES) for k in ("single", "pair")],
+                ids=lambda p: "%s-%s" % p)
 def case(request):
     import mixture_experts_layer_fp32_gb300 as moe
-    w = CASES[request.param]
+    name, kernel = request.param
+    w = CASES[name]
     inp, r = make_case(w)
     dy = _dy(w, 170)
     d = to_dev(inp)
@@ -72,10 +76,12 @@ def case(request):
     cfg = gpu_config(w)
     g = moe.Grads(cfg)
     ws = moe.alloc_workspace_backward(cfg)
-    moe.backward(cfg, d["x"], d["Wg"], d["gate_bias"], d["W1"], d["W3"], d["W2"], b, dy.cuda(), g,
-                 ws)
-    moe.check(ws)
-    torch.cuda.synchronize()
+    with pytest.MonkeyPatch.context() as mp:
+        mp.setenv("MOE_TC_PAIR", "1" if kernel == "pair" else "0")
+        moe.backward(cfg, d["x"], d["Wg"], d["gate_bias"], d["W1"], d["W3"], d["W2"], b,
+                     dy.cuda(), g, ws)
+        moe.check(ws)
+        torch.cuda.synchronize()
     ref = oracle.backward(np_view(inp["x"]), np_view(inp["Wg"]), np_view(inp["W1"]),
                           np_view(inp["W3"]), np_view(inp["W2"]), w.k, w.score, r["topk_idx"],
                           r["topk_prob"], r["keep"], np_view(dy), np_view(inp["gate_bias"]),
