@@ -28,6 +28,8 @@
 //    every parity wait sees the phase it means.
 //  * Every wait is bounded as in the forward kernel (error word, abort flag,
 //    drain before TMEM is freed).
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -77,11 +79,13 @@ struct WCtl {
   }
 };
 
-__device__ __forceinline__ void decode_wtile(int tile, int MT, int NT, int& e, int& m0, int& n0) {
+// Tiles listed expert by expert, row tiles (tile_m rows of M) fastest.
+__device__ __forceinline__ void decode_wtile(int tile, int MT, int NT, int& e, int& m0, int& n0,
+                                             int tile_m = WM) {
   e = tile / (MT * NT);
   const int u = tile - e * MT * NT;
   const int nt = u / MT;
-  m0 = (u - nt * MT) * WM;
+  m0 = (u - nt * MT) * tile_m;
   n0 = nt * WN;
 }
 
@@ -329,6 +333,346 @@ __global__ void __launch_bounds__(W_THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------------ SM pairs
+// The same weight gradients on pairs of SMs (a 2-CTA cluster sharing each
+// MMA, tcgen05 cta_group::2): tile = (expert, 256 rows of M, 256 columns of
+// N), M=256,N=256,K=16 MMAs.  Rank r stages X's columns m0+128r..+127 (its
+// accumulator rows) and Y's columns n0+128r..+127 (its half of B): a stage
+// is two 64x64 boxes of each, 32 KB per CTA, 6 deep.  Each SM stages half of
+// the B tile it multiplies by, as in the forward's pair kernel.
+//  * Both CTAs' copies of a block count on one barrier in rank 0, armed by
+//    rank 0 with both halves' bytes: `full` for a block inside the expert,
+//    `tfull` for its last, partial block.  Each of the two completes once per
+//    fill of its own kind, so its waiters keep a parity per stage (the ring
+//    phase only describes `empty`, which every fill passes through).  Rank 0's seventh warp waits only
+//    on `tfull` (phases complete in order, and the next tail fill of a stage
+//    needs the MMA to have consumed this one, so no phase is skipped),
+//    clears the rows up to the next 16-row MMA step in both CTAs' boxes (the
+//    peer's through distributed shared memory), fences them for the tensor
+//    core (fence.proxy.async.shared::cluster) and arrives on `masked`.
+//  * Rank 0 issues the MMAs; its commits arrive on the empty/acc_full
+//    barriers of both CTAs.  Each CTA's epilogue drains its 128 rows and
+//    arrives on rank 0's acc_empty (8 arrivals).  When M % 256 == 128 the
+//    last row tile's rank-1 half reads zeros (TMA fill) and stores nothing.
+//  * A timed-out wait also raises the other CTA's abort flag; a CTA that
+//    gives up waits (bounded) for the copies counted on its own barriers, or
+//    pauses for the ones counted on its peer's; every cross-CTA access
+//    happens before the final cluster barrier.
+constexpr int PW_M = 256;                          // dW rows per pair tile
+constexpr int PW_STAGE = 4 * W_BOX;                // 2 X boxes + 2 Y boxes: 32 KB
+constexpr int PW_STAGES = 6;
+constexpr int PW_NUM_BARS = 5 * PW_STAGES + 5;     // full, tfull, masked, empty, acc_*, drain
+constexpr int PW_SMEM = 1024 + PW_STAGES * PW_STAGE + W_EPI_BYTES + PW_NUM_BARS * 8 + 16 +
+                        (MOE_MAX_EXPERTS + 1) * 4;
+static_assert(PW_SMEM <= 227 * 1024, "shared memory budget (pair)");
+constexpr uint32_t PW_IDESC = ptx::idesc_bf16_f32(PW_M, WN, /*b_mn_major=*/true) | (1u << 15);
+constexpr long long kPeerDrainCycles = 20000000LL;
+
+struct PWCtl {
+  uint64_t* bar;
+  volatile int* abort_flag;
+  int* err;
+  uint32_t peer_abort;  // the other CTA's abort flag (shared::cluster)
+  __device__ uint32_t full(int s) const { return ptx::smem_u32(bar + s); }
+  __device__ uint32_t tfull(int s) const { return ptx::smem_u32(bar + PW_STAGES + s); }
+  __device__ uint32_t masked(int s) const { return ptx::smem_u32(bar + 2 * PW_STAGES + s); }
+  __device__ uint32_t empty(int s) const { return ptx::smem_u32(bar + 3 * PW_STAGES + s); }
+  __device__ uint32_t acc_full(int b) const { return ptx::smem_u32(bar + 4 * PW_STAGES + b); }
+  __device__ uint32_t acc_empty(int b) const { return ptx::smem_u32(bar + 4 * PW_STAGES + 2 + b); }
+  __device__ uint32_t drain() const { return ptx::smem_u32(bar + 4 * PW_STAGES + 4); }
+  __device__ bool wait(uint32_t b, uint32_t parity, int site, bool honour_abort = true) const {
+    bool timed_out;
+    if (ptx::mbar_wait_bounded(b, parity, kWaitCycles, abort_flag, honour_abort, &timed_out))
+      return true;
+    if (timed_out) {
+      report_error(err, DEV_ERR_TIMEOUT, site);
+      ptx::st_cluster_u32(peer_abort, 1u);
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ void st_cluster_zero16(uint32_t cluster_addr) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(cluster_addr), "r"(0u)
+               : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
+    tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmX,
+                         const __grid_constant__ CUtensorMap tmY, WgradArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  float* epi = reinterpret_cast<float*>(smem + PW_STAGES * PW_STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PW_STAGES * PW_STAGE + W_EPI_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + PW_NUM_BARS);
+  int* abort_word = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* abort_flag = abort_word;
+  int* off = reinterpret_cast<int*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int E = args.E;
+  const int MT = (args.M + PW_M - 1) / PW_M, NT = (args.N + WN - 1) / WN;
+  const int total = E * MT * NT;
+  const PWCtl ctl{bars, abort_flag, args.err, ptx::mapa_shared(ptx::smem_u32(abort_word), rank ^ 1u)};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PW_STAGES; ++s) {
+      ptx::mbar_init(ctl.full(s), 1);
+      ptx::mbar_init(ctl.tfull(s), 1);
+      ptx::mbar_init(ctl.masked(s), 1);
+      ptx::mbar_init(ctl.empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(ctl.acc_full(b), 1);
+      ptx::mbar_init(ctl.acc_empty(b), 8);  // 4 epilogue warps in each CTA
+    }
+    ptx::mbar_init(ctl.drain(), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&tmX);
+    ptx::prefetch_tensormap(&tmY);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish_pair();
+  }
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = args.offsets[e];
+  __syncthreads();
+  if (threadIdx.x == 0) {  // offsets must start at 0, never decrease, end within the buffers
+    bool ok = off[0] == 0 && off[E] <= args.max_rows;
+    for (int e = 0; e < E; ++e) ok = ok && off[e + 1] >= off[e];
+    if (!ok) {
+      for (int e = 0; e <= E; ++e) off[e] = 0;
+      if (blockIdx.x == 0) report_error(args.err, DEV_ERR_INDEX, -1);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers initialised before any cross-CTA signal
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      // per stage: filled, fill went to tfull, parity of the phase that
+      // completes the latest fill, parity of the next full / tfull phase
+      uint32_t filled = 0, tailbits = 0, fill_parity = 0, fnext = 0, tnext = 0;
+      bool alive = true;
+      for (int tile = pair; alive && tile < total; tile += npairs) {
+        int e, m0, n0;
+        decode_wtile(tile, MT, NT, e, m0, n0, PW_M);
+        const int r0 = off[e], rows = off[e + 1] - off[e];
+        const int KB = (rows + WK - 1) / WK;
+        const int mx = m0 + static_cast<int>(rank) * 128, ny = n0 + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!ctl.wait(ctl.empty(stage), phase ^ 1u, 21)) {
+            alive = false;
+            break;
+          }
+          const bool tail = rows - kb * WK < WK;
+          const uint32_t bar = tail ? ctl.tfull(stage) : ctl.full(stage);
+          if (rank == 0) ptx::mbar_arrive_expect_tx(bar, 2 * PW_STAGE);
+          const uint32_t fb = ptx::mapa_shared(bar, 0);
+          const uint32_t a = ptx::smem_u32(stages + stage * PW_STAGE);
+          const uint32_t b = a + 2 * W_BOX;
+          const int row = r0 + kb * WK;
+          ptx::tma_load_2d_pair(a, &tmX, mx, row, fb);
+          ptx::tma_load_2d_pair(a + W_BOX, &tmX, mx + 64, row, fb);
+          ptx::tma_load_2d_pair(b, &tmY, ny, row, fb);
+          ptx::tma_load_2d_pair(b + W_BOX, &tmY, ny + 64, row, fb);
+          const uint32_t bit = 1u << stage;
+          const uint32_t par = tail ? (tnext & bit) : (fnext & bit);
+          if (tail)
+            tnext ^= bit;
+          else
+            fnext ^= bit;
+          filled |= bit;
+          fill_parity = (fill_parity & ~bit) | par;
+          tailbits = (tailbits & ~bit) | (tail ? bit : 0u);
+          if (++stage == PW_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (alive) {
+        for (int i = 0; i < PW_STAGES; ++i) {
+          if (!ctl.wait(ctl.empty(stage), phase ^ 1u, 22, false)) break;
+          if (++stage == PW_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      } else if (rank == 0) {
+        // give up: wait (bounded) for the copies counted on this CTA's barriers
+        for (int s = 0; s < PW_STAGES; ++s)
+          if (filled >> s & 1u)
+            ctl.wait((tailbits >> s & 1u) ? ctl.tfull(s) : ctl.full(s), fill_parity >> s & 1u, 23,
+                     false);
+      } else {
+        // this CTA's copies complete on rank 0's barriers: pause (bounded)
+        const long long t0 = clock64();
+        while (clock64() - t0 < kPeerDrainCycles) {
+        }
+      }
+    }
+  } else if (warp == 6) {
+    if (rank == 0) {
+      // ------------------------------------------------ tail zeroing (rank 0, whole warp)
+      int stage = 0;
+      uint32_t tpar = 0;  // per stage: parity of its next tfull phase
+      const uint32_t peer_stages = ptx::mapa_shared(ptx::smem_u32(stages), 1);
+      for (int tile = pair; tile < total; tile += npairs) {
+        int e, m0, n0;
+        decode_wtile(tile, MT, NT, e, m0, n0, PW_M);
+        const int rows = off[e + 1] - off[e];
+        const int KB = (rows + WK - 1) / WK;
+        bool alive = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          const int valid = min(WK, rows - kb * WK);
+          if (valid < WK) {
+            if (!__all_sync(0xffffffffu, ctl.wait(ctl.tfull(stage), tpar >> stage & 1u, 24))) {
+              alive = false;
+              break;
+            }
+            tpar ^= 1u << stage;
+            const int n = (((valid + 15) & ~15) - valid) * 8;  // 16-byte words per box
+            const uint32_t off_bytes = stage * PW_STAGE + valid * 128;
+            uint4* own = reinterpret_cast<uint4*>(stages + off_bytes);
+#pragma unroll
+            for (int box = 0; box < 4; ++box)
+              for (int i = lane; i < n; i += 32) {
+                own[box * (W_BOX / 16) + i] = make_uint4(0u, 0u, 0u, 0u);
+                st_cluster_zero16(peer_stages + off_bytes + box * W_BOX + i * 16);
+              }
+            asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ctl.masked(stage));
+          }
+          if (++stage == PW_STAGES) stage = 0;
+        }
+        if (!alive) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------ MMA issuer (rank 0)
+      int stage = 0;
+      uint32_t fpar = 0, mpar = 0;  // per stage: parity of the next full / masked phase
+      bool alive = true;
+      int it = 0;
+      for (int tile = pair; alive && tile < total; tile += npairs, ++it) {
+        int e, m0, n0;
+        decode_wtile(tile, MT, NT, e, m0, n0, PW_M);
+        const int rows = off[e + 1] - off[e];
+        const int KB = (rows + WK - 1) / WK;
+        const int buf = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!ctl.wait(ctl.acc_empty(buf), aph ^ 1u, 25)) {
+          alive = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + buf * WN;
+        for (int kb = 0; kb < KB; ++kb) {
+          const int valid = min(WK, rows - kb * WK);
+          const bool tail = valid < WK;
+          const bool ok = tail ? ctl.wait(ctl.masked(stage), mpar >> stage & 1u, 26)
+                               : ctl.wait(ctl.full(stage), fpar >> stage & 1u, 27);
+          if (!ok) {
+            alive = false;
+            break;
+          }
+          if (tail)
+            mpar ^= 1u << stage;
+          else
+            fpar ^= 1u << stage;
+          ptx::tc_fence_after();
+          const uint32_t a = ptx::smem_u32(stages + stage * PW_STAGE);
+          const uint32_t b = a + 2 * W_BOX;
+          const int steps = (valid + 15) >> 4;
+#pragma unroll
+          for (int s = 0; s < WK / 16; ++s) {
+            if (s >= steps) break;
+            // each CTA's halves: two 64-wide MN chunks one box apart (LBO),
+            // 8-row K groups 1 KB apart (SBO), 2 KB per 16-row K step
+            const uint64_t adesc = ptx::sw128_desc(a + s * 2048, W_BOX, 1024);
+            const uint64_t bdesc = ptx::sw128_desc(b + s * 2048, W_BOX, 1024);
+            ptx::umma_bf16_pair(d, adesc, bdesc, PW_IDESC, (kb | s) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit_pair(ctl.empty(stage), 3);
+          if (++stage == PW_STAGES) stage = 0;
+        }
+        if (!alive) break;
+        ptx::umma_commit_pair(ctl.acc_full(buf), 3);  // also for an expert without rows
+      }
+      if (!alive) {
+        ptx::umma_commit_pair(ctl.drain(), 1);
+        ctl.wait(ctl.drain(), 0, 28, false);
+      }
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ------------------------------------------------ epilogue warps 2..5 (both CTAs)
+    const int q = warp & 3;
+    float* etile = epi + q * (32 * W_PITCH);
+    const int sub = lane >> 3, col4 = (lane & 7) * 4;
+    int it = 0;
+    for (int tile = pair; tile < total; tile += npairs, ++it) {
+      int e, m0, n0;
+      decode_wtile(tile, MT, NT, e, m0, n0, PW_M);
+      const bool empty_expert = off[e + 1] == off[e];
+      const int buf = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      bool ok = ctl.wait(ctl.acc_full(buf), aph, 29);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * WN;
+      const int mbase = m0 + static_cast<int>(rank) * 128 + q * 32;  // lane l: row mbase + l
+      if (mbase < args.M) {
+        float* out0 = args.out + (static_cast<int64_t>(e) * args.M) * args.N + n0;
+        const int valid = min(WN, args.N - n0);
+#pragma unroll 1
+        for (int c = 0; c < valid; c += 32) {
+          uint32_t y[32];
+          ptx::tmem_ld32(tb + c, y);
+          ptx::tmem_wait_ld();
+          float4* mine = reinterpret_cast<float4*>(etile + lane * W_PITCH);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            mine[v] = empty_expert ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                   : make_float4(__uint_as_float(y[4 * v]), __uint_as_float(y[4 * v + 1]),
+                                                 __uint_as_float(y[4 * v + 2]), __uint_as_float(y[4 * v + 3]));
+          __syncwarp();
+#pragma unroll
+          for (int r8 = 0; r8 < 8; ++r8) {
+            const int r = r8 * 4 + sub;
+            *reinterpret_cast<float4*>(out0 + static_cast<int64_t>(mbase + r) * args.N + c + col4) =
+                *reinterpret_cast<const float4*>(etile + r * W_PITCH + col4);
+          }
+          __syncwarp();
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ctl.acc_empty(buf), 0));
+    }
+  }
+  __syncthreads();
+  ptx::cluster_sync();  // no cross-CTA access after this point
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -360,8 +704,33 @@ bool map_mn(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows, int64_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Pairs of SMs that can be resident at once for the pair kernel (0: none, or
+// the query failed).
+int wgrad_pair_slots() {
+  static int cache[64] = {0};  // per device; -1 = queried, unusable
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(W_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = PW_SMEM;
+    if (cudaFuncSetAttribute(tc_wgrad_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PW_SMEM) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, tc_wgrad_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();  // clear a failed query; the one-SM kernel is used instead
+      n = -1;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev] > 0 ? cache[dev] : 0;
+}
+
 }  // namespace
 
+// SM pairs unless MOE_TC_PAIR=0 in the environment (a tuning override shared
+// with the grouped GEMMs) or no 2-CTA cluster fits.
 cudaError_t launch_tc_wgrad(int E, int M, int N, int64_t max_rows, const void* X, int ldx,
                             const void* Y, int ldy, const int32_t* offsets, float* dW, int* err,
                             cudaStream_t s) {
@@ -370,6 +739,15 @@ cudaError_t launch_tc_wgrad(int E, int M, int N, int64_t max_rows, const void* X
   const int64_t rows = max_rows > 0 ? max_rows : 1;  // a map needs a positive extent
   CUtensorMap mx, my;
   if (!map_mn(&mx, X, M, rows, ldx) || !map_mn(&my, Y, N, rows, ldy)) return cudaErrorInvalidValue;
+  WgradArgs args{offsets, E, M, N, max_rows, dW, err};
+  const char* force = getenv("MOE_TC_PAIR");
+  const int slots = (force && force[0] == '0') ? 0 : wgrad_pair_slots();
+  if (slots > 0) {
+    const int64_t tiles = static_cast<int64_t>(E) * ((M + PW_M - 1) / PW_M) * ((N + WN - 1) / WN);
+    const int64_t pairs = slots < tiles ? slots : tiles;
+    tc_wgrad_pair_kernel<<<static_cast<unsigned>(2 * pairs), W_THREADS, PW_SMEM, s>>>(mx, my, args);
+    return cudaGetLastError();
+  }
   static bool configured[64] = {false};
   int dev = 0;
   cudaError_t st = cudaGetDevice(&dev);
@@ -382,7 +760,6 @@ cudaError_t launch_tc_wgrad(int E, int M, int N, int64_t max_rows, const void* X
   const int64_t tiles = static_cast<int64_t>(E) * (M / WM) * ((N + WN - 1) / WN);
   int64_t grid = device_sm_count();
   if (grid > tiles) grid = tiles;
-  WgradArgs args{offsets, E, M, N, max_rows, dW, err};
   tc_wgrad_kernel<<<static_cast<unsigned>(grid), W_THREADS, W_SMEM, s>>>(mx, my, args);
   return cudaGetLastError();
 }
