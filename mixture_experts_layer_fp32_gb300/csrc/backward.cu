@@ -13,8 +13,15 @@
 //                       tokens split across CTAs (partial sums added in
 //                       split order by dwg_reduce_kernel) and streamed
 //                       through shared memory
+//   dwg_small_kernel    the same for E <= 32: a thread owns two rows of dWg
+//                       and all E columns, x streamed straight from memory
 //   dgb_kernel          dgate_bias[e] = sum_t dlogits[t,e], one CTA per expert
 //   dx_router_kernel    dx_router [T,h] = dlogits . Wg^T: 64 x 64 tiles
+//   dx_router_small_kernel  the same for E <= 16: a thread owns four columns
+//                       of h with their Wg rows in registers (write-bound)
+//   split3_kernel       fp32 -> bf16 hi/lo triples for the tensor-core path
+//                       (E % 64 == 0): dWg and dx_router as tcgen05 GEMMs
+//   fold_halves_kernel  dWg = the hi and lo halves of that GEMM's output
 // The token gradient dx = sum_j dx_perm[row(t,j)] + dx_router[t] is the
 // combine kernel with unit weights and dx_router as its addend.
 #include <float.h>
@@ -266,6 +273,70 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// dWg [h,E] = x^T dl for E <= EC (EC = 8, 16 or 32): thread j of the grid
+// owns rows i = 2j, 2j+1 of dWg and their EC columns (packed fp32x2 FMAs on
+// the two rows); tokens of split z are [z * tps, (z+1) * tps), their dl rows
+// staged 64 at a time in shared memory.  Each split writes its partial sums
+// to out + z * h * E (added in split order by dwg_reduce_kernel).
+template <int EC>
+__global__ void __launch_bounds__(256)
+    dwg_small_kernel(int T, int h, int E, int tps, const __nv_bfloat16* __restrict__ x,
+                     const float* __restrict__ dl, float* __restrict__ out) {
+  constexpr int TCH = 64;
+  __shared__ __align__(16) float ls[TCH][EC];
+  const int i = (blockIdx.x * 256 + threadIdx.x) * 2;
+  const int tbeg = blockIdx.z * tps, tend = min(T, tbeg + tps);
+  float2 acc[EC];
+#pragma unroll
+  for (int e = 0; e < EC; ++e) acc[e] = make_float2(0.f, 0.f);
+  const __nv_bfloat162* xr = reinterpret_cast<const __nv_bfloat162*>(x + i);
+  const int64_t step = h / 2;  // bf16 pairs per token row
+  for (int t0 = tbeg; t0 < tend; t0 += TCH) {
+    const int n = min(TCH, tend - t0);
+    for (int v = threadIdx.x; v < TCH * EC; v += 256) {
+      const int tt = v / EC, e = v - tt * EC;
+      ls[tt][e] = (tt < n && e < E) ? dl[static_cast<int64_t>(t0 + tt) * E + e] : 0.f;
+    }
+    __syncthreads();
+    if (i < h) {
+      const __nv_bfloat162* xp = xr + static_cast<int64_t>(t0) * step;
+      int tt = 0;
+      for (; tt + 8 <= n; tt += 8) {
+        float2 xv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) xv[u] = __bfloat1622float2(xp[static_cast<int64_t>(tt + u) * step]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4* lr = reinterpret_cast<const float4*>(ls[tt + u]);
+#pragma unroll
+          for (int e4 = 0; e4 < EC / 4; ++e4) {
+            const float4 l = lr[e4];
+            acc[4 * e4] = __ffma2_rn(xv[u], make_float2(l.x, l.x), acc[4 * e4]);
+            acc[4 * e4 + 1] = __ffma2_rn(xv[u], make_float2(l.y, l.y), acc[4 * e4 + 1]);
+            acc[4 * e4 + 2] = __ffma2_rn(xv[u], make_float2(l.z, l.z), acc[4 * e4 + 2]);
+            acc[4 * e4 + 3] = __ffma2_rn(xv[u], make_float2(l.w, l.w), acc[4 * e4 + 3]);
+          }
+        }
+      }
+      for (; tt < n; ++tt) {
+        const float2 xv = __bfloat1622float2(xp[static_cast<int64_t>(tt) * step]);
+#pragma unroll
+        for (int e = 0; e < EC; ++e) acc[e] = __ffma2_rn(xv, make_float2(ls[tt][e], ls[tt][e]), acc[e]);
+      }
+    }
+    __syncthreads();
+  }
+  if (i < h) {
+    float* o = out + static_cast<int64_t>(blockIdx.z) * h * E + static_cast<int64_t>(i) * E;
+#pragma unroll
+    for (int e = 0; e < EC; ++e)
+      if (e < E) {
+        o[e] = acc[e].x;
+        o[E + e] = acc[e].y;
+      }
+  }
+}
+
 // dWg = the S partial sums of dwg_kernel, added in split order
 __global__ void __launch_bounds__(256)
     dwg_reduce_kernel(int64_t n, int S, const float* __restrict__ part, float* __restrict__ dWg) {
@@ -335,6 +406,83 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// dx_router [T,h] = dl . Wg^T for E <= EC (EC = 8 or 16): a block covers 256
+// columns of h (64 threads x 4) and 64 tokens (4 thread rows x 16); a thread
+// keeps Wg's rows for its 4 columns in registers and reads each token's dl
+// row from shared memory (a broadcast), writing 16 bytes per token.
+template <int EC>
+__global__ void __launch_bounds__(256)
+    dx_router_small_kernel(int T, int h, int E, const float* __restrict__ dl,
+                           const float* __restrict__ Wg, float* __restrict__ out) {
+  __shared__ __align__(16) float ls[64][EC];
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+  const int i = (blockIdx.y * 64 + tx) * 4, t0 = blockIdx.x * 64;
+  for (int v = threadIdx.x; v < 64 * EC; v += 256) {
+    const int tt = v / EC, e = v - tt * EC;
+    ls[tt][e] = (t0 + tt < T && e < E) ? dl[static_cast<int64_t>(t0 + tt) * E + e] : 0.f;
+  }
+  float w[4][EC];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int e = 0; e < EC; ++e)
+      w[c][e] = (i + c < h && e < E) ? Wg[static_cast<int64_t>(i + c) * E + e] : 0.f;
+  __syncthreads();
+  if (i >= h) return;
+#pragma unroll 4
+  for (int tt = ty; tt < 64; tt += 4) {
+    const int t = t0 + tt;
+    if (t >= T) break;
+    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
+    const float4* lr = reinterpret_cast<const float4*>(ls[tt]);
+#pragma unroll
+    for (int e4 = 0; e4 < EC / 4; ++e4) {
+      const float4 l = lr[e4];
+      const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = 4 * e4 + u;
+        a01 = __ffma2_rn(make_float2(w[0][e], w[1][e]), make_float2(lv[u], lv[u]), a01);
+        a23 = __ffma2_rn(make_float2(w[2][e], w[3][e]), make_float2(lv[u], lv[u]), a23);
+      }
+    }
+    *reinterpret_cast<float4*>(out + static_cast<int64_t>(t) * h + i) =
+        make_float4(a01.x, a01.y, a23.x, a23.y);
+  }
+}
+
+// v [rows, E] fp32 -> dst [rows, 3E] bf16: hi = bf16(v), lo = bf16(v - hi)
+// (v - hi is exact in fp32), written as [hi | lo | hi] (lo_last == 0) or
+// [hi | hi | lo] (lo_last == 1).
+__global__ void __launch_bounds__(256)
+    split3_kernel(int64_t rows, int E, int lo_last, const float* __restrict__ v,
+                  __nv_bfloat16* __restrict__ dst) {
+  const int64_t n = rows * E;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * 256) {
+    const int64_t r = i / E;
+    const int e = static_cast<int>(i - r * E);
+    const float x = v[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+    __nv_bfloat16* d = dst + r * 3 * E + e;
+    d[0] = hi;
+    d[E] = lo_last ? hi : lo;
+    d[2 * E] = lo_last ? lo : hi;
+  }
+}
+
+// dWg [h, E] = out [h, 2E]: columns e and E + e added
+__global__ void __launch_bounds__(256)
+    fold_halves_kernel(int64_t n, int E, const float* __restrict__ two, float* __restrict__ dWg) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * 256) {
+    const int64_t r = i / E;
+    const int e = static_cast<int>(i - r * E);
+    dWg[i] = two[r * 2 * E + e] + two[r * 2 * E + E + e];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_combine_bwd(int T, int h, int k, const void* dy, const int32_t* row_map,
@@ -361,13 +509,16 @@ cudaError_t launch_router_bwd(int T, int E, int k, int score, const float* logit
 }
 
 int dwg_splits(int T, int h, int E) {
-  // about four CTAs per SM over (h tiles) x (E tiles) x splits, each split
-  // at least 256 tokens, at most 32 splits
-  const int64_t tiles = static_cast<int64_t>((h + 63) / 64) * ((E + 63) / 64);
+  // about four CTAs per SM over (blocks of dWg) x splits; E <= 32: blocks of
+  // 512 rows, each split at least 64 tokens, at most 128 splits; else 64 x 64
+  // tiles, each split at least 256 tokens, at most 32 splits
+  const bool small = E <= 32;
+  const int64_t tiles = small ? (h + 511) / 512
+                              : static_cast<int64_t>((h + 63) / 64) * ((E + 63) / 64);
   int64_t S = (4LL * device_sm_count() + tiles - 1) / tiles;
-  const int64_t by_tokens = (T + 255) / 256;
+  const int64_t by_tokens = small ? (T + 63) / 64 : (T + 255) / 256;
   if (S > by_tokens) S = by_tokens;
-  if (S > 32) S = 32;
+  if (S > (small ? 128 : 32)) S = small ? 128 : 32;
   return S < 1 ? 1 : static_cast<int>(S);
 }
 
@@ -375,8 +526,17 @@ cudaError_t launch_router_param_grads(int T, int h, int E, const void* x, const 
                                       float* dWg, float* part, float* dgb, cudaStream_t s) {
   const int S = dwg_splits(T, h, E);
   const int tps = S > 1 ? (T + S - 1) / S : (T > 0 ? T : 1);
-  dwg_kernel<<<dim3((h + 63) / 64, (E + 63) / 64, S), 256, 0, s>>>(
-      T, h, E, tps, static_cast<const __nv_bfloat16*>(x), dl, S > 1 ? part : dWg);
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  float* dst = S > 1 ? part : dWg;
+  const dim3 small_grid((h + 511) / 512, 1, S);
+  if (E <= 8)
+    dwg_small_kernel<8><<<small_grid, 256, 0, s>>>(T, h, E, tps, xb, dl, dst);
+  else if (E <= 16)
+    dwg_small_kernel<16><<<small_grid, 256, 0, s>>>(T, h, E, tps, xb, dl, dst);
+  else if (E <= 32)
+    dwg_small_kernel<32><<<small_grid, 256, 0, s>>>(T, h, E, tps, xb, dl, dst);
+  else
+    dwg_kernel<<<dim3((h + 63) / 64, (E + 63) / 64, S), 256, 0, s>>>(T, h, E, tps, xb, dl, dst);
   cudaError_t st = cudaGetLastError();
   if (st != cudaSuccess) return st;
   if (S > 1) {
@@ -394,8 +554,46 @@ cudaError_t launch_router_param_grads(int T, int h, int E, const void* x, const 
 cudaError_t launch_dx_router(int T, int h, int E, const float* dl, const float* Wg, float* out,
                              cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  dx_router_kernel<<<dim3((T + 63) / 64, (h + 63) / 64), 256, 0, s>>>(T, h, E, dl, Wg, out);
+  const dim3 small_grid((T + 63) / 64, (h + 255) / 256);
+  if (E <= 8)
+    dx_router_small_kernel<8><<<small_grid, 256, 0, s>>>(T, h, E, dl, Wg, out);
+  else if (E <= 16)
+    dx_router_small_kernel<16><<<small_grid, 256, 0, s>>>(T, h, E, dl, Wg, out);
+  else
+    dx_router_kernel<<<dim3((T + 63) / 64, (h + 63) / 64), 256, 0, s>>>(T, h, E, dl, Wg, out);
   return cudaGetLastError();
+}
+
+bool router_grads_on_tc(int E) { return E >= 64 && E % 64 == 0; }
+
+cudaError_t launch_router_grads_tc(int T, int h, int E, const void* x, const float* dl,
+                                   const float* Wg, void* dl3, void* wg3, float* dwg2, float* dWg,
+                                   float* dgb, float* dx_router, int* err, cudaStream_t s) {
+  if (!router_grads_on_tc(E)) return cudaErrorInvalidValue;
+  const int cap = 8 * device_sm_count();
+  auto blocks = [&](int64_t n) {
+    const int64_t b = (n + 255) / 256;
+    return static_cast<unsigned>(b < cap ? (b > 0 ? b : 1) : cap);
+  };
+  __nv_bfloat16* d3 = static_cast<__nv_bfloat16*>(dl3);
+  __nv_bfloat16* w3 = static_cast<__nv_bfloat16*>(wg3);
+  split3_kernel<<<blocks(static_cast<int64_t>(T) * E), 256, 0, s>>>(T, E, 0, dl, d3);
+  split3_kernel<<<blocks(static_cast<int64_t>(h) * E), 256, 0, s>>>(h, E, 1, Wg, w3);
+  cudaError_t st = cudaGetLastError();
+  if (st != cudaSuccess) return st;
+  // dWg: one dense group over the T tokens, M = h, N = 2E ([hi | lo] of dl3)
+  st = launch_tc_wgrad(1, h, 2 * E, T, x, h, d3, 3 * E, nullptr, dwg2, err, s);
+  if (st != cudaSuccess) return st;
+  fold_halves_kernel<<<blocks(static_cast<int64_t>(h) * E), 256, 0, s>>>(
+      static_cast<int64_t>(h) * E, E, dwg2, dWg);
+  st = cudaGetLastError();
+  if (st != cudaSuccess) return st;
+  if (dgb != nullptr) {
+    dgb_kernel<<<E, 256, 0, s>>>(T, E, dl, dgb);
+    st = cudaGetLastError();
+    if (st != cudaSuccess) return st;
+  }
+  return launch_tc_dense_nt_f32(T, 3 * E, h, d3, w3, dx_router, h, err, s);
 }
 
 }  // namespace moe

@@ -403,7 +403,7 @@ moe_status do_mlp_e4m3(const moe_config& c, const uint8_t* xperm_q, const float*
 // dlogits [T,E], dWg partial sums, dx_router [T,h] fp32, dY_perm [T*k,h] bf16, dH [T*k,f] bf16,
 // dA = [da | dg] [T*k,2f] bf16, dx_perm [T*k,h] fp32.
 struct BwdLayout {
-  size_t err, logits, dp, dl, dwg_part, dx_router, dY_perm, dH, dA, dx_perm, total;
+  size_t err, logits, dp, dl, dwg_part, dl3, wg3, dwg2, dx_router, dY_perm, dH, dA, dx_perm, total;
 };
 BwdLayout make_bwd_layout(const moe_config& c) {
   BwdLayout B;
@@ -419,7 +419,11 @@ BwdLayout make_bwd_layout(const moe_config& c) {
   B.logits = take(T * E * 4 * kRouterMaxSplits);
   B.dp = take(T * k * 4);
   B.dl = take(T * E * 4);
-  B.dwg_part = take(static_cast<size_t>(dwg_splits(c.num_tokens, c.hidden, c.num_experts)) * h * E * 4);
+  const bool tc = router_grads_on_tc(c.num_experts);
+  B.dwg_part = take(tc ? 0 : static_cast<size_t>(dwg_splits(c.num_tokens, c.hidden, c.num_experts)) * h * E * 4);
+  B.dl3 = take(tc ? T * 3 * E * 2 : 0);
+  B.wg3 = take(tc ? h * 3 * E * 2 : 0);
+  B.dwg2 = take(tc ? h * 2 * E * 4 : 0);
   B.dx_router = take(T * h * 4);
   B.dY_perm = take(R * h * 2);
   B.dH = take(R * f * 2);
@@ -983,9 +987,15 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* Wg,
   MOE_CUDA(launch_combine_bwd(Ti, hi, ki, dy, row_map, topk_prob, y_perm, dY_perm, dp, stream));
   MOE_CUDA(launch_router_bwd(Ti, Ei, ki, c.score, logits, nsplit, gate_bias, topk_idx, dp, dl,
                              stream));
-  MOE_CUDA(launch_router_param_grads(Ti, hi, Ei, x, dl, dWg, at<float>(ws, B.dwg_part),
-                                     dgate_bias, stream));
-  MOE_CUDA(launch_dx_router(Ti, hi, Ei, dl, Wg, dx_router, stream));
+  if (router_grads_on_tc(Ei)) {
+    MOE_CUDA(launch_router_grads_tc(Ti, hi, Ei, x, dl, Wg, at<void>(ws, B.dl3), at<void>(ws, B.wg3),
+                                    at<float>(ws, B.dwg2), dWg, dgate_bias, dx_router, err,
+                                    stream));
+  } else {
+    MOE_CUDA(launch_router_param_grads(Ti, hi, Ei, x, dl, dWg, at<float>(ws, B.dwg_part),
+                                       dgate_bias, stream));
+    MOE_CUDA(launch_dx_router(Ti, hi, Ei, dl, Wg, dx_router, stream));
+  }
   // experts: dgrad chain, then the token gradient, then the weight gradients
   MOE_CUDA(launch_tc_dgrad_fc2(Ei, hi, fi, rows, dY_perm, expert_offsets, W2, dH, err, stream));
   MOE_CUDA(launch_tc_fc1_bwd(Ei, hi, fi, rows, x_perm, expert_offsets, W1, W3, dH, dA, err,

@@ -113,6 +113,11 @@ cudaError_t launch_tc_wgrad(int E, int M, int N, int64_t max_rows, const void* X
                             const void* Y, int ldy, const int32_t* offsets, float* dW, int* err,
                             cudaStream_t s);
 
+// C [rows, N] fp32 (row stride ldc) = A [rows, K] . Bk [N, K]^T, bf16, one
+// dense group; K % 64 == 0, N % 256 == 0
+cudaError_t launch_tc_dense_nt_f32(int64_t rows, int K, int N, const void* A, const void* Bk,
+                                   float* C, int ldc, int* err, cudaStream_t s);
+
 // ---- backward around the GEMMs (backward.cu)
 cudaError_t launch_combine_bwd(int T, int h, int k, const void* dy, const int32_t* row_map,
                                const float* topk_prob, const float* y_perm, void* dY_perm,
@@ -126,6 +131,16 @@ cudaError_t launch_router_param_grads(int T, int h, int E, const void* x, const 
                                       float* dWg, float* part, float* dgb, cudaStream_t s);
 cudaError_t launch_dx_router(int T, int h, int E, const float* dl, const float* Wg, float* out,
                              cudaStream_t s);
+// The router's gradients on the tensor cores when E % 64 == 0: fp32 dl and
+// Wg split into bf16 hi + lo (hi = bf16(v), lo = bf16(v - hi)), staged as
+// dl3 [T, 3E] = [dl_hi | dl_lo | dl_hi] and wg3 [h, 3E] = [Wg_hi | Wg_hi |
+// Wg_lo]; dWg = x^T [dl_hi | dl_lo] with the halves added (via dwg2 [h, 2E]),
+// dx_router = dl3 . wg3^T (the lo . lo term, ~2^-16 relative, is dropped);
+// dgate_bias (if given) as on the CUDA-core path
+bool router_grads_on_tc(int E);
+cudaError_t launch_router_grads_tc(int T, int h, int E, const void* x, const float* dl,
+                                   const float* Wg, void* dl3, void* wg3, float* dwg2, float* dWg,
+                                   float* dgb, float* dx_router, int* err, cudaStream_t s);
 
 // ---- E4M3 quantisation (FP8 experts) ----
 // rows of bf16 [rows, cols] -> codes + per-row power-of-two scales (rows >=

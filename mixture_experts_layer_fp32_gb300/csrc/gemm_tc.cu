@@ -1118,6 +1118,23 @@ cudaError_t launch_tc_dgrad_fc1(int E, int h, int f, int64_t max_rows, const voi
   return launch_grouped<DGRAD_F32, false>(a, b0, b1, args, s);
 }
 
+// C [rows, N] fp32 (row stride ldc) = A [rows, K] . Bk [N, K]^T, bf16
+// operands, one dense group (the DGRAD_F32 mainloop with every K block from
+// Bk); K % 64 == 0, N % 256 == 0.  The router's dx = dl . Wg^T runs here on
+// bf16 hi/lo splits of its fp32 operands.
+cudaError_t launch_tc_dense_nt_f32(int64_t rows, int K, int N, const void* A, const void* Bk,
+                                   float* C, int ldc, int* err, cudaStream_t s) {
+  if (BK != 64) return cudaErrorNotSupported;
+  if (K % BK != 0 || N % BN != 0) return cudaErrorInvalidValue;
+  if (rows == 0) return cudaSuccess;
+  CUtensorMap a, b0;
+  if (!map_rows(&a, A, K, rows) || !map_weights_kmajor(&b0, Bk, K, N, 1))
+    return cudaErrorInvalidValue;
+  TcArgs args{nullptr, 1, N / BN, K / BK, rows, C, ldc, err};
+  args.kb_split = K / BK;
+  return launch_grouped<DGRAD_F32, false>(a, b0, b0, args, s);
+}
+
 cudaError_t launch_tc_fc1_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* xq,
                                const float* x_scale, const int32_t* row_src,
                                const int32_t* offsets, const uint8_t* W1q, const float* s1,

@@ -26,6 +26,11 @@
 //    each fill and arrives on the stage's empty barrier beside the MMA's
 //    commit), so it can neither lap the producer nor be lapped by it and
 //    every parity wait sees the phase it means.
+//  * The epilogue warps move each 32-column slice of the fp32 accumulator
+//    from TMEM to a swizzled 4 KB staging block and one lane stores it with
+//    TMA (two blocks per warp, so the store of one overlaps the drain of the
+//    next); the output is 4 bytes per element, which makes this store the
+//    bound of the GEMM when experts have few rows.
 //  * Every wait is bounded as in the forward kernel (error word, abort flag,
 //    drain before TMEM is freed).
 #include <stdlib.h>
@@ -42,8 +47,11 @@ constexpr int W_A_BYTES = 2 * W_BOX;
 constexpr int W_STAGE = W_A_BYTES + 4 * W_BOX;     // 48 KB
 constexpr int W_STAGES = 4;
 constexpr int W_THREADS = 224;                     // TMA, MMA, 4 epilogue warps, tail zeroing
-constexpr int W_PITCH = 36;
-constexpr int W_EPI_BYTES = 4 * 32 * W_PITCH * 4;
+// Output staging: per epilogue warp two 32 x 32 fp32 blocks (4 KB each) in
+// the TMA's 128-byte swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)),
+// stored by TMA while the warp drains the next 32 columns.
+constexpr int W_STG_BYTES = 4096;
+constexpr int W_EPI_BYTES = 4 * 2 * W_STG_BYTES;
 constexpr int W_NUM_BARS = 3 * W_STAGES + 5;       // full, masked, empty, acc_full[2], acc_empty[2], drain
 constexpr int W_SMEM = 1024 + W_STAGES * W_STAGE + W_EPI_BYTES + W_NUM_BARS * 8 + 16 +
                        (MOE_MAX_EXPERTS + 1) * 4;
@@ -89,14 +97,55 @@ __device__ __forceinline__ void decode_wtile(int tile, int MT, int NT, int& e, i
   n0 = nt * WN;
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+
+// One epilogue warp drains its 32 accumulator rows (TMEM lanes; output rows
+// orow .. orow+31 of dW viewed as [E*M, N]) for columns [0, valid), to
+// output columns n0 + c, 32 columns per TMA store.  Lane 0 issues the stores
+// and owns their bulk groups; `ck` counts this warp's stores across tiles
+// (staging block ck & 1, reused once the store two back has read it).
+__device__ __forceinline__ void drain_to_tma(uint32_t tb, const CUtensorMap* tmO, int orow, int n0,
+                                             int valid, bool zero, uint32_t stg, int lane,
+                                             uint32_t& ck) {
+#pragma unroll 1
+  for (int c = 0; c < valid; c += 32) {
+    uint32_t y[32];
+    ptx::tmem_ld32(tb + c, y);
+    ptx::tmem_wait_ld();
+    const uint32_t buf = stg + (ck & 1u) * W_STG_BYTES;
+    if (ck >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();
+    __syncwarp();
+    const uint32_t row = buf + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t a = row + ((j ^ (lane & 7)) << 4);
+      if (zero)
+        st_shared_v4(a, 0u, 0u, 0u, 0u);
+      else
+        st_shared_v4(a, y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      ptx::tma_store_2d(tmO, n0 + c, orow, buf);
+      ptx::bulk_commit_group();
+    }
+    ++ck;
+  }
+}
+
 __global__ void __launch_bounds__(W_THREADS, 1)
     tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
-                    WgradArgs args) {
+                    const __grid_constant__ CUtensorMap tmO, WgradArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  float* epi = reinterpret_cast<float*>(smem + W_STAGES * W_STAGE);
+  const uint32_t epi = ptx::smem_u32(smem + W_STAGES * W_STAGE);  // 1 KB aligned
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + W_STAGES * W_STAGE + W_EPI_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + W_NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -123,12 +172,15 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     ptx::fence_mbar_init();
     ptx::prefetch_tensormap(&tmX);
     ptx::prefetch_tensormap(&tmY);
+    ptx::prefetch_tensormap(&tmO);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
     ptx::tmem_relinquish();
   }
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = args.offsets[e];
+  // no offsets: one dense group over rows [0, max_rows) (E == 1)
+  for (int e = threadIdx.x; e <= E; e += blockDim.x)
+    off[e] = args.offsets ? args.offsets[e] : (e == 0 ? 0 : static_cast<int>(args.max_rows));
   __syncthreads();
   if (threadIdx.x == 0) {  // offsets must start at 0, never decrease, end within the buffers
     bool ok = off[0] == 0 && off[E] <= args.max_rows;
@@ -284,8 +336,8 @@ __global__ void __launch_bounds__(W_THREADS, 1)
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------ epilogue warps 2..5
     const int q = warp & 3;
-    float* etile = epi + q * (32 * W_PITCH);
-    const int sub = lane >> 3, col4 = (lane & 7) * 4;
+    const uint32_t stg = epi + q * 2 * W_STG_BYTES;
+    uint32_t ck = 0;
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       int e, m0, n0;
@@ -298,33 +350,13 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * WN;
-      const int mbase = m0 + q * 32;  // lane l holds output row mbase + l
-      float* out0 = args.out + (static_cast<int64_t>(e) * args.M) * args.N + n0;
-      const int valid = min(WN, args.N - n0);
-#pragma unroll 1
-      for (int c = 0; c < valid; c += 32) {
-        uint32_t y[32];
-        ptx::tmem_ld32(tb + c, y);
-        ptx::tmem_wait_ld();
-        float4* mine = reinterpret_cast<float4*>(etile + lane * W_PITCH);
-#pragma unroll
-        for (int v = 0; v < 8; ++v)
-          mine[v] = empty_expert ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                 : make_float4(__uint_as_float(y[4 * v]), __uint_as_float(y[4 * v + 1]),
-                                               __uint_as_float(y[4 * v + 2]), __uint_as_float(y[4 * v + 3]));
-        __syncwarp();
-#pragma unroll
-        for (int r8 = 0; r8 < 8; ++r8) {
-          const int r = r8 * 4 + sub;
-          *reinterpret_cast<float4*>(out0 + static_cast<int64_t>(mbase + r) * args.N + c + col4) =
-              *reinterpret_cast<const float4*>(etile + r * W_PITCH + col4);
-        }
-        __syncwarp();
-      }
+      drain_to_tma(tb, &tmO, e * args.M + m0 + q * 32, n0, min(WN, args.N - n0), empty_expert, stg,
+                   lane, ck);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ctl.acc_empty(buf));
     }
+    if (lane == 0) ptx::bulk_wait_group_all();
   }
   __syncthreads();
   if (warp == 1) {
@@ -399,12 +431,13 @@ __device__ __forceinline__ void st_cluster_zero16(uint32_t cluster_addr) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
     tc_wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmX,
-                         const __grid_constant__ CUtensorMap tmY, WgradArgs args) {
+                         const __grid_constant__ CUtensorMap tmY,
+                         const __grid_constant__ CUtensorMap tmO, WgradArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  float* epi = reinterpret_cast<float*>(smem + PW_STAGES * PW_STAGE);
+  const uint32_t epi = ptx::smem_u32(smem + PW_STAGES * PW_STAGE);  // 1 KB aligned
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PW_STAGES * PW_STAGE + W_EPI_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + PW_NUM_BARS);
   int* abort_word = reinterpret_cast<int*>(tmem_slot + 1);
@@ -435,12 +468,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
     ptx::fence_mbar_init();
     ptx::prefetch_tensormap(&tmX);
     ptx::prefetch_tensormap(&tmY);
+    ptx::prefetch_tensormap(&tmO);
   }
   if (warp == 1) {
     ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), 512);
     ptx::tmem_relinquish_pair();
   }
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = args.offsets[e];
+  // no offsets: one dense group over rows [0, max_rows) (E == 1)
+  for (int e = threadIdx.x; e <= E; e += blockDim.x)
+    off[e] = args.offsets ? args.offsets[e] : (e == 0 ? 0 : static_cast<int>(args.max_rows));
   __syncthreads();
   if (threadIdx.x == 0) {  // offsets must start at 0, never decrease, end within the buffers
     bool ok = off[0] == 0 && off[E] <= args.max_rows;
@@ -621,8 +657,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
   } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------ epilogue warps 2..5 (both CTAs)
     const int q = warp & 3;
-    float* etile = epi + q * (32 * W_PITCH);
-    const int sub = lane >> 3, col4 = (lane & 7) * 4;
+    const uint32_t stg = epi + q * 2 * W_STG_BYTES;
+    uint32_t ck = 0;
     int it = 0;
     for (int tile = pair; tile < total; tile += npairs, ++it) {
       int e, m0, n0;
@@ -636,34 +672,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * WN;
       const int mbase = m0 + static_cast<int>(rank) * 128 + q * 32;  // lane l: row mbase + l
-      if (mbase < args.M) {
-        float* out0 = args.out + (static_cast<int64_t>(e) * args.M) * args.N + n0;
-        const int valid = min(WN, args.N - n0);
-#pragma unroll 1
-        for (int c = 0; c < valid; c += 32) {
-          uint32_t y[32];
-          ptx::tmem_ld32(tb + c, y);
-          ptx::tmem_wait_ld();
-          float4* mine = reinterpret_cast<float4*>(etile + lane * W_PITCH);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            mine[v] = empty_expert ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                   : make_float4(__uint_as_float(y[4 * v]), __uint_as_float(y[4 * v + 1]),
-                                                 __uint_as_float(y[4 * v + 2]), __uint_as_float(y[4 * v + 3]));
-          __syncwarp();
-#pragma unroll
-          for (int r8 = 0; r8 < 8; ++r8) {
-            const int r = r8 * 4 + sub;
-            *reinterpret_cast<float4*>(out0 + static_cast<int64_t>(mbase + r) * args.N + c + col4) =
-                *reinterpret_cast<const float4*>(etile + r * W_PITCH + col4);
-          }
-          __syncwarp();
-        }
-      }
+      if (mbase < args.M)
+        drain_to_tma(tb, &tmO, e * args.M + mbase, n0, min(WN, args.N - n0), empty_expert, stg,
+                     lane, ck);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ctl.acc_empty(buf), 0));
     }
+    if (lane == 0) ptx::bulk_wait_group_all();
   }
   __syncthreads();
   ptx::cluster_sync();  // no cross-CTA access after this point
@@ -704,6 +720,20 @@ bool map_mn(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows, int64_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// dW [rows, N] fp32 (rows = E * M), box 32 (N) x 32 (rows), 128-byte swizzle:
+// the epilogue's TMA stores.
+bool map_out(CUtensorMap* m, float* ptr, int64_t N, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Pairs of SMs that can be resident at once for the pair kernel (0: none, or
 // the query failed).
 int wgrad_pair_slots() {
@@ -736,16 +766,20 @@ cudaError_t launch_tc_wgrad(int E, int M, int N, int64_t max_rows, const void* X
                             cudaStream_t s) {
   if (E == 0) return cudaSuccess;
   if (M % WM != 0 || N % 128 != 0) return cudaErrorInvalidValue;
+  if (offsets == nullptr && (E != 1 || max_rows > INT32_MAX)) return cudaErrorInvalidValue;
   const int64_t rows = max_rows > 0 ? max_rows : 1;  // a map needs a positive extent
-  CUtensorMap mx, my;
-  if (!map_mn(&mx, X, M, rows, ldx) || !map_mn(&my, Y, N, rows, ldy)) return cudaErrorInvalidValue;
+  CUtensorMap mx, my, mo;
+  if (!map_mn(&mx, X, M, rows, ldx) || !map_mn(&my, Y, N, rows, ldy) ||
+      !map_out(&mo, dW, N, static_cast<int64_t>(E) * M))
+    return cudaErrorInvalidValue;
   WgradArgs args{offsets, E, M, N, max_rows, dW, err};
   const char* force = getenv("MOE_TC_PAIR");
   const int slots = (force && force[0] == '0') ? 0 : wgrad_pair_slots();
   if (slots > 0) {
     const int64_t tiles = static_cast<int64_t>(E) * ((M + PW_M - 1) / PW_M) * ((N + WN - 1) / WN);
     const int64_t pairs = slots < tiles ? slots : tiles;
-    tc_wgrad_pair_kernel<<<static_cast<unsigned>(2 * pairs), W_THREADS, PW_SMEM, s>>>(mx, my, args);
+    tc_wgrad_pair_kernel<<<static_cast<unsigned>(2 * pairs), W_THREADS, PW_SMEM, s>>>(mx, my, mo,
+                                                                                       args);
     return cudaGetLastError();
   }
   static bool configured[64] = {false};
@@ -760,7 +794,7 @@ cudaError_t launch_tc_wgrad(int E, int M, int N, int64_t max_rows, const void* X
   const int64_t tiles = static_cast<int64_t>(E) * (M / WM) * ((N + WN - 1) / WN);
   int64_t grid = device_sm_count();
   if (grid > tiles) grid = tiles;
-  tc_wgrad_kernel<<<static_cast<unsigned>(grid), W_THREADS, W_SMEM, s>>>(mx, my, args);
+  tc_wgrad_kernel<<<static_cast<unsigned>(grid), W_THREADS, W_SMEM, s>>>(mx, my, mo, args);
   return cudaGetLastError();
 }
 
