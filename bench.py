@@ -526,10 +526,28 @@ def run_backward(args, moe, w, cfg, inp, b, R, flush, stream, world, rank, local
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                      "traffic": None, "algorithmic_per_launch": gemm_flops},
         "e2e": None,
-        "gpu_launches": 14 * args.steps,  # moe_backward launches 14 kernels
+        "gpu_launches": backward_launches(w) * args.steps,
         "clocks": clk,
         "peaks": peaks,
     }
+
+
+def backward_launches(w):
+    """Kernels moe_backward launches for workload w: router logits, combine
+    backward, router backward, the router's parameter and token gradients
+    (tensor-core path for E % 64 == 0: two bf16 splits, the dWg GEMM, its
+    fold, dgate_bias, the dx GEMM; else dWg (+ its split reduction), dgate_bias,
+    dx), three dgrad/recompute GEMMs, the token-gradient combine, three
+    wgrad GEMMs."""
+    if w.E >= 64 and w.E % 64 == 0:
+        router = 6
+    else:
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        small = w.E <= 32
+        tiles = (w.h + 511) // 512 if small else ((w.h + 63) // 64) * ((w.E + 63) // 64)
+        S = min(-(-4 * sms // tiles), -(-w.T // (64 if small else 256)), 128 if small else 32)
+        router = 3 + (1 if S > 1 else 0)
+    return 3 + router + 3 + 1 + 3
 
 
 def barrier(world):
