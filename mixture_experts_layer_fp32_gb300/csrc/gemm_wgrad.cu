@@ -9,7 +9,8 @@
 // Design (one CTA per SM, persistent, the roles of the forward kernel):
 //  * Tile = (expert, 128 rows of M, 256 columns of N); the accumulator is a
 //    128 x 256 fp32 block in TMEM (two buffers).  Tiles are listed expert by
-//    expert; an expert with no rows gets a zero block.
+//    expert, the smaller output dimension fastest; an expert with no rows
+//    gets a zero block.
 //  * K runs over the expert's rows in blocks of 64.  Both operands are
 //    MN-major in shared memory (X's M and Y's N contiguous): per stage two
 //    64 (M) x 64 (rows) boxes of X and four 64 (N) x 64 (rows) boxes of Y,
@@ -54,7 +55,8 @@ constexpr int W_STG_BYTES = 4096;
 constexpr int W_EPI_BYTES = 4 * 2 * W_STG_BYTES;
 constexpr int W_NUM_BARS = 3 * W_STAGES + 5;       // full, masked, empty, acc_full[2], acc_empty[2], drain
 constexpr int W_SMEM = 1024 + W_STAGES * W_STAGE + W_EPI_BYTES + W_NUM_BARS * 8 + 16 +
-                       (MOE_MAX_EXPERTS + 1) * 4;
+                       (MOE_MAX_EXPERTS + 1) * 4 + MOE_MAX_EXPERTS;
+static_assert(MOE_MAX_EXPERTS <= 256, "the expert order is kept in bytes");
 static_assert(W_SMEM <= 227 * 1024, "shared memory budget");
 // kind::f16, bf16 A and B, fp32 D, A and B MN-major (bits 15 and 16), N=256, M=128
 constexpr uint32_t W_IDESC = ptx::idesc_bf16_f32(WM, WN, /*b_mn_major=*/true) | (1u << 15);
@@ -87,13 +89,48 @@ struct WCtl {
   }
 };
 
-// Tiles listed expert by expert, row tiles (tile_m rows of M) fastest.
-__device__ __forceinline__ void decode_wtile(int tile, int MT, int NT, int& e, int& m0, int& n0,
+// The j-th tile of worker p of P (a CTA, or an SM pair), -1 past its last.
+// Balanced loads (`zig` false): tile p + j*P, experts in index order.
+// Skewed loads (`zig`: the largest expert has more than 4x the mean rows):
+// the experts are sorted by rows, most first (see decode_wtile), and the
+// tiles are taken from both ends of that list: wave j gives worker p the
+// position g = j*P + (p+j) mod P of the sequence front, back, front, back...
+// (g even: tile g/2; g odd: tile total-1-g/2).  The front tiles are long and
+// bound by the MMA, the back ones short and bound by their fp32 stores: each
+// wave puts half the workers on each kind and every worker alternates, so
+// stores and MMAs overlap across the GPU instead of all workers moving
+// through the same expert together.  Each end keeps an expert's tiles
+// together (L2 reuse of its rows); balanced loads keep one expert at a time.
+__device__ __forceinline__ int sched_tile(int j, int p, int P, int total, bool zig) {
+  if (!zig) {
+    const int tile = p + j * P;
+    return tile < total ? tile : -1;
+  }
+  const int g = j * P + (p + j) % P;
+  if (g >= total) return -1;
+  return (g & 1) ? total - 1 - (g >> 1) : (g >> 1);
+}
+
+// Tiles listed expert by expert; inside an expert the smaller of the two
+// output dimensions varies fastest (n_fast = N < M), so the tiles in flight
+// together cover all of the smaller operand's columns and a few stripes of
+// the larger one: the expert's rows of both stay in L2 while they are used
+// (the other order streams the larger operand once per stripe of the smaller).
+__device__ __forceinline__ void decode_wtile(int tile, int MT, int NT, bool n_fast,
+                                             const uint8_t* ord, int& e, int& m0, int& n0,
                                              int tile_m = WM) {
-  e = tile / (MT * NT);
-  const int u = tile - e * MT * NT;
-  const int nt = u / MT;
-  m0 = (u - nt * MT) * tile_m;
+  const int s = tile / (MT * NT);
+  e = ord[s];
+  const int u = tile - s * MT * NT;
+  int mt, nt;
+  if (n_fast) {
+    mt = u / NT;
+    nt = u - mt * NT;
+  } else {
+    nt = u / MT;
+    mt = u - nt * MT;
+  }
+  m0 = mt * tile_m;
   n0 = nt * WN;
 }
 
@@ -150,11 +187,14 @@ __global__ void __launch_bounds__(W_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + W_NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* off = reinterpret_cast<int*>(tmem_slot + 4);
+  uint8_t* ord = reinterpret_cast<uint8_t*>(off + MOE_MAX_EXPERTS + 1);
+  int* zig_word = reinterpret_cast<int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E;
   const int MT = args.M / WM, NT = (args.N + WN - 1) / WN;
   const int total = E * MT * NT;
+  const bool n_fast = args.N < args.M;
   const WCtl ctl{bars, abort_flag, args.err};
 
   if (threadIdx.x == 0) {
@@ -189,6 +229,25 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       for (int e = 0; e <= E; ++e) off[e] = 0;
       if (blockIdx.x == 0) report_error(args.err, DEV_ERR_INDEX, -1);
     }
+    int most = 0;
+    for (int e = 0; e < E; ++e) most = max(most, off[e + 1] - off[e]);
+    *zig_word = static_cast<int64_t>(most) * E > 4LL * off[E];
+  }
+  __syncthreads();
+  const bool zig = *zig_word != 0;
+  // skewed loads: experts by rows, most first (equal counts: lower index
+  // first); balanced: index order
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int n = off[e + 1] - off[e];
+    int r = e;
+    if (zig) {
+      r = 0;
+      for (int q = 0; q < E; ++q) {
+        const int m = off[q + 1] - off[q];
+        r += (m > n) || (m == n && q < e);
+      }
+    }
+    ord[r] = static_cast<uint8_t>(e);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -202,9 +261,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       uint32_t phase = 0;
       uint32_t fill_parity = 0, filled = 0;
       bool alive = true;
-      for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x) {
+      for (int j = 0, tile; alive && (tile = sched_tile(j, blockIdx.x, gridDim.x, total, zig)) >= 0; ++j) {
         int e, m0, n0;
-        decode_wtile(tile, MT, NT, e, m0, n0);
+        decode_wtile(tile, MT, NT, n_fast, ord, e, m0, n0);
         const int r0 = off[e], rows = off[e + 1] - off[e];
         const int KB = (rows + WK - 1) / WK;
         for (int kb = 0; kb < KB; ++kb) {
@@ -247,9 +306,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool alive = true;
-    for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x) {
+    for (int j = 0, tile; alive && (tile = sched_tile(j, blockIdx.x, gridDim.x, total, zig)) >= 0; ++j) {
       int e, m0, n0;
-      decode_wtile(tile, MT, NT, e, m0, n0);
+      decode_wtile(tile, MT, NT, n_fast, ord, e, m0, n0);
       const int rows = off[e + 1] - off[e];
       const int KB = (rows + WK - 1) / WK;
       for (int kb = 0; kb < KB; ++kb) {
@@ -283,9 +342,10 @@ __global__ void __launch_bounds__(W_THREADS, 1)
       uint32_t phase = 0, mpar = 0;  // mpar: per stage, parity of its next masked phase
       bool alive = true;
       int it = 0;
-      for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x, ++it) {
+      for (int j = 0, tile; alive && (tile = sched_tile(j, blockIdx.x, gridDim.x, total, zig)) >= 0;
+           ++j, ++it) {
         int e, m0, n0;
-        decode_wtile(tile, MT, NT, e, m0, n0);
+        decode_wtile(tile, MT, NT, n_fast, ord, e, m0, n0);
         const int rows = off[e + 1] - off[e];
         const int KB = (rows + WK - 1) / WK;
         const int buf = it & 1;
@@ -339,9 +399,9 @@ __global__ void __launch_bounds__(W_THREADS, 1)
     const uint32_t stg = epi + q * 2 * W_STG_BYTES;
     uint32_t ck = 0;
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+    for (int j = 0, tile; (tile = sched_tile(j, blockIdx.x, gridDim.x, total, zig)) >= 0; ++j, ++it) {
       int e, m0, n0;
-      decode_wtile(tile, MT, NT, e, m0, n0);
+      decode_wtile(tile, MT, NT, n_fast, ord, e, m0, n0);
       const bool empty_expert = off[e + 1] == off[e];
       const int buf = it & 1;
       const uint32_t aph = (it >> 1) & 1;
@@ -395,7 +455,7 @@ constexpr int PW_STAGE = 4 * W_BOX;                // 2 X boxes + 2 Y boxes: 32 
 constexpr int PW_STAGES = 6;
 constexpr int PW_NUM_BARS = 5 * PW_STAGES + 5;     // full, tfull, masked, empty, acc_*, drain
 constexpr int PW_SMEM = 1024 + PW_STAGES * PW_STAGE + W_EPI_BYTES + PW_NUM_BARS * 8 + 16 +
-                        (MOE_MAX_EXPERTS + 1) * 4;
+                        (MOE_MAX_EXPERTS + 1) * 4 + MOE_MAX_EXPERTS;
 static_assert(PW_SMEM <= 227 * 1024, "shared memory budget (pair)");
 constexpr uint32_t PW_IDESC = ptx::idesc_bf16_f32(PW_M, WN, /*b_mn_major=*/true) | (1u << 15);
 constexpr long long kPeerDrainCycles = 20000000LL;
@@ -443,6 +503,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
   int* abort_word = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* abort_flag = abort_word;
   int* off = reinterpret_cast<int*>(tmem_slot + 4);
+  uint8_t* ord = reinterpret_cast<uint8_t*>(off + MOE_MAX_EXPERTS + 1);
+  int* zig_word = reinterpret_cast<int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
@@ -450,6 +512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
   const int E = args.E;
   const int MT = (args.M + PW_M - 1) / PW_M, NT = (args.N + WN - 1) / WN;
   const int total = E * MT * NT;
+  const bool n_fast = args.N < args.M;
   const PWCtl ctl{bars, abort_flag, args.err, ptx::mapa_shared(ptx::smem_u32(abort_word), rank ^ 1u)};
 
   if (threadIdx.x == 0) {
@@ -485,6 +548,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
       for (int e = 0; e <= E; ++e) off[e] = 0;
       if (blockIdx.x == 0) report_error(args.err, DEV_ERR_INDEX, -1);
     }
+    int most = 0;
+    for (int e = 0; e < E; ++e) most = max(most, off[e + 1] - off[e]);
+    *zig_word = static_cast<int64_t>(most) * E > 4LL * off[E];
+  }
+  __syncthreads();
+  const bool zig = *zig_word != 0;
+  // skewed loads: experts by rows, most first (equal counts: lower index
+  // first); balanced: index order
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int n = off[e + 1] - off[e];
+    int r = e;
+    if (zig) {
+      r = 0;
+      for (int q = 0; q < E; ++q) {
+        const int m = off[q + 1] - off[q];
+        r += (m > n) || (m == n && q < e);
+      }
+    }
+    ord[r] = static_cast<uint8_t>(e);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -501,9 +583,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
       // completes the latest fill, parity of the next full / tfull phase
       uint32_t filled = 0, tailbits = 0, fill_parity = 0, fnext = 0, tnext = 0;
       bool alive = true;
-      for (int tile = pair; alive && tile < total; tile += npairs) {
+      for (int j = 0, tile; alive && (tile = sched_tile(j, pair, npairs, total, zig)) >= 0; ++j) {
         int e, m0, n0;
-        decode_wtile(tile, MT, NT, e, m0, n0, PW_M);
+        decode_wtile(tile, MT, NT, n_fast, ord, e, m0, n0, PW_M);
         const int r0 = off[e], rows = off[e + 1] - off[e];
         const int KB = (rows + WK - 1) / WK;
         const int mx = m0 + static_cast<int>(rank) * 128, ny = n0 + static_cast<int>(rank) * 128;
@@ -565,9 +647,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
       int stage = 0;
       uint32_t tpar = 0;  // per stage: parity of its next tfull phase
       const uint32_t peer_stages = ptx::mapa_shared(ptx::smem_u32(stages), 1);
-      for (int tile = pair; tile < total; tile += npairs) {
+      for (int j = 0, tile; (tile = sched_tile(j, pair, npairs, total, zig)) >= 0; ++j) {
         int e, m0, n0;
-        decode_wtile(tile, MT, NT, e, m0, n0, PW_M);
+        decode_wtile(tile, MT, NT, n_fast, ord, e, m0, n0, PW_M);
         const int rows = off[e + 1] - off[e];
         const int KB = (rows + WK - 1) / WK;
         bool alive = true;
@@ -604,9 +686,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
       uint32_t fpar = 0, mpar = 0;  // per stage: parity of the next full / masked phase
       bool alive = true;
       int it = 0;
-      for (int tile = pair; alive && tile < total; tile += npairs, ++it) {
+      for (int j = 0, tile; alive && (tile = sched_tile(j, pair, npairs, total, zig)) >= 0; ++j, ++it) {
         int e, m0, n0;
-        decode_wtile(tile, MT, NT, e, m0, n0, PW_M);
+        decode_wtile(tile, MT, NT, n_fast, ord, e, m0, n0, PW_M);
         const int rows = off[e + 1] - off[e];
         const int KB = (rows + WK - 1) / WK;
         const int buf = it & 1;
@@ -660,9 +742,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W_THREADS, 1)
     const uint32_t stg = epi + q * 2 * W_STG_BYTES;
     uint32_t ck = 0;
     int it = 0;
-    for (int tile = pair; tile < total; tile += npairs, ++it) {
+    for (int j = 0, tile; (tile = sched_tile(j, pair, npairs, total, zig)) >= 0; ++j, ++it) {
       int e, m0, n0;
-      decode_wtile(tile, MT, NT, e, m0, n0, PW_M);
+      decode_wtile(tile, MT, NT, n_fast, ord, e, m0, n0, PW_M);
       const bool empty_expert = off[e + 1] == off[e];
       const int buf = it & 1;
       const uint32_t aph = (it >> 1) & 1;
