@@ -62,6 +62,8 @@ def _load():
         L.oracle_backward.argtypes = [i64, i32, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp,
                                       vp, vp, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp,
                                       vp, i32]
+        L.oracle_expert_wgrad_cols.argtypes = [i64, i32, i32, vp, i32, vp, vp, i32, vp, vp, vp,
+                                               i32, i32, vp, i32, vp, vp, vp, vp, i32]
         L.oracle_e4m3_values.argtypes = [vp]
         L.oracle_e4m3_codes.argtypes = [i64, vp, vp]
         _lib = L
@@ -339,10 +341,11 @@ def forward_fp8(x, Wg, q, k, score, gate_bias=None, expert_bias=None, capacity_f
 # -------------------------------------------------------------- backward --
 
 def backward(x, Wg, W1, W3, W2, k, score, topk_idx, topk_prob, keep, dy, gate_bias=None,
-             expert_bias=None, nthreads=0):
+             expert_bias=None, nthreads=0, weight_grads=True):
     """Gradients of sum(dy * y) for the routing decisions topk_idx / keep and
     the combine weights topk_prob (as route() returns them).  Returns a dict of float64 arrays: dx [T,h],
-    dWg [h,E], dgate_bias [E], dW1/dW3 [E,h,f], dW2 [E,f,h], dlogits [T,E]."""
+    dWg [h,E], dgate_bias [E], dW1/dW3 [E,h,f], dW2 [E,f,h], dlogits [T,E];
+    weight_grads=False leaves the expert weight gradients out (None)."""
     x, dy = _c(x), _c(dy)
     Wg = _c(Wg, np.float32)
     gate_bias = _c(gate_bias, np.float32)
@@ -356,7 +359,9 @@ def backward(x, Wg, W1, W3, W2, k, score, topk_idx, topk_prob, keep, dy, gate_bi
     f = W1.shape[-1]
     wd = _dtype_code(W1)
     out = {"dx": np.empty((T, h)), "dWg": np.empty((h, E)), "dgate_bias": np.empty(E),
-           "dW1": np.empty((E, h, f)), "dW3": np.empty((E, h, f)), "dW2": np.empty((E, f, h)),
+           "dW1": np.empty((E, h, f)) if weight_grads else None,
+           "dW3": np.empty((E, h, f)) if weight_grads else None,
+           "dW2": np.empty((E, f, h)) if weight_grads else None,
            "dlogits": np.empty((T, E))}
     _load().oracle_backward(T, h, E, k, f, SCORES[score], _ptr(x), _dtype_code(x), _ptr(Wg),
                             _ptr(gate_bias), _ptr(expert_bias), _ptr(W1), _ptr(W3), _ptr(W2), wd,
@@ -366,3 +371,27 @@ def backward(x, Wg, W1, W3, W2, k, score, topk_idx, topk_prob, keep, dy, gate_bi
                             _ptr(out["dW1"]), _ptr(out["dW3"]), _ptr(out["dW2"]),
                             _ptr(out["dlogits"]), nthreads)
     return out
+
+
+def expert_wgrad_cols(x_rows, p, dy_rows, W1e, W3e, W2e, rows_c, cols_c, nthreads=0):
+    """Selected weight gradients of ONE expert from its rows: x_rows [R,h],
+    combine weights p [R], dy_rows [R,h] (dy of the tokens behind the rows),
+    weights W1e/W3e [h,f], W2e [f,h].  Returns float64 arrays dW2 rows
+    [len(rows_c), h] (dW2[c, :] for c in rows_c) and dW1 / dW3 columns
+    [h, len(cols_c)] (dW1[:, c] for c in cols_c)."""
+    x_rows, dy_rows = _c(x_rows), _c(dy_rows)
+    p = _c(p, np.float32)
+    W1e, W3e, W2e = _c(W1e), _c(W3e), _c(W2e)
+    rows_c = _c(np.asarray(rows_c), np.int32)
+    cols_c = _c(np.asarray(cols_c), np.int32)
+    R, h = x_rows.shape
+    f = W1e.shape[1]
+    n2, n13 = rows_c.size, cols_c.size
+    d2 = np.empty((n2, h))
+    d1 = np.empty((h, n13))
+    d3 = np.empty((h, n13))
+    _load().oracle_expert_wgrad_cols(R, h, f, _ptr(x_rows), _dtype_code(x_rows), _ptr(p),
+                                     _ptr(dy_rows), _dtype_code(dy_rows), _ptr(W1e), _ptr(W3e),
+                                     _ptr(W2e), _dtype_code(W1e), n2, _ptr(rows_c), n13,
+                                     _ptr(cols_c), _ptr(d2), _ptr(d1), _ptr(d3), nthreads)
+    return {"dW2_rows": d2, "dW1_cols": d1, "dW3_cols": d3}

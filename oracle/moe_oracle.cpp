@@ -139,7 +139,7 @@ double bf16_round(double v) {
 
 extern "C" {
 
-int oracle_abi_version(void) { return 4; }
+int oracle_abi_version(void) { return 5; }
 
 // [MC] §3 Gating: logits = x . Wg (+ bias) with the router math in fp32.
 // The oracle forms the exact sum in double over the exact fp32 values of x
@@ -542,7 +542,8 @@ void oracle_expert_rows_fp8(int64_t R, int h, int f, const uint8_t* xq, const fl
 // dp = 0 but stay in the renormalisation), then
 //   dWg = x^T dlogits,  dgate_bias = sum_t dlogits,  dx[t] += dlogits[t] . Wg^T.
 // All sums in double over the exact inputs.  Outputs: dx [T,h], dWg [h,E],
-// dgb [E], dW1/dW3 [E,h,f], dW2 [E,f,h], dlogits [T,E] (may be NULL).
+// dgb [E], dW1/dW3 [E,h,f], dW2 [E,f,h] (all three may be NULL: not formed),
+// dlogits [T,E] (may be NULL).
 void oracle_backward(int64_t T, int h, int E, int k, int f, int score, const void* x,
                      int x_dtype, const float* Wg, const float* gate_bias,
                      const float* expert_bias, const void* W1, const void* W3, const void* W2,
@@ -680,7 +681,7 @@ void oracle_backward(int64_t T, int h, int E, int k, int f, int score, const voi
     dgb[e] = acc;
   }
   // expert weight gradients, per expert (pairs in token order)
-  parallel_for(E, nthreads, [&](int64_t e) {
+  if (dW1 && dW3 && dW2) parallel_for(E, nthreads, [&](int64_t e) {
     for (int64_t i = 0; i < (int64_t)h * f; ++i) dW1[e * (int64_t)h * f + i] = dW3[e * (int64_t)h * f + i] = 0.0;
     for (int64_t i = 0; i < (int64_t)f * h; ++i) dW2[e * (int64_t)f * h + i] = 0.0;
     for (int64_t t = 0; t < T; ++t)
@@ -705,6 +706,63 @@ void oracle_backward(int64_t T, int h, int E, int k, int f, int score, const voi
   });
   if (dlogits_out)
     for (size_t i = 0; i < dl.size(); ++i) dlogits_out[i] = dl[i];
+}
+
+// Selected weight gradients of one expert, for checks at sizes where the
+// whole backward is out of reach: the expert's R rows are x_rows [R,h] with
+// combine weights p [R] and output gradients dy_rows [R,h] (the rows of dy
+// of the tokens behind them); W1e, W3e [h,f] and W2e [f,h] are its weights.
+// With the definitions of oracle_backward (dY = p dy, a = x.W1, g = x.W3,
+// H = silu(a) g, dH = dY.W2^T, da = dH g silu'(a), dg = dH silu(a)):
+//   for each c of rows_c (n2 of them):  dW2_rows[q,:] = sum_r H[r,c] dY[r,:]
+//   for each c of cols_c (n13):         dW1_cols[:,q] = sum_r x[r,:] da[r,c]
+//                                       dW3_cols[:,q] = sum_r x[r,:] dg[r,c]
+// Only column c of a, g, H, dH is needed for index c.  All sums in double.
+void oracle_expert_wgrad_cols(int64_t R, int h, int f, const void* x_rows, int x_dtype,
+                              const float* p, const void* dy_rows, int dy_dtype, const void* W1e,
+                              const void* W3e, const void* W2e, int w_dtype, int n2,
+                              const int32_t* rows_c, int n13, const int32_t* cols_c,
+                              double* dW2_rows, double* dW1_cols, double* dW3_cols,
+                              int nthreads) {
+  parallel_for(n2 + n13, nthreads, [&](int64_t q) {
+    const bool second = q < n2;
+    const int64_t c = second ? rows_c[q] : cols_c[q - n2];
+    std::vector<double> acc1(h, 0.0), acc3(h, 0.0);
+    for (int64_t r = 0; r < R; ++r) {
+      double a = 0.0, g = 0.0;
+      for (int i = 0; i < h; ++i) {
+        const double xi = value_at(x_rows, x_dtype, r * h + i);
+        a += xi * value_at(W1e, w_dtype, (int64_t)i * f + c);
+        g += xi * value_at(W3e, w_dtype, (int64_t)i * f + c);
+      }
+      const double sg = 1.0 / (1.0 + std::exp(-a));
+      const double pr = (double)p[r];
+      if (second) {
+        const double H = a * sg * g;
+        for (int n = 0; n < h; ++n) acc1[n] += H * pr * value_at(dy_rows, dy_dtype, r * h + n);
+      } else {
+        double dH = 0.0;
+        for (int n = 0; n < h; ++n)
+          dH += pr * value_at(dy_rows, dy_dtype, r * h + n) * value_at(W2e, w_dtype, c * h + n);
+        const double da = dH * g * sg * (1.0 + a * (1.0 - sg));
+        const double dg = dH * a * sg;
+        for (int i = 0; i < h; ++i) {
+          const double xi = value_at(x_rows, x_dtype, r * h + i);
+          acc1[i] += xi * da;
+          acc3[i] += xi * dg;
+        }
+      }
+    }
+    if (second) {
+      for (int n = 0; n < h; ++n) dW2_rows[q * h + n] = acc1[n];
+    } else {
+      const int64_t qq = q - n2;
+      for (int i = 0; i < h; ++i) {
+        dW1_cols[(int64_t)i * n13 + qq] = acc1[i];
+        dW3_cols[(int64_t)i * n13 + qq] = acc3[i];
+      }
+    }
+  });
 }
 
 // The E4M3 value of every code 0..255 (for the pins).

@@ -119,3 +119,43 @@ def test_backward_is_linear_in_dy_and_zero_for_dropped_tokens():
     # a dropped token reaches no expert; only the router term remains
     router_only = g1["dlogits"][dropped] @ p["Wg"].astype(np.float64).T
     np.testing.assert_allclose(g1["dx"][dropped], router_only, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("score,k,cf", [("softmax_post", 2, 0.0), ("sigmoid", 3, 0.0),
+                                        ("softmax_pre", 1, 0.75)])
+def test_expert_wgrad_cols_match_the_full_backward(score, k, cf):
+    # the column oracle (used where the full backward is out of reach) against
+    # the finite-difference-pinned backward: every row of dW2[e] and every
+    # column of dW1[e] / dW3[e], from the expert's kept rows in token order
+    p, dy = _problem(160 + k, T=12, E=3, eb=(score == "sigmoid"))
+    _, base = _loss(p, dy, k, score, cf, (0, 0))
+    g = oracle.backward(p["x"], p["Wg"], p["W1"], p["W3"], p["W2"], k, score, base["topk_idx"],
+                        base["topk_prob"], base["keep"], dy, p["gate_bias"], p["expert_bias"])
+    f = p["W1"].shape[-1]
+    checked = 0
+    for e in range(3):
+        pairs = [(t, j) for t in range(12) for j in range(k)
+                 if base["topk_idx"][t, j] == e and base["keep"][t, j]]
+        if not pairs:
+            continue
+        rows = np.array([t for t, _ in pairs])
+        prob = np.array([base["topk_prob"][t, j] for t, j in pairs], np.float32)
+        c = oracle.expert_wgrad_cols(p["x"][rows], prob, dy[rows], p["W1"][e], p["W3"][e],
+                                     p["W2"][e], np.arange(f), np.arange(f))
+        np.testing.assert_allclose(c["dW2_rows"], g["dW2"][e], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(c["dW1_cols"], g["dW1"][e], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(c["dW3_cols"], g["dW3"][e], rtol=1e-12, atol=1e-14)
+        checked += 1
+    assert checked >= 2
+
+
+def test_weight_grads_off_leaves_the_rest_unchanged():
+    p, dy = _problem(165)
+    _, base = _loss(p, dy, 2, "softmax_post", 0.0, (0, 0))
+    args = (p["x"], p["Wg"], p["W1"], p["W3"], p["W2"], 2, "softmax_post", base["topk_idx"],
+            base["topk_prob"], base["keep"], dy, p["gate_bias"])
+    full = oracle.backward(*args)
+    part = oracle.backward(*args, weight_grads=False)
+    for key in ("dx", "dWg", "dgate_bias", "dlogits"):
+        assert np.array_equal(full[key], part[key]), key
+    assert part["dW1"] is None and part["dW2"] is None
