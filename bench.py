@@ -473,8 +473,9 @@ def fp32_fma_rate(moe, dev, stream, iters=4096, reps=5):
 
 def run_backward(args, moe, w, cfg, inp, b, R, flush, stream, world, rank, local):
     """Time moe_backward (the saved buffers of one staged forward, a seeded dy)."""
-    if w.dtype != "bf16" or args.precision != "bf16":
-        raise SystemExit("--pass backward needs a bf16 workload and --precision bf16")
+    if w.dtype != "bf16" or args.precision != "bf16" or w.shared_f > 0:
+        raise SystemExit("--pass backward needs a bf16 workload without a shared expert "
+                         "(moe_backward covers the routed layer) and --precision bf16")
     dev = b.y.device
     g = torch.Generator(device="cpu").manual_seed(w.seed + 7)
     dy = torch.randn((w.T, w.h), generator=g).to(torch.bfloat16).to(dev)
