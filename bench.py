@@ -295,6 +295,8 @@ def run_native(args, rank, world, local):
     R = int(b.expert_offsets[-1].item())
     tpe = b.tokens_per_expert.cpu().numpy()
     if args.which == "backward":
+        if w.shared_f > 0:
+            b.h_mid_s = h_mid_s  # saved by the shared expert's forward
         return run_backward(args, moe, w, cfg, inp, b, R, flush, stream, world, rank, local)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
@@ -473,18 +475,27 @@ def fp32_fma_rate(moe, dev, stream, iters=4096, reps=5):
 
 def run_backward(args, moe, w, cfg, inp, b, R, flush, stream, world, rank, local):
     """Time moe_backward (the saved buffers of one staged forward, a seeded dy)."""
-    if w.dtype != "bf16" or args.precision != "bf16" or w.shared_f > 0:
-        raise SystemExit("--pass backward needs a bf16 workload without a shared expert "
-                         "(moe_backward covers the routed layer) and --precision bf16")
+    if w.dtype != "bf16" or args.precision != "bf16":
+        raise SystemExit("--pass backward needs a bf16 workload and --precision bf16")
     dev = b.y.device
     g = torch.Generator(device="cpu").manual_seed(w.seed + 7)
     dy = torch.randn((w.T, w.h), generator=g).to(torch.bfloat16).to(dev)
     grads = moe.Grads(cfg, dev)
-    ws = moe.alloc_workspace_backward(cfg, dev)
+    fs = w.shared_f
+    if fs > 0:
+        sgrads = moe.SharedGrads(cfg, fs, dev)
+        ws = moe.alloc_workspace_backward_shared(cfg, fs, dev)
+    else:
+        ws = moe.alloc_workspace_backward(cfg, dev)
 
     def bwd():
-        moe.backward(cfg, inp["x"], inp["Wg"], inp["gate_bias"], inp["W1"], inp["W3"], inp["W2"],
-                     b, dy, grads, ws)
+        if fs > 0:  # moe_backward_shared: the routed layer and the shared expert
+            moe.backward_shared(cfg, fs, inp["x"], inp["Wg"], inp["gate_bias"], inp["W1"],
+                                inp["W3"], inp["W2"], inp["W1s"], inp["W3s"], inp["W2s"], b, dy,
+                                grads, sgrads, ws)
+        else:
+            moe.backward(cfg, inp["x"], inp["Wg"], inp["gate_bias"], inp["W1"], inp["W3"],
+                         inp["W2"], b, dy, grads, ws)
 
     for _ in range(max(3, args.warmup)):
         bwd()
@@ -511,8 +522,8 @@ def run_backward(args, moe, w, cfg, inp, b, R, flush, stream, world, rank, local
         return None
     peaks = measured_peaks()
     # expert GEMMs of the backward: fc2 dgrad 2Rfh, fc1 recompute 4Rhf, fc1
-    # dgrad 4Rhf, wgrad 2Rfh + 4Rhf
-    gemm_flops = 16 * R * w.h * w.f
+    # dgrad 4Rhf, wgrad 2Rfh + 4Rhf; the shared expert the same over T rows
+    gemm_flops = 16 * R * w.h * w.f + 16 * w.T * w.h * fs
     achieved = gemm_flops / (ms * 1e-3) / 1e12
     return {
         "metric": "MoE bwd tokens/sec", "value": tokens_per_s, "unit": UNIT, "n_gpus": world,
@@ -548,7 +559,7 @@ def backward_launches(w):
         tiles = (w.h + 511) // 512 if small else ((w.h + 63) // 64) * ((w.E + 63) // 64)
         S = min(-(-4 * sms // tiles), -(-w.T // (64 if small else 256)), 128 if small else 32)
         router = 3 + (1 if S > 1 else 0)
-    return 3 + router + 3 + 1 + 3
+    return 3 + router + 3 + 1 + 3 + (6 if w.shared_f > 0 else 0)
 
 
 def barrier(world):

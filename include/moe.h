@@ -337,6 +337,43 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* Wg,
                         size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * Backward with the shared expert (the shared path of §11 of the Megatron
+ * Core page, y = routed output + SwiGLU_s(x), no gate): moe_backward's
+ * gradients plus the shared expert's, dx including the shared path's
+ * dx_s = [da_s | dg_s] [W1s ; W3s]^T before its one rounding.  The shared
+ * expert is the routed formula for one expert of weight 1 over every token:
+ * dH_s = dy W2s^T, a_s and g_s recomputed, dW2s = H_s^T dy, dW1s = x^T da_s,
+ * dW3s = x^T dg_s.  bf16 only; fs as in moe_shared_expert.
+ *   Extra inputs: W1s, W3s [h,fs], W2s [fs,h] bf16 and h_mid_s [T,fs] (saved by
+ *   moe_shared_expert).  Extra outputs: dW1s, dW3s [h,fs], dW2s [fs,h] fp32
+ *   (overwritten).
+ *   ws: moe_workspace_size_backward_shared bytes.
+ */
+moe_status moe_workspace_size_backward_shared(const moe_config* cfg, int32_t fs, size_t* bytes);
+moe_status moe_backward_shared(const moe_config* cfg, int32_t fs, const void* x, const float* Wg,
+                               const float* gate_bias, const void* W1, const void* W3,
+                               const void* W2, const void* W1s, const void* W3s, const void* W2s,
+                               const int32_t* topk_idx, const float* topk_prob,
+                               const int32_t* row_map, const int32_t* expert_offsets,
+                               const void* x_perm, const void* h_mid, const float* y_perm,
+                               const void* h_mid_s, const void* dy, void* dx, float* dWg,
+                               float* dgate_bias, float* dW1, float* dW3, float* dW2, float* dW1s,
+                               float* dW3s, float* dW2s, void* ws, size_t ws_bytes,
+                               moe_stream_t stream);
+
+/*
+ * The shared expert's backward alone (the counterpart of moe_shared_expert):
+ * its token gradient is ADDED to dx_acc [T,h] fp32 (the caller's running
+ * sum), its weight gradients dW1s, dW3s [h,fs], dW2s [fs,h] fp32 overwritten.
+ * Inputs as moe_backward_shared; ws: moe_workspace_size_backward_shared bytes.
+ */
+moe_status moe_shared_expert_backward(const moe_config* cfg, int32_t fs, const void* x,
+                                      const void* W1s, const void* W3s, const void* W2s,
+                                      const void* h_mid_s, const void* dy, float* dx_acc,
+                                      float* dW1s, float* dW3s, float* dW2s, void* ws,
+                                      size_t ws_bytes, moe_stream_t stream);
+
+/*
  * The layer forward over a sequence of batches held in HOST memory (not a
  * step of the method: the serving loop around moe_forward).  For each batch
  * b in [0, num_batches): its input x_host + b*x_batch_stride ([T,h] dtype)

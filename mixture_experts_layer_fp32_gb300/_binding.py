@@ -30,7 +30,8 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_c
            "moe_quantize_rows_e4m3", "moe_quantize_experts_e4m3", "moe_workspace_size_e4m3",
            "moe_permute_e4m3", "moe_grouped_mlp_e4m3", "moe_forward_e4m3",
            "moe_grouped_fc1_e4m3", "moe_grouped_fc2_e4m3", "moe_workspace_size_backward",
-           "moe_backward"]
+           "moe_backward", "moe_workspace_size_backward_shared", "moe_backward_shared",
+           "moe_shared_expert_backward"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -99,6 +100,9 @@ def lib():
             "moe_grouped_fc2_e4m3": ([cfgp] + [vp] * 7 + [vp, sz, vp], i32),
             "moe_workspace_size_backward": ([cfgp, ctypes.POINTER(sz)], i32),
             "moe_backward": ([cfgp] + [vp] * 20 + [vp, sz, vp], i32),
+            "moe_workspace_size_backward_shared": ([cfgp, i32, ctypes.POINTER(sz)], i32),
+            "moe_backward_shared": ([cfgp, i32] + [vp] * 27 + [vp, sz, vp], i32),
+            "moe_shared_expert_backward": ([cfgp, i32] + [vp] * 10 + [vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -416,6 +420,50 @@ def backward(cfg, x, Wg, gate_bias, W1, W3, W2, saved, dy, g, ws):
                               _p(saved.expert_offsets), _p(saved.x_perm), _p(saved.h_mid),
                               _p(saved.y_perm), _p(dy), _p(g.dx), _p(g.dWg), _p(g.dgate_bias),
                               _p(g.dW1), _p(g.dW3), _p(g.dW2), w, wb, _stream()), "moe_backward")
+
+
+class SharedGrads:
+    """The shared expert's weight gradients (fp32): dW1s, dW3s [h,fs], dW2s [fs,h]."""
+
+    def __init__(self, cfg, fs, device="cuda"):
+        h = cfg.hidden
+        d = torch.device(device)
+        self.dW1s = torch.empty((h, fs), dtype=torch.float32, device=d)
+        self.dW3s = torch.empty((h, fs), dtype=torch.float32, device=d)
+        self.dW2s = torch.empty((fs, h), dtype=torch.float32, device=d)
+
+
+def workspace_size_backward_shared(cfg, fs):
+    v = ctypes.c_size_t()
+    _check(lib().moe_workspace_size_backward_shared(ctypes.byref(cfg), int(fs), ctypes.byref(v)),
+           "moe_workspace_size_backward_shared")
+    return v.value
+
+
+def alloc_workspace_backward_shared(cfg, fs, device="cuda"):
+    return torch.zeros(workspace_size_backward_shared(cfg, fs), dtype=torch.uint8, device=device)
+
+
+def backward_shared(cfg, fs, x, Wg, gate_bias, W1, W3, W2, W1s, W3s, W2s, saved, dy, g, gs, ws):
+    """The layer backward with the shared expert: saved as for backward() plus
+    h_mid_s; g: Grads (dx includes the shared path), gs: SharedGrads."""
+    w, wb = _ws(ws)
+    _check(lib().moe_backward_shared(
+        ctypes.byref(cfg), int(fs), _p(x), _p(Wg), _p(gate_bias), _p(W1), _p(W3), _p(W2),
+        _p(W1s), _p(W3s), _p(W2s), _p(saved.topk_idx), _p(saved.topk_prob), _p(saved.row_map),
+        _p(saved.expert_offsets), _p(saved.x_perm), _p(saved.h_mid), _p(saved.y_perm),
+        _p(saved.h_mid_s), _p(dy), _p(g.dx), _p(g.dWg), _p(g.dgate_bias), _p(g.dW1), _p(g.dW3),
+        _p(g.dW2), _p(gs.dW1s), _p(gs.dW3s), _p(gs.dW2s), w, wb, _stream()),
+        "moe_backward_shared")
+
+
+def shared_expert_backward(cfg, fs, x, W1s, W3s, W2s, h_mid_s, dy, dx_acc, gs, ws):
+    """The shared expert's backward alone: its dx is ADDED to dx_acc (fp32 [T,h])."""
+    w, wb = _ws(ws)
+    _check(lib().moe_shared_expert_backward(ctypes.byref(cfg), int(fs), _p(x), _p(W1s), _p(W3s),
+                                            _p(W2s), _p(h_mid_s), _p(dy), _p(dx_acc),
+                                            _p(gs.dW1s), _p(gs.dW3s), _p(gs.dW2s), w, wb,
+                                            _stream()), "moe_shared_expert_backward")
 
 
 def probe_fp32_fma(iters, out):

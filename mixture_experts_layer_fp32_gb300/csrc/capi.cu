@@ -402,10 +402,13 @@ moe_status do_mlp_e4m3(const moe_config& c, const uint8_t* xperm_q, const float*
 // Backward workspace: error word, router partial logits [S,T,E], dp [T,k],
 // dlogits [T,E], dWg partial sums, dx_router [T,h] fp32, dY_perm [T*k,h] bf16, dH [T*k,f] bf16,
 // dA = [da | dg] [T*k,2f] bf16, dx_perm [T*k,h] fp32.
+// moe_backward's workspace; with a shared expert of width fs (> 0), its dH_s
+// [T,fs] and dA_s [T,2fs] (bf16) follow.
 struct BwdLayout {
-  size_t err, logits, dp, dl, dwg_part, dl3, wg3, dwg2, dx_router, dY_perm, dH, dA, dx_perm, total;
+  size_t err, logits, dp, dl, dwg_part, dl3, wg3, dwg2, dx_router, dY_perm, dH, dA, dx_perm;
+  size_t dH_s, dA_s, total;
 };
-BwdLayout make_bwd_layout(const moe_config& c) {
+BwdLayout make_bwd_layout(const moe_config& c, int32_t fs = 0) {
   BwdLayout B;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -429,6 +432,9 @@ BwdLayout make_bwd_layout(const moe_config& c) {
   B.dH = take(R * f * 2);
   B.dA = take(R * 2 * f * 2);
   B.dx_perm = take(R * h * 4);
+  const size_t F = fs > 0 ? static_cast<size_t>(fs) : 0;
+  B.dH_s = take(T * F * 2);
+  B.dA_s = take(T * 2 * F * 2);
   B.total = o;
   return B;
 }
@@ -482,6 +488,130 @@ HostLayout make_host_layout(const moe_config& c) {
   }
   H.total = o;
   return H;
+}
+
+// The shared expert's backward (dense, over all T tokens, weight 1): the
+// dgrad chain with its dx added to dx_acc (fp32 [T,h]), then its weight
+// gradients.  The first half runs before the routed token-gradient combine,
+// the second after it (see do_backward).
+struct SharedBwd {
+  int32_t fs;
+  const void *W1s, *W3s, *W2s, *h_mid_s;
+  float *dW1s, *dW3s, *dW2s;
+};
+moe_status shared_bwd_dgrad(const moe_config& c, const SharedBwd& sh, const void* x,
+                            const void* dy, float* dx_acc, void* dH_s, void* dA_s, int* err,
+                            cudaStream_t s) {
+  const int T = c.num_tokens, h = c.hidden, fs = sh.fs;
+  MOE_CUDA(launch_tc_dgrad_fc2(1, h, fs, T, dy, nullptr, sh.W2s, dH_s, err, s));
+  MOE_CUDA(launch_tc_fc1_bwd(1, h, fs, T, x, nullptr, sh.W1s, sh.W3s, dH_s, dA_s, err, s));
+  MOE_CUDA(launch_tc_dgrad_fc1(1, h, fs, T, dA_s, nullptr, sh.W1s, sh.W3s, dx_acc, err, s,
+                               /*accumulate=*/true));
+  return MOE_OK;
+}
+moe_status shared_bwd_wgrad(const moe_config& c, const SharedBwd& sh, const void* x,
+                            const void* dy, const void* dA_s, int* err, cudaStream_t s) {
+  const int T = c.num_tokens, h = c.hidden, fs = sh.fs;
+  MOE_CUDA(launch_tc_wgrad(1, fs, h, T, sh.h_mid_s, fs, dy, h, nullptr, sh.dW2s, err, s));
+  MOE_CUDA(launch_tc_wgrad(1, h, fs, T, x, h, dA_s, 2 * fs, nullptr, sh.dW1s, err, s));
+  MOE_CUDA(launch_tc_wgrad(1, h, fs, T, x, h, static_cast<const __nv_bfloat16*>(dA_s) + fs,
+                           2 * fs, nullptr, sh.dW3s, err, s));
+  return MOE_OK;
+}
+
+moe_status check_shared_bwd(const moe_config& c, const SharedBwd& sh) {
+  MOE_TRY(validate_fs(c, sh.fs));
+  const size_t T = c.num_tokens, h = c.hidden, fs = sh.fs;
+  MOE_TRY(need(sh.W1s, h * fs, 16));
+  MOE_TRY(need(sh.W3s, h * fs, 16));
+  MOE_TRY(need(sh.W2s, h * fs, 16));
+  MOE_TRY(need(sh.h_mid_s, T * fs, 16));
+  MOE_TRY(need(sh.dW1s, h * fs, 16));
+  MOE_TRY(need(sh.dW3s, h * fs, 16));
+  MOE_TRY(need(sh.dW2s, h * fs, 16));
+  return MOE_OK;
+}
+
+moe_status do_backward(const moe_config* cfg, const void* x, const float* Wg,
+                       const float* gate_bias, const void* W1, const void* W3, const void* W2,
+                       const int32_t* topk_idx, const float* topk_prob, const int32_t* row_map,
+                       const int32_t* expert_offsets, const void* x_perm, const void* h_mid,
+                       const float* y_perm, const void* dy, void* dx, float* dWg,
+                       float* dgate_bias, float* dW1, float* dW3, float* dW2,
+                       const SharedBwd* sh, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (sh) MOE_TRY(check_shared_bwd(c, *sh));
+  const size_t T = c.num_tokens, E = c.num_experts, k = c.topk, h = c.hidden, f = c.ffn_hidden;
+  const size_t R = T * k, wsz = E * h * f;
+  MOE_TRY(need(x, T * h, 16));
+  MOE_TRY(need(Wg, h * E, 4));
+  MOE_TRY(optional(gate_bias, 4));
+  MOE_TRY(need(W1, wsz, 16));
+  MOE_TRY(need(W3, wsz, 16));
+  MOE_TRY(need(W2, wsz, 16));
+  MOE_TRY(need(topk_idx, T * k, 4));
+  MOE_TRY(need(topk_prob, T * k, 4));
+  MOE_TRY(need(row_map, T * k, 4));
+  MOE_TRY(need(expert_offsets, E + 1, 4));
+  MOE_TRY(need(x_perm, R * h, 16));
+  MOE_TRY(need(h_mid, R * f, 16));
+  MOE_TRY(need(y_perm, R * h, 16));
+  MOE_TRY(need(dy, T * h, 16));
+  MOE_TRY(need(dx, T * h, 16));
+  MOE_TRY(need(dWg, h * E, 4));
+  MOE_TRY(optional(dgate_bias, 4));
+  MOE_TRY(need(dW1, wsz, 16));
+  MOE_TRY(need(dW3, wsz, 16));
+  MOE_TRY(need(dW2, wsz, 16));
+  const BwdLayout B = make_bwd_layout(c, sh ? sh->fs : 0);
+  MOE_TRY(check_ws(c, ws, ws_bytes, B.total));
+  int* err = at<int>(ws, B.err);
+  const int Ti = c.num_tokens, Ei = c.num_experts, ki = c.topk, hi = c.hidden, fi = c.ffn_hidden;
+  const int64_t rows = static_cast<int64_t>(R);
+  float* logits = at<float>(ws, B.logits);
+  float* dp = at<float>(ws, B.dp);
+  float* dl = at<float>(ws, B.dl);
+  float* dx_router = at<float>(ws, B.dx_router);
+  void* dY_perm = at<void>(ws, B.dY_perm);
+  void* dH = at<void>(ws, B.dH);
+  void* dA = at<void>(ws, B.dA);
+  float* dx_perm = at<float>(ws, B.dx_perm);
+  // router: logits again (the forward does not keep them), then its gradients
+  int nsplit = 1;
+  MOE_CUDA(launch_router_logits(Ti, hi, Ei, c.dtype, x, Wg, logits, &nsplit, stream));
+  MOE_CUDA(launch_combine_bwd(Ti, hi, ki, dy, row_map, topk_prob, y_perm, dY_perm, dp, stream));
+  MOE_CUDA(launch_router_bwd(Ti, Ei, ki, c.score, logits, nsplit, gate_bias, topk_idx, dp, dl,
+                             stream));
+  if (router_grads_on_tc(Ei)) {
+    MOE_CUDA(launch_router_grads_tc(Ti, hi, Ei, x, dl, Wg, at<void>(ws, B.dl3), at<void>(ws, B.wg3),
+                                    at<float>(ws, B.dwg2), dWg, dgate_bias, dx_router, err,
+                                    stream));
+  } else {
+    MOE_CUDA(launch_router_param_grads(Ti, hi, Ei, x, dl, dWg, at<float>(ws, B.dwg_part),
+                                       dgate_bias, stream));
+    MOE_CUDA(launch_dx_router(Ti, hi, Ei, dl, Wg, dx_router, stream));
+  }
+  // experts: dgrad chain, then the token gradient, then the weight gradients
+  MOE_CUDA(launch_tc_dgrad_fc2(Ei, hi, fi, rows, dY_perm, expert_offsets, W2, dH, err, stream));
+  MOE_CUDA(launch_tc_fc1_bwd(Ei, hi, fi, rows, x_perm, expert_offsets, W1, W3, dH, dA, err,
+                             stream));
+  MOE_CUDA(launch_tc_dgrad_fc1(Ei, hi, fi, rows, dA, expert_offsets, W1, W3, dx_perm, err,
+                               stream));
+  if (sh)  // the shared expert's dx joins dx_router before the one rounding
+    MOE_TRY(shared_bwd_dgrad(c, *sh, x, dy, dx_router, at<void>(ws, B.dH_s), at<void>(ws, B.dA_s),
+                             err, stream));
+  MOE_CUDA(launch_combine(Ti, hi, ki, c.dtype, dx_perm, row_map, nullptr, dx_router, dx, stream));
+  MOE_CUDA(launch_tc_wgrad(Ei, fi, hi, rows, h_mid, fi, dY_perm, hi, expert_offsets, dW2, err,
+                           stream));
+  MOE_CUDA(launch_tc_wgrad(Ei, hi, fi, rows, x_perm, hi, dA, 2 * fi, expert_offsets, dW1, err,
+                           stream));
+  MOE_CUDA(launch_tc_wgrad(Ei, hi, fi, rows, x_perm, hi,
+                           static_cast<const __nv_bfloat16*>(dA) + fi, 2 * fi, expert_offsets,
+                           dW3, err, stream));
+  if (sh) MOE_TRY(shared_bwd_wgrad(c, *sh, x, dy, at<void>(ws, B.dA_s), err, stream));
+  return MOE_OK;
 }
 
 }  // namespace
@@ -943,74 +1073,56 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* Wg,
                         const float* y_perm, const void* dy, void* dx, float* dWg,
                         float* dgate_bias, float* dW1, float* dW3, float* dW2, void* ws,
                         size_t ws_bytes, moe_stream_t stream) {
+  return do_backward(cfg, x, Wg, gate_bias, W1, W3, W2, topk_idx, topk_prob, row_map,
+                     expert_offsets, x_perm, h_mid, y_perm, dy, dx, dWg, dgate_bias, dW1, dW3, dW2,
+                     nullptr, ws, ws_bytes, stream);
+}
+
+moe_status moe_workspace_size_backward_shared(const moe_config* cfg, int32_t fs, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(validate_fs(*cfg, fs));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = make_bwd_layout(*cfg, fs).total;
+  return MOE_OK;
+}
+
+moe_status moe_backward_shared(const moe_config* cfg, int32_t fs, const void* x, const float* Wg,
+                               const float* gate_bias, const void* W1, const void* W3,
+                               const void* W2, const void* W1s, const void* W3s, const void* W2s,
+                               const int32_t* topk_idx, const float* topk_prob,
+                               const int32_t* row_map, const int32_t* expert_offsets,
+                               const void* x_perm, const void* h_mid, const float* y_perm,
+                               const void* h_mid_s, const void* dy, void* dx, float* dWg,
+                               float* dgate_bias, float* dW1, float* dW3, float* dW2, float* dW1s,
+                               float* dW3s, float* dW2s, void* ws, size_t ws_bytes,
+                               moe_stream_t stream) {
+  const SharedBwd sh{fs, W1s, W3s, W2s, h_mid_s, dW1s, dW3s, dW2s};
+  return do_backward(cfg, x, Wg, gate_bias, W1, W3, W2, topk_idx, topk_prob, row_map,
+                     expert_offsets, x_perm, h_mid, y_perm, dy, dx, dWg, dgate_bias, dW1, dW3, dW2,
+                     &sh, ws, ws_bytes, stream);
+}
+
+moe_status moe_shared_expert_backward(const moe_config* cfg, int32_t fs, const void* x,
+                                      const void* W1s, const void* W3s, const void* W2s,
+                                      const void* h_mid_s, const void* dy, float* dx_acc,
+                                      float* dW1s, float* dW3s, float* dW2s, void* ws,
+                                      size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
   if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
-  const size_t T = c.num_tokens, E = c.num_experts, k = c.topk, h = c.hidden, f = c.ffn_hidden;
-  const size_t R = T * k, wsz = E * h * f;
+  const SharedBwd sh{fs, W1s, W3s, W2s, h_mid_s, dW1s, dW3s, dW2s};
+  MOE_TRY(check_shared_bwd(c, sh));
+  const size_t T = c.num_tokens, h = c.hidden;
   MOE_TRY(need(x, T * h, 16));
-  MOE_TRY(need(Wg, h * E, 4));
-  MOE_TRY(optional(gate_bias, 4));
-  MOE_TRY(need(W1, wsz, 16));
-  MOE_TRY(need(W3, wsz, 16));
-  MOE_TRY(need(W2, wsz, 16));
-  MOE_TRY(need(topk_idx, T * k, 4));
-  MOE_TRY(need(topk_prob, T * k, 4));
-  MOE_TRY(need(row_map, T * k, 4));
-  MOE_TRY(need(expert_offsets, E + 1, 4));
-  MOE_TRY(need(x_perm, R * h, 16));
-  MOE_TRY(need(h_mid, R * f, 16));
-  MOE_TRY(need(y_perm, R * h, 16));
   MOE_TRY(need(dy, T * h, 16));
-  MOE_TRY(need(dx, T * h, 16));
-  MOE_TRY(need(dWg, h * E, 4));
-  MOE_TRY(optional(dgate_bias, 4));
-  MOE_TRY(need(dW1, wsz, 16));
-  MOE_TRY(need(dW3, wsz, 16));
-  MOE_TRY(need(dW2, wsz, 16));
-  const BwdLayout B = make_bwd_layout(c);
+  MOE_TRY(need(dx_acc, T * h, 16));
+  const BwdLayout B = make_bwd_layout(c, fs);
   MOE_TRY(check_ws(c, ws, ws_bytes, B.total));
   int* err = at<int>(ws, B.err);
-  const int Ti = c.num_tokens, Ei = c.num_experts, ki = c.topk, hi = c.hidden, fi = c.ffn_hidden;
-  const int64_t rows = static_cast<int64_t>(R);
-  float* logits = at<float>(ws, B.logits);
-  float* dp = at<float>(ws, B.dp);
-  float* dl = at<float>(ws, B.dl);
-  float* dx_router = at<float>(ws, B.dx_router);
-  void* dY_perm = at<void>(ws, B.dY_perm);
-  void* dH = at<void>(ws, B.dH);
-  void* dA = at<void>(ws, B.dA);
-  float* dx_perm = at<float>(ws, B.dx_perm);
-  // router: logits again (the forward does not keep them), then its gradients
-  int nsplit = 1;
-  MOE_CUDA(launch_router_logits(Ti, hi, Ei, c.dtype, x, Wg, logits, &nsplit, stream));
-  MOE_CUDA(launch_combine_bwd(Ti, hi, ki, dy, row_map, topk_prob, y_perm, dY_perm, dp, stream));
-  MOE_CUDA(launch_router_bwd(Ti, Ei, ki, c.score, logits, nsplit, gate_bias, topk_idx, dp, dl,
-                             stream));
-  if (router_grads_on_tc(Ei)) {
-    MOE_CUDA(launch_router_grads_tc(Ti, hi, Ei, x, dl, Wg, at<void>(ws, B.dl3), at<void>(ws, B.wg3),
-                                    at<float>(ws, B.dwg2), dWg, dgate_bias, dx_router, err,
-                                    stream));
-  } else {
-    MOE_CUDA(launch_router_param_grads(Ti, hi, Ei, x, dl, dWg, at<float>(ws, B.dwg_part),
-                                       dgate_bias, stream));
-    MOE_CUDA(launch_dx_router(Ti, hi, Ei, dl, Wg, dx_router, stream));
-  }
-  // experts: dgrad chain, then the token gradient, then the weight gradients
-  MOE_CUDA(launch_tc_dgrad_fc2(Ei, hi, fi, rows, dY_perm, expert_offsets, W2, dH, err, stream));
-  MOE_CUDA(launch_tc_fc1_bwd(Ei, hi, fi, rows, x_perm, expert_offsets, W1, W3, dH, dA, err,
-                             stream));
-  MOE_CUDA(launch_tc_dgrad_fc1(Ei, hi, fi, rows, dA, expert_offsets, W1, W3, dx_perm, err,
-                               stream));
-  MOE_CUDA(launch_combine(Ti, hi, ki, c.dtype, dx_perm, row_map, nullptr, dx_router, dx, stream));
-  MOE_CUDA(launch_tc_wgrad(Ei, fi, hi, rows, h_mid, fi, dY_perm, hi, expert_offsets, dW2, err,
+  MOE_TRY(shared_bwd_dgrad(c, sh, x, dy, dx_acc, at<void>(ws, B.dH_s), at<void>(ws, B.dA_s), err,
                            stream));
-  MOE_CUDA(launch_tc_wgrad(Ei, hi, fi, rows, x_perm, hi, dA, 2 * fi, expert_offsets, dW1, err,
-                           stream));
-  MOE_CUDA(launch_tc_wgrad(Ei, hi, fi, rows, x_perm, hi,
-                           static_cast<const __nv_bfloat16*>(dA) + fi, 2 * fi, expert_offsets,
-                           dW3, err, stream));
-  return MOE_OK;
+  return shared_bwd_wgrad(c, sh, x, dy, at<void>(ws, B.dA_s), err, stream);
 }
 
 moe_status moe_workspace_size_host(const moe_config* cfg, size_t* bytes) {

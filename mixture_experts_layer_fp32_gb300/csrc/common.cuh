@@ -95,7 +95,8 @@ cudaError_t launch_tc_fc2_e4m3(int E, int h, int f, int64_t max_rows, const uint
 
 // backward (bf16): fc2 dgrad dH [rows,f] = dY [rows,h] . W2[e]^T; fc1 recompute
 // with the SwiGLU backward dA [rows,2f] = [da | dg] from dH; fc1 dgrad
-// dX [rows,h] fp32 = dA . [W1[e] ; W3[e]]^T
+// dX [rows,h] fp32 = dA . [W1[e] ; W3[e]]^T (added to dX when accumulate).
+// With no offsets each runs as one dense group over rows [0, max_rows) (E = 1).
 cudaError_t launch_tc_dgrad_fc2(int E, int h, int f, int64_t max_rows, const void* dY,
                                 const int32_t* offsets, const void* W2, void* dH, int* err,
                                 cudaStream_t s);
@@ -104,7 +105,7 @@ cudaError_t launch_tc_fc1_bwd(int E, int h, int f, int64_t max_rows, const void*
                               const void* dH, void* dA, int* err, cudaStream_t s);
 cudaError_t launch_tc_dgrad_fc1(int E, int h, int f, int64_t max_rows, const void* dA,
                                 const int32_t* offsets, const void* W1, const void* W3,
-                                float* dX, int* err, cudaStream_t s);
+                                float* dX, int* err, cudaStream_t s, bool accumulate = false);
 
 // wgrad: dW [E, M, N] fp32 = per expert X_e^T . Y_e over the expert's rows
 // (X [rows, M] with row stride ldx, Y [rows, N] with row stride ldy, bf16);

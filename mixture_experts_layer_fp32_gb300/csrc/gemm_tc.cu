@@ -119,6 +119,8 @@ struct TcArgs {
   const void* aux = nullptr;
   int ldaux = 0;
   int kb_split = 0;
+  // DGRAD_F32: add to the output instead of overwriting it
+  int accumulate = 0;
 };
 
 // Barriers of an NS-stage ring: full[NS], empty[NS], acc_full[2],
@@ -387,10 +389,16 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, int
 #pragma unroll
       for (int it = 0; it < 8; ++it) {
         const int r = it * 4 + sub;
-        const float4 val = *reinterpret_cast<const float4*>(etile + r * EPI_PITCH + col4);
-        if (rbase + r < rend)
-          *reinterpret_cast<float4*>(out0 + static_cast<int64_t>(rbase + r) * args.ldo + c +
-                                     col4) = val;
+        float4 val = *reinterpret_cast<const float4*>(etile + r * EPI_PITCH + col4);
+        if (rbase + r < rend) {
+          float4* dst = reinterpret_cast<float4*>(out0 + static_cast<int64_t>(rbase + r) * args.ldo +
+                                                  c + col4);
+          if (MODE == DGRAD_F32 && args.accumulate) {
+            const float4 o = *dst;
+            val = make_float4(o.x + val.x, o.y + val.y, o.z + val.z, o.w + val.w);
+          }
+          *dst = val;
+        }
       }
       __syncwarp();
     }
@@ -1106,7 +1114,7 @@ cudaError_t launch_tc_fc1_bwd(int E, int h, int f, int64_t max_rows, const void*
 
 cudaError_t launch_tc_dgrad_fc1(int E, int h, int f, int64_t max_rows, const void* dA,
                                 const int32_t* offsets, const void* W1, const void* W3,
-                                float* dX, int* err, cudaStream_t s) {
+                                float* dX, int* err, cudaStream_t s, bool accumulate) {
   if (BK != 64) return cudaErrorNotSupported;
   if (max_rows == 0) return cudaSuccess;
   CUtensorMap a, b0, b1;
@@ -1115,6 +1123,7 @@ cudaError_t launch_tc_dgrad_fc1(int E, int h, int f, int64_t max_rows, const voi
     return cudaErrorInvalidValue;
   TcArgs args{offsets, E, h / BN, 2 * f / BK, max_rows, dX, h, err};
   args.kb_split = f / BK;
+  args.accumulate = accumulate ? 1 : 0;
   return launch_grouped<DGRAD_F32, false>(a, b0, b1, args, s);
 }
 

@@ -373,6 +373,22 @@ def backward(x, Wg, W1, W3, W2, k, score, topk_idx, topk_prob, keep, dy, gate_bi
     return out
 
 
+def shared_backward(x, W1s, W3s, W2s, dy, nthreads=0):
+    """Gradients of sum(dy * Y_shared) for the shared expert (weights W1s,
+    W3s [h,fs], W2s [fs,h]): the routed backward of ONE expert that every
+    token reaches with weight 1 (E = 1, k = 1, softmax after top-1: the
+    softmax over one logit is exactly 1 and passes no gradient to the
+    router).  Returns float64 dx [T,h], dW1s, dW3s [h,fs], dW2s [fs,h]."""
+    x = _c(x)
+    T, h = x.shape
+    one = np.zeros((T, 1), np.int32)
+    g = backward(x, np.zeros((h, 1), np.float32), _c(W1s)[None], _c(W3s)[None], _c(W2s)[None],
+                 1, "softmax_post", one, np.ones((T, 1), np.float32), np.ones((T, 1), np.uint8),
+                 dy, nthreads=nthreads)
+    assert not np.any(g["dlogits"]), "one expert of weight 1 passes no router gradient"
+    return {"dx": g["dx"], "dW1s": g["dW1"][0], "dW3s": g["dW3"][0], "dW2s": g["dW2"][0]}
+
+
 def expert_wgrad_cols(x_rows, p, dy_rows, W1e, W3e, W2e, rows_c, cols_c, nthreads=0):
     """Selected weight gradients of ONE expert from its rows: x_rows [R,h],
     combine weights p [R], dy_rows [R,h] (dy of the tokens behind the rows),

@@ -179,6 +179,40 @@ def test_shared_expert_host_checks(moe):
                                   None) == INVALID
 
 
+def test_backward_shared_host_checks(moe):
+    lib = moe.lib()
+    cfg = moe.config(T=128, h=4096, E=8, k=2, f=1536)
+    size, base = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.moe_workspace_size_backward(ctypes.byref(cfg), ctypes.byref(base)) == OK
+    assert lib.moe_workspace_size_backward_shared(ctypes.byref(cfg), 0, ctypes.byref(size)) == INVALID
+    assert lib.moe_workspace_size_backward_shared(ctypes.byref(cfg), 200,
+                                                  ctypes.byref(size)) == UNSUPPORTED
+    assert lib.moe_workspace_size_backward_shared(ctypes.byref(cfg), 256, ctypes.byref(size)) == OK
+    # the routed backward's workspace + dH_s [T,256] + dA_s [T,512] bf16
+    assert size.value >= base.value + 128 * 256 * 2 + 128 * 512 * 2
+    f32 = moe.config(T=16, h=136, E=4, k=2, f=200, dtype="f32")
+    assert lib.moe_workspace_size_backward_shared(ctypes.byref(f32), 72,
+                                                  ctypes.byref(size)) == UNSUPPORTED
+    need = size.value
+    # moe_backward_shared: W1s missing, then a misaligned dW2s, then the routed-only workspace
+    args = [FAKE] * 27
+    args[6] = None                                   # W1s
+    assert lib.moe_backward_shared(ctypes.byref(cfg), 256, *args, FAKE, need, None) == INVALID
+    args = [FAKE] * 27
+    args[26] = MISALIGNED                            # dW2s
+    assert lib.moe_backward_shared(ctypes.byref(cfg), 256, *args, FAKE, need, None) == INVALID
+    args = [FAKE] * 27
+    assert lib.moe_backward_shared(ctypes.byref(cfg), 256, *args, FAKE, base.value,
+                                   None) == WORKSPACE
+    # moe_shared_expert_backward: dx_acc missing; fp32 refused
+    assert lib.moe_shared_expert_backward(ctypes.byref(cfg), 256, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                          FAKE, None, FAKE, FAKE, FAKE, FAKE, need,
+                                          None) == INVALID
+    assert lib.moe_shared_expert_backward(ctypes.byref(f32), 72, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                          FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need,
+                                          None) == UNSUPPORTED
+
+
 @pytest.mark.parametrize("E,k,G,gk,want", [
     (256, 8, 8, 4, OK), (256, 8, 1, 0, OK), (256, 8, 0, 5, OK),   # off when num_groups <= 1
     (256, 8, 6, 2, UNSUPPORTED),    # E not a multiple of the groups

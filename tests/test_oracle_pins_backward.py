@@ -159,3 +159,53 @@ def test_weight_grads_off_leaves_the_rest_unchanged():
     for key in ("dx", "dWg", "dgate_bias", "dlogits"):
         assert np.array_equal(full[key], part[key]), key
     assert part["dW1"] is None and part["dW2"] is None
+
+
+@pytest.mark.parametrize("score,k,cf", [("softmax_post", 2, 0.0), ("sigmoid", 3, 0.0),
+                                        ("softmax_pre", 1, 0.75)])
+def test_shared_expert_backward_matches_finite_differences(score, k, cf):
+    # the layer with a shared expert (y = routed + SwiGLU_s(x)): routed
+    # backward + oracle.shared_backward against central differences of the
+    # whole forward, for x and the shared weights
+    p, dy = _problem(170 + k, eb=(score == "sigmoid"))
+    r = rng(171)
+    h = p["x"].shape[1]
+    fs = 5
+    p.update({"W1s": (0.5 * r.standard_normal((h, fs))).astype(np.float32),
+              "W3s": (0.5 * r.standard_normal((h, fs))).astype(np.float32),
+              "W2s": (0.5 * r.standard_normal((fs, h))).astype(np.float32)})
+
+    def loss(q):
+        out = oracle.forward(q["x"], q["Wg"], q["W1"], q["W3"], q["W2"], k, score,
+                             q["gate_bias"], q["expert_bias"], capacity_factor=cf,
+                             W1s=q["W1s"], W3s=q["W3s"], W2s=q["W2s"])
+        return float(np.sum(dy.astype(np.float64) * out["y"])), out
+
+    L0, base = loss(p)
+    g = oracle.backward(p["x"], p["Wg"], p["W1"], p["W3"], p["W2"], k, score, base["topk_idx"],
+                        base["topk_prob"], base["keep"], dy, p["gate_bias"], p["expert_bias"])
+    gs = oracle.shared_backward(p["x"], p["W1s"], p["W3s"], p["W2s"], dy)
+    grads = {"x": g["dx"] + gs["dx"], "W1s": gs["dW1s"], "W3s": gs["dW3s"], "W2s": gs["dW2s"]}
+    pick = rng(172)
+    checked = 0
+    for name, an_all in grads.items():
+        arr = p[name]
+        for flat in pick.choice(arr.size, size=min(arr.size, 12), replace=False):
+            idx = np.unravel_index(flat, arr.shape)
+            v = float(arr[idx])
+            d = 1e-3 * max(1.0, abs(v))
+            plus, minus = dict(p), dict(p)
+            plus[name], minus[name] = arr.copy(), arr.copy()
+            plus[name][idx] = np.float32(v + d)
+            minus[name][idx] = np.float32(v - d)
+            lp, op = loss(plus)
+            lm, om = loss(minus)
+            if not all(np.array_equal(o["topk_idx"], base["topk_idx"]) and
+                       np.array_equal(o["keep"], base["keep"]) for o in (op, om)):
+                continue
+            fd = (lp - lm) / (float(plus[name][idx]) - float(minus[name][idx]))
+            an = an_all[idx]
+            tol = 1e-3 if name == "x" else 2e-5   # x reaches the router's fp32 roundings
+            assert abs(fd - an) <= tol * (abs(an) + 1.0), (name, idx, fd, an)
+            checked += 1
+    assert checked >= 30
