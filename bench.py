@@ -71,6 +71,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay of the step (an extra measurement)")
     ap.add_argument("--precision", default="bf16", choices=["bf16", "e4m3"],
                     help="expert GEMM operands: bf16 (the default workload) or E4M3 (FP8 "
                          "experts, weights quantised once outside the timed region)")
@@ -391,6 +393,35 @@ def run_native(args, rank, world, local):
                          "exceed" if 3 * w.E * w.h * w.f * (4 if w.dtype == "f32" else 2)
                          > 129e6 else "fit in")}
 
+    # ---- the same step captured once into a CUDA graph and replayed: the same
+    # kernels on the same buffers, without the launch gaps between them (the
+    # L2 flush stays outside the graph, between replays)
+    graph = None
+    if not args.no_graph:
+        step()
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            step()
+        torch.cuda.synchronize()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            gev[i][0].record(stream)
+            cg.replay()
+            gev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        moe.check(b.ws)
+        g_ms = max_over_ranks(sum(a.elapsed_time(c) for a, c in gev) / args.steps, world)
+        graph = {"value": world * w.T / (g_ms / 1e3), "unit": UNIT, "ms_per_step": g_ms,
+                 "api": "the timed step's C-ABI calls captured once into a CUDA graph, "
+                        "replayed per step (L2 flushed between replays)"}
+        del cg
+
     if rank != 0:
         return None
 
@@ -447,6 +478,7 @@ def run_native(args, rank, world, local):
         "rows": R, "tokens_per_expert_cv": float(np.std(tpe) / max(np.mean(tpe), 1e-9)),
         "roofline": roof,
         "e2e": e2e,
+        "graph": graph,
         "gpu_launches": kernels_per_forward(w, cfg, fp8) * args.steps,
         "clocks": clk,
         "wall_s_timed_region": t_wall,
