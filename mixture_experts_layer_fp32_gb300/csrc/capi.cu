@@ -199,13 +199,10 @@ moe_status do_route(const moe_config& c, const void* x, const float* Wg, const f
                               eb, topk_idx, topk_prob, keep, routing_map, assigned, err, s));
   // candidate lists: every routed pair, expert-major, ascending token order
   const int64_t np = static_cast<int64_t>(T) * k;
-  const int64_t nt = perm_tiles(np);
   int32_t* ctiles = at<int32_t>(ws, L.cand_tiles);
   int32_t* coff = at<int32_t>(ws, L.cand_off);
-  MOE_CUDA(launch_perm_hist(np, E, topk_idx, nullptr, ctiles, err, s));
-  MOE_CUDA(launch_perm_scan(nt, E, ctiles, coff, nullptr, s));
-  MOE_CUDA(launch_perm_rank(np, E, topk_idx, nullptr, ctiles, at<int32_t>(ws, L.cand_rowmap),
-                            at<int32_t>(ws, L.cand_src), s));
+  MOE_CUDA(launch_perm_index(np, E, topk_idx, nullptr, ctiles, at<int32_t>(ws, L.cand_rowmap),
+                             at<int32_t>(ws, L.cand_src), coff, nullptr, err, s));
   MOE_CUDA(launch_drop_select(T, E, k, cap, c.drop_policy, coff, at<int32_t>(ws, L.cand_src),
                               topk_prob, keep, routing_map, tpe, s));
   return MOE_OK;
@@ -223,9 +220,8 @@ moe_status do_permute(const moe_config& c, const void* x, const int32_t* topk_id
     return MOE_OK;
   }
   int32_t* tiles = at<int32_t>(ws, L.tiles);
-  MOE_CUDA(launch_perm_hist(np, E, topk_idx, keep, tiles, err, s));
-  MOE_CUDA(launch_perm_scan(perm_tiles(np), E, tiles, offsets, nullptr, s));
-  MOE_CUDA(launch_perm_rank(np, E, topk_idx, keep, tiles, row_map, nullptr, s));
+  MOE_CUDA(launch_perm_index(np, E, topk_idx, keep, tiles, row_map, nullptr, offsets, nullptr,
+                             err, s));
   MOE_CUDA(launch_perm_copy(T, c.hidden, k, c.dtype, x, row_map, x_perm, s));
   return MOE_OK;
 }
@@ -374,9 +370,8 @@ moe_status do_permute_e4m3(const moe_config& c, const void* x, const int32_t* to
     return MOE_OK;
   }
   int32_t* tiles = at<int32_t>(ws, L.tiles);
-  MOE_CUDA(launch_perm_hist(np, E, topk_idx, keep, tiles, err, s));
-  MOE_CUDA(launch_perm_scan(perm_tiles(np), E, tiles, offsets, nullptr, s));
-  MOE_CUDA(launch_perm_rank(np, E, topk_idx, keep, tiles, row_map, nullptr, s));
+  MOE_CUDA(launch_perm_index(np, E, topk_idx, keep, tiles, row_map, nullptr, offsets, nullptr,
+                             err, s));
   MOE_CUDA(launch_perm_copy_e4m3(T, c.hidden, k, x, row_map, xperm_q, xperm_s, s));
   return MOE_OK;
 }

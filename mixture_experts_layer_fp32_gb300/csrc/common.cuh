@@ -45,6 +45,15 @@ cudaError_t launch_drop_select(int T, int E, int k, int64_t capacity, int policy
                                int32_t* kept_per_expert, cudaStream_t s);
 
 // ---- permutation / combine ----
+// The stable expert-major order of the T*k (token, slot) pairs: expert
+// offsets [E+1], row_map [T*k] (-1 for dropped pairs), optionally row_src
+// (pair of each row) and tokens_per_expert.  hist, then scan + rank in one
+// launch (up to 128 tiles of 2048 pairs) or in two; tile_counts is
+// perm_tiles(npairs) * E ints of scratch.
+cudaError_t launch_perm_index(int64_t npairs, int E, const int32_t* topk_idx, const uint8_t* keep,
+                              int32_t* tile_counts, int32_t* row_map, int32_t* row_src,
+                              int32_t* offsets, int32_t* tokens_per_expert, int* err,
+                              cudaStream_t s);
 cudaError_t launch_perm_hist(int64_t npairs, int E, const int32_t* topk_idx, const uint8_t* keep,
                              int32_t* tile_counts, int* err, cudaStream_t s);
 cudaError_t launch_perm_scan(int64_t ntiles, int E, int32_t* tile_counts, int32_t* offsets,

@@ -91,11 +91,8 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
                ? MOE_OK
                : MOE_ERR_CUDA;
   }
-  if (launch_perm_hist(np, c.num_experts, topk_idx, keep, scratch, nullptr, stream) != cudaSuccess ||
-      launch_perm_scan(ntiles, c.num_experts, scratch, expert_offsets, nullptr, stream) !=
-          cudaSuccess ||
-      launch_perm_rank(np, c.num_experts, topk_idx, keep, scratch, row_map, nullptr, stream) !=
-          cudaSuccess ||
+  if (launch_perm_index(np, c.num_experts, topk_idx, keep, scratch, row_map, nullptr,
+                        expert_offsets, nullptr, nullptr, stream) != cudaSuccess ||
       launch_perm_copy(c.num_tokens, c.hidden, c.topk, c.dtype, x, row_map, x_perm, stream) !=
           cudaSuccess)
     return MOE_ERR_CUDA;

@@ -10,6 +10,10 @@
 //   perm_scan_kernel  one CTA: per-expert prefix over tiles, expert offsets
 //   perm_rank_kernel  per tile: stable rank of each pair inside its tile
 //                     (warp match_any + per-warp counts) -> row_map
+//   perm_scan_rank_kernel  scan and rank in one launch for up to 128 tiles:
+//                     each tile's CTA sums the per-tile counts itself (all
+//                     tiles, and those before it), scans the totals into the
+//                     expert offsets and ranks its tile
 //   perm_copy_kernel  per token: read the x row once (16-byte vectors),
 //                     write it to each of its kept rows
 //   perm_copy_e4m3_kernel  the same for E4M3 rows: the token's row is
@@ -30,19 +34,28 @@ __global__ void __launch_bounds__(kPermThreads)
     perm_hist_kernel(int64_t npairs, int E, const int32_t* __restrict__ topk_idx,
                      const uint8_t* __restrict__ keep, int32_t* __restrict__ tile_counts,
                      int* __restrict__ err) {
+  constexpr int kPer = kPermTile / kPermThreads;
   __shared__ int hist[MOE_MAX_EXPERTS];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  // every load of this thread's pairs issued before the first atomic (one
+  // round trip to memory, not one per pair)
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kPermTile + threadIdx.x;
+  int ev[kPer];
+  uint8_t kv[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int64_t p = base + u * kPermThreads;
+    ev[u] = p < npairs ? topk_idx[p] : 0;
+    kv[u] = p < npairs ? (keep ? keep[p] : 1) : 0;
+  }
   __syncthreads();
-  const int64_t base = static_cast<int64_t>(blockIdx.x) * kPermTile;
-  for (int i = threadIdx.x; i < kPermTile; i += blockDim.x) {
-    const int64_t p = base + i;
-    if (p < npairs && (keep == nullptr || keep[p])) {
-      const int e = topk_idx[p];
-      if (e >= 0 && e < E)
-        atomicAdd(&hist[e], 1);
-      else
-        report_error(err, DEV_ERR_INDEX, static_cast<int>(p));
-    }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    if (!kv[u]) continue;
+    if (ev[u] >= 0 && ev[u] < E)
+      atomicAdd(&hist[ev[u]], 1);
+    else
+      report_error(err, DEV_ERR_INDEX, static_cast<int>(base + u * kPermThreads));
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -117,21 +130,27 @@ __global__ void __launch_bounds__(kPermThreads)
   const int64_t base = static_cast<int64_t>(blockIdx.x) * kPermTile + warp * (kChunks * 32);
   const uint32_t lt_mask = (1u << lane) - 1u;
   int key[kChunks], rank[kChunks];
+  // all of this lane's loads first (one round trip), then the ranking
 #pragma unroll
   for (int c = 0; c < kChunks; ++c) {
     const int64_t p = base + c * 32 + lane;
     int e = -1;
-    if (p < npairs && (keep == nullptr || keep[p])) {
+    if (p < npairs) {
       e = topk_idx[p];
+      if (keep && !keep[p]) e = -1;
       if (e < 0 || e >= E) e = -1;  // flagged by perm_hist_kernel
     }
+    key[c] = e;
+  }
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int e = key[c];
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     int before = 0;
     if (e >= 0) before = cnt[warp][e];
     __syncwarp();
     if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp][e] = before + __popc(peers);
     __syncwarp();
-    key[c] = e;
     rank[c] = before + __popc(peers & lt_mask);
   }
   __syncthreads();
@@ -161,23 +180,147 @@ __global__ void __launch_bounds__(kPermThreads)
   }
 }
 
+// Scan and rank in one launch (after perm_hist_kernel) when there are at
+// most kFusedMaxTiles tiles: each tile's CTA sums the per-tile counts itself
+// (all tiles for the totals, the earlier ones for its base), scans the
+// totals into the expert offsets and ranks its tile; CTA 0 writes the
+// offsets and tokens_per_expert.  The same order as perm_scan + perm_rank.
+constexpr int64_t kFusedMaxTiles = 128;
+
+__global__ void __launch_bounds__(kPermThreads)
+    perm_scan_rank_kernel(int64_t npairs, int E, const int32_t* __restrict__ topk_idx,
+                          const uint8_t* __restrict__ keep, const int32_t* __restrict__ tile_counts,
+                          int32_t* __restrict__ row_map, int32_t* __restrict__ row_src,
+                          int32_t* __restrict__ offsets, int32_t* __restrict__ tokens_per_expert) {
+  __shared__ int before[MOE_MAX_EXPERTS], total[MOE_MAX_EXPERTS], start[MOE_MAX_EXPERTS + 1];
+  __shared__ int cnt[kWarps][MOE_MAX_EXPERTS];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t ntiles = gridDim.x;  // one CTA per tile
+  const int64_t tile = blockIdx.x;
+  for (int i = threadIdx.x; i < kWarps * MOE_MAX_EXPERTS; i += blockDim.x) (&cnt[0][0])[i] = 0;
+  // this tile's pairs: every load issued before the ranking
+  const int64_t base = tile * kPermTile + warp * (kChunks * 32);
+  int key[kChunks], rank[kChunks];
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int64_t p = base + c * 32 + lane;
+    int e = -1;
+    if (p < npairs) {
+      e = topk_idx[p];
+      if (keep && !keep[p]) e = -1;
+      if (e < 0 || e >= E) e = -1;  // flagged by perm_hist_kernel
+    }
+    key[c] = e;
+  }
+  // the totals and this tile's base, one expert per thread
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int all = 0, bef = 0;
+#pragma unroll 8
+    for (int64_t t = 0; t < ntiles; ++t) {
+      const int c = tile_counts[t * E + e];
+      all += c;
+      bef += t < tile ? c : 0;
+    }
+    total[e] = all;
+    before[e] = bef;
+  }
+  __syncthreads();
+  if (warp == 0) {  // expert offsets: exclusive scan of the totals (E <= 256)
+    int v[MOE_MAX_EXPERTS / 32];
+    int run = 0;
+#pragma unroll
+    for (int i = 0; i < MOE_MAX_EXPERTS / 32; ++i) {
+      const int e = lane * (MOE_MAX_EXPERTS / 32) + i;
+      v[i] = (e < E) ? total[e] : 0;
+      run += v[i];
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int excl = incl - run;
+#pragma unroll
+    for (int i = 0; i < MOE_MAX_EXPERTS / 32; ++i) {
+      const int e = lane * (MOE_MAX_EXPERTS / 32) + i;
+      if (e <= E) start[e] = excl;
+      excl += v[i];
+    }
+    if (lane == 31 && E == MOE_MAX_EXPERTS) start[E] = excl;
+  }
+  // stable rank inside the tile, as perm_rank_kernel
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int e = key[c];
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int bef = 0;
+    if (e >= 0) bef = cnt[warp][e];
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) cnt[warp][e] = bef + __popc(peers);
+    __syncwarp();
+    rank[c] = bef + __popc(peers & lt_mask);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = start[e];
+    if (tokens_per_expert)
+      for (int e = threadIdx.x; e < E; e += blockDim.x) tokens_per_expert[e] = total[e];
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int sum = start[e] + before[e];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int v = cnt[w][e];
+      cnt[w][e] = sum;
+      sum += v;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int64_t p = base + c * 32 + lane;
+    if (p >= npairs) continue;
+    const int e = key[c];
+    if (e >= 0) {
+      const int row = cnt[warp][e] + rank[c];
+      row_map[p] = row;
+      if (row_src) row_src[row] = static_cast<int32_t>(p);
+    } else {
+      row_map[p] = -1;
+    }
+  }
+}
+
 constexpr int kCopyThreads = 128;
 constexpr int kCopyUnroll = 4;
 
-// x_perm[row_map[t, j]] = x[t] for every kept slot j; 16-byte vectors.
+// x_perm[row_map[t, j]] = x[t] for every kept slot j; 16-byte vectors.  A
+// CTA moves 2^tpi_log2 tokens per round with kCopyThreads >> tpi_log2
+// threads each, chosen so that short rows still give every thread
+// kCopyUnroll loads in flight (one token per round for rows of >= 512
+// vectors).
+template <int TPI_LOG2>
 __global__ void __launch_bounds__(kCopyThreads)
     perm_copy_kernel(int T, int row_vecs, int k, const uint4* __restrict__ x,
                      const int32_t* __restrict__ row_map, uint4* __restrict__ x_perm) {
-  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+  constexpr int tpt = kCopyThreads >> TPI_LOG2;  // threads per token
+  const int sub = threadIdx.x / tpt, lt = threadIdx.x % tpt;
+  constexpr int64_t tpi = int64_t{1} << TPI_LOG2;
+  for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * tpi; t0 < T; t0 += gridDim.x * tpi) {
+    const int64_t t = t0 + sub;
+    if (t >= T) continue;  // no barriers in this kernel
     int rows[MOE_MAX_TOPK];
 #pragma unroll
-    for (int j = 0; j < MOE_MAX_TOPK; ++j) rows[j] = (j < k) ? row_map[(int64_t)t * k + j] : -1;
-    const uint4* src = x + (int64_t)t * row_vecs;
-    for (int v0 = threadIdx.x; v0 < row_vecs; v0 += kCopyThreads * kCopyUnroll) {
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) rows[j] = (j < k) ? row_map[t * k + j] : -1;
+    const uint4* src = x + t * row_vecs;
+    for (int v0 = lt; v0 < row_vecs; v0 += tpt * kCopyUnroll) {
       uint4 buf[kCopyUnroll];
 #pragma unroll
       for (int u = 0; u < kCopyUnroll; ++u) {
-        const int v = v0 + u * kCopyThreads;
+        const int v = v0 + u * tpt;
         if (v < row_vecs) buf[u] = __ldcs(src + v);
       }
 #pragma unroll
@@ -186,12 +329,20 @@ __global__ void __launch_bounds__(kCopyThreads)
         uint4* dst = x_perm + (int64_t)rows[j] * row_vecs;
 #pragma unroll
         for (int u = 0; u < kCopyUnroll; ++u) {
-          const int v = v0 + u * kCopyThreads;
+          const int v = v0 + u * tpt;
           if (v < row_vecs) dst[v] = buf[u];
         }
       }
     }
   }
+}
+
+// log2 of the tokens a CTA handles per round: the largest power of two
+// (<= 2^max_log2) that does not exceed threads * per_thread / vecs_per_row.
+int tokens_per_round_log2(int vecs_per_row, int threads, int per_thread, int max_log2) {
+  int l = 0;
+  while (l < max_log2 && (int64_t{2} << l) * vecs_per_row <= int64_t{threads} * per_thread) ++l;
+  return l;
 }
 
 // E4M3 rows (FP8 experts): the token's bf16 row is reduced to its largest
@@ -253,14 +404,21 @@ struct Out4<__nv_bfloat16> {
 
 constexpr int kCombineThreads = 256;
 
-template <typename OT>
+// A CTA combines 2^TPI_LOG2 tokens per round, kCombineThreads >> TPI_LOG2
+// threads each (several tokens per round when rows are short).
+template <typename OT, int TPI_LOG2>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(int T, int h, int k, const float* __restrict__ y_perm,
                    const int32_t* __restrict__ row_map, const float* __restrict__ topk_prob,
                    const float* __restrict__ y_shared, OT* __restrict__ y) {
   const int h4 = h >> 2;
   const int64_t max_rows = static_cast<int64_t>(T) * k;
-  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+  constexpr int tpt = kCombineThreads >> TPI_LOG2;  // threads per token
+  const int sub = threadIdx.x / tpt, lt = threadIdx.x % tpt;
+  constexpr int tpi = 1 << TPI_LOG2;
+  for (int t0 = blockIdx.x * tpi; t0 < T; t0 += gridDim.x * tpi) {
+    const int t = t0 + sub;
+    if (t >= T) continue;  // no barriers in this kernel
     int rows[MOE_MAX_TOPK];
     float p[MOE_MAX_TOPK];
 #pragma unroll
@@ -270,7 +428,7 @@ __global__ void __launch_bounds__(kCombineThreads)
       // no weights (the backward's unpermute-sum of dx rows): weight 1
       p[j] = (rows[j] >= 0) ? (topk_prob ? topk_prob[(int64_t)t * k + j] : 1.f) : 0.f;
     }
-    for (int v = threadIdx.x; v < h4; v += kCombineThreads) {
+    for (int v = lt; v < h4; v += tpt) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < MOE_MAX_TOPK; ++j) {
@@ -290,6 +448,18 @@ __global__ void __launch_bounds__(kCombineThreads)
       }
       Out4<OT>::store(y + (int64_t)t * h + 4 * v, acc);
     }
+  }
+}
+
+template <typename OT>
+void launch_combine_t(int l, int grid, cudaStream_t s, int T, int h, int k, const float* y_perm,
+                      const int32_t* row_map, const float* topk_prob, const float* y_shared,
+                      OT* y) {
+  switch (l) {
+    case 0: combine_kernel<OT, 0><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
+    case 1: combine_kernel<OT, 1><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
+    case 2: combine_kernel<OT, 2><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
+    default: combine_kernel<OT, 3><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
   }
 }
 
@@ -325,12 +495,40 @@ cudaError_t launch_perm_rank(int64_t npairs, int E, const int32_t* topk_idx, con
   return cudaGetLastError();
 }
 
+cudaError_t launch_perm_index(int64_t npairs, int E, const int32_t* topk_idx, const uint8_t* keep,
+                              int32_t* tile_counts, int32_t* row_map, int32_t* row_src,
+                              int32_t* offsets, int32_t* tokens_per_expert, int* err,
+                              cudaStream_t s) {
+  const int64_t nt = perm_tiles(npairs);
+  cudaError_t st = launch_perm_hist(npairs, E, topk_idx, keep, tile_counts, err, s);
+  if (st != cudaSuccess) return st;
+  if (nt == 0 || nt > kFusedMaxTiles) {
+    st = launch_perm_scan(nt, E, tile_counts, offsets, tokens_per_expert, s);
+    if (st == cudaSuccess)
+      st = launch_perm_rank(npairs, E, topk_idx, keep, tile_counts, row_map, row_src, s);
+    return st;
+  }
+  perm_scan_rank_kernel<<<static_cast<unsigned>(nt), kPermThreads, 0, s>>>(
+      npairs, E, topk_idx, keep, tile_counts, row_map, row_src, offsets, tokens_per_expert);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, const int32_t* row_map,
                              void* x_perm, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int row_vecs = h * (dtype == MOE_F32 ? 4 : 2) / 16;
-  perm_copy_kernel<<<grid_for_tokens(T, 16), kCopyThreads, 0, s>>>(
-      T, row_vecs, k, static_cast<const uint4*>(x), row_map, static_cast<uint4*>(x_perm));
+  const int l = tokens_per_round_log2(row_vecs, kCopyThreads, kCopyUnroll, 5);
+  const int grid = grid_for_tokens((T + (1 << l) - 1) >> l, 16);
+  const uint4* src = static_cast<const uint4*>(x);
+  uint4* dst = static_cast<uint4*>(x_perm);
+  switch (l) {
+    case 0: perm_copy_kernel<0><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
+    case 1: perm_copy_kernel<1><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
+    case 2: perm_copy_kernel<2><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
+    case 3: perm_copy_kernel<3><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
+    case 4: perm_copy_kernel<4><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
+    default: perm_copy_kernel<5><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
+  }
   return cudaGetLastError();
 }
 
@@ -346,13 +544,14 @@ cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
                            const int32_t* row_map, const float* topk_prob, const float* y_shared,
                            void* y, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int grid = grid_for_tokens(T, 8);
+  const int l = tokens_per_round_log2(h / 4, kCombineThreads, 4, 3);
+  const int grid = grid_for_tokens((T + (1 << l) - 1) >> l, 8);
   if (dtype == MOE_F32)
-    combine_kernel<float><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob,
-                                                           y_shared, static_cast<float*>(y));
+    launch_combine_t<float>(l, grid, s, T, h, k, y_perm, row_map, topk_prob, y_shared,
+                            static_cast<float*>(y));
   else
-    combine_kernel<__nv_bfloat16><<<grid, kCombineThreads, 0, s>>>(
-        T, h, k, y_perm, row_map, topk_prob, y_shared, static_cast<__nv_bfloat16*>(y));
+    launch_combine_t<__nv_bfloat16>(l, grid, s, T, h, k, y_perm, row_map, topk_prob, y_shared,
+                                    static_cast<__nv_bfloat16*>(y));
   return cudaGetLastError();
 }
 
