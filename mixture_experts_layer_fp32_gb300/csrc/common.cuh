@@ -15,6 +15,33 @@ namespace moe {
 enum : int { DEV_ERR_NONE = 0, DEV_ERR_INDEX = 1, DEV_ERR_TIMEOUT = 2 };
 constexpr size_t kErrBytes = 256;
 
+// Programmatic dependent launch: a kernel launched with launch_dependent may
+// start while the kernel before it on the stream is still running; it calls
+// pdl_wait() before its first read of that kernel's output (the wait returns
+// once that kernel has completed and its writes are visible; it returns at
+// once when the kernel was launched normally).  pdl_trigger() lets the next
+// dependent kernel launch before this one finishes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 __device__ __forceinline__ void report_error(int* err, int code, int info) {
   if (err == nullptr) return;
   if (atomicCAS(err, 0, code) == 0) atomicExch(err + 1, info);

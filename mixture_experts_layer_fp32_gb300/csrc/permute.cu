@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kPermThreads)
                      const uint8_t* __restrict__ keep, int32_t* __restrict__ tile_counts,
                      int* __restrict__ err) {
   constexpr int kPer = kPermTile / kPermThreads;
+  pdl_trigger();  // the scan+rank kernel may launch (it waits for these counts)
   __shared__ int hist[MOE_MAX_EXPERTS];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   // every load of this thread's pairs issued before the first atomic (one
@@ -189,7 +190,7 @@ constexpr int64_t kFusedMaxTiles = 128;
 
 __global__ void __launch_bounds__(kPermThreads)
     perm_scan_rank_kernel(int64_t npairs, int E, const int32_t* __restrict__ topk_idx,
-                          const uint8_t* __restrict__ keep, const int32_t* __restrict__ tile_counts,
+                          const uint8_t* __restrict__ keep, const int32_t* tile_counts,
                           int32_t* __restrict__ row_map, int32_t* __restrict__ row_src,
                           int32_t* __restrict__ offsets, int32_t* __restrict__ tokens_per_expert) {
   __shared__ int before[MOE_MAX_EXPERTS], total[MOE_MAX_EXPERTS], start[MOE_MAX_EXPERTS + 1];
@@ -213,12 +214,14 @@ __global__ void __launch_bounds__(kPermThreads)
     }
     key[c] = e;
   }
+  pdl_trigger();  // the copy may launch (it waits for row_map)
+  pdl_wait();     // the per-tile counts of perm_hist_kernel
   // the totals and this tile's base, one expert per thread
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int all = 0, bef = 0;
 #pragma unroll 8
     for (int64_t t = 0; t < ntiles; ++t) {
-      const int c = tile_counts[t * E + e];
+      const int c = __ldcg(tile_counts + t * E + e);  // written by perm_hist_kernel
       all += c;
       bef += t < tile ? c : 0;
     }
@@ -305,23 +308,33 @@ constexpr int kCopyUnroll = 4;
 template <int TPI_LOG2>
 __global__ void __launch_bounds__(kCopyThreads)
     perm_copy_kernel(int T, int row_vecs, int k, const uint4* __restrict__ x,
-                     const int32_t* __restrict__ row_map, uint4* __restrict__ x_perm) {
+                     const int32_t* row_map, uint4* __restrict__ x_perm) {
+  // row_map comes from the kernel before this one, which may still be running
+  // until pdl_wait: it is read after the wait with coherent loads (no
+  // read-only assumption a restrict qualifier would allow)
   constexpr int tpt = kCopyThreads >> TPI_LOG2;  // threads per token
   const int sub = threadIdx.x / tpt, lt = threadIdx.x % tpt;
   constexpr int64_t tpi = int64_t{1} << TPI_LOG2;
+  bool waited = false;
   for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * tpi; t0 < T; t0 += gridDim.x * tpi) {
     const int64_t t = t0 + sub;
     if (t >= T) continue;  // no barriers in this kernel
-    int rows[MOE_MAX_TOPK];
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_TOPK; ++j) rows[j] = (j < k) ? row_map[t * k + j] : -1;
     const uint4* src = x + t * row_vecs;
+    int rows[MOE_MAX_TOPK];
     for (int v0 = lt; v0 < row_vecs; v0 += tpt * kCopyUnroll) {
       uint4 buf[kCopyUnroll];
 #pragma unroll
       for (int u = 0; u < kCopyUnroll; ++u) {
         const int v = v0 + u * tpt;
         if (v < row_vecs) buf[u] = __ldcs(src + v);
+      }
+      if (v0 == lt) {  // the token's first vectors are in flight: now its rows
+        if (!waited) {
+          pdl_wait();  // row_map from the rank kernel
+          waited = true;
+        }
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_TOPK; ++j) rows[j] = (j < k) ? __ldcg(row_map + t * k + j) : -1;
       }
 #pragma unroll
       for (int j = 0; j < MOE_MAX_TOPK; ++j) {
@@ -405,8 +418,9 @@ struct Out4<__nv_bfloat16> {
 constexpr int kCombineThreads = 256;
 
 // A CTA combines 2^TPI_LOG2 tokens per round, kCombineThreads >> TPI_LOG2
-// threads each (several tokens per round when rows are short).
-template <typename OT, int TPI_LOG2>
+// threads each (several tokens per round when rows are short).  K1: top-1
+// (one row per token), four vectors per thread in flight.
+template <typename OT, int TPI_LOG2, bool K1>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(int T, int h, int k, const float* __restrict__ y_perm,
                    const int32_t* __restrict__ row_map, const float* __restrict__ topk_prob,
@@ -428,38 +442,73 @@ __global__ void __launch_bounds__(kCombineThreads)
       // no weights (the backward's unpermute-sum of dx rows): weight 1
       p[j] = (rows[j] >= 0) ? (topk_prob ? topk_prob[(int64_t)t * k + j] : 1.f) : 0.f;
     }
-    for (int v = lt; v < h4; v += tpt) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (K1) {
+      const int64_t r = rows[0];
+      for (int v0 = lt; v0 < h4; v0 += 4 * tpt) {
+        float4 a[4], b[4];
 #pragma unroll
-      for (int j = 0; j < MOE_MAX_TOPK; ++j) {
-        if (rows[j] < 0) continue;
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(y_perm + (int64_t)rows[j] * h) + v);
-        acc.x = fmaf(p[j], a.x, acc.x);
-        acc.y = fmaf(p[j], a.y, acc.y);
-        acc.z = fmaf(p[j], a.z, acc.z);
-        acc.w = fmaf(p[j], a.w, acc.w);
+        for (int u = 0; u < 4; ++u) {
+          const int v = v0 + u * tpt;
+          a[u] = b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (v < h4 && r >= 0) a[u] = __ldcs(reinterpret_cast<const float4*>(y_perm + r * h) + v);
+          if (v < h4 && y_shared)
+            b[u] = __ldcs(reinterpret_cast<const float4*>(y_shared + (int64_t)t * h) + v);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int v = v0 + u * tpt;
+          if (v >= h4) continue;
+          // the same operations as below: fma with the weight, then the shared row
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (r >= 0) {
+            acc.x = fmaf(p[0], a[u].x, acc.x);
+            acc.y = fmaf(p[0], a[u].y, acc.y);
+            acc.z = fmaf(p[0], a[u].z, acc.z);
+            acc.w = fmaf(p[0], a[u].w, acc.w);
+          }
+          if (y_shared) {
+            acc.x += b[u].x;
+            acc.y += b[u].y;
+            acc.z += b[u].z;
+            acc.w += b[u].w;
+          }
+          Out4<OT>::store(y + (int64_t)t * h + 4 * v, acc);
+        }
       }
-      if (y_shared) {  // the shared expert's output, added after the routed sum
-        const float4 b = __ldcs(reinterpret_cast<const float4*>(y_shared + (int64_t)t * h) + v);
-        acc.x += b.x;
-        acc.y += b.y;
-        acc.z += b.z;
-        acc.w += b.w;
+    } else {
+      for (int v = lt; v < h4; v += tpt) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+          if (rows[j] < 0) continue;
+          const float4 a = __ldcs(reinterpret_cast<const float4*>(y_perm + (int64_t)rows[j] * h) + v);
+          acc.x = fmaf(p[j], a.x, acc.x);
+          acc.y = fmaf(p[j], a.y, acc.y);
+          acc.z = fmaf(p[j], a.z, acc.z);
+          acc.w = fmaf(p[j], a.w, acc.w);
+        }
+        if (y_shared) {  // the shared expert's output, added after the routed sum
+          const float4 b = __ldcs(reinterpret_cast<const float4*>(y_shared + (int64_t)t * h) + v);
+          acc.x += b.x;
+          acc.y += b.y;
+          acc.z += b.z;
+          acc.w += b.w;
+        }
+        Out4<OT>::store(y + (int64_t)t * h + 4 * v, acc);
       }
-      Out4<OT>::store(y + (int64_t)t * h + 4 * v, acc);
     }
   }
 }
 
-template <typename OT>
+template <typename OT, bool K1>
 void launch_combine_t(int l, int grid, cudaStream_t s, int T, int h, int k, const float* y_perm,
                       const int32_t* row_map, const float* topk_prob, const float* y_shared,
                       OT* y) {
   switch (l) {
-    case 0: combine_kernel<OT, 0><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
-    case 1: combine_kernel<OT, 1><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
-    case 2: combine_kernel<OT, 2><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
-    default: combine_kernel<OT, 3><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
+    case 0: combine_kernel<OT, 0, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
+    case 1: combine_kernel<OT, 1, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
+    case 2: combine_kernel<OT, 2, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
+    default: combine_kernel<OT, 3, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
   }
 }
 
@@ -508,9 +557,10 @@ cudaError_t launch_perm_index(int64_t npairs, int E, const int32_t* topk_idx, co
       st = launch_perm_rank(npairs, E, topk_idx, keep, tile_counts, row_map, row_src, s);
     return st;
   }
-  perm_scan_rank_kernel<<<static_cast<unsigned>(nt), kPermThreads, 0, s>>>(
-      npairs, E, topk_idx, keep, tile_counts, row_map, row_src, offsets, tokens_per_expert);
-  return cudaGetLastError();
+  return launch_dependent(perm_scan_rank_kernel, dim3(static_cast<unsigned>(nt)),
+                          dim3(kPermThreads), 0, s, npairs, E, topk_idx, keep,
+                          static_cast<const int32_t*>(tile_counts), row_map, row_src, offsets,
+                          tokens_per_expert);
 }
 
 cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, const int32_t* row_map,
@@ -521,15 +571,12 @@ cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, cons
   const int grid = grid_for_tokens((T + (1 << l) - 1) >> l, 16);
   const uint4* src = static_cast<const uint4*>(x);
   uint4* dst = static_cast<uint4*>(x_perm);
-  switch (l) {
-    case 0: perm_copy_kernel<0><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
-    case 1: perm_copy_kernel<1><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
-    case 2: perm_copy_kernel<2><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
-    case 3: perm_copy_kernel<3><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
-    case 4: perm_copy_kernel<4><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
-    default: perm_copy_kernel<5><<<grid, kCopyThreads, 0, s>>>(T, row_vecs, k, src, row_map, dst); break;
-  }
-  return cudaGetLastError();
+  // launched as a dependent of the rank kernel: the x loads start early
+  void (*kern)(int, int, int, const uint4*, const int32_t*, uint4*) =
+      l == 0 ? perm_copy_kernel<0> : l == 1 ? perm_copy_kernel<1> : l == 2 ? perm_copy_kernel<2>
+      : l == 3 ? perm_copy_kernel<3> : l == 4 ? perm_copy_kernel<4> : perm_copy_kernel<5>;
+  return launch_dependent(kern, dim3(grid), dim3(kCopyThreads), 0, s, T, row_vecs, k, src,
+                          row_map, dst);
 }
 
 cudaError_t launch_perm_copy_e4m3(int T, int h, int k, const void* x, const int32_t* row_map,
@@ -546,12 +593,20 @@ cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
   if (T == 0) return cudaSuccess;
   const int l = tokens_per_round_log2(h / 4, kCombineThreads, 4, 3);
   const int grid = grid_for_tokens((T + (1 << l) - 1) >> l, 8);
-  if (dtype == MOE_F32)
-    launch_combine_t<float>(l, grid, s, T, h, k, y_perm, row_map, topk_prob, y_shared,
-                            static_cast<float*>(y));
-  else
-    launch_combine_t<__nv_bfloat16>(l, grid, s, T, h, k, y_perm, row_map, topk_prob, y_shared,
-                                    static_cast<__nv_bfloat16*>(y));
+  if (dtype == MOE_F32) {
+    if (k == 1)
+      launch_combine_t<float, true>(l, grid, s, T, h, k, y_perm, row_map, topk_prob, y_shared,
+                                    static_cast<float*>(y));
+    else
+      launch_combine_t<float, false>(l, grid, s, T, h, k, y_perm, row_map, topk_prob, y_shared,
+                                     static_cast<float*>(y));
+  } else if (k == 1) {
+    launch_combine_t<__nv_bfloat16, true>(l, grid, s, T, h, k, y_perm, row_map, topk_prob,
+                                          y_shared, static_cast<__nv_bfloat16*>(y));
+  } else {
+    launch_combine_t<__nv_bfloat16, false>(l, grid, s, T, h, k, y_perm, row_map, topk_prob,
+                                           y_shared, static_cast<__nv_bfloat16*>(y));
+  }
   return cudaGetLastError();
 }
 
