@@ -337,14 +337,21 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// dWg = the S partial sums of dwg_kernel, added in split order
+// dWg = the S partial sums of dwg_kernel: 8 threads per output (lanes 8j..
+// 8j+7 of a warp hold output j of 4), thread q summing splits q, q+8, ...
+// in order, then the 8 sums added in a fixed tree: a deterministic order
+// with S/8 loads per thread in flight instead of S in a row.
 __global__ void __launch_bounds__(256)
     dwg_reduce_kernel(int64_t n, int S, const float* __restrict__ part, float* __restrict__ dWg) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * 256) {
-    float v = part[i];
-    for (int z = 1; z < S; ++z) v += part[z * n + i];
-    dWg[i] = v;
+  const int q = threadIdx.x & 7;
+  const unsigned group = 0xffu << (threadIdx.x & 24);  // the 8 lanes sharing an output
+  for (int64_t i = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) >> 3; i < n;
+       i += static_cast<int64_t>(gridDim.x) * 32) {
+    float v = 0.f;
+    for (int z = q; z < S; z += 8) v += part[z * n + i];
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) v += __shfl_xor_sync(group, v, o);
+    if (q == 0) dWg[i] = v;
   }
 }
 
@@ -422,11 +429,26 @@ __global__ void __launch_bounds__(256)
     ls[tt][e] = (t0 + tt < T && e < E) ? dl[static_cast<int64_t>(t0 + tt) * E + e] : 0.f;
   }
   float w[4][EC];
+  if (E == EC && (reinterpret_cast<uintptr_t>(Wg) & 15) == 0) {  // whole, aligned rows: 16-byte loads
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 4; ++c)
 #pragma unroll
-    for (int e = 0; e < EC; ++e)
-      w[c][e] = (i + c < h && e < E) ? Wg[static_cast<int64_t>(i + c) * E + e] : 0.f;
+      for (int e4 = 0; e4 < EC / 4; ++e4) {
+        const float4 v = i + c < h ? *reinterpret_cast<const float4*>(
+                                         Wg + static_cast<int64_t>(i + c) * E + 4 * e4)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[c][4 * e4] = v.x;
+        w[c][4 * e4 + 1] = v.y;
+        w[c][4 * e4 + 2] = v.z;
+        w[c][4 * e4 + 3] = v.w;
+      }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int e = 0; e < EC; ++e)
+        w[c][e] = (i + c < h && e < E) ? Wg[static_cast<int64_t>(i + c) * E + e] : 0.f;
+  }
   __syncthreads();
   if (i >= h) return;
 #pragma unroll 4
@@ -541,8 +563,8 @@ cudaError_t launch_router_param_grads(int T, int h, int E, const void* x, const 
   if (st != cudaSuccess) return st;
   if (S > 1) {
     const int64_t n = static_cast<int64_t>(h) * E;
-    int64_t grid = (n + 255) / 256;
-    if (grid > 4LL * device_sm_count()) grid = 4LL * device_sm_count();
+    int64_t grid = (n + 31) / 32;  // 32 outputs per CTA
+    if (grid > 8LL * device_sm_count()) grid = 8LL * device_sm_count();
     dwg_reduce_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(n, S, part, dWg);
     st = cudaGetLastError();
   }
