@@ -331,33 +331,25 @@ def run_native(args, rank, world, local):
         x_host = inp["x"].cpu().pin_memory()
         y_host = torch.empty(b.y.shape, dtype=b.y.dtype).pin_memory()
         if fp8:
-            x_dev = torch.empty_like(inp["x"])
-            y_dev = torch.empty_like(b.y)
-            ws2 = moe.alloc_workspace_e4m3(cfg, dev)
+            ws2 = moe.alloc_workspace_host_e4m3(cfg, dev)
 
             def run(n):
-                for _ in range(n):
-                    x_dev.copy_(x_host, non_blocking=True)
-                    moe.forward_e4m3(cfg, x_dev, inp["Wg"], inp["gate_bias"], inp["expert_bias"],
-                                     q, y_dev, ws2)
-                    y_host.copy_(y_dev, non_blocking=True)
-            api = ("moe_forward_e4m3 (C ABI) with pinned host x/y copied by torch on the same "
-                   "stream inside the timed region, one step at a time")
+                moe.forward_host_e4m3(cfg, x_host, y_host, inp["Wg"], inp["gate_bias"],
+                                      inp["expert_bias"], q, ws2, num_batches=n)
+            api = ("moe_forward_host_e4m3 (C ABI): %d batches from a pinned host buffer, each "
+                   "batch's H2D input and D2H output copy inside the timed region, pipelined on "
+                   "the library's copy streams" % args.steps)
         elif w.shared_f > 0:
-            # moe_forward_shared on device buffers, torch copies around it
-            x_dev = torch.empty_like(inp["x"])
-            y_dev = torch.empty_like(b.y)
-            ws2 = moe.alloc_workspace_shared(cfg, w.shared_f, dev)
+            ws2 = moe.alloc_workspace_host_shared(cfg, w.shared_f, dev)
 
             def run(n):
-                for _ in range(n):
-                    x_dev.copy_(x_host, non_blocking=True)
-                    moe.forward_shared(cfg, w.shared_f, x_dev, inp["Wg"], inp["gate_bias"],
-                                       inp["expert_bias"], inp["W1"], inp["W3"], inp["W2"],
-                                       inp["W1s"], inp["W3s"], inp["W2s"], y_dev, ws2)
-                    y_host.copy_(y_dev, non_blocking=True)
-            api = ("moe_forward_shared (C ABI) with pinned host x/y copied by torch on the same "
-                   "stream inside the timed region, one step at a time")
+                moe.forward_host_shared(cfg, w.shared_f, x_host, y_host, inp["Wg"],
+                                        inp["gate_bias"], inp["expert_bias"], inp["W1"],
+                                        inp["W3"], inp["W2"], inp["W1s"], inp["W3s"], inp["W2s"],
+                                        ws2, num_batches=n)
+            api = ("moe_forward_host_shared (C ABI): %d batches from a pinned host buffer, each "
+                   "batch's H2D input and D2H output copy inside the timed region, pipelined on "
+                   "the library's copy streams" % args.steps)
         else:
             # moe_forward_host: every step's input copied from the pinned host buffer and its
             # output copied back (stride 0: one buffer reused), the copies of neighbouring

@@ -425,6 +425,28 @@ moe_status moe_permute_noalloc(const moe_config* cfg, const void* x, const int32
                                const uint8_t* keep, void* x_perm, int32_t* row_map,
                                int32_t* expert_offsets, moe_stream_t stream);
 
+/*
+ * moe_forward_host for the layer with a shared expert (the forward of
+ * moe_forward_shared per batch) and for E4M3 experts (moe_forward_e4m3 per
+ * batch): the same host-buffer contract, staging and copy pipelining.
+ *   ws: moe_workspace_size_host_shared / moe_workspace_size_host_e4m3 bytes.
+ */
+moe_status moe_workspace_size_host_shared(const moe_config* cfg, int32_t fs, size_t* bytes);
+moe_status moe_forward_host_shared(const moe_config* cfg, int32_t fs, int32_t num_batches,
+                                   const void* x_host, size_t x_batch_stride, void* y_host,
+                                   size_t y_batch_stride, const float* Wg, const float* gate_bias,
+                                   const float* expert_bias, const void* W1, const void* W3,
+                                   const void* W2, const void* W1s, const void* W3s,
+                                   const void* W2s, void* ws, size_t ws_bytes,
+                                   moe_stream_t stream);
+moe_status moe_workspace_size_host_e4m3(const moe_config* cfg, size_t* bytes);
+moe_status moe_forward_host_e4m3(const moe_config* cfg, int32_t num_batches, const void* x_host,
+                                 size_t x_batch_stride, void* y_host, size_t y_batch_stride,
+                                 const float* Wg, const float* gate_bias,
+                                 const float* expert_bias, const uint8_t* W1q, const float* s1,
+                                 const uint8_t* W3q, const float* s3, const uint8_t* W2q,
+                                 const float* s2, void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Reads and clears the device error word in `ws` (synchronises `stream`):
  * MOE_OK, MOE_ERR_DEVICE_CHECK or MOE_ERR_TIMEOUT.  *info (nullable) gets
  * the first failing index or wait site. */

@@ -31,7 +31,8 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_c
            "moe_permute_e4m3", "moe_grouped_mlp_e4m3", "moe_forward_e4m3",
            "moe_grouped_fc1_e4m3", "moe_grouped_fc2_e4m3", "moe_workspace_size_backward",
            "moe_backward", "moe_workspace_size_backward_shared", "moe_backward_shared",
-           "moe_shared_expert_backward"]
+           "moe_shared_expert_backward", "moe_workspace_size_host_shared",
+           "moe_forward_host_shared", "moe_workspace_size_host_e4m3", "moe_forward_host_e4m3"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -103,6 +104,11 @@ def lib():
             "moe_workspace_size_backward_shared": ([cfgp, i32, ctypes.POINTER(sz)], i32),
             "moe_backward_shared": ([cfgp, i32] + [vp] * 27 + [vp, sz, vp], i32),
             "moe_shared_expert_backward": ([cfgp, i32] + [vp] * 10 + [vp, sz, vp], i32),
+            "moe_workspace_size_host_shared": ([cfgp, i32, ctypes.POINTER(sz)], i32),
+            "moe_forward_host_shared": ([cfgp, i32, i32, vp, sz, vp, sz] + [vp] * 9 +
+                                        [vp, sz, vp], i32),
+            "moe_workspace_size_host_e4m3": ([cfgp, ctypes.POINTER(sz)], i32),
+            "moe_forward_host_e4m3": ([cfgp, i32, vp, sz, vp, sz] + [vp] * 9 + [vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -302,6 +308,64 @@ def forward_host(cfg, x_host, y_host, Wg, gate_bias, expert_bias, W1, W3, W2, ws
     _check(lib().moe_forward_host(ctypes.byref(cfg), int(num_batches), _host(x_host), xs,
                                   _host(y_host), ys, _p(Wg), _p(gate_bias), _p(expert_bias),
                                   _p(W1), _p(W3), _p(W2), w, wb, _stream()), "moe_forward_host")
+
+
+def _host_batches(cfg, x_host, y_host, num_batches):
+    """Batch count and byte strides of host buffers [B,T,h] (or [T,h] reused)."""
+    T, h = cfg.num_tokens, cfg.hidden
+    if num_batches is None:
+        num_batches = x_host.shape[0] if x_host.dim() == 3 else 1
+    xs = x_host[0].numel() * x_host.element_size() if x_host.dim() == 3 else 0
+    ys = y_host[0].numel() * y_host.element_size() if y_host.dim() == 3 else 0
+    for t, stride in ((x_host, xs), (y_host, ys)):
+        per = T * h * t.element_size()
+        if (t.numel() * t.element_size()) < (per if stride == 0 else per * num_batches):
+            raise ValueError("host buffer smaller than its batches")
+    return num_batches, xs, ys
+
+
+def workspace_size_host_shared(cfg, fs):
+    v = ctypes.c_size_t()
+    _check(lib().moe_workspace_size_host_shared(ctypes.byref(cfg), int(fs), ctypes.byref(v)),
+           "moe_workspace_size_host_shared")
+    return v.value
+
+
+def alloc_workspace_host_shared(cfg, fs, device="cuda"):
+    return torch.zeros(workspace_size_host_shared(cfg, fs), dtype=torch.uint8, device=device)
+
+
+def forward_host_shared(cfg, fs, x_host, y_host, Wg, gate_bias, expert_bias, W1, W3, W2, W1s,
+                        W3s, W2s, ws, num_batches=None):
+    """forward_host with the shared expert (moe_forward_shared per batch)."""
+    n, xs, ys = _host_batches(cfg, x_host, y_host, num_batches)
+    w, wb = _ws(ws)
+    _check(lib().moe_forward_host_shared(ctypes.byref(cfg), int(fs), int(n), _host(x_host), xs,
+                                         _host(y_host), ys, _p(Wg), _p(gate_bias),
+                                         _p(expert_bias), _p(W1), _p(W3), _p(W2), _p(W1s),
+                                         _p(W3s), _p(W2s), w, wb, _stream()),
+           "moe_forward_host_shared")
+
+
+def workspace_size_host_e4m3(cfg):
+    v = ctypes.c_size_t()
+    _check(lib().moe_workspace_size_host_e4m3(ctypes.byref(cfg), ctypes.byref(v)),
+           "moe_workspace_size_host_e4m3")
+    return v.value
+
+
+def alloc_workspace_host_e4m3(cfg, device="cuda"):
+    return torch.zeros(workspace_size_host_e4m3(cfg), dtype=torch.uint8, device=device)
+
+
+def forward_host_e4m3(cfg, x_host, y_host, Wg, gate_bias, expert_bias, q, ws, num_batches=None):
+    """forward_host with E4M3 experts (moe_forward_e4m3 per batch); q: E4m3Experts."""
+    n, xs, ys = _host_batches(cfg, x_host, y_host, num_batches)
+    w, wb = _ws(ws)
+    _check(lib().moe_forward_host_e4m3(ctypes.byref(cfg), int(n), _host(x_host), xs,
+                                       _host(y_host), ys, _p(Wg), _p(gate_bias), _p(expert_bias),
+                                       _p(q.W1q), _p(q.s1), _p(q.W3q), _p(q.s3), _p(q.W2q),
+                                       _p(q.s2), w, wb, _stream()), "moe_forward_host_e4m3")
 
 
 # ------------------------------------------------------------- E4M3 experts

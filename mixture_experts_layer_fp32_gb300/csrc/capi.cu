@@ -469,10 +469,13 @@ moe_status copy_streams(CopyStreams** out) {
 struct HostLayout {
   size_t x_stage[2], y_stage[2], total;
 };
-HostLayout make_host_layout(const moe_config& c) {
+// Staging for the host-I/O forward: two input and two output slots of [T,h]
+// after the forward's own workspace (`base` bytes: the routed, shared or
+// E4M3 layout).
+HostLayout make_host_layout(const moe_config& c, size_t base) {
   HostLayout H;
   const size_t row = static_cast<size_t>(c.num_tokens) * c.hidden * (c.dtype == MOE_F32 ? 4 : 2);
-  size_t o = make_layout(c).total;
+  size_t o = base;
   for (int i = 0; i < 2; ++i) {
     H.x_stage[i] = o;
     o = align_up(o + row);
@@ -606,6 +609,124 @@ moe_status do_backward(const moe_config* cfg, const void* x, const float* Wg,
                            static_cast<const __nv_bfloat16*>(dA) + fi, 2 * fi, expert_offsets,
                            dW3, err, stream));
   if (sh) MOE_TRY(shared_bwd_wgrad(c, *sh, x, dy, at<void>(ws, B.dA_s), err, stream));
+  return MOE_OK;
+}
+
+// moe_forward_shared after its argument checks (also one batch of
+// moe_forward_host_shared): the shared expert forked onto the side stream,
+// the routed path on `stream`, joined before the combine.
+moe_status shared_forward_body(const moe_config& c, int32_t fs, const void* x, const float* Wg,
+                               const float* gate_bias, const float* expert_bias, const void* W1,
+                               const void* W3, const void* W2, const void* W1s, const void* W3s,
+                               const void* W2s, void* y, int32_t* topk_idx, float* topk_prob,
+                               int32_t* tokens_per_expert, void* ws, cudaStream_t stream) {
+  const SharedLayout S = make_shared_layout(c, fs);
+  void* h_mid_s = at<void>(ws, S.h_mid_s);
+  float* y_shared = at<float>(ws, S.y_shared);
+  int* err = at<int>(ws, make_layout(c).err);
+
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream* side = nullptr;
+  MOE_TRY(side_stream(&side));
+  // fork: the shared expert on the side stream, after everything already on `stream`
+  MOE_CUDA(cudaEventRecord(side->fork, stream));
+  MOE_CUDA(cudaStreamWaitEvent(side->stream, side->fork, 0));
+  const moe_status st_side = do_shared(c, fs, x, W1s, W3s, W2s, h_mid_s, y_shared, err,
+                                       side->stream);
+  const cudaError_t rec = cudaEventRecord(side->join, side->stream);
+  Routed r{};
+  const moe_status st = routed_path(c, x, Wg, gate_bias, expert_bias, W1, W3, W2, topk_idx,
+                                    topk_prob, tokens_per_expert, ws, stream, &r);
+  // join even after a failure, so that `stream` never stays forked (a capture
+  // in progress would be invalidated)
+  const cudaError_t wait = rec == cudaSuccess ? cudaStreamWaitEvent(stream, side->join, 0) : rec;
+  MOE_TRY(st_side);
+  MOE_TRY(st);
+  MOE_CUDA(wait);
+  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm, r.row_map, r.prob,
+                          y_shared, y, stream));
+  return MOE_OK;
+}
+
+// moe_forward_e4m3 after its argument checks (also one batch of
+// moe_forward_host_e4m3).
+moe_status e4m3_forward_body(const moe_config& c, const void* x, const float* Wg,
+                             const float* gate_bias, const float* expert_bias, const uint8_t* W1q,
+                             const float* s1, const uint8_t* W3q, const float* s3,
+                             const uint8_t* W2q, const float* s2, void* y, int32_t* topk_idx,
+                             float* topk_prob, int32_t* tokens_per_expert, void* ws,
+                             cudaStream_t stream) {
+  const E4m3Layout Q = make_e4m3_layout(c);
+  const Layout L = make_layout(c);
+  int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
+  float* prob = topk_prob ? topk_prob : at<float>(ws, L.topk_prob);
+  int32_t* tpe = tokens_per_expert ? tokens_per_expert : at<int32_t>(ws, L.tpe);
+  uint8_t* keep = at<uint8_t>(ws, L.keep);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* row_map = at<int32_t>(ws, L.row_map);
+  uint8_t* xperm_q = at<uint8_t>(ws, Q.xperm_q);
+  float* xperm_s = at<float>(ws, Q.xperm_s);
+  MOE_TRY(do_route(c, x, Wg, gate_bias, expert_bias, idx, prob, keep, tpe, nullptr, ws, stream));
+  MOE_TRY(do_permute_e4m3(c, x, idx, keep, xperm_q, xperm_s, row_map, offsets, ws, stream));
+  MOE_TRY(do_mlp_e4m3(c, xperm_q, xperm_s, offsets, W1q, s1, W3q, s3, W2q, s2,
+                      at<void>(ws, L.h_mid), at<uint8_t>(ws, Q.hq), at<float>(ws, Q.hs),
+                      at<float>(ws, L.y_perm), ws, stream));
+  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, at<float>(ws, L.y_perm),
+                          row_map, prob, nullptr, y, stream));
+  return MOE_OK;
+}
+
+// The host-I/O loop of the moe_forward_host family: batch b's input is
+// copied from the pinned host buffer into staging slot b & 1 on the h2d copy
+// stream, forward(x_stage, y_stage) enqueues the forward on `stream`, and the
+// output is copied back on the d2h stream, so that neighbouring batches'
+// copies overlap the current batch's compute.  Per slot, events order input
+// ready / input free / output ready / output free.
+template <typename F>
+moe_status host_pipeline(const moe_config& c, int32_t num_batches, const void* x_host,
+                         size_t x_batch_stride, void* y_host, size_t y_batch_stride,
+                         size_t row_bytes, const HostLayout& H, void* ws, cudaStream_t stream,
+                         F&& forward) {
+  std::lock_guard<std::mutex> lock(g_copy_mu);
+  CopyStreams* cs = nullptr;
+  MOE_TRY(copy_streams(&cs));
+  // both copy streams start after everything already enqueued on `stream`
+  MOE_CUDA(cudaEventRecord(cs->fork, stream));
+  MOE_CUDA(cudaStreamWaitEvent(cs->h2d, cs->fork, 0));
+  MOE_CUDA(cudaStreamWaitEvent(cs->d2h, cs->fork, 0));
+  moe_status st = MOE_OK;
+  for (int32_t b = 0; b < num_batches && st == MOE_OK; ++b) {
+    const int slot = b & 1;
+    void* xs = at<void>(ws, H.x_stage[slot]);
+    void* ys = at<void>(ws, H.y_stage[slot]);
+    const char* xb = static_cast<const char*>(x_host) + static_cast<size_t>(b) * x_batch_stride;
+    char* yb = static_cast<char*>(y_host) + static_cast<size_t>(b) * y_batch_stride;
+    // input copy: after the forward that last read this staging slot
+    st = cuda_status(cudaStreamWaitEvent(cs->h2d, cs->x_free[slot], 0));
+    if (st == MOE_OK && row_bytes)
+      st = cuda_status(cudaMemcpyAsync(xs, xb, row_bytes, cudaMemcpyHostToDevice, cs->h2d));
+    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->x_ready[slot], cs->h2d));
+    // forward: after its input landed and the output slot was copied out
+    if (st == MOE_OK) st = cuda_status(cudaStreamWaitEvent(stream, cs->x_ready[slot], 0));
+    if (st == MOE_OK) st = cuda_status(cudaStreamWaitEvent(stream, cs->y_free[slot], 0));
+    if (st == MOE_OK) st = forward(xs, ys);
+    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->x_free[slot], stream));
+    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->y_ready[slot], stream));
+    // output copy: after the forward wrote it
+    if (st == MOE_OK) st = cuda_status(cudaStreamWaitEvent(cs->d2h, cs->y_ready[slot], 0));
+    if (st == MOE_OK && row_bytes)
+      st = cuda_status(cudaMemcpyAsync(yb, ys, row_bytes, cudaMemcpyDeviceToHost, cs->d2h));
+    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->y_free[slot], cs->d2h));
+  }
+  // join: `stream` completes only after every copy (also after a failure, so
+  // that no copy stream is left running ahead of the caller's stream)
+  const cudaError_t j1 = cudaEventRecord(cs->h2d_done, cs->h2d);
+  const cudaError_t j2 = cudaEventRecord(cs->d2h_done, cs->d2h);
+  const cudaError_t w1 = j1 == cudaSuccess ? cudaStreamWaitEvent(stream, cs->h2d_done, 0) : j1;
+  const cudaError_t w2 = j2 == cudaSuccess ? cudaStreamWaitEvent(stream, cs->d2h_done, 0) : j2;
+  MOE_TRY(st);
+  MOE_CUDA(w1);
+  MOE_CUDA(w2);
   return MOE_OK;
 }
 
@@ -809,33 +930,9 @@ moe_status moe_forward_shared(const moe_config* cfg, int32_t fs, const void* x, 
   MOE_TRY(optional(topk_idx, 4));
   MOE_TRY(optional(topk_prob, 4));
   MOE_TRY(optional(tokens_per_expert, 4));
-  const SharedLayout S = make_shared_layout(c, fs);
-  MOE_TRY(check_ws(c, ws, ws_bytes, S.total));
-  void* h_mid_s = at<void>(ws, S.h_mid_s);
-  float* y_shared = at<float>(ws, S.y_shared);
-  int* err = at<int>(ws, make_layout(c).err);
-
-  std::lock_guard<std::mutex> lock(g_side_mu);
-  SideStream* side = nullptr;
-  MOE_TRY(side_stream(&side));
-  // fork: the shared expert on the side stream, after everything already on `stream`
-  MOE_CUDA(cudaEventRecord(side->fork, stream));
-  MOE_CUDA(cudaStreamWaitEvent(side->stream, side->fork, 0));
-  const moe_status st_side = do_shared(c, fs, x, W1s, W3s, W2s, h_mid_s, y_shared, err,
-                                       side->stream);
-  const cudaError_t rec = cudaEventRecord(side->join, side->stream);
-  Routed r{};
-  const moe_status st = routed_path(c, x, Wg, gate_bias, expert_bias, W1, W3, W2, topk_idx,
-                                    topk_prob, tokens_per_expert, ws, stream, &r);
-  // join even after a failure, so that `stream` never stays forked (a capture
-  // in progress would be invalidated)
-  const cudaError_t wait = rec == cudaSuccess ? cudaStreamWaitEvent(stream, side->join, 0) : rec;
-  MOE_TRY(st_side);
-  MOE_TRY(st);
-  MOE_CUDA(wait);
-  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm, r.row_map, r.prob,
-                          y_shared, y, stream));
-  return MOE_OK;
+  MOE_TRY(check_ws(c, ws, ws_bytes, make_shared_layout(c, fs).total));
+  return shared_forward_body(c, fs, x, Wg, gate_bias, expert_bias, W1, W3, W2, W1s, W3s, W2s, y,
+                             topk_idx, topk_prob, tokens_per_expert, ws, stream);
 }
 
 moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
@@ -1032,25 +1129,9 @@ moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* W
   MOE_TRY(optional(topk_idx, 4));
   MOE_TRY(optional(topk_prob, 4));
   MOE_TRY(optional(tokens_per_expert, 4));
-  const E4m3Layout Q = make_e4m3_layout(c);
-  MOE_TRY(check_ws(c, ws, ws_bytes, Q.total));
-  const Layout L = make_layout(c);
-  int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
-  float* prob = topk_prob ? topk_prob : at<float>(ws, L.topk_prob);
-  int32_t* tpe = tokens_per_expert ? tokens_per_expert : at<int32_t>(ws, L.tpe);
-  uint8_t* keep = at<uint8_t>(ws, L.keep);
-  int32_t* offsets = at<int32_t>(ws, L.offsets);
-  int32_t* row_map = at<int32_t>(ws, L.row_map);
-  uint8_t* xperm_q = at<uint8_t>(ws, Q.xperm_q);
-  float* xperm_s = at<float>(ws, Q.xperm_s);
-  MOE_TRY(do_route(c, x, Wg, gate_bias, expert_bias, idx, prob, keep, tpe, nullptr, ws, stream));
-  MOE_TRY(do_permute_e4m3(c, x, idx, keep, xperm_q, xperm_s, row_map, offsets, ws, stream));
-  MOE_TRY(do_mlp_e4m3(c, xperm_q, xperm_s, offsets, W1q, s1, W3q, s3, W2q, s2,
-                      at<void>(ws, L.h_mid), at<uint8_t>(ws, Q.hq), at<float>(ws, Q.hs),
-                      at<float>(ws, L.y_perm), ws, stream));
-  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, at<float>(ws, L.y_perm),
-                          row_map, prob, nullptr, y, stream));
-  return MOE_OK;
+  MOE_TRY(check_ws(c, ws, ws_bytes, make_e4m3_layout(c).total));
+  return e4m3_forward_body(c, x, Wg, gate_bias, expert_bias, W1q, s1, W3q, s3, W2q, s2, y,
+                           topk_idx, topk_prob, tokens_per_expert, ws, stream);
 }
 
 moe_status moe_workspace_size_backward(const moe_config* cfg, size_t* bytes) {
@@ -1123,7 +1204,7 @@ moe_status moe_shared_expert_backward(const moe_config* cfg, int32_t fs, const v
 moe_status moe_workspace_size_host(const moe_config* cfg, size_t* bytes) {
   MOE_TRY(validate(cfg));
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
-  *bytes = make_host_layout(*cfg).total;
+  *bytes = make_host_layout(*cfg, make_layout(*cfg).total).total;
   return MOE_OK;
 }
 
@@ -1148,57 +1229,114 @@ moe_status moe_forward_host(const moe_config* cfg, int32_t num_batches, const vo
   MOE_TRY(need(W1, wsz, 16));
   MOE_TRY(need(W3, wsz, 16));
   MOE_TRY(need(W2, wsz, 16));
-  const HostLayout H = make_host_layout(c);
+  const HostLayout H = make_host_layout(c, make_layout(c).total);
   MOE_TRY(check_ws(c, ws, ws_bytes, H.total));
   if (num_batches == 0) return MOE_OK;
 
-  std::lock_guard<std::mutex> lock(g_copy_mu);
-  CopyStreams* cs = nullptr;
-  MOE_TRY(copy_streams(&cs));
-  // both copy streams start after everything already enqueued on `stream`
-  MOE_CUDA(cudaEventRecord(cs->fork, stream));
-  MOE_CUDA(cudaStreamWaitEvent(cs->h2d, cs->fork, 0));
-  MOE_CUDA(cudaStreamWaitEvent(cs->d2h, cs->fork, 0));
-  moe_status st = MOE_OK;
-  for (int32_t b = 0; b < num_batches && st == MOE_OK; ++b) {
-    const int slot = b & 1;
-    void* xs = at<void>(ws, H.x_stage[slot]);
-    void* ys = at<void>(ws, H.y_stage[slot]);
-    const char* xb = static_cast<const char*>(x_host) + static_cast<size_t>(b) * x_batch_stride;
-    char* yb = static_cast<char*>(y_host) + static_cast<size_t>(b) * y_batch_stride;
-    // input copy: after the forward that last read this staging slot
-    st = cuda_status(cudaStreamWaitEvent(cs->h2d, cs->x_free[slot], 0));
-    if (st == MOE_OK && row_bytes)
-      st = cuda_status(cudaMemcpyAsync(xs, xb, row_bytes, cudaMemcpyHostToDevice, cs->h2d));
-    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->x_ready[slot], cs->h2d));
-    // forward: after its input landed and the output slot was copied out
-    if (st == MOE_OK) st = cuda_status(cudaStreamWaitEvent(stream, cs->x_ready[slot], 0));
-    if (st == MOE_OK) st = cuda_status(cudaStreamWaitEvent(stream, cs->y_free[slot], 0));
-    Routed r{};
-    if (st == MOE_OK)
-      st = routed_path(c, xs, Wg, gate_bias, expert_bias, W1, W3, W2, nullptr, nullptr, nullptr,
-                       ws, stream, &r);
-    if (st == MOE_OK)
-      st = cuda_status(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm,
-                                      r.row_map, r.prob, nullptr, ys, stream));
-    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->x_free[slot], stream));
-    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->y_ready[slot], stream));
-    // output copy: after the forward wrote it
-    if (st == MOE_OK) st = cuda_status(cudaStreamWaitEvent(cs->d2h, cs->y_ready[slot], 0));
-    if (st == MOE_OK && row_bytes)
-      st = cuda_status(cudaMemcpyAsync(yb, ys, row_bytes, cudaMemcpyDeviceToHost, cs->d2h));
-    if (st == MOE_OK) st = cuda_status(cudaEventRecord(cs->y_free[slot], cs->d2h));
-  }
-  // join: `stream` completes only after every copy (also after a failure, so
-  // that no copy stream is left running ahead of the caller's stream)
-  const cudaError_t j1 = cudaEventRecord(cs->h2d_done, cs->h2d);
-  const cudaError_t j2 = cudaEventRecord(cs->d2h_done, cs->d2h);
-  const cudaError_t w1 = j1 == cudaSuccess ? cudaStreamWaitEvent(stream, cs->h2d_done, 0) : j1;
-  const cudaError_t w2 = j2 == cudaSuccess ? cudaStreamWaitEvent(stream, cs->d2h_done, 0) : j2;
-  MOE_TRY(st);
-  MOE_CUDA(w1);
-  MOE_CUDA(w2);
+  return host_pipeline(c, num_batches, x_host, x_batch_stride, y_host, y_batch_stride, row_bytes,
+                       H, ws, stream, [&](void* xs, void* ys) {
+                         Routed r{};
+                         MOE_TRY(routed_path(c, xs, Wg, gate_bias, expert_bias, W1, W3, W2,
+                                             nullptr, nullptr, nullptr, ws, stream, &r));
+                         MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype,
+                                                 r.y_perm, r.row_map, r.prob, nullptr, ys,
+                                                 stream));
+                         return MOE_OK;
+                       });
+}
+
+// Host-buffer argument checks shared by the moe_forward_host family.
+static moe_status check_host_io(const moe_config& c, int32_t num_batches, const void* x_host,
+                                void* y_host, size_t y_batch_stride, size_t* row_bytes) {
+  if (num_batches < 0) return MOE_ERR_INVALID_ARG;
+  *row_bytes = static_cast<size_t>(c.num_tokens) * c.hidden * (c.dtype == MOE_F32 ? 4 : 2);
+  if (num_batches > 0 && *row_bytes > 0 && (x_host == nullptr || y_host == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (num_batches > 1 && y_batch_stride != 0 && y_batch_stride < *row_bytes)
+    return MOE_ERR_INVALID_ARG;  // output batches would overlap
   return MOE_OK;
+}
+
+moe_status moe_workspace_size_host_shared(const moe_config* cfg, int32_t fs, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  MOE_TRY(validate_fs(*cfg, fs));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = make_host_layout(*cfg, make_shared_layout(*cfg, fs).total).total;
+  return MOE_OK;
+}
+
+moe_status moe_forward_host_shared(const moe_config* cfg, int32_t fs, int32_t num_batches,
+                                   const void* x_host, size_t x_batch_stride, void* y_host,
+                                   size_t y_batch_stride, const float* Wg, const float* gate_bias,
+                                   const float* expert_bias, const void* W1, const void* W3,
+                                   const void* W2, const void* W1s, const void* W3s,
+                                   const void* W2s, void* ws, size_t ws_bytes,
+                                   moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_fs(c, fs));
+  size_t row_bytes = 0;
+  MOE_TRY(check_host_io(c, num_batches, x_host, y_host, y_batch_stride, &row_bytes));
+  const size_t E = c.num_experts, h = c.hidden, wsz = E * h * c.ffn_hidden;
+  MOE_TRY(need(Wg, h * E, 4));
+  MOE_TRY(optional(gate_bias, 4));
+  MOE_TRY(optional(expert_bias, 4));
+  MOE_TRY(need(W1, wsz, 16));
+  MOE_TRY(need(W3, wsz, 16));
+  MOE_TRY(need(W2, wsz, 16));
+  MOE_TRY(need(W1s, h * fs, 16));
+  MOE_TRY(need(W3s, h * fs, 16));
+  MOE_TRY(need(W2s, h * fs, 16));
+  const HostLayout H = make_host_layout(c, make_shared_layout(c, fs).total);
+  MOE_TRY(check_ws(c, ws, ws_bytes, H.total));
+  if (num_batches == 0) return MOE_OK;
+  return host_pipeline(c, num_batches, x_host, x_batch_stride, y_host, y_batch_stride, row_bytes,
+                       H, ws, stream, [&](void* xs, void* ys) {
+                         return shared_forward_body(c, fs, xs, Wg, gate_bias, expert_bias, W1, W3,
+                                                    W2, W1s, W3s, W2s, ys, nullptr, nullptr,
+                                                    nullptr, ws, stream);
+                       });
+}
+
+moe_status moe_workspace_size_host_e4m3(const moe_config* cfg, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  MOE_TRY(validate_e4m3(*cfg));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = make_host_layout(*cfg, make_e4m3_layout(*cfg).total).total;
+  return MOE_OK;
+}
+
+moe_status moe_forward_host_e4m3(const moe_config* cfg, int32_t num_batches, const void* x_host,
+                                 size_t x_batch_stride, void* y_host, size_t y_batch_stride,
+                                 const float* Wg, const float* gate_bias,
+                                 const float* expert_bias, const uint8_t* W1q, const float* s1,
+                                 const uint8_t* W3q, const float* s3, const uint8_t* W2q,
+                                 const float* s2, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_e4m3(c));
+  size_t row_bytes = 0;
+  MOE_TRY(check_host_io(c, num_batches, x_host, y_host, y_batch_stride, &row_bytes));
+  const size_t E = c.num_experts, h = c.hidden, f = c.ffn_hidden, wsz = E * h * f;
+  MOE_TRY(need(Wg, h * E, 4));
+  MOE_TRY(optional(gate_bias, 4));
+  MOE_TRY(optional(expert_bias, 4));
+  MOE_TRY(need(W1q, wsz, 16));
+  MOE_TRY(need(W3q, wsz, 16));
+  MOE_TRY(need(W2q, wsz, 16));
+  MOE_TRY(need(s1, E * f, 16));
+  MOE_TRY(need(s3, E * f, 16));
+  MOE_TRY(need(s2, E * h, 16));
+  const HostLayout H = make_host_layout(c, make_e4m3_layout(c).total);
+  MOE_TRY(check_ws(c, ws, ws_bytes, H.total));
+  if (num_batches == 0) return MOE_OK;
+  return host_pipeline(c, num_batches, x_host, x_batch_stride, y_host, y_batch_stride, row_bytes,
+                       H, ws, stream, [&](void* xs, void* ys) {
+                         return e4m3_forward_body(c, xs, Wg, gate_bias, expert_bias, W1q, s1, W3q,
+                                                  s3, W2q, s2, ys, nullptr, nullptr, nullptr, ws,
+                                                  stream);
+                       });
 }
 
 moe_status moe_check(void* ws, moe_stream_t stream, int32_t* info) {

@@ -73,3 +73,49 @@ def test_forward_host_zero_batches_and_empty_tokens():
                      num_batches=0)
     torch.cuda.current_stream().synchronize()
     moe.check(ws)
+
+
+def test_forward_host_shared_batches_equal_forward_shared():
+    # the shared-expert variant: each batch forks the shared expert onto the
+    # library's side stream inside the copy pipeline
+    import mixture_experts_layer_fp32_gb300 as moe
+    w = synthetic.scaled("dsv3_shared", T=300, h=512, f=256, E=32, k=4, shared_f=256, seed=111)
+    cfg = gpu_config(w)
+    B = 4
+    d, x_host = _inputs(w, B)
+    y_host = torch.full((B, w.T, w.h), float("nan"), dtype=x_host.dtype).pin_memory()
+    ws = moe.alloc_workspace_host_shared(cfg, w.shared_f)
+    moe.forward_host_shared(cfg, w.shared_f, x_host, y_host, d["Wg"], d["gate_bias"],
+                            d["expert_bias"], d["W1"], d["W3"], d["W2"], d["W1s"], d["W3s"],
+                            d["W2s"], ws)
+    moe.check(ws)
+    torch.cuda.synchronize()
+    ws1 = moe.alloc_workspace_shared(cfg, w.shared_f)
+    for b in range(B):
+        y = torch.empty((w.T, w.h), dtype=moe.act_dtype(cfg), device="cuda")
+        moe.forward_shared(cfg, w.shared_f, x_host[b].cuda(), d["Wg"], d["gate_bias"],
+                           d["expert_bias"], d["W1"], d["W3"], d["W2"], d["W1s"], d["W3s"],
+                           d["W2s"], y, ws1)
+        moe.check(ws1)
+        assert torch.equal(y_host[b], y.cpu()), b
+
+
+def test_forward_host_e4m3_batches_equal_forward_e4m3():
+    import mixture_experts_layer_fp32_gb300 as moe
+    w = synthetic.scaled("mixtral", T=700, h=512, f=256, seed=112)
+    cfg = gpu_config(w)
+    B = 4
+    d, x_host = _inputs(w, B)
+    q = moe.E4m3Experts(cfg, d["W1"], d["W3"], d["W2"])
+    y_host = torch.full((B, w.T, w.h), float("nan"), dtype=x_host.dtype).pin_memory()
+    ws = moe.alloc_workspace_host_e4m3(cfg)
+    moe.forward_host_e4m3(cfg, x_host, y_host, d["Wg"], d["gate_bias"], d["expert_bias"], q, ws)
+    moe.check(ws)
+    torch.cuda.synchronize()
+    ws1 = moe.alloc_workspace_e4m3(cfg)
+    for b in range(B):
+        y = torch.empty((w.T, w.h), dtype=moe.act_dtype(cfg), device="cuda")
+        moe.forward_e4m3(cfg, x_host[b].cuda(), d["Wg"], d["gate_bias"], d["expert_bias"], q, y,
+                         ws1)
+        moe.check(ws1)
+        assert torch.equal(y_host[b], y.cpu()), b
