@@ -527,6 +527,9 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
+// PL: experts per lane (E <= 32 * PL): the per-lane loops cover no more
+// entries than E needs.
+template <int PL>
 __global__ void __launch_bounds__(256)
     router_topk_kernel(int T, int E, int k, int score, int num_groups, int group_topk,
                        const float* __restrict__ logits,
@@ -546,9 +549,9 @@ __global__ void __launch_bounds__(256)
   const int per_group = num_groups > 1 ? E / num_groups : E;
   for (int t = blockIdx.x * nwarps + warp; t < T; t += gridDim.x * nwarps) {
     // logits = (partial sums in split order) + gate bias
-    float s[kMaxPerLane], sel[kMaxPerLane];
+    float s[PL], sel[PL];
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < PL; ++i) {
       const int e = lane + 32 * i;
       if (e < E) {
         float l = logits[(int64_t)t * E + e];
@@ -561,12 +564,12 @@ __global__ void __launch_bounds__(256)
     if (score == MOE_SCORE_SOFTMAX_PRE) {
       float m = -FLT_MAX;
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) m = fmaxf(m, s[i]);
+      for (int i = 0; i < PL; ++i) m = fmaxf(m, s[i]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       float z = 0.f;
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < PL; ++i) {
         const int e = lane + 32 * i;
         s[i] = (e < E) ? expf(s[i] - m) : 0.f;
         z += s[i];
@@ -574,14 +577,14 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < PL; ++i) {
         const int e = lane + 32 * i;
         s[i] = (e < E) ? s[i] / z : 0.f;
         sel[i] = (e < E) ? s[i] : -FLT_MAX;
       }
     } else if (score == MOE_SCORE_SIGMOID || score == MOE_SCORE_SQRTSOFTPLUS) {
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < PL; ++i) {
         const int e = lane + 32 * i;
         if (e < E) {
           if (score == MOE_SCORE_SIGMOID) {
@@ -598,7 +601,7 @@ __global__ void __launch_bounds__(256)
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) sel[i] = s[i];
+      for (int i = 0; i < PL; ++i) sel[i] = s[i];
     }
 
     // group-limited top-k: lane g < num_groups scores group g (the sum of its
@@ -608,7 +611,7 @@ __global__ void __launch_bounds__(256)
     uint32_t taken = 0;
     if (num_groups > 1) {
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < PL; ++i) {
         const int e = lane + 32 * i;
         if (e < E) gsel[warp][e] = sel[i];
       }
@@ -649,7 +652,7 @@ __global__ void __launch_bounds__(256)
         if (bi < num_groups) kept |= 1u << bi;
       }
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < PL; ++i) {
         const int e = lane + 32 * i;
         if (e < E && !(kept >> (e / per_group) & 1u)) taken |= 1u << i;
       }
@@ -662,7 +665,7 @@ __global__ void __launch_bounds__(256)
       float bv = -INFINITY;
       int bi = 0x7fffffff;
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < PL; ++i) {
         const int e = lane + 32 * i;
         if (e < E && !(taken >> i & 1u) && better(sel[i], e, bv, bi)) {
           bv = sel[i];
@@ -685,7 +688,7 @@ __global__ void __launch_bounds__(256)
       const int owner = bi & 31;
       float sv = 0.f;
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i)
+      for (int i = 0; i < PL; ++i)
         if (lane == owner && (bi >> 5) == i) {
           taken |= 1u << i;
           sv = s[i];
@@ -752,9 +755,12 @@ __global__ void __launch_bounds__(1024)
     return;
   }
   const int cap = static_cast<int>(capacity);
+  constexpr int kCache = 4096;  // candidates whose keys stay in shared memory (32 KB)
+  __shared__ unsigned long long skey[kCache];
   __shared__ int hist[256];
   __shared__ unsigned long long s_prefix;
   __shared__ int s_remaining;
+  const int lane = threadIdx.x & 31;
 
   auto key_of = [&](int r) -> unsigned long long {
     const int pair = cand_pair[begin + r];
@@ -762,6 +768,11 @@ __global__ void __launch_bounds__(1024)
     const uint32_t tok = static_cast<uint32_t>(pair / k);
     return (static_cast<unsigned long long>(pb) << 32) | (0xFFFFFFFFu - tok);
   };
+  // keys read from memory once (two dependent loads each), not once per pass
+  const bool cached = policy == MOE_DROP_PROBS && n <= kCache;
+  if (cached)
+    for (int r = threadIdx.x; r < n; r += blockDim.x) skey[r] = key_of(r);
+  auto key_at = [&](int r) -> unsigned long long { return cached ? skey[r] : key_of(r); };
 
   unsigned long long thr = 0;
   if (policy == MOE_DROP_PROBS) {
@@ -775,19 +786,39 @@ __global__ void __launch_bounds__(1024)
       __syncthreads();
       const unsigned long long prefix = s_prefix;
       for (int r = threadIdx.x; r < n; r += blockDim.x) {
-        const unsigned long long key = key_of(r);
+        const unsigned long long key = key_at(r);
         if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int cum = 0, rem = s_remaining;
-        for (int b = 255; b >= 0; --b) {
-          if (cum + hist[b] >= rem) {
-            s_remaining = rem - cum;
-            s_prefix = prefix | (static_cast<unsigned long long>(b) << shift);
-            break;
+      if (threadIdx.x < 32) {
+        // the bin holding the rem-th largest key: lane l owns bins 255-8l ..
+        // 248-8l (descending), a warp prefix sum over the lanes' totals, the
+        // first lane whose running total reaches rem walks its 8 bins
+        const int rem = s_remaining;
+        int c[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = hist[255 - (lane * 8 + j)];
+          sum += c[j];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const uint32_t hit = __ballot_sync(0xffffffffu, incl >= rem);
+        if (hit && lane == __ffs(hit) - 1) {
+          int cum = incl - sum;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (cum + c[j] >= rem) {
+              s_remaining = rem - cum;
+              s_prefix = prefix | (static_cast<unsigned long long>(255 - (lane * 8 + j)) << shift);
+              break;
+            }
+            cum += c[j];
           }
-          cum += hist[b];
         }
       }
       mask |= 255ull << shift;
@@ -796,7 +827,7 @@ __global__ void __launch_bounds__(1024)
     thr = s_prefix;  // keys are unique: exactly `cap` keys are >= thr
   }
   for (int r = threadIdx.x; r < n; r += blockDim.x) {
-    const bool kept = (policy == MOE_DROP_PROBS) ? (key_of(r) >= thr) : (r < cap);
+    const bool kept = (policy == MOE_DROP_PROBS) ? (key_at(r) >= thr) : (r < cap);
     if (!kept) {
       const int pair = cand_pair[begin + r];
       keep[pair] = 0;
@@ -831,10 +862,11 @@ cudaError_t launch_router_topk(int T, int E, int k, int score, int num_groups, i
   int blocks = (T + warps_per_block - 1) / warps_per_block;
   const int cap = device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
-  router_topk_kernel<<<blocks, 32 * warps_per_block, 0, s>>>(
-      T, E, k, score, num_groups, group_topk, logits, nsplit, gate_bias, expert_bias, topk_idx,
-      topk_prob, keep,
-      routing_map, counts, err);
+  auto kern = E <= 32 ? router_topk_kernel<1> : E <= 64 ? router_topk_kernel<2>
+             : E <= 128 ? router_topk_kernel<4> : router_topk_kernel<kMaxPerLane>;
+  kern<<<blocks, 32 * warps_per_block, 0, s>>>(T, E, k, score, num_groups, group_topk, logits,
+                                               nsplit, gate_bias, expert_bias, topk_idx, topk_prob,
+                                               keep, routing_map, counts, err);
   return cudaGetLastError();
 }
 

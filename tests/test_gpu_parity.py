@@ -23,6 +23,10 @@ CASES = {
     "switch_small": synthetic.scaled("switch", T=4096, h=256, f=256, seed=14),
     "switch_small_position": synthetic.scaled("switch", T=2048, h=256, f=256, seed=15,
                                               drop_policy="position"),
+    # one expert with ~7000 routed tokens: more drop candidates than the
+    # drop kernel keeps in shared memory (4096), so its keys are re-read
+    "switch_one_hot": synthetic.scaled("switch", T=12000, h=256, f=256, E=8, seed=16,
+                                       gate_bias="hot:1:4.6"),
 }
 
 
