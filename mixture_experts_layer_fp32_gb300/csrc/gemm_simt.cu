@@ -5,15 +5,19 @@
 // expert-major rows.  SwiGLU: fc1 computes silu(X.W1[e]) * (X.W3[e]); fc2
 // computes H.W2[e].  The tensor cores have no fp32 mode that keeps fp32
 // accuracy (TF32 rounds operands to 10 mantissa bits), so fp32 stays on the
-// FMA units.  CTA tile 64 rows x 64 columns, K in chunks of 16, 256 threads
-// with a 4x4 micro-tile each; a CTA belongs to one expert's row block,
-// found from the expert offsets.
+// FMA units.  CTA tile 32 rows x 32 columns, K in chunks of 64, 256 threads
+// with a 2x2 micro-tile each; a CTA belongs to one expert's row block,
+// found from the expert offsets.  The fp32 workloads are small (latency
+// bound): small tiles give many CTAs and wide K chunks few memory round
+// trips per CTA, each thread's loads of a chunk issued before its stores.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int SBM = 64, SBN = 64, SBK = 16, SThreads = 256;
+constexpr int SBM = 32, SBN = 32, SBK = 64, SThreads = 256;
+constexpr int SPA = SBM * SBK / SThreads;  // A values per thread per chunk (8)
+constexpr int SPB = SBK * SBN / SThreads;  // B values per thread per chunk (8)
 
 template <bool SWIGLU>
 __global__ void __launch_bounds__(SThreads)
@@ -23,7 +27,7 @@ __global__ void __launch_bounds__(SThreads)
                         int* __restrict__ err) {
   __shared__ int off[MOE_MAX_EXPERTS + 1];
   __shared__ int tstart[MOE_MAX_EXPERTS + 1];
-  __shared__ __align__(16) float As[SBK][SBM];
+  __shared__ __align__(16) float As[SBK][SBM + 1];  // +1: the transposing stores spread over the banks
   __shared__ __align__(16) float Bs0[SBK][SBN];
   __shared__ __align__(16) float Bs1[SWIGLU ? SBK : 1][SWIGLU ? SBN : 4];
 
@@ -59,34 +63,50 @@ __global__ void __launch_bounds__(SThreads)
   const float* b1 = SWIGLU ? B1 + (int64_t)e * K * N : nullptr;
 
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;  // 16 x 16 threads
-  float acc0[4][4] = {}, acc1[4][4] = {};
+  float acc0[2][2] = {}, acc1[2][2] = {};
   for (int k0 = 0; k0 < K; k0 += SBK) {
-    for (int i = threadIdx.x; i < SBM * SBK; i += SThreads) {
+    float ra[SPA], rb0[SPB], rb1[SWIGLU ? SPB : 1];
+#pragma unroll
+    for (int u = 0; u < SPA; ++u) {
+      const int i = threadIdx.x + u * SThreads;
       const int r = i / SBK, kk = i % SBK;
       const int row = m0 + r;
-      As[kk][r] = (row < mend && k0 + kk < K) ? A[(int64_t)row * K + k0 + kk] : 0.f;
+      ra[u] = (row < mend && k0 + kk < K) ? A[(int64_t)row * K + k0 + kk] : 0.f;
     }
-    for (int i = threadIdx.x; i < SBK * SBN; i += SThreads) {
+#pragma unroll
+    for (int u = 0; u < SPB; ++u) {
+      const int i = threadIdx.x + u * SThreads;
       const int kk = i / SBN, c = i % SBN;
       const bool ok = (k0 + kk < K) && (n0 + c < N);
-      Bs0[kk][c] = ok ? b0[(int64_t)(k0 + kk) * N + n0 + c] : 0.f;
-      if (SWIGLU) Bs1[kk][c] = ok ? b1[(int64_t)(k0 + kk) * N + n0 + c] : 0.f;
+      rb0[u] = ok ? b0[(int64_t)(k0 + kk) * N + n0 + c] : 0.f;
+      if (SWIGLU) rb1[u] = ok ? b1[(int64_t)(k0 + kk) * N + n0 + c] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < SPA; ++u) {
+      const int i = threadIdx.x + u * SThreads;
+      As[i % SBK][i / SBK] = ra[u];
+    }
+#pragma unroll
+    for (int u = 0; u < SPB; ++u) {
+      const int i = threadIdx.x + u * SThreads;
+      Bs0[i / SBN][i % SBN] = rb0[u];
+      if (SWIGLU) Bs1[i / SBN][i % SBN] = rb1[u];
     }
     __syncthreads();
-#pragma unroll
+#pragma unroll 16
     for (int kk = 0; kk < SBK; ++kk) {
-      float a[4], b[4], g[4];
+      float a[2], b[2], g[2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+      for (int i = 0; i < 2; ++i) a[i] = As[kk][ty * 2 + i];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        b[j] = Bs0[kk][tx * 4 + j];
-        if (SWIGLU) g[j] = Bs1[kk][tx * 4 + j];
+      for (int j = 0; j < 2; ++j) {
+        b[j] = Bs0[kk][tx * 2 + j];
+        if (SWIGLU) g[j] = Bs1[kk][tx * 2 + j];
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
           acc0[i][j] = fmaf(a[i], b[j], acc0[i][j]);
           if (SWIGLU) acc1[i][j] = fmaf(a[i], g[j], acc1[i][j]);
         }
@@ -94,12 +114,12 @@ __global__ void __launch_bounds__(SThreads)
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int row = m0 + ty * 4 + i;
+  for (int i = 0; i < 2; ++i) {
+    const int row = m0 + ty * 2 + i;
     if (row >= mend) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = n0 + tx * 4 + j;
+    for (int j = 0; j < 2; ++j) {
+      const int c = n0 + tx * 2 + j;
       if (c >= N) continue;
       float v = acc0[i][j];
       if (SWIGLU) v = v / (1.f + expf(-v)) * acc1[i][j];
