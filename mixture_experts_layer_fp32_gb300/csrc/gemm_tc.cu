@@ -17,8 +17,9 @@
 //    columns of W2.
 //  * The tile list is built on the device from the expert offsets (written
 //    by the permutation kernel): expert e owns ceil(rows_e/128) row blocks x
-//    n-tiles, row blocks inner so that CTAs running together share the
-//    weight tile (L2) and the expert's rows.  No host synchronisation.
+//    n-tiles, the smaller side inner (row blocks, unless the expert has
+//    more rows than accumulator columns) so that CTAs running together share
+//    the re-read operand through L2.  No host synchronisation.
 //  * Warp roles: warp 0 lane 0 issues TMA loads (A tile 128x64 and four
 //    64xBK weight boxes per stage; a 4-deep ring of K=64 stages), warp 1
 //    allocates TMEM and lane 0 issues tcgen05.mma, warps 2-5 drain TMEM with
@@ -154,19 +155,34 @@ using Ctl = CtlN<STAGES>;
 
 // Tile `tile` of the device-built list: expert e, first row m0 of its row
 // block (ROWS rows per block), the expert's row end, and the n-tile.
+// Inside an expert the smaller side varies fastest, so that the ~150 tiles in
+// flight share the operand that is re-read: with fewer rows than accumulator
+// columns (NT x BN) the row blocks are inner and the CTAs in flight share one
+// weight n-tile while the expert's rows stay in L2; with more rows (an expert
+// holding a large share of the tokens) the n-tiles are inner, the expert's
+// weights stay in L2 and its rows stream once (row blocks inner would read
+// them once per n-tile).
 template <int ROWS = BM>
 __device__ __forceinline__ void decode_tile(int tile, const int* tstart, const int* off, int E,
-                                            int& e, int& m0, int& rend, int& nt) {
+                                            int NT, int& e, int& m0, int& rend, int& nt) {
   int lo = 0, hi = E;  // largest e in [0, E) with tstart[e] <= tile
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if (tstart[mid] <= tile) lo = mid; else hi = mid;
   }
   e = lo;
-  const int mt = (off[e + 1] - off[e] + ROWS - 1) / ROWS;
+  const int rows = off[e + 1] - off[e];
+  const int mt = (rows + ROWS - 1) / ROWS;
   const int u = tile - tstart[e];
-  nt = u / mt;
-  m0 = off[e] + (u - nt * mt) * ROWS;
+  int rb;
+  if (rows > NT * BN) {
+    rb = u / NT;
+    nt = u - rb * NT;
+  } else {
+    nt = u / mt;
+    rb = u - nt * mt;
+  }
+  m0 = off[e] + rb * ROWS;
   rend = off[e + 1];
 }
 
@@ -466,7 +482,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool alive = true;
       for (int tile = blockIdx.x; alive && tile < total; tile += gridDim.x) {
         int e, m0, rend, nt;
-        decode_tile(tile, tstart, off, E, e, m0, rend, nt);
+        decode_tile(tile, tstart, off, E, NT, e, m0, rend, nt);
         for (int kb = 0; kb < KB; ++kb) {
           if (!ctl.wait(ctl.empty(stage), phase ^ 1u, 1)) {
             alive = false;
@@ -605,7 +621,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int buf = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       int e, m0, rend, nt;
-      decode_tile(tile, tstart, off, E, e, m0, rend, nt);
+      decode_tile(tile, tstart, off, E, NT, e, m0, rend, nt);
       bool ok = ctl.wait(ctl.acc_full(buf), aph, 7);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -734,7 +750,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const CUtensorMap* tmB = (kGate && rank == 1) ? &tmB1 : &tmB0;
       for (int tile = pair; alive && tile < total; tile += npairs) {
         int e, m0, rend, nt;
-        decode_tile<PM>(tile, tstart, off, E, e, m0, rend, nt);
+        decode_tile<PM>(tile, tstart, off, E, NT, e, m0, rend, nt);
         const int n0 = kGate ? nt * (BN / 2) : nt * BN + static_cast<int>(rank) * (BN / 2);
         const int a_row = m0 + static_cast<int>(rank) * BM;
         for (int kb = 0; kb < KB; ++kb) {
@@ -861,7 +877,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int buf = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       int e, m0, rend, nt;
-      decode_tile<PM>(tile, tstart, off, E, e, m0, rend, nt);
+      decode_tile<PM>(tile, tstart, off, E, NT, e, m0, rend, nt);
       bool ok = ctl.wait(ctl.acc_full(buf), aph, 7);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
