@@ -205,7 +205,10 @@ def kernels_per_forward(w, cfg, fp8=False):
     import mixture_experts_layer_fp32_gb300 as moe
     cap = moe.capacity(cfg)
     drops = 0 <= cap < w.T
-    route = 2 + (4 if drops else 0)   # logits, top-k (+ hist, scan, rank, select)
+    # logits and top-k (one fused kernel when E <= 8 without groups and h <= 6144,
+    # the library's rule), + hist, scan, rank, select with drops
+    fused = w.E <= 8 and w.k <= w.E and w.num_groups <= 1 and w.h <= 6144
+    route = (1 if fused else 2) + (4 if drops else 0)
     shared = 2 if w.shared_f > 0 else 0  # the shared expert's fc1 and fc2
     quant = 2 if fp8 else 0           # E4M3: x rows before the permute, h rows before fc2
     return route + 4 + 1 + 1 + shared + quant + 1  # permute hist/scan/rank/copy, fc1, fc2, combine

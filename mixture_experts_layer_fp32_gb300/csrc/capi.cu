@@ -185,18 +185,26 @@ moe_status do_route(const moe_config& c, const void* x, const float* Wg, const f
   const bool drops = cap >= 0 && cap < T;
   MOE_CUDA(cudaMemsetAsync(tpe, 0, E * sizeof(int32_t), s));
   if (T == 0) return MOE_OK;
-  float* logits = at<float>(ws, L.logits);
-  int nsplit = 1;
-  MOE_CUDA(launch_router_logits(T, c.hidden, E, c.dtype, x, Wg, logits, &nsplit, s));
+  // logits then top-k, or both in one kernel for E <= 8; the per-expert
+  // counts go to tokens_per_expert, or (with drops) to the assigned counts
+  auto route_topk = [&](int32_t* counts) -> cudaError_t {
+    if (router_fused_ok(c.hidden, E, k, c.num_groups))
+      return launch_router_fused(T, c.hidden, E, k, c.dtype, c.score, x, Wg, gb, eb, topk_idx,
+                                 topk_prob, keep, routing_map, counts, err, s);
+    float* logits = at<float>(ws, L.logits);
+    int nsplit = 1;
+    cudaError_t st = launch_router_logits(T, c.hidden, E, c.dtype, x, Wg, logits, &nsplit, s);
+    if (st != cudaSuccess) return st;
+    return launch_router_topk(T, E, k, c.score, c.num_groups, c.group_topk, logits, nsplit, gb,
+                              eb, topk_idx, topk_prob, keep, routing_map, counts, err, s);
+  };
   if (!drops) {
-    MOE_CUDA(launch_router_topk(T, E, k, c.score, c.num_groups, c.group_topk, logits, nsplit, gb,
-                                eb, topk_idx, topk_prob, keep, routing_map, tpe, err, s));
+    MOE_CUDA(route_topk(tpe));
     return MOE_OK;
   }
   int32_t* assigned = at<int32_t>(ws, L.assigned);
   MOE_CUDA(cudaMemsetAsync(assigned, 0, E * sizeof(int32_t), s));
-  MOE_CUDA(launch_router_topk(T, E, k, c.score, c.num_groups, c.group_topk, logits, nsplit, gb,
-                              eb, topk_idx, topk_prob, keep, routing_map, assigned, err, s));
+  MOE_CUDA(route_topk(assigned));
   // candidate lists: every routed pair, expert-major, ascending token order
   const int64_t np = static_cast<int64_t>(T) * k;
   int32_t* ctiles = at<int32_t>(ws, L.cand_tiles);

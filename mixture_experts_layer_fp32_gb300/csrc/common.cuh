@@ -66,6 +66,14 @@ cudaError_t launch_router_topk(int T, int E, int k, int score, int num_groups, i
                                int32_t* topk_idx, float* topk_prob,
                                uint8_t* keep, uint8_t* routing_map, int32_t* counts, int* err,
                                cudaStream_t s);
+// E <= 8 without groups (and h small enough for the whole gate matrix in
+// shared memory): logits and top-k fused in one kernel
+bool router_fused_ok(int h, int E, int k, int num_groups);
+cudaError_t launch_router_fused(int T, int h, int E, int k, int dtype, int score, const void* x,
+                                const float* Wg, const float* gate_bias,
+                                const float* expert_bias, int32_t* topk_idx, float* topk_prob,
+                                uint8_t* keep, uint8_t* routing_map, int32_t* counts, int* err,
+                                cudaStream_t s);
 cudaError_t launch_drop_select(int T, int E, int k, int64_t capacity, int policy,
                                const int32_t* cand_offsets, const int32_t* cand_pair,
                                float* topk_prob, uint8_t* keep, uint8_t* routing_map,

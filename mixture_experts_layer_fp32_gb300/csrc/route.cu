@@ -210,18 +210,14 @@ struct Packed<__nv_bfloat16> {
   }
 };
 
-template <typename XT>
-__global__ void __launch_bounds__(kRouteThreads, 2)
-    router_logits_small_e_kernel(int T, int h, int E, int hslice, const XT* __restrict__ x,
-                                 const float* __restrict__ Wg, float* __restrict__ partials) {
-  extern __shared__ __align__(16) float wsm_small[];  // [hslice][8], chunk-swizzled
-  const int hb = blockIdx.y * hslice;                  // first feature of this slice
-  const int hn = min(hslice, h - hb);                  // features in this slice
-  float* logits = partials + (int64_t)blockIdx.y * T * E;
+// Gate rows [hb, hb + hn) of Wg [h, E], padded to 8 experts, into shared
+// memory in the chunk swizzle (by the whole CTA; the caller synchronises).
+__device__ __forceinline__ void stage_gate_rows(const float* __restrict__ Wg, int E, int hb,
+                                                int hn, float* wsm) {
   if (E == kSmallE && (reinterpret_cast<uintptr_t>(Wg) & 15) == 0) {
     // 16-byte copies, 8 loads in flight per thread before their stores
     const float4* src = reinterpret_cast<const float4*>(Wg + (int64_t)hb * kSmallE);
-    float4* dst = reinterpret_cast<float4*>(wsm_small);
+    float4* dst = reinterpret_cast<float4*>(wsm);
     const int n4 = hn * kSmallE / 4;
     for (int i0 = threadIdx.x; i0 < n4; i0 += blockDim.x * 8) {
       float4 r[8];
@@ -244,70 +240,92 @@ __global__ void __launch_bounds__(kRouteThreads, 2)
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int i = i0 + u * blockDim.x;
-        if (i < hn * kSmallE) wsm_small[swz_chunk(i >> 2) * 4 + (i & 3)] = r[u];
+        if (i < hn * kSmallE) wsm[swz_chunk(i >> 2) * 4 + (i & 3)] = r[u];
       }
     }
   }
-  __syncthreads();
+}
+
+// Dot products of the 4 tokens t0 .. t0+3 with the 8 staged gate columns over
+// features [hb, hb + hn) (hb, hn multiples of the vector width), by one
+// warp: lane l returns the sum for token t0 + l/8, expert l%8 (0 past T).
+template <typename XT>
+__device__ __forceinline__ float small_e_group_logits(const XT* __restrict__ x, int T, int h,
+                                                      int hb, int hn, const float* wsm, int t0,
+                                                      int lane) {
   constexpr int V = XVec<XT>::N;
   const int nvec = hn / V;
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int groups = (T + kSmallTok - 1) / kSmallTok;
   const uint4* xq = reinterpret_cast<const uint4*>(x);
   const int row_vecs = h / V;
   const int vb = hb / V;
-  for (int g = blockIdx.x * (kRouteThreads / 32) + warp; g < groups;
-       g += gridDim.x * (kRouteThreads / 32)) {
-    const int t0 = g * kSmallTok;
-    float acc[kSmallTok * kSmallE];
+  float acc[kSmallTok * kSmallE];
 #pragma unroll
-    for (int i = 0; i < kSmallTok * kSmallE; ++i) acc[i] = 0.f;
-    for (int v0 = lane; v0 < nvec; v0 += 32 * kSmallUnroll) {
-      uint4 xr[kSmallUnroll][kSmallTok];
+  for (int i = 0; i < kSmallTok * kSmallE; ++i) acc[i] = 0.f;
+  for (int v0 = lane; v0 < nvec; v0 += 32 * kSmallUnroll) {
+    uint4 xr[kSmallUnroll][kSmallTok];
 #pragma unroll
-      for (int u = 0; u < kSmallUnroll; ++u) {
-        const int v = v0 + 32 * u;
+    for (int u = 0; u < kSmallUnroll; ++u) {
+      const int v = v0 + 32 * u;
 #pragma unroll
-        for (int tk = 0; tk < kSmallTok; ++tk)
-          xr[u][tk] = (v < nvec && t0 + tk < T) ? xq[(int64_t)(t0 + tk) * row_vecs + vb + v]
-                                                 : make_uint4(0u, 0u, 0u, 0u);
-      }
+      for (int tk = 0; tk < kSmallTok; ++tk)
+        xr[u][tk] = (v < nvec && t0 + tk < T) ? xq[(int64_t)(t0 + tk) * row_vecs + vb + v]
+                                               : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
-      for (int u = 0; u < kSmallUnroll; ++u) {
-        const int v = v0 + 32 * u;
-        if (v >= nvec) break;
+    for (int u = 0; u < kSmallUnroll; ++u) {
+      const int v = v0 + 32 * u;
+      if (v >= nvec) break;
 #pragma unroll
-        for (int c = 0; c < V; ++c) {
-          const float4* wr = reinterpret_cast<const float4*>(wsm_small);
-          const int chunk = 2 * (v * V + c);
-          const float4 w0 = wr[swz_chunk(chunk)], w1 = wr[swz_chunk(chunk + 1)];
-          const float w[kSmallE] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      for (int c = 0; c < V; ++c) {
+        const float4* wr = reinterpret_cast<const float4*>(wsm);
+        const int chunk = 2 * (v * V + c);
+        const float4 w0 = wr[swz_chunk(chunk)], w1 = wr[swz_chunk(chunk + 1)];
+        const float w[kSmallE] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-          for (int tk = 0; tk < kSmallTok; ++tk) {
-            const float xe = Packed<XT>::at(xr[u][tk], c);
+        for (int tk = 0; tk < kSmallTok; ++tk) {
+          const float xe = Packed<XT>::at(xr[u][tk], c);
 #pragma unroll
-            for (int e = 0; e < kSmallE; ++e)
-              acc[tk * kSmallE + e] = fmaf(xe, w[e], acc[tk * kSmallE + e]);
-          }
+          for (int e = 0; e < kSmallE; ++e)
+            acc[tk * kSmallE + e] = fmaf(xe, w[e], acc[tk * kSmallE + e]);
         }
       }
     }
-    // reduce-scatter: after the step with offset o, a lane keeps the half of
-    // its values selected by (lane & o); at the end lane l holds index l.
+  }
+  // reduce-scatter: after the step with offset o, a lane keeps the half of
+  // its values selected by (lane & o); at the end lane l holds index l.
 #pragma unroll
-    for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
-      const bool upper = (lane & o) != 0;
+  for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+    const bool upper = (lane & o) != 0;
 #pragma unroll
-      for (int j = 0; j < n / 2; ++j) {
-        const float keep = upper ? acc[j + n / 2] : acc[j];
-        const float send = upper ? acc[j] : acc[j + n / 2];
-        acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-      }
+    for (int j = 0; j < n / 2; ++j) {
+      const float keep = upper ? acc[j + n / 2] : acc[j];
+      const float send = upper ? acc[j] : acc[j + n / 2];
+      acc[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
+  }
+  return acc[0];
+}
+
+template <typename XT>
+__global__ void __launch_bounds__(kRouteThreads, 2)
+    router_logits_small_e_kernel(int T, int h, int E, int hslice, const XT* __restrict__ x,
+                                 const float* __restrict__ Wg, float* __restrict__ partials) {
+  extern __shared__ __align__(16) float wsm_small[];  // [hslice][8], chunk-swizzled
+  const int hb = blockIdx.y * hslice;                  // first feature of this slice
+  const int hn = min(hslice, h - hb);                  // features in this slice
+  float* logits = partials + (int64_t)blockIdx.y * T * E;
+  stage_gate_rows(Wg, E, hb, hn, wsm_small);
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int groups = (T + kSmallTok - 1) / kSmallTok;
+  for (int g = blockIdx.x * (kRouteThreads / 32) + warp; g < groups;
+       g += gridDim.x * (kRouteThreads / 32)) {
+    const int t0 = g * kSmallTok;
+    const float v = small_e_group_logits<XT>(x, T, h, hb, hn, wsm_small, t0, lane);
     const int t = t0 + lane / kSmallE;
     const int e = lane % kSmallE;
-    if (t < T && e < E) logits[(int64_t)t * E + e] = acc[0];
+    if (t < T && e < E) logits[(int64_t)t * E + e] = v;
   }
 }
 
@@ -740,6 +758,130 @@ __global__ void __launch_bounds__(256)
     if (hist[e]) atomicAdd(&counts[e], hist[e]);
 }
 
+// ------------------------------------------------------------------ fused small-E router
+// E <= 8 without expert groups: logits and top-k in one kernel (one pass over
+// x, no logits buffer, one launch instead of two).  The whole gate matrix,
+// padded to 8 experts, sits in shared memory (one CTA per SM).  A warp forms
+// the logits of 4 tokens the way the small-E logits kernel does, over all of
+// h; afterwards lane 8q + e holds expert e of token t0 + q, so each 8-lane
+// segment is one token.  The segment then applies the gate bias, the score
+// function, k rounds of an arg-max (ties to the lower expert) and the
+// combine weights, with the formulas of the warp-per-token top-k kernel.
+constexpr int kFusedThreads = 512;
+constexpr int kFusedMaxHidden = 6144;  // 6144 x 8 x 4 B = 192 KB of gate rows
+
+template <typename XT>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    router_fused_small_e_kernel(int T, int h, int E, int k, int score, const XT* __restrict__ x,
+                                const float* __restrict__ Wg, const float* __restrict__ gate_bias,
+                                const float* __restrict__ expert_bias,
+                                int32_t* __restrict__ topk_idx, float* __restrict__ topk_prob,
+                                uint8_t* __restrict__ keep, uint8_t* __restrict__ routing_map,
+                                int32_t* __restrict__ counts, int* __restrict__ err) {
+  extern __shared__ __align__(16) float wsm_fused[];  // [h][8] chunk-swizzled, then hist[8]
+  int* hist = reinterpret_cast<int*>(wsm_fused + static_cast<size_t>(h) * kSmallE);
+  if (threadIdx.x < kSmallE) hist[threadIdx.x] = 0;
+  stage_gate_rows(Wg, E, 0, h, wsm_fused);
+  __syncthreads();
+  constexpr unsigned kAll = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int e = lane & (kSmallE - 1);  // this lane's expert in its segment
+  const int seg0 = lane & ~(kSmallE - 1);
+  const bool ev = e < E;
+  const int groups = (T + kSmallTok - 1) / kSmallTok;
+  for (int g = blockIdx.x * (kFusedThreads / 32) + warp; g < groups;
+       g += gridDim.x * (kFusedThreads / 32)) {
+    const int t = g * kSmallTok + lane / kSmallE;  // this segment's token
+    const float l = small_e_group_logits<XT>(x, T, h, 0, h, wsm_fused, g * kSmallTok, lane);
+    float sv = ev ? (gate_bias ? l + gate_bias[e] : l) : -FLT_MAX;
+    float sel;
+    if (score == MOE_SCORE_SOFTMAX_PRE) {
+      float m = sv;
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kAll, m, o));
+      sv = ev ? expf(sv - m) : 0.f;
+      float z = sv;
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) z += __shfl_xor_sync(kAll, z, o);
+      sv = ev ? sv / z : 0.f;
+      sel = ev ? sv : -FLT_MAX;
+    } else if (score == MOE_SCORE_SIGMOID || score == MOE_SCORE_SQRTSOFTPLUS) {
+      if (ev) {
+        if (score == MOE_SCORE_SIGMOID)
+          sv = 1.f / (1.f + expf(-sv));
+        else  // softplus(l) = max(l, 0) + log1p(e^-|l|): no overflow
+          sv = sqrtf(fmaxf(sv, 0.f) + log1pf(expf(-fabsf(sv))));
+        sel = expert_bias ? sv + expert_bias[e] : sv;
+      } else {
+        sv = 0.f;
+        sel = -FLT_MAX;
+      }
+    } else {
+      sel = sv;
+    }
+
+    // k rounds of an arg-max over the segment's not-yet-taken experts; the
+    // lane of expert j (j < k) keeps slot j
+    bool taken = false;
+    int my_idx = -1;
+    float my_s = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const bool cand = ev && !taken && better(sel, e, -INFINITY, 0x7fffffff);
+      float bv = cand ? sel : -INFINITY;
+      int bi = cand ? e : 0x7fffffff;
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(kAll, bv, o);
+        const int oi = __shfl_xor_sync(kAll, bi, o);
+        if (better(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (bi < 0 || bi >= E) {  // only on NaN logits
+        if (e == 0 && t < T) report_error(err, DEV_ERR_INDEX, t);
+        bi = 0;
+      }
+      if (e == bi) taken = true;
+      const float chosen = __shfl_sync(kAll, sv, seg0 + bi);
+      if (e == j) {
+        my_idx = bi;
+        my_s = chosen;
+      }
+    }
+
+    // combine weights
+    float p = 0.f;
+    if (score == MOE_SCORE_SOFTMAX_POST) {
+      const float m = __shfl_sync(kAll, my_s, seg0);  // slot 0 holds the largest
+      const float ex = (e < k) ? expf(my_s - m) : 0.f;
+      float z = ex;
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) z += __shfl_xor_sync(kAll, z, o);
+      p = ex / z;
+    } else if (score == MOE_SCORE_SOFTMAX_PRE) {
+      p = my_s;
+    } else {
+      float z = (e < k) ? my_s : 0.f;
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) z += __shfl_xor_sync(kAll, z, o);
+      p = my_s / (z + 1e-20f);
+    }
+    if (t < T) {
+      if (e < k) {
+        topk_idx[(int64_t)t * k + e] = my_idx;
+        topk_prob[(int64_t)t * k + e] = p;
+        keep[(int64_t)t * k + e] = 1;
+        atomicAdd(&hist[my_idx], 1);
+      }
+      if (routing_map && ev) routing_map[(int64_t)t * E + e] = taken ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < E && hist[threadIdx.x]) atomicAdd(&counts[threadIdx.x], hist[threadIdx.x]);
+}
+
 // ------------------------------------------------------------------ drop
 __global__ void __launch_bounds__(1024)
     drop_select_kernel(int k, int E, int64_t capacity, int policy,
@@ -867,6 +1009,47 @@ cudaError_t launch_router_topk(int T, int E, int k, int score, int num_groups, i
   kern<<<blocks, 32 * warps_per_block, 0, s>>>(T, E, k, score, num_groups, group_topk, logits,
                                                nsplit, gate_bias, expert_bias, topk_idx, topk_prob,
                                                keep, routing_map, counts, err);
+  return cudaGetLastError();
+}
+
+bool router_fused_ok(int h, int E, int k, int num_groups) {
+  return E >= 1 && E <= kSmallE && k >= 1 && k <= E && num_groups <= 1 && h >= 1 &&
+         h <= kFusedMaxHidden;
+}
+
+cudaError_t launch_router_fused(int T, int h, int E, int k, int dtype, int score, const void* x,
+                                const float* Wg, const float* gate_bias,
+                                const float* expert_bias, int32_t* topk_idx, float* topk_prob,
+                                uint8_t* keep, uint8_t* routing_map, int32_t* counts, int* err,
+                                cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (!router_fused_ok(h, E, k, 0)) return cudaErrorInvalidValue;
+  const int smem = h * kSmallE * static_cast<int>(sizeof(float)) + kSmallE * 4;
+  static bool configured[2][64] = {{false}};
+  int dev = 0;
+  cudaError_t st = cudaGetDevice(&dev);
+  if (st != cudaSuccess) return st;
+  const int ti = dtype == MOE_F32 ? 0 : 1;
+  if (dev < 64 && !configured[ti][dev]) {
+    const int max_smem = kFusedMaxHidden * kSmallE * static_cast<int>(sizeof(float)) + kSmallE * 4;
+    st = ti == 0 ? cudaFuncSetAttribute(router_fused_small_e_kernel<float>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem)
+                 : cudaFuncSetAttribute(router_fused_small_e_kernel<__nv_bfloat16>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (st != cudaSuccess) return st;
+    configured[ti][dev] = true;
+  }
+  const int groups = (T + kSmallTok - 1) / kSmallTok;
+  int grid = (groups + kFusedThreads / 32 - 1) / (kFusedThreads / 32);
+  if (grid > device_sm_count()) grid = device_sm_count();
+  if (ti == 0)
+    router_fused_small_e_kernel<float><<<grid, kFusedThreads, smem, s>>>(
+        T, h, E, k, score, static_cast<const float*>(x), Wg, gate_bias, expert_bias, topk_idx,
+        topk_prob, keep, routing_map, counts, err);
+  else
+    router_fused_small_e_kernel<__nv_bfloat16><<<grid, kFusedThreads, smem, s>>>(
+        T, h, E, k, score, static_cast<const __nv_bfloat16*>(x), Wg, gate_bias, expert_bias,
+        topk_idx, topk_prob, keep, routing_map, counts, err);
   return cudaGetLastError();
 }
 

@@ -1,7 +1,8 @@
 """Router variants against the oracle on the GPU: the sqrtsoftplus score
 and group-limited top-k (alone and together, with every score function and
-with capacity drops).  Routing and the permutation are bit-exact, outputs
-within the tolerances of the other parity tests."""
+with capacity drops), and every score function on the fused small-E router
+(E <= 8).  Routing and the permutation are bit-exact, outputs within the
+tolerances of the other parity tests."""
 
 import pytest
 import torch
@@ -29,6 +30,17 @@ CASES = {
     # 32 groups (the largest number) of 8 experts
     "grouped_32_groups": synthetic.scaled("dsv3_grouped", T=300, h=256, f=128, E=256,
                                           num_groups=32, group_topk=8, seed=97),
+    # E <= 8 without groups: the fused logits + top-k kernel, every score
+    # function, expert counts that leave idle lanes in a token's 8-lane
+    # segment, capacity drops, and the largest h whose gate rows it stages
+    "small_e_sigmoid_bias": synthetic.scaled("dsv3", T=500, h=512, f=256, E=8, k=4, seed=81),
+    "small_e_sqrtsoftplus_bias": synthetic.scaled("dsv3", T=500, h=512, f=256, E=8, k=2,
+                                                  score="sqrtsoftplus", seed=82),
+    "small_e_softmax_post_E5_k3": synthetic.scaled("mixtral", T=700, h=512, f=128, E=5, k=3,
+                                                   seed=83),
+    "small_e_softmax_pre_drop_E6": synthetic.scaled("switch", T=2000, h=256, f=256, E=6,
+                                                    gate_bias="hot:1:3", seed=84),
+    "small_e_max_hidden": synthetic.scaled("mixtral", T=300, h=6144, f=128, seed=85),
 }
 
 
