@@ -790,8 +790,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int seg0 = lane & ~(kSmallE - 1);
   const bool ev = e < E;
   const int groups = (T + kSmallTok - 1) / kSmallTok;
-  for (int g = blockIdx.x * (kFusedThreads / 32) + warp; g < groups;
-       g += gridDim.x * (kFusedThreads / 32)) {
+  // groups dealt round-robin over the CTAs first (group = warp * grid + CTA),
+  // so that every SM gets work when there are fewer groups than warps
+  for (int g = warp * gridDim.x + blockIdx.x; g < groups; g += gridDim.x * (kFusedThreads / 32)) {
     const int t = g * kSmallTok + lane / kSmallE;  // this segment's token
     const float l = small_e_group_logits<XT>(x, T, h, 0, h, wsm_fused, g * kSmallTok, lane);
     float sv = ev ? (gate_bias ? l + gate_bias[e] : l) : -FLT_MAX;
@@ -1040,7 +1041,7 @@ cudaError_t launch_router_fused(int T, int h, int E, int k, int dtype, int score
     configured[ti][dev] = true;
   }
   const int groups = (T + kSmallTok - 1) / kSmallTok;
-  int grid = (groups + kFusedThreads / 32 - 1) / (kFusedThreads / 32);
+  int grid = groups;  // one CTA per SM, as many SMs as there are 4-token groups
   if (grid > device_sm_count()) grid = device_sm_count();
   if (ti == 0)
     router_fused_small_e_kernel<float><<<grid, kFusedThreads, smem, s>>>(
