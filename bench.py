@@ -206,12 +206,15 @@ def kernels_per_forward(w, cfg, fp8=False):
     cap = moe.capacity(cfg)
     drops = 0 <= cap < w.T
     # logits and top-k (one fused kernel when E <= 8 without groups and h <= 6144,
-    # the library's rule), + hist, scan, rank, select with drops
+    # the library's rule); the permutation index is hist + scan/rank (one
+    # kernel up to 128 tiles of 2048 pairs, else scan and rank), run again for
+    # the drop candidates before the select kernel
     fused = w.E <= 8 and w.k <= w.E and w.num_groups <= 1 and w.h <= 6144
-    route = (1 if fused else 2) + (4 if drops else 0)
+    index = 2 if -(-w.T * w.k // 2048) <= 128 else 3
+    route = (1 if fused else 2) + (index + 1 if drops else 0)
     shared = 2 if w.shared_f > 0 else 0  # the shared expert's fc1 and fc2
-    quant = 2 if fp8 else 0           # E4M3: x rows before the permute, h rows before fc2
-    return route + 4 + 1 + 1 + shared + quant + 1  # permute hist/scan/rank/copy, fc1, fc2, combine
+    quant = 1 if fp8 else 0           # E4M3: the SwiGLU rows before fc2 (x is quantised by the copy)
+    return route + index + 1 + 1 + 1 + shared + quant + 1  # permute index + copy, fc1, fc2, combine
 
 
 def stage_work(w, R, fp8=False, active=None):
