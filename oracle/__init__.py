@@ -51,6 +51,9 @@ def _load():
         L.oracle_capacity_drop.argtypes = [i64, i32, i32, i64, i32, vp, vp, vp, vp]
         L.oracle_permute.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp]
         L.oracle_permute.restype = i64
+        L.oracle_pad_to_capacity.argtypes = [i64, i32, i32, i64, vp, vp, vp, vp]
+        L.oracle_permute_map.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.oracle_permute_map.restype = i64
         L.oracle_expert_rows.argtypes = [i64, i32, i32, vp, i32, vp, vp, vp, vp, i32, vp, vp, i32]
         L.oracle_combine.argtypes = [i64, i32, i32, vp, vp, vp, vp, i32]
         L.oracle_forward_dense.argtypes = [i64, i32, i32, i32, i32, vp, i32, vp, vp, vp,
@@ -154,6 +157,35 @@ def permute(topk_idx, keep, E):
     return offsets, row_map, row_token[:R].copy()
 
 
+def pad_to_capacity_map(topk_idx, keep, E, cap):
+    """final_map of apply_router_token_dropping with pad_to_capacity: every
+    expert column holds min(cap, T) tokens (the kept pairs, then the
+    lowest-index tokens not yet set).  Returns (map [T,E] u8, column sums)."""
+    topk_idx = _c(topk_idx, np.int32)
+    keep = _c(keep, np.uint8)
+    T, k = topk_idx.shape
+    m = np.empty((T, E), np.uint8)
+    n = np.empty((E,), np.int32)
+    _load().oracle_pad_to_capacity(T, E, k, int(cap), _ptr(topk_idx), _ptr(keep), _ptr(m), _ptr(n))
+    return m, n
+
+
+def permute_map(routing_map, topk_idx, keep):
+    """Permutation by a [T,E] routing map: rows of expert e are its tokens in
+    ascending order; row_map [T,k] holds the rows of the kept pairs."""
+    routing_map = _c(routing_map, np.uint8)
+    topk_idx = _c(topk_idx, np.int32)
+    keep = _c(keep, np.uint8)
+    T, E = routing_map.shape
+    k = topk_idx.shape[1]
+    offsets = np.empty((E + 1,), np.int32)
+    row_map = np.empty((T, k), np.int32)
+    row_token = np.empty((int(routing_map.sum()),), np.int32)
+    R = _load().oracle_permute_map(T, E, k, _ptr(routing_map), _ptr(topk_idx), _ptr(keep),
+                                   _ptr(offsets), _ptr(row_map), _ptr(row_token))
+    return offsets, row_map, row_token[:R].copy()
+
+
 def expert_rows(x_rows, row_expert, W1, W3, W2, want_h_mid=False, nthreads=0):
     """SwiGLU expert MLP on rows; returns y_rows [R,h] (and h_mid [R,f]) in float64."""
     x_rows = _c(x_rows)
@@ -199,8 +231,11 @@ def forward_dense(x, topk_idx, topk_prob, keep, W1, W3, W2, nthreads=0):
 
 
 def route(x, Wg, k, score, gate_bias=None, expert_bias=None, capacity_factor=0.0,
-          min_capacity=0, drop_policy="probs", nthreads=0, num_groups=0, group_topk=0):
-    """Router + optional capacity drop.  Returns a dict of numpy arrays."""
+          min_capacity=0, drop_policy="probs", nthreads=0, num_groups=0, group_topk=0,
+          pad_to_capacity=False):
+    """Router + optional capacity drop (and, with pad_to_capacity, the padded
+    routing map: "routing_map", with tokens_per_expert its column sums).
+    Returns a dict of numpy arrays."""
     T = x.shape[0]
     E = Wg.shape[1]
     logits = router_logits(x, Wg, gate_bias, nthreads)
@@ -209,9 +244,14 @@ def route(x, Wg, k, score, gate_bias=None, expert_bias=None, capacity_factor=0.0
     assigned = np.bincount(idx.reshape(-1), minlength=E).astype(np.int32)
     cap = capacity(T, E, k, capacity_factor, min_capacity)
     prob_final, keep, kept = capacity_drop(idx, prob, E, cap, drop_policy)
-    return {"logits": logits, "topk_idx": idx, "topk_prob_raw": prob, "margin": margin,
-            "assigned": assigned, "capacity": cap, "topk_prob": prob_final, "keep": keep,
-            "tokens_per_expert": kept}
+    out = {"logits": logits, "topk_idx": idx, "topk_prob_raw": prob, "margin": margin,
+           "assigned": assigned, "capacity": cap, "topk_prob": prob_final, "keep": keep,
+           "tokens_per_expert": kept}
+    if pad_to_capacity:
+        assert cap >= 0, "pad_to_capacity needs a capacity factor"
+        m, padded = pad_to_capacity_map(idx, keep, E, cap)
+        out.update({"routing_map": m, "tokens_per_expert": padded, "kept_per_expert": kept})
+    return out
 
 
 def shared_expert(x, W1s, W3s, W2s, want_h_mid=False, nthreads=0):
@@ -230,14 +270,20 @@ def shared_expert(x, W1s, W3s, W2s, want_h_mid=False, nthreads=0):
 
 def forward(x, Wg, W1, W3, W2, k, score, gate_bias=None, expert_bias=None,
             capacity_factor=0.0, min_capacity=0, drop_policy="probs", nthreads=0,
-            want_h_mid=False, W1s=None, W3s=None, W2s=None, num_groups=0, group_topk=0):
+            want_h_mid=False, W1s=None, W3s=None, W2s=None, num_groups=0, group_topk=0,
+            pad_to_capacity=False):
     """The whole layer: route -> drop -> permute -> SwiGLU experts -> combine,
     plus the shared expert's output when W1s/W3s/W2s are given (added to the
-    routed sum in double: y = sum_j p_j Y_j + Y_shared)."""
+    routed sum in double: y = sum_j p_j Y_j + Y_shared).  pad_to_capacity:
+    the experts run on the padded routing map's rows (the padding rows carry
+    no combine weight)."""
     r = route(x, Wg, k, score, gate_bias, expert_bias, capacity_factor, min_capacity,
-              drop_policy, nthreads, num_groups, group_topk)
+              drop_policy, nthreads, num_groups, group_topk, pad_to_capacity)
     E = Wg.shape[1]
-    offsets, row_map, row_token = permute(r["topk_idx"], r["keep"], E)
+    if pad_to_capacity:
+        offsets, row_map, row_token = permute_map(r["routing_map"], r["topk_idx"], r["keep"])
+    else:
+        offsets, row_map, row_token = permute(r["topk_idx"], r["keep"], E)
     row_expert = np.repeat(np.arange(E, dtype=np.int32), np.diff(offsets))
     x_perm = np.ascontiguousarray(np.asarray(x)[row_token])
     res = expert_rows(x_perm, row_expert, W1, W3, W2, want_h_mid=want_h_mid, nthreads=nthreads)

@@ -139,7 +139,7 @@ double bf16_round(double v) {
 
 extern "C" {
 
-int oracle_abi_version(void) { return 5; }
+int oracle_abi_version(void) { return 6; }
 
 // [MC] §3 Gating: logits = x . Wg (+ bias) with the router math in fp32.
 // The oracle forms the exact sum in double over the exact fp32 values of x
@@ -344,6 +344,69 @@ int64_t oracle_permute(int64_t T, int E, int k, const int32_t* topk_idx, const u
       if (row_token) row_token[r] = (int32_t)t;
     }
   }
+  return offsets[E];
+}
+
+// [MC] §8 apply_router_token_dropping with pad_to_capacity: final_map =
+// capacity_mask, the `capacity` tokens chosen per expert column of the dense
+// [T,E] probability map (capacity > T: every token).  Under capacity an expert
+// has fewer routed tokens than it keeps, so its capacity_mask is its routed
+// tokens plus tokens whose probability in that column is 0; the pages'
+// topk(..., sorted=False) leaves open which of those equal zeros are taken,
+// and the reading is the one used for every tie here: lower token index
+// first.  Over capacity it is the kept set of oracle_capacity_drop.  In map
+// form: start from the kept pairs (keep [T,k]) and give each expert column
+// min(capacity, T) ones, adding the lowest-index tokens that are not yet
+// set.  map [T,E] u8 out; padded_per_expert [E] out (the column sums).
+void oracle_pad_to_capacity(int64_t T, int E, int k, int64_t capacity, const int32_t* topk_idx,
+                            const uint8_t* keep, uint8_t* map, int32_t* padded_per_expert) {
+  for (int64_t i = 0; i < T * E; ++i) map[i] = 0;
+  for (int64_t t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j)
+      if (keep[t * k + j]) map[t * E + topk_idx[t * k + j]] = 1;
+  const int64_t quota = capacity > T ? T : capacity;
+  for (int e = 0; e < E; ++e) {
+    int64_t n = 0;
+    for (int64_t t = 0; t < T; ++t) n += map[t * E + e];
+    for (int64_t t = 0; t < T && n < quota; ++t) {
+      if (!map[t * E + e]) {
+        map[t * E + e] = 1;
+        ++n;
+      }
+    }
+    padded_per_expert[e] = (int32_t)n;
+  }
+}
+
+// [MC] §9 Token dispatcher from a [T,E] routing map (the dispatcher permutes
+// by the map: expert-major, ascending token index inside an expert).  Rows of
+// expert e are the tokens t with map[t,e] = 1; row_map [T,k] gives the row of
+// each kept pair (t,j) (its expert's column is set in the map) and -1 for the
+// others; row_token [rows] the source token of each row; offsets [E+1].
+// Returns the row count (the sum of the map).
+int64_t oracle_permute_map(int64_t T, int E, int k, const uint8_t* map, const int32_t* topk_idx,
+                           const uint8_t* keep, int32_t* offsets, int32_t* row_map,
+                           int32_t* row_token) {
+  std::vector<int64_t> count(E, 0);
+  for (int64_t t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) count[e] += map[t * E + e];
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = (int32_t)(offsets[e] + count[e]);
+  std::vector<int64_t> cursor(E);
+  for (int e = 0; e < E; ++e) cursor[e] = offsets[e];
+  std::vector<int64_t> row_of((size_t)(T * E), -1);
+  for (int64_t t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e)
+      if (map[t * E + e]) {
+        const int64_t r = cursor[e]++;
+        row_of[(size_t)(t * E + e)] = r;
+        if (row_token) row_token[r] = (int32_t)t;
+      }
+  for (int64_t t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      const int64_t p = t * k + j;
+      row_map[p] = keep[p] ? (int32_t)row_of[(size_t)(t * E + topk_idx[p])] : -1;
+    }
   return offsets[E];
 }
 
