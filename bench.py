@@ -211,7 +211,9 @@ def kernels_per_forward(w, cfg, fp8=False):
     # the drop candidates before the select kernel
     fused = w.E <= 8 and w.k <= w.E and w.num_groups <= 1 and w.h <= 6144
     index = 2 if -(-w.T * w.k // 2048) <= 128 else 3
-    route = (1 if fused else 2) + (index + 1 if drops else 0)
+    route = (1 if fused else 2) + (index + 1 if drops else 0) + (1 if w.pad_to_capacity else 0)
+    if w.pad_to_capacity:  # permutation by the padded map: hist, scan, rank, gather
+        return route + 4 + 1 + 1 + (2 if w.shared_f > 0 else 0) + 1
     shared = 2 if w.shared_f > 0 else 0  # the shared expert's fc1 and fc2
     quant = 1 if fp8 else 0           # E4M3: the SwiGLU rows before fc2 (x is quantised by the copy)
     return route + index + 1 + 1 + 1 + shared + quant + 1  # permute index + copy, fc1, fc2, combine
@@ -248,7 +250,8 @@ def run_native(args, rank, world, local):
     w = workload_of(args)
     inp = synthetic.generate(w, device=dev, seed=w.seed + 1000 * rank)
     cfg = moe.config(w.T, w.h, w.E, w.k, w.f, w.score, w.dtype, w.capacity_factor,
-                     w.min_capacity, w.drop_policy, w.num_groups, w.group_topk)
+                     w.min_capacity, w.drop_policy, w.num_groups, w.group_topk,
+                     w.pad_to_capacity)
     b = moe.Buffers(cfg, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -272,7 +275,8 @@ def run_native(args, rank, world, local):
     def step(ev=None):
         if ev: ev[0].record(stream)
         moe.route(cfg, inp["x"], inp["Wg"], inp["gate_bias"], inp["expert_bias"], b.topk_idx,
-                  b.topk_prob, b.keep, b.tokens_per_expert, None, b.ws)
+                  b.topk_prob, b.keep, b.tokens_per_expert,
+                  b.routing_map if w.pad_to_capacity else None, b.ws)
         if ev: ev[1].record(stream)
         if fp8:
             moe.permute_e4m3(cfg, inp["x"], b.topk_idx, b.keep, xq, xs, b.row_map,
@@ -282,8 +286,12 @@ def run_native(args, rank, world, local):
             if ev: ev[3].record(stream)
             moe.grouped_fc2_e4m3(cfg, b.h_mid, b.expert_offsets, q, hq, hs, b.y_perm, b.ws)
         else:
-            moe.permute(cfg, inp["x"], b.topk_idx, b.keep, b.x_perm, b.row_map,
-                        b.expert_offsets, b.ws)
+            if w.pad_to_capacity:  # the padded routing map drives the permutation
+                moe.permute_map(cfg, inp["x"], b.routing_map, b.topk_idx, b.keep, b.x_perm,
+                                b.row_map, b.expert_offsets, b.ws)
+            else:
+                moe.permute(cfg, inp["x"], b.topk_idx, b.keep, b.x_perm, b.row_map,
+                            b.expert_offsets, b.ws)
             if ev: ev[2].record(stream)
             moe.grouped_fc1(cfg, b.x_perm, b.expert_offsets, inp["W1"], inp["W3"], b.h_mid,
                             b.ws)

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 #define MOE_MAX_EXPERTS 256
 #define MOE_MAX_TOPK 8
 
@@ -97,6 +97,18 @@ typedef struct moe_config {
    * k <= group_topk * E/num_groups (MOE_ERR_UNSUPPORTED otherwise). */
   int32_t num_groups;
   int32_t group_topk;
+  /* pad_to_capacity of apply_router_token_dropping (§8 of the Megatron Core
+   * page; moe_pad_expert_input_to_capacity): 1 needs capacity_factor > 0
+   * (MOE_ERR_INVALID_ARG otherwise).  The routing map becomes the page's
+   * capacity_mask: each expert's column holds exactly min(capacity, T)
+   * tokens, its kept pairs and then, for an expert under capacity, the
+   * lowest-index tokens not routed to it (the page leaves the order of those
+   * equal zero probabilities open; lower token index first is the reading,
+   * as for every tie here).  Padding tokens carry no combine weight, so the
+   * layer output equals the unpadded one; the permuted buffers hold
+   * E * min(capacity, T) rows (moe_max_rows).  0: off.  The E4M3 and
+   * backward entry points return MOE_ERR_UNSUPPORTED when it is 1. */
+  int32_t pad_to_capacity;
 } moe_config;
 
 /* ABI version of the loaded library (MOE_ABI_VERSION). */
@@ -118,7 +130,8 @@ moe_status moe_capacity(const moe_config* cfg, int64_t* capacity);
  * (the forward's need, which covers each stage).  Host-only. */
 moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
-/* Row capacity of the permuted buffers: T*k (every pair kept). */
+/* Row capacity of the permuted buffers (x_perm, h_mid, y_perm): T*k (every
+ * pair kept), or with pad_to_capacity max(T*k, E * min(capacity, T)). */
 moe_status moe_max_rows(const moe_config* cfg, int64_t* rows);
 
 /*
@@ -133,8 +146,11 @@ moe_status moe_max_rows(const moe_config* cfg, int64_t* rows);
  *                       (equal scores: lower expert index first)
  *   topk_prob    [T,k]  fp32 out: combine weights; 0 for dropped pairs
  *   keep         [T,k]  uint8 out: 1 kept, 0 dropped (all 1 when dropless)
- *   tokens_per_expert [E] int32 out: kept pairs per expert
- *   routing_map  [T,E]  uint8 out or NULL: 1 where (t,e) is a kept pair
+ *   tokens_per_expert [E] int32 out: kept pairs per expert (pad_to_capacity:
+ *                       the padded count min(capacity, T) of every expert)
+ *   routing_map  [T,E]  uint8 out or NULL: 1 where (t,e) is a kept pair; with
+ *                       pad_to_capacity it is required and also holds the
+ *                       padding tokens (the input of moe_permute_map)
  */
 moe_status moe_route(const moe_config* cfg, const void* x, const float* Wg,
                      const float* gate_bias, const float* expert_bias, int32_t* topk_idx,
@@ -151,6 +167,8 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* Wg,
  *   row_map        [T,k]       int32 out: row of each pair, -1 if dropped
  *   expert_offsets [E+1]       int32 out: exclusive prefix of kept counts
  * An expert id outside [0,E) is skipped and flagged (MOE_ERR_DEVICE_CHECK).
+ * With pad_to_capacity the rows come from the padded routing map:
+ * MOE_ERR_INVALID_ARG (use moe_permute_map).
  */
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
                        const uint8_t* keep, void* x_perm, int32_t* row_map,
@@ -158,11 +176,34 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
                        moe_stream_t stream);
 
 /*
+ * The permutation of §9 driven by a routing map, as the dispatcher does with
+ * the map: expert e's rows are the tokens t with routing_map[t,e] = 1 in
+ * ascending order, so padding tokens sit among the kept ones.
+ *   x              [T,h]       dtype
+ *   routing_map    [T,E]       uint8 (any nonzero byte counts as 1)
+ *   topk_idx, keep [T,k]       (keep may be NULL = all kept); a kept pair's
+ *                              expert column must be set in the map
+ *   x_perm         [moe_max_rows,h] dtype out: rows [0, R) filled, R = the
+ *                              map's ones (expert_offsets[E])
+ *   row_map        [T,k]       int32 out: row of each kept pair, -1 otherwise
+ *   expert_offsets [E+1]       int32 out: exclusive prefix of the column sums
+ * A map with more ones than moe_max_rows rows: the rows past it are not
+ * written and moe_check reports MOE_ERR_DEVICE_CHECK.  Any configuration;
+ * with the routing map of moe_route and no padding it gives moe_permute's
+ * result.
+ */
+moe_status moe_permute_map(const moe_config* cfg, const void* x, const uint8_t* routing_map,
+                           const int32_t* topk_idx, const uint8_t* keep, void* x_perm,
+                           int32_t* row_map, int32_t* expert_offsets, void* ws,
+                           size_t ws_bytes, moe_stream_t stream);
+
+/*
  * Grouped expert MLP of §10 (TEGroupedMLP: every local expert in one call),
  * SwiGLU: for the rows [expert_offsets[e], expert_offsets[e+1]) of expert e,
  *   h_mid = silu(x_perm . W1[e]) * (x_perm . W3[e]),  y_perm = h_mid . W2[e].
- *   x_perm [T*k,h] dtype, W1/W3 [E,h,f] dtype, W2 [E,f,h] dtype,
- *   h_mid [T*k,f] dtype out, y_perm [T*k,h] fp32 out (rows >= R untouched).
+ *   x_perm [R_max,h] dtype, W1/W3 [E,h,f] dtype, W2 [E,f,h] dtype,
+ *   h_mid [R_max,f] dtype out, y_perm [R_max,h] fp32 out (rows >= R untouched),
+ *   R_max = moe_max_rows (T*k unless pad_to_capacity).
  * moe_grouped_fc1 / moe_grouped_fc2 are the two halves.
  */
 moe_status moe_grouped_mlp(const moe_config* cfg, const void* x_perm,
@@ -181,7 +222,7 @@ moe_status moe_grouped_fc2(const moe_config* cfg, const void* h_mid,
  * page): y[t] = sum over kept slots j, in slot order, of
  * topk_prob[t,j] * y_perm[row_map[t,j]], accumulated in fp32 and rounded
  * once to dtype.  A token with no kept pair gets 0.
- *   y_perm [T*k,h] fp32, row_map [T,k] int32, topk_prob [T,k] fp32, y [T,h] dtype out.
+ *   y_perm [R_max,h] fp32, row_map [T,k] int32, topk_prob [T,k] fp32, y [T,h] dtype out.
  */
 moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* row_map,
                        const float* topk_prob, void* y, moe_stream_t stream);

@@ -32,7 +32,8 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_c
            "moe_grouped_fc1_e4m3", "moe_grouped_fc2_e4m3", "moe_workspace_size_backward",
            "moe_backward", "moe_workspace_size_backward_shared", "moe_backward_shared",
            "moe_shared_expert_backward", "moe_workspace_size_host_shared",
-           "moe_forward_host_shared", "moe_workspace_size_host_e4m3", "moe_forward_host_e4m3"]
+           "moe_forward_host_shared", "moe_workspace_size_host_e4m3", "moe_forward_host_e4m3",
+           "moe_permute_map"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -41,7 +42,8 @@ class MoeConfig(ctypes.Structure):
                 ("ffn_hidden", ctypes.c_int32), ("score", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("drop_policy", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int32),
-                ("num_groups", ctypes.c_int32), ("group_topk", ctypes.c_int32)]
+                ("num_groups", ctypes.c_int32), ("group_topk", ctypes.c_int32),
+                ("pad_to_capacity", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -74,6 +76,7 @@ def lib():
             "moe_max_rows": ([cfgp, ctypes.POINTER(i64)], i32),
             "moe_route": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_permute": ([cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_permute_map": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_grouped_mlp": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_grouped_fc1": ([cfgp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_grouped_fc2": ([cfgp, vp, vp, vp, vp, vp, sz, vp], i32),
@@ -119,10 +122,11 @@ def lib():
 
 
 def config(T, h, E, k, f, score="softmax_post", dtype="bf16", capacity_factor=0.0,
-           min_capacity=0, drop_policy="probs", num_groups=0, group_topk=0):
+           min_capacity=0, drop_policy="probs", num_groups=0, group_topk=0,
+           pad_to_capacity=False):
     return MoeConfig(int(T), int(h), int(E), int(k), int(f), SCORE[score], DTYPE[dtype],
                      DROP_POLICY[drop_policy], float(capacity_factor), int(min_capacity),
-                     int(num_groups), int(group_topk))
+                     int(num_groups), int(group_topk), int(bool(pad_to_capacity)))
 
 
 def _check(code, where):
@@ -201,6 +205,14 @@ def permute(cfg, x, topk_idx, keep, x_perm, row_map, expert_offsets, ws):
     w, wb = _ws(ws)
     _check(lib().moe_permute(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(keep), _p(x_perm),
                              _p(row_map), _p(expert_offsets), w, wb, _stream()), "moe_permute")
+
+
+def permute_map(cfg, x, routing_map, topk_idx, keep, x_perm, row_map, expert_offsets, ws):
+    """moe_permute_map: the permutation driven by a [T,E] routing map."""
+    w, wb = _ws(ws)
+    _check(lib().moe_permute_map(ctypes.byref(cfg), _p(x), _p(routing_map), _p(topk_idx),
+                                 _p(keep), _p(x_perm), _p(row_map), _p(expert_offsets), w, wb,
+                                 _stream()), "moe_permute_map")
 
 
 def permute_noalloc(cfg, x, topk_idx, keep, x_perm, row_map, expert_offsets):

@@ -38,10 +38,31 @@ thread_local char g_last_cuda_error[256] = "";
 
 struct Layout {
   size_t err, logits, assigned, tiles, cand_rowmap, cand_src, cand_off, cand_tiles;
-  size_t topk_idx, topk_prob, keep, tpe, offsets, row_map, x_perm, h_mid, y_perm, total;
+  size_t topk_idx, topk_prob, keep, tpe, offsets, row_map, x_perm, h_mid, y_perm;
+  size_t map, map_tiles, row_src, total;
 };
 
 size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int64_t capacity_of(const moe_config& c) {
+  if (c.capacity_factor <= 0.f) return -1;
+  const double v = ceil((static_cast<double>(c.num_tokens) * c.topk / c.num_experts) *
+                        static_cast<double>(c.capacity_factor));
+  int64_t cap = static_cast<int64_t>(v);
+  if (cap < c.min_capacity) cap = c.min_capacity;
+  return cap;
+}
+
+// Rows of the permuted buffers: T*k, or with pad_to_capacity E * min(cap, T)
+// when that is more (every expert padded to its capacity).
+int64_t rows_of(const moe_config& c) {
+  const int64_t np = static_cast<int64_t>(c.num_tokens) * c.topk;
+  if (!c.pad_to_capacity) return np;
+  int64_t q = capacity_of(c);
+  if (q < 0 || q > c.num_tokens) q = c.num_tokens;
+  const int64_t padded = q * c.num_experts;
+  return padded > np ? padded : np;
+}
 
 Layout make_layout(const moe_config& c) {
   Layout L;
@@ -69,9 +90,14 @@ Layout make_layout(const moe_config& c) {
   L.tpe = take(E * 4);
   L.offsets = take((E + 1) * 4);
   L.row_map = take(np * 4);
-  L.x_perm = take(np * h * el);
-  L.h_mid = take(np * f * el);
-  L.y_perm = take(np * h * 4);
+  const size_t rows = static_cast<size_t>(rows_of(c));
+  L.x_perm = take(rows * h * el);
+  L.h_mid = take(rows * f * el);
+  L.y_perm = take(rows * h * 4);
+  // the permutation by a routing map (moe_permute_map, and the padded forward)
+  L.map = take(c.pad_to_capacity ? T * E : 0);
+  L.map_tiles = take(static_cast<size_t>(map_tiles(static_cast<int>(T))) * E * 4);
+  L.row_src = take(rows * 4);
   L.total = o;
   return L;
 }
@@ -88,6 +114,8 @@ moe_status validate(const moe_config* c) {
   if (c->drop_policy != MOE_DROP_PROBS && c->drop_policy != MOE_DROP_POSITION)
     return MOE_ERR_INVALID_ARG;
   if (isnan(c->capacity_factor) || isinf(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+  if (c->pad_to_capacity != 0 && c->pad_to_capacity != 1) return MOE_ERR_INVALID_ARG;
+  if (c->pad_to_capacity && c->capacity_factor <= 0.f) return MOE_ERR_INVALID_ARG;
   if (c->num_experts > MOE_MAX_EXPERTS || c->topk > MOE_MAX_TOPK || c->topk > c->num_experts)
     return MOE_ERR_UNSUPPORTED;
   if (c->hidden % 8 != 0 || c->ffn_hidden % 8 != 0) return MOE_ERR_UNSUPPORTED;
@@ -100,7 +128,7 @@ moe_status validate(const moe_config* c) {
       return MOE_ERR_UNSUPPORTED;
   }
   const int64_t np = static_cast<int64_t>(c->num_tokens) * c->topk;
-  if (np > (int64_t{1} << 30)) return MOE_ERR_UNSUPPORTED;
+  if (np > (int64_t{1} << 30) || rows_of(*c) > (int64_t{1} << 30)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -129,15 +157,6 @@ moe_status cuda_status(cudaError_t e) {
 }
 
 #define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
-
-int64_t capacity_of(const moe_config& c) {
-  if (c.capacity_factor <= 0.f) return -1;
-  const double v = ceil((static_cast<double>(c.num_tokens) * c.topk / c.num_experts) *
-                        static_cast<double>(c.capacity_factor));
-  int64_t cap = static_cast<int64_t>(v);
-  if (cap < c.min_capacity) cap = c.min_capacity;
-  return cap;
-}
 
 moe_status check_ws(const moe_config& c, const void* ws, size_t ws_bytes, size_t need_bytes = 0) {
   if (ws == nullptr || reinterpret_cast<uintptr_t>(ws) % 16 != 0) return MOE_ERR_INVALID_ARG;
@@ -200,6 +219,8 @@ moe_status do_route(const moe_config& c, const void* x, const float* Wg, const f
   };
   if (!drops) {
     MOE_CUDA(route_topk(tpe));
+    if (c.pad_to_capacity)  // capacity >= T: every token to every expert
+      MOE_CUDA(launch_pad_fill(T, E, k, T, nullptr, nullptr, tpe, routing_map, s));
     return MOE_OK;
   }
   int32_t* assigned = at<int32_t>(ws, L.assigned);
@@ -213,6 +234,22 @@ moe_status do_route(const moe_config& c, const void* x, const float* Wg, const f
                              at<int32_t>(ws, L.cand_src), coff, nullptr, err, s));
   MOE_CUDA(launch_drop_select(T, E, k, cap, c.drop_policy, coff, at<int32_t>(ws, L.cand_src),
                               topk_prob, keep, routing_map, tpe, s));
+  if (c.pad_to_capacity)  // fill the experts under capacity with the lowest free tokens
+    MOE_CUDA(launch_pad_fill(T, E, k, static_cast<int>(cap), coff, at<int32_t>(ws, L.cand_src),
+                             tpe, routing_map, s));
+  return MOE_OK;
+}
+
+// Permutation by a [T,E] routing map: an expert's rows are the tokens of its
+// column in ascending order; row_map holds the rows of the kept pairs.
+moe_status do_permute_map(const moe_config& c, const void* x, const uint8_t* map,
+                          const int32_t* topk_idx, const uint8_t* keep, void* x_perm,
+                          int32_t* row_map, int32_t* offsets, void* ws, cudaStream_t s) {
+  const Layout L = make_layout(c);
+  MOE_CUDA(launch_perm_by_map(c.num_tokens, c.hidden, c.num_experts, c.topk, c.dtype, rows_of(c),
+                              x, map, topk_idx, keep, at<int32_t>(ws, L.map_tiles),
+                              at<int32_t>(ws, L.row_src), x_perm, row_map, offsets,
+                              at<int>(ws, L.err), s));
   return MOE_OK;
 }
 
@@ -238,7 +275,7 @@ moe_status do_fc1(const moe_config& c, const void* x_perm, const int32_t* offset
                   const void* W3, void* h_mid, void* ws, cudaStream_t s) {
   const Layout L = make_layout(c);
   int* err = at<int>(ws, L.err);
-  const int64_t rows = static_cast<int64_t>(c.num_tokens) * c.topk;
+  const int64_t rows = rows_of(c);
   if (c.dtype == MOE_F32)
     MOE_CUDA(launch_simt_fc1(c.num_experts, c.hidden, c.ffn_hidden, rows,
                              static_cast<const float*>(x_perm), offsets,
@@ -254,7 +291,7 @@ moe_status do_fc2(const moe_config& c, const void* h_mid, const int32_t* offsets
                   float* y_perm, void* ws, cudaStream_t s) {
   const Layout L = make_layout(c);
   int* err = at<int>(ws, L.err);
-  const int64_t rows = static_cast<int64_t>(c.num_tokens) * c.topk;
+  const int64_t rows = rows_of(c);
   if (c.dtype == MOE_F32)
     MOE_CUDA(launch_simt_fc2(c.num_experts, c.hidden, c.ffn_hidden, rows,
                              static_cast<const float*>(h_mid), offsets,
@@ -307,8 +344,13 @@ moe_status routed_path(const moe_config& c, const void* x, const float* Wg,
   void* x_perm = at<void>(ws, L.x_perm);
   void* h_mid = at<void>(ws, L.h_mid);
   float* y_perm = at<float>(ws, L.y_perm);
-  MOE_TRY(do_route(c, x, Wg, gate_bias, expert_bias, idx, prob, keep, tpe, nullptr, ws, stream));
-  MOE_TRY(do_permute(c, x, idx, keep, x_perm, row_map, offsets, ws, stream));
+  // pad_to_capacity: the padded routing map (workspace) drives the permutation
+  uint8_t* map = c.pad_to_capacity ? at<uint8_t>(ws, L.map) : nullptr;
+  MOE_TRY(do_route(c, x, Wg, gate_bias, expert_bias, idx, prob, keep, tpe, map, ws, stream));
+  if (map)
+    MOE_TRY(do_permute_map(c, x, map, idx, keep, x_perm, row_map, offsets, ws, stream));
+  else
+    MOE_TRY(do_permute(c, x, idx, keep, x_perm, row_map, offsets, ws, stream));
   MOE_TRY(do_fc1(c, x_perm, offsets, W1, W3, h_mid, ws, stream));
   MOE_TRY(do_fc2(c, h_mid, offsets, W2, y_perm, ws, stream));
   *out = Routed{idx, prob, tpe, row_map, y_perm};
@@ -362,7 +404,8 @@ E4m3Layout make_e4m3_layout(const moe_config& c) {
 }
 
 moe_status validate_e4m3(const moe_config& c) {
-  return c.dtype == MOE_BF16 ? MOE_OK : MOE_ERR_UNSUPPORTED;  // bf16 in/out, E4M3 experts
+  // bf16 in/out, E4M3 experts; the padded layout is not built for them
+  return c.dtype == MOE_BF16 && !c.pad_to_capacity ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 
 // E4M3 permute: quantise x per token, rank the pairs, copy code rows and scales.
@@ -547,7 +590,7 @@ moe_status do_backward(const moe_config* cfg, const void* x, const float* Wg,
                        const SharedBwd* sh, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
-  if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c.dtype != MOE_BF16 || c.pad_to_capacity) return MOE_ERR_UNSUPPORTED;
   if (sh) MOE_TRY(check_shared_bwd(c, *sh));
   const size_t T = c.num_tokens, E = c.num_experts, k = c.topk, h = c.hidden, f = c.ffn_hidden;
   const size_t R = T * k, wsz = E * h * f;
@@ -652,7 +695,7 @@ moe_status shared_forward_body(const moe_config& c, int32_t fs, const void* x, c
   MOE_TRY(st);
   MOE_CUDA(wait);
   MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm, r.row_map, r.prob,
-                          y_shared, y, stream));
+                          y_shared, y, stream, rows_of(c)));
   return MOE_OK;
 }
 
@@ -776,7 +819,7 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
 moe_status moe_max_rows(const moe_config* cfg, int64_t* rows) {
   MOE_TRY(validate(cfg));
   if (rows == nullptr) return MOE_ERR_INVALID_ARG;
-  *rows = static_cast<int64_t>(cfg->num_tokens) * cfg->topk;
+  *rows = rows_of(*cfg);
   return MOE_OK;
 }
 
@@ -795,7 +838,10 @@ moe_status moe_route(const moe_config* cfg, const void* x, const float* Wg,
   MOE_TRY(need(topk_prob, T * k, 4));
   MOE_TRY(need(keep, T * k, 1));
   MOE_TRY(need(tokens_per_expert, E, 4));
-  MOE_TRY(optional(routing_map, 1));
+  if (c.pad_to_capacity)  // the padded map is the output the padded permutation needs
+    MOE_TRY(need(routing_map, T * E, 1));
+  else
+    MOE_TRY(optional(routing_map, 1));
   MOE_TRY(check_ws(c, ws, ws_bytes));
   return do_route(c, x, Wg, gate_bias, expert_bias, topk_idx, topk_prob, keep, tokens_per_expert,
                   routing_map, ws, stream);
@@ -807,6 +853,7 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
                        moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
+  if (c.pad_to_capacity) return MOE_ERR_INVALID_ARG;  // padding rows come from the map
   const size_t T = c.num_tokens, k = c.topk;
   MOE_TRY(need(x, T * c.hidden, 16));
   MOE_TRY(need(topk_idx, T * k, 4));
@@ -818,12 +865,31 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
   return do_permute(c, x, topk_idx, keep, x_perm, row_map, expert_offsets, ws, stream);
 }
 
+moe_status moe_permute_map(const moe_config* cfg, const void* x, const uint8_t* routing_map,
+                           const int32_t* topk_idx, const uint8_t* keep, void* x_perm,
+                           int32_t* row_map, int32_t* expert_offsets, void* ws, size_t ws_bytes,
+                           moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  const size_t T = c.num_tokens, k = c.topk, E = c.num_experts;
+  MOE_TRY(need(x, T * c.hidden, 16));
+  MOE_TRY(need(routing_map, T * E, 1));
+  MOE_TRY(need(topk_idx, T * k, 4));
+  MOE_TRY(optional(keep, 1));
+  MOE_TRY(need(x_perm, static_cast<size_t>(rows_of(c)) * c.hidden, 16));
+  MOE_TRY(need(row_map, T * k, 4));
+  MOE_TRY(need(expert_offsets, E + 1, 4));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  return do_permute_map(c, x, routing_map, topk_idx, keep, x_perm, row_map, expert_offsets, ws,
+                        stream);
+}
+
 moe_status moe_grouped_fc1(const moe_config* cfg, const void* x_perm,
                            const int32_t* expert_offsets, const void* W1, const void* W3,
                            void* h_mid, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
-  const size_t R = static_cast<size_t>(c.num_tokens) * c.topk;
+  const size_t R = static_cast<size_t>(rows_of(c));
   const size_t wsz = static_cast<size_t>(c.num_experts) * c.hidden * c.ffn_hidden;
   MOE_TRY(need(x_perm, R * c.hidden, 16));
   MOE_TRY(need(expert_offsets, c.num_experts + 1, 4));
@@ -839,7 +905,7 @@ moe_status moe_grouped_fc2(const moe_config* cfg, const void* h_mid,
                            void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
-  const size_t R = static_cast<size_t>(c.num_tokens) * c.topk;
+  const size_t R = static_cast<size_t>(rows_of(c));
   const size_t wsz = static_cast<size_t>(c.num_experts) * c.hidden * c.ffn_hidden;
   MOE_TRY(need(h_mid, R * c.ffn_hidden, 16));
   MOE_TRY(need(expert_offsets, c.num_experts + 1, 4));
@@ -862,12 +928,12 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
   const size_t T = c.num_tokens, k = c.topk;
-  MOE_TRY(need(y_perm, T * k * c.hidden, 16));
+  MOE_TRY(need(y_perm, static_cast<size_t>(rows_of(c)) * c.hidden, 16));
   MOE_TRY(need(row_map, T * k, 4));
   MOE_TRY(need(topk_prob, T * k, 4));
   MOE_TRY(need(y, T * c.hidden, 16));
   MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, y_perm, row_map, topk_prob,
-                          nullptr, y, stream));
+                          nullptr, y, stream, rows_of(c)));
   return MOE_OK;
 }
 
@@ -877,13 +943,13 @@ moe_status moe_combine_shared(const moe_config* cfg, const float* y_perm, const 
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
   const size_t T = c.num_tokens, k = c.topk;
-  MOE_TRY(need(y_perm, T * k * c.hidden, 16));
+  MOE_TRY(need(y_perm, static_cast<size_t>(rows_of(c)) * c.hidden, 16));
   MOE_TRY(need(row_map, T * k, 4));
   MOE_TRY(need(topk_prob, T * k, 4));
   MOE_TRY(optional(y_shared, 16));
   MOE_TRY(need(y, T * c.hidden, 16));
   MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, y_perm, row_map, topk_prob,
-                          y_shared, y, stream));
+                          y_shared, y, stream, rows_of(c)));
   return MOE_OK;
 }
 
@@ -968,7 +1034,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
   MOE_TRY(routed_path(c, x, Wg, gate_bias, expert_bias, W1, W3, W2, topk_idx, topk_prob,
                       tokens_per_expert, ws, stream, &r));
   MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm, r.row_map, r.prob,
-                          nullptr, y, stream));
+                          nullptr, y, stream, rows_of(c)));
   return MOE_OK;
 }
 
@@ -1144,7 +1210,7 @@ moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* W
 
 moe_status moe_workspace_size_backward(const moe_config* cfg, size_t* bytes) {
   MOE_TRY(validate(cfg));
-  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (cfg->dtype != MOE_BF16 || cfg->pad_to_capacity) return MOE_ERR_UNSUPPORTED;
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
   *bytes = make_bwd_layout(*cfg).total;
   return MOE_OK;
@@ -1164,7 +1230,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* Wg,
 
 moe_status moe_workspace_size_backward_shared(const moe_config* cfg, int32_t fs, size_t* bytes) {
   MOE_TRY(validate(cfg));
-  if (cfg->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (cfg->dtype != MOE_BF16 || cfg->pad_to_capacity) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(validate_fs(*cfg, fs));
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
   *bytes = make_bwd_layout(*cfg, fs).total;
@@ -1248,7 +1314,7 @@ moe_status moe_forward_host(const moe_config* cfg, int32_t num_batches, const vo
                                              nullptr, nullptr, nullptr, ws, stream, &r));
                          MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype,
                                                  r.y_perm, r.row_map, r.prob, nullptr, ys,
-                                                 stream));
+                                                 stream, rows_of(c)));
                          return MOE_OK;
                        });
 }

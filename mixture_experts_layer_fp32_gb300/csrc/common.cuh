@@ -66,6 +66,22 @@ cudaError_t launch_router_topk(int T, int E, int k, int score, int num_groups, i
                                int32_t* topk_idx, float* topk_prob,
                                uint8_t* keep, uint8_t* routing_map, int32_t* counts, int* err,
                                cudaStream_t s);
+// Permutation by a [T,E] routing map (pad_to_capacity): tile_counts holds
+// map_tiles(T) x E ints, row_src max_rows ints; offsets [E+1] out; rows past
+// max_rows are reported in err and not written.
+int64_t map_tiles(int T);
+cudaError_t launch_perm_by_map(int T, int h, int E, int k, int dtype, int64_t max_rows,
+                               const void* x, const uint8_t* map, const int32_t* topk_idx,
+                               const uint8_t* keep, int32_t* tile_counts, int32_t* row_src,
+                               void* x_perm, int32_t* row_map, int32_t* offsets, int* err,
+                               cudaStream_t s);
+// pad_to_capacity: fill each expert's column of the routing map up to quota
+// ones with the lowest-index tokens not routed to it (cand_off / cand_pair:
+// the drop candidate lists; NULL when nothing is dropped: every token);
+// tokens_per_expert holds the kept counts in and the quota out.
+cudaError_t launch_pad_fill(int T, int E, int k, int quota, const int32_t* cand_off,
+                            const int32_t* cand_pair, int32_t* tokens_per_expert, uint8_t* map,
+                            cudaStream_t s);
 // E <= 8 without groups (and h small enough for the whole gate matrix in
 // shared memory): logits and top-k fused in one kernel
 bool router_fused_ok(int h, int E, int k, int num_groups);
@@ -104,9 +120,10 @@ cudaError_t launch_perm_copy_e4m3(int T, int h, int k, const void* x, const int3
                                   uint8_t* x_perm_q, float* row_scale, cudaStream_t s);
 // y_shared [T, h] fp32 (nullable): the shared expert's output, added last;
 // topk_prob nullable: unit weights (the backward's sum of dx rows)
+// rows of y_perm at or past max_rows (default T*k) count as dropped pairs
 cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
                            const int32_t* row_map, const float* topk_prob, const float* y_shared,
-                           void* y, cudaStream_t s);
+                           void* y, cudaStream_t s, int64_t max_rows = -1);
 
 // ---- grouped GEMMs ----
 // offsets == nullptr: one dense group (E must be 1) over rows [0, max_rows)

@@ -72,6 +72,7 @@ extern "C" moe_status moe_permute_noalloc(const moe_config* cfg, const void* x,
   const moe_status v = moe_workspace_size(cfg, &ws_unused);  // validates the configuration
   if (v != MOE_OK) return v;
   const moe_config& c = *cfg;
+  if (c.pad_to_capacity) return MOE_ERR_INVALID_ARG;  // padding rows come from the map
   const int64_t np = static_cast<int64_t>(c.num_tokens) * c.topk;
   const int64_t ntiles = perm_tiles(np);
   if (ntiles * c.num_experts > kScratchInts) return MOE_ERR_UNSUPPORTED;

@@ -18,6 +18,17 @@
 //                     write it to each of its kept rows
 //   perm_copy_e4m3_kernel  the same for E4M3 rows: the token's row is
 //                     quantised once (power-of-two scale) on the way
+// Permutation by a [T,E] routing map (the padded map of pad_to_capacity, §8:
+// the dispatcher permutes by the map, so an expert's rows are the tokens of
+// its column in ascending order, padding tokens among them):
+//   map_hist_kernel   per tile of 128 tokens: the map's ones per expert
+//   map_scan_kernel   one CTA: first row of each (tile, expert), the offsets
+//   map_rank_kernel   per tile: a thread per expert walks the tile's tokens
+//                     in order -> row_src of each row, row_map of the kept
+//                     pairs (-1 for the other slots)
+//   perm_gather_kernel  per row: x_perm[r] = x[row_src[r]]
+//   pad_fill_kernel   per (256-token chunk, expert): the lowest-index tokens
+//                     not routed to the expert fill its column up to the quota
 //
 // Combine, after §2 (combine) of the Megatron Core page and step 8 of §8 of
 // the DeepSpeed page (unpermute, weight by the router probabilities):
@@ -422,11 +433,10 @@ constexpr int kCombineThreads = 256;
 // (one row per token), four vectors per thread in flight.
 template <typename OT, int TPI_LOG2, bool K1>
 __global__ void __launch_bounds__(kCombineThreads)
-    combine_kernel(int T, int h, int k, const float* __restrict__ y_perm,
+    combine_kernel(int T, int h, int k, int64_t max_rows, const float* __restrict__ y_perm,
                    const int32_t* __restrict__ row_map, const float* __restrict__ topk_prob,
                    const float* __restrict__ y_shared, OT* __restrict__ y) {
   const int h4 = h >> 2;
-  const int64_t max_rows = static_cast<int64_t>(T) * k;
   constexpr int tpt = kCombineThreads >> TPI_LOG2;  // threads per token
   const int sub = threadIdx.x / tpt, lt = threadIdx.x % tpt;
   constexpr int tpi = 1 << TPI_LOG2;
@@ -500,15 +510,242 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
 }
 
+// ------------------------------------------------ permutation by a routing map
+constexpr int kMapTile = 128;  // tokens per tile
+
+// The tile's rows of the routing map [t0, t1) x E into shared memory (16-byte
+// copies when the map and E allow them); the caller synchronises.
+__device__ __forceinline__ void stage_map_tile(const uint8_t* __restrict__ map, int64_t t0,
+                                               int64_t t1, int E, uint8_t* tile) {
+  const int64_t n = (t1 - t0) * E;
+  const uint8_t* src = map + t0 * E;
+  if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 && (n & 15) == 0) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(tile);
+    for (int64_t i = threadIdx.x; i < n / 16; i += blockDim.x) d4[i] = s4[i];
+  } else {
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) tile[i] = src[i];
+  }
+}
+
+// per tile: the map's ones of each expert (thread e counts column e)
+__global__ void __launch_bounds__(kPermThreads)
+    map_hist_kernel(int T, int E, const uint8_t* __restrict__ map,
+                    int32_t* __restrict__ tile_counts) {
+  __shared__ __align__(16) uint8_t tile[kMapTile * MOE_MAX_EXPERTS];
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kMapTile;
+  const int64_t t1 = min(static_cast<int64_t>(T), t0 + kMapTile);
+  stage_map_tile(map, t0, t1, E, tile);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int64_t t = 0; t < t1 - t0; ++t) c += tile[t * E + e] != 0;
+    tile_counts[static_cast<int64_t>(blockIdx.x) * E + e] = c;
+  }
+}
+
+// tile_counts [ntiles][E]: counts in, first row of each (tile, expert) out;
+// offsets [E+1] out.  The map has many short tiles, so each expert's tiles
+// are split over G = 1024/E threads: chunk sums, an exclusive scan of the
+// chunks per expert and of the expert totals, then each thread rewrites its
+// chunk from its base (loads of a batch issued before its stores).
+constexpr int kMapScanThreads = 1024;
+constexpr int kMapScanBatch = 16;
+__global__ void __launch_bounds__(kMapScanThreads)
+    map_scan_kernel(int64_t ntiles, int E, int32_t* __restrict__ tile_counts,
+                    int32_t* __restrict__ offsets) {
+  __shared__ int part[kMapScanThreads];
+  __shared__ int start[MOE_MAX_EXPERTS + 1];
+  const int G = kMapScanThreads / E;
+  const int e = threadIdx.x % E, g = threadIdx.x / E;
+  const int64_t per = (ntiles + G - 1) / G;
+  const int64_t a = min(ntiles, static_cast<int64_t>(g) * per), b = min(ntiles, a + per);
+  const bool active = g < G;
+  int sum = 0;
+  if (active)
+    for (int64_t t = a; t < b; ++t) sum += tile_counts[t * E + e];
+  if (active) part[g * E + e] = sum;
+  __syncthreads();
+  if (threadIdx.x < E) {  // exclusive prefix of expert e's chunk sums
+    int run = 0;
+    for (int q = 0; q < G; ++q) {
+      const int v = part[q * E + threadIdx.x];
+      part[q * E + threadIdx.x] = run;
+      run += v;
+    }
+    start[threadIdx.x] = run;  // the total, scanned below
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {  // exclusive scan of E <= 256 totals
+    int run = 0;
+    for (int x = 0; x < E; ++x) {
+      const int v = start[x];
+      start[x] = run;
+      run += v;
+    }
+    start[E] = run;
+  }
+  __syncthreads();
+  for (int x = threadIdx.x; x <= E; x += blockDim.x) offsets[x] = start[x];
+  if (!active) return;
+  int base = start[e] + part[g * E + e];
+  for (int64_t t = a; t < b; t += kMapScanBatch) {
+    int c[kMapScanBatch];
+#pragma unroll
+    for (int u = 0; u < kMapScanBatch; ++u) c[u] = (t + u < b) ? tile_counts[(t + u) * E + e] : 0;
+#pragma unroll
+    for (int u = 0; u < kMapScanBatch; ++u)
+      if (t + u < b) {
+        tile_counts[(t + u) * E + e] = base;
+        base += c[u];
+      }
+  }
+}
+
+// Per tile: the map, topk_idx and keep of its tokens in shared memory.  Each
+// expert column is split over Q = blockDim/E threads (Q token ranges): every
+// thread counts its range, adds the counts of the ranges before it to the
+// tile's first row of the expert and walks its range in token order.  Rows
+// past max_rows (a map with more ones than the permuted buffers hold) are
+// reported and not written.
+__global__ void __launch_bounds__(kPermThreads)
+    map_rank_kernel(int T, int E, int k, int64_t max_rows, const uint8_t* __restrict__ map,
+                    const int32_t* __restrict__ topk_idx, const uint8_t* __restrict__ keep,
+                    const int32_t* __restrict__ tile_base, int32_t* __restrict__ row_map,
+                    int32_t* __restrict__ row_src, int* __restrict__ err) {
+  __shared__ __align__(16) uint8_t tile[kMapTile * MOE_MAX_EXPERTS];
+  __shared__ int32_t sidx[kMapTile * MOE_MAX_TOPK];
+  __shared__ uint8_t skeep[kMapTile * MOE_MAX_TOPK];
+  __shared__ int cnt[kPermThreads];
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kMapTile;
+  const int64_t t1 = min(static_cast<int64_t>(T), t0 + kMapTile);
+  stage_map_tile(map, t0, t1, E, tile);
+  const int64_t np = (t1 - t0) * k;
+  for (int64_t i = threadIdx.x; i < np; i += blockDim.x) {
+    sidx[i] = topk_idx[t0 * k + i];
+    skeep[i] = keep ? keep[t0 * k + i] : 1;
+    row_map[t0 * k + i] = -1;  // the kept pairs are overwritten below
+  }
+  __syncthreads();
+  const int Q = blockDim.x / E;  // >= 1 (E <= 256)
+  const int e = threadIdx.x % E, q = threadIdx.x / E;
+  const int n = static_cast<int>(t1 - t0);
+  const int len = (n + Q - 1) / Q;
+  const int u0 = min(n, q * len), u1 = min(n, u0 + len);
+  int c = 0;
+  if (q < Q)
+    for (int u = u0; u < u1; ++u) c += tile[u * E + e] != 0;
+  cnt[threadIdx.x] = c;
+  __syncthreads();
+  if (q >= Q) return;
+  int64_t row = tile_base[static_cast<int64_t>(blockIdx.x) * E + e];
+  for (int qq = 0; qq < q; ++qq) row += cnt[qq * E + e];
+  for (int u = u0; u < u1; ++u) {
+    if (!tile[u * E + e]) continue;
+    if (row >= max_rows) {
+      report_error(err, DEV_ERR_INDEX, static_cast<int>(t0 + u));
+      return;
+    }
+    row_src[row] = static_cast<int32_t>(t0 + u);
+    for (int j = 0; j < k; ++j)  // a token routes to an expert through one slot at most
+      if (sidx[u * k + j] == e && skeep[u * k + j])
+        row_map[(t0 + u) * k + j] = static_cast<int32_t>(row);
+    ++row;
+  }
+}
+
+// One warp per row (grid-stride): rows [0, min(offsets[E], max_rows)).
+__global__ void __launch_bounds__(kCopyThreads)
+    perm_gather_kernel(int64_t max_rows, int row_vecs, const int32_t* __restrict__ total_rows,
+                       const int32_t* __restrict__ row_src, const uint4* __restrict__ x,
+                       uint4* __restrict__ x_perm) {
+  const int64_t R = min(static_cast<int64_t>(*total_rows), max_rows);
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < R;
+       r += nwarps) {
+    const uint4* src = x + static_cast<int64_t>(row_src[r]) * row_vecs;
+    uint4* dst = x_perm + r * row_vecs;
+    for (int v = lane; v < row_vecs; v += 32) dst[v] = src[v];
+  }
+}
+
+constexpr int kPadChunk = 256;
+
+// First index i in [0, m) with cand_pair[begin + i] / k >= bound, by one warp:
+// each round the 32 lanes test 32 evenly spaced pivots, shrinking the range
+// 32-fold (a handful of dependent loads instead of log2(m)).
+__device__ __forceinline__ int warp_lower_bound(const int32_t* __restrict__ cand_pair, int begin,
+                                                int m, int k, int bound, int lane) {
+  int lo = 0, hi = m;  // the answer lies in [lo, hi]
+  while (hi - lo > 32) {
+    const int step = (hi - lo + 31) / 32;
+    const int pos = lo + lane * step;
+    const bool below = pos < hi && cand_pair[begin + pos] / k < bound;
+    const int c = __popc(__ballot_sync(0xffffffffu, below));  // pivots below: lanes 0 .. c-1
+    const int nlo = c == 0 ? lo : lo + (c - 1) * step + 1;
+    hi = min(hi, lo + c * step);
+    lo = nlo;
+  }
+  const int pos = lo + lane;
+  const bool below = pos < hi && cand_pair[begin + pos] / k < bound;
+  return lo + __popc(__ballot_sync(0xffffffffu, below));
+}
+
+// Expert blockIdx.y's column of the routing map, tokens [t0, t0 + 256): an
+// expert under capacity kept all of its m routed pairs (the candidate pairs
+// cand_pair[cand_off[e] ..], ascending), so it needs quota - m padding
+// tokens, the lowest-index tokens not routed to it.  A token's rank among
+// the free tokens is (t0 - the routed tokens below t0) plus the free tokens
+// before it in the chunk (a block scan).  Without candidate lists (capacity
+// >= T: nothing dropped) every token is taken.  tokens_per_expert becomes the
+// quota (the column sums of the padded map).
+__global__ void __launch_bounds__(kPadChunk)
+    pad_fill_kernel(int T, int E, int k, int quota, const int32_t* __restrict__ cand_off,
+                    const int32_t* __restrict__ cand_pair, int32_t* __restrict__ tokens_per_expert,
+                    uint8_t* __restrict__ map) {
+  __shared__ int s_lo, s_hi;
+  __shared__ uint8_t routed[kPadChunk];
+  __shared__ int warp_free[kPadChunk / 32];
+  const int e = blockIdx.y;
+  const int t0 = blockIdx.x * kPadChunk;
+  const int begin = cand_off ? cand_off[e] : 0;
+  const int m = cand_off ? cand_off[e + 1] - begin : 0;
+  const int need = quota - m;  // <= 0: at or over capacity, nothing to add
+  if (blockIdx.x == 0 && threadIdx.x == 0) tokens_per_expert[e] = quota;
+  if (need <= 0) return;
+  routed[threadIdx.x] = 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp < 2) {  // routed tokens below t0 (warp 0) and below t0 + 256 (warp 1)
+    const int v = warp_lower_bound(cand_pair, begin, m, k, t0 + warp * kPadChunk, lane);
+    if (lane == 0) {
+      if (warp) s_hi = v; else s_lo = v;
+    }
+  }
+  __syncthreads();
+  for (int i = s_lo + threadIdx.x; i < s_hi; i += blockDim.x)
+    routed[cand_pair[begin + i] / k - t0] = 1;
+  __syncthreads();
+  const int t = t0 + threadIdx.x;
+  const bool free_tok = t < T && !routed[threadIdx.x];
+  const unsigned ballot = __ballot_sync(0xffffffffu, free_tok);
+  if (lane == 0) warp_free[warp] = __popc(ballot);
+  __syncthreads();
+  int before = __popc(ballot & ((1u << lane) - 1u));
+  for (int w = 0; w < warp; ++w) before += warp_free[w];
+  if (free_tok && (t0 - s_lo) + before < need) map[static_cast<int64_t>(t) * E + e] = 1;
+}
+
 template <typename OT, bool K1>
-void launch_combine_t(int l, int grid, cudaStream_t s, int T, int h, int k, const float* y_perm,
+void launch_combine_t(int l, int grid, cudaStream_t s, int T, int h, int k, int64_t max_rows,
+                      const float* y_perm,
                       const int32_t* row_map, const float* topk_prob, const float* y_shared,
                       OT* y) {
   switch (l) {
-    case 0: combine_kernel<OT, 0, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
-    case 1: combine_kernel<OT, 1, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
-    case 2: combine_kernel<OT, 2, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
-    default: combine_kernel<OT, 3, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, y_perm, row_map, topk_prob, y_shared, y); break;
+    case 0: combine_kernel<OT, 0, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
+    case 1: combine_kernel<OT, 1, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
+    case 2: combine_kernel<OT, 2, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
+    default: combine_kernel<OT, 3, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
   }
 }
 
@@ -579,6 +816,44 @@ cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, cons
                           row_map, dst);
 }
 
+int64_t map_tiles(int T) { return (static_cast<int64_t>(T) + kMapTile - 1) / kMapTile; }
+
+cudaError_t launch_perm_by_map(int T, int h, int E, int k, int dtype, int64_t max_rows,
+                               const void* x, const uint8_t* map, const int32_t* topk_idx,
+                               const uint8_t* keep, int32_t* tile_counts, int32_t* row_src,
+                               void* x_perm, int32_t* row_map, int32_t* offsets, int* err,
+                               cudaStream_t s) {
+  const int64_t nt = map_tiles(T);
+  if (nt > 0) {
+    map_hist_kernel<<<static_cast<unsigned>(nt), kPermThreads, 0, s>>>(T, E, map, tile_counts);
+    cudaError_t st = cudaGetLastError();
+    if (st != cudaSuccess) return st;
+  }
+  map_scan_kernel<<<1, kMapScanThreads, 0, s>>>(nt, E, tile_counts, offsets);
+  cudaError_t st = cudaGetLastError();
+  if (st != cudaSuccess || nt == 0) return st;
+  map_rank_kernel<<<static_cast<unsigned>(nt), kPermThreads, 0, s>>>(
+      T, E, k, max_rows, map, topk_idx, keep, tile_counts, row_map, row_src, err);
+  st = cudaGetLastError();
+  if (st != cudaSuccess) return st;
+  const int row_vecs = h * (dtype == MOE_F32 ? 4 : 2) / 16;
+  perm_gather_kernel<<<device_sm_count() * 8, kCopyThreads, 0, s>>>(
+      max_rows, row_vecs, offsets + E, row_src, static_cast<const uint4*>(x),
+      static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_fill(int T, int E, int k, int quota, const int32_t* cand_off,
+                            const int32_t* cand_pair, int32_t* tokens_per_expert, uint8_t* map,
+                            cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((T + kPadChunk - 1) / kPadChunk > 0
+                                            ? (T + kPadChunk - 1) / kPadChunk : 1),
+                  static_cast<unsigned>(E));
+  pad_fill_kernel<<<grid, kPadChunk, 0, s>>>(T, E, k, quota, cand_off, cand_pair,
+                                             tokens_per_expert, map);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_perm_copy_e4m3(int T, int h, int k, const void* x, const int32_t* row_map,
                                   uint8_t* x_perm_q, float* row_scale, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
@@ -589,23 +864,24 @@ cudaError_t launch_perm_copy_e4m3(int T, int h, int k, const void* x, const int3
 
 cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
                            const int32_t* row_map, const float* topk_prob, const float* y_shared,
-                           void* y, cudaStream_t s) {
+                           void* y, cudaStream_t s, int64_t max_rows) {
   if (T == 0) return cudaSuccess;
+  if (max_rows < 0) max_rows = static_cast<int64_t>(T) * k;
   const int l = tokens_per_round_log2(h / 4, kCombineThreads, 4, 3);
   const int grid = grid_for_tokens((T + (1 << l) - 1) >> l, 8);
   if (dtype == MOE_F32) {
     if (k == 1)
-      launch_combine_t<float, true>(l, grid, s, T, h, k, y_perm, row_map, topk_prob, y_shared,
-                                    static_cast<float*>(y));
+      launch_combine_t<float, true>(l, grid, s, T, h, k, max_rows, y_perm, row_map, topk_prob,
+                                    y_shared, static_cast<float*>(y));
     else
-      launch_combine_t<float, false>(l, grid, s, T, h, k, y_perm, row_map, topk_prob, y_shared,
-                                     static_cast<float*>(y));
+      launch_combine_t<float, false>(l, grid, s, T, h, k, max_rows, y_perm, row_map, topk_prob,
+                                     y_shared, static_cast<float*>(y));
   } else if (k == 1) {
-    launch_combine_t<__nv_bfloat16, true>(l, grid, s, T, h, k, y_perm, row_map, topk_prob,
-                                          y_shared, static_cast<__nv_bfloat16*>(y));
+    launch_combine_t<__nv_bfloat16, true>(l, grid, s, T, h, k, max_rows, y_perm, row_map,
+                                          topk_prob, y_shared, static_cast<__nv_bfloat16*>(y));
   } else {
-    launch_combine_t<__nv_bfloat16, false>(l, grid, s, T, h, k, y_perm, row_map, topk_prob,
-                                           y_shared, static_cast<__nv_bfloat16*>(y));
+    launch_combine_t<__nv_bfloat16, false>(l, grid, s, T, h, k, max_rows, y_perm, row_map,
+                                           topk_prob, y_shared, static_cast<__nv_bfloat16*>(y));
   }
   return cudaGetLastError();
 }

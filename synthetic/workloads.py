@@ -52,6 +52,7 @@ class Workload:
     shared_f: int = 0              # > 0: a shared expert of this SwiGLU width
     num_groups: int = 0            # > 1: group-limited top-k over this many expert groups
     group_topk: int = 0            # groups kept per token when num_groups > 1
+    pad_to_capacity: bool = False  # every expert padded to its capacity (needs a capacity factor)
     description: str = ""
 
     @property
@@ -100,6 +101,10 @@ WORKLOADS["dsv3_grouped"] = replace(
     WORKLOADS["dsv3"], name="dsv3_grouped", num_groups=8, group_topk=4,
     description="dsv3 with group-limited routing: 8 expert groups of 32, the 4 best groups "
                 "(group score = sum of its top-2 selection scores) kept per token")
+WORKLOADS["switch_pad"] = replace(
+    WORKLOADS["switch"], name="switch_pad", pad_to_capacity=True,
+    description="switch with pad_to_capacity: every expert's input padded to its capacity "
+                "(640 rows; 40960 rows in all) with tokens of probability 0")
 WORKLOADS["dsv3_shared"] = replace(
     WORKLOADS["dsv3"], name="dsv3_shared", shared_f=2048,
     description="dsv3 plus one shared SwiGLU expert (width 2048) applied to every token and "

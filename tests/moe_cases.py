@@ -89,7 +89,8 @@ def condition_inputs(w, inp, max_rounds=64, nthreads=0):
         raise RuntimeError("margin conditioning did not converge")
     x.copy_(x_cpu.to(x.device))
     r = oracle.route(np_view(x_cpu), Wg, w.k, w.score, gb, eb, w.capacity_factor,
-                     w.min_capacity, w.drop_policy, nthreads, *groups)
+                     w.min_capacity, w.drop_policy, nthreads, *groups,
+                     pad_to_capacity=w.pad_to_capacity)
     assert np.all(r["margin"] >= MARGIN)
     return r
 
@@ -109,13 +110,14 @@ def oracle_forward(w, inp, nthreads=0, want_h_mid=True):
                           np_view(inp["gate_bias"]), np_view(inp["expert_bias"]),
                           w.capacity_factor, w.min_capacity, w.drop_policy, nthreads,
                           want_h_mid=want_h_mid, num_groups=w.num_groups,
-                          group_topk=w.group_topk, **shared)
+                          group_topk=w.group_topk, pad_to_capacity=w.pad_to_capacity, **shared)
 
 
 def gpu_config(w):
     import mixture_experts_layer_fp32_gb300 as moe
     return moe.config(w.T, w.h, w.E, w.k, w.f, w.score, w.dtype, w.capacity_factor,
-                      w.min_capacity, w.drop_policy, w.num_groups, w.group_topk)
+                      w.min_capacity, w.drop_policy, w.num_groups, w.group_topk,
+                      w.pad_to_capacity)
 
 
 def to_dev(inp, device="cuda"):
@@ -129,8 +131,13 @@ def gpu_stages(w, dinp, with_routing_map=True):
     b = moe.Buffers(cfg)
     moe.route(cfg, dinp["x"], dinp["Wg"], dinp["gate_bias"], dinp["expert_bias"], b.topk_idx,
               b.topk_prob, b.keep, b.tokens_per_expert,
-              b.routing_map if with_routing_map else None, b.ws)
-    moe.permute(cfg, dinp["x"], b.topk_idx, b.keep, b.x_perm, b.row_map, b.expert_offsets, b.ws)
+              b.routing_map if (with_routing_map or w.pad_to_capacity) else None, b.ws)
+    if w.pad_to_capacity:  # the padded routing map drives the permutation
+        moe.permute_map(cfg, dinp["x"], b.routing_map, b.topk_idx, b.keep, b.x_perm, b.row_map,
+                        b.expert_offsets, b.ws)
+    else:
+        moe.permute(cfg, dinp["x"], b.topk_idx, b.keep, b.x_perm, b.row_map, b.expert_offsets,
+                    b.ws)
     moe.grouped_fc1(cfg, b.x_perm, b.expert_offsets, dinp["W1"], dinp["W3"], b.h_mid, b.ws)
     moe.grouped_fc2(cfg, b.h_mid, b.expert_offsets, dinp["W2"], b.y_perm, b.ws)
     if w.shared_f > 0:

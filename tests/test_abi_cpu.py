@@ -41,7 +41,7 @@ def test_library_exports_every_declared_function(moe):
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
     assert sorted(moe.EXPORTS) == declared_functions()
-    assert moe.lib().moe_abi_version() == 2
+    assert moe.lib().moe_abi_version() == 3
     assert moe.lib().moe_status_string(3) == b"MOE_ERR_WORKSPACE"
 
 
@@ -268,3 +268,43 @@ def test_binding_signatures_match_header(moe):
     lib = moe.lib()
     for name in moe.EXPORTS:
         assert len(getattr(lib, name).argtypes) == counts[name], name
+
+
+def test_pad_to_capacity_configuration(moe):
+    size = ctypes.c_size_t()
+    lib = moe.lib()
+    # needs a capacity factor, and is 0 or 1
+    cfg = moe.config(T=64, h=4096, E=8, k=2, f=1536, pad_to_capacity=True)
+    assert _status(moe, "moe_workspace_size", _cfgp(cfg), ctypes.byref(size)) == INVALID
+    cfg = moe.config(T=64, h=4096, E=8, k=2, f=1536, capacity_factor=1.0)
+    cfg.pad_to_capacity = 2
+    assert _status(moe, "moe_workspace_size", _cfgp(cfg), ctypes.byref(size)) == INVALID
+    # the permuted buffers hold E * min(capacity, T) rows when that is more than T*k
+    sw = dict(T=32768, h=1024, E=64, k=1, f=4096, score="softmax_pre", capacity_factor=1.25)
+    assert moe.max_rows(moe.config(**sw, pad_to_capacity=True)) == 64 * 640
+    assert moe.max_rows(moe.config(**sw)) == 32768
+    assert moe.workspace_size(moe.config(**sw, pad_to_capacity=True)) > \
+        moe.workspace_size(moe.config(**sw))
+    assert moe.max_rows(moe.config(T=100, h=256, E=8, k=2, f=128, capacity_factor=20.0,
+                                   pad_to_capacity=True)) == 8 * 100
+    assert moe.max_rows(moe.config(T=1000, h=256, E=8, k=2, f=128, capacity_factor=0.5,
+                                   pad_to_capacity=True)) == 2000
+    # the E4M3 and backward paths are not built for it
+    cfg = moe.config(T=128, h=4096, E=8, k=2, f=1536, capacity_factor=1.0, pad_to_capacity=True)
+    assert _status(moe, "moe_workspace_size_e4m3", _cfgp(cfg), ctypes.byref(size)) == UNSUPPORTED
+    assert _status(moe, "moe_workspace_size_backward", _cfgp(cfg), ctypes.byref(size)) == \
+        UNSUPPORTED
+    need = moe.workspace_size(cfg)
+    # the pair permutation cannot place padding rows; the route must return the map
+    assert lib.moe_permute(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need,
+                           None) == INVALID
+    assert lib.moe_permute_noalloc(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                   None) == INVALID
+    assert lib.moe_route(*_route_args(cfg, need, rm=None)) == INVALID
+    # moe_permute_map checks its map and buffers like the other stages
+    assert lib.moe_permute_map(ctypes.byref(cfg), FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               need, None) == INVALID
+    assert lib.moe_permute_map(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, MISALIGNED, FAKE,
+                               FAKE, FAKE, need, None) == INVALID
+    assert lib.moe_permute_map(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               need - 1, None) == WORKSPACE

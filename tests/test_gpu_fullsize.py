@@ -22,7 +22,7 @@ from moe_cases import (assert_close, assert_equal, assert_probs, condition_input
 pytestmark = pytest.mark.gpu
 
 MAX_EXPERTS = {"tiny_fp32": 8, "mixtral": 8, "dsv3": 48, "dsv3_grouped": 48, "dsv3_shared": 48,
-               "qwen3": 48, "switch": 32}
+               "qwen3": 48, "switch": 32, "switch_pad": 32}
 MAX_TOKENS = 32
 
 
@@ -51,7 +51,12 @@ def test_routing_full(full):
 
 def test_permutation_full(full):
     w, inp, r, b = full
-    offsets, row_map, row_token = oracle.permute(r["topk_idx"], r["keep"], w.E)
+    if w.pad_to_capacity:  # the permutation of the padded routing map
+        assert_equal("routing_map", to_np(b.routing_map), r["routing_map"])
+        offsets, row_map, row_token = oracle.permute_map(r["routing_map"], r["topk_idx"],
+                                                         r["keep"])
+    else:
+        offsets, row_map, row_token = oracle.permute(r["topk_idx"], r["keep"], w.E)
     assert_equal("expert_offsets", to_np(b.expert_offsets), offsets)
     assert_equal("row_map", to_np(b.row_map), row_map)
     R = int(offsets[-1])

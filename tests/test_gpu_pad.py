@@ -1,0 +1,103 @@
+"""pad_to_capacity on the GPU against the oracle (apply_router_token_dropping
+with pad_to_capacity, §8 of the Megatron Core page, and the dispatcher's
+permutation by the padded routing map, §9).
+
+Every expert's input holds exactly min(capacity, T) rows: its kept pairs and,
+under capacity, the lowest-index tokens not routed to it, in token order.
+Checked bit for bit: the padded routing map, tokens_per_expert, the expert
+offsets, row_map and every permuted row; h_mid, y_perm (padding rows
+included) and y within the parity tolerances.  Padding rows carry no combine
+weight, so the layer output equals the unpadded layer's bit for bit (each
+output row of the grouped GEMM depends on its own row only).  Also: the
+padded moe_forward reproduces the staged calls, and moe_permute_map on an
+unpadded routing map gives moe_permute's result.
+"""
+
+import pytest
+import torch
+
+import synthetic
+from moe_cases import (assert_equal, compare_all, gpu_config, gpu_forward, gpu_stages,
+                       make_case, oracle_forward, to_dev, to_np)
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # Switch-like top-1: 4 hot experts dropped to capacity, the rest padded
+    "switch_probs": synthetic.scaled("switch", T=4096, h=256, f=256, seed=14,
+                                     pad_to_capacity=True),
+    "switch_position": synthetic.scaled("switch", T=2048, h=256, f=256, seed=15,
+                                        drop_policy="position", pad_to_capacity=True),
+    # top-2 of 8 with two hot experts: drops and padding in one layer
+    "top2_hot": synthetic.scaled("mixtral", T=700, h=256, f=256, capacity_factor=1.0,
+                                 gate_bias="hot:2:2.5", seed=71, pad_to_capacity=True),
+    # capacity above T: every token goes to every expert
+    "capacity_above_tokens": synthetic.scaled("mixtral", T=300, h=256, f=128,
+                                              capacity_factor=20.0, seed=72,
+                                              pad_to_capacity=True),
+    # fp32 experts (SIMT GEMM)
+    "tiny_fp32": synthetic.scaled("tiny_fp32", T=500, capacity_factor=1.1, seed=73,
+                                  pad_to_capacity=True),
+}
+
+
+@pytest.fixture(scope="module", params=sorted(CASES))
+def case(request):
+    w = CASES[request.param]
+    inp, r = make_case(w)
+    ref = oracle_forward(w, inp)
+    dinp = to_dev(inp)
+    b = gpu_stages(w, dinp)
+    torch.cuda.synchronize()
+    return w, inp, ref, dinp, b
+
+
+def test_padded_layer_matches_oracle(case):
+    w, inp, ref, dinp, b = case
+    assert_equal("routing_map", to_np(b.routing_map), ref["routing_map"])
+    compare_all(w, inp, ref, b)
+    q = min(ref["capacity"], w.T)
+    assert (to_np(b.tokens_per_expert) == q).all()
+    assert int(ref["offsets"][-1]) == w.E * q
+
+
+def test_padding_never_reaches_the_output(case):
+    w, inp, ref, dinp, b = case
+    from dataclasses import replace
+    u = gpu_stages(replace(w, pad_to_capacity=False), dinp)
+    torch.cuda.synchronize()
+    for n in ("topk_idx", "topk_prob", "keep"):
+        assert torch.equal(getattr(u, n), getattr(b, n)), n
+    assert torch.equal(u.y, b.y)
+
+
+def test_padded_forward_reproduces_stages(case):
+    w, inp, ref, dinp, b = case
+    y, idx, prob, tpe = gpu_forward(w, dinp)
+    assert torch.equal(idx, b.topk_idx)
+    assert torch.equal(prob, b.topk_prob)
+    assert torch.equal(tpe, b.tokens_per_expert)
+    assert torch.equal(y, b.y)
+
+
+@pytest.mark.parametrize("name,w", [
+    ("mixtral", synthetic.scaled("mixtral", T=600, h=512, f=384, seed=11)),
+    ("switch_drop", synthetic.scaled("switch", T=4096, h=256, f=256, seed=14)),
+    ("qwen3", synthetic.scaled("qwen3", T=1024, h=512, f=384, seed=13)),
+])
+def test_permute_map_equals_permute_without_padding(name, w):
+    import mixture_experts_layer_fp32_gb300 as moe
+    inp, _ = make_case(w)
+    dinp = to_dev(inp)
+    b = gpu_stages(w, dinp)  # moe_route with the routing map, moe_permute
+    cfg = gpu_config(w)
+    x_perm = torch.empty_like(b.x_perm)
+    row_map = torch.empty_like(b.row_map)
+    offsets = torch.empty_like(b.expert_offsets)
+    moe.permute_map(cfg, dinp["x"], b.routing_map, b.topk_idx, b.keep, x_perm, row_map, offsets,
+                    b.ws)
+    moe.check(b.ws)
+    R = int(b.expert_offsets[-1])
+    assert torch.equal(offsets, b.expert_offsets)
+    assert torch.equal(row_map, b.row_map)
+    assert torch.equal(x_perm[:R], b.x_perm[:R])
