@@ -527,11 +527,11 @@ def fp32_fma_rate(moe, dev, stream, iters=4096, reps=5):
 
 def run_backward(args, moe, w, cfg, inp, b, R, flush, stream, world, rank, local):
     """Time moe_backward (the saved buffers of one staged forward, a seeded dy)."""
-    if w.dtype != "bf16" or args.precision != "bf16":
-        raise SystemExit("--pass backward needs a bf16 workload and --precision bf16")
+    if args.precision != "bf16" or w.pad_to_capacity:
+        raise SystemExit("--pass backward needs --precision bf16 and no pad_to_capacity")
     dev = b.y.device
     g = torch.Generator(device="cpu").manual_seed(w.seed + 7)
-    dy = torch.randn((w.T, w.h), generator=g).to(torch.bfloat16).to(dev)
+    dy = torch.randn((w.T, w.h), generator=g).to(moe.act_dtype(cfg)).to(dev)
     grads = moe.Grads(cfg, dev)
     fs = w.shared_f
     if fs > 0:
@@ -573,6 +573,8 @@ def run_backward(args, moe, w, cfg, inp, b, R, flush, stream, world, rank, local
     if rank != 0:
         return None
     peaks = measured_peaks()
+    if w.dtype != "bf16":  # the fp32 backward runs on the FMA units: their rate, measured now
+        peaks["fp32_fma_tflops"] = fp32_fma_rate(moe, dev, stream)
     # expert GEMMs of the backward: fc2 dgrad 2Rfh, fc1 recompute 4Rhf, fc1
     # dgrad 4Rhf, wgrad 2Rfh + 4Rhf; the shared expert the same over T rows
     gemm_flops = 16 * R * w.h * w.f + 16 * w.T * w.h * fs
@@ -585,10 +587,17 @@ def run_backward(args, moe, w, cfg, inp, b, R, flush, stream, world, rank, local
         "config": dict(workload_desc(w), parallelism="replicas" if world > 1 else "single",
                        precision=args.precision, pass_="backward"),
         "rows": R,
-        "roofline": {"kernel": "whole backward (expert GEMM flops / backward time)",
-                     "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                     "traffic": None, "algorithmic_per_launch": gemm_flops},
+        "roofline": ({"kernel": "whole backward (expert GEMM flops / backward time)",
+                      "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                      "traffic": None, "algorithmic_per_launch": gemm_flops}
+                     if w.dtype == "bf16" else
+                     {"kernel": "whole backward (expert GEMM flops / backward time), FMA units",
+                      "bound": "alu", "achieved": achieved,
+                      "peak": peaks.get("fp32_fma_tflops"), "unit": "TFLOP/s",
+                      "frac": achieved / peaks["fp32_fma_tflops"]
+                      if peaks.get("fp32_fma_tflops") else None,
+                      "traffic": None, "algorithmic_per_launch": gemm_flops}),
         "e2e": None,
         "gpu_launches": backward_launches(w) * args.steps,
         "clocks": clk,
@@ -603,7 +612,7 @@ def backward_launches(w):
     fold, dgate_bias, the dx GEMM; else dWg (+ its split reduction), dgate_bias,
     dx), three dgrad/recompute GEMMs, the token-gradient combine, three
     wgrad GEMMs."""
-    if w.E >= 64 and w.E % 64 == 0:
+    if w.dtype == "bf16" and w.E >= 64 and w.E % 64 == 0:
         router = 6
     else:
         sms = torch.cuda.get_device_properties(0).multi_processor_count

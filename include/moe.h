@@ -356,15 +356,16 @@ moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* W
  * recomputed by fc1), dX = [da|dg] [W1;W3]^T, dW2 = H^T dY, dW1 = X^T da,
  * dW3 = X^T dg; the router gets dlogits from dp through the score function,
  * dWg = x^T dlogits, dgate_bias = sum_t dlogits, and dx gains dlogits Wg^T.
- * bf16 only (MOE_ERR_UNSUPPORTED for MOE_F32): the expert GEMMs run on the
- * tensor cores (dgrad with the weights read in place, wgrad reducing over
- * each expert's rows); dY, dH, da and dg are rounded to bf16 as GEMM
- * operands; accumulation is fp32.
+ * bf16: the expert GEMMs run on the tensor cores (dgrad with the weights
+ * read in place, wgrad reducing over each expert's rows); dY, dH, da and dg
+ * are rounded to bf16 as GEMM operands; accumulation is fp32.  MOE_F32: the
+ * same GEMMs on the FMA units, every intermediate fp32.  pad_to_capacity:
+ * MOE_ERR_UNSUPPORTED.
  *   Saved from the forward (the staged calls' outputs): topk_idx and
  *   topk_prob [T,k] (moe_route), row_map [T,k], expert_offsets [E+1] and
  *   x_perm [T*k,h] (moe_permute), h_mid [T*k,f] and y_perm [T*k,h] fp32
  *   (moe_grouped_mlp).  Parameters as in moe_forward.
- *   dy [T,h] bf16 in; dx [T,h] bf16 out; dWg [h,E], dgate_bias [E]
+ *   dy [T,h] dtype in; dx [T,h] dtype out; dWg [h,E], dgate_bias [E]
  *   (nullable), dW1/dW3 [E,h,f], dW2 [E,f,h] fp32 out (overwritten).
  *   ws: moe_workspace_size_backward bytes (zero-filled once).
  */
@@ -384,8 +385,8 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* Wg,
  * dx_s = [da_s | dg_s] [W1s ; W3s]^T before its one rounding.  The shared
  * expert is the routed formula for one expert of weight 1 over every token:
  * dH_s = dy W2s^T, a_s and g_s recomputed, dW2s = H_s^T dy, dW1s = x^T da_s,
- * dW3s = x^T dg_s.  bf16 only; fs as in moe_shared_expert.
- *   Extra inputs: W1s, W3s [h,fs], W2s [fs,h] bf16 and h_mid_s [T,fs] (saved by
+ * dW3s = x^T dg_s.  bf16 or fp32 as moe_backward; fs as in moe_shared_expert.
+ *   Extra inputs: W1s, W3s [h,fs], W2s [fs,h] dtype and h_mid_s [T,fs] (saved by
  *   moe_shared_expert).  Extra outputs: dW1s, dW3s [h,fs], dW2s [fs,h] fp32
  *   (overwritten).
  *   ws: moe_workspace_size_backward_shared bytes.

@@ -33,11 +33,51 @@ namespace {
 
 constexpr int kBwdThreads = 128;
 
-// dy [T,h] bf16, y_perm [rows,h] fp32 -> dY_perm [rows,h] bf16, dp [T,k] fp32
+// 8 consecutive activations (bf16 or fp32) of a row as floats: vector v
+// covers elements 8v .. 8v+7
+template <typename AT>
+struct Act8;
+template <>
+struct Act8<__nv_bfloat16> {
+  __device__ static void load(const __nv_bfloat16* row, int v, float (&d)[8]) {
+    const uint4 u = reinterpret_cast<const uint4*>(row)[v];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      d[2 * i] = __uint_as_float(w[i] << 16);
+      d[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ static void store(__nv_bfloat16* row, int v, const float (&o)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    reinterpret_cast<uint4*>(row)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+template <>
+struct Act8<float> {
+  __device__ static void load(const float* row, int v, float (&d)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(row)[2 * v];
+    const float4 b = reinterpret_cast<const float4*>(row)[2 * v + 1];
+    d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w;
+    d[4] = b.x; d[5] = b.y; d[6] = b.z; d[7] = b.w;
+  }
+  __device__ static void store(float* row, int v, const float (&o)[8]) {
+    reinterpret_cast<float4*>(row)[2 * v] = make_float4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<float4*>(row)[2 * v + 1] = make_float4(o[4], o[5], o[6], o[7]);
+  }
+};
+
+// dy [T,h] (AT), y_perm [rows,h] fp32 -> dY_perm [rows,h] (AT), dp [T,k] fp32
+template <typename AT>
 __global__ void __launch_bounds__(kBwdThreads)
-    combine_bwd_kernel(int T, int h, int k, const __nv_bfloat16* __restrict__ dy,
+    combine_bwd_kernel(int T, int h, int k, const AT* __restrict__ dy,
                        const int32_t* __restrict__ row_map, const float* __restrict__ topk_prob,
-                       const float* __restrict__ y_perm, __nv_bfloat16* __restrict__ dY_perm,
+                       const float* __restrict__ y_perm, AT* __restrict__ dY_perm,
                        float* __restrict__ dp) {
   __shared__ float red[kBwdThreads / 32][MOE_MAX_TOPK];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -51,16 +91,9 @@ __global__ void __launch_bounds__(kBwdThreads)
       p[j] = rows[j] >= 0 ? topk_prob[(int64_t)t * k + j] : 0.f;
       dot[j] = 0.f;
     }
-    const uint4* src = reinterpret_cast<const uint4*>(dy + (int64_t)t * h);
     for (int v = threadIdx.x; v < h8; v += kBwdThreads) {
-      const uint4 u = src[v];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
       float d[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        d[2 * i] = __uint_as_float(w[i] << 16);
-        d[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-      }
+      Act8<AT>::load(dy + (int64_t)t * h, v, d);
 #pragma unroll
       for (int j = 0; j < MOE_MAX_TOPK; ++j) {
         if (rows[j] < 0) continue;
@@ -68,13 +101,10 @@ __global__ void __launch_bounds__(kBwdThreads)
         const float4 y0 = yp[0], y1 = yp[1];
         dot[j] += d[0] * y0.x + d[1] * y0.y + d[2] * y0.z + d[3] * y0.w + d[4] * y1.x +
                   d[5] * y1.y + d[6] * y1.z + d[7] * y1.w;
-        uint32_t o[4];
+        float o[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          __nv_bfloat162 b = __floats2bfloat162_rn(p[j] * d[2 * i], p[j] * d[2 * i + 1]);
-          o[i] = *reinterpret_cast<uint32_t*>(&b);
-        }
-        reinterpret_cast<uint4*>(dY_perm + (int64_t)rows[j] * h)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int i = 0; i < 8; ++i) o[i] = p[j] * d[i];
+        Act8<AT>::store(dY_perm + (int64_t)rows[j] * h, v, o);
       }
     }
 #pragma unroll
@@ -232,8 +262,9 @@ __global__ void __launch_bounds__(256)
 // 256 threads, 4 x 4 outputs each.  gridDim.z splits the tokens: split z
 // covers tokens [z * tps, (z+1) * tps) and writes its own partial sums
 // (out + z * h * E), which dwg_reduce_kernel adds in split order.
+template <typename XT>
 __global__ void __launch_bounds__(256)
-    dwg_kernel(int T, int h, int E, int tps, const __nv_bfloat16* __restrict__ x,
+    dwg_kernel(int T, int h, int E, int tps, const XT* __restrict__ x,
                const float* __restrict__ dl, float* __restrict__ out) {
   __shared__ float xs[32][64 + 4];
   __shared__ float ls[32][64 + 4];
@@ -246,7 +277,7 @@ __global__ void __launch_bounds__(256)
     for (int v = threadIdx.x; v < 32 * 64; v += 256) {
       const int tt = v >> 6, c = v & 63;
       const int t = t0 + tt;
-      xs[tt][c] = (t < tend && i0 + c < h) ? __bfloat162float(x[(int64_t)t * h + i0 + c]) : 0.f;
+      xs[tt][c] = (t < tend && i0 + c < h) ? static_cast<float>(x[(int64_t)t * h + i0 + c]) : 0.f;
       ls[tt][c] = (t < tend && e0 + c < E) ? dl[(int64_t)t * E + e0 + c] : 0.f;
     }
     __syncthreads();
@@ -278,10 +309,25 @@ __global__ void __launch_bounds__(256)
 // the two rows); tokens of split z are [z * tps, (z+1) * tps), their dl rows
 // staged 64 at a time in shared memory.  Each split writes its partial sums
 // to out + z * h * E (added in split order by dwg_reduce_kernel).
-template <int EC>
+// x as pairs of consecutive features: bf16x2 or float2, widened to float2
+template <typename XT>
+struct XPair;
+template <>
+struct XPair<__nv_bfloat16> {
+  using P = __nv_bfloat162;
+  __device__ static float2 get(P v) { return __bfloat1622float2(v); }
+};
+template <>
+struct XPair<float> {
+  using P = float2;
+  __device__ static float2 get(P v) { return v; }
+};
+
+template <int EC, typename XT>
 __global__ void __launch_bounds__(256)
-    dwg_small_kernel(int T, int h, int E, int tps, const __nv_bfloat16* __restrict__ x,
+    dwg_small_kernel(int T, int h, int E, int tps, const XT* __restrict__ x,
                      const float* __restrict__ dl, float* __restrict__ out) {
+  using P = typename XPair<XT>::P;
   constexpr int TCH = 64;
   __shared__ __align__(16) float ls[TCH][EC];
   const int i = (blockIdx.x * 256 + threadIdx.x) * 2;
@@ -289,8 +335,8 @@ __global__ void __launch_bounds__(256)
   float2 acc[EC];
 #pragma unroll
   for (int e = 0; e < EC; ++e) acc[e] = make_float2(0.f, 0.f);
-  const __nv_bfloat162* xr = reinterpret_cast<const __nv_bfloat162*>(x + i);
-  const int64_t step = h / 2;  // bf16 pairs per token row
+  const P* xr = reinterpret_cast<const P*>(x + i);
+  const int64_t step = h / 2;  // pairs per token row
   for (int t0 = tbeg; t0 < tend; t0 += TCH) {
     const int n = min(TCH, tend - t0);
     for (int v = threadIdx.x; v < TCH * EC; v += 256) {
@@ -299,12 +345,12 @@ __global__ void __launch_bounds__(256)
     }
     __syncthreads();
     if (i < h) {
-      const __nv_bfloat162* xp = xr + static_cast<int64_t>(t0) * step;
+      const P* xp = xr + static_cast<int64_t>(t0) * step;
       int tt = 0;
       for (; tt + 8 <= n; tt += 8) {
         float2 xv[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) xv[u] = __bfloat1622float2(xp[static_cast<int64_t>(tt + u) * step]);
+        for (int u = 0; u < 8; ++u) xv[u] = XPair<XT>::get(xp[static_cast<int64_t>(tt + u) * step]);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const float4* lr = reinterpret_cast<const float4*>(ls[tt + u]);
@@ -319,7 +365,7 @@ __global__ void __launch_bounds__(256)
         }
       }
       for (; tt < n; ++tt) {
-        const float2 xv = __bfloat1622float2(xp[static_cast<int64_t>(tt) * step]);
+        const float2 xv = XPair<XT>::get(xp[static_cast<int64_t>(tt) * step]);
 #pragma unroll
         for (int e = 0; e < EC; ++e) acc[e] = __ffma2_rn(xv, make_float2(ls[tt][e], ls[tt][e]), acc[e]);
       }
@@ -507,14 +553,20 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_combine_bwd(int T, int h, int k, const void* dy, const int32_t* row_map,
-                               const float* topk_prob, const float* y_perm, void* dY_perm,
-                               float* dp, cudaStream_t s) {
+cudaError_t launch_combine_bwd(int T, int h, int k, int dtype, const void* dy,
+                               const int32_t* row_map, const float* topk_prob,
+                               const float* y_perm, void* dY_perm, float* dp, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int cap = device_sm_count() * 16;
-  combine_bwd_kernel<<<T < cap ? T : cap, kBwdThreads, 0, s>>>(
-      T, h, k, static_cast<const __nv_bfloat16*>(dy), row_map, topk_prob, y_perm,
-      static_cast<__nv_bfloat16*>(dY_perm), dp);
+  const int grid = T < cap ? T : cap;
+  if (dtype == MOE_F32)
+    combine_bwd_kernel<float><<<grid, kBwdThreads, 0, s>>>(
+        T, h, k, static_cast<const float*>(dy), row_map, topk_prob, y_perm,
+        static_cast<float*>(dY_perm), dp);
+  else
+    combine_bwd_kernel<__nv_bfloat16><<<grid, kBwdThreads, 0, s>>>(
+        T, h, k, static_cast<const __nv_bfloat16*>(dy), row_map, topk_prob, y_perm,
+        static_cast<__nv_bfloat16*>(dY_perm), dp);
   return cudaGetLastError();
 }
 
@@ -544,21 +596,30 @@ int dwg_splits(int T, int h, int E) {
   return S < 1 ? 1 : static_cast<int>(S);
 }
 
-cudaError_t launch_router_param_grads(int T, int h, int E, const void* x, const float* dl,
-                                      float* dWg, float* part, float* dgb, cudaStream_t s) {
-  const int S = dwg_splits(T, h, E);
-  const int tps = S > 1 ? (T + S - 1) / S : (T > 0 ? T : 1);
-  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  float* dst = S > 1 ? part : dWg;
+template <typename XT>
+void launch_dwg(int T, int h, int E, int S, int tps, const XT* x, const float* dl, float* dst,
+                cudaStream_t s) {
   const dim3 small_grid((h + 511) / 512, 1, S);
   if (E <= 8)
-    dwg_small_kernel<8><<<small_grid, 256, 0, s>>>(T, h, E, tps, xb, dl, dst);
+    dwg_small_kernel<8, XT><<<small_grid, 256, 0, s>>>(T, h, E, tps, x, dl, dst);
   else if (E <= 16)
-    dwg_small_kernel<16><<<small_grid, 256, 0, s>>>(T, h, E, tps, xb, dl, dst);
+    dwg_small_kernel<16, XT><<<small_grid, 256, 0, s>>>(T, h, E, tps, x, dl, dst);
   else if (E <= 32)
-    dwg_small_kernel<32><<<small_grid, 256, 0, s>>>(T, h, E, tps, xb, dl, dst);
+    dwg_small_kernel<32, XT><<<small_grid, 256, 0, s>>>(T, h, E, tps, x, dl, dst);
   else
-    dwg_kernel<<<dim3((h + 63) / 64, (E + 63) / 64, S), 256, 0, s>>>(T, h, E, tps, xb, dl, dst);
+    dwg_kernel<XT><<<dim3((h + 63) / 64, (E + 63) / 64, S), 256, 0, s>>>(T, h, E, tps, x, dl, dst);
+}
+
+cudaError_t launch_router_param_grads(int T, int h, int E, int dtype, const void* x,
+                                      const float* dl, float* dWg, float* part, float* dgb,
+                                      cudaStream_t s) {
+  const int S = dwg_splits(T, h, E);
+  const int tps = S > 1 ? (T + S - 1) / S : (T > 0 ? T : 1);
+  float* dst = S > 1 ? part : dWg;
+  if (dtype == MOE_F32)
+    launch_dwg(T, h, E, S, tps, static_cast<const float*>(x), dl, dst, s);
+  else
+    launch_dwg(T, h, E, S, tps, static_cast<const __nv_bfloat16*>(x), dl, dst, s);
   cudaError_t st = cudaGetLastError();
   if (st != cudaSuccess) return st;
   if (S > 1) {

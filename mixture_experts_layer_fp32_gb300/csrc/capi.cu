@@ -450,6 +450,54 @@ moe_status do_mlp_e4m3(const moe_config& c, const uint8_t* xperm_q, const float*
 // dA = [da | dg] [T*k,2f] bf16, dx_perm [T*k,h] fp32.
 // moe_backward's workspace; with a shared expert of width fs (> 0), its dH_s
 // [T,fs] and dA_s [T,2fs] (bf16) follow.
+// The router's gradients on the tensor cores (hi/lo bf16 splits) for bf16
+// layers with E % 64 == 0; otherwise (and for fp32) on the FMA units.
+bool bwd_router_on_tc(const moe_config& c) {
+  return c.dtype == MOE_BF16 && router_grads_on_tc(c.num_experts);
+}
+
+// The backward's expert GEMMs for the configuration's dtype: the tcgen05
+// kernels for bf16, the SIMT kernels for fp32 (offsets NULL: one dense group).
+cudaError_t bwd_dgrad_fc2(const moe_config& c, int E, int f, int64_t rows, const void* dY,
+                          const int32_t* off, const void* W2, void* dH, int* err, cudaStream_t s) {
+  if (c.dtype == MOE_F32)
+    return launch_simt_dgrad_fc2(E, c.hidden, f, rows, static_cast<const float*>(dY), off,
+                                 static_cast<const float*>(W2), static_cast<float*>(dH), err, s);
+  return launch_tc_dgrad_fc2(E, c.hidden, f, rows, dY, off, W2, dH, err, s);
+}
+cudaError_t bwd_fc1_recompute(const moe_config& c, int E, int f, int64_t rows, const void* x,
+                              const int32_t* off, const void* W1, const void* W3, const void* dH,
+                              void* dA, int* err, cudaStream_t s) {
+  if (c.dtype == MOE_F32)
+    return launch_simt_fc1_bwd(E, c.hidden, f, rows, static_cast<const float*>(x), off,
+                               static_cast<const float*>(W1), static_cast<const float*>(W3),
+                               static_cast<const float*>(dH), static_cast<float*>(dA), err, s);
+  return launch_tc_fc1_bwd(E, c.hidden, f, rows, x, off, W1, W3, dH, dA, err, s);
+}
+cudaError_t bwd_dgrad_fc1(const moe_config& c, int E, int f, int64_t rows, const void* dA,
+                          const int32_t* off, const void* W1, const void* W3, float* dx, int* err,
+                          cudaStream_t s, bool accumulate = false) {
+  if (c.dtype == MOE_F32)
+    return launch_simt_dgrad_fc1(E, c.hidden, f, rows, static_cast<const float*>(dA), off,
+                                 static_cast<const float*>(W1), static_cast<const float*>(W3), dx,
+                                 err, s, accumulate);
+  return launch_tc_dgrad_fc1(E, c.hidden, f, rows, dA, off, W1, W3, dx, err, s, accumulate);
+}
+// dW [E, M, N] fp32 = A_e^T . B_e; lda / ldb in elements, B may start at a
+// column offset (dA's dg half)
+cudaError_t bwd_wgrad(const moe_config& c, int E, int M, int N, int64_t rows, const void* A,
+                      int lda, const void* B, int ldb, const int32_t* off, float* dW, int* err,
+                      cudaStream_t s) {
+  if (c.dtype == MOE_F32)
+    return launch_simt_wgrad(E, M, N, rows, static_cast<const float*>(A), lda,
+                             static_cast<const float*>(B), ldb, off, dW, err, s);
+  return launch_tc_wgrad(E, M, N, rows, A, lda, B, ldb, off, dW, err, s);
+}
+// element `i` of an activation buffer of the configuration's dtype
+const void* act_at(const moe_config& c, const void* p, size_t i) {
+  return static_cast<const char*>(p) + i * (c.dtype == MOE_F32 ? 4 : 2);
+}
+
 struct BwdLayout {
   size_t err, logits, dp, dl, dwg_part, dl3, wg3, dwg2, dx_router, dY_perm, dH, dA, dx_perm;
   size_t dH_s, dA_s, total;
@@ -464,23 +512,24 @@ BwdLayout make_bwd_layout(const moe_config& c, int32_t fs = 0) {
   };
   const size_t T = c.num_tokens, E = c.num_experts, k = c.topk, h = c.hidden, f = c.ffn_hidden;
   const size_t R = T * k;
+  const size_t el = c.dtype == MOE_F32 ? 4 : 2;  // the activation gradients' element
   B.err = take(kErrBytes);
   B.logits = take(T * E * 4 * kRouterMaxSplits);
   B.dp = take(T * k * 4);
   B.dl = take(T * E * 4);
-  const bool tc = router_grads_on_tc(c.num_experts);
+  const bool tc = bwd_router_on_tc(c);
   B.dwg_part = take(tc ? 0 : static_cast<size_t>(dwg_splits(c.num_tokens, c.hidden, c.num_experts)) * h * E * 4);
   B.dl3 = take(tc ? T * 3 * E * 2 : 0);
   B.wg3 = take(tc ? h * 3 * E * 2 : 0);
   B.dwg2 = take(tc ? h * 2 * E * 4 : 0);
   B.dx_router = take(T * h * 4);
-  B.dY_perm = take(R * h * 2);
-  B.dH = take(R * f * 2);
-  B.dA = take(R * 2 * f * 2);
+  B.dY_perm = take(R * h * el);
+  B.dH = take(R * f * el);
+  B.dA = take(R * 2 * f * el);
   B.dx_perm = take(R * h * 4);
   const size_t F = fs > 0 ? static_cast<size_t>(fs) : 0;
-  B.dH_s = take(T * F * 2);
-  B.dA_s = take(T * 2 * F * 2);
+  B.dH_s = take(T * F * el);
+  B.dA_s = take(T * 2 * F * el);
   B.total = o;
   return B;
 }
@@ -551,20 +600,20 @@ struct SharedBwd {
 moe_status shared_bwd_dgrad(const moe_config& c, const SharedBwd& sh, const void* x,
                             const void* dy, float* dx_acc, void* dH_s, void* dA_s, int* err,
                             cudaStream_t s) {
-  const int T = c.num_tokens, h = c.hidden, fs = sh.fs;
-  MOE_CUDA(launch_tc_dgrad_fc2(1, h, fs, T, dy, nullptr, sh.W2s, dH_s, err, s));
-  MOE_CUDA(launch_tc_fc1_bwd(1, h, fs, T, x, nullptr, sh.W1s, sh.W3s, dH_s, dA_s, err, s));
-  MOE_CUDA(launch_tc_dgrad_fc1(1, h, fs, T, dA_s, nullptr, sh.W1s, sh.W3s, dx_acc, err, s,
-                               /*accumulate=*/true));
+  const int T = c.num_tokens, fs = sh.fs;
+  MOE_CUDA(bwd_dgrad_fc2(c, 1, fs, T, dy, nullptr, sh.W2s, dH_s, err, s));
+  MOE_CUDA(bwd_fc1_recompute(c, 1, fs, T, x, nullptr, sh.W1s, sh.W3s, dH_s, dA_s, err, s));
+  MOE_CUDA(bwd_dgrad_fc1(c, 1, fs, T, dA_s, nullptr, sh.W1s, sh.W3s, dx_acc, err, s,
+                         /*accumulate=*/true));
   return MOE_OK;
 }
 moe_status shared_bwd_wgrad(const moe_config& c, const SharedBwd& sh, const void* x,
                             const void* dy, const void* dA_s, int* err, cudaStream_t s) {
   const int T = c.num_tokens, h = c.hidden, fs = sh.fs;
-  MOE_CUDA(launch_tc_wgrad(1, fs, h, T, sh.h_mid_s, fs, dy, h, nullptr, sh.dW2s, err, s));
-  MOE_CUDA(launch_tc_wgrad(1, h, fs, T, x, h, dA_s, 2 * fs, nullptr, sh.dW1s, err, s));
-  MOE_CUDA(launch_tc_wgrad(1, h, fs, T, x, h, static_cast<const __nv_bfloat16*>(dA_s) + fs,
-                           2 * fs, nullptr, sh.dW3s, err, s));
+  MOE_CUDA(bwd_wgrad(c, 1, fs, h, T, sh.h_mid_s, fs, dy, h, nullptr, sh.dW2s, err, s));
+  MOE_CUDA(bwd_wgrad(c, 1, h, fs, T, x, h, dA_s, 2 * fs, nullptr, sh.dW1s, err, s));
+  MOE_CUDA(bwd_wgrad(c, 1, h, fs, T, x, h, act_at(c, dA_s, fs), 2 * fs, nullptr, sh.dW3s, err,
+                     s));
   return MOE_OK;
 }
 
@@ -590,7 +639,7 @@ moe_status do_backward(const moe_config* cfg, const void* x, const float* Wg,
                        const SharedBwd* sh, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
-  if (c.dtype != MOE_BF16 || c.pad_to_capacity) return MOE_ERR_UNSUPPORTED;
+  if (c.pad_to_capacity) return MOE_ERR_UNSUPPORTED;
   if (sh) MOE_TRY(check_shared_bwd(c, *sh));
   const size_t T = c.num_tokens, E = c.num_experts, k = c.topk, h = c.hidden, f = c.ffn_hidden;
   const size_t R = T * k, wsz = E * h * f;
@@ -630,35 +679,34 @@ moe_status do_backward(const moe_config* cfg, const void* x, const float* Wg,
   // router: logits again (the forward does not keep them), then its gradients
   int nsplit = 1;
   MOE_CUDA(launch_router_logits(Ti, hi, Ei, c.dtype, x, Wg, logits, &nsplit, stream));
-  MOE_CUDA(launch_combine_bwd(Ti, hi, ki, dy, row_map, topk_prob, y_perm, dY_perm, dp, stream));
+  MOE_CUDA(launch_combine_bwd(Ti, hi, ki, c.dtype, dy, row_map, topk_prob, y_perm, dY_perm, dp,
+                              stream));
   MOE_CUDA(launch_router_bwd(Ti, Ei, ki, c.score, logits, nsplit, gate_bias, topk_idx, dp, dl,
                              stream));
-  if (router_grads_on_tc(Ei)) {
+  if (bwd_router_on_tc(c)) {
     MOE_CUDA(launch_router_grads_tc(Ti, hi, Ei, x, dl, Wg, at<void>(ws, B.dl3), at<void>(ws, B.wg3),
                                     at<float>(ws, B.dwg2), dWg, dgate_bias, dx_router, err,
                                     stream));
   } else {
-    MOE_CUDA(launch_router_param_grads(Ti, hi, Ei, x, dl, dWg, at<float>(ws, B.dwg_part),
+    MOE_CUDA(launch_router_param_grads(Ti, hi, Ei, c.dtype, x, dl, dWg, at<float>(ws, B.dwg_part),
                                        dgate_bias, stream));
     MOE_CUDA(launch_dx_router(Ti, hi, Ei, dl, Wg, dx_router, stream));
   }
   // experts: dgrad chain, then the token gradient, then the weight gradients
-  MOE_CUDA(launch_tc_dgrad_fc2(Ei, hi, fi, rows, dY_perm, expert_offsets, W2, dH, err, stream));
-  MOE_CUDA(launch_tc_fc1_bwd(Ei, hi, fi, rows, x_perm, expert_offsets, W1, W3, dH, dA, err,
+  MOE_CUDA(bwd_dgrad_fc2(c, Ei, fi, rows, dY_perm, expert_offsets, W2, dH, err, stream));
+  MOE_CUDA(bwd_fc1_recompute(c, Ei, fi, rows, x_perm, expert_offsets, W1, W3, dH, dA, err,
                              stream));
-  MOE_CUDA(launch_tc_dgrad_fc1(Ei, hi, fi, rows, dA, expert_offsets, W1, W3, dx_perm, err,
-                               stream));
+  MOE_CUDA(bwd_dgrad_fc1(c, Ei, fi, rows, dA, expert_offsets, W1, W3, dx_perm, err, stream));
   if (sh)  // the shared expert's dx joins dx_router before the one rounding
     MOE_TRY(shared_bwd_dgrad(c, *sh, x, dy, dx_router, at<void>(ws, B.dH_s), at<void>(ws, B.dA_s),
                              err, stream));
   MOE_CUDA(launch_combine(Ti, hi, ki, c.dtype, dx_perm, row_map, nullptr, dx_router, dx, stream));
-  MOE_CUDA(launch_tc_wgrad(Ei, fi, hi, rows, h_mid, fi, dY_perm, hi, expert_offsets, dW2, err,
-                           stream));
-  MOE_CUDA(launch_tc_wgrad(Ei, hi, fi, rows, x_perm, hi, dA, 2 * fi, expert_offsets, dW1, err,
-                           stream));
-  MOE_CUDA(launch_tc_wgrad(Ei, hi, fi, rows, x_perm, hi,
-                           static_cast<const __nv_bfloat16*>(dA) + fi, 2 * fi, expert_offsets,
-                           dW3, err, stream));
+  MOE_CUDA(bwd_wgrad(c, Ei, fi, hi, rows, h_mid, fi, dY_perm, hi, expert_offsets, dW2, err,
+                     stream));
+  MOE_CUDA(bwd_wgrad(c, Ei, hi, fi, rows, x_perm, hi, dA, 2 * fi, expert_offsets, dW1, err,
+                     stream));
+  MOE_CUDA(bwd_wgrad(c, Ei, hi, fi, rows, x_perm, hi, act_at(c, dA, fi), 2 * fi, expert_offsets,
+                     dW3, err, stream));
   if (sh) MOE_TRY(shared_bwd_wgrad(c, *sh, x, dy, at<void>(ws, B.dA_s), err, stream));
   return MOE_OK;
 }
@@ -1210,7 +1258,7 @@ moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* W
 
 moe_status moe_workspace_size_backward(const moe_config* cfg, size_t* bytes) {
   MOE_TRY(validate(cfg));
-  if (cfg->dtype != MOE_BF16 || cfg->pad_to_capacity) return MOE_ERR_UNSUPPORTED;
+  if (cfg->pad_to_capacity) return MOE_ERR_UNSUPPORTED;
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
   *bytes = make_bwd_layout(*cfg).total;
   return MOE_OK;
@@ -1230,7 +1278,7 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* Wg,
 
 moe_status moe_workspace_size_backward_shared(const moe_config* cfg, int32_t fs, size_t* bytes) {
   MOE_TRY(validate(cfg));
-  if (cfg->dtype != MOE_BF16 || cfg->pad_to_capacity) return MOE_ERR_UNSUPPORTED;
+  if (cfg->pad_to_capacity) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(validate_fs(*cfg, fs));
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
   *bytes = make_bwd_layout(*cfg, fs).total;
@@ -1260,7 +1308,7 @@ moe_status moe_shared_expert_backward(const moe_config* cfg, int32_t fs, const v
                                       size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
-  if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c.pad_to_capacity) return MOE_ERR_UNSUPPORTED;
   const SharedBwd sh{fs, W1s, W3s, W2s, h_mid_s, dW1s, dW3s, dW2s};
   MOE_TRY(check_shared_bwd(c, sh));
   const size_t T = c.num_tokens, h = c.hidden;

@@ -134,6 +134,23 @@ cudaError_t launch_simt_fc1(int E, int h, int f, int64_t max_rows, const float* 
 cudaError_t launch_simt_fc2(int E, int h, int f, int64_t max_rows, const float* h_mid,
                             const int32_t* offsets, const float* W2, float* y_perm, int* err,
                             cudaStream_t s);
+// the layer backward on the FMA units (fp32): dH = dY . W2[e]^T; the fc1
+// recompute with the SwiGLU backward ([da | dg] [rows, 2f] from dH);
+// dx = [da | dg] . [W1[e] ; W3[e]]^T (added to dx when accumulate);
+// dW[e] [M, N] = A_e^T . B_e over expert e's rows (offsets NULL: one dense
+// group of max_rows rows)
+cudaError_t launch_simt_dgrad_fc2(int E, int h, int f, int64_t max_rows, const float* dY,
+                                  const int32_t* offsets, const float* W2, float* dH, int* err,
+                                  cudaStream_t s);
+cudaError_t launch_simt_fc1_bwd(int E, int h, int f, int64_t max_rows, const float* x_perm,
+                                const int32_t* offsets, const float* W1, const float* W3,
+                                const float* dH, float* dA, int* err, cudaStream_t s);
+cudaError_t launch_simt_dgrad_fc1(int E, int h, int f, int64_t max_rows, const float* dA,
+                                  const int32_t* offsets, const float* W1, const float* W3,
+                                  float* dx, int* err, cudaStream_t s, bool accumulate = false);
+cudaError_t launch_simt_wgrad(int E, int M, int N, int64_t max_rows, const float* A, int lda,
+                              const float* B, int ldb, const int32_t* offsets, float* dW,
+                              int* err, cudaStream_t s);
 // tcgen05 path (dtype MOE_BF16)
 cudaError_t launch_tc_fc1(int E, int h, int f, int64_t max_rows, const void* x_perm,
                           const int32_t* offsets, const void* W1, const void* W3, void* h_mid,
@@ -181,16 +198,17 @@ cudaError_t launch_tc_dense_nt_f32(int64_t rows, int K, int N, const void* A, co
                                    float* C, int ldc, int* err, cudaStream_t s);
 
 // ---- backward around the GEMMs (backward.cu)
-cudaError_t launch_combine_bwd(int T, int h, int k, const void* dy, const int32_t* row_map,
-                               const float* topk_prob, const float* y_perm, void* dY_perm,
-                               float* dp, cudaStream_t s);
+cudaError_t launch_combine_bwd(int T, int h, int k, int dtype, const void* dy,
+                               const int32_t* row_map, const float* topk_prob,
+                               const float* y_perm, void* dY_perm, float* dp, cudaStream_t s);
 cudaError_t launch_router_bwd(int T, int E, int k, int score, const float* logits, int nsplit,
                               const float* gate_bias, const int32_t* topk_idx, const float* dp,
                               float* dlogits, cudaStream_t s);
 // dWg partial sums need dwg_splits(T, h, E) * h * E floats at `part`
 int dwg_splits(int T, int h, int E);
-cudaError_t launch_router_param_grads(int T, int h, int E, const void* x, const float* dl,
-                                      float* dWg, float* part, float* dgb, cudaStream_t s);
+cudaError_t launch_router_param_grads(int T, int h, int E, int dtype, const void* x,
+                                      const float* dl, float* dWg, float* part, float* dgb,
+                                      cudaStream_t s);
 cudaError_t launch_dx_router(int T, int h, int E, const float* dl, const float* Wg, float* out,
                              cudaStream_t s);
 // The router's gradients on the tensor cores when E % 64 == 0: fp32 dl and

@@ -190,10 +190,14 @@ def test_backward_shared_host_checks(moe):
     assert lib.moe_workspace_size_backward_shared(ctypes.byref(cfg), 256, ctypes.byref(size)) == OK
     # the routed backward's workspace + dH_s [T,256] + dA_s [T,512] bf16
     assert size.value >= base.value + 128 * 256 * 2 + 128 * 512 * 2
-    f32 = moe.config(T=16, h=136, E=4, k=2, f=200, dtype="f32")
-    assert lib.moe_workspace_size_backward_shared(ctypes.byref(f32), 72,
-                                                  ctypes.byref(size)) == UNSUPPORTED
     need = size.value
+    # fp32 runs the backward on the FMA units: fp32 gradient buffers
+    f32 = moe.config(T=16, h=136, E=4, k=2, f=200, dtype="f32")
+    f32_size, f32_base = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.moe_workspace_size_backward(ctypes.byref(f32), ctypes.byref(f32_base)) == OK
+    assert lib.moe_workspace_size_backward_shared(ctypes.byref(f32), 72,
+                                                  ctypes.byref(f32_size)) == OK
+    assert f32_size.value >= f32_base.value + 16 * 72 * 4 + 16 * 144 * 4
     # moe_backward_shared: W1s missing, then a misaligned dW2s, then the routed-only workspace
     args = [FAKE] * 27
     args[6] = None                                   # W1s
@@ -204,13 +208,13 @@ def test_backward_shared_host_checks(moe):
     args = [FAKE] * 27
     assert lib.moe_backward_shared(ctypes.byref(cfg), 256, *args, FAKE, base.value,
                                    None) == WORKSPACE
-    # moe_shared_expert_backward: dx_acc missing; fp32 refused
+    # moe_shared_expert_backward: dx_acc missing; an fp32 call with too small a workspace
     assert lib.moe_shared_expert_backward(ctypes.byref(cfg), 256, FAKE, FAKE, FAKE, FAKE, FAKE,
                                           FAKE, None, FAKE, FAKE, FAKE, FAKE, need,
                                           None) == INVALID
     assert lib.moe_shared_expert_backward(ctypes.byref(f32), 72, FAKE, FAKE, FAKE, FAKE, FAKE,
-                                          FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need,
-                                          None) == UNSUPPORTED
+                                          FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, f32_base.value,
+                                          None) == WORKSPACE
 
 
 @pytest.mark.parametrize("E,k,G,gk,want", [

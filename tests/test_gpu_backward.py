@@ -136,8 +136,8 @@ def test_backward_is_deterministic(case):
         assert torch.equal(getattr(outs[0], n), getattr(outs[1], n)), n
 
 
-def test_backward_rejects_fp32():
+def test_backward_rejects_pad_to_capacity():
     import mixture_experts_layer_fp32_gb300 as moe
-    cfg = moe.config(T=16, h=136, E=4, k=2, f=200, dtype="f32")
+    cfg = moe.config(T=16, h=256, E=4, k=2, f=128, capacity_factor=1.0, pad_to_capacity=True)
     with pytest.raises(moe.MoeError):
         moe.workspace_size_backward(cfg)
