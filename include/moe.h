@@ -106,8 +106,9 @@ typedef struct moe_config {
    * equal zero probabilities open; lower token index first is the reading,
    * as for every tie here).  Padding tokens carry no combine weight, so the
    * layer output equals the unpadded one; the permuted buffers hold
-   * E * min(capacity, T) rows (moe_max_rows).  0: off.  The E4M3 and
-   * backward entry points return MOE_ERR_UNSUPPORTED when it is 1. */
+   * E * min(capacity, T) rows (moe_max_rows).  0: off.  The E4M3 entry
+   * points return MOE_ERR_UNSUPPORTED when it is 1; the backward gives the
+   * padding rows zero gradients (they carry no combine weight). */
   int32_t pad_to_capacity;
 } moe_config;
 
@@ -360,7 +361,8 @@ moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* W
  * read in place, wgrad reducing over each expert's rows); dY, dH, da and dg
  * are rounded to bf16 as GEMM operands; accumulation is fp32.  MOE_F32: the
  * same GEMMs on the FMA units, every intermediate fp32.  pad_to_capacity:
- * MOE_ERR_UNSUPPORTED.
+ * the saved buffers hold the padded rows (moe_max_rows); their dY rows are
+ * zero, so they add nothing to any gradient.
  *   Saved from the forward (the staged calls' outputs): topk_idx and
  *   topk_prob [T,k] (moe_route), row_map [T,k], expert_offsets [E+1] and
  *   x_perm [T*k,h] (moe_permute), h_mid [T*k,f] and y_perm [T*k,h] fp32

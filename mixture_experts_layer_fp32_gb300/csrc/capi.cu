@@ -510,12 +510,12 @@ BwdLayout make_bwd_layout(const moe_config& c, int32_t fs = 0) {
     o = align_up(o + bytes);
     return r;
   };
-  const size_t T = c.num_tokens, E = c.num_experts, k = c.topk, h = c.hidden, f = c.ffn_hidden;
-  const size_t R = T * k;
+  const size_t T = c.num_tokens, E = c.num_experts, h = c.hidden, f = c.ffn_hidden;
+  const size_t R = static_cast<size_t>(rows_of(c));  // padded rows with pad_to_capacity
   const size_t el = c.dtype == MOE_F32 ? 4 : 2;  // the activation gradients' element
   B.err = take(kErrBytes);
   B.logits = take(T * E * 4 * kRouterMaxSplits);
-  B.dp = take(T * k * 4);
+  B.dp = take(T * c.topk * 4);
   B.dl = take(T * E * 4);
   const bool tc = bwd_router_on_tc(c);
   B.dwg_part = take(tc ? 0 : static_cast<size_t>(dwg_splits(c.num_tokens, c.hidden, c.num_experts)) * h * E * 4);
@@ -639,10 +639,9 @@ moe_status do_backward(const moe_config* cfg, const void* x, const float* Wg,
                        const SharedBwd* sh, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
-  if (c.pad_to_capacity) return MOE_ERR_UNSUPPORTED;
   if (sh) MOE_TRY(check_shared_bwd(c, *sh));
   const size_t T = c.num_tokens, E = c.num_experts, k = c.topk, h = c.hidden, f = c.ffn_hidden;
-  const size_t R = T * k, wsz = E * h * f;
+  const size_t R = static_cast<size_t>(rows_of(c)), wsz = E * h * f;
   MOE_TRY(need(x, T * h, 16));
   MOE_TRY(need(Wg, h * E, 4));
   MOE_TRY(optional(gate_bias, 4));
@@ -676,6 +675,10 @@ moe_status do_backward(const moe_config* cfg, const void* x, const float* Wg,
   void* dH = at<void>(ws, B.dH);
   void* dA = at<void>(ws, B.dA);
   float* dx_perm = at<float>(ws, B.dx_perm);
+  // pad_to_capacity: the padding rows have no slot, so the combine backward
+  // writes no dY row for them; zeros make every gradient they reach zero
+  if (c.pad_to_capacity)
+    MOE_CUDA(cudaMemsetAsync(dY_perm, 0, R * h * (c.dtype == MOE_F32 ? 4 : 2), stream));
   // router: logits again (the forward does not keep them), then its gradients
   int nsplit = 1;
   MOE_CUDA(launch_router_logits(Ti, hi, Ei, c.dtype, x, Wg, logits, &nsplit, stream));
@@ -700,7 +703,8 @@ moe_status do_backward(const moe_config* cfg, const void* x, const float* Wg,
   if (sh)  // the shared expert's dx joins dx_router before the one rounding
     MOE_TRY(shared_bwd_dgrad(c, *sh, x, dy, dx_router, at<void>(ws, B.dH_s), at<void>(ws, B.dA_s),
                              err, stream));
-  MOE_CUDA(launch_combine(Ti, hi, ki, c.dtype, dx_perm, row_map, nullptr, dx_router, dx, stream));
+  MOE_CUDA(launch_combine(Ti, hi, ki, c.dtype, dx_perm, row_map, nullptr, dx_router, dx, stream,
+                          rows));
   MOE_CUDA(bwd_wgrad(c, Ei, fi, hi, rows, h_mid, fi, dY_perm, hi, expert_offsets, dW2, err,
                      stream));
   MOE_CUDA(bwd_wgrad(c, Ei, hi, fi, rows, x_perm, hi, dA, 2 * fi, expert_offsets, dW1, err,
@@ -1258,7 +1262,6 @@ moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* W
 
 moe_status moe_workspace_size_backward(const moe_config* cfg, size_t* bytes) {
   MOE_TRY(validate(cfg));
-  if (cfg->pad_to_capacity) return MOE_ERR_UNSUPPORTED;
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
   *bytes = make_bwd_layout(*cfg).total;
   return MOE_OK;
@@ -1278,7 +1281,6 @@ moe_status moe_backward(const moe_config* cfg, const void* x, const float* Wg,
 
 moe_status moe_workspace_size_backward_shared(const moe_config* cfg, int32_t fs, size_t* bytes) {
   MOE_TRY(validate(cfg));
-  if (cfg->pad_to_capacity) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(validate_fs(*cfg, fs));
   if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
   *bytes = make_bwd_layout(*cfg, fs).total;
@@ -1308,7 +1310,6 @@ moe_status moe_shared_expert_backward(const moe_config* cfg, int32_t fs, const v
                                       size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
-  if (c.pad_to_capacity) return MOE_ERR_UNSUPPORTED;
   const SharedBwd sh{fs, W1s, W3s, W2s, h_mid_s, dW1s, dW3s, dW2s};
   MOE_TRY(check_shared_bwd(c, sh));
   const size_t T = c.num_tokens, h = c.hidden;

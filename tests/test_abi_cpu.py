@@ -293,11 +293,15 @@ def test_pad_to_capacity_configuration(moe):
                                    pad_to_capacity=True)) == 8 * 100
     assert moe.max_rows(moe.config(T=1000, h=256, E=8, k=2, f=128, capacity_factor=0.5,
                                    pad_to_capacity=True)) == 2000
-    # the E4M3 and backward paths are not built for it
+    # the E4M3 path is not built for it; the backward's buffers hold the padded rows
     cfg = moe.config(T=128, h=4096, E=8, k=2, f=1536, capacity_factor=1.0, pad_to_capacity=True)
     assert _status(moe, "moe_workspace_size_e4m3", _cfgp(cfg), ctypes.byref(size)) == UNSUPPORTED
-    assert _status(moe, "moe_workspace_size_backward", _cfgp(cfg), ctypes.byref(size)) == \
-        UNSUPPORTED
+    assert _status(moe, "moe_workspace_size_backward", _cfgp(cfg), ctypes.byref(size)) == OK
+    padded = size.value
+    cfg.pad_to_capacity = 0
+    assert _status(moe, "moe_workspace_size_backward", _cfgp(cfg), ctypes.byref(size)) == OK
+    assert padded >= size.value
+    cfg.pad_to_capacity = 1
     need = moe.workspace_size(cfg)
     # the pair permutation cannot place padding rows; the route must return the map
     assert lib.moe_permute(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need,

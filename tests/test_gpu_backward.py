@@ -134,10 +134,3 @@ def test_backward_is_deterministic(case):
     torch.cuda.synchronize()
     for n in ("dx", "dWg", "dW1", "dW3", "dW2"):
         assert torch.equal(getattr(outs[0], n), getattr(outs[1], n)), n
-
-
-def test_backward_rejects_pad_to_capacity():
-    import mixture_experts_layer_fp32_gb300 as moe
-    cfg = moe.config(T=16, h=256, E=4, k=2, f=128, capacity_factor=1.0, pad_to_capacity=True)
-    with pytest.raises(moe.MoeError):
-        moe.workspace_size_backward(cfg)

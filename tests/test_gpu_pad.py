@@ -9,8 +9,11 @@ offsets, row_map and every permuted row; h_mid, y_perm (padding rows
 included) and y within the parity tolerances.  Padding rows carry no combine
 weight, so the layer output equals the unpadded layer's bit for bit (each
 output row of the grouped GEMM depends on its own row only).  Also: the
-padded moe_forward reproduces the staged calls, and moe_permute_map on an
-unpadded routing map gives moe_permute's result.
+padded moe_forward reproduces the staged calls, moe_permute_map on an
+unpadded routing map gives moe_permute's result, and the backward of the
+padded layer gives the unpadded layer's gradients (the oracle backward of the
+same routing; the padding rows' gradients are zero) within the criteria of
+the bf16 and fp32 backward tests.
 """
 
 import pytest
@@ -101,3 +104,38 @@ def test_permute_map_equals_permute_without_padding(name, w):
     assert torch.equal(offsets, b.expert_offsets)
     assert torch.equal(row_map, b.row_map)
     assert torch.equal(x_perm[:R], b.x_perm[:R])
+
+
+@pytest.mark.parametrize("name", ["switch_probs", "top2_hot", "tiny_fp32"])
+def test_padded_backward_matches_oracle(name):
+    import mixture_experts_layer_fp32_gb300 as moe
+    import oracle
+    from moe_cases import assert_close, np_view
+    from test_gpu_backward import assert_grad
+    w = CASES[name]
+    inp, r = make_case(w)
+    dinp = to_dev(inp)
+    b = gpu_stages(w, dinp)
+    cfg = gpu_config(w)
+    dy = torch.randn((w.T, w.h), generator=torch.Generator().manual_seed(420)).to(
+        moe.act_dtype(cfg))
+    g = moe.Grads(cfg)
+    ws = moe.alloc_workspace_backward(cfg)
+    moe.backward(cfg, dinp["x"], dinp["Wg"], dinp["gate_bias"], dinp["W1"], dinp["W3"],
+                 dinp["W2"], b, dy.cuda(), g, ws)
+    moe.check(ws)
+    torch.cuda.synchronize()
+    ref = oracle.backward(np_view(inp["x"]), np_view(inp["Wg"]), np_view(inp["W1"]),
+                          np_view(inp["W3"]), np_view(inp["W2"]), w.k, w.score, r["topk_idx"],
+                          r["topk_prob"], r["keep"], np_view(dy), np_view(inp["gate_bias"]),
+                          np_view(inp["expert_bias"]))
+    for n in ("dx", "dWg", "dgate_bias", "dW1", "dW3", "dW2"):
+        got = to_np(getattr(g, n))
+        if w.dtype == "f32":
+            assert_close(n, got, ref[n], "f32")
+        elif n == "dWg" and not ref[n].any():  # top-1 after softmax: nothing reaches the router
+            assert not got.any()
+        elif n == "dgate_bias" and not ref[n].any():
+            assert not got.any()
+        else:
+            assert_grad(n, got, ref[n])
