@@ -431,7 +431,7 @@ constexpr int kCombineThreads = 256;
 // A CTA combines 2^TPI_LOG2 tokens per round, kCombineThreads >> TPI_LOG2
 // threads each (several tokens per round when rows are short).  K1: top-1
 // (one row per token), four vectors per thread in flight.
-template <typename OT, int TPI_LOG2, bool K1>
+template <typename OT, int TPI_LOG2, bool K1, int U>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(int T, int h, int k, int64_t max_rows, const float* __restrict__ y_perm,
                    const int32_t* __restrict__ row_map, const float* __restrict__ topk_prob,
@@ -486,25 +486,45 @@ __global__ void __launch_bounds__(kCombineThreads)
         }
       }
     } else {
-      for (int v = lt; v < h4; v += tpt) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      // U vectors of the row per thread at a time: each slot's U loads are
+      // issued together (k x U in flight; U = 4 for k <= 2, where k loads
+      // alone leave the HBM idle, 1 for more slots, where the registers of
+      // more would cost occupancy), the fp32 sum still in slot order
+      for (int v0 = lt; v0 < h4; v0 += U * tpt) {
+        float4 acc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < MOE_MAX_TOPK; ++j) {
           if (rows[j] < 0) continue;
-          const float4 a = __ldcs(reinterpret_cast<const float4*>(y_perm + (int64_t)rows[j] * h) + v);
-          acc.x = fmaf(p[j], a.x, acc.x);
-          acc.y = fmaf(p[j], a.y, acc.y);
-          acc.z = fmaf(p[j], a.z, acc.z);
-          acc.w = fmaf(p[j], a.w, acc.w);
+          const float4* src = reinterpret_cast<const float4*>(y_perm + (int64_t)rows[j] * h);
+          float4 a[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * tpt;
+            a[u] = v < h4 ? __ldcs(src + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            acc[u].x = fmaf(p[j], a[u].x, acc[u].x);
+            acc[u].y = fmaf(p[j], a[u].y, acc[u].y);
+            acc[u].z = fmaf(p[j], a[u].z, acc[u].z);
+            acc[u].w = fmaf(p[j], a[u].w, acc[u].w);
+          }
         }
-        if (y_shared) {  // the shared expert's output, added after the routed sum
-          const float4 b = __ldcs(reinterpret_cast<const float4*>(y_shared + (int64_t)t * h) + v);
-          acc.x += b.x;
-          acc.y += b.y;
-          acc.z += b.z;
-          acc.w += b.w;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * tpt;
+          if (v >= h4) continue;
+          if (y_shared) {  // the shared expert's output, added after the routed sum
+            const float4 b = __ldcs(reinterpret_cast<const float4*>(y_shared + (int64_t)t * h) + v);
+            acc[u].x += b.x;
+            acc[u].y += b.y;
+            acc[u].z += b.z;
+            acc[u].w += b.w;
+          }
+          Out4<OT>::store(y + (int64_t)t * h + 4 * v, acc[u]);
         }
-        Out4<OT>::store(y + (int64_t)t * h + 4 * v, acc);
       }
     }
   }
@@ -736,16 +756,15 @@ __global__ void __launch_bounds__(kPadChunk)
   if (free_tok && (t0 - s_lo) + before < need) map[static_cast<int64_t>(t) * E + e] = 1;
 }
 
-template <typename OT, bool K1>
+template <typename OT, bool K1, int U>
 void launch_combine_t(int l, int grid, cudaStream_t s, int T, int h, int k, int64_t max_rows,
-                      const float* y_perm,
-                      const int32_t* row_map, const float* topk_prob, const float* y_shared,
-                      OT* y) {
+                      const float* y_perm, const int32_t* row_map, const float* topk_prob,
+                      const float* y_shared, OT* y) {
   switch (l) {
-    case 0: combine_kernel<OT, 0, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
-    case 1: combine_kernel<OT, 1, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
-    case 2: combine_kernel<OT, 2, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
-    default: combine_kernel<OT, 3, K1><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
+    case 0: combine_kernel<OT, 0, K1, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
+    case 1: combine_kernel<OT, 1, K1, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
+    case 2: combine_kernel<OT, 2, K1, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
+    default: combine_kernel<OT, 3, K1, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, y_perm, row_map, topk_prob, y_shared, y); break;
   }
 }
 
@@ -870,18 +889,27 @@ cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
   const int l = tokens_per_round_log2(h / 4, kCombineThreads, 4, 3);
   const int grid = grid_for_tokens((T + (1 << l) - 1) >> l, 8);
   if (dtype == MOE_F32) {
+    float* o = static_cast<float*>(y);
     if (k == 1)
-      launch_combine_t<float, true>(l, grid, s, T, h, k, max_rows, y_perm, row_map, topk_prob,
-                                    y_shared, static_cast<float*>(y));
+      launch_combine_t<float, true, 1>(l, grid, s, T, h, k, max_rows, y_perm, row_map, topk_prob,
+                                       y_shared, o);
+    else if (k == 2)
+      launch_combine_t<float, false, 4>(l, grid, s, T, h, k, max_rows, y_perm, row_map,
+                                        topk_prob, y_shared, o);
     else
-      launch_combine_t<float, false>(l, grid, s, T, h, k, max_rows, y_perm, row_map, topk_prob,
-                                     y_shared, static_cast<float*>(y));
-  } else if (k == 1) {
-    launch_combine_t<__nv_bfloat16, true>(l, grid, s, T, h, k, max_rows, y_perm, row_map,
-                                          topk_prob, y_shared, static_cast<__nv_bfloat16*>(y));
+      launch_combine_t<float, false, 1>(l, grid, s, T, h, k, max_rows, y_perm, row_map,
+                                        topk_prob, y_shared, o);
   } else {
-    launch_combine_t<__nv_bfloat16, false>(l, grid, s, T, h, k, max_rows, y_perm, row_map,
-                                           topk_prob, y_shared, static_cast<__nv_bfloat16*>(y));
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(y);
+    if (k == 1)
+      launch_combine_t<__nv_bfloat16, true, 1>(l, grid, s, T, h, k, max_rows, y_perm, row_map,
+                                               topk_prob, y_shared, o);
+    else if (k == 2)
+      launch_combine_t<__nv_bfloat16, false, 4>(l, grid, s, T, h, k, max_rows, y_perm, row_map,
+                                                topk_prob, y_shared, o);
+    else
+      launch_combine_t<__nv_bfloat16, false, 1>(l, grid, s, T, h, k, max_rows, y_perm, row_map,
+                                                topk_prob, y_shared, o);
   }
   return cudaGetLastError();
 }
