@@ -367,13 +367,19 @@ def expert_rows_fp8(xq, xs, row_expert, q, nthreads=0):
 
 
 def forward_fp8(x, Wg, q, k, score, gate_bias=None, expert_bias=None, capacity_factor=0.0,
-                min_capacity=0, drop_policy="probs", nthreads=0, num_groups=0, group_topk=0):
+                min_capacity=0, drop_policy="probs", nthreads=0, num_groups=0, group_topk=0,
+                pad_to_capacity=False):
     """The layer with FP8 experts: route -> drop -> permute -> (x quantised per
-    token) FP8 SwiGLU experts -> combine.  q: quantize_experts_e4m3(...)."""
+    token) FP8 SwiGLU experts -> combine.  q: quantize_experts_e4m3(...).
+    pad_to_capacity: the experts run on the padded routing map's rows, as in
+    forward()."""
     r = route(x, Wg, k, score, gate_bias, expert_bias, capacity_factor, min_capacity,
-              drop_policy, nthreads, num_groups, group_topk)
+              drop_policy, nthreads, num_groups, group_topk, pad_to_capacity)
     E = Wg.shape[1]
-    offsets, row_map, row_token = permute(r["topk_idx"], r["keep"], E)
+    if pad_to_capacity:
+        offsets, row_map, row_token = permute_map(r["routing_map"], r["topk_idx"], r["keep"])
+    else:
+        offsets, row_map, row_token = permute(r["topk_idx"], r["keep"], E)
     row_expert = np.repeat(np.arange(E, dtype=np.int32), np.diff(offsets))
     xq, xs = quantize_rows_e4m3(x, nthreads)
     res = expert_rows_fp8(xq[row_token], xs[row_token], row_expert, q, nthreads)

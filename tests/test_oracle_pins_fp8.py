@@ -155,3 +155,23 @@ def test_fp8_forward_close_to_the_unquantised_layer():
     np.testing.assert_array_equal(out["topk_idx"], ref["topk_idx"])   # routing is not quantised
     rel = np.sqrt(np.mean((out["y"] - ref["y"]) ** 2) / np.mean(ref["y"] ** 2))
     assert 1e-4 < rel < 0.1, rel
+
+
+def test_fp8_padded_forward_equals_unpadded():
+    # pad_to_capacity adds rows of probability 0: the FP8 layer's output is
+    # unchanged bit for bit, and each padded row is its token's code row
+    T, h, E, k, f = 120, 32, 6, 2, 32
+    r = rng(124)
+    x = r.standard_normal((T, h)).astype(np.float32)
+    Wg = (0.2 * r.standard_normal((h, E))).astype(np.float32)
+    gb = np.linspace(1.0, -1.0, E).astype(np.float32)
+    W1, W3 = ((0.1 * r.standard_normal((E, h, f))).astype(np.float32) for _ in range(2))
+    W2 = (0.1 * r.standard_normal((E, f, h))).astype(np.float32)
+    q = oracle.quantize_experts_e4m3(W1, W3, W2)
+    a = oracle.forward_fp8(x, Wg, q, k, "softmax_post", gate_bias=gb, capacity_factor=1.25,
+                           pad_to_capacity=True)
+    b = oracle.forward_fp8(x, Wg, q, k, "softmax_post", gate_bias=gb, capacity_factor=1.25)
+    cap = a["capacity"]
+    assert int(a["offsets"][-1]) == E * min(cap, T) > int(b["offsets"][-1])
+    np.testing.assert_array_equal(a["y"], b["y"])
+    np.testing.assert_array_equal(a["xq"][a["row_token"]].shape[0], a["offsets"][-1])
