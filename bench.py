@@ -213,7 +213,8 @@ def kernels_per_forward(w, cfg, fp8=False):
     index = 2 if -(-w.T * w.k // 2048) <= 128 else 3
     route = (1 if fused else 2) + (index + 1 if drops else 0) + (1 if w.pad_to_capacity else 0)
     if w.pad_to_capacity:  # permutation by the padded map: hist, scan, rank, gather
-        return route + 4 + 1 + 1 + (2 if w.shared_f > 0 else 0) + 1
+        # E4M3: x quantised per token first, the scales gathered, the SwiGLU rows quantised
+        return route + 4 + 1 + 1 + (2 if w.shared_f > 0 else 0) + (3 if fp8 else 0) + 1
     shared = 2 if w.shared_f > 0 else 0  # the shared expert's fc1 and fc2
     quant = 1 if fp8 else 0           # E4M3: the SwiGLU rows before fc2 (x is quantised by the copy)
     return route + index + 1 + 1 + 1 + shared + quant + 1  # permute index + copy, fc1, fc2, combine
@@ -266,7 +267,7 @@ def run_native(args, rank, world, local):
             raise SystemExit("--precision e4m3 needs a bf16 workload without a shared expert")
         q = moe.E4m3Experts(cfg, inp["W1"], inp["W3"], inp["W2"])  # once, outside the timing
         b.ws = moe.alloc_workspace_e4m3(cfg, dev)
-        Rmax = w.T * w.k
+        Rmax = moe.max_rows(cfg)
         xq = torch.empty((Rmax, w.h), dtype=torch.uint8, device=dev)
         xs = torch.empty((Rmax,), dtype=torch.float32, device=dev)
         hq = torch.empty((Rmax, w.f), dtype=torch.uint8, device=dev)
@@ -279,8 +280,12 @@ def run_native(args, rank, world, local):
                   b.routing_map if w.pad_to_capacity else None, b.ws)
         if ev: ev[1].record(stream)
         if fp8:
-            moe.permute_e4m3(cfg, inp["x"], b.topk_idx, b.keep, xq, xs, b.row_map,
-                             b.expert_offsets, b.ws)
+            if w.pad_to_capacity:
+                moe.permute_map_e4m3(cfg, inp["x"], b.routing_map, b.topk_idx, b.keep, xq, xs,
+                                     b.row_map, b.expert_offsets, b.ws)
+            else:
+                moe.permute_e4m3(cfg, inp["x"], b.topk_idx, b.keep, xq, xs, b.row_map,
+                                 b.expert_offsets, b.ws)
             if ev: ev[2].record(stream)
             moe.grouped_fc1_e4m3(cfg, xq, xs, b.expert_offsets, q, b.h_mid, b.ws)
             if ev: ev[3].record(stream)

@@ -106,9 +106,10 @@ typedef struct moe_config {
    * equal zero probabilities open; lower token index first is the reading,
    * as for every tie here).  Padding tokens carry no combine weight, so the
    * layer output equals the unpadded one; the permuted buffers hold
-   * E * min(capacity, T) rows (moe_max_rows).  0: off.  The E4M3 entry
-   * points return MOE_ERR_UNSUPPORTED when it is 1; the backward gives the
-   * padding rows zero gradients (they carry no combine weight). */
+   * E * min(capacity, T) rows (moe_max_rows).  0: off.  The E4M3 layer
+   * permutes with moe_permute_map_e4m3 (moe_permute_e4m3 returns
+   * MOE_ERR_INVALID_ARG); the backward gives the padding rows zero
+   * gradients (they carry no combine weight). */
   int32_t pad_to_capacity;
 } moe_config;
 
@@ -307,9 +308,10 @@ moe_status moe_forward_shared(const moe_config* cfg, int32_t fs, const void* x, 
  * moe_permute_e4m3: moe_permute on E4M3 rows: x quantised per token, the
  *   kept pairs' code rows x_perm_q [T*k,h] and their scales x_perm_scale
  *   [T*k] in expert-major order; row_map and expert_offsets as moe_permute.
- * moe_grouped_mlp_e4m3: the E4M3 SwiGLU experts: h_mid [T*k,f] bf16,
- *   h_q [T*k,f] codes and h_scale [T*k] (the quantised SwiGLU output), and
- *   y_perm [T*k,h] fp32 out; rows >= expert_offsets[E] untouched.
+ * moe_grouped_mlp_e4m3: the E4M3 SwiGLU experts: h_mid [R_max,f] bf16,
+ *   h_q [R_max,f] codes and h_scale [R_max] (the quantised SwiGLU output), and
+ *   y_perm [R_max,h] fp32 out; rows >= expert_offsets[E] untouched (R_max =
+ *   moe_max_rows: T*k unless pad_to_capacity).
  *   moe_grouped_fc1_e4m3 / moe_grouped_fc2_e4m3 are its two halves: fc1
  *   writes h_mid; fc2 quantises h_mid's rows (h_q, h_scale) and writes y_perm.
  * moe_forward_e4m3: the whole layer with E4M3 experts (arguments of
@@ -325,6 +327,14 @@ moe_status moe_permute_e4m3(const moe_config* cfg, const void* x, const int32_t*
                             const uint8_t* keep, uint8_t* x_perm_q, float* x_perm_scale,
                             int32_t* row_map, int32_t* expert_offsets, void* ws,
                             size_t ws_bytes, moe_stream_t stream);
+/* The E4M3 permutation by the padded routing map of pad_to_capacity (needs
+ * it set; MOE_ERR_INVALID_ARG otherwise): every token's row quantised once,
+ * the code rows and their scales placed as moe_permute_map places rows;
+ * x_perm_q [moe_max_rows,h], x_perm_scale [moe_max_rows]. */
+moe_status moe_permute_map_e4m3(const moe_config* cfg, const void* x, const uint8_t* routing_map,
+                                const int32_t* topk_idx, const uint8_t* keep, uint8_t* x_perm_q,
+                                float* x_perm_scale, int32_t* row_map, int32_t* expert_offsets,
+                                void* ws, size_t ws_bytes, moe_stream_t stream);
 moe_status moe_grouped_mlp_e4m3(const moe_config* cfg, const uint8_t* x_perm_q,
                                 const float* x_perm_scale, const int32_t* expert_offsets,
                                 const uint8_t* W1q, const float* s1, const uint8_t* W3q,
@@ -365,7 +375,7 @@ moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* W
  * zero, so they add nothing to any gradient.
  *   Saved from the forward (the staged calls' outputs): topk_idx and
  *   topk_prob [T,k] (moe_route), row_map [T,k], expert_offsets [E+1] and
- *   x_perm [T*k,h] (moe_permute), h_mid [T*k,f] and y_perm [T*k,h] fp32
+ *   x_perm [R_max,h] (moe_permute), h_mid [R_max,f] and y_perm [R_max,h] fp32
  *   (moe_grouped_mlp).  Parameters as in moe_forward.
  *   dy [T,h] dtype in; dx [T,h] dtype out; dWg [h,E], dgate_bias [E]
  *   (nullable), dW1/dW3 [E,h,f], dW2 [E,f,h] fp32 out (overwritten).

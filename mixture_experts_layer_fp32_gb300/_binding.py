@@ -33,7 +33,7 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_c
            "moe_backward", "moe_workspace_size_backward_shared", "moe_backward_shared",
            "moe_shared_expert_backward", "moe_workspace_size_host_shared",
            "moe_forward_host_shared", "moe_workspace_size_host_e4m3", "moe_forward_host_e4m3",
-           "moe_permute_map"]
+           "moe_permute_map", "moe_permute_map_e4m3"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -77,6 +77,7 @@ def lib():
             "moe_route": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_permute": ([cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_permute_map": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_permute_map_e4m3": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_grouped_mlp": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_grouped_fc1": ([cfgp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_grouped_fc2": ([cfgp, vp, vp, vp, vp, vp, sz, vp], i32),
@@ -417,6 +418,16 @@ def workspace_size_e4m3(cfg):
 
 def alloc_workspace_e4m3(cfg, device="cuda"):
     return torch.zeros(workspace_size_e4m3(cfg), dtype=torch.uint8, device=device)
+
+
+def permute_map_e4m3(cfg, x, routing_map, topk_idx, keep, x_perm_q, x_perm_scale, row_map,
+                     expert_offsets, ws):
+    """moe_permute_map_e4m3: the E4M3 permutation by the padded routing map."""
+    w, wb = _ws(ws)
+    _check(lib().moe_permute_map_e4m3(ctypes.byref(cfg), _p(x), _p(routing_map), _p(topk_idx),
+                                      _p(keep), _p(x_perm_q), _p(x_perm_scale), _p(row_map),
+                                      _p(expert_offsets), w, wb, _stream()),
+           "moe_permute_map_e4m3")
 
 
 def permute_e4m3(cfg, x, topk_idx, keep, x_perm_q, x_perm_scale, row_map, expert_offsets, ws):

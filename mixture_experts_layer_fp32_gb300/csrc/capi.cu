@@ -246,7 +246,8 @@ moe_status do_permute_map(const moe_config& c, const void* x, const uint8_t* map
                           const int32_t* topk_idx, const uint8_t* keep, void* x_perm,
                           int32_t* row_map, int32_t* offsets, void* ws, cudaStream_t s) {
   const Layout L = make_layout(c);
-  MOE_CUDA(launch_perm_by_map(c.num_tokens, c.hidden, c.num_experts, c.topk, c.dtype, rows_of(c),
+  const int row_bytes = c.hidden * (c.dtype == MOE_F32 ? 4 : 2);
+  MOE_CUDA(launch_perm_by_map(c.num_tokens, row_bytes, c.num_experts, c.topk, rows_of(c),
                               x, map, topk_idx, keep, at<int32_t>(ws, L.map_tiles),
                               at<int32_t>(ws, L.row_src), x_perm, row_map, offsets,
                               at<int>(ws, L.err), s));
@@ -384,11 +385,12 @@ moe_status side_stream(SideStream** out) {
 // output), then the permuted codes [T*k,h] and their row scales [T*k], the
 // SwiGLU codes [T*k,f] and scales.
 struct E4m3Layout {
-  size_t xperm_q, xperm_s, hq, hs, total;
+  size_t xperm_q, xperm_s, hq, hs, xq_tok, xs_tok, total;
 };
 E4m3Layout make_e4m3_layout(const moe_config& c) {
   E4m3Layout Q;
-  const size_t T = c.num_tokens, np = T * c.topk, h = c.hidden, f = c.ffn_hidden;
+  const size_t T = c.num_tokens, np = static_cast<size_t>(rows_of(c)), h = c.hidden,
+               f = c.ffn_hidden;
   size_t o = make_layout(c).total;
   auto take = [&](size_t bytes) {
     const size_t r = o;
@@ -399,13 +401,15 @@ E4m3Layout make_e4m3_layout(const moe_config& c) {
   Q.xperm_s = take(np * 4);
   Q.hq = take(np * f);
   Q.hs = take(np * 4);
+  // pad_to_capacity: x quantised once per token, then gathered by the map
+  Q.xq_tok = take(c.pad_to_capacity ? T * h : 0);
+  Q.xs_tok = take(c.pad_to_capacity ? T * 4 : 0);
   Q.total = o;
   return Q;
 }
 
 moe_status validate_e4m3(const moe_config& c) {
-  // bf16 in/out, E4M3 experts; the padded layout is not built for them
-  return c.dtype == MOE_BF16 && !c.pad_to_capacity ? MOE_OK : MOE_ERR_UNSUPPORTED;
+  return c.dtype == MOE_BF16 ? MOE_OK : MOE_ERR_UNSUPPORTED;  // bf16 in/out, E4M3 experts
 }
 
 // E4M3 permute: quantise x per token, rank the pairs, copy code rows and scales.
@@ -427,6 +431,26 @@ moe_status do_permute_e4m3(const moe_config& c, const void* x, const int32_t* to
   return MOE_OK;
 }
 
+// E4M3 permutation by a routing map (pad_to_capacity): every token's row
+// quantised once, the code rows gathered by the map, their scales after them.
+moe_status do_permute_map_e4m3(const moe_config& c, const void* x, const uint8_t* map,
+                               const int32_t* topk_idx, const uint8_t* keep, uint8_t* xperm_q,
+                               float* xperm_s, int32_t* row_map, int32_t* offsets, void* ws,
+                               cudaStream_t s) {
+  const Layout L = make_layout(c);
+  const E4m3Layout Q = make_e4m3_layout(c);
+  uint8_t* xq_tok = at<uint8_t>(ws, Q.xq_tok);
+  float* xs_tok = at<float>(ws, Q.xs_tok);
+  int32_t* row_src = at<int32_t>(ws, L.row_src);
+  const int64_t rows = rows_of(c);
+  MOE_CUDA(launch_quantize_rows(c.num_tokens, c.hidden, x, xq_tok, xs_tok, nullptr, s));
+  MOE_CUDA(launch_perm_by_map(c.num_tokens, c.hidden, c.num_experts, c.topk, rows, xq_tok, map,
+                              topk_idx, keep, at<int32_t>(ws, L.map_tiles), row_src, xperm_q,
+                              row_map, offsets, at<int>(ws, L.err), s));
+  MOE_CUDA(launch_gather_scales(rows, offsets + c.num_experts, row_src, xs_tok, xperm_s, s));
+  return MOE_OK;
+}
+
 // E4M3 experts: fc1 (scaled, SwiGLU, bf16 h_mid), per-row quantisation of the
 // rows that exist (expert_offsets[E] on the device), fc2 (scaled, fp32).
 moe_status do_mlp_e4m3(const moe_config& c, const uint8_t* xperm_q, const float* xperm_s,
@@ -436,7 +460,7 @@ moe_status do_mlp_e4m3(const moe_config& c, const uint8_t* xperm_q, const float*
                        cudaStream_t s) {
   const Layout L = make_layout(c);
   int* err = at<int>(ws, L.err);
-  const int64_t rows = static_cast<int64_t>(c.num_tokens) * c.topk;
+  const int64_t rows = rows_of(c);
   const int E = c.num_experts, h = c.hidden, f = c.ffn_hidden;
   MOE_CUDA(launch_tc_fc1_e4m3(E, h, f, rows, xperm_q, xperm_s, nullptr, offsets, W1q, s1, W3q,
                               s3, h_mid, err, s));
@@ -769,13 +793,18 @@ moe_status e4m3_forward_body(const moe_config& c, const void* x, const float* Wg
   int32_t* row_map = at<int32_t>(ws, L.row_map);
   uint8_t* xperm_q = at<uint8_t>(ws, Q.xperm_q);
   float* xperm_s = at<float>(ws, Q.xperm_s);
-  MOE_TRY(do_route(c, x, Wg, gate_bias, expert_bias, idx, prob, keep, tpe, nullptr, ws, stream));
-  MOE_TRY(do_permute_e4m3(c, x, idx, keep, xperm_q, xperm_s, row_map, offsets, ws, stream));
+  uint8_t* map = c.pad_to_capacity ? at<uint8_t>(ws, L.map) : nullptr;
+  MOE_TRY(do_route(c, x, Wg, gate_bias, expert_bias, idx, prob, keep, tpe, map, ws, stream));
+  if (map)
+    MOE_TRY(do_permute_map_e4m3(c, x, map, idx, keep, xperm_q, xperm_s, row_map, offsets, ws,
+                                stream));
+  else
+    MOE_TRY(do_permute_e4m3(c, x, idx, keep, xperm_q, xperm_s, row_map, offsets, ws, stream));
   MOE_TRY(do_mlp_e4m3(c, xperm_q, xperm_s, offsets, W1q, s1, W3q, s3, W2q, s2,
                       at<void>(ws, L.h_mid), at<uint8_t>(ws, Q.hq), at<float>(ws, Q.hs),
                       at<float>(ws, L.y_perm), ws, stream));
   MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, at<float>(ws, L.y_perm),
-                          row_map, prob, nullptr, y, stream));
+                          row_map, prob, nullptr, y, stream, rows_of(c)));
   return MOE_OK;
 }
 
@@ -1137,6 +1166,7 @@ moe_status moe_permute_e4m3(const moe_config* cfg, const void* x, const int32_t*
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
   MOE_TRY(validate_e4m3(c));
+  if (c.pad_to_capacity) return MOE_ERR_INVALID_ARG;  // padding rows come from the map
   const size_t T = c.num_tokens, k = c.topk;
   MOE_TRY(need(x, T * c.hidden, 16));
   MOE_TRY(need(topk_idx, T * k, 4));
@@ -1150,6 +1180,29 @@ moe_status moe_permute_e4m3(const moe_config* cfg, const void* x, const int32_t*
                          ws, stream);
 }
 
+moe_status moe_permute_map_e4m3(const moe_config* cfg, const void* x, const uint8_t* routing_map,
+                                const int32_t* topk_idx, const uint8_t* keep, uint8_t* x_perm_q,
+                                float* x_perm_scale, int32_t* row_map, int32_t* expert_offsets,
+                                void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_e4m3(c));
+  if (!c.pad_to_capacity) return MOE_ERR_INVALID_ARG;  // its token scratch is the padded layout's
+  const size_t T = c.num_tokens, k = c.topk, E = c.num_experts;
+  const size_t R = static_cast<size_t>(rows_of(c));
+  MOE_TRY(need(x, T * c.hidden, 16));
+  MOE_TRY(need(routing_map, T * E, 1));
+  MOE_TRY(need(topk_idx, T * k, 4));
+  MOE_TRY(optional(keep, 1));
+  MOE_TRY(need(x_perm_q, R * c.hidden, 16));
+  MOE_TRY(need(x_perm_scale, R, 4));
+  MOE_TRY(need(row_map, T * k, 4));
+  MOE_TRY(need(expert_offsets, E + 1, 4));
+  MOE_TRY(check_ws(c, ws, ws_bytes, make_e4m3_layout(c).total));
+  return do_permute_map_e4m3(c, x, routing_map, topk_idx, keep, x_perm_q, x_perm_scale, row_map,
+                             expert_offsets, ws, stream);
+}
+
 moe_status moe_grouped_mlp_e4m3(const moe_config* cfg, const uint8_t* x_perm_q,
                                 const float* x_perm_scale, const int32_t* expert_offsets,
                                 const uint8_t* W1q, const float* s1, const uint8_t* W3q,
@@ -1159,7 +1212,7 @@ moe_status moe_grouped_mlp_e4m3(const moe_config* cfg, const uint8_t* x_perm_q,
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
   MOE_TRY(validate_e4m3(c));
-  const size_t R = static_cast<size_t>(c.num_tokens) * c.topk, E = c.num_experts;
+  const size_t R = static_cast<size_t>(rows_of(c)), E = c.num_experts;
   const size_t h = c.hidden, f = c.ffn_hidden, wsz = E * h * f;
   MOE_TRY(need(x_perm_q, R * h, 16));
   MOE_TRY(need(x_perm_scale, R, 4));
@@ -1187,7 +1240,7 @@ moe_status moe_grouped_fc1_e4m3(const moe_config* cfg, const uint8_t* x_perm_q,
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
   MOE_TRY(validate_e4m3(c));
-  const size_t R = static_cast<size_t>(c.num_tokens) * c.topk, E = c.num_experts;
+  const size_t R = static_cast<size_t>(rows_of(c)), E = c.num_experts;
   const size_t h = c.hidden, f = c.ffn_hidden, wsz = E * h * f;
   MOE_TRY(need(x_perm_q, R * h, 16));
   MOE_TRY(need(x_perm_scale, R, 4));
@@ -1212,7 +1265,7 @@ moe_status moe_grouped_fc2_e4m3(const moe_config* cfg, const void* h_mid,
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
   MOE_TRY(validate_e4m3(c));
-  const size_t R = static_cast<size_t>(c.num_tokens) * c.topk, E = c.num_experts;
+  const size_t R = static_cast<size_t>(rows_of(c)), E = c.num_experts;
   const size_t h = c.hidden, f = c.ffn_hidden;
   MOE_TRY(need(h_mid, R * f, 16));
   MOE_TRY(need(expert_offsets, E + 1, 4));

@@ -66,15 +66,20 @@ cudaError_t launch_router_topk(int T, int E, int k, int score, int num_groups, i
                                int32_t* topk_idx, float* topk_prob,
                                uint8_t* keep, uint8_t* routing_map, int32_t* counts, int* err,
                                cudaStream_t s);
-// Permutation by a [T,E] routing map (pad_to_capacity): tile_counts holds
-// map_tiles(T) x E ints, row_src max_rows ints; offsets [E+1] out; rows past
-// max_rows are reported in err and not written.
+// Permutation by a [T,E] routing map (pad_to_capacity): x rows of row_bytes
+// (a multiple of 16) each; tile_counts holds map_tiles(T) x E ints, row_src
+// max_rows ints; offsets [E+1] out; rows past max_rows are reported in err
+// and not written.
 int64_t map_tiles(int T);
-cudaError_t launch_perm_by_map(int T, int h, int E, int k, int dtype, int64_t max_rows,
+cudaError_t launch_perm_by_map(int T, int row_bytes, int E, int k, int64_t max_rows,
                                const void* x, const uint8_t* map, const int32_t* topk_idx,
                                const uint8_t* keep, int32_t* tile_counts, int32_t* row_src,
                                void* x_perm, int32_t* row_map, int32_t* offsets, int* err,
                                cudaStream_t s);
+// dst[r] = src[row_src[r]] for the rows of a map permutation (E4M3 scales)
+cudaError_t launch_gather_scales(int64_t max_rows, const int32_t* total_rows,
+                                 const int32_t* row_src, const float* src, float* dst,
+                                 cudaStream_t s);
 // pad_to_capacity: fill each expert's column of the routing map up to quota
 // ones with the lowest-index tokens not routed to it (cand_off / cand_pair:
 // the drop candidate lists; NULL when nothing is dropped: every token);

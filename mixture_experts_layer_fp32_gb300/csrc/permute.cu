@@ -712,6 +712,18 @@ __device__ __forceinline__ int warp_lower_bound(const int32_t* __restrict__ cand
   return lo + __popc(__ballot_sync(0xffffffffu, below));
 }
 
+// dst[r] = src[row_src[r]] for rows [0, min(offsets[E], max_rows)): the
+// E4M3 rows' scales after a permutation by the map
+__global__ void __launch_bounds__(256)
+    perm_gather_scale_kernel(int64_t max_rows, const int32_t* __restrict__ total_rows,
+                             const int32_t* __restrict__ row_src, const float* __restrict__ src,
+                             float* __restrict__ dst) {
+  const int64_t R = min(static_cast<int64_t>(*total_rows), max_rows);
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < R;
+       r += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[r] = src[row_src[r]];
+}
+
 // Expert blockIdx.y's column of the routing map, tokens [t0, t0 + 256): an
 // expert under capacity kept all of its m routed pairs (the candidate pairs
 // cand_pair[cand_off[e] ..], ascending), so it needs quota - m padding
@@ -837,7 +849,7 @@ cudaError_t launch_perm_copy(int T, int h, int k, int dtype, const void* x, cons
 
 int64_t map_tiles(int T) { return (static_cast<int64_t>(T) + kMapTile - 1) / kMapTile; }
 
-cudaError_t launch_perm_by_map(int T, int h, int E, int k, int dtype, int64_t max_rows,
+cudaError_t launch_perm_by_map(int T, int row_bytes, int E, int k, int64_t max_rows,
                                const void* x, const uint8_t* map, const int32_t* topk_idx,
                                const uint8_t* keep, int32_t* tile_counts, int32_t* row_src,
                                void* x_perm, int32_t* row_map, int32_t* offsets, int* err,
@@ -855,10 +867,21 @@ cudaError_t launch_perm_by_map(int T, int h, int E, int k, int dtype, int64_t ma
       T, E, k, max_rows, map, topk_idx, keep, tile_counts, row_map, row_src, err);
   st = cudaGetLastError();
   if (st != cudaSuccess) return st;
-  const int row_vecs = h * (dtype == MOE_F32 ? 4 : 2) / 16;
+  const int row_vecs = row_bytes / 16;
   perm_gather_kernel<<<device_sm_count() * 8, kCopyThreads, 0, s>>>(
       max_rows, row_vecs, offsets + E, row_src, static_cast<const uint4*>(x),
       static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_scales(int64_t max_rows, const int32_t* total_rows,
+                                 const int32_t* row_src, const float* src, float* dst,
+                                 cudaStream_t s) {
+  int64_t grid = (max_rows + 255) / 256;
+  if (grid > 8LL * device_sm_count()) grid = 8LL * device_sm_count();
+  if (grid < 1) return cudaSuccess;
+  perm_gather_scale_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(max_rows, total_rows,
+                                                                        row_src, src, dst);
   return cudaGetLastError();
 }
 

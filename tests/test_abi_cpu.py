@@ -293,9 +293,16 @@ def test_pad_to_capacity_configuration(moe):
                                    pad_to_capacity=True)) == 8 * 100
     assert moe.max_rows(moe.config(T=1000, h=256, E=8, k=2, f=128, capacity_factor=0.5,
                                    pad_to_capacity=True)) == 2000
-    # the E4M3 path is not built for it; the backward's buffers hold the padded rows
+    # the E4M3 and backward buffers hold the padded rows
     cfg = moe.config(T=128, h=4096, E=8, k=2, f=1536, capacity_factor=1.0, pad_to_capacity=True)
-    assert _status(moe, "moe_workspace_size_e4m3", _cfgp(cfg), ctypes.byref(size)) == UNSUPPORTED
+    assert _status(moe, "moe_workspace_size_e4m3", _cfgp(cfg), ctypes.byref(size)) == OK
+    e4m3_need = size.value
+    # the E4M3 pair permutation refuses padding; its map permutation needs it
+    assert lib.moe_permute_e4m3(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                FAKE, e4m3_need, None) == INVALID
+    plain = moe.config(T=128, h=4096, E=8, k=2, f=1536, capacity_factor=1.0)
+    assert lib.moe_permute_map_e4m3(ctypes.byref(plain), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                    FAKE, FAKE, FAKE, e4m3_need, None) == INVALID
     assert _status(moe, "moe_workspace_size_backward", _cfgp(cfg), ctypes.byref(size)) == OK
     padded = size.value
     cfg.pad_to_capacity = 0

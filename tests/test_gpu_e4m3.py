@@ -75,6 +75,11 @@ CASES = {
     "qwen3_sparse": synthetic.scaled("qwen3", T=300, h=256, f=256, seed=133),
     "switch_drop": synthetic.scaled("switch", T=2048, h=256, f=256, seed=134),
     "dsv3_grouped": synthetic.scaled("dsv3_grouped", T=400, h=512, f=256, E=64, seed=135),
+    # pad_to_capacity: x quantised per token, code rows and scales placed by the padded map
+    "switch_pad": synthetic.scaled("switch", T=2048, h=256, f=256, seed=136,
+                                   pad_to_capacity=True),
+    "top2_pad": synthetic.scaled("mixtral", T=600, h=512, f=384, E=4, capacity_factor=1.0,
+                                 gate_bias="hot:1:2", seed=137, pad_to_capacity=True),
 }
 
 
@@ -83,7 +88,8 @@ def oracle_forward_e4m3(w, inp):
     return oracle.forward_fp8(_bits(inp["x"]), _bits(inp["Wg"]), q, w.k, w.score,
                               np_view(inp["gate_bias"]), np_view(inp["expert_bias"]),
                               w.capacity_factor, w.min_capacity, w.drop_policy,
-                              num_groups=w.num_groups, group_topk=w.group_topk)
+                              num_groups=w.num_groups, group_topk=w.group_topk,
+                              pad_to_capacity=w.pad_to_capacity)
 
 
 def gpu_stages_e4m3(w, d):
@@ -92,15 +98,19 @@ def gpu_stages_e4m3(w, d):
     b = moe.Buffers(cfg)
     ws = moe.alloc_workspace_e4m3(cfg)
     q = moe.E4m3Experts(cfg, d["W1"], d["W3"], d["W2"])
-    R = w.T * w.k
+    R = moe.max_rows(cfg)
     b.x_perm_q = torch.empty((R, w.h), dtype=torch.uint8, device="cuda")
     b.x_perm_s = torch.empty((R,), dtype=torch.float32, device="cuda")
     b.h_q = torch.empty((R, w.f), dtype=torch.uint8, device="cuda")
     b.h_s = torch.empty((R,), dtype=torch.float32, device="cuda")
     moe.route(cfg, d["x"], d["Wg"], d["gate_bias"], d["expert_bias"], b.topk_idx, b.topk_prob,
-              b.keep, b.tokens_per_expert, None, ws)
-    moe.permute_e4m3(cfg, d["x"], b.topk_idx, b.keep, b.x_perm_q, b.x_perm_s, b.row_map,
-                     b.expert_offsets, ws)
+              b.keep, b.tokens_per_expert, b.routing_map if w.pad_to_capacity else None, ws)
+    if w.pad_to_capacity:
+        moe.permute_map_e4m3(cfg, d["x"], b.routing_map, b.topk_idx, b.keep, b.x_perm_q,
+                             b.x_perm_s, b.row_map, b.expert_offsets, ws)
+    else:
+        moe.permute_e4m3(cfg, d["x"], b.topk_idx, b.keep, b.x_perm_q, b.x_perm_s, b.row_map,
+                         b.expert_offsets, ws)
     moe.grouped_mlp_e4m3(cfg, b.x_perm_q, b.x_perm_s, b.expert_offsets, q, b.h_mid, b.h_q,
                          b.h_s, b.y_perm, ws)
     moe.combine(cfg, b.y_perm, b.row_map, b.topk_prob, b.y)
