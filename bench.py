@@ -472,7 +472,9 @@ def run_native(args, rank, world, local):
                 "bound": "tensor", "achieved": stages[dom]["tflops"],
                 "peak": ratio * peaks["bf16_tflops"], "unit": "TFLOP/s"}
     elif gemm_hbm_bound:
-        roof = {"kernel": gemm_kernel_name(w, w.T * w.k, dom) + ("[E4M3]" if fp8 else ""),
+        name = gemm_kernel_name(w, w.T * w.k, dom) if w.dtype == "bf16" else \
+            "simt_grouped_kernel<%s>" % ("FC1" if dom == "fc1" else "FC2")
+        roof = {"kernel": name + ("[E4M3]" if fp8 else ""),
                 "bound": "hbm", "achieved": stages[dom].get("gbs"),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "tensor_frac": stages[dom]["tflops"] / ((2.0 if fp8 else 1.0) * peaks["bf16_tflops"])}
