@@ -70,10 +70,15 @@ constexpr int ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int THREADS = 192;
 constexpr int NUM_BARS = 2 * STAGES + 5;     // full, empty, acc_full[2], acc_empty[2], drain
-// fc2 epilogue staging: per epilogue warp a 32 x 32 fp32 tile with rows padded
-// to 36 floats (16-byte accesses of a quarter-warp hit distinct banks).
+// fp32-output epilogue staging, per epilogue warp a 5 KB region (1 KB
+// aligned): a 32 x 32 fp32 block in the 128-byte swizzle that a TMA store
+// reads, or, for a warp whose rows cross the expert's end, a 32 x 32 tile
+// with rows padded to 36 floats for masked row-segment stores (16-byte
+// accesses of a quarter-warp hit distinct banks).
 constexpr int EPI_PITCH = 36;
-constexpr int EPI_BYTES = 4 * 32 * EPI_PITCH * 4;
+constexpr int EPI_WARP_BYTES = 5120;
+constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
+static_assert(32 * EPI_PITCH * 4 <= EPI_WARP_BYTES && 4096 <= EPI_WARP_BYTES, "staging");
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16 +
                            2 * (MOE_MAX_EXPERTS + 1) * 4;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -122,6 +127,10 @@ struct TcArgs {
   int kb_split = 0;
   // DGRAD_F32: add to the output instead of overwriting it
   int accumulate = 0;
+  // FC2 / DGRAD_F32 without accumulate: fp32 output rows stored by TMA
+  // through the output tensor map (32 x 32 boxes) when a warp's 32 rows all
+  // belong to the tile's expert
+  int tma_out = 0;
 };
 
 // Barriers of an NS-stage ring: full[NS], empty[NS], acc_full[2],
@@ -246,8 +255,15 @@ __device__ __forceinline__ float silu_mul(float a, float g) { return a / (1.0f +
 // `tb` hold rows rbase .. rbase+31 (lane l holds row rbase + l) of a tile of
 // n-tile `nt`; rows at or past `rend` belong to no row of this expert and are
 // not stored.  fc1 applies silu(a) * g and stores bf16, fc2 stores fp32.
+__device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+
 template <int MODE, bool FP8>
-__device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, int rbase, int rend,
+__device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, uint32_t stg,
+                                                  const CUtensorMap* tmC, int rbase, int rend,
                                                   int nt, int e, const TcArgs& args, int lane) {
   const int sub = lane >> 3;
   const int col4 = (lane & 7) * 4;
@@ -374,6 +390,49 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, int
       }
     }
   } else {
+    // the warp's staging region is free once its last TMA store has read it
+    if (args.tma_out) {
+      if (lane == 0) ptx::bulk_wait_group_read<0>();
+      __syncwarp();
+    }
+    if (args.tma_out && !(MODE == DGRAD_F32 && args.accumulate) && rbase + 32 <= rend) {
+      // every row of the warp is the expert's: 32 x 32 blocks in the
+      // 128-byte swizzle (16-byte chunk j of row l at chunk j ^ (l & 7)),
+      // one TMA store each from lane 0
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t y[32];
+        ptx::tmem_ld32(tb + c, y);
+        ptx::tmem_wait_ld();
+        if (FP8) {  // acc * row scale * channel scale
+          const float* cs = args.col_scale0 + static_cast<int64_t>(e) * args.ncols + nt * BN + c;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const float4 u = __ldg(reinterpret_cast<const float4*>(cs + 4 * v));
+            y[4 * v] = __float_as_uint(__uint_as_float(y[4 * v]) * (rs * u.x));
+            y[4 * v + 1] = __float_as_uint(__uint_as_float(y[4 * v + 1]) * (rs * u.y));
+            y[4 * v + 2] = __float_as_uint(__uint_as_float(y[4 * v + 2]) * (rs * u.z));
+            y[4 * v + 3] = __float_as_uint(__uint_as_float(y[4 * v + 3]) * (rs * u.w));
+          }
+        }
+        if (c > 0) {
+          if (lane == 0) ptx::bulk_wait_group_read<0>();
+          __syncwarp();
+        }
+        const uint32_t row = stg + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_shared_v4(row + ((j ^ (lane & 7)) << 4), y[4 * j], y[4 * j + 1], y[4 * j + 2],
+                       y[4 * j + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(tmC, nt * BN + c, rbase, stg);
+          ptx::bulk_commit_group();
+        }
+      }
+      return;
+    }
     // Stage the warp's 32 rows x 32 columns in shared memory, then store
     // them by row segments: lanes 8s..8s+7 write the 128 contiguous bytes
     // of one row, 4 rows per instruction (full lines, not one 16-byte
@@ -425,7 +484,8 @@ template <int MODE, bool FP8>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB0,
-                      const __grid_constant__ CUtensorMap tmB1, TcArgs args) {
+                      const __grid_constant__ CUtensorMap tmB1,
+                      const __grid_constant__ CUtensorMap tmC, TcArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -627,13 +687,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
-      float* etile = epi + q * (32 * EPI_PITCH);  // this warp's staging tile
+      float* etile = epi + q * (EPI_WARP_BYTES / 4);  // this warp's staging region
+      const uint32_t stg = ptx::smem_u32(etile);
       const int rbase = m0 + q * 32;  // this warp's first row; lane l holds row rbase + l
-      drain_accumulator<MODE, FP8>(tb, etile, rbase, rend, nt, e, args, lane);
+      drain_accumulator<MODE, FP8>(tb, etile, stg, &tmC, rbase, rend, nt, e, args, lane);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ctl.acc_empty(buf));
     }
+    if (args.tma_out && lane == 0) ptx::bulk_wait_group_all();  // the stores have completed
   }
   __syncthreads();
   if (warp == 1) {
@@ -683,7 +745,8 @@ template <int MODE, bool FP8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_grouped_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB0,
-                           const __grid_constant__ CUtensorMap tmB1, TcArgs args) {
+                           const __grid_constant__ CUtensorMap tmB1,
+                           const __grid_constant__ CUtensorMap tmC, TcArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -883,13 +946,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * ACC_COLS;
-      float* etile = epi + q * (32 * EPI_PITCH);
+      float* etile = epi + q * (EPI_WARP_BYTES / 4);
+      const uint32_t stg = ptx::smem_u32(etile);
       const int rbase = m0 + static_cast<int>(rank) * BM + q * 32;
-      drain_accumulator<MODE, FP8>(tb, etile, rbase, rend, nt, e, args, lane);
+      drain_accumulator<MODE, FP8>(tb, etile, stg, &tmC, rbase, rend, nt, e, args, lane);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa_shared(ctl.acc_empty(buf), 0));
     }
+    if (args.tma_out && lane == 0) ptx::bulk_wait_group_all();  // the stores have completed
   }
   __syncthreads();
   ptx::cluster_sync();  // no cross-CTA access after this point
@@ -989,9 +1054,36 @@ bool map_weights_kmajor(CUtensorMap* m, const void* ptr, int64_t K, int64_t N, i
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 output [rows, N] with row stride ld floats, box 32 (N) x 32 (rows),
+// 128-byte swizzle: the epilogue's TMA stores.  False when the layout cannot
+// be stored by TMA (stride or base not 16-byte aligned).
+bool map_out_f32(CUtensorMap* m, float* ptr, int64_t N, int64_t ld, int64_t rows) {
+  if (ld % 4 != 0 || (reinterpret_cast<uintptr_t>(ptr) & 15) != 0 || N % 32 != 0) return false;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Sets args->tma_out and fills *c when the fp32 output [max_rows, N] (row
+// stride args->ldo) can be stored by TMA; MOE_TC_TMA_OUT=0 in the
+// environment keeps the row-segment stores (a tuning override).
+void setup_tma_out(CUtensorMap* c, TcArgs* args, int64_t N) {
+  const char* force = getenv("MOE_TC_TMA_OUT");
+  if (force && force[0] == '0') return;
+  if (args->accumulate) return;
+  if (map_out_f32(c, static_cast<float*>(args->out), N, args->ldo, args->max_rows))
+    args->tma_out = 1;
+}
+
 template <int MODE, bool FP8>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                      const TcArgs& args, cudaStream_t s) {
+                      const CUtensorMap& c, const TcArgs& args, cudaStream_t s) {
   static bool configured[64] = {false};
   int dev = 0;
   cudaError_t st = cudaGetDevice(&dev);
@@ -1006,7 +1098,7 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   int64_t grid = device_sm_count();
   if (grid > max_tiles) grid = max_tiles;
   if (grid <= 0) return cudaSuccess;
-  tc_grouped_kernel<MODE, FP8><<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, s>>>(a, b0, b1,
+  tc_grouped_kernel<MODE, FP8><<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, s>>>(a, b0, b1, c,
                                                                                      args);
   return cudaGetLastError();
 }
@@ -1040,13 +1132,13 @@ int pair_slots() {
 
 template <int MODE, bool FP8>
 cudaError_t launch_tc_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                           const TcArgs& args, int slots, cudaStream_t s) {
+                           const CUtensorMap& c, const TcArgs& args, int slots, cudaStream_t s) {
   const int64_t max_tiles = ((args.max_rows + PM - 1) / PM + args.E) * args.num_n_tiles;
   int64_t pairs = slots;
   if (pairs > max_tiles) pairs = max_tiles;
   if (pairs <= 0) return cudaSuccess;
   tc_grouped_pair_kernel<MODE, FP8><<<static_cast<unsigned>(2 * pairs), THREADS, P_SMEM_BYTES, s>>>(
-      a, b0, b1, args);
+      a, b0, b1, c, args);
   return cudaGetLastError();
 }
 
@@ -1058,16 +1150,16 @@ constexpr int64_t kPairMinRows = 768;
 
 template <int MODE, bool FP8>
 cudaError_t launch_grouped(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                           const TcArgs& args, cudaStream_t s) {
+                           const CUtensorMap& c, const TcArgs& args, cudaStream_t s) {
   const char* force = getenv("MOE_TC_PAIR");
   bool pair = args.max_rows >= static_cast<int64_t>(args.E) * kPairMinRows;
   if (force && force[0] == '0') pair = false;
   if (force && force[0] == '1') pair = true;
   if (pair) {
     const int slots = pair_slots<MODE, FP8>();
-    if (slots > 0) return launch_tc_pair<MODE, FP8>(a, b0, b1, args, slots, s);
+    if (slots > 0) return launch_tc_pair<MODE, FP8>(a, b0, b1, c, args, slots, s);
   }
-  return launch_tc<MODE, FP8>(a, b0, b1, args, s);
+  return launch_tc<MODE, FP8>(a, b0, b1, c, args, s);
 }
 
 }  // namespace
@@ -1081,7 +1173,7 @@ cudaError_t launch_tc_fc1(int E, int h, int f, int64_t max_rows, const void* x_p
       !map_weights(&b1, W3, f, h, E))
     return cudaErrorInvalidValue;
   TcArgs args{offsets, E, f / (BN / 2), h / BK, max_rows, h_mid, f, err};
-  return launch_grouped<FC1, false>(a, b0, b1, args, s);
+  return launch_grouped<FC1, false>(a, b0, b1, a, args, s);
 }
 
 cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_mid,
@@ -1092,7 +1184,9 @@ cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_m
   if (!map_rows(&a, h_mid, f, max_rows) || !map_weights(&b0, W2, h, f, E))
     return cudaErrorInvalidValue;
   TcArgs args{offsets, E, h / BN, f / BK, max_rows, y_perm, h, err};
-  return launch_grouped<FC2, false>(a, b0, b0, args, s);
+  CUtensorMap c = a;
+  setup_tma_out(&c, &args, h);
+  return launch_grouped<FC2, false>(a, b0, b0, c, args, s);
 }
 
 // ---- backward GEMMs (bf16 operands, 64-wide K stages; SM pairs by the
@@ -1109,7 +1203,7 @@ cudaError_t launch_tc_dgrad_fc2(int E, int h, int f, int64_t max_rows, const voi
   // f % 128 == 0: the last 256-column tile may hold only 128 valid columns
   TcArgs args{offsets, E, (f + BN - 1) / BN, h / BK, max_rows, dH, f, err};
   args.ncols = f;
-  return launch_grouped<DGRAD_BF16, false>(a, b0, b0, args, s);
+  return launch_grouped<DGRAD_BF16, false>(a, b0, b0, a, args, s);
 }
 
 cudaError_t launch_tc_fc1_bwd(int E, int h, int f, int64_t max_rows, const void* x_perm,
@@ -1125,7 +1219,7 @@ cudaError_t launch_tc_fc1_bwd(int E, int h, int f, int64_t max_rows, const void*
   args.aux = dH;
   args.ldaux = f;
   args.ncols = f;
-  return launch_grouped<FC1_BWD, false>(a, b0, b1, args, s);
+  return launch_grouped<FC1_BWD, false>(a, b0, b1, a, args, s);
 }
 
 cudaError_t launch_tc_dgrad_fc1(int E, int h, int f, int64_t max_rows, const void* dA,
@@ -1140,7 +1234,9 @@ cudaError_t launch_tc_dgrad_fc1(int E, int h, int f, int64_t max_rows, const voi
   TcArgs args{offsets, E, h / BN, 2 * f / BK, max_rows, dX, h, err};
   args.kb_split = f / BK;
   args.accumulate = accumulate ? 1 : 0;
-  return launch_grouped<DGRAD_F32, false>(a, b0, b1, args, s);
+  CUtensorMap c = a;
+  setup_tma_out(&c, &args, h);
+  return launch_grouped<DGRAD_F32, false>(a, b0, b1, c, args, s);
 }
 
 // C [rows, N] fp32 (row stride ldc) = A [rows, K] . Bk [N, K]^T, bf16
@@ -1157,7 +1253,9 @@ cudaError_t launch_tc_dense_nt_f32(int64_t rows, int K, int N, const void* A, co
     return cudaErrorInvalidValue;
   TcArgs args{nullptr, 1, N / BN, K / BK, rows, C, ldc, err};
   args.kb_split = K / BK;
-  return launch_grouped<DGRAD_F32, false>(a, b0, b0, args, s);
+  CUtensorMap c = a;
+  setup_tma_out(&c, &args, N);
+  return launch_grouped<DGRAD_F32, false>(a, b0, b0, c, args, s);
 }
 
 cudaError_t launch_tc_fc1_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* xq,
@@ -1176,7 +1274,7 @@ cudaError_t launch_tc_fc1_e4m3(int E, int h, int f, int64_t max_rows, const uint
   args.col_scale0 = s1;
   args.col_scale1 = s3;
   args.ncols = f;
-  return launch_grouped<FC1, true>(a, b0, b1, args, s);
+  return launch_grouped<FC1, true>(a, b0, b1, a, args, s);
 }
 
 cudaError_t launch_tc_fc2_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* hq,
@@ -1190,7 +1288,9 @@ cudaError_t launch_tc_fc2_e4m3(int E, int h, int f, int64_t max_rows, const uint
   args.row_scale = h_scale;
   args.col_scale0 = s2;
   args.ncols = h;
-  return launch_grouped<FC2, true>(a, b0, b0, args, s);
+  CUtensorMap c = a;
+  setup_tma_out(&c, &args, h);
+  return launch_grouped<FC2, true>(a, b0, b0, c, args, s);
 }
 
 }  // namespace moe
