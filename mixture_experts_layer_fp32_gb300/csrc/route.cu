@@ -566,18 +566,36 @@ __global__ void __launch_bounds__(256)
   const int nwarps = blockDim.x >> 5;
   const int per_group = num_groups > 1 ? E / num_groups : E;
   for (int t = blockIdx.x * nwarps + warp; t < T; t += gridDim.x * nwarps) {
-    // logits = (partial sums in split order) + gate bias
+    // logits = (partial sums in split order) + gate bias; the partial sums
+    // are loaded SB splits at a time before they are added, so the loads
+    // overlap instead of waiting on one another (SB = 2 at 8 experts per
+    // lane keeps the batch in registers)
+    constexpr int SB = PL >= 8 ? 2 : 4;
     float s[PL], sel[PL];
 #pragma unroll
     for (int i = 0; i < PL; ++i) {
       const int e = lane + 32 * i;
-      if (e < E) {
-        float l = logits[(int64_t)t * E + e];
-        for (int sp = 1; sp < nsplit; ++sp) l += logits[((int64_t)sp * T + t) * E + e];
-        s[i] = gate_bias ? l + gate_bias[e] : l;
-      } else {
-        s[i] = -FLT_MAX;
-      }
+      s[i] = e < E ? logits[(int64_t)t * E + e] : 0.f;
+    }
+    for (int sp = 1; sp < nsplit; sp += SB) {
+      float v[SB][PL];
+#pragma unroll
+      for (int j = 0; j < SB; ++j)
+#pragma unroll
+        for (int i = 0; i < PL; ++i) {
+          const int e = lane + 32 * i;
+          v[j][i] = (sp + j < nsplit && e < E) ? logits[((int64_t)(sp + j) * T + t) * E + e] : 0.f;
+        }
+#pragma unroll
+      for (int j = 0; j < SB; ++j)
+#pragma unroll
+        for (int i = 0; i < PL; ++i)
+          if (sp + j < nsplit) s[i] += v[j][i];
+    }
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      const int e = lane + 32 * i;
+      s[i] = e < E ? (gate_bias ? s[i] + gate_bias[e] : s[i]) : -FLT_MAX;
     }
     if (score == MOE_SCORE_SOFTMAX_PRE) {
       float m = -FLT_MAX;
