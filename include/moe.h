@@ -469,8 +469,10 @@ moe_status moe_forward_host(const moe_config* cfg, int32_t num_batches, const vo
  *   MOE_ERR_UNSUPPORTED is returned before anything is enqueued.
  *   All calls share the array: calls whose kernels overlap on the GPU race
  *   and corrupt each other; order them (one stream, or events).
- *   The first call on a device looks the array's address up on that device
- *   (it must be the current device); make it before any stream capture.
+ *   Every call looks the array's address up on the current device and keeps
+ *   no copy, so calls stay valid after a cudaDeviceReset.  The first call on
+ *   a device may load the library's device code there: make it before any
+ *   stream capture.
  *   Expert ids outside [0,E) are skipped (row_map -1) without a device
  *   error report.
  */

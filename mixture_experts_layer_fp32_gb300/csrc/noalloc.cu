@@ -18,11 +18,11 @@
 //    no ordering between them) race on the array and corrupt each other;
 //  * expert ids outside [0, E) are skipped (their row_map entry is -1)
 //    without being reported: there is no workspace to hold an error word;
-//  * the first call on a device looks up the array's device address there
-//    (cudaGetSymbolAddress, with that device current).  Make that first call
-//    before any stream capture on the device.
-#include <mutex>
-
+//  * every call looks up the array's address on the current device
+//    (cudaGetSymbolAddress) and keeps no copy of it, so no address survives a
+//    cudaDeviceReset or any other re-creation of the device's context.  The
+//    first call on a device may load the library's device code there, so
+//    make that first call before any stream capture on the device.
 #include "common.cuh"
 
 namespace moe {
@@ -32,29 +32,14 @@ constexpr int64_t kScratchInts = MOE_PERMUTE_NOALLOC_MAX_COUNTERS;  // 256 KB pe
 
 static __device__ __align__(256) int32_t g_perm_scratch[kScratchInts];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-int32_t* g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Device address of g_perm_scratch on the current device (set up once per
-// device).  Returns nullptr and the CUDA error on failure.
+// Device address of g_perm_scratch in the current device's context.  Looked
+// up on every call: a cached address would outlive the context it was read
+// in (a cudaDeviceReset makes a new one) and then point at freed memory.
+// Returns nullptr and the CUDA error on failure.
 int32_t* scratch_on_current_device(cudaError_t* err) {
-  int dev = -1;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= kMaxDevices) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_perm_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    g_scratch_addr[dev] = static_cast<int32_t*>(p);
-  }
-  *err = cudaSuccess;
-  return g_scratch_addr[dev];
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_perm_scratch);
+  return *err == cudaSuccess ? static_cast<int32_t*>(p) : nullptr;
 }
 
 bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }

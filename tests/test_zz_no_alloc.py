@@ -18,9 +18,11 @@ from moe_cases import gpu_config, to_dev
 
 pytestmark = pytest.mark.gpu
 
-# the second case is larger, then smaller again: stale counters from the
-# previous call must not leak into the next
+# sizes go up and down so that stale counters from the previous call would
+# show; the second case has 137 tiles of 2048 pairs (more than 128), so its
+# scan and ranking run as two launches on the fixed array
 CASES = [synthetic.scaled("qwen3", T=1500, h=256, f=128, seed=31),
+         synthetic.scaled("mixtral", T=140000, h=256, f=128, seed=34),
          synthetic.scaled("switch", T=3000, h=256, f=128, seed=32),
          synthetic.scaled("mixtral", T=700, h=256, f=128, seed=33)]
 
