@@ -236,8 +236,12 @@ def stage_work(w, R, fp8=False, active=None):
         "permute": {"bytes": T * h * b + R * h * q + T * k * (4 + 1 + 4)},
         "fc1": {"flops": 4 * R * h * f, "bytes": 2 * A * h * f * q + R * h * q + R * f * b},
         "fc2": {"flops": 2 * R * f * h,
-                "bytes": A * f * h * q + R * f * b + (2 * R * f if fp8 else 0) + R * h * 4},
-        "combine": {"bytes": R * h * 4 + T * h * b + T * k * 8 + (T * h * 4 if w.shared_f else 0)},
+                "bytes": A * f * h * q + R * f * b + (2 * R * f if fp8 else 0) + R * h * 4,
+                "bytes_algorithmic": A * f * h * q + R * f * b + (2 * R * f if fp8 else 0)
+                + R * h * b},
+        "combine": {"bytes": R * h * 4 + T * h * b + T * k * 8 + (T * h * 4 if w.shared_f else 0),
+                    # the scope's algorithmic bytes: y_perm in the activation dtype
+                    "bytes_algorithmic": R * h * b + T * h * b},
         "shared": {"flops": 6 * T * h * w.shared_f,
                    "bytes": 3 * h * w.shared_f * b + T * h * b + 2 * T * w.shared_f * b + T * h * 4},
     }
@@ -449,6 +453,13 @@ def run_native(args, rank, world, local):
             ent["tflops"] = work[s]["flops"] / (t * 1e-3) / 1e12
         if "bytes" in work[s]:
             ent["gbs"] = work[s]["bytes"] / (t * 1e-3) / 1e9
+            if s in ("route", "permute", "combine"):
+                ent["hbm_frac"] = ent["gbs"] / peaks["hbm_gbs"]
+        if "bytes_algorithmic" in work[s]:
+            # y_perm counted in the activation dtype (2 bytes for bf16) although
+            # the library stores it in fp32: the fraction of HBM on those bytes
+            ent["gbs_algorithmic"] = work[s]["bytes_algorithmic"] / (t * 1e-3) / 1e9
+            ent["frac_algorithmic"] = ent["gbs_algorithmic"] / peaks["hbm_gbs"]
         stages[s] = ent
     # the fp32 router GEMM at E >= 64 is bound by the FMA pipe: its fraction of
     # the FMA rate measured in this run (the small-E router is HBM-bound)
@@ -713,11 +724,17 @@ def cpu_baseline(w, inp_cpu, budget_s=15.0):
     n = int(min(w.T, max(4, budget_s / max(per_token, 1e-6))))
     toks = np.sort(rng.choice(w.T, size=n, replace=False))
     sec = oracle_sample_run(w, inp_cpu, toks, cores)
+    # the same oracle on one thread: a smaller sample (about budget_s / 2)
+    n1 = int(min(n, max(2, 0.5 * budget_s / max(per_token * cores, 1e-6))))
+    toks1 = np.sort(rng.choice(w.T, size=n1, replace=False))
+    sec1 = oracle_sample_run(w, inp_cpu, toks1, 1)
     return {"value": n / sec, "unit": UNIT, "cores": cores, "kind": "oracle",
             "cpu": cpu_model(), "seconds": sec,
             "sample": "%d random tokens (fixed seed) of the %s workload; oracle forward (route, "
                       "permute, SwiGLU experts, combine) in double on %d threads"
-                      % (n, w.name, cores)}
+                      % (n, w.name, cores),
+            "one_thread": {"value": n1 / sec1, "unit": UNIT, "cores": 1, "seconds": sec1,
+                           "sample": "%d random tokens of the same workload, one thread" % n1}}
 
 
 def run_reference(args, rank, world):
@@ -742,7 +759,8 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_desc(w),
+            "config": dict(workload_desc(w), parallelism="replicas" if world > 1 else "single",
+                           precision=args.precision),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": desc, "cpu": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
