@@ -184,10 +184,11 @@ void oracle_router_logits(int64_t T, int h, int E, const void* x, int x_dtype,
 // only.  num_groups <= 1 switches grouping off.
 //
 // Outputs: topk_idx [T,k] (slot order = selection score, descending),
-// topk_prob [T,k] fp32, margin [T] = the smaller of (k-th - (k+1)-th
-// selection score among the eligible experts) and, with groups,
-// (group_topk-th - next group score); +inf where there is no next one.
-// The margin is used by the input conditioner, not by the method.
+// topk_prob [T,k] fp32, margin [T] = the smallest gap between consecutive
+// selection scores among the k+1 largest of the eligible experts (so both
+// the chosen set and the slot order of the k chosen are decided by it) and,
+// with groups, (group_topk-th - next group score); +inf where there is no
+// gap.  The margin is used by the input conditioner, not by the method.
 void oracle_topk_scores(int64_t T, int E, int k, int score, int num_groups, int group_topk,
                         const float* logits, const float* expert_bias, int32_t* topk_idx,
                         float* topk_prob, float* margin, int nthreads) {
@@ -248,7 +249,8 @@ void oracle_topk_scores(int64_t T, int E, int k, int score, int num_groups, int 
     for (int j = 0; j < k; ++j) oi[j] = idx[j];
     if (margin) {
       double em = inf;
-      if (k < E && std::isfinite(cand[idx[k]])) em = (double)cand[idx[k - 1]] - (double)cand[idx[k]];
+      for (int j = 0; j + 1 < kk && std::isfinite(cand[idx[j + 1]]); ++j)
+        em = std::min(em, (double)cand[idx[j]] - (double)cand[idx[j + 1]]);
       margin[t] = (float)std::min(em, group_margin);
     }
     if (score == SCORE_SOFTMAX_POST) {

@@ -141,13 +141,16 @@ def test_ties_take_lower_expert_index():
     assert margin[0] == 0.0
 
 
-def test_margin_is_gap_between_kth_and_next():
+def test_margin_is_smallest_gap_among_top_k_plus_one():
+    # the set of k experts and their slot order are both decided by the margin
     logits = rng(35).standard_normal((20, 8)).astype(np.float32)
     _, _, margin = oracle.topk_scores(logits, 3, "softmax_post")
     srt = -np.sort(-logits.astype(np.float64), axis=1)
-    np.testing.assert_allclose(margin, srt[:, 2] - srt[:, 3], rtol=1e-6)
-    _, _, m_all = oracle.topk_scores(logits, 8, "softmax_post")
-    assert np.all(np.isinf(m_all))
+    np.testing.assert_allclose(margin, np.diff(-srt[:, :4], axis=1).min(axis=1), rtol=1e-6)
+    _, _, m_all = oracle.topk_scores(logits, 8, "softmax_post")  # k = E: the order of all 8
+    np.testing.assert_allclose(m_all, np.diff(-srt, axis=1).min(axis=1), rtol=1e-6)
+    _, _, m_one = oracle.topk_scores(logits[:, :1], 1, "softmax_post")  # one expert: no gap
+    assert np.all(np.isinf(m_one))
 
 
 # --------------------------------------------------------------- capacity --
@@ -495,7 +498,8 @@ def test_group_limited_keeps_experts_inside_chosen_groups():
     logits = np.array([[5.0, -9.0, -9.0, -9.0, 4.0, 3.9, -9.0, -9.0]], np.float32)
     idx, prob, margin = oracle.topk_scores(logits, 2, "softmax_post", num_groups=2, group_topk=1)
     assert list(idx[0]) == [4, 5]
-    # next eligible expert is -9 (k-th 3.9); group scores 7.9 against -4.0
-    np.testing.assert_allclose(margin[0], min(3.9 - (-9.0), (4.0 + 3.9) - (5.0 - 9.0)), rtol=1e-6)
+    # eligible scores 4.0, 3.9, then -9; group scores 7.9 against -4.0
+    np.testing.assert_allclose(margin[0], min(4.0 - 3.9, 3.9 - (-9.0), (4.0 + 3.9) - (5.0 - 9.0)),
+                               rtol=1e-6)
     idx_u, _, _ = oracle.topk_scores(logits, 2, "softmax_post")
     assert list(idx_u[0]) == [0, 4]
