@@ -46,8 +46,16 @@ STAGES = ["route", "permute", "fc1", "fc2", "combine"]
 PAIR_MIN_ROWS = 768
 
 
-def stages_of(w):
+def fused_top1(w, fp8=False):
+    """Top-1 layers without padding or a shared expert run fc2 and the combine
+    as one call (moe_grouped_fc2_combine: the combine in fc2's epilogue)."""
+    return w.k == 1 and not w.pad_to_capacity and w.shared_f == 0 and not fp8
+
+
+def stages_of(w, fp8=False):
     """Timed stages of one forward (the shared expert between fc2 and combine)."""
+    if fused_top1(w, fp8):
+        return STAGES[:3] + ["fc2+combine"]
     return STAGES[:4] + (["shared"] if w.shared_f > 0 else []) + STAGES[4:]
 
 
@@ -242,6 +250,11 @@ def stage_work(w, R, fp8=False, active=None):
         "combine": {"bytes": R * h * 4 + T * h * b + T * k * 8 + (T * h * 4 if w.shared_f else 0),
                     # the scope's algorithmic bytes: y_perm in the activation dtype
                     "bytes_algorithmic": R * h * b + T * h * b},
+        # top-1: fc2 writes each row, weighted, straight into the token's output
+        # row (no y_perm); dropped tokens' rows are zeroed
+        "fc2+combine": {"flops": 2 * R * f * h,
+                        "bytes": A * f * h * q + R * f * b + T * h * b + T * k * 8,
+                        "bytes_algorithmic": A * f * h * q + R * f * b + T * h * b},
         "shared": {"flops": 6 * T * h * w.shared_f,
                    "bytes": 3 * h * w.shared_f * b + T * h * b + 2 * T * w.shared_f * b + T * h * 4},
     }
@@ -260,12 +273,12 @@ def run_native(args, rank, world, local):
     b = moe.Buffers(cfg, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    stage_names = stages_of(w)
+    fp8 = args.precision == "e4m3"
+    stage_names = stages_of(w, fp8)
     if w.shared_f > 0:
         h_mid_s = torch.empty((w.T, w.shared_f), dtype=moe.act_dtype(cfg), device=dev)
         y_shared = torch.empty((w.T, w.h), dtype=torch.float32, device=dev)
 
-    fp8 = args.precision == "e4m3"
     if fp8:
         if w.dtype != "bf16" or w.shared_f > 0:
             raise SystemExit("--precision e4m3 needs a bf16 workload without a shared expert")
@@ -305,6 +318,11 @@ def run_native(args, rank, world, local):
             moe.grouped_fc1(cfg, b.x_perm, b.expert_offsets, inp["W1"], inp["W3"], b.h_mid,
                             b.ws)
             if ev: ev[3].record(stream)
+            if fused_top1(w):
+                moe.grouped_fc2_combine(cfg, b.h_mid, b.expert_offsets, inp["W2"], b.row_map,
+                                        b.topk_prob, b.y, b.ws)
+                if ev: ev[4].record(stream)
+                return
             moe.grouped_fc2(cfg, b.h_mid, b.expert_offsets, inp["W2"], b.y_perm, b.ws)
         if ev: ev[4].record(stream)
         if w.shared_f > 0:
@@ -466,8 +484,9 @@ def run_native(args, rank, world, local):
     if w.E >= 64:
         stages["route"]["alu_frac"] = stages["route"]["tflops"] / fma_tflops
     peaks["fp32_fma_tflops"] = fma_tflops
-    gemm_ms = stages["fc1"]["ms"] + stages["fc2"]["ms"]
-    gemm_tflops = (work["fc1"]["flops"] + work["fc2"]["flops"]) / (gemm_ms * 1e-3) / 1e12
+    fc2_name = "fc2+combine" if "fc2+combine" in stages else "fc2"
+    gemm_ms = stages["fc1"]["ms"] + stages[fc2_name]["ms"]
+    gemm_tflops = (work["fc1"]["flops"] + work[fc2_name]["flops"]) / (gemm_ms * 1e-3) / 1e12
 
     dom = max(stage_names, key=lambda s: stages[s]["ms"])
     # a GEMM whose FLOP per algorithmic byte is below the ridge (peak FLOP/s

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 #define MOE_MAX_EXPERTS 256
 #define MOE_MAX_TOPK 8
 
@@ -228,6 +228,25 @@ moe_status moe_grouped_fc2(const moe_config* cfg, const void* h_mid,
  */
 moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* row_map,
                        const float* topk_prob, void* y, moe_stream_t stream);
+
+/*
+ * fc2 and the combine of a top-1 layer (k == 1, without pad_to_capacity) in
+ * one call: y[t] = bf16/fp32 of topk_prob[t,0] * (h_mid[r] . W2[e]) for the
+ * row r = row_map[t,0] of expert e, 0 for a token whose pair was dropped.
+ * The result is bit for bit that of moe_grouped_fc2 followed by moe_combine
+ * (the same fp32 products, the same single rounding).  For bf16 layers the
+ * combine runs in fc2's epilogue (no y_perm is written or read: the step
+ * moves half the bytes); fp32 layers run the two kernels.
+ * Megatron Core walkthrough §10 (experts) and §2 (combine).
+ *   h_mid [R_max,f] dtype, expert_offsets [E+1], W2 [E,f,h] dtype,
+ *   row_map [T,1] int32, topk_prob [T,1] fp32, y [T,h] dtype out.
+ * MOE_ERR_UNSUPPORTED for k != 1 or pad_to_capacity; ws: moe_workspace_size
+ * bytes (the rows' tokens and weights are kept there).
+ */
+moe_status moe_grouped_fc2_combine(const moe_config* cfg, const void* h_mid,
+                                   const int32_t* expert_offsets, const void* W2,
+                                   const int32_t* row_map, const float* topk_prob, void* y,
+                                   void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * The whole layer forward (route -> drop -> permute -> experts -> combine),

@@ -33,7 +33,7 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_c
            "moe_backward", "moe_workspace_size_backward_shared", "moe_backward_shared",
            "moe_shared_expert_backward", "moe_workspace_size_host_shared",
            "moe_forward_host_shared", "moe_workspace_size_host_e4m3", "moe_forward_host_e4m3",
-           "moe_permute_map", "moe_permute_map_e4m3"]
+           "moe_permute_map", "moe_permute_map_e4m3", "moe_grouped_fc2_combine"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -82,6 +82,7 @@ def lib():
             "moe_grouped_fc1": ([cfgp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_grouped_fc2": ([cfgp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_combine": ([cfgp, vp, vp, vp, vp, vp], i32),
+            "moe_grouped_fc2_combine": ([cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_forward": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_check": ([vp, vp, ctypes.POINTER(i32)], i32),
             "moe_permute_noalloc": ([cfgp, vp, vp, vp, vp, vp, vp, vp], i32),
@@ -241,6 +242,14 @@ def grouped_mlp(cfg, x_perm, expert_offsets, W1, W3, W2, h_mid, y_perm, ws):
     _check(lib().moe_grouped_mlp(ctypes.byref(cfg), _p(x_perm), _p(expert_offsets), _p(W1),
                                  _p(W3), _p(W2), _p(h_mid), _p(y_perm), w, wb, _stream()),
            "moe_grouped_mlp")
+
+
+def grouped_fc2_combine(cfg, h_mid, expert_offsets, W2, row_map, topk_prob, y, ws):
+    """moe_grouped_fc2_combine: fc2 and the combine of a top-1 layer in one call."""
+    w, wb = _ws(ws)
+    _check(lib().moe_grouped_fc2_combine(ctypes.byref(cfg), _p(h_mid), _p(expert_offsets),
+                                         _p(W2), _p(row_map), _p(topk_prob), _p(y), w, wb,
+                                         _stream()), "moe_grouped_fc2_combine")
 
 
 def combine(cfg, y_perm, row_map, topk_prob, y):

@@ -39,7 +39,7 @@ thread_local char g_last_cuda_error[256] = "";
 struct Layout {
   size_t err, logits, assigned, tiles, cand_rowmap, cand_src, cand_off, cand_tiles;
   size_t topk_idx, topk_prob, keep, tpe, offsets, row_map, x_perm, h_mid, y_perm;
-  size_t map, map_tiles, row_src, total;
+  size_t map, map_tiles, row_src, top1_token, top1_weight, total;
 };
 
 size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -98,6 +98,9 @@ Layout make_layout(const moe_config& c) {
   L.map = take(c.pad_to_capacity ? T * E : 0);
   L.map_tiles = take(static_cast<size_t>(map_tiles(static_cast<int>(T))) * E * 4);
   L.row_src = take(rows * 4);
+  // top-1 layers whose combine runs in fc2's epilogue: each row's token and weight
+  L.top1_token = take(k == 1 ? rows * 4 : 0);
+  L.top1_weight = take(k == 1 ? rows * 4 : 0);
   L.total = o;
   return L;
 }
@@ -303,6 +306,33 @@ moe_status do_fc2(const moe_config& c, const void* h_mid, const int32_t* offsets
   return MOE_OK;
 }
 
+// Top-1 layers: fc2 and the combine.  bf16: the combine runs in fc2's epilogue
+// (the rows' tokens and weights prepared first); fp32: fc2 into the
+// workspace's y_perm, then the combine kernel.  Same bits either way.
+bool top1_fusable(const moe_config& c) { return c.topk == 1 && !c.pad_to_capacity; }
+
+moe_status do_fc2_combine(const moe_config& c, const void* h_mid, const int32_t* offsets,
+                          const void* W2, const int32_t* row_map, const float* topk_prob, void* y,
+                          void* ws, cudaStream_t s) {
+  const Layout L = make_layout(c);
+  int* err = at<int>(ws, L.err);
+  const int64_t rows = rows_of(c);
+  if (c.dtype == MOE_F32) {
+    float* y_perm = at<float>(ws, L.y_perm);
+    MOE_TRY(do_fc2(c, h_mid, offsets, W2, y_perm, ws, s));
+    MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, y_perm, row_map, topk_prob,
+                            nullptr, y, s, rows));
+    return MOE_OK;
+  }
+  int32_t* tok = at<int32_t>(ws, L.top1_token);
+  float* wgt = at<float>(ws, L.top1_weight);
+  MOE_CUDA(launch_top1_rows(c.num_tokens, c.hidden, c.dtype, rows, row_map, topk_prob, tok, wgt,
+                            y, s));
+  MOE_CUDA(launch_tc_fc2_top1(c.num_experts, c.hidden, c.ffn_hidden, rows, h_mid, offsets, W2,
+                              tok, wgt, y, err, s));
+  return MOE_OK;
+}
+
 // Shared expert: the grouped MLP kernels as one dense group of all T rows of x.
 moe_status do_shared(const moe_config& c, int32_t fs, const void* x, const void* W1s,
                      const void* W3s, const void* W2s, void* h_mid_s, float* y_shared, int* err,
@@ -334,7 +364,8 @@ struct Routed {
 moe_status routed_path(const moe_config& c, const void* x, const float* Wg,
                        const float* gate_bias, const float* expert_bias, const void* W1,
                        const void* W3, const void* W2, int32_t* topk_idx, float* topk_prob,
-                       int32_t* tokens_per_expert, void* ws, cudaStream_t stream, Routed* out) {
+                       int32_t* tokens_per_expert, void* ws, cudaStream_t stream, Routed* out,
+                       bool skip_fc2 = false) {
   const Layout L = make_layout(c);
   int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.topk_idx);
   float* prob = topk_prob ? topk_prob : at<float>(ws, L.topk_prob);
@@ -353,7 +384,7 @@ moe_status routed_path(const moe_config& c, const void* x, const float* Wg,
   else
     MOE_TRY(do_permute(c, x, idx, keep, x_perm, row_map, offsets, ws, stream));
   MOE_TRY(do_fc1(c, x_perm, offsets, W1, W3, h_mid, ws, stream));
-  MOE_TRY(do_fc2(c, h_mid, offsets, W2, y_perm, ws, stream));
+  if (!skip_fc2) MOE_TRY(do_fc2(c, h_mid, offsets, W2, y_perm, ws, stream));
   *out = Routed{idx, prob, tpe, row_map, y_perm};
   return MOE_OK;
 }
@@ -1004,6 +1035,26 @@ moe_status moe_grouped_mlp(const moe_config* cfg, const void* x_perm,
   return moe_grouped_fc2(cfg, h_mid, expert_offsets, W2, y_perm, ws, ws_bytes, stream);
 }
 
+moe_status moe_grouped_fc2_combine(const moe_config* cfg, const void* h_mid,
+                                   const int32_t* expert_offsets, const void* W2,
+                                   const int32_t* row_map, const float* topk_prob, void* y,
+                                   void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  if (!top1_fusable(c)) return MOE_ERR_UNSUPPORTED;
+  const size_t T = c.num_tokens;
+  const size_t R = static_cast<size_t>(rows_of(c));
+  const size_t wsz = static_cast<size_t>(c.num_experts) * c.hidden * c.ffn_hidden;
+  MOE_TRY(need(h_mid, R * c.ffn_hidden, 16));
+  MOE_TRY(need(expert_offsets, c.num_experts + 1, 4));
+  MOE_TRY(need(W2, wsz, 16));
+  MOE_TRY(need(row_map, T, 4));
+  MOE_TRY(need(topk_prob, T, 4));
+  MOE_TRY(need(y, T * c.hidden, 16));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  return do_fc2_combine(c, h_mid, expert_offsets, W2, row_map, topk_prob, y, ws, stream);
+}
+
 moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* row_map,
                        const float* topk_prob, void* y, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
@@ -1112,8 +1163,14 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
   MOE_TRY(optional(tokens_per_expert, 4));
   MOE_TRY(check_ws(c, ws, ws_bytes));
   Routed r;
+  const bool fuse = top1_fusable(c);  // top-1: the combine in fc2's epilogue
   MOE_TRY(routed_path(c, x, Wg, gate_bias, expert_bias, W1, W3, W2, topk_idx, topk_prob,
-                      tokens_per_expert, ws, stream, &r));
+                      tokens_per_expert, ws, stream, &r, fuse));
+  if (fuse) {
+    const Layout L = make_layout(c);
+    return do_fc2_combine(c, at<void>(ws, L.h_mid), at<int32_t>(ws, L.offsets), W2, r.row_map,
+                          r.prob, y, ws, stream);
+  }
   MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm, r.row_map, r.prob,
                           nullptr, y, stream, rows_of(c)));
   return MOE_OK;
@@ -1412,8 +1469,15 @@ moe_status moe_forward_host(const moe_config* cfg, int32_t num_batches, const vo
   return host_pipeline(c, num_batches, x_host, x_batch_stride, y_host, y_batch_stride, row_bytes,
                        H, ws, stream, [&](void* xs, void* ys) {
                          Routed r{};
+                         const bool fuse = top1_fusable(c);
                          MOE_TRY(routed_path(c, xs, Wg, gate_bias, expert_bias, W1, W3, W2,
-                                             nullptr, nullptr, nullptr, ws, stream, &r));
+                                             nullptr, nullptr, nullptr, ws, stream, &r, fuse));
+                         if (fuse) {
+                           const Layout L = make_layout(c);
+                           return do_fc2_combine(c, at<void>(ws, L.h_mid),
+                                                 at<int32_t>(ws, L.offsets), W2, r.row_map,
+                                                 r.prob, ys, ws, stream);
+                         }
                          MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype,
                                                  r.y_perm, r.row_map, r.prob, nullptr, ys,
                                                  stream, rows_of(c)));

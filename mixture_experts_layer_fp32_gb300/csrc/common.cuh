@@ -129,6 +129,11 @@ cudaError_t launch_perm_copy_e4m3(int T, int h, int k, const void* x, const int3
 cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
                            const int32_t* row_map, const float* topk_prob, const float* y_shared,
                            void* y, cudaStream_t s, int64_t max_rows = -1);
+// Top-1 layers with the combine in fc2's epilogue: row -> (token, weight)
+// and zero output rows for dropped tokens.
+cudaError_t launch_top1_rows(int T, int h, int dtype, int64_t max_rows, const int32_t* row_map,
+                             const float* topk_prob, int32_t* row_token, float* row_weight,
+                             void* y, cudaStream_t s);
 
 // ---- grouped GEMMs ----
 // offsets == nullptr: one dense group (E must be 1) over rows [0, max_rows)
@@ -163,6 +168,11 @@ cudaError_t launch_tc_fc1(int E, int h, int f, int64_t max_rows, const void* x_p
 cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_mid,
                           const int32_t* offsets, const void* W2, float* y_perm, int* err,
                           cudaStream_t s);
+// fc2 of a top-1 layer with the combine in the epilogue: y[row_token[r]] =
+// bf16(row_weight[r] * (h_mid[r] . W2[e]))
+cudaError_t launch_tc_fc2_top1(int E, int h, int f, int64_t max_rows, const void* h_mid,
+                               const int32_t* offsets, const void* W2, const int32_t* row_token,
+                               const float* row_weight, void* y, int* err, cudaStream_t s);
 
 // E4M3 operands (kind::f8f6f4): xq / hq [rows, K] codes with per-row scales
 // (x's through row_src: row r uses x_scale[row_src[r]]), K-major weights

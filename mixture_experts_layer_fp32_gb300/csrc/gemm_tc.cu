@@ -101,7 +101,11 @@ constexpr long long kWaitCycles = 4000000000LL;
 //   DGRAD_F32  the same with K split between two weights (the first kb_split
 //              K blocks from tmB0, the rest from tmB1), fp32 out: fc1's
 //              dX = [da | dg] . [W1[e] ; W3[e]]^T
-enum { FC1 = 0, FC2 = 1, FC1_BWD = 2, DGRAD_BF16 = 3, DGRAD_F32 = 4 };
+//   FC2_Y      fc2 of a top-1 layer with the combine in its epilogue: row r
+//              is the one slot of token row_token[r], whose output row gets
+//              bf16(row_weight[r] * acc) -- the combine's arithmetic, so the
+//              bits equal fc2 followed by the combine kernel
+enum { FC1 = 0, FC2 = 1, FC1_BWD = 2, DGRAD_BF16 = 3, DGRAD_F32 = 4, FC2_Y = 5 };
 
 struct TcArgs {
   const int32_t* offsets;
@@ -131,6 +135,9 @@ struct TcArgs {
   // through the output tensor map (32 x 32 boxes) when a warp's 32 rows all
   // belong to the tile's expert
   int tma_out = 0;
+  // FC2_Y: the token of each row (-1: none) and its combine weight
+  const int32_t* row_token = nullptr;
+  const float* row_weight = nullptr;
 };
 
 // Barriers of an NS-stage ring: full[NS], empty[NS], acc_full[2],
@@ -363,6 +370,49 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, uin
           dst_a[v] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
           dst_g[v] = make_uint4(og[0], og[1], og[2], og[3]);
         }
+      }
+    }
+  } else if (MODE == FC2_Y) {
+    // the top-1 combine: this lane's row goes, weighted, to its token's output
+    // row (64 contiguous bytes per 32-column chunk); fmaf(w, acc, 0) is the
+    // combine kernel's first (and, for one slot, only) step
+    const int row = rbase + lane;
+    int tok = -1;
+    float w = 0.f;
+    if (row < rend) {
+      tok = args.row_token[row];
+      w = args.row_weight[row];
+    }
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) +
+                         static_cast<int64_t>(tok < 0 ? 0 : tok) * args.ldo +
+                         static_cast<int64_t>(nt) * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t y[32];
+      ptx::tmem_ld32(tb + c, y);
+      ptx::tmem_wait_ld();
+      if (tok >= 0) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(y[j]);
+        if (FP8) {  // acc * row scale * channel scale, as fc2 stores it
+          const float* cs = args.col_scale0 + static_cast<int64_t>(e) * args.ncols + nt * BN + c;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 u = __ldg(reinterpret_cast<const float4*>(cs + 4 * q));
+            v[4 * q] *= rs * u.x;
+            v[4 * q + 1] *= rs * u.y;
+            v[4 * q + 2] *= rs * u.z;
+            v[4 * q + 3] *= rs * u.w;
+          }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[q] = make_uint4(pack_bf16x2(fmaf(w, v[8 * q], 0.f), fmaf(w, v[8 * q + 1], 0.f)),
+                              pack_bf16x2(fmaf(w, v[8 * q + 2], 0.f), fmaf(w, v[8 * q + 3], 0.f)),
+                              pack_bf16x2(fmaf(w, v[8 * q + 4], 0.f), fmaf(w, v[8 * q + 5], 0.f)),
+                              pack_bf16x2(fmaf(w, v[8 * q + 6], 0.f), fmaf(w, v[8 * q + 7], 0.f)));
       }
     }
   } else if (MODE == DGRAD_BF16) {
@@ -1187,6 +1237,19 @@ cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_m
   CUtensorMap c = a;
   setup_tma_out(&c, &args, h);
   return launch_grouped<FC2, false>(a, b0, b0, c, args, s);
+}
+
+cudaError_t launch_tc_fc2_top1(int E, int h, int f, int64_t max_rows, const void* h_mid,
+                               const int32_t* offsets, const void* W2, const int32_t* row_token,
+                               const float* row_weight, void* y, int* err, cudaStream_t s) {
+  if (max_rows == 0) return cudaSuccess;
+  CUtensorMap a, b0;
+  if (!map_rows(&a, h_mid, f, max_rows) || !map_weights(&b0, W2, h, f, E))
+    return cudaErrorInvalidValue;
+  TcArgs args{offsets, E, h / BN, f / BK, max_rows, y, h, err};
+  args.row_token = row_token;
+  args.row_weight = row_weight;
+  return launch_grouped<FC2_Y, false>(a, b0, b0, a, args, s);
 }
 
 // ---- backward GEMMs (bf16 operands, 64-wide K stages; SM pairs by the

@@ -904,6 +904,39 @@ cudaError_t launch_perm_copy_e4m3(int T, int h, int k, const void* x, const int3
   return cudaGetLastError();
 }
 
+// Top-1 layers whose combine runs in fc2's epilogue: each row's token and
+// combine weight (row_map inverted: a top-1 token owns at most one row), and
+// zeros for the output rows of tokens whose pair was dropped -- what the
+// combine kernel writes for them.  A warp per token, grid-stride.
+__global__ void __launch_bounds__(256)
+    top1_rows_kernel(int T, int row_vecs, int64_t max_rows, const int32_t* __restrict__ row_map,
+                     const float* __restrict__ topk_prob, int32_t* __restrict__ row_token,
+                     float* __restrict__ row_weight, uint4* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += gridDim.x * 8) {
+    const int r = row_map[t];
+    if (r >= 0 && r < max_rows) {
+      if (lane == 0) {
+        row_token[r] = t;
+        row_weight[r] = topk_prob[t];
+      }
+    } else {
+      uint4* dst = y + static_cast<int64_t>(t) * row_vecs;
+      for (int v = lane; v < row_vecs; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+cudaError_t launch_top1_rows(int T, int h, int dtype, int64_t max_rows, const int32_t* row_map,
+                             const float* topk_prob, int32_t* row_token, float* row_weight,
+                             void* y, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int row_vecs = h * (dtype == MOE_F32 ? 4 : 2) / 16;
+  top1_rows_kernel<<<grid_for_tokens((T + 7) / 8, 8), 256, 0, s>>>(
+      T, row_vecs, max_rows, row_map, topk_prob, row_token, row_weight, static_cast<uint4*>(y));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(int T, int h, int k, int dtype, const float* y_perm,
                            const int32_t* row_map, const float* topk_prob, const float* y_shared,
                            void* y, cudaStream_t s, int64_t max_rows) {

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_function(moe):
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
     assert sorted(moe.EXPORTS) == declared_functions()
-    assert moe.lib().moe_abi_version() == 3
+    assert moe.lib().moe_abi_version() == 4
     assert moe.lib().moe_status_string(3) == b"MOE_ERR_WORKSPACE"
 
 
@@ -125,6 +125,30 @@ def test_forward_and_stage_argument_checks(moe):
     assert lib.moe_combine(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, None) == INVALID
     # moe_check: no workspace
     assert lib.moe_check(None, None, None) == INVALID
+
+
+def test_fc2_combine_host_checks(moe):
+    lib = moe.lib()
+    top1 = moe.config(T=128, h=1024, E=8, k=1, f=512)
+    need = moe.workspace_size(top1)
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need, None]
+    # only top-1 layers without padding have one row per token to fuse
+    top2 = moe.config(T=128, h=1024, E=8, k=2, f=512)
+    assert lib.moe_grouped_fc2_combine(ctypes.byref(top2), *args[:-2],
+                                       moe.workspace_size(top2), None) == UNSUPPORTED
+    pad = moe.config(T=128, h=1024, E=8, k=1, f=512, capacity_factor=1.0, pad_to_capacity=True)
+    assert lib.moe_grouped_fc2_combine(ctypes.byref(pad), *args[:-2],
+                                       moe.workspace_size(pad), None) == UNSUPPORTED
+    # missing or misaligned pointers, short workspace
+    bad = list(args)
+    bad[6] = None  # y
+    assert lib.moe_grouped_fc2_combine(ctypes.byref(top1), *bad) == INVALID
+    bad = list(args)
+    bad[0] = MISALIGNED  # h_mid
+    assert lib.moe_grouped_fc2_combine(ctypes.byref(top1), *bad) == INVALID
+    bad = list(args)
+    bad[7] = need - 1
+    assert lib.moe_grouped_fc2_combine(ctypes.byref(top1), *bad) == WORKSPACE
 
 
 def test_permute_noalloc_host_checks(moe):

@@ -1,0 +1,63 @@
+"""fc2 with the combine of a top-1 layer in its epilogue
+(moe_grouped_fc2_combine), on the GPU through the C ABI.
+
+With one slot per token the combine is y[t] = p[t] * Y[row(t)], rounded
+once to the output dtype (0 for a dropped token): the Megatron Core
+walkthrough (r00kie-liu.github.io), section 10 Experts and section 2 (the
+combine).  The fused call computes the same fp32 product and rounds it the
+same way, so its output must equal moe_grouped_fc2 followed by moe_combine
+bit for bit, on both tensor-core kernels, with every dropped token's row
+zero; and the output is checked against the oracle.
+"""
+
+import pytest
+import torch
+
+import synthetic
+from moe_cases import assert_close, gpu_config, gpu_stages, make_case, oracle_forward, to_dev
+from moe_cases import to_np
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # Switch-shaped: four hot experts over capacity, so tokens are dropped
+    "switch_drop": synthetic.scaled("switch", T=4096, h=512, f=256, seed=61),
+    # one hot expert with ~7000 candidates (the drop's keys re-read), few experts
+    "switch_one_hot": synthetic.scaled("switch", T=12000, h=256, f=256, E=8, seed=62,
+                                       gate_bias="hot:1:4.6"),
+    # top-1 without drops: every token has a row; ~1000 rows per expert (pair tiles)
+    "top1_dropless": synthetic.scaled("mixtral", T=4000, h=256, f=384, E=4, k=1, seed=63),
+    # fp32: the two kernels behind the same call
+    "top1_fp32": synthetic.scaled("tiny_fp32", T=700, h=136, f=200, k=1, seed=64),
+}
+
+
+@pytest.fixture(scope="module", params=sorted(CASES))
+def case(request):
+    w = CASES[request.param]
+    inp, _ = make_case(w)
+    ref = oracle_forward(w, inp)
+    d = to_dev(inp)
+    b = gpu_stages(w, d)  # route, permute, fc1, fc2, combine (unfused)
+    torch.cuda.synchronize()
+    return w, inp, ref, d, b
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_fused_equals_fc2_then_combine(case, kernel, monkeypatch):
+    import mixture_experts_layer_fp32_gb300 as moe
+    w, inp, ref, d, b = case
+    monkeypatch.setenv("MOE_TC_PAIR", "1" if kernel == "pair" else "0")
+    cfg = gpu_config(w)
+    for _ in range(2):  # a second call on the same workspace gives the same bits
+        y = torch.full_like(b.y, float("nan"))
+        moe.grouped_fc2_combine(cfg, b.h_mid, b.expert_offsets, d["W2"], b.row_map, b.topk_prob,
+                                y, b.ws)
+        moe.check(b.ws)
+        bits = torch.int16 if y.dtype == torch.bfloat16 else torch.int32
+        assert torch.equal(y.view(bits), b.y.view(bits))
+    dropped = to_np(b.keep)[:, 0] == 0
+    if w.capacity_factor > 0:
+        assert dropped.any()
+    assert (to_np(y)[dropped] == 0).all()
+    assert_close("y", to_np(y), ref["y"], w.dtype)
