@@ -47,9 +47,11 @@ PAIR_MIN_ROWS = 768
 
 
 def fused_top1(w, fp8=False):
-    """Top-1 layers without padding or a shared expert run fc2 and the combine
-    as one call (moe_grouped_fc2_combine: the combine in fc2's epilogue)."""
-    return w.k == 1 and not w.pad_to_capacity and w.shared_f == 0 and not fp8
+    """Top-1 bf16 layers without padding or a shared expert run fc2 and the
+    combine as one call (moe_grouped_fc2_combine: the combine in fc2's
+    epilogue)."""
+    return (w.k == 1 and w.dtype == "bf16" and not w.pad_to_capacity and w.shared_f == 0
+            and not fp8)
 
 
 def stages_of(w, fp8=False):

@@ -230,18 +230,19 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
                        const float* topk_prob, void* y, moe_stream_t stream);
 
 /*
- * fc2 and the combine of a top-1 layer (k == 1, without pad_to_capacity) in
- * one call: y[t] = bf16/fp32 of topk_prob[t,0] * (h_mid[r] . W2[e]) for the
- * row r = row_map[t,0] of expert e, 0 for a token whose pair was dropped.
- * The result is bit for bit that of moe_grouped_fc2 followed by moe_combine
- * (the same fp32 products, the same single rounding).  For bf16 layers the
- * combine runs in fc2's epilogue (no y_perm is written or read: the step
- * moves half the bytes); fp32 layers run the two kernels.
+ * fc2 and the combine in one call (layers without pad_to_capacity): the
+ * output of moe_grouped_fc2 followed by moe_combine, bit for bit (the same
+ * fp32 products, the same slot order, the same single rounding).  For bf16
+ * top-1 layers the combine runs in fc2's epilogue: each row goes, weighted,
+ * straight into its token's output row, so no y_perm is written or read;
+ * the rows of dropped tokens are zeroed.  Other layers run fc2 into the
+ * workspace's y_perm and then the combine kernel.
  * Megatron Core walkthrough §10 (experts) and §2 (combine).
  *   h_mid [R_max,f] dtype, expert_offsets [E+1], W2 [E,f,h] dtype,
- *   row_map [T,1] int32, topk_prob [T,1] fp32, y [T,h] dtype out.
- * MOE_ERR_UNSUPPORTED for k != 1 or pad_to_capacity; ws: moe_workspace_size
- * bytes (the rows' tokens and weights are kept there).
+ *   row_map [T,k] int32, topk_prob [T,k] fp32, y [T,h] dtype out.
+ * MOE_ERR_UNSUPPORTED with pad_to_capacity (padding rows have no slot);
+ * ws: moe_workspace_size bytes (holds y_perm and the rows' tokens and
+ * weights).  Calls that share a workspace must not overlap on the GPU.
  */
 moe_status moe_grouped_fc2_combine(const moe_config* cfg, const void* h_mid,
                                    const int32_t* expert_offsets, const void* W2,

@@ -306,10 +306,14 @@ moe_status do_fc2(const moe_config& c, const void* h_mid, const int32_t* offsets
   return MOE_OK;
 }
 
-// Top-1 layers: fc2 and the combine.  bf16: the combine runs in fc2's epilogue
-// (the rows' tokens and weights prepared first); fp32: fc2 into the
-// workspace's y_perm, then the combine kernel.  Same bits either way.
-bool top1_fusable(const moe_config& c) { return c.topk == 1 && !c.pad_to_capacity; }
+// fc2 and the combine in one call (layers without pad_to_capacity).  bf16
+// top-1: the combine runs in fc2's epilogue (each row, weighted, straight into
+// its token's output row).  Otherwise fc2 into the workspace's y_perm, then
+// the combine kernel.  The same bits in every case.
+bool fc2_combine_ok(const moe_config& c) { return !c.pad_to_capacity; }
+bool fc2_combine_fused(const moe_config& c) {
+  return c.topk == 1 && !c.pad_to_capacity && c.dtype == MOE_BF16;
+}
 
 moe_status do_fc2_combine(const moe_config& c, const void* h_mid, const int32_t* offsets,
                           const void* W2, const int32_t* row_map, const float* topk_prob, void* y,
@@ -317,7 +321,7 @@ moe_status do_fc2_combine(const moe_config& c, const void* h_mid, const int32_t*
   const Layout L = make_layout(c);
   int* err = at<int>(ws, L.err);
   const int64_t rows = rows_of(c);
-  if (c.dtype == MOE_F32) {
+  if (!fc2_combine_fused(c)) {
     float* y_perm = at<float>(ws, L.y_perm);
     MOE_TRY(do_fc2(c, h_mid, offsets, W2, y_perm, ws, s));
     MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, y_perm, row_map, topk_prob,
@@ -1041,15 +1045,15 @@ moe_status moe_grouped_fc2_combine(const moe_config* cfg, const void* h_mid,
                                    void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
-  if (!top1_fusable(c)) return MOE_ERR_UNSUPPORTED;
-  const size_t T = c.num_tokens;
+  if (!fc2_combine_ok(c)) return MOE_ERR_UNSUPPORTED;
+  const size_t T = c.num_tokens, k = c.topk;
   const size_t R = static_cast<size_t>(rows_of(c));
   const size_t wsz = static_cast<size_t>(c.num_experts) * c.hidden * c.ffn_hidden;
   MOE_TRY(need(h_mid, R * c.ffn_hidden, 16));
   MOE_TRY(need(expert_offsets, c.num_experts + 1, 4));
   MOE_TRY(need(W2, wsz, 16));
-  MOE_TRY(need(row_map, T, 4));
-  MOE_TRY(need(topk_prob, T, 4));
+  MOE_TRY(need(row_map, T * k, 4));
+  MOE_TRY(need(topk_prob, T * k, 4));
   MOE_TRY(need(y, T * c.hidden, 16));
   MOE_TRY(check_ws(c, ws, ws_bytes));
   return do_fc2_combine(c, h_mid, expert_offsets, W2, row_map, topk_prob, y, ws, stream);
@@ -1163,7 +1167,7 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
   MOE_TRY(optional(tokens_per_expert, 4));
   MOE_TRY(check_ws(c, ws, ws_bytes));
   Routed r;
-  const bool fuse = top1_fusable(c);  // top-1: the combine in fc2's epilogue
+  const bool fuse = fc2_combine_fused(c);  // top-1: the combine in fc2's epilogue
   MOE_TRY(routed_path(c, x, Wg, gate_bias, expert_bias, W1, W3, W2, topk_idx, topk_prob,
                       tokens_per_expert, ws, stream, &r, fuse));
   if (fuse) {
@@ -1469,7 +1473,7 @@ moe_status moe_forward_host(const moe_config* cfg, int32_t num_batches, const vo
   return host_pipeline(c, num_batches, x_host, x_batch_stride, y_host, y_batch_stride, row_bytes,
                        H, ws, stream, [&](void* xs, void* ys) {
                          Routed r{};
-                         const bool fuse = top1_fusable(c);
+                         const bool fuse = fc2_combine_fused(c);
                          MOE_TRY(routed_path(c, xs, Wg, gate_bias, expert_bias, W1, W3, W2,
                                              nullptr, nullptr, nullptr, ws, stream, &r, fuse));
                          if (fuse) {

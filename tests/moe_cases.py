@@ -34,6 +34,13 @@ BF16_ULP = 2.0 ** -7
 BF16_STORED_RMS_TOL = 1e-2
 
 
+def cf32(w):
+    """The capacity factor as the layer gets it: an fp32 field of the config
+    (0.6 arrives as 0.60000002384...).  The oracle is given the same value, so
+    that ceil(T*k/E * cf) is the same number on both sides."""
+    return float(np.float32(w.capacity_factor))
+
+
 def np_view(t):
     """A CPU torch tensor as the numpy array the oracle takes."""
     if t is None:
@@ -73,7 +80,7 @@ def condition_inputs(w, inp, max_rounds=64, nthreads=0):
     groups = (w.num_groups, w.group_topk)
     idx, prob, margin = oracle.topk_scores(logits, w.k, w.score, eb, nthreads, *groups)
     for rnd in range(max_rounds):
-        part = {"capacity": oracle.capacity(w.T, w.E, w.k, w.capacity_factor, w.min_capacity),
+        part = {"capacity": oracle.capacity(w.T, w.E, w.k, cf32(w), w.min_capacity),
                 "topk_idx": idx, "topk_prob_raw": prob,
                 "assigned": np.bincount(idx.reshape(-1), minlength=w.E)}
         bad = sorted(set(np.nonzero(margin < MARGIN)[0].tolist()) |
@@ -88,7 +95,7 @@ def condition_inputs(w, inp, max_rounds=64, nthreads=0):
     else:
         raise RuntimeError("margin conditioning did not converge")
     x.copy_(x_cpu.to(x.device))
-    r = oracle.route(np_view(x_cpu), Wg, w.k, w.score, gb, eb, w.capacity_factor,
+    r = oracle.route(np_view(x_cpu), Wg, w.k, w.score, gb, eb, cf32(w),
                      w.min_capacity, w.drop_policy, nthreads, *groups,
                      pad_to_capacity=w.pad_to_capacity)
     assert np.all(r["margin"] >= MARGIN)
@@ -108,7 +115,7 @@ def oracle_forward(w, inp, nthreads=0, want_h_mid=True):
     return oracle.forward(np_view(inp["x"]), np_view(inp["Wg"]), np_view(inp["W1"]),
                           np_view(inp["W3"]), np_view(inp["W2"]), w.k, w.score,
                           np_view(inp["gate_bias"]), np_view(inp["expert_bias"]),
-                          w.capacity_factor, w.min_capacity, w.drop_policy, nthreads,
+                          cf32(w), w.min_capacity, w.drop_policy, nthreads,
                           want_h_mid=want_h_mid, num_groups=w.num_groups,
                           group_topk=w.group_topk, pad_to_capacity=w.pad_to_capacity, **shared)
 

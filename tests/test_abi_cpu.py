@@ -132,10 +132,7 @@ def test_fc2_combine_host_checks(moe):
     top1 = moe.config(T=128, h=1024, E=8, k=1, f=512)
     need = moe.workspace_size(top1)
     args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, need, None]
-    # only top-1 layers without padding have one row per token to fuse
-    top2 = moe.config(T=128, h=1024, E=8, k=2, f=512)
-    assert lib.moe_grouped_fc2_combine(ctypes.byref(top2), *args[:-2],
-                                       moe.workspace_size(top2), None) == UNSUPPORTED
+    # padding rows have no slot to combine into
     pad = moe.config(T=128, h=1024, E=8, k=1, f=512, capacity_factor=1.0, pad_to_capacity=True)
     assert lib.moe_grouped_fc2_combine(ctypes.byref(pad), *args[:-2],
                                        moe.workspace_size(pad), None) == UNSUPPORTED

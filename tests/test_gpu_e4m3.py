@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import synthetic
-from moe_cases import (assert_close, assert_equal, assert_probs, gpu_config, make_case, np_view,
+from moe_cases import (assert_close, assert_equal, assert_probs, cf32, gpu_config, make_case, np_view,
                        to_dev, to_np)
 
 pytestmark = pytest.mark.gpu
@@ -87,7 +87,7 @@ def oracle_forward_e4m3(w, inp):
     q = oracle.quantize_experts_e4m3(_bits(inp["W1"]), _bits(inp["W3"]), _bits(inp["W2"]))
     return oracle.forward_fp8(_bits(inp["x"]), _bits(inp["Wg"]), q, w.k, w.score,
                               np_view(inp["gate_bias"]), np_view(inp["expert_bias"]),
-                              w.capacity_factor, w.min_capacity, w.drop_policy,
+                              cf32(w), w.min_capacity, w.drop_policy,
                               num_groups=w.num_groups, group_topk=w.group_topk,
                               pad_to_capacity=w.pad_to_capacity)
 

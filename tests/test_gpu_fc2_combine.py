@@ -1,13 +1,16 @@
-"""fc2 with the combine of a top-1 layer in its epilogue
-(moe_grouped_fc2_combine), on the GPU through the C ABI.
+"""fc2 with the combine in its epilogue (moe_grouped_fc2_combine), on the
+GPU through the C ABI.
 
-With one slot per token the combine is y[t] = p[t] * Y[row(t)], rounded
-once to the output dtype (0 for a dropped token): the Megatron Core
-walkthrough (r00kie-liu.github.io), section 10 Experts and section 2 (the
-combine).  The fused call computes the same fp32 product and rounds it the
-same way, so its output must equal moe_grouped_fc2 followed by moe_combine
-bit for bit, on both tensor-core kernels, with every dropped token's row
-zero; and the output is checked against the oracle.
+The combine is y[t] = sum over kept slots j, in slot order, of
+p[t,j] * Y[row(t,j)], in fp32, rounded once to the output dtype (0 for a
+token with no kept slot): the Megatron Core walkthrough
+(r00kie-liu.github.io), section 10 Experts and section 2 (the combine).
+Top-1 rows go, weighted, straight to their token's output row; with k >= 2
+the epilogue that stores the last of a token's rows sums them.  Either way
+the arithmetic is the combine kernel's, so the output must equal
+moe_grouped_fc2 followed by moe_combine bit for bit, on both tensor-core
+kernels, with every dropped token's row zero; and it is checked against
+the oracle.
 """
 
 import pytest
@@ -29,6 +32,17 @@ CASES = {
     "top1_dropless": synthetic.scaled("mixtral", T=4000, h=256, f=384, E=4, k=1, seed=63),
     # fp32: the two kernels behind the same call
     "top1_fp32": synthetic.scaled("tiny_fp32", T=700, h=136, f=200, k=1, seed=64),
+    # top-2, ~1000 rows per expert, 4 n-tiles of fc2: rows of a token in different tiles
+    "top2": synthetic.scaled("mixtral", T=2000, h=1024, f=256, E=4, seed=65),
+    # top-8 over 128 experts with Zipf loads: eight rows per token to add up
+    "top8_zipf": synthetic.scaled("qwen3", T=1500, h=512, f=256, seed=66),
+    # top-8 sigmoid with the selection bias, 64 experts
+    "top8_sigmoid": synthetic.scaled("dsv3", T=600, h=768, f=256, E=64, seed=67),
+    # top-2 with capacity drops: tokens with one kept slot and with none
+    "top2_drop": synthetic.scaled("switch", T=3000, h=256, f=256, E=8, k=2, seed=68,
+                                  capacity_factor=0.6),
+    # fp32 top-2: fc2 and the combine kernel behind the same call
+    "top2_fp32": synthetic.scaled("tiny_fp32", T=500, h=136, f=200, seed=69),
 }
 
 
@@ -56,7 +70,7 @@ def test_fused_equals_fc2_then_combine(case, kernel, monkeypatch):
         moe.check(b.ws)
         bits = torch.int16 if y.dtype == torch.bfloat16 else torch.int32
         assert torch.equal(y.view(bits), b.y.view(bits))
-    dropped = to_np(b.keep)[:, 0] == 0
+    dropped = (to_np(b.keep) == 0).all(axis=1)
     if w.capacity_factor > 0:
         assert dropped.any()
     assert (to_np(y)[dropped] == 0).all()
