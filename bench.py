@@ -54,6 +54,13 @@ def fused_top1(w, fp8=False):
             and not fp8)
 
 
+def uses_f16s(w, fp8=False):
+    """bf16 layers with k >= 2 (no padding, no shared expert) keep y_perm as
+    fp16 with a power-of-two scale per 32 columns (moe_grouped_fc2_f16s +
+    moe_combine_f16s), as moe_forward does."""
+    return w.dtype == "bf16" and w.k > 1 and not w.pad_to_capacity and w.shared_f == 0 and not fp8
+
+
 def stages_of(w, fp8=False):
     """Timed stages of one forward (the shared expert between fc2 and combine)."""
     if fused_top1(w, fp8):
@@ -230,7 +237,7 @@ def kernels_per_forward(w, cfg, fp8=False):
     return route + index + 1 + 1 + 1 + shared + quant + 1  # permute index + copy, fc1, fc2, combine
 
 
-def stage_work(w, R, fp8=False, active=None):
+def stage_work(w, R, fp8=False, active=None, y16=False):
     """Algorithmic work of each stage (bytes moved or flops), per forward.
     fp8: E4M3 expert operands (1-byte codes of x_perm, the weights and the
     SwiGLU output; fc2 also reads the bf16 SwiGLU output once to quantise it).
@@ -240,16 +247,17 @@ def stage_work(w, R, fp8=False, active=None):
     q = 1 if fp8 else b          # bytes of a GEMM operand element
     T, h, E, k, f = w.T, w.h, w.E, w.k, w.f
     A = E if active is None else active
+    yb = 2 + 1 / 32 if y16 else 4  # bytes of a y_perm value: fp16 + exponent byte, or fp32
     return {
         "route": {"bytes": T * h * b + h * E * 4 + T * k * (4 + 4 + 1),
                   "flops": 2 * T * h * E},
         "permute": {"bytes": T * h * b + R * h * q + T * k * (4 + 1 + 4)},
         "fc1": {"flops": 4 * R * h * f, "bytes": 2 * A * h * f * q + R * h * q + R * f * b},
         "fc2": {"flops": 2 * R * f * h,
-                "bytes": A * f * h * q + R * f * b + (2 * R * f if fp8 else 0) + R * h * 4,
+                "bytes": A * f * h * q + R * f * b + (2 * R * f if fp8 else 0) + R * h * yb,
                 "bytes_algorithmic": A * f * h * q + R * f * b + (2 * R * f if fp8 else 0)
                 + R * h * b},
-        "combine": {"bytes": R * h * 4 + T * h * b + T * k * 8 + (T * h * 4 if w.shared_f else 0),
+        "combine": {"bytes": R * h * yb + T * h * b + T * k * 8 + (T * h * 4 if w.shared_f else 0),
                     # the scope's algorithmic bytes: y_perm in the activation dtype
                     "bytes_algorithmic": R * h * b + T * h * b},
         # top-1: fc2 writes each row, weighted, straight into the token's output
@@ -277,6 +285,11 @@ def run_native(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
     fp8 = args.precision == "e4m3"
     stage_names = stages_of(w, fp8)
+    # the backward reads the forward's fp32 y_perm: its staged forward keeps it
+    f16s = uses_f16s(w, fp8) and args.which == "forward"
+    if f16s:  # y_perm as fp16 + one exponent byte per 32 columns
+        y16 = torch.empty((b.y_perm.shape[0], w.h), dtype=torch.float16, device=dev)
+        y16_exp = torch.empty((b.y_perm.shape[0], w.h // 32), dtype=torch.int8, device=dev)
     if w.shared_f > 0:
         h_mid_s = torch.empty((w.T, w.shared_f), dtype=moe.act_dtype(cfg), device=dev)
         y_shared = torch.empty((w.T, w.h), dtype=torch.float32, device=dev)
@@ -325,13 +338,18 @@ def run_native(args, rank, world, local):
                                         b.topk_prob, b.y, b.ws)
                 if ev: ev[4].record(stream)
                 return
-            moe.grouped_fc2(cfg, b.h_mid, b.expert_offsets, inp["W2"], b.y_perm, b.ws)
+            if f16s:
+                moe.grouped_fc2_f16s(cfg, b.h_mid, b.expert_offsets, inp["W2"], y16, y16_exp, b.ws)
+            else:
+                moe.grouped_fc2(cfg, b.h_mid, b.expert_offsets, inp["W2"], b.y_perm, b.ws)
         if ev: ev[4].record(stream)
         if w.shared_f > 0:
             moe.shared_expert(cfg, w.shared_f, inp["x"], inp["W1s"], inp["W3s"], inp["W2s"],
                               h_mid_s, y_shared, b.ws)
             if ev: ev[5].record(stream)
             moe.combine_shared(cfg, b.y_perm, b.row_map, b.topk_prob, y_shared, b.y)
+        elif f16s:
+            moe.combine_f16s(cfg, y16, y16_exp, b.row_map, b.topk_prob, b.y)
         else:
             moe.combine(cfg, b.y_perm, b.row_map, b.topk_prob, b.y)
         if ev: ev[-1].record(stream)
@@ -464,7 +482,7 @@ def run_native(args, rank, world, local):
         return None
 
     peaks = measured_peaks()
-    work = stage_work(w, R, fp8, active=int(np.count_nonzero(tpe)))
+    work = stage_work(w, R, fp8, active=int(np.count_nonzero(tpe)), y16=f16s)
     stages = {}
     for s in stage_names:
         t = sum(stage_ms[s]) / len(stage_ms[s])

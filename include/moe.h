@@ -230,13 +230,37 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
                        const float* topk_prob, void* y, moe_stream_t stream);
 
 /*
- * fc2 and the combine in one call (layers without pad_to_capacity): the
- * output of moe_grouped_fc2 followed by moe_combine, bit for bit (the same
- * fp32 products, the same slot order, the same single rounding).  For bf16
- * top-1 layers the combine runs in fc2's epilogue: each row goes, weighted,
- * straight into its token's output row, so no y_perm is written or read;
- * the rows of dropped tokens are zeroed.  Other layers run fc2 into the
- * workspace's y_perm and then the combine kernel.
+ * fc2 and the combine over a compact y_perm (bf16 layers): y_perm stored as
+ * fp16 with one power-of-two scale per 32 columns, 2 + 1/32 bytes per value
+ * instead of 4.  Row r's columns 32c .. 32c+31 hold
+ *   y16[r, 32c + i] = fp16(y_perm[r, 32c + i] * 2^-y16_exp[r, c]),
+ * the exponent chosen so that the chunk's largest magnitude lands in
+ * [2^14, 2^15) (clamped to [-126, 113]; 0 for a non-finite chunk): a relative
+ * error of at most 2^-11 per value, against bf16's 2^-8, which measured too
+ * coarse for the layer's bf16 output bar (the output's error beyond its own
+ * rounding must stay under 2e-2 of its RMS).  moe_combine_f16s is
+ * moe_combine over the decoded values (fp16 * 2^exp, exact in fp32): the
+ * same slot-order fp32 sum and one rounding.  moe_forward uses this pair for
+ * bf16 layers with k >= 2 and no pad_to_capacity.
+ * Megatron Core walkthrough §10 (experts) and §2 (combine).
+ *   y16 [R_max,h] fp16, y16_exp [R_max,h/32] int8 (8-byte aligned); other arguments as
+ *   moe_grouped_fc2 / moe_combine.  MOE_ERR_UNSUPPORTED for fp32 layers.
+ */
+moe_status moe_grouped_fc2_f16s(const moe_config* cfg, const void* h_mid,
+                                const int32_t* expert_offsets, const void* W2, void* y16,
+                                int8_t* y16_exp, void* ws, size_t ws_bytes, moe_stream_t stream);
+moe_status moe_combine_f16s(const moe_config* cfg, const void* y16, const int8_t* y16_exp,
+                            const int32_t* row_map, const float* topk_prob, void* y,
+                            moe_stream_t stream);
+
+/*
+ * fc2 and the combine in one call (layers without pad_to_capacity), as
+ * moe_forward runs them.  bf16 top-1 layers: the combine runs in fc2's
+ * epilogue -- each row goes, weighted, straight into its token's output row
+ * (no y_perm; the rows of dropped tokens are zeroed) -- with the bits of
+ * moe_grouped_fc2 followed by moe_combine.  bf16 layers with k >= 2:
+ * moe_grouped_fc2_f16s then moe_combine_f16s over the workspace.  fp32
+ * layers: moe_grouped_fc2 into the workspace, then moe_combine.
  * Megatron Core walkthrough §10 (experts) and §2 (combine).
  *   h_mid [R_max,f] dtype, expert_offsets [E+1], W2 [E,f,h] dtype,
  *   row_map [T,k] int32, topk_prob [T,k] fp32, y [T,h] dtype out.

@@ -33,7 +33,8 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_c
            "moe_backward", "moe_workspace_size_backward_shared", "moe_backward_shared",
            "moe_shared_expert_backward", "moe_workspace_size_host_shared",
            "moe_forward_host_shared", "moe_workspace_size_host_e4m3", "moe_forward_host_e4m3",
-           "moe_permute_map", "moe_permute_map_e4m3", "moe_grouped_fc2_combine"]
+           "moe_permute_map", "moe_permute_map_e4m3", "moe_grouped_fc2_combine",
+           "moe_grouped_fc2_f16s", "moe_combine_f16s"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -83,6 +84,8 @@ def lib():
             "moe_grouped_fc2": ([cfgp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_combine": ([cfgp, vp, vp, vp, vp, vp], i32),
             "moe_grouped_fc2_combine": ([cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_grouped_fc2_f16s": ([cfgp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+            "moe_combine_f16s": ([cfgp, vp, vp, vp, vp, vp, vp], i32),
             "moe_forward": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_check": ([vp, vp, ctypes.POINTER(i32)], i32),
             "moe_permute_noalloc": ([cfgp, vp, vp, vp, vp, vp, vp, vp], i32),
@@ -250,6 +253,21 @@ def grouped_fc2_combine(cfg, h_mid, expert_offsets, W2, row_map, topk_prob, y, w
     _check(lib().moe_grouped_fc2_combine(ctypes.byref(cfg), _p(h_mid), _p(expert_offsets),
                                          _p(W2), _p(row_map), _p(topk_prob), _p(y), w, wb,
                                          _stream()), "moe_grouped_fc2_combine")
+
+
+def grouped_fc2_f16s(cfg, h_mid, expert_offsets, W2, y16, y16_exp, ws):
+    """moe_grouped_fc2_f16s: fc2 with y_perm as fp16 (y16, torch.float16
+    [R, h]) and one power-of-two exponent per 32 columns (y16_exp, int8)."""
+    w, wb = _ws(ws)
+    _check(lib().moe_grouped_fc2_f16s(ctypes.byref(cfg), _p(h_mid), _p(expert_offsets), _p(W2),
+                                      _p(y16), _p(y16_exp), w, wb, _stream()),
+           "moe_grouped_fc2_f16s")
+
+
+def combine_f16s(cfg, y16, y16_exp, row_map, topk_prob, y):
+    """moe_combine_f16s: the combine over that y_perm."""
+    _check(lib().moe_combine_f16s(ctypes.byref(cfg), _p(y16), _p(y16_exp), _p(row_map),
+                                  _p(topk_prob), _p(y), _stream()), "moe_combine_f16s")
 
 
 def combine(cfg, y_perm, row_map, topk_prob, y):

@@ -308,11 +308,23 @@ moe_status do_fc2(const moe_config& c, const void* h_mid, const int32_t* offsets
 
 // fc2 and the combine in one call (layers without pad_to_capacity).  bf16
 // top-1: the combine runs in fc2's epilogue (each row, weighted, straight into
-// its token's output row).  Otherwise fc2 into the workspace's y_perm, then
-// the combine kernel.  The same bits in every case.
+// its token's output row; the bits of fc2 + combine).  bf16 top-k (k >= 2):
+// fc2 writes y_perm as fp16 with one power-of-two scale per 32 columns into
+// the workspace and the combine reads that.  fp32: fc2 into the workspace's
+// y_perm, then the combine kernel.
 bool fc2_combine_ok(const moe_config& c) { return !c.pad_to_capacity; }
 bool fc2_combine_fused(const moe_config& c) {
   return c.topk == 1 && !c.pad_to_capacity && c.dtype == MOE_BF16;
+}
+bool fc2_combine_f16s(const moe_config& c) {
+  return c.topk > 1 && !c.pad_to_capacity && c.dtype == MOE_BF16;
+}
+// The fp16 y_perm inside the workspace's y_perm region: [R, h] fp16, then
+// [R, h/32] exponent bytes (2 + 1/32 bytes per value, within the region's 4).
+void* ws_y16(void* ws, const Layout& L) { return at<void>(ws, L.y_perm); }
+int8_t* ws_y16_exp(const moe_config& c, void* ws, const Layout& L) {
+  const size_t bytes16 = static_cast<size_t>(rows_of(c)) * c.hidden * 2;
+  return at<int8_t>(ws, L.y_perm + align_up(bytes16));
 }
 
 moe_status do_fc2_combine(const moe_config& c, const void* h_mid, const int32_t* offsets,
@@ -321,6 +333,15 @@ moe_status do_fc2_combine(const moe_config& c, const void* h_mid, const int32_t*
   const Layout L = make_layout(c);
   int* err = at<int>(ws, L.err);
   const int64_t rows = rows_of(c);
+  if (fc2_combine_f16s(c)) {
+    void* y16 = ws_y16(ws, L);
+    int8_t* y16e = ws_y16_exp(c, ws, L);
+    MOE_CUDA(launch_tc_fc2_f16s(c.num_experts, c.hidden, c.ffn_hidden, rows, h_mid, offsets, W2,
+                                y16, y16e, err, s));
+    MOE_CUDA(launch_combine_f16s(c.num_tokens, c.hidden, c.topk, y16, y16e, row_map, topk_prob,
+                                 y, s, rows));
+    return MOE_OK;
+  }
   if (!fc2_combine_fused(c)) {
     float* y_perm = at<float>(ws, L.y_perm);
     MOE_TRY(do_fc2(c, h_mid, offsets, W2, y_perm, ws, s));
@@ -1039,6 +1060,44 @@ moe_status moe_grouped_mlp(const moe_config* cfg, const void* x_perm,
   return moe_grouped_fc2(cfg, h_mid, expert_offsets, W2, y_perm, ws, ws_bytes, stream);
 }
 
+moe_status moe_grouped_fc2_f16s(const moe_config* cfg, const void* h_mid,
+                                const int32_t* expert_offsets, const void* W2, void* y16,
+                                int8_t* y16_exp, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const size_t R = static_cast<size_t>(rows_of(c));
+  const size_t wsz = static_cast<size_t>(c.num_experts) * c.hidden * c.ffn_hidden;
+  MOE_TRY(need(h_mid, R * c.ffn_hidden, 16));
+  MOE_TRY(need(expert_offsets, c.num_experts + 1, 4));
+  MOE_TRY(need(W2, wsz, 16));
+  MOE_TRY(need(y16, R * c.hidden, 16));
+  MOE_TRY(need(y16_exp, R * (c.hidden / 32), 8));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  const Layout L = make_layout(c);
+  MOE_CUDA(launch_tc_fc2_f16s(c.num_experts, c.hidden, c.ffn_hidden, rows_of(c), h_mid,
+                              expert_offsets, W2, y16, y16_exp, at<int>(ws, L.err), stream));
+  return MOE_OK;
+}
+
+moe_status moe_combine_f16s(const moe_config* cfg, const void* y16, const int8_t* y16_exp,
+                            const int32_t* row_map, const float* topk_prob, void* y,
+                            moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const size_t T = c.num_tokens, k = c.topk;
+  const size_t R = static_cast<size_t>(rows_of(c));
+  MOE_TRY(need(y16, R * c.hidden, 16));
+  MOE_TRY(need(y16_exp, R * (c.hidden / 32), 8));
+  MOE_TRY(need(row_map, T * k, 4));
+  MOE_TRY(need(topk_prob, T * k, 4));
+  MOE_TRY(need(y, T * c.hidden, 16));
+  MOE_CUDA(launch_combine_f16s(c.num_tokens, c.hidden, c.topk, y16, y16_exp, row_map, topk_prob,
+                               y, stream, rows_of(c)));
+  return MOE_OK;
+}
+
 moe_status moe_grouped_fc2_combine(const moe_config* cfg, const void* h_mid,
                                    const int32_t* expert_offsets, const void* W2,
                                    const int32_t* row_map, const float* topk_prob, void* y,
@@ -1167,7 +1226,9 @@ moe_status moe_forward(const moe_config* cfg, const void* x, const float* Wg,
   MOE_TRY(optional(tokens_per_expert, 4));
   MOE_TRY(check_ws(c, ws, ws_bytes));
   Routed r;
-  const bool fuse = fc2_combine_fused(c);  // top-1: the combine in fc2's epilogue
+  // non-padded layers: fc2 and the combine through do_fc2_combine (top-1 fused,
+  // top-k over the fp16 y_perm)
+  const bool fuse = fc2_combine_ok(c);
   MOE_TRY(routed_path(c, x, Wg, gate_bias, expert_bias, W1, W3, W2, topk_idx, topk_prob,
                       tokens_per_expert, ws, stream, &r, fuse));
   if (fuse) {
@@ -1473,7 +1534,7 @@ moe_status moe_forward_host(const moe_config* cfg, int32_t num_batches, const vo
   return host_pipeline(c, num_batches, x_host, x_batch_stride, y_host, y_batch_stride, row_bytes,
                        H, ws, stream, [&](void* xs, void* ys) {
                          Routed r{};
-                         const bool fuse = fc2_combine_fused(c);
+                         const bool fuse = fc2_combine_ok(c);
                          MOE_TRY(routed_path(c, xs, Wg, gate_bias, expert_bias, W1, W3, W2,
                                              nullptr, nullptr, nullptr, ws, stream, &r, fuse));
                          if (fuse) {

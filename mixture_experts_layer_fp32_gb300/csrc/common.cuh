@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -168,6 +169,16 @@ cudaError_t launch_tc_fc1(int E, int h, int f, int64_t max_rows, const void* x_p
 cudaError_t launch_tc_fc2(int E, int h, int f, int64_t max_rows, const void* h_mid,
                           const int32_t* offsets, const void* W2, float* y_perm, int* err,
                           cudaStream_t s);
+// fc2 with y_perm as fp16 and one power-of-two scale per 32 columns:
+// y16 [rows, h] fp16, y16_exp [rows, h/32] int8, value = fp16 * 2^exp
+cudaError_t launch_tc_fc2_f16s(int E, int h, int f, int64_t max_rows, const void* h_mid,
+                               const int32_t* offsets, const void* W2, void* y16, int8_t* y16_exp,
+                               int* err, cudaStream_t s);
+// The combine reading that y_perm (bf16 output): the same slot-order fp32 sum
+// of p * value, one rounding.
+cudaError_t launch_combine_f16s(int T, int h, int k, const void* y16, const int8_t* y16_exp,
+                                const int32_t* row_map, const float* topk_prob, void* y,
+                                cudaStream_t s, int64_t max_rows);
 // fc2 of a top-1 layer with the combine in the epilogue: y[row_token[r]] =
 // bf16(row_weight[r] * (h_mid[r] . W2[e]))
 cudaError_t launch_tc_fc2_top1(int E, int h, int f, int64_t max_rows, const void* h_mid,

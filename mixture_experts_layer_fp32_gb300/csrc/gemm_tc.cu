@@ -105,7 +105,22 @@ constexpr long long kWaitCycles = 4000000000LL;
 //              is the one slot of token row_token[r], whose output row gets
 //              bf16(row_weight[r] * acc) -- the combine's arithmetic, so the
 //              bits equal fc2 followed by the combine kernel
-enum { FC1 = 0, FC2 = 1, FC1_BWD = 2, DGRAD_BF16 = 3, DGRAD_F32 = 4, FC2_Y = 5 };
+//   FC2_F16S   fc2 with y_perm stored as fp16 plus one power-of-two scale per 32
+//              columns (a row's chunk scaled so that its largest magnitude lands
+//              in [2^14, 2^15)): 2 bytes per value instead of 4, relative error
+//              2^-11 instead of 2^-24
+enum { FC1 = 0, FC2 = 1, FC1_BWD = 2, DGRAD_BF16 = 3, DGRAD_F32 = 4, FC2_Y = 5, FC2_F16S = 6 };
+
+// Exponent of the power-of-two scale of a 32-value chunk whose largest
+// magnitude is amax: amax * 2^-e lies in [2^14, 2^15) for normal amax (e from
+// the float's exponent field, clamped so that 2^-e and 2^e are normal floats);
+// 0 for a non-finite amax (the values pass through the conversion unchanged).
+__device__ __forceinline__ int f16s_exponent(float amax) {
+  const int be = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  if (be == 0xFF) return 0;
+  const int e = be - 127 - 14;
+  return e < -126 ? -126 : e;
+}
 
 struct TcArgs {
   const int32_t* offsets;
@@ -138,6 +153,8 @@ struct TcArgs {
   // FC2_Y: the token of each row (-1: none) and its combine weight
   const int32_t* row_token = nullptr;
   const float* row_weight = nullptr;
+  // FC2_F16S: the chunk exponents [rows, ldo / 32] int8 (the fp16 values go to out)
+  int8_t* exp_out = nullptr;
 };
 
 // Barriers of an NS-stage ring: full[NS], empty[NS], acc_full[2],
@@ -415,6 +432,56 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, uin
                               pack_bf16x2(fmaf(w, v[8 * q + 6], 0.f), fmaf(w, v[8 * q + 7], 0.f)));
       }
     }
+  } else if (MODE == FC2_F16S) {
+    // each lane's row, 32 columns at a time: the chunk's exponent from its
+    // largest magnitude, the values times 2^-e (exact) rounded to fp16, 64
+    // contiguous bytes of fp16 and one exponent byte
+    const int row = rbase + lane;
+    __half* out = static_cast<__half*>(args.out) + static_cast<int64_t>(row) * args.ldo +
+                  static_cast<int64_t>(nt) * BN;
+    int8_t* ex = args.exp_out + static_cast<int64_t>(row) * (args.ldo / 32) + nt * (BN / 32);
+    uint32_t ex_lo = 0, ex_hi = 0;  // the row's 8 exponent bytes of this n-tile, stored together
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t y[32];
+      ptx::tmem_ld32(tb + c, y);
+      ptx::tmem_wait_ld();
+      if (row < rend) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(y[j]);
+        if (FP8) {  // acc * row scale * channel scale, as fc2 stores it
+          const float* cs = args.col_scale0 + static_cast<int64_t>(e) * args.ncols + nt * BN + c;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 u = __ldg(reinterpret_cast<const float4*>(cs + 4 * q));
+            v[4 * q] *= rs * u.x;
+            v[4 * q + 1] *= rs * u.y;
+            v[4 * q + 2] *= rs * u.z;
+            v[4 * q + 3] *= rs * u.w;
+          }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        const int e8 = f16s_exponent(amax);
+        const float down = __uint_as_float(static_cast<uint32_t>(127 - e8) << 23);  // 2^-e
+        uint32_t hw[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          __half2 hv = __floats2half2_rn(v[2 * j] * down, v[2 * j + 1] * down);
+          hw[j] = *reinterpret_cast<uint32_t*>(&hv);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[q] = make_uint4(hw[4 * q], hw[4 * q + 1], hw[4 * q + 2], hw[4 * q + 3]);
+        const uint32_t byte = static_cast<uint32_t>(e8) & 0xFFu;
+        if (c < 128) ex_lo |= byte << (c / 4);  // chunk c/32 at bit 8 * (c/32)
+        else ex_hi |= byte << ((c - 128) / 4);
+      }
+    }
+    if (row < rend) *reinterpret_cast<uint2*>(ex) = make_uint2(ex_lo, ex_hi);
   } else if (MODE == DGRAD_BF16) {
     // plain bf16 output, 256 columns: each lane writes 64 bytes of its row per
     // chunk; chunks at or past ncols (the last tile when ncols % 256 == 128)
@@ -1250,6 +1317,18 @@ cudaError_t launch_tc_fc2_top1(int E, int h, int f, int64_t max_rows, const void
   args.row_token = row_token;
   args.row_weight = row_weight;
   return launch_grouped<FC2_Y, false>(a, b0, b0, a, args, s);
+}
+
+cudaError_t launch_tc_fc2_f16s(int E, int h, int f, int64_t max_rows, const void* h_mid,
+                               const int32_t* offsets, const void* W2, void* y16, int8_t* y16_exp,
+                               int* err, cudaStream_t s) {
+  if (max_rows == 0) return cudaSuccess;
+  CUtensorMap a, b0;
+  if (!map_rows(&a, h_mid, f, max_rows) || !map_weights(&b0, W2, h, f, E))
+    return cudaErrorInvalidValue;
+  TcArgs args{offsets, E, h / BN, f / BK, max_rows, y16, h, err};
+  args.exp_out = y16_exp;
+  return launch_grouped<FC2_F16S, false>(a, b0, b0, a, args, s);
 }
 
 // ---- backward GEMMs (bf16 operands, 64-wide K stages; SM pairs by the

@@ -904,6 +904,110 @@ cudaError_t launch_perm_copy_e4m3(int T, int h, int k, const void* x, const int3
   return cudaGetLastError();
 }
 
+// Combine over a y_perm stored as fp16 with one power-of-two scale per 32
+// columns (value = fp16 * 2^exp, exact in fp32): per token the kept slots'
+// values in slot order, fp32 FMA with the weights, one rounding to bf16 --
+// the combine kernel's arithmetic on the decoded values.  A thread takes 8
+// columns (16 bytes of fp16 and the chunk's exponent byte) of U vectors at a
+// time; the loads of every slot (at most KMAX) are issued before the sum, so
+// KMAX * U * 16 bytes per thread are in flight.
+template <int TPI_LOG2, int KMAX, int U>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_f16s_kernel(int T, int h, int k, int64_t max_rows, const uint4* __restrict__ y16,
+                        const int8_t* __restrict__ y16_exp, const int32_t* __restrict__ row_map,
+                        const float* __restrict__ topk_prob, uint4* __restrict__ y) {
+  const int h8 = h >> 3;    // 16-byte vectors per row
+  const int nch = h >> 5;   // exponent bytes per row
+  constexpr int tpt = kCombineThreads >> TPI_LOG2;
+  const int sub = threadIdx.x / tpt, lt = threadIdx.x % tpt;
+  constexpr int tpi = 1 << TPI_LOG2;
+  for (int t0 = blockIdx.x * tpi; t0 < T; t0 += gridDim.x * tpi) {
+    const int t = t0 + sub;
+    if (t >= T) continue;  // no barriers in this kernel
+    int rows[KMAX];
+    float p[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      rows[j] = (j < k) ? row_map[(int64_t)t * k + j] : -1;
+      if (rows[j] >= max_rows) rows[j] = -1;  // a row outside y_perm is treated as dropped
+      p[j] = (rows[j] >= 0) ? topk_prob[(int64_t)t * k + j] : 0.f;
+    }
+    for (int v0 = lt; v0 < h8; v0 += U * tpt) {
+      uint4 a[KMAX][U];
+      int ex[KMAX][U];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * tpt;
+          const bool ld = rows[j] >= 0 && v < h8;
+          a[j][u] = ld ? __ldcs(y16 + (int64_t)rows[j] * h8 + v) : make_uint4(0u, 0u, 0u, 0u);
+          ex[j][u] = ld ? y16_exp[(int64_t)rows[j] * nch + (v >> 2)] : 0;
+        }
+      // one vector at a time: its slots in order, then its store (8 sums live)
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * tpt;
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          if (rows[j] < 0) continue;
+          const float up = __uint_as_float(static_cast<uint32_t>(127 + ex[j][u]) << 23);  // 2^e
+          const uint32_t w4[4] = {a[j][u].x, a[j][u].y, a[j][u].z, a[j][u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[q]));
+            acc[2 * q] = fmaf(p[j], f.x * up, acc[2 * q]);
+            acc[2 * q + 1] = fmaf(p[j], f.y * up, acc[2 * q + 1]);
+          }
+        }
+        if (v >= h8) continue;
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+          o[q] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        __stcs(y + (int64_t)t * h8 + v, make_uint4(o[0], o[1], o[2], o[3]));
+      }
+    }
+  }
+}
+
+template <int KMAX, int U>
+void launch_combine_f16s_t(int l, int grid, cudaStream_t s, int T, int h, int k, int64_t max_rows,
+                           const uint4* src, const int8_t* ex, const int32_t* row_map,
+                           const float* topk_prob, uint4* dst) {
+  switch (l) {
+    case 0: combine_f16s_kernel<0, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, dst); break;
+    case 1: combine_f16s_kernel<1, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, dst); break;
+    case 2: combine_f16s_kernel<2, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, dst); break;
+    default: combine_f16s_kernel<3, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, dst); break;
+  }
+}
+
+cudaError_t launch_combine_f16s(int T, int h, int k, const void* y16, const int8_t* y16_exp,
+                                const int32_t* row_map, const float* topk_prob, void* y,
+                                cudaStream_t s, int64_t max_rows) {
+  if (T == 0) return cudaSuccess;
+  const uint4* src = static_cast<const uint4*>(y16);
+  uint4* dst = static_cast<uint4*>(y);
+  // 128 bytes of loads per thread in flight: 2 slots x 4 vectors, 4 x 2 or 8 x 1
+  const int U = k <= 2 ? 4 : k <= 4 ? 2 : 1;
+  const int l = tokens_per_round_log2(h / 8, kCombineThreads, U, 3);
+  const int grid = grid_for_tokens((T + (1 << l) - 1) >> l, 8);
+  if (k <= 2)
+    launch_combine_f16s_t<2, 4>(l, grid, s, T, h, k, max_rows, src, y16_exp, row_map, topk_prob, dst);
+  else if (k <= 4)
+    launch_combine_f16s_t<4, 2>(l, grid, s, T, h, k, max_rows, src, y16_exp, row_map, topk_prob, dst);
+  else
+    launch_combine_f16s_t<MOE_MAX_TOPK, 1>(l, grid, s, T, h, k, max_rows, src, y16_exp, row_map,
+                                           topk_prob, dst);
+  return cudaGetLastError();
+}
+
 // Top-1 layers whose combine runs in fc2's epilogue: each row's token and
 // combine weight (row_map inverted: a top-1 token owns at most one row), and
 // zeros for the output rows of tokens whose pair was dropped -- what the

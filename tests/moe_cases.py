@@ -131,8 +131,19 @@ def to_dev(inp, device="cuda"):
     return {k: (None if v is None else v.to(device).contiguous()) for k, v in inp.items()}
 
 
-def gpu_stages(w, dinp, with_routing_map=True):
-    """Run the five stages through the C ABI; returns the Buffers object."""
+def uses_f16s(w):
+    """bf16 layers with k >= 2 (no padding, no shared expert): the forward
+    combines over y_perm stored as fp16 with a power-of-two scale per 32
+    columns (moe_grouped_fc2_f16s + moe_combine_f16s)."""
+    return w.dtype == "bf16" and w.k > 1 and not w.pad_to_capacity and w.shared_f == 0
+
+
+def gpu_stages(w, dinp, with_routing_map=True, fp32_combine=False):
+    """Run the stages through the C ABI as the forward does; returns the
+    Buffers object.  y_perm (fp32, moe_grouped_fc2) is always computed for
+    the intermediate checks; y comes from the combine the forward uses (for
+    uses_f16s layers the fp16 y_perm path, its y16 / y16_exp kept on the
+    Buffers) unless fp32_combine."""
     import mixture_experts_layer_fp32_gb300 as moe
     cfg = gpu_config(w)
     b = moe.Buffers(cfg)
@@ -153,6 +164,11 @@ def gpu_stages(w, dinp, with_routing_map=True):
         moe.shared_expert(cfg, w.shared_f, dinp["x"], dinp["W1s"], dinp["W3s"], dinp["W2s"],
                           b.h_mid_s, b.y_shared, b.ws)
         moe.combine_shared(cfg, b.y_perm, b.row_map, b.topk_prob, b.y_shared, b.y)
+    elif uses_f16s(w) and not fp32_combine:
+        b.y16 = torch.empty((b.y_perm.shape[0], w.h), dtype=torch.float16, device="cuda")
+        b.y16_exp = torch.empty((b.y_perm.shape[0], w.h // 32), dtype=torch.int8, device="cuda")
+        moe.grouped_fc2_f16s(cfg, b.h_mid, b.expert_offsets, dinp["W2"], b.y16, b.y16_exp, b.ws)
+        moe.combine_f16s(cfg, b.y16, b.y16_exp, b.row_map, b.topk_prob, b.y)
     else:
         moe.combine(cfg, b.y_perm, b.row_map, b.topk_prob, b.y)
     moe.check(b.ws)

@@ -13,6 +13,7 @@ kernels, with every dropped token's row zero; and it is checked against
 the oracle.
 """
 
+import numpy as np
 import pytest
 import torch
 
@@ -59,6 +60,8 @@ def case(request):
 
 @pytest.mark.parametrize("kernel", ["single", "pair"])
 def test_fused_equals_fc2_then_combine(case, kernel, monkeypatch):
+    # gpu_stages ran the staged calls the forward uses: fc2 + combine over the
+    # fp32 y_perm (top-1, fp32), or fc2_f16s + combine_f16s (bf16, k >= 2)
     import mixture_experts_layer_fp32_gb300 as moe
     w, inp, ref, d, b = case
     monkeypatch.setenv("MOE_TC_PAIR", "1" if kernel == "pair" else "0")
@@ -75,3 +78,29 @@ def test_fused_equals_fc2_then_combine(case, kernel, monkeypatch):
         assert dropped.any()
     assert (to_np(y)[dropped] == 0).all()
     assert_close("y", to_np(y), ref["y"], w.dtype)
+
+
+def _decode(y16, y16_exp):
+    """Values of the fp16 y_perm: fp16 * 2^exp per 32-column chunk (float64)."""
+    v = y16.double().cpu()
+    e = torch.repeat_interleave(y16_exp.cpu().long(), 32, dim=1)
+    return (v * torch.pow(2.0, e.double())).numpy()
+
+
+def test_f16s_y_perm_against_fp32(case):
+    # the fp16 y_perm against the fp32 one from the same fc2 products: each chunk's
+    # scale puts its largest magnitude in [2^14, 2^15] (2^15 when it rounds up to
+    # it), so every value is within
+    # 2^-11 of its magnitude (round to nearest fp16) plus the fp16 underflow step
+    w, inp, ref, d, b = case
+    if not hasattr(b, "y16"):
+        pytest.skip("this layer combines over the fp32 y_perm")
+    R = int(b.expert_offsets[-1].item())
+    got = _decode(b.y16[:R], b.y16_exp[:R])
+    want = to_np(b.y_perm[:R]).astype(np.float64)
+    chunk_max = np.abs(want).reshape(R, -1, 32).max(axis=2)
+    floor = np.repeat(chunk_max * 2.0 ** -29, 32, axis=1)
+    assert (np.abs(got - want) <= 2.0 ** -11 * np.abs(want) + floor).all()
+    h16 = np.abs(b.y16[:R].float().cpu().numpy()).reshape(R, -1, 32).max(axis=2)
+    nz = chunk_max > 0
+    assert ((h16[nz] >= 2.0 ** 14) & (h16[nz] <= 2.0 ** 15)).all()
