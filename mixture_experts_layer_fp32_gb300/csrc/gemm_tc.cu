@@ -434,13 +434,79 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, uin
     }
   } else if (MODE == FC2_F16S) {
     // each lane's row, 32 columns at a time: the chunk's exponent from its
-    // largest magnitude, the values times 2^-e (exact) rounded to fp16, 64
-    // contiguous bytes of fp16 and one exponent byte
+    // largest magnitude, the values times 2^-e (exact) rounded to fp16, and
+    // one exponent byte per chunk (the row's 8 of this n-tile stored together)
     const int row = rbase + lane;
+    int8_t* ex = args.exp_out + static_cast<int64_t>(row) * (args.ldo / 32) + nt * (BN / 32);
+    uint32_t ex_lo = 0, ex_hi = 0;
+    if (args.tma_out) {
+      if (lane == 0) ptx::bulk_wait_group_read<0>();  // the staging block is free
+      __syncwarp();
+    }
+    if (args.tma_out && rbase + 32 <= rend) {
+      // every row of the warp is the expert's: 64 columns (two chunks) at a
+      // time, 32 rows x 128 bytes of fp16 in the 128-byte swizzle (16-byte
+      // piece j of row l at piece j ^ (l & 7)), one TMA store from lane 0
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 64) {
+        uint32_t y[2][32];
+        ptx::tmem_ld32(tb + c, y[0]);
+        ptx::tmem_ld32(tb + c + 32, y[1]);
+        ptx::tmem_wait_ld();
+        uint32_t hw[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(y[half][j]);
+          if (FP8) {  // acc * row scale * channel scale, as fc2 stores it
+            const float* cs =
+                args.col_scale0 + static_cast<int64_t>(e) * args.ncols + nt * BN + c + 32 * half;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 u = __ldg(reinterpret_cast<const float4*>(cs + 4 * q));
+              v[4 * q] *= rs * u.x;
+              v[4 * q + 1] *= rs * u.y;
+              v[4 * q + 2] *= rs * u.z;
+              v[4 * q + 3] *= rs * u.w;
+            }
+          }
+          float amax = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+          const int e8 = f16s_exponent(amax);
+          const float down = __uint_as_float(static_cast<uint32_t>(127 - e8) << 23);  // 2^-e
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            __half2 hv = __floats2half2_rn(v[2 * j] * down, v[2 * j + 1] * down);
+            hw[16 * half + j] = *reinterpret_cast<uint32_t*>(&hv);
+          }
+          const int cc = c + 32 * half;  // chunk cc/32 at byte cc/32 of the 8
+          const uint32_t byte = static_cast<uint32_t>(e8) & 0xFFu;
+          if (cc < 128) ex_lo |= byte << (cc / 4);
+          else ex_hi |= byte << ((cc - 128) / 4);
+        }
+        if (c > 0) {
+          if (lane == 0) ptx::bulk_wait_group_read<0>();
+          __syncwarp();
+        }
+        const uint32_t srow = stg + lane * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_shared_v4(srow + ((j ^ (lane & 7)) << 4), hw[4 * j], hw[4 * j + 1], hw[4 * j + 2],
+                       hw[4 * j + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(tmC, nt * BN + c, rbase, stg);
+          ptx::bulk_commit_group();
+        }
+      }
+      *reinterpret_cast<uint2*>(ex) = make_uint2(ex_lo, ex_hi);
+      return;
+    }
     __half* out = static_cast<__half*>(args.out) + static_cast<int64_t>(row) * args.ldo +
                   static_cast<int64_t>(nt) * BN;
-    int8_t* ex = args.exp_out + static_cast<int64_t>(row) * (args.ldo / 32) + nt * (BN / 32);
-    uint32_t ex_lo = 0, ex_hi = 0;  // the row's 8 exponent bytes of this n-tile, stored together
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t y[32];
@@ -1187,6 +1253,21 @@ bool map_out_f32(CUtensorMap* m, float* ptr, int64_t N, int64_t ld, int64_t rows
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp16 output map [rows, N] (row stride ld elements), box 64 x 32 in the
+// 128-byte swizzle: one epilogue warp's 32 rows x 64 columns per store.
+bool map_out_f16(CUtensorMap* m, void* ptr, int64_t N, int64_t ld, int64_t rows) {
+  if (ld % 8 != 0 || (reinterpret_cast<uintptr_t>(ptr) & 15) != 0 || N % 64 != 0) return false;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ptr, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Sets args->tma_out and fills *c when the fp32 output [max_rows, N] (row
 // stride args->ldo) can be stored by TMA; MOE_TC_TMA_OUT=0 in the
 // environment keeps the row-segment stores (a tuning override).
@@ -1328,7 +1409,10 @@ cudaError_t launch_tc_fc2_f16s(int E, int h, int f, int64_t max_rows, const void
     return cudaErrorInvalidValue;
   TcArgs args{offsets, E, h / BN, f / BK, max_rows, y16, h, err};
   args.exp_out = y16_exp;
-  return launch_grouped<FC2_F16S, false>(a, b0, b0, a, args, s);
+  CUtensorMap c = a;  // whole warps store by TMA (MOE_TC_TMA_OUT=0 keeps per-lane stores)
+  const char* force = getenv("MOE_TC_TMA_OUT");
+  if (!(force && force[0] == '0') && map_out_f16(&c, y16, h, h, max_rows)) args.tma_out = 1;
+  return launch_grouped<FC2_F16S, false>(a, b0, b0, c, args, s);
 }
 
 // ---- backward GEMMs (bf16 operands, 64-wide K stages; SM pairs by the

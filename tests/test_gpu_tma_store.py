@@ -1,6 +1,7 @@
-"""The two stores of the grouped GEMM's fp32 outputs give the same bits.
+"""The two stores of the grouped GEMM's fp32 and fp16 outputs give the same bits.
 
-fc2's y_perm, the E4M3 fc2's y_perm and the backward's fp32 dx (fc1's dgrad
+fc2's y_perm (fp32, or fp16 with a scale per 32 columns for bf16 top-k
+layers), the E4M3 fc2's y_perm and the backward's fp32 dx (fc1's dgrad
 over [W1 ; W3], and the router's dx on the dense tensor-core path) leave the
 accumulator either through TMA tile stores of 32 x 32 blocks (a warp whose 32
 rows all belong to the tile's expert) or through masked row-segment stores (a
@@ -54,6 +55,9 @@ def test_forward_stores_agree(name, kernel):
     assert R > 0
     assert torch.equal(a.expert_offsets, b.expert_offsets)
     assert torch.equal(a.y_perm[:R], b.y_perm[:R])
+    if hasattr(a, "y16"):  # the fp16 y_perm: 32 x 64 TMA boxes or per-lane row stores
+        assert torch.equal(a.y16[:R].view(torch.int16), b.y16[:R].view(torch.int16))
+        assert torch.equal(a.y16_exp[:R], b.y16_exp[:R])
     assert torch.equal(a.y, b.y)
 
 
