@@ -55,10 +55,13 @@ def fused_top1(w, fp8=False):
 
 
 def uses_f16s(w, fp8=False):
-    """bf16 layers with k >= 2 (no padding, no shared expert) keep y_perm as
-    fp16 with a power-of-two scale per 32 columns (moe_grouped_fc2_f16s +
-    moe_combine_f16s), as moe_forward does."""
-    return w.dtype == "bf16" and w.k > 1 and not w.pad_to_capacity and w.shared_f == 0 and not fp8
+    """bf16 layers with k >= 2 (no padding, no shared expert) and every E4M3
+    layer keep y_perm as fp16 with a power-of-two scale per 32 columns
+    (moe_grouped_fc2_f16s or moe_grouped_fc2_e4m3_f16s, then moe_combine_f16s),
+    as moe_forward and moe_forward_e4m3 do."""
+    if fp8:
+        return True
+    return w.dtype == "bf16" and w.k > 1 and not w.pad_to_capacity and w.shared_f == 0
 
 
 def stages_of(w, fp8=False):
@@ -321,7 +324,8 @@ def run_native(args, rank, world, local):
             if ev: ev[2].record(stream)
             moe.grouped_fc1_e4m3(cfg, xq, xs, b.expert_offsets, q, b.h_mid, b.ws)
             if ev: ev[3].record(stream)
-            moe.grouped_fc2_e4m3(cfg, b.h_mid, b.expert_offsets, q, hq, hs, b.y_perm, b.ws)
+            moe.grouped_fc2_e4m3_f16s(cfg, b.h_mid, b.expert_offsets, q, hq, hs, y16, y16_exp,
+                                      b.ws)
         else:
             if w.pad_to_capacity:  # the padded routing map drives the permutation
                 moe.permute_map(cfg, inp["x"], b.routing_map, b.topk_idx, b.keep, b.x_perm,

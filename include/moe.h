@@ -394,6 +394,14 @@ moe_status moe_grouped_fc2_e4m3(const moe_config* cfg, const void* h_mid,
                                 const int32_t* expert_offsets, const uint8_t* W2q,
                                 const float* s2, uint8_t* h_q, float* h_scale, float* y_perm,
                                 void* ws, size_t ws_bytes, moe_stream_t stream);
+/* moe_grouped_fc2_e4m3 with y_perm stored as fp16 and one power-of-two scale
+ * per 32 columns (y16, y16_exp: the layout of moe_grouped_fc2_f16s), for
+ * moe_combine_f16s.  moe_forward_e4m3 runs this pair. */
+moe_status moe_grouped_fc2_e4m3_f16s(const moe_config* cfg, const void* h_mid,
+                                     const int32_t* expert_offsets, const uint8_t* W2q,
+                                     const float* s2, uint8_t* h_q, float* h_scale, void* y16,
+                                     int8_t* y16_exp, void* ws, size_t ws_bytes,
+                                     moe_stream_t stream);
 moe_status moe_forward_e4m3(const moe_config* cfg, const void* x, const float* Wg,
                             const float* gate_bias, const float* expert_bias, const uint8_t* W1q,
                             const float* s1, const uint8_t* W3q, const float* s3,

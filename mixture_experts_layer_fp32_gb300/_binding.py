@@ -34,7 +34,7 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_last_cuda_error", "moe_c
            "moe_shared_expert_backward", "moe_workspace_size_host_shared",
            "moe_forward_host_shared", "moe_workspace_size_host_e4m3", "moe_forward_host_e4m3",
            "moe_permute_map", "moe_permute_map_e4m3", "moe_grouped_fc2_combine",
-           "moe_grouped_fc2_f16s", "moe_combine_f16s"]
+           "moe_grouped_fc2_f16s", "moe_combine_f16s", "moe_grouped_fc2_e4m3_f16s"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -107,6 +107,7 @@ def lib():
             "moe_forward_e4m3": ([cfgp] + [vp] * 14 + [vp, sz, vp], i32),
             "moe_grouped_fc1_e4m3": ([cfgp] + [vp] * 8 + [vp, sz, vp], i32),
             "moe_grouped_fc2_e4m3": ([cfgp] + [vp] * 7 + [vp, sz, vp], i32),
+            "moe_grouped_fc2_e4m3_f16s": ([cfgp] + [vp] * 8 + [vp, sz, vp], i32),
             "moe_workspace_size_backward": ([cfgp, ctypes.POINTER(sz)], i32),
             "moe_backward": ([cfgp] + [vp] * 20 + [vp, sz, vp], i32),
             "moe_workspace_size_backward_shared": ([cfgp, i32, ctypes.POINTER(sz)], i32),
@@ -487,6 +488,16 @@ def grouped_fc2_e4m3(cfg, h_mid, expert_offsets, q, h_q, h_scale, y_perm, ws):
     _check(lib().moe_grouped_fc2_e4m3(ctypes.byref(cfg), _p(h_mid), _p(expert_offsets),
                                       _p(q.W2q), _p(q.s2), _p(h_q), _p(h_scale), _p(y_perm), w,
                                       wb, _stream()), "moe_grouped_fc2_e4m3")
+
+
+def grouped_fc2_e4m3_f16s(cfg, h_mid, expert_offsets, q, h_q, h_scale, y16, y16_exp, ws):
+    """moe_grouped_fc2_e4m3_f16s: the E4M3 fc2 into the fp16 y_perm (a
+    power-of-two scale per 32 columns), for combine_f16s."""
+    w, wb = _ws(ws)
+    _check(lib().moe_grouped_fc2_e4m3_f16s(ctypes.byref(cfg), _p(h_mid), _p(expert_offsets),
+                                           _p(q.W2q), _p(q.s2), _p(h_q), _p(h_scale), _p(y16),
+                                           _p(y16_exp), w, wb, _stream()),
+           "moe_grouped_fc2_e4m3_f16s")
 
 
 def forward_e4m3(cfg, x, Wg, gate_bias, expert_bias, q, y, ws, topk_idx=None, topk_prob=None,

@@ -508,12 +508,13 @@ moe_status do_permute_map_e4m3(const moe_config& c, const void* x, const uint8_t
 }
 
 // E4M3 experts: fc1 (scaled, SwiGLU, bf16 h_mid), per-row quantisation of the
-// rows that exist (expert_offsets[E] on the device), fc2 (scaled, fp32).
+// rows that exist (expert_offsets[E] on the device), fc2 (scaled) into the
+// fp32 y_perm, or, with y16, into the fp16 y_perm with a scale per 32 columns.
 moe_status do_mlp_e4m3(const moe_config& c, const uint8_t* xperm_q, const float* xperm_s,
                        const int32_t* offsets, const uint8_t* W1q, const float* s1,
                        const uint8_t* W3q, const float* s3, const uint8_t* W2q, const float* s2,
                        void* h_mid, uint8_t* hq, float* hs, float* y_perm, void* ws,
-                       cudaStream_t s) {
+                       cudaStream_t s, void* y16 = nullptr, int8_t* y16_exp = nullptr) {
   const Layout L = make_layout(c);
   int* err = at<int>(ws, L.err);
   const int64_t rows = rows_of(c);
@@ -521,7 +522,11 @@ moe_status do_mlp_e4m3(const moe_config& c, const uint8_t* xperm_q, const float*
   MOE_CUDA(launch_tc_fc1_e4m3(E, h, f, rows, xperm_q, xperm_s, nullptr, offsets, W1q, s1, W3q,
                               s3, h_mid, err, s));
   MOE_CUDA(launch_quantize_rows(rows, f, h_mid, hq, hs, offsets + E, s));
-  MOE_CUDA(launch_tc_fc2_e4m3(E, h, f, rows, hq, hs, offsets, W2q, s2, y_perm, err, s));
+  if (y16)
+    MOE_CUDA(launch_tc_fc2_e4m3_f16s(E, h, f, rows, hq, hs, offsets, W2q, s2, y16, y16_exp, err,
+                                     s));
+  else
+    MOE_CUDA(launch_tc_fc2_e4m3(E, h, f, rows, hq, hs, offsets, W2q, s2, y_perm, err, s));
   return MOE_OK;
 }
 
@@ -856,11 +861,15 @@ moe_status e4m3_forward_body(const moe_config& c, const void* x, const float* Wg
                                 stream));
   else
     MOE_TRY(do_permute_e4m3(c, x, idx, keep, xperm_q, xperm_s, row_map, offsets, ws, stream));
+  // y_perm as fp16 with one power-of-two scale per 32 columns (the compact
+  // y_perm of the bf16 forward), in the workspace's y_perm region
+  void* y16 = ws_y16(ws, L);
+  int8_t* y16e = ws_y16_exp(c, ws, L);
   MOE_TRY(do_mlp_e4m3(c, xperm_q, xperm_s, offsets, W1q, s1, W3q, s3, W2q, s2,
-                      at<void>(ws, L.h_mid), at<uint8_t>(ws, Q.hq), at<float>(ws, Q.hs),
-                      at<float>(ws, L.y_perm), ws, stream));
-  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, at<float>(ws, L.y_perm),
-                          row_map, prob, nullptr, y, stream, rows_of(c)));
+                      at<void>(ws, L.h_mid), at<uint8_t>(ws, Q.hq), at<float>(ws, Q.hs), nullptr,
+                      ws, stream, y16, y16e));
+  MOE_CUDA(launch_combine_f16s(c.num_tokens, c.hidden, c.topk, y16, y16e, row_map, prob, y, stream,
+                               rows_of(c)));
   return MOE_OK;
 }
 
@@ -1402,6 +1411,34 @@ moe_status moe_grouped_fc2_e4m3(const moe_config* cfg, const void* h_mid,
                                 expert_offsets + c.num_experts, stream));
   MOE_CUDA(launch_tc_fc2_e4m3(c.num_experts, c.hidden, c.ffn_hidden, static_cast<int64_t>(R), h_q,
                               h_scale, expert_offsets, W2q, s2, y_perm, err, stream));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_fc2_e4m3_f16s(const moe_config* cfg, const void* h_mid,
+                                     const int32_t* expert_offsets, const uint8_t* W2q,
+                                     const float* s2, uint8_t* h_q, float* h_scale, void* y16,
+                                     int8_t* y16_exp, void* ws, size_t ws_bytes,
+                                     moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config& c = *cfg;
+  MOE_TRY(validate_e4m3(c));
+  const size_t R = static_cast<size_t>(rows_of(c)), E = c.num_experts;
+  const size_t h = c.hidden, f = c.ffn_hidden;
+  MOE_TRY(need(h_mid, R * f, 16));
+  MOE_TRY(need(expert_offsets, E + 1, 4));
+  MOE_TRY(need(W2q, E * h * f, 16));
+  MOE_TRY(need(s2, E * h, 16));
+  MOE_TRY(need(h_q, R * f, 16));
+  MOE_TRY(need(h_scale, R, 4));
+  MOE_TRY(need(y16, R * h, 16));
+  MOE_TRY(need(y16_exp, R * (h / 32), 8));
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  int* err = at<int>(ws, make_layout(c).err);
+  MOE_CUDA(launch_quantize_rows(static_cast<int64_t>(R), c.ffn_hidden, h_mid, h_q, h_scale,
+                                expert_offsets + c.num_experts, stream));
+  MOE_CUDA(launch_tc_fc2_e4m3_f16s(c.num_experts, c.hidden, c.ffn_hidden, static_cast<int64_t>(R),
+                                   h_q, h_scale, expert_offsets, W2q, s2, y16, y16_exp, err,
+                                   stream));
   return MOE_OK;
 }
 

@@ -193,6 +193,11 @@ cudaError_t launch_tc_fc1_e4m3(int E, int h, int f, int64_t max_rows, const uint
                                const int32_t* offsets, const uint8_t* W1q, const float* s1,
                                const uint8_t* W3q, const float* s3, void* h_mid, int* err,
                                cudaStream_t s);
+// E4M3 fc2 with the fp16 y_perm (one power-of-two scale per 32 columns)
+cudaError_t launch_tc_fc2_e4m3_f16s(int E, int h, int f, int64_t max_rows, const uint8_t* hq,
+                                    const float* h_scale, const int32_t* offsets,
+                                    const uint8_t* W2q, const float* s2, void* y16,
+                                    int8_t* y16_exp, int* err, cudaStream_t s);
 cudaError_t launch_tc_fc2_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* hq,
                                const float* h_scale, const int32_t* offsets, const uint8_t* W2q,
                                const float* s2, float* y_perm, int* err, cudaStream_t s);

@@ -1503,6 +1503,25 @@ cudaError_t launch_tc_fc1_e4m3(int E, int h, int f, int64_t max_rows, const uint
   return launch_grouped<FC1, true>(a, b0, b1, a, args, s);
 }
 
+cudaError_t launch_tc_fc2_e4m3_f16s(int E, int h, int f, int64_t max_rows, const uint8_t* hq,
+                                    const float* h_scale, const int32_t* offsets,
+                                    const uint8_t* W2q, const float* s2, void* y16,
+                                    int8_t* y16_exp, int* err, cudaStream_t s) {
+  if (max_rows == 0) return cudaSuccess;
+  CUtensorMap a, b0;
+  if (!map_rows_e4m3(&a, hq, f, max_rows) || !map_weights_e4m3(&b0, W2q, f, h, E))
+    return cudaErrorInvalidValue;
+  TcArgs args{offsets, E, h / BN, f / KE_FP8, max_rows, y16, h, err};
+  args.row_scale = h_scale;
+  args.col_scale0 = s2;
+  args.ncols = h;
+  args.exp_out = y16_exp;
+  CUtensorMap c = a;
+  const char* force = getenv("MOE_TC_TMA_OUT");
+  if (!(force && force[0] == '0') && map_out_f16(&c, y16, h, h, max_rows)) args.tma_out = 1;
+  return launch_grouped<FC2_F16S, true>(a, b0, b0, c, args, s);
+}
+
 cudaError_t launch_tc_fc2_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* hq,
                                const float* h_scale, const int32_t* offsets, const uint8_t* W2q,
                                const float* s2, float* y_perm, int* err, cudaStream_t s) {

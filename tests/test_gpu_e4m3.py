@@ -113,7 +113,12 @@ def gpu_stages_e4m3(w, d):
                          b.expert_offsets, ws)
     moe.grouped_mlp_e4m3(cfg, b.x_perm_q, b.x_perm_s, b.expert_offsets, q, b.h_mid, b.h_q,
                          b.h_s, b.y_perm, ws)
-    moe.combine(cfg, b.y_perm, b.row_map, b.topk_prob, b.y)
+    # the forward's fc2 and combine: y_perm as fp16 with a scale per 32 columns
+    b.y16 = torch.empty((R, w.h), dtype=torch.float16, device="cuda")
+    b.y16_exp = torch.empty((R, w.h // 32), dtype=torch.int8, device="cuda")
+    moe.grouped_fc2_e4m3_f16s(cfg, b.h_mid, b.expert_offsets, q, b.h_q, b.h_s, b.y16, b.y16_exp,
+                              ws)
+    moe.combine_f16s(cfg, b.y16, b.y16_exp, b.row_map, b.topk_prob, b.y)
     moe.check(ws)
     b.q, b.ws_e4m3 = q, ws
     return b
@@ -151,6 +156,12 @@ def test_e4m3_layer_matches_oracle(case, kernel, monkeypatch):
         d_rows = np.nonzero(diff)[0]
         assert np.all(np.abs(hq - ref["hq"].astype(np.int32))[diff][same_scale[d_rows]] == 1)
     assert_close("y_perm", to_np(b.y_perm[:R]), ref["y_perm"], "bf16")
+    # the fp16 y_perm: within 2^-11 of the fp32 one (plus the fp16 underflow step of its chunk)
+    got = b.y16[:R].double().cpu() * torch.pow(2.0, torch.repeat_interleave(
+        b.y16_exp[:R].cpu().long(), 32, dim=1).double())
+    want = b.y_perm[:R].double().cpu()
+    cmax = torch.repeat_interleave(want.abs().reshape(R, -1, 32).amax(dim=2), 32, dim=1)
+    assert ((got - want).abs() <= 2.0 ** -11 * want.abs() + 2.0 ** -29 * cmax).all()
     assert_close("y", to_np(b.y), ref["y"], w.dtype)
 
 
