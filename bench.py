@@ -61,7 +61,9 @@ def uses_f16s(w, fp8=False):
     as moe_forward and moe_forward_e4m3 do."""
     if fp8:
         return True
-    return w.dtype == "bf16" and w.k > 1 and not w.pad_to_capacity and w.shared_f == 0
+    if w.dtype != "bf16" or w.pad_to_capacity:
+        return False
+    return w.k > 1 or w.shared_f > 0  # top-1 without a shared expert: fc2+combine fused
 
 
 def stages_of(w, fp8=False):
@@ -351,7 +353,11 @@ def run_native(args, rank, world, local):
             moe.shared_expert(cfg, w.shared_f, inp["x"], inp["W1s"], inp["W3s"], inp["W2s"],
                               h_mid_s, y_shared, b.ws)
             if ev: ev[5].record(stream)
-            moe.combine_shared(cfg, b.y_perm, b.row_map, b.topk_prob, y_shared, b.y)
+            if f16s:
+                moe.combine_f16s(cfg, y16, y16_exp, b.row_map, b.topk_prob, b.y,
+                                 y_shared=y_shared)
+            else:
+                moe.combine_shared(cfg, b.y_perm, b.row_map, b.topk_prob, y_shared, b.y)
         elif f16s:
             moe.combine_f16s(cfg, y16, y16_exp, b.row_map, b.topk_prob, b.y)
         else:

@@ -240,8 +240,11 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm, const int32_t
  * coarse for the layer's bf16 output bar (the output's error beyond its own
  * rounding must stay under 2e-2 of its RMS).  moe_combine_f16s is
  * moe_combine over the decoded values (fp16 * 2^exp, exact in fp32): the
- * same slot-order fp32 sum and one rounding.  moe_forward uses this pair for
- * bf16 layers with k >= 2 and no pad_to_capacity.
+ * same slot-order fp32 sum and one rounding; y_shared (nullable, fp32
+ * [T,h]) is the shared expert's output, added after the routed sum as in
+ * moe_combine_shared.  moe_forward uses this pair for bf16 layers with k >= 2
+ * and no pad_to_capacity, moe_forward_shared for bf16 layers without
+ * pad_to_capacity, and moe_forward_e4m3 (with moe_grouped_fc2_e4m3_f16s).
  * Megatron Core walkthrough §10 (experts) and §2 (combine).
  *   y16 [R_max,h] fp16, y16_exp [R_max,h/32] int8 (8-byte aligned); other arguments as
  *   moe_grouped_fc2 / moe_combine.  MOE_ERR_UNSUPPORTED for fp32 layers.
@@ -250,8 +253,8 @@ moe_status moe_grouped_fc2_f16s(const moe_config* cfg, const void* h_mid,
                                 const int32_t* expert_offsets, const void* W2, void* y16,
                                 int8_t* y16_exp, void* ws, size_t ws_bytes, moe_stream_t stream);
 moe_status moe_combine_f16s(const moe_config* cfg, const void* y16, const int8_t* y16_exp,
-                            const int32_t* row_map, const float* topk_prob, void* y,
-                            moe_stream_t stream);
+                            const int32_t* row_map, const float* topk_prob,
+                            const float* y_shared, void* y, moe_stream_t stream);
 
 /*
  * fc2 and the combine in one call (layers without pad_to_capacity), as

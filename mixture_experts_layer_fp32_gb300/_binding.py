@@ -85,7 +85,7 @@ def lib():
             "moe_combine": ([cfgp, vp, vp, vp, vp, vp], i32),
             "moe_grouped_fc2_combine": ([cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_grouped_fc2_f16s": ([cfgp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
-            "moe_combine_f16s": ([cfgp, vp, vp, vp, vp, vp, vp], i32),
+            "moe_combine_f16s": ([cfgp, vp, vp, vp, vp, vp, vp, vp], i32),
             "moe_forward": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
             "moe_check": ([vp, vp, ctypes.POINTER(i32)], i32),
             "moe_permute_noalloc": ([cfgp, vp, vp, vp, vp, vp, vp, vp], i32),
@@ -265,10 +265,12 @@ def grouped_fc2_f16s(cfg, h_mid, expert_offsets, W2, y16, y16_exp, ws):
            "moe_grouped_fc2_f16s")
 
 
-def combine_f16s(cfg, y16, y16_exp, row_map, topk_prob, y):
-    """moe_combine_f16s: the combine over that y_perm."""
+def combine_f16s(cfg, y16, y16_exp, row_map, topk_prob, y, y_shared=None):
+    """moe_combine_f16s: the combine over that y_perm (plus the shared
+    expert's fp32 output y_shared, if given)."""
     _check(lib().moe_combine_f16s(ctypes.byref(cfg), _p(y16), _p(y16_exp), _p(row_map),
-                                  _p(topk_prob), _p(y), _stream()), "moe_combine_f16s")
+                                  _p(topk_prob), _p(y_shared), _p(y), _stream()),
+           "moe_combine_f16s")
 
 
 def combine(cfg, y_perm, row_map, topk_prob, y):

@@ -339,7 +339,7 @@ moe_status do_fc2_combine(const moe_config& c, const void* h_mid, const int32_t*
     MOE_CUDA(launch_tc_fc2_f16s(c.num_experts, c.hidden, c.ffn_hidden, rows, h_mid, offsets, W2,
                                 y16, y16e, err, s));
     MOE_CUDA(launch_combine_f16s(c.num_tokens, c.hidden, c.topk, y16, y16e, row_map, topk_prob,
-                                 y, s, rows));
+                                 nullptr, y, s, rows));
     return MOE_OK;
   }
   if (!fc2_combine_fused(c)) {
@@ -823,16 +823,29 @@ moe_status shared_forward_body(const moe_config& c, int32_t fs, const void* x, c
                                        side->stream);
   const cudaError_t rec = cudaEventRecord(side->join, side->stream);
   Routed r{};
-  const moe_status st = routed_path(c, x, Wg, gate_bias, expert_bias, W1, W3, W2, topk_idx,
-                                    topk_prob, tokens_per_expert, ws, stream, &r);
+  // bf16 without padding: fc2 into the fp16 y_perm (a scale per 32 columns)
+  const bool f16s = c.dtype == MOE_BF16 && !c.pad_to_capacity;
+  const Layout L = make_layout(c);
+  moe_status st = routed_path(c, x, Wg, gate_bias, expert_bias, W1, W3, W2, topk_idx, topk_prob,
+                              tokens_per_expert, ws, stream, &r, f16s);
+  if (st == MOE_OK && f16s &&
+      launch_tc_fc2_f16s(c.num_experts, c.hidden, c.ffn_hidden, rows_of(c), at<void>(ws, L.h_mid),
+                         at<int32_t>(ws, L.offsets), W2, ws_y16(ws, L), ws_y16_exp(c, ws, L), err,
+                         stream) != cudaSuccess)
+    st = MOE_ERR_CUDA;
   // join even after a failure, so that `stream` never stays forked (a capture
   // in progress would be invalidated)
   const cudaError_t wait = rec == cudaSuccess ? cudaStreamWaitEvent(stream, side->join, 0) : rec;
   MOE_TRY(st_side);
   MOE_TRY(st);
   MOE_CUDA(wait);
-  MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm, r.row_map, r.prob,
-                          y_shared, y, stream, rows_of(c)));
+  if (f16s)
+    MOE_CUDA(launch_combine_f16s(c.num_tokens, c.hidden, c.topk, ws_y16(ws, L),
+                                 ws_y16_exp(c, ws, L), r.row_map, r.prob, y_shared, y, stream,
+                                 rows_of(c)));
+  else
+    MOE_CUDA(launch_combine(c.num_tokens, c.hidden, c.topk, c.dtype, r.y_perm, r.row_map, r.prob,
+                            y_shared, y, stream, rows_of(c)));
   return MOE_OK;
 }
 
@@ -868,8 +881,8 @@ moe_status e4m3_forward_body(const moe_config& c, const void* x, const float* Wg
   MOE_TRY(do_mlp_e4m3(c, xperm_q, xperm_s, offsets, W1q, s1, W3q, s3, W2q, s2,
                       at<void>(ws, L.h_mid), at<uint8_t>(ws, Q.hq), at<float>(ws, Q.hs), nullptr,
                       ws, stream, y16, y16e));
-  MOE_CUDA(launch_combine_f16s(c.num_tokens, c.hidden, c.topk, y16, y16e, row_map, prob, y, stream,
-                               rows_of(c)));
+  MOE_CUDA(launch_combine_f16s(c.num_tokens, c.hidden, c.topk, y16, y16e, row_map, prob, nullptr,
+                               y, stream, rows_of(c)));
   return MOE_OK;
 }
 
@@ -1090,8 +1103,8 @@ moe_status moe_grouped_fc2_f16s(const moe_config* cfg, const void* h_mid,
 }
 
 moe_status moe_combine_f16s(const moe_config* cfg, const void* y16, const int8_t* y16_exp,
-                            const int32_t* row_map, const float* topk_prob, void* y,
-                            moe_stream_t stream) {
+                            const int32_t* row_map, const float* topk_prob,
+                            const float* y_shared, void* y, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   const moe_config& c = *cfg;
   if (c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
@@ -1101,9 +1114,10 @@ moe_status moe_combine_f16s(const moe_config* cfg, const void* y16, const int8_t
   MOE_TRY(need(y16_exp, R * (c.hidden / 32), 8));
   MOE_TRY(need(row_map, T * k, 4));
   MOE_TRY(need(topk_prob, T * k, 4));
+  MOE_TRY(optional(y_shared, 16));
   MOE_TRY(need(y, T * c.hidden, 16));
   MOE_CUDA(launch_combine_f16s(c.num_tokens, c.hidden, c.topk, y16, y16_exp, row_map, topk_prob,
-                               y, stream, rows_of(c)));
+                               y_shared, y, stream, rows_of(c)));
   return MOE_OK;
 }
 

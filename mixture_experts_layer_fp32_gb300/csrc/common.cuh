@@ -175,10 +175,11 @@ cudaError_t launch_tc_fc2_f16s(int E, int h, int f, int64_t max_rows, const void
                                const int32_t* offsets, const void* W2, void* y16, int8_t* y16_exp,
                                int* err, cudaStream_t s);
 // The combine reading that y_perm (bf16 output): the same slot-order fp32 sum
-// of p * value, one rounding.
+// of p * value, then the shared expert's fp32 row if given, one rounding.
 cudaError_t launch_combine_f16s(int T, int h, int k, const void* y16, const int8_t* y16_exp,
-                                const int32_t* row_map, const float* topk_prob, void* y,
-                                cudaStream_t s, int64_t max_rows);
+                                const int32_t* row_map, const float* topk_prob,
+                                const float* y_shared, void* y, cudaStream_t s,
+                                int64_t max_rows);
 // fc2 of a top-1 layer with the combine in the epilogue: y[row_token[r]] =
 // bf16(row_weight[r] * (h_mid[r] . W2[e]))
 cudaError_t launch_tc_fc2_top1(int E, int h, int f, int64_t max_rows, const void* h_mid,

@@ -915,7 +915,8 @@ template <int TPI_LOG2, int KMAX, int U>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_f16s_kernel(int T, int h, int k, int64_t max_rows, const uint4* __restrict__ y16,
                         const int8_t* __restrict__ y16_exp, const int32_t* __restrict__ row_map,
-                        const float* __restrict__ topk_prob, uint4* __restrict__ y) {
+                        const float* __restrict__ topk_prob, const float4* __restrict__ y_shared,
+                        uint4* __restrict__ y) {
   const int h8 = h >> 3;    // 16-byte vectors per row
   const int nch = h >> 5;   // exponent bytes per row
   constexpr int tpt = kCombineThreads >> TPI_LOG2;
@@ -964,6 +965,18 @@ __global__ void __launch_bounds__(kCombineThreads)
           }
         }
         if (v >= h8) continue;
+        if (y_shared) {  // the shared expert's output, added after the routed sum
+          const float4 s0 = __ldcs(y_shared + ((int64_t)t * h8 + v) * 2);
+          const float4 s1 = __ldcs(y_shared + ((int64_t)t * h8 + v) * 2 + 1);
+          acc[0] += s0.x;
+          acc[1] += s0.y;
+          acc[2] += s0.z;
+          acc[3] += s0.w;
+          acc[4] += s1.x;
+          acc[5] += s1.y;
+          acc[6] += s1.z;
+          acc[7] += s1.w;
+        }
         uint32_t o[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -979,32 +992,36 @@ __global__ void __launch_bounds__(kCombineThreads)
 template <int KMAX, int U>
 void launch_combine_f16s_t(int l, int grid, cudaStream_t s, int T, int h, int k, int64_t max_rows,
                            const uint4* src, const int8_t* ex, const int32_t* row_map,
-                           const float* topk_prob, uint4* dst) {
+                           const float* topk_prob, const float4* ys, uint4* dst) {
   switch (l) {
-    case 0: combine_f16s_kernel<0, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, dst); break;
-    case 1: combine_f16s_kernel<1, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, dst); break;
-    case 2: combine_f16s_kernel<2, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, dst); break;
-    default: combine_f16s_kernel<3, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, dst); break;
+    case 0: combine_f16s_kernel<0, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, ys, dst); break;
+    case 1: combine_f16s_kernel<1, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, ys, dst); break;
+    case 2: combine_f16s_kernel<2, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, ys, dst); break;
+    default: combine_f16s_kernel<3, KMAX, U><<<grid, kCombineThreads, 0, s>>>(T, h, k, max_rows, src, ex, row_map, topk_prob, ys, dst); break;
   }
 }
 
 cudaError_t launch_combine_f16s(int T, int h, int k, const void* y16, const int8_t* y16_exp,
-                                const int32_t* row_map, const float* topk_prob, void* y,
-                                cudaStream_t s, int64_t max_rows) {
+                                const int32_t* row_map, const float* topk_prob,
+                                const float* y_shared, void* y, cudaStream_t s,
+                                int64_t max_rows) {
   if (T == 0) return cudaSuccess;
   const uint4* src = static_cast<const uint4*>(y16);
+  const float4* ys = reinterpret_cast<const float4*>(y_shared);
   uint4* dst = static_cast<uint4*>(y);
   // 128 bytes of loads per thread in flight: 2 slots x 4 vectors, 4 x 2 or 8 x 1
   const int U = k <= 2 ? 4 : k <= 4 ? 2 : 1;
   const int l = tokens_per_round_log2(h / 8, kCombineThreads, U, 3);
   const int grid = grid_for_tokens((T + (1 << l) - 1) >> l, 8);
   if (k <= 2)
-    launch_combine_f16s_t<2, 4>(l, grid, s, T, h, k, max_rows, src, y16_exp, row_map, topk_prob, dst);
+    launch_combine_f16s_t<2, 4>(l, grid, s, T, h, k, max_rows, src, y16_exp, row_map, topk_prob, ys,
+                                dst);
   else if (k <= 4)
-    launch_combine_f16s_t<4, 2>(l, grid, s, T, h, k, max_rows, src, y16_exp, row_map, topk_prob, dst);
+    launch_combine_f16s_t<4, 2>(l, grid, s, T, h, k, max_rows, src, y16_exp, row_map, topk_prob, ys,
+                                dst);
   else
     launch_combine_f16s_t<MOE_MAX_TOPK, 1>(l, grid, s, T, h, k, max_rows, src, y16_exp, row_map,
-                                           topk_prob, dst);
+                                           topk_prob, ys, dst);
   return cudaGetLastError();
 }
 

@@ -163,7 +163,17 @@ def gpu_stages(w, dinp, with_routing_map=True, fp32_combine=False):
         b.y_shared = torch.empty((w.T, w.h), dtype=torch.float32, device="cuda")
         moe.shared_expert(cfg, w.shared_f, dinp["x"], dinp["W1s"], dinp["W3s"], dinp["W2s"],
                           b.h_mid_s, b.y_shared, b.ws)
-        moe.combine_shared(cfg, b.y_perm, b.row_map, b.topk_prob, b.y_shared, b.y)
+        if w.dtype == "bf16" and not w.pad_to_capacity and not fp32_combine:
+            # the shared forward's path: the fp16 y_perm and its combine with the shared row
+            b.y16 = torch.empty((b.y_perm.shape[0], w.h), dtype=torch.float16, device="cuda")
+            b.y16_exp = torch.empty((b.y_perm.shape[0], w.h // 32), dtype=torch.int8,
+                                    device="cuda")
+            moe.grouped_fc2_f16s(cfg, b.h_mid, b.expert_offsets, dinp["W2"], b.y16, b.y16_exp,
+                                 b.ws)
+            moe.combine_f16s(cfg, b.y16, b.y16_exp, b.row_map, b.topk_prob, b.y,
+                             y_shared=b.y_shared)
+        else:
+            moe.combine_shared(cfg, b.y_perm, b.row_map, b.topk_prob, b.y_shared, b.y)
     elif uses_f16s(w) and not fp32_combine:
         b.y16 = torch.empty((b.y_perm.shape[0], w.h), dtype=torch.float16, device="cuda")
         b.y16_exp = torch.empty((b.y_perm.shape[0], w.h // 32), dtype=torch.int8, device="cuda")
