@@ -242,7 +242,7 @@ def kernels_per_forward(w, cfg, fp8=False):
     return route + index + 1 + 1 + 1 + shared + quant + 1  # permute index + copy, fc1, fc2, combine
 
 
-def stage_work(w, R, fp8=False, active=None, y16=False):
+def stage_work(w, R, fp8=False, active=None, y16=False, kept=None):
     """Algorithmic work of each stage (bytes moved or flops), per forward.
     fp8: E4M3 expert operands (1-byte codes of x_perm, the weights and the
     SwiGLU output; fc2 also reads the bf16 SwiGLU output once to quantise it).
@@ -253,6 +253,7 @@ def stage_work(w, R, fp8=False, active=None, y16=False):
     T, h, E, k, f = w.T, w.h, w.E, w.k, w.f
     A = E if active is None else active
     yb = 2 + 1 / 32 if y16 else 4  # bytes of a y_perm value: fp16 + exponent byte, or fp32
+    K = R if kept is None else kept  # rows the combine reads (padding rows have no slot)
     return {
         "route": {"bytes": T * h * b + h * E * 4 + T * k * (4 + 4 + 1),
                   "flops": 2 * T * h * E},
@@ -262,9 +263,9 @@ def stage_work(w, R, fp8=False, active=None, y16=False):
                 "bytes": A * f * h * q + R * f * b + (2 * R * f if fp8 else 0) + R * h * yb,
                 "bytes_algorithmic": A * f * h * q + R * f * b + (2 * R * f if fp8 else 0)
                 + R * h * b},
-        "combine": {"bytes": R * h * yb + T * h * b + T * k * 8 + (T * h * 4 if w.shared_f else 0),
+        "combine": {"bytes": K * h * yb + T * h * b + T * k * 8 + (T * h * 4 if w.shared_f else 0),
                     # the scope's algorithmic bytes: y_perm in the activation dtype
-                    "bytes_algorithmic": R * h * b + T * h * b},
+                    "bytes_algorithmic": K * h * b + T * h * b},
         # top-1: fc2 writes each row, weighted, straight into the token's output
         # row (no y_perm); dropped tokens' rows are zeroed
         "fc2+combine": {"flops": 2 * R * f * h,
@@ -492,7 +493,8 @@ def run_native(args, rank, world, local):
         return None
 
     peaks = measured_peaks()
-    work = stage_work(w, R, fp8, active=int(np.count_nonzero(tpe)), y16=f16s)
+    kept = int(b.keep.sum().item())
+    work = stage_work(w, R, fp8, active=int(np.count_nonzero(tpe)), y16=f16s, kept=kept)
     stages = {}
     for s in stage_names:
         t = sum(stage_ms[s]) / len(stage_ms[s])
