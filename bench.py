@@ -66,6 +66,24 @@ def uses_f16s(w, fp8=False):
     return w.k > 1 or w.shared_f > 0  # top-1 without a shared expert: fc2+combine fused
 
 
+def router_on_tc(w):
+    """The opt-in tensor-core router (MOE_ROUTER_TC=1 in the environment, off
+    by default: the layer keeps the tensor cores to the expert GEMMs): bf16
+    layers with more experts than the fused small-E router, E % 4 == 0, the
+    gate weights split into three bf16 pieces (the library's rule)."""
+    fused = w.E <= 8 and w.k <= w.E and w.num_groups <= 1 and w.h <= 6144
+    return (w.dtype == "bf16" and w.E % 4 == 0 and not fused
+            and os.environ.get("MOE_ROUTER_TC", "")[:1] == "1")
+
+
+def router_ksplit(w):
+    """K splits of the tensor-core router GEMM: fp32 accumulation chains of at
+    most 1024 products, at most 5 splits (the library's rule)."""
+    force = os.environ.get("MOE_ROUTER_KSPLIT", "")
+    S = int(force[0]) if force[:1].isdigit() and force[0] != "0" else -(-w.h // 1024)
+    return max(1, min(S, 5, w.h // 64))
+
+
 def stages_of(w, fp8=False):
     """Timed stages of one forward (the shared expert between fc2 and combine)."""
     if fused_top1(w, fp8):
@@ -233,7 +251,9 @@ def kernels_per_forward(w, cfg, fp8=False):
     # the drop candidates before the select kernel
     fused = w.E <= 8 and w.k <= w.E and w.num_groups <= 1 and w.h <= 6144
     index = 2 if -(-w.T * w.k // 2048) <= 128 else 3
-    route = (1 if fused else 2) + (index + 1 if drops else 0) + (1 if w.pad_to_capacity else 0)
+    # the tensor-core router: split of the gate weights, logits GEMM, top-k
+    logits = 1 if fused else 3 if router_on_tc(w) else 2
+    route = logits + (index + 1 if drops else 0) + (1 if w.pad_to_capacity else 0)
     if w.pad_to_capacity:  # permutation by the padded map: hist, scan, rank, gather
         # E4M3: x quantised per token first, the scales gathered, the SwiGLU rows quantised
         return route + 4 + 1 + 1 + (2 if w.shared_f > 0 else 0) + (3 if fp8 else 0) + 1
@@ -511,9 +531,17 @@ def run_native(args, rank, world, local):
             ent["gbs_algorithmic"] = work[s]["bytes_algorithmic"] / (t * 1e-3) / 1e9
             ent["frac_algorithmic"] = ent["gbs_algorithmic"] / peaks["hbm_gbs"]
         stages[s] = ent
-    # the fp32 router GEMM at E >= 64 is bound by the FMA pipe: its fraction of
-    # the FMA rate measured in this run (the small-E router is HBM-bound)
-    if w.E >= 64:
+    if router_on_tc(w):
+        # the logits on the tensor cores: three bf16 pieces of the gate weights,
+        # so 3x the algorithmic flops run as MMAs (columns padded to 256)
+        S = router_ksplit(w)
+        t = stages["route"]["ms"] * 1e-3
+        stages["route"]["tensor_tflops"] = 3 * work["route"]["flops"] / t / 1e12
+        stages["route"]["tensor_frac"] = stages["route"]["tensor_tflops"] / peaks["bf16_tflops"]
+        stages["route"]["logit_partials"] = 3 * S
+    elif w.E >= 64:
+        # the fp32 router GEMM at E >= 64 is bound by the FMA pipe: its fraction
+        # of the FMA rate measured in this run (the small-E router is HBM-bound)
         stages["route"]["alu_frac"] = stages["route"]["tflops"] / fma_tflops
     peaks["fp32_fma_tflops"] = fma_tflops
     fc2_name = "fc2+combine" if "fc2+combine" in stages else "fc2"
@@ -675,8 +703,9 @@ def run_backward(args, moe, w, cfg, inp, b, R, flush, stream, world, rank, local
 
 
 def backward_launches(w):
-    """Kernels moe_backward launches for workload w: router logits, combine
-    backward, router backward, the router's parameter and token gradients
+    """Kernels moe_backward launches for workload w: router logits (two on
+    the tensor cores: the weight split and the GEMM), combine backward,
+    router backward, the router's parameter and token gradients
     (tensor-core path for E % 64 == 0: two bf16 splits, the dWg GEMM, its
     fold, dgate_bias, the dx GEMM; else dWg (+ its split reduction), dgate_bias,
     dx), three dgrad/recompute GEMMs, the token-gradient combine, three
@@ -689,7 +718,8 @@ def backward_launches(w):
         tiles = (w.h + 511) // 512 if small else ((w.h + 63) // 64) * ((w.E + 63) // 64)
         S = min(-(-4 * sms // tiles), -(-w.T // (64 if small else 256)), 128 if small else 32)
         router = 3 + (1 if S > 1 else 0)
-    return 3 + router + 3 + 1 + 3 + (6 if w.shared_f > 0 else 0)
+    logits = 2 if router_on_tc(w) else 1  # the tensor-core logits: weight split + GEMM
+    return logits + 2 + router + 3 + 1 + 3 + (6 if w.shared_f > 0 else 0)
 
 
 def barrier(world):

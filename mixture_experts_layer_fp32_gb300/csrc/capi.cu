@@ -39,7 +39,7 @@ thread_local char g_last_cuda_error[256] = "";
 struct Layout {
   size_t err, logits, assigned, tiles, cand_rowmap, cand_src, cand_off, cand_tiles;
   size_t topk_idx, topk_prob, keep, tpe, offsets, row_map, x_perm, h_mid, y_perm;
-  size_t map, map_tiles, row_src, top1_token, top1_weight, total;
+  size_t map, map_tiles, row_src, top1_token, top1_weight, router_wk, total;
 };
 
 size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -62,6 +62,35 @@ int64_t rows_of(const moe_config& c) {
   if (q < 0 || q > c.num_tokens) q = c.num_tokens;
   const int64_t padded = q * c.num_experts;
   return padded > np ? padded : np;
+}
+
+// bf16 layers whose router GEMM can run on the tensor cores (over the gate
+// weights split into three bf16 pieces): every expert count past the fused
+// small-E kernel's, E % 4 == 0.
+bool router_tc_capable(const moe_config& c) {
+  return c.dtype == MOE_BF16 && c.num_experts % 4 == 0 && c.hidden % 64 == 0 &&
+         !router_fused_ok(c.hidden, c.num_experts, c.topk, c.num_groups);
+}
+// The layer's router runs on the CUDA cores (fp32 FMA) unless
+// MOE_ROUTER_TC=1 is set in the environment: an opt-in outside the layer's
+// specification, which keeps the tensor cores to the expert GEMMs.
+bool router_on_tc(const moe_config& c) {
+  const char* opt = getenv("MOE_ROUTER_TC");
+  return router_tc_capable(c) && opt && opt[0] == '1';
+}
+
+// Router logits into `partials` (*nsplit partial sums [nsplit, T, E] that the
+// top-k and the router backward add in order); wk: 3 E h bf16 of scratch for
+// the split gate weights when router_tc_capable.
+cudaError_t router_logits(const moe_config& c, const void* x, const float* Wg, void* wk,
+                          float* partials, int* nsplit, int* err, cudaStream_t s) {
+  if (!router_on_tc(c))
+    return launch_router_logits(c.num_tokens, c.hidden, c.num_experts, c.dtype, x, Wg, partials,
+                                nsplit, s);
+  cudaError_t st = launch_router_split3(c.hidden, c.num_experts, Wg, wk, s);
+  if (st != cudaSuccess) return st;
+  return launch_tc_router_logits(c.num_tokens, c.hidden, c.num_experts, x, wk, partials, nsplit,
+                                 err, s);
 }
 
 Layout make_layout(const moe_config& c) {
@@ -101,6 +130,7 @@ Layout make_layout(const moe_config& c) {
   // top-1 layers whose combine runs in fc2's epilogue: each row's token and weight
   L.top1_token = take(k == 1 ? rows * 4 : 0);
   L.top1_weight = take(k == 1 ? rows * 4 : 0);
+  L.router_wk = take(router_tc_capable(c) ? 3 * E * h * 2 : 0);
   L.total = o;
   return L;
 }
@@ -215,7 +245,7 @@ moe_status do_route(const moe_config& c, const void* x, const float* Wg, const f
                                  topk_prob, keep, routing_map, counts, err, s);
     float* logits = at<float>(ws, L.logits);
     int nsplit = 1;
-    cudaError_t st = launch_router_logits(T, c.hidden, E, c.dtype, x, Wg, logits, &nsplit, s);
+    cudaError_t st = router_logits(c, x, Wg, at<void>(ws, L.router_wk), logits, &nsplit, err, s);
     if (st != cudaSuccess) return st;
     return launch_router_topk(T, E, k, c.score, c.num_groups, c.group_topk, logits, nsplit, gb,
                               eb, topk_idx, topk_prob, keep, routing_map, counts, err, s);
@@ -584,7 +614,7 @@ const void* act_at(const moe_config& c, const void* p, size_t i) {
 }
 
 struct BwdLayout {
-  size_t err, logits, dp, dl, dwg_part, dl3, wg3, dwg2, dx_router, dY_perm, dH, dA, dx_perm;
+  size_t err, logits, dp, dl, dwg_part, dl3, wg3, dwg2, router_wk, dx_router, dY_perm, dH, dA, dx_perm;
   size_t dH_s, dA_s, total;
 };
 BwdLayout make_bwd_layout(const moe_config& c, int32_t fs = 0) {
@@ -607,6 +637,7 @@ BwdLayout make_bwd_layout(const moe_config& c, int32_t fs = 0) {
   B.dl3 = take(tc ? T * 3 * E * 2 : 0);
   B.wg3 = take(tc ? h * 3 * E * 2 : 0);
   B.dwg2 = take(tc ? h * 2 * E * 4 : 0);
+  B.router_wk = take(router_tc_capable(c) ? 3 * E * h * 2 : 0);
   B.dx_router = take(T * h * 4);
   B.dY_perm = take(R * h * el);
   B.dH = take(R * f * el);
@@ -766,7 +797,7 @@ moe_status do_backward(const moe_config* cfg, const void* x, const float* Wg,
     MOE_CUDA(cudaMemsetAsync(dY_perm, 0, R * h * (c.dtype == MOE_F32 ? 4 : 2), stream));
   // router: logits again (the forward does not keep them), then its gradients
   int nsplit = 1;
-  MOE_CUDA(launch_router_logits(Ti, hi, Ei, c.dtype, x, Wg, logits, &nsplit, stream));
+  MOE_CUDA(router_logits(c, x, Wg, at<void>(ws, B.router_wk), logits, &nsplit, err, stream));
   MOE_CUDA(launch_combine_bwd(Ti, hi, ki, c.dtype, dy, row_map, topk_prob, y_perm, dY_perm, dp,
                               stream));
   MOE_CUDA(launch_router_bwd(Ti, Ei, ki, c.score, logits, nsplit, gate_bias, topk_idx, dp, dl,

@@ -229,6 +229,20 @@ cudaError_t launch_tc_wgrad(int E, int M, int N, int64_t max_rows, const void* X
 cudaError_t launch_tc_dense_nt_f32(int64_t rows, int K, int N, const void* A, const void* Bk,
                                    float* C, int ldc, int* err, cudaStream_t s);
 
+// Router logits of a bf16 layer on the tensor cores: the fp32 gate weights
+// split exactly into three bf16 pieces (launch_router_split3: Wk [3E, h],
+// row p*E + e = piece p of Wg[:, e], K contiguous), then, with h cut into S
+// splits of at most kRouterChainK (S <= kRouterMaxSplits / 3),
+// partials[p*S + q][t][e] = x[t, split q] . piece p of Wg[split q, e] (bf16
+// products, exact in fp32, accumulated in fp32 on the tensor cores): *nsplit
+// = 3S partial sums that the top-k kernel adds in order.  h % 64 == 0,
+// E % 4 == 0.
+constexpr int kRouterChainK = 1024;
+int router_ksplit(int h);
+cudaError_t launch_router_split3(int h, int E, const float* Wg, void* Wk, cudaStream_t s);
+cudaError_t launch_tc_router_logits(int T, int h, int E, const void* x, const void* Wk,
+                                    float* partials, int* nsplit, int* err, cudaStream_t s);
+
 // ---- backward around the GEMMs (backward.cu)
 cudaError_t launch_combine_bwd(int T, int h, int k, int dtype, const void* dy,
                                const int32_t* row_map, const float* topk_prob,

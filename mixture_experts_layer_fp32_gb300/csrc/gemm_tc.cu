@@ -155,6 +155,18 @@ struct TcArgs {
   const float* row_weight = nullptr;
   // FC2_F16S: the chunk exponents [rows, ldo / 32] int8 (the fp16 values go to out)
   int8_t* exp_out = nullptr;
+  // DGRAD_F32 with piece_cols > 0 (the router's logits over the split gate
+  // weights): output column n goes to column n % piece_cols of partial
+  // n / piece_cols, partials [num_pieces][rows][piece_cols] piece_stride
+  // floats apart; columns of pieces >= num_pieces are not stored
+  int piece_cols = 0;
+  int num_pieces = 0;
+  int64_t piece_stride = 0;
+  // DGRAD_F32, dense A split along K (ksplit != 0, offsets == nullptr): group
+  // e is K blocks [e * k_blocks, (e + 1) * k_blocks) of the same A rows, its
+  // output rows the virtual rows [e * R, (e + 1) * R) with R = max_rows / E;
+  // the weight is the map's first (and only) matrix
+  int ksplit = 0;
 };
 
 // Barriers of an NS-stage ring: full[NS], empty[NS], acc_full[2],
@@ -220,10 +232,12 @@ __device__ __forceinline__ void decode_tile(int tile, const int* tstart, const i
 }
 
 // Expert offsets into shared memory.  Without an offsets array (dense
-// mode, E = 1) the single group is rows [0, max_rows).
+// mode) the E groups are max_rows / E rows each (E = 1: rows [0, max_rows);
+// E > 1: the K splits of a dense GEMM).
 __device__ __forceinline__ void load_offsets(int* off, const TcArgs& args) {
   for (int e = threadIdx.x; e <= args.E; e += blockDim.x)
-    off[e] = args.offsets ? args.offsets[e] : (e == 0 ? 0 : static_cast<int>(args.max_rows));
+    off[e] = args.offsets ? args.offsets[e]
+                          : static_cast<int>(static_cast<int64_t>(e) * (args.max_rows / args.E));
 }
 
 // Per-expert tile prefix (tstart[0..E]) from the expert offsets, by warp 0:
@@ -648,7 +662,15 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, uin
       for (int it = 0; it < 8; ++it) {
         const int r = it * 4 + sub;
         float4 val = *reinterpret_cast<const float4*>(etile + r * EPI_PITCH + col4);
-        if (rbase + r < rend) {
+        if (MODE == DGRAD_F32 && args.piece_cols > 0) {
+          // piece_cols % 4 == 0: the 4 columns lie in one piece
+          const int n = nt * BN + c + col4;
+          const int pc = n / args.piece_cols;
+          if (rbase + r < rend && pc < args.num_pieces)
+            *reinterpret_cast<float4*>(static_cast<float*>(args.out) + pc * args.piece_stride +
+                                       static_cast<int64_t>(rbase + r) * args.piece_cols + n -
+                                       pc * args.piece_cols) = val;
+        } else if (rbase + r < rend) {
           float4* dst = reinterpret_cast<float4*>(out0 + static_cast<int64_t>(rbase + r) * args.ldo +
                                                   c + col4);
           if (MODE == DGRAD_F32 && args.accumulate) {
@@ -735,8 +757,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           ptx::mbar_arrive_expect_tx(fb, STAGE_BYTES);
           const uint32_t a = ptx::smem_u32(stages + stage * STAGE_BYTES);
           const uint32_t b = a + A_BYTES;
-          const int kc = kb * (FP8 ? KE_FP8 : BK);
-          ptx::tma_load_2d(a, &tmA, kc, m0, fb);
+          int kc = kb * (FP8 ? KE_FP8 : BK);
+          int arow = m0, eb = e;
+          if (MODE == DGRAD_F32 && args.ksplit) {  // K split e of the dense rows
+            arow = m0 - off[e];
+            kc += e * KB * BK;
+            eb = 0;
+          }
+          ptx::tma_load_2d(a, &tmA, kc, arow, fb);
           if (FP8) {
             // K-major weight rows: two boxes of 128 output channels x 128 K
             const int n0 = MODE == FC1 ? nt * (BN / 2) : nt * BN;
@@ -756,8 +784,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             const bool first = MODE == DGRAD_BF16 || kb < args.kb_split;
             const CUtensorMap* m = first ? &tmB0 : &tmB1;
             const int k1 = first ? kc : kc - args.kb_split * BK;
-            ptx::tma_load_3d(b, m, k1, nt * BN, e, fb);
-            ptx::tma_load_3d(b + 2 * BOX_BYTES, m, k1, nt * BN + BN / 2, e, fb);
+            ptx::tma_load_3d(b, m, k1, nt * BN, eb, fb);
+            ptx::tma_load_3d(b + 2 * BOX_BYTES, m, k1, nt * BN + BN / 2, eb, fb);
           } else {
             const int n0 = nt * BN;
 #pragma unroll
@@ -1008,8 +1036,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t fb = ptx::mapa_shared(ctl.full(stage), 0);
           const uint32_t a = ptx::smem_u32(stages + stage * P_STAGE_BYTES);
           const uint32_t b = a + A_BYTES;
-          const int kc = kb * (FP8 ? KE_FP8 : BK);
-          ptx::tma_load_2d_pair(a, &tmA, kc, a_row, fb);
+          int kc = kb * (FP8 ? KE_FP8 : BK);
+          int arow = a_row, eb = e;
+          if (MODE == DGRAD_F32 && args.ksplit) {  // K split e of the dense rows
+            arow = a_row - off[e];
+            kc += e * KB * BK;
+            eb = 0;
+          }
+          ptx::tma_load_2d_pair(a, &tmA, kc, arow, fb);
           if (FP8) {
             // K-major weight rows: one box of this CTA's 128 output channels x 128 K
             ptx::tma_load_3d_pair(b, tmB, kc, n0, e, fb);
@@ -1018,7 +1052,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             // 64 K, from the weight that holds this K block
             const bool first = MODE == DGRAD_BF16 || kb < args.kb_split;
             ptx::tma_load_3d_pair(b, first ? &tmB0 : &tmB1, first ? kc : kc - args.kb_split * BK,
-                                  n0, e, fb);
+                                  n0, eb, fb);
           } else {
             ptx::tma_load_3d_pair(b, tmB, n0, kc, e, fb);
             ptx::tma_load_3d_pair(b + BOX_BYTES, tmB, n0 + 64, kc, e, fb);
@@ -1482,6 +1516,39 @@ cudaError_t launch_tc_dense_nt_f32(int64_t rows, int K, int N, const void* A, co
   CUtensorMap c = a;
   setup_tma_out(&c, &args, N);
   return launch_grouped<DGRAD_F32, false>(a, b0, b0, c, args, s);
+}
+
+int router_ksplit(int h) {
+  const char* force = getenv("MOE_ROUTER_KSPLIT");  // a tuning override
+  int S = (h + kRouterChainK - 1) / kRouterChainK;
+  if (force && force[0] >= '1' && force[0] <= '9') S = force[0] - '0';
+  if (S > kRouterMaxSplits / 3) S = kRouterMaxSplits / 3;
+  const int kb = h / BK;
+  if (S > kb) S = kb;
+  return S < 1 ? 1 : S;
+}
+
+cudaError_t launch_tc_router_logits(int T, int h, int E, const void* x, const void* Wk,
+                                    float* partials, int* nsplit, int* err, cudaStream_t s) {
+  if (BK != 64) return cudaErrorNotSupported;
+  if (h % BK != 0 || E % 4 != 0) return cudaErrorInvalidValue;
+  const int S = router_ksplit(h);
+  *nsplit = 3 * S;
+  if (T == 0) return cudaSuccess;
+  CUtensorMap a, b0;
+  // B rows past the 3E of the pieces, and K past h (the last split's ragged
+  // end), read as zeros; columns past 3E are not stored
+  if (!map_rows(&a, x, h, T) || !map_weights_kmajor(&b0, Wk, h, 3 * E, 1))
+    return cudaErrorInvalidValue;
+  const int kbs = (h / BK + S - 1) / S;  // K blocks per split
+  TcArgs args{nullptr, S, (3 * E + BN - 1) / BN, kbs, static_cast<int64_t>(S) * T, partials, E,
+              err};
+  args.kb_split = kbs;
+  args.ksplit = 1;
+  args.piece_cols = E;
+  args.num_pieces = 3;
+  args.piece_stride = static_cast<int64_t>(S) * T * E;  // partial (piece p, split e): p * S + e
+  return launch_grouped<DGRAD_F32, false>(a, b0, b0, a, args, s);
 }
 
 cudaError_t launch_tc_fc1_e4m3(int E, int h, int f, int64_t max_rows, const uint8_t* xq,

@@ -999,7 +999,50 @@ __global__ void __launch_bounds__(1024)
   if (threadIdx.x == 0) kept_per_expert[e] = cap;
 }
 
+// Gate weights for the tensor-core logits: Wg [h, E] fp32 -> Wk [3E, h] bf16
+// (transposed: K contiguous), row p*E + e holding piece p of column e, where
+// v = p0 + p1 + p2 + r with p0 = bf16(v), p1 = bf16(v - p0), p2 =
+// bf16(v - p0 - p1): each difference is exact in fp32 (it keeps the bits
+// below the piece just taken), so the pieces hold v's 24 significant bits and
+// |r| <= 2^-27 |v| (normal range).  A non-finite weight goes whole into piece
+// 0.  32 x 32 tiles through shared memory, coalesced on both sides.
+__global__ void __launch_bounds__(256)
+    router_split3_kernel(int h, int E, const float* __restrict__ Wg,
+                         __nv_bfloat16* __restrict__ Wk) {
+  __shared__ float tile[32][33];
+  const int e0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int k = k0 + ty + 8 * i, e = e0 + tx;
+    tile[ty + 8 * i][tx] = (k < h && e < E) ? Wg[static_cast<int64_t>(k) * E + e] : 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = e0 + ty + 8 * i, k = k0 + tx;
+    if (e >= E || k >= h) continue;
+    const float v = tile[tx][ty + 8 * i];
+    __nv_bfloat16 p0 = __float2bfloat16_rn(v), p1 = __float2bfloat16_rn(0.f), p2 = p1;
+    if (isfinite(v)) {
+      const float r1 = v - __bfloat162float(p0);
+      p1 = __float2bfloat16_rn(r1);
+      p2 = __float2bfloat16_rn(r1 - __bfloat162float(p1));
+    }
+    Wk[static_cast<int64_t>(e) * h + k] = p0;
+    Wk[static_cast<int64_t>(E + e) * h + k] = p1;
+    Wk[static_cast<int64_t>(2 * E + e) * h + k] = p2;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_router_split3(int h, int E, const float* Wg, void* Wk, cudaStream_t s) {
+  if (h == 0 || E == 0) return cudaSuccess;
+  dim3 grid((E + 31) / 32, (h + 31) / 32);
+  router_split3_kernel<<<grid, 256, 0, s>>>(h, E, Wg, static_cast<__nv_bfloat16*>(Wk));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_router_logits(int T, int h, int E, int dtype, const void* x, const float* Wg,
                                  float* partials, int* nsplit, cudaStream_t s) {
