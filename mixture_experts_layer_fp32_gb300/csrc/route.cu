@@ -374,10 +374,40 @@ cudaError_t launch_logits_small_e(int T, int h, int E, const XT* x, const float*
 // DeepSeek-V3 route stage 349 us against 411 us with scalar FMAs, Qwen3
 // 434 against 483; two CTAs per SM (128 registers, a few spilled) beat one
 // CTA per SM without spills (427 / 513 us).  gridDim.z splits K; each split writes its own
-// partial sums, which the top-k kernel adds in split order.
+// partial sums, which the top-k kernel adds in split order.  Operands move by
+// cp.async through a 4-stage ring (raw x and gate rows, 3 K tiles ahead),
+// and each K tile's x is converted to fp32 into a transposed double buffer
+// one tile ahead of its use.
 constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 16;
 constexpr int kMaxSplits = kRouterMaxSplits;
+
+// 16-byte asynchronous global -> shared copy (cp.async, cached in L2 only);
+// src_bytes 0 fills the 16 bytes with zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Stages of the SGEMM's copy ring: a K tile's raw x rows and gate rows are
+// copied kStages - 2 tiles ahead of their conversion and kStages - 1 ahead of
+// their use, with no registers held for them.
+constexpr int kSgemmStages = 4;
+
+template <int BN, typename XT>
+constexpr int sgemm_smem_bytes() {
+  return kSgemmStages * (kGemmBM * kGemmBK * static_cast<int>(sizeof(XT)) + kGemmBK * BN * 4) +
+         2 * kGemmBK * kGemmBM * 4;
+}
 
 template <int BN, typename XT>
 __global__ void __launch_bounds__(BN * 2, 256 / BN)
@@ -386,12 +416,17 @@ __global__ void __launch_bounds__(BN * 2, 256 / BN)
   constexpr int TX = BN / 8;          // threads along experts
   constexpr int NT = TX * 16;         // threads
   constexpr int V = XVec<XT>::N;
-  constexpr int AV = kGemmBM * kGemmBK / V;      // x vectors per tile
+  constexpr int AV = kGemmBM * kGemmBK / V;      // x vectors (16 bytes) per tile
   constexpr int APT = (AV + NT - 1) / NT;
   constexpr int BV = kGemmBK * BN / 4;           // Wg float4 per tile
   constexpr int BPT = BV / NT;
-  __shared__ __align__(16) float As[2][kGemmBK][kGemmBM];
-  __shared__ __align__(16) float Bs[2][kGemmBK][BN];
+  static_assert(AV % NT == 0 && BV % NT == 0, "copy split");
+  // dynamic shared memory: Araw[kSgemmStages][BM][BK] (x as stored), then
+  // Bs[kSgemmStages][BK][BN], then As[2][BK][BM] (x in fp32, transposed)
+  extern __shared__ __align__(16) uint8_t sgemm_smem[];
+  XT* Araw = reinterpret_cast<XT*>(sgemm_smem);
+  float* Bs = reinterpret_cast<float*>(sgemm_smem + kSgemmStages * kGemmBM * kGemmBK * sizeof(XT));
+  float* As = Bs + kSgemmStages * kGemmBK * BN;
 
   const int tid = threadIdx.x;
   const int tx = tid % TX, ty = tid / TX;
@@ -401,44 +436,45 @@ __global__ void __launch_bounds__(BN * 2, 256 / BN)
   const int kend = min(h, kbeg + k_per_split);
   float* out = partials + (int64_t)blockIdx.z * T * E;
 
-  float ar[APT][V];
-  float4 br[BPT];
-  auto load = [&](int k0) {
+  // copies of K tile kt into ring stage kt % kSgemmStages (zeros past T, E or
+  // the split's end), one commit group per tile (empty past the last)
+  const int nk = (kend - kbeg + kGemmBK - 1) / kGemmBK;
+  auto issue = [&](int kt) {
+    if (kt < nk) {
+      const int k0 = kbeg + kt * kGemmBK;
+      const int st = kt % kSgemmStages;
+#pragma unroll
+      for (int r = 0; r < APT; ++r) {
+        const int v = tid + r * NT;
+        const int row = v / (kGemmBK / V), kk = (v % (kGemmBK / V)) * V;
+        const bool ok = t0 + row < T && k0 + kk < kend;
+        cp_async16(Araw + ((int64_t)st * kGemmBM + row) * kGemmBK + kk,
+                   ok ? static_cast<const void*>(x + (int64_t)(t0 + row) * h + k0 + kk) : x,
+                   ok ? 16 : 0);
+      }
+#pragma unroll
+      for (int r = 0; r < BPT; ++r) {
+        const int v = tid + r * NT;
+        const int kk = v / (BN / 4), cc = (v % (BN / 4)) * 4;
+        const bool ok = k0 + kk < kend && e0 + cc < E;
+        cp_async16(Bs + ((int64_t)st * kGemmBK + kk) * BN + cc,
+                   ok ? static_cast<const void*>(Wg + (int64_t)(k0 + kk) * E + e0 + cc) : Wg,
+                   ok ? 16 : 0);
+      }
+    }
+    cp_async_commit();
+  };
+  // x of K tile kt, from its ring stage to fp32 in As[buf] (transposed: [k][row])
+  auto convert = [&](int kt, int buf) {
+    const int st = kt % kSgemmStages;
 #pragma unroll
     for (int r = 0; r < APT; ++r) {
       const int v = tid + r * NT;
       const int row = v / (kGemmBK / V), kk = (v % (kGemmBK / V)) * V;
-      if (v < AV && t0 + row < T && k0 + kk < kend) {
-        XVec<XT>::load(x + (int64_t)(t0 + row) * h + k0 + kk, ar[r]);
-      } else {
+      float f[V];
+      XVec<XT>::load(Araw + ((int64_t)st * kGemmBM + row) * kGemmBK + kk, f);
 #pragma unroll
-        for (int c = 0; c < V; ++c) ar[r][c] = 0.f;
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < BPT; ++r) {
-      const int v = tid + r * NT;
-      const int kk = v / (BN / 4), cc = (v % (BN / 4)) * 4;
-      br[r] = (k0 + kk < kend && e0 + cc < E)
-                  ? *reinterpret_cast<const float4*>(Wg + (int64_t)(k0 + kk) * E + e0 + cc)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  };
-  auto store = [&](int buf) {
-#pragma unroll
-    for (int r = 0; r < APT; ++r) {
-      const int v = tid + r * NT;
-      if (v < AV) {
-        const int row = v / (kGemmBK / V), kk = (v % (kGemmBK / V)) * V;
-#pragma unroll
-        for (int c = 0; c < V; ++c) As[buf][kk + c][row] = ar[r][c];
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < BPT; ++r) {
-      const int v = tid + r * NT;
-      const int kk = v / (BN / 4), cc = (v % (BN / 4)) * 4;
-      *reinterpret_cast<float4*>(&Bs[buf][kk][cc]) = br[r];
+      for (int c2 = 0; c2 < V; ++c2) As[(buf * kGemmBK + kk + c2) * kGemmBM + row] = f[c2];
     }
   };
 
@@ -450,21 +486,29 @@ __global__ void __launch_bounds__(BN * 2, 256 / BN)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
-  const int nk = (kend - kbeg + kGemmBK - 1) / kGemmBK;
+#pragma unroll
+  for (int kt = 0; kt < kSgemmStages - 1; ++kt) issue(kt);
   if (nk > 0) {
-    load(kbeg);
-    store(0);
+    cp_async_wait<kSgemmStages - 2>();  // tile 0 has landed (this thread's copies)
+    __syncthreads();
+    convert(0, 0);
   }
-  __syncthreads();
   for (int kt = 0; kt < nk; ++kt) {
     const int cur = kt & 1;
-    if (kt + 1 < nk) load(kbeg + (kt + 1) * kGemmBK);
+    // tiles <= kt + 1 have landed; the barrier also publishes As[cur] and
+    // frees the ring stage and As buffer that iteration kt - 1 read
+    cp_async_wait<kSgemmStages - 3>();
+    __syncthreads();
+    if (kt + 1 < nk) convert(kt + 1, cur ^ 1);
+    issue(kt + kSgemmStages - 1);
+    const float* Ac = As + cur * kGemmBK * kGemmBM;
+    const float* Bc = Bs + (kt % kSgemmStages) * kGemmBK * BN;
 #pragma unroll
     for (int kk = 0; kk < kGemmBK; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][kk][ty * 4]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][kk][64 + ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][kk][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][kk][BN / 2 + tx * 4]);
+      const float4 a0 = *reinterpret_cast<const float4*>(Ac + kk * kGemmBM + ty * 4);
+      const float4 a1 = *reinterpret_cast<const float4*>(Ac + kk * kGemmBM + 64 + ty * 4);
+      const float4 b0 = *reinterpret_cast<const float4*>(Bc + kk * BN + tx * 4);
+      const float4 b1 = *reinterpret_cast<const float4*>(Bc + kk * BN + BN / 2 + tx * 4);
       const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const float2 b[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
                            make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
@@ -475,9 +519,8 @@ __global__ void __launch_bounds__(BN * 2, 256 / BN)
         for (int j = 0; j < 4; ++j) acc[i][j] = __ffma2_rn(ai, b[j], acc[i][j]);
       }
     }
-    if (kt + 1 < nk) store(cur ^ 1);
-    __syncthreads();
   }
+  cp_async_wait<0>();
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int t = t0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
@@ -515,7 +558,18 @@ cudaError_t launch_sgemm(int T, int h, int E, const XT* x, const float* Wg, floa
   splits = (h + kps - 1) / kps;
   *nsplit = splits;
   dim3 grid((T + kGemmBM - 1) / kGemmBM, (E + BN - 1) / BN, splits);
-  router_sgemm_kernel<BN, XT><<<grid, BN * 2, 0, s>>>(T, h, E, kps, x, Wg, partials);
+  constexpr int smem = sgemm_smem_bytes<BN, XT>();
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaError_t st = cudaGetDevice(&dev);
+  if (st != cudaSuccess) return st;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    st = cudaFuncSetAttribute(router_sgemm_kernel<BN, XT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (st != cudaSuccess) return st;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  router_sgemm_kernel<BN, XT><<<grid, BN * 2, smem, s>>>(T, h, E, kps, x, Wg, partials);
   return cudaGetLastError();
 }
 
