@@ -27,6 +27,12 @@ CASES = {
     # drop kernel keeps in shared memory (4096), so its keys are re-read
     "switch_one_hot": synthetic.scaled("switch", T=12000, h=256, f=256, E=8, seed=16,
                                        gate_bias="hot:1:4.6"),
+    # fp32 x with 64 experts: the large-E router GEMM's fp32 operand path, one
+    # K split whose last 16-wide K tile is half past h = 136 (zero-filled)
+    "fp32_e64": synthetic.scaled("qwen3", T=777, h=136, f=64, E=64, k=4, dtype="f32",
+                                 seed=17),
+    # 192 experts: 64-wide expert tiles, 3 of them, and 8 experts per top-k lane
+    "e192": synthetic.scaled("qwen3", T=700, h=512, f=128, E=192, k=6, seed=18),
 }
 
 
