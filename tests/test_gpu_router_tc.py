@@ -17,7 +17,7 @@ three partial logits in piece order before the top-k.
     expected experts and weights follow from Wg alone;
   * on the workloads' shapes the routing equals the oracle's bit for bit
     and the CUDA-core fp32 GEMM's (the default), weights within the parity
-    tolerance.
+    tolerance; at the workloads' full sizes, against the oracle.
 """
 
 import numpy as np
@@ -115,3 +115,26 @@ def test_tensor_core_router_matches_cuda_cores(case, monkeypatch):
     assert torch.equal(tc.tokens_per_expert, cc.tokens_per_expert)
     got, want = to_np(tc.topk_prob).astype(np.float64), to_np(cc.topk_prob).astype(np.float64)
     assert np.all(np.abs(got - want) <= PROB_RTOL * np.abs(want) + PROB_ATOL)
+
+
+@pytest.fixture(scope="module", params=["dsv3", "qwen3", "switch"])
+def full(request):
+    from moe_cases import condition_inputs
+    w = synthetic.WORKLOADS[request.param]
+    torch.cuda.empty_cache()
+    inp = synthetic.generate(w, device="cuda")
+    r = condition_inputs(w, inp)
+    yield w, inp, r
+    del inp
+    torch.cuda.empty_cache()
+
+
+def test_full_size_routing(full, monkeypatch):
+    # the workloads' full sizes, with the K split the library picks (four
+    # 1024-long accumulation chains at h = 4096, five at h = 7168, one at 1024)
+    w, inp, r = full
+    b = _route(w, inp)
+    assert_equal("topk_idx", to_np(b.topk_idx), r["topk_idx"])
+    assert_equal("keep", to_np(b.keep), r["keep"])
+    assert_equal("tokens_per_expert", to_np(b.tokens_per_expert), r["tokens_per_expert"])
+    assert_probs(to_np(b.topk_prob), r["topk_prob"])
