@@ -153,6 +153,12 @@ moe_status moe_max_rows(const moe_config* cfg, int64_t* rows);
  *   routing_map  [T,E]  uint8 out or NULL: 1 where (t,e) is a kept pair; with
  *                       pad_to_capacity it is required and also holds the
  *                       padding tokens (the input of moe_permute_map)
+ * The logits are fp32 fused multiply-adds on the CUDA cores.  With
+ * MOE_ROUTER_TC=1 in the environment (an opt-in), bf16 layers with E > 8 and
+ * E % 4 == 0 form them on the tensor cores instead: Wg split exactly into
+ * three bf16 pieces, bf16 products (exact in fp32) accumulated in fp32 chains
+ * of at most 1024 products; the result differs from the default only by fp32
+ * rounding.  The same applies to moe_forward and the backward's logits.
  */
 moe_status moe_route(const moe_config* cfg, const void* x, const float* Wg,
                      const float* gate_bias, const float* expert_bias, int32_t* topk_idx,
