@@ -63,13 +63,11 @@ constexpr int BOX_BYTES = 64 * BK * 2;       // 64 (N) x BK (K) weight box, 128-
 constexpr int B_BYTES = 4 * BOX_BYTES;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int SMEM_BUDGET = 227 * 1024;
-constexpr int STAGES = (SMEM_BUDGET - 1024 - 4096) / STAGE_BYTES;  // 9 (BK=32) or 4 (BK=64)
 constexpr uint32_t A_LAYOUT = (BK == 64) ? ptx::kLayoutSw128 : ptx::kLayoutSw64;
 constexpr uint32_t A_SBO = 8 * BK * 2;       // 8-row groups of A
 constexpr int ACC_COLS = BN;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int THREADS = 192;
-constexpr int NUM_BARS = 2 * STAGES + 5;     // full, empty, acc_full[2], acc_empty[2], drain
 // fp32-output epilogue staging, per epilogue warp a 5 KB region (1 KB
 // aligned): a 32 x 32 fp32 block in the 128-byte swizzle that a TMA store
 // reads, or, for a warp whose rows cross the expert's end, a 32 x 32 tile
@@ -79,6 +77,10 @@ constexpr int EPI_PITCH = 36;
 constexpr int EPI_WARP_BYTES = 5120;
 constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
 static_assert(32 * EPI_PITCH * 4 <= EPI_WARP_BYTES && 4096 <= EPI_WARP_BYTES, "staging");
+// the ring takes what the alignment slack, the epilogue staging and ~4 KB of
+// barriers and offsets leave: 8 stages (BK=32) or 4 (BK=64)
+constexpr int STAGES = (SMEM_BUDGET - 1024 - EPI_BYTES - 4096) / STAGE_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 5;     // full, empty, acc_full[2], acc_empty[2], drain
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + NUM_BARS * 8 + 16 +
                            2 * (MOE_MAX_EXPERTS + 1) * 4;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
