@@ -50,9 +50,10 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;                      // MMA N = accumulator columns
 // K per pipeline stage.  64 (the default) gives 48 KB stages and a 4-deep
-// ring; 32 gives 24 KB stages and a 9-deep ring.  Measured on GB300 with the
-// Mixtral-shaped workload: 64 runs at ~1670 TFLOP/s, 32 at ~1000 (twice the
-// per-stage barrier/TMA work and half-width A rows outweigh the deeper ring).
+// ring; 32 (bf16 forward modes only) gives 24 KB stages and an 8-deep ring.
+// Measured on GB300: 32 is 30-45% slower on every workload (Mixtral fc1 2170
+// -> 3088 us, Switch fc1 445 -> 572 us): twice the per-stage barrier and TMA
+// work and half-width A rows outweigh the deeper ring.
 #ifndef MOE_TC_BK
 #define MOE_TC_BK 64
 #endif
