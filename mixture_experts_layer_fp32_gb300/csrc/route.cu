@@ -9,9 +9,16 @@
 //   §8 Token dropping    per-expert capacity, policy "probs" or "position"
 //
 // Kernels:
-//   router_logits_kernel  fp32 SIMT GEMM, CTA tile BT tokens x ET experts,
-//                         K staged through shared memory in BK chunks
-//                         (double-buffered), each thread a TT x TE micro-tile.
+//   router_fused_small_e_kernel  E <= 8: logits and top-k in one pass over x,
+//                         the gate matrix staged in shared memory.
+//   router_sgemm_kernel   E >= 64 (E % 4 == 0): register-blocked fp32 GEMM
+//                         (8 x 8 micro-tiles, paired FMAs), operands through a
+//                         4-stage cp.async ring, K split S ways into partial sums.
+//   router_logits_kernel  other shapes: fp32 SIMT GEMM, CTA tile BT tokens x
+//                         ET experts, K staged through shared memory in BK
+//                         chunks (double-buffered), a TT x TE micro-tile each.
+//   router_split3_kernel  the opt-in tensor-core logits: Wg as three exact
+//                         bf16 pieces, transposed (the GEMM is gemm_tc.cu's).
 //   router_topk_kernel    one warp per token: scores, (group scores and the
 //                         kept groups), top-k by k rounds of a warp arg-max
 //                         (ties -> lower expert / group id), weights,
