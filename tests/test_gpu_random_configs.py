@@ -106,3 +106,51 @@ def test_random_config_forward_reproduces_stages(case):
     assert torch.equal(tpe, b.tokens_per_expert)
     bits = torch.int16 if y.dtype == torch.bfloat16 else torch.int32
     assert torch.equal(y.view(bits), b.y.view(bits))
+
+
+BACKWARD = sorted(n for n, w in CONFIGS.items() if w.shared_f == 0 and not w.pad_to_capacity)
+
+
+@pytest.mark.parametrize("name", BACKWARD)
+def test_random_config_backward(name):
+    # moe_backward after the staged forward against the oracle's backward for
+    # the routing the forward took, with the criteria of the backward's parity
+    # tests (relative L2 error and a bound on every element)
+    import numpy as np
+    import mixture_experts_layer_fp32_gb300 as moe
+    import oracle
+    from moe_cases import gpu_config, np_view, to_np
+    from test_gpu_backward import _dy, assert_grad, rel_l2
+    w = CONFIGS[name]
+    inp, r = make_case(w)
+    d = to_dev(inp)
+    b = gpu_stages(w, d)
+    cfg = gpu_config(w)
+    g = moe.Grads(cfg)
+    ws = moe.alloc_workspace_backward(cfg)
+    dy = _dy(w, 171)
+    if w.dtype == "f32":
+        dy = dy.float()
+    moe.backward(cfg, d["x"], d["Wg"], d["gate_bias"], d["W1"], d["W3"], d["W2"], b, dy.cuda(),
+                 g, ws)
+    moe.check(ws)
+    torch.cuda.synchronize()
+    ref = oracle.backward(np_view(inp["x"]), np_view(inp["Wg"]), np_view(inp["W1"]),
+                          np_view(inp["W3"]), np_view(inp["W2"]), w.k, w.score, r["topk_idx"],
+                          r["topk_prob"], r["keep"], np_view(dy), np_view(inp["gate_bias"]),
+                          np_view(inp["expert_bias"]))
+    assert_grad("dx", to_np(g.dx), ref["dx"])
+    if w.k == 1 and w.score != "softmax_pre":
+        # one renormalised weight is 1 whatever the logits: the exact router
+        # gradient is zero and both sides hold only rounding residue (a
+        # relative error of that is meaningless); it must still be finite
+        assert np.all(np.isfinite(to_np(g.dWg))) and np.all(np.isfinite(to_np(g.dgate_bias)))
+    else:
+        assert_grad("dWg", to_np(g.dWg), ref["dWg"])
+        assert_grad("dgate_bias", to_np(g.dgate_bias), ref["dgate_bias"])
+    for n in ("dW1", "dW3", "dW2"):
+        got = to_np(getattr(g, n))
+        if np.any(ref[n] != 0):
+            assert_grad(n, got, ref[n])
+        for e in np.nonzero(r["tokens_per_expert"] == 0)[0]:
+            assert np.all(got[e] == 0.0), (n, e)
