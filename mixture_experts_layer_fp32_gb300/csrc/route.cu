@@ -759,26 +759,30 @@ __global__ void __launch_bounds__(256)
     int my_idx = -1;   // lane j < k keeps slot j
     float my_s = 0.f;
     for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
+      // this lane's best candidate as an ordered key (a larger score, a larger
+      // key; -0 as +0; 0 = none, NaN scores never count), the lower expert on
+      // ties (i rises with e); then the warp's largest key and, among the
+      // lanes holding it, the lowest expert: two warp reductions
+      uint32_t bk = 0;
       int bi = 0x7fffffff;
 #pragma unroll
       for (int i = 0; i < PL; ++i) {
         const int e = lane + 32 * i;
-        if (e < E && !(taken >> i & 1u) && better(sel[i], e, bv, bi)) {
-          bv = sel[i];
-          bi = e;
+        if (e < E && !(taken >> i & 1u) && !isnan(sel[i])) {
+          uint32_t u = __float_as_uint(sel[i]);
+          if (u == 0x80000000u) u = 0u;
+          const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+          if (key > bk) {
+            bk = key;
+            bi = e;
+          }
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (better(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if (bi < 0 || bi >= E) {  // only on NaN logits
+      const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+      bi = static_cast<int>(
+          __reduce_min_sync(0xffffffffu, (mk != 0u && bk == mk) ? static_cast<uint32_t>(bi)
+                                                                : 0x7fffffffu));
+      if (mk == 0u || bi >= E) {  // only on NaN logits
         if (lane == 0) report_error(err, DEV_ERR_INDEX, t);
         bi = 0;
       }
