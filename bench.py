@@ -585,6 +585,9 @@ def run_native(args, rank, world, local):
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all,
+        # the per-step event times' median and spread beside the mean the value uses
+        "step_ms_stats": {"median": statistics.median(step_ms), "min": min(step_ms),
+                          "max": max(step_ms)},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 experts, bf16 activations" if fp8 else w.dtype,
         "data": "synthetic (seeded, x~N(0,%g), weights~N(0,%g), random-init)" % (w.x_std, w.w_std),
