@@ -41,9 +41,9 @@ CASES = {
     "small_e_softmax_pre_drop_E6": synthetic.scaled("switch", T=2000, h=256, f=256, E=6,
                                                     gate_bias="hot:1:3", seed=84),
     "small_e_max_hidden": synthetic.scaled("mixtral", T=300, h=6144, f=128, seed=85),
-    # bf16 with h <= 4096 takes the streamed kernel (x through shared-memory
-    # stages); fp32 and h > 4096 the register-tile one: both with several
-    # score functions; fewer tokens than SMs (one token per block)
+    # fp32 activations (4 features per 16-byte vector, h not a multiple of
+    # the 128 features a warp covers per step) with several score functions;
+    # fewer 4-token groups than SMs
     "small_e_fp32_sigmoid_bias": synthetic.scaled("dsv3", T=400, h=136, f=64, E=8, k=3,
                                                   dtype="f32", seed=86),
     "small_e_fp32_softmax_pre_drop": synthetic.scaled("switch", T=1500, h=200, f=64, E=7,
