@@ -290,7 +290,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu_mul(float a, float g) { return a / (1.0f + __expf(-a)) * g; }
+// silu(a) * g with the approximate divide (a times the hardware reciprocal
+// of 1 + e^-a, within 2 ulp of fp32; 0 once e^-a overflows): the rounding
+// to bf16 that follows is 2^-9 relative.  The IEEE division's longer
+// instruction sequence made the fc1 epilogue outlast a K = 1024 mainloop.
+__device__ __forceinline__ float silu_mul(float a, float g) {
+  return __fdividef(a, 1.0f + __expf(-a)) * g;
+}
 
 // Drain one accumulator buffer into the output: this warp's 32 TMEM lanes at
 // `tb` hold rows rbase .. rbase+31 (lane l holds row rbase + l) of a tile of
@@ -394,7 +400,7 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, uin
               const int j = 8 * v + 2 * q + u;
               const float dH = __uint_as_float(u ? (hw[q] & 0xffff0000u) : (hw[q] << 16));
               const float av = __uint_as_float(a[j]), gv = __uint_as_float(g[j]);
-              const float sg = 1.0f / (1.0f + __expf(-av));
+              const float sg = __fdividef(1.0f, 1.0f + __expf(-av));  // as silu_mul
               r_a[u] = dH * gv * (sg * (1.0f + av * (1.0f - sg)));
               r_g[u] = dH * (av * sg);
             }
