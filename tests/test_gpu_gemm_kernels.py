@@ -5,6 +5,8 @@ MOE_TC_PAIR override.  The cases put the pair tile's boundaries everywhere
 it matters: experts with rows a multiple of 256, with a tail that ends in
 the first or the second CTA's half, with fewer rows than one half, and
 empty experts; plus the automatic choice on a shape that selects pairs.
+In the boundary case, tails of 1, 44, 100 and exactly 128 rows leave the
+pair's second CTA without rows; tails of 148 and 255 fill it in part.
 """
 
 import numpy as np
@@ -46,10 +48,10 @@ def test_grouped_gemm_kernel(case, kernel, monkeypatch):
 
 
 def test_experts_on_pair_boundaries(monkeypatch):
-    # rows per expert chosen by gate bias: 0, 128, 256, 300, 511 and the rest
+    # rows per expert: 0, 128, 256, 300, 511, 1, 100 and the rest (404)
     w = synthetic.scaled("mixtral", T=1700, h=256, f=128, E=8, k=1, gate_bias=None, seed=75)
     inp, _ = make_case(w)
-    counts = [0, 128, 256, 300, 511, 1, 255]
+    counts = [0, 128, 256, 300, 511, 1, 100]
     counts.append(w.T - sum(counts))
     owner = np.repeat(np.arange(w.E), counts)
     rng = np.random.default_rng(75)
