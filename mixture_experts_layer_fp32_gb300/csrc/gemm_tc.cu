@@ -114,6 +114,19 @@ constexpr long long kWaitCycles = 4000000000LL;
 //              2^-11 instead of 2^-24
 enum { FC1 = 0, FC2 = 1, FC1_BWD = 2, DGRAD_BF16 = 3, DGRAD_F32 = 4, FC2_Y = 5, FC2_F16S = 6 };
 
+// The one-SM kernel's E4M3 fc1 drains each accumulator with two warps per
+// TMEM lane quarter (each takes half the output columns): with K = 1024 the
+// scaled SwiGLU epilogue of four warps took longer than a tile's mainloop,
+// which runs twice as fast as in bf16.
+template <int MODE, bool FP8>
+__host__ __device__ constexpr int epi_warps() {
+  return MODE == FC1 && FP8 ? 8 : 4;
+}
+template <int MODE, bool FP8>
+__host__ __device__ constexpr int one_sm_threads() {
+  return 64 + 32 * epi_warps<MODE, FP8>();
+}
+
 // Exponent of the power-of-two scale of a 32-value chunk whose largest
 // magnitude is amax: amax * 2^-e lies in [2^14, 2^15) for normal amax (e from
 // the float's exponent field, clamped so that 2^-e and 2^e are normal floats);
@@ -302,6 +315,8 @@ __device__ __forceinline__ float silu_mul(float a, float g) {
 // `tb` hold rows rbase .. rbase+31 (lane l holds row rbase + l) of a tile of
 // n-tile `nt`; rows at or past `rend` belong to no row of this expert and are
 // not stored.  fc1 applies silu(a) * g and stores bf16, fc2 stores fp32.
+// ch >= 0 (E4M3 fc1 on one SM, two warps per lane quarter): the warp drains
+// output columns 64*ch .. 64*ch+63 of the n-tile only.
 __device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z,
                                              uint32_t w) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w)
@@ -311,7 +326,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t a, uint32_t x, uint32_t y,
 template <int MODE, bool FP8>
 __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, uint32_t stg,
                                                   const CUtensorMap* tmC, int rbase, int rend,
-                                                  int nt, int e, const TcArgs& args, int lane) {
+                                                  int nt, int e, const TcArgs& args, int lane,
+                                                  int ch = -1) {
   const int sub = lane >> 3;
   const int col4 = (lane & 7) * 4;
   // E4M3: this lane's row scale (rows past the expert's end are not read)
@@ -325,18 +341,20 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, uin
     // of its own row per 32-column chunk (whole 32-byte sectors; staging
     // through shared memory as fc2 does was measured slower here).
     const int row = rbase + lane;
+    const int npair = ch >= 0 ? BN / 4 : BN / 2;  // output columns of this warp
+    const int cofs = ch >= 0 ? ch * (BN / 4) : 0;  // and the first of them
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out) +
-                         static_cast<int64_t>(row) * args.ldo + nt * (BN / 2);
+                         static_cast<int64_t>(row) * args.ldo + nt * (BN / 2) + cofs;
 #pragma unroll 1
-    for (int c = 0; c < BN / 2; c += 32) {
+    for (int c = 0; c < npair; c += 32) {
       uint32_t a[32], g[32];
-      ptx::tmem_ld32(tb + c, a);
-      ptx::tmem_ld32(tb + BN / 2 + c, g);
+      ptx::tmem_ld32(tb + cofs + c, a);
+      ptx::tmem_ld32(tb + BN / 2 + cofs + c, g);
       ptx::tmem_wait_ld();
       if (row < rend) {
         uint4* dst = reinterpret_cast<uint4*>(out + c);
         if (FP8) {  // acc * row scale * channel scale (W1 half and W3 half)
-          const int64_t cb = static_cast<int64_t>(e) * args.ncols + nt * (BN / 2) + c;
+          const int64_t cb = static_cast<int64_t>(e) * args.ncols + nt * (BN / 2) + cofs + c;
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
             const float4 u = __ldg(reinterpret_cast<const float4*>(args.col_scale0 + cb + j));
@@ -695,7 +713,7 @@ __device__ __forceinline__ void drain_accumulator(uint32_t tb, float* etile, uin
 }
 
 template <int MODE, bool FP8>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(one_sm_threads<MODE, FP8>(), 1)
     tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB0,
                       const __grid_constant__ CUtensorMap tmB1,
@@ -725,7 +743,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ctl.acc_full(b), 1);
-      ptx::mbar_init(ctl.acc_empty(b), 4);
+      ptx::mbar_init(ctl.acc_empty(b), epi_warps<MODE, FP8>());
     }
     ptx::mbar_init(ctl.drain(), 1);
     *abort_flag = 0;
@@ -894,8 +912,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else {
-    // ------------------------------------------------ epilogue warps 2..5
+    // ------------------------------------------------ epilogue warps 2..5 (2..9: E4M3 fc1)
     const int q = warp & 3;  // TMEM lane quarter this warp may read
+    const int ch = epi_warps<MODE, FP8>() == 8 ? (warp - 2) / 4 : -1;  // its column half
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const int buf = it & 1;
@@ -910,7 +929,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       float* etile = epi + q * (EPI_WARP_BYTES / 4);  // this warp's staging region
       const uint32_t stg = ptx::smem_u32(etile);
       const int rbase = m0 + q * 32;  // this warp's first row; lane l holds row rbase + l
-      drain_accumulator<MODE, FP8>(tb, etile, stg, &tmC, rbase, rend, nt, e, args, lane);
+      drain_accumulator<MODE, FP8>(tb, etile, stg, &tmC, rbase, rend, nt, e, args, lane, ch);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ctl.acc_empty(buf));
@@ -1339,8 +1358,8 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   int64_t grid = device_sm_count();
   if (grid > max_tiles) grid = max_tiles;
   if (grid <= 0) return cudaSuccess;
-  tc_grouped_kernel<MODE, FP8><<<static_cast<unsigned>(grid), THREADS, SMEM_BYTES, s>>>(a, b0, b1, c,
-                                                                                     args);
+  tc_grouped_kernel<MODE, FP8><<<static_cast<unsigned>(grid), one_sm_threads<MODE, FP8>(),
+                                 SMEM_BYTES, s>>>(a, b0, b1, c, args);
   return cudaGetLastError();
 }
 
