@@ -23,7 +23,8 @@
 //  * Warp roles: warp 0 lane 0 issues TMA loads (A tile 128x64 and four
 //    64xBK weight boxes per stage; a 4-deep ring of K=64 stages), warp 1
 //    allocates TMEM and lane 0 issues tcgen05.mma, warps 2-5 drain TMEM with
-//    tcgen05.ld, apply the epilogue and store.  Two accumulator buffers
+//    tcgen05.ld, apply the epilogue and store (warps 2-9 in the E4M3 fc1,
+//    two per TMEM lane quarter, each half the columns).  Two accumulator buffers
 //    (2 x 256 of the 512 TMEM columns) overlap the epilogue of one tile with
 //    the main loop of the next.
 //  * A tile's rows past its expert's end are computed but never stored;
