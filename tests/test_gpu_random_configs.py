@@ -10,8 +10,9 @@ layers, a shared expert: the combinations of the Megatron Core walkthrough
 (token dropping), 9 (dispatcher), 10 (experts), 11 (shared expert) and 2
 (combine) that the fixed cases do not meet one by one.  Every output is
 compared as the other parity tests compare it (routing, drops and the
-permutation bit-exact, the rest within the tolerances), and moe_forward must
-reproduce the staged calls bit for bit.  Draws whose routing margin cannot be
+permutation bit-exact, the rest within the tolerances), also with the SM-pair
+grouped GEMM forced, and moe_forward must reproduce the staged calls bit for
+bit.  Draws whose routing margin cannot be
 conditioned (a near-tie that no redraw of the seeded rows removes) are left
 out of the list.
 """
@@ -96,6 +97,16 @@ def case(request):
 def test_random_config_matches_oracle(case):
     w, inp, ref, dinp, b = case
     compare_all(w, inp, ref, b)
+
+
+def test_random_config_on_sm_pairs(case, monkeypatch):
+    # the same draw with the SM-pair grouped GEMM forced (the automatic rule
+    # picks it only for 768 rows per expert or more; fp32 layers ignore it)
+    w, inp, ref, dinp, b = case
+    monkeypatch.setenv("MOE_TC_PAIR", "1")
+    b2 = gpu_stages(w, dinp)
+    torch.cuda.synchronize()
+    compare_all(w, inp, ref, b2)
 
 
 def test_random_config_forward_reproduces_stages(case):
