@@ -175,6 +175,11 @@ def test_e4m3_layer_matches_oracle(case, kernel, monkeypatch):
     monkeypatch.setenv("MOE_TC_PAIR", "1" if kernel == "pair" else "0")
     b = gpu_stages_e4m3(w, d)
     torch.cuda.synchronize()
+    check_layer(w, inp, ref, b)
+
+
+def check_layer(w, inp, ref, b):
+    """Every stage of gpu_stages_e4m3's result against the FP8 oracle."""
     assert_equal("topk_idx", to_np(b.topk_idx), ref["topk_idx"])
     assert_equal("keep", to_np(b.keep), ref["keep"])
     assert_probs(to_np(b.topk_prob), ref["topk_prob"])

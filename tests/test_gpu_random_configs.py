@@ -11,8 +11,9 @@ layers, a shared expert: the combinations of the Megatron Core walkthrough
 (combine) that the fixed cases do not meet one by one.  Every output is
 compared as the other parity tests compare it (routing, drops and the
 permutation bit-exact, the rest within the tolerances), also with the SM-pair
-grouped GEMM forced, and moe_forward must reproduce the staged calls bit for
-bit.  Draws whose routing margin cannot be conditioned (a near-tie that no
+grouped GEMM forced and, for the bf16 draws without a shared expert, with
+E4M3 experts against the oracle's FP8 arithmetic; moe_forward must reproduce
+the staged calls bit for bit.  Draws whose routing margin cannot be conditioned (a near-tie that no
 redraw of the seeded rows removes) are left out of the list, and so are the
 few that miss a per-element bound for a reason stated with the sweeps below.
 """
@@ -134,6 +135,22 @@ def test_random_config_forward_reproduces_stages(case):
     assert torch.equal(tpe, b.tokens_per_expert)
     bits = torch.int16 if y.dtype == torch.bfloat16 else torch.int32
     assert torch.equal(y.view(bits), b.y.view(bits))
+
+
+E4M3 = sorted(n for n, w in CONFIGS.items() if w.dtype == "bf16" and w.shared_f == 0)
+
+
+@pytest.mark.parametrize("name", E4M3)
+def test_random_config_e4m3(name):
+    # the bf16 draws with FP8 experts, against the oracle's FP8 arithmetic
+    # with the criteria of the FP8 parity tests
+    from test_gpu_e4m3 import check_layer, gpu_stages_e4m3, oracle_forward_e4m3
+    w = CONFIGS[name]
+    inp, _ = make_case(w)
+    ref = oracle_forward_e4m3(w, inp)
+    b = gpu_stages_e4m3(w, to_dev(inp))
+    torch.cuda.synchronize()
+    check_layer(w, inp, ref, b)
 
 
 BACKWARD = sorted(n for n, w in CONFIGS.items()
